@@ -1,0 +1,30 @@
+"""CPU oracle for the self-speculative decode round.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke check and the
+benchmark's CPU-baseline leg may import this package.  The CUDA path never
+calls it and shares no code with it (the seeded input generators, which hold
+none of the method's arithmetic, are the only thing both sides consume).
+
+Plain NumPy in float64 by default, with explicit dense mask matrices.
+
+Parity notes: the pages print no worked numeric example (their B = 4 example
+and their Figure 4 are images missing from the text), so no function here is
+pinned to a printed decode trace: "parity unpinned" for a worked example.
+Every function is pinned instead to closed forms, library routines, brute-force
+constructions and the method's own invariants (exact AR equivalence, commit
+bounds, the causal-cache invariant) in the CPU tests.
+"""
+from .model import (Model, argmax_lowest, attention, causal_mask, draft_mask, forward,
+                    prefill_cache, rmsnorm, rope, silu, softmax_masked, token_rows,
+                    top2_margin, verify_mask)
+from .decode import (RoundLog, State, accept_length, ar_decode, ar_forward, ar_step,
+                     draft_forward, forced_override, prefill, round_stats, selfspec_decode,
+                     selfspec_round, tokens_per_forward, verify_forward)
+
+__all__ = [
+    "Model", "argmax_lowest", "attention", "causal_mask", "draft_mask", "forward",
+    "prefill_cache", "rmsnorm", "rope", "silu", "softmax_masked", "token_rows", "top2_margin",
+    "verify_mask", "RoundLog", "State", "accept_length", "ar_decode", "ar_forward", "ar_step",
+    "draft_forward", "forced_override", "prefill", "round_stats", "selfspec_decode",
+    "selfspec_round", "tokens_per_forward", "verify_forward",
+]
