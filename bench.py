@@ -1,0 +1,331 @@
+"""Benchmark of the self-speculative decode round on one GB300 (or N replicas).
+
+Default workload: text-region decode on the 0.5B-class bf16 decoder (16 layers,
+hidden 1536, 12 q / 4 kv heads of 128, SwiGLU 4096, vocab 65536), random-init
+N(0, 0.02) weights, a 1024-row N(0, 1) synthetic prefix, B = 32, 73 output
+tokens, batch 1, natural drafts.  One step = one decode of that region
+through the C ABI (the whole round loop on the device); the prefill that sets
+up each step is not timed (decode-only, the pages' Table 3 definition).
+
+Prints one JSON line.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from self_speculative_block_gb300 import synth  # noqa: E402
+
+MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    try:
+        with open(MEASURED_PEAKS) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.th = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# --------------------------------------------------------------------------- workload
+
+def workload(name: str):
+    return synth.WORKLOADS[name]
+
+
+def round_bytes(cfg: synth.ModelConfig, p: int, B: int) -> int:
+    """Algorithmic HBM bytes of one round: all weights twice (draft + verify),
+    the KV cache read by each forward, and the 2 (B + 1) KV rows written."""
+    kv_tok = cfg.kv_bytes_per_token()
+    return (2 * cfg.weight_bytes_per_forward() + (p + B + 1) * kv_tok + (p + B + 2) * kv_tok
+            + 2 * (B + 1) * kv_tok)
+
+
+def kernels_per_forward(cfg: synth.ModelConfig) -> int:
+    # embed + per layer (norm, qkv, attention, o, norm, gate/up, down) + final norm + LM head
+    return 1 + 7 * cfg.n_layers + 2
+
+
+# --------------------------------------------------------------------------- CPU oracle arm
+
+class OracleArm:
+    """The CPU oracle on a bounded sample of the workload: one untimed prefill,
+    then each sample runs self-speculative rounds from a copy of that state
+    until ~`seconds` of round time or the end of the workload."""
+
+    def __init__(self, wl):
+        import oracle
+        self.oracle = oracle
+        self.wl = wl
+        cfg = wl.model
+        W = synth.make_weights(cfg)
+        self.model = oracle.Model(W, cfg)
+        del W
+        prefix = synth.make_prefix(cfg, wl.prefix_len).astype(np.float64)
+        self.st0 = oracle.prefill(self.model, prefix)
+
+    def sample(self, seconds: float):
+        o, wl = self.oracle, self.wl
+        st = o.State(list(self.st0.cache_k), list(self.st0.cache_v), self.st0.x0, list(self.st0.out))
+        committed, rounds, t_total = 0, 0, 0.0
+        while len(st.out) < wl.max_new and t_total < seconds:
+            t0 = time.perf_counter()
+            log = o.selfspec_round(self.model, st, wl.block, wl.max_new)
+            t_total += time.perf_counter() - t0
+            committed += len(log.committed)
+            rounds += 1
+        try:
+            from threadpoolctl import threadpool_info
+            cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [os.cpu_count() or 1])
+        except Exception:
+            cores = os.cpu_count() or 1
+        return {"value": committed / t_total, "unit": "tokens/s", "cores": int(cores), "kind": "oracle",
+                "sample": f"{rounds} self-speculative rounds (B={wl.block}, fp64 NumPy) after an untimed "
+                          f"{wl.prefix_len}-row prefill of {wl.name}; {committed} tokens in {t_total:.1f} s"}
+
+
+# --------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gocr", choices=["gocr", "reference"])
+    ap.add_argument("--workload", default="text", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = workload(args.workload)
+    metric = "committed tokens/s per region at B=32 (batch 1)"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals = []
+        samples = []
+        arm = OracleArm(wl)
+        for i in range(args.warmup + args.steps):
+            s = arm.sample(seconds=max(2.0, args.cpu_seconds / max(1, args.steps)))
+            if i >= args.warmup:
+                vals.append(s["value"])
+                samples.append(s)
+        v = statistics.median(vals)
+        cb = dict(samples[-1])
+        cb["value"] = v
+        line = {"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": wl.name, "prefix": wl.prefix_len, "B": wl.block,
+                           "max_new": wl.max_new, "batch": 1},
+                "cpu_baseline": cb, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                            "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    from self_speculative_block_gb300 import gocr
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    cfg = wl.model
+    W = synth.make_weights(cfg)
+    prefix = synth.make_prefix(cfg, wl.prefix_len)
+    prefix_bits = np.ascontiguousarray(synth.bf16_bits(prefix) if cfg.dtype == synth.BF16 else prefix)
+    B = wl.block
+    max_ctx = wl.prefix_len + wl.max_new + B + 8
+    dec = gocr.Decoder(cfg, W, max_ctx=max_ctx, max_block=B, device=str(dev))
+    del W
+    prefix_dev = torch.from_numpy(prefix_bits.view(np.int16) if cfg.dtype == synth.BF16 else prefix_bits).to(dev)
+    if wl.forced_mean is not None:
+        dec.prefill(0, prefix_dev)
+        ref, _ = dec.decode(0, gocr.MODE_AR, 0, wl.max_new)
+        sched = synth.accept_schedule(wl.forced_mean, wl.max_new)
+        dec.set_draft_override(0, ref, sched)
+
+    def step():
+        dec.prefill(0, prefix_dev)
+        out, st = dec.decode(0, gocr.MODE_SELFSPEC, B, wl.max_new)
+        return out, st
+
+    for _ in range(args.warmup):
+        step()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    dev_ms, tokens, rounds = [], 0, 0
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            out, st = step()
+            dev_ms.append(st["device_ms"])
+            tokens += st["committed"]
+            rounds += st["rounds"]
+    torch.cuda.synchronize()
+    total_s = sum(dev_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s, tokens], dtype=torch.float64, device=dev)
+        tt = [torch.zeros_like(t) for _ in range(world)]
+        torch.distributed.all_gather(tt, t)
+        total_s = max(float(x[0]) for x in tt)
+        tokens = sum(int(x[1]) for x in tt)
+    value = tokens / total_s
+    ms_per_step = sum(dev_ms) / len(dev_ms)
+    round_us = 1e3 * sum(dev_ms) / rounds
+    hbm, peak_kind = peaks()
+    # round roofline: algorithmic bytes of an average round at the mean cache length
+    p_mid = wl.prefix_len + wl.max_new // 2
+    rb = round_bytes(cfg, p_mid, B)
+    round_frac = (rb / (hbm * 1e9)) / (round_us * 1e-6)
+
+    # dominant kernel: the gate/up GEMM of the draft/verify forwards, timed live on
+    # the stream it is launched on, sweeping all layers' weights (> L2) like a forward
+    kern = kernel_roofline(dec, cfg, B, hbm, dev)
+
+    # end to end through the C ABI with host buffers: H2D prefix, prefill, decode, D2H tokens
+    pinned = torch.from_numpy(prefix_bits.view(np.int16) if cfg.dtype == synth.BF16 else prefix_bits).pin_memory()
+    e2e_tok, e2e_s = 0, 0.0
+    for _ in range(max(1, args.steps)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dec.prefill(0, pinned)
+        out, st = dec.decode(0, gocr.MODE_SELFSPEC, B, wl.max_new)
+        e2e_s += time.perf_counter() - t0
+        e2e_tok += st["committed"]
+    h2d = int(prefix_bits.nbytes)
+    d2h = wl.max_new * 4
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dec.close()
+        torch.cuda.empty_cache()
+        cpu = OracleArm(wl).sample(seconds=args.cpu_seconds)
+    launches = rounds * (2 * kernels_per_forward(cfg) + 4) + args.steps
+    if rank == 0:
+        line = {
+            "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if cfg.dtype == synth.BF16 else "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "prefix": wl.prefix_len, "B": B, "max_new": wl.max_new,
+                       "batch": 1, "parallelism": "replicas" if world > 1 else "single-gpu",
+                       "l2": "inputs larger than L2 (1.0 GB of weights per forward)",
+                       "drafts": "natural" if wl.forced_mean is None else f"forced mean {wl.forced_mean}"},
+            "round_us": round_us, "rounds_per_step": rounds / args.steps,
+            "round_roofline": {"bytes": rb, "peak_gbs": hbm, "frac": round_frac, "peak": peak_kind},
+            "roofline": kern,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_tok / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def kernel_roofline(dec, cfg, B, hbm, dev):
+    """gate/up GEMM with the decode launch shape (B + 1 rows), all layers' packed
+    weights in turn so every launch streams from HBM; CUDA events on its stream."""
+    import torch
+    from self_speculative_block_gb300 import gocr
+    T, N, K = B + 1, 2 * cfg.ffn, cfg.hidden
+    es = 2 if cfg.dtype == synth.BF16 else 4
+    tdt = torch.bfloat16 if es == 2 else torch.float32
+    x = torch.randn(T, K, device=dev).to(tdt)
+    ws = [torch.randn(N, K, device=dev).to(tdt) for _ in range(8)]  # 8 x 25 MB > L2
+    need = dec.lib.gocr_op_linear_workspace(T, N, K)
+    wk = torch.zeros(need, dtype=torch.uint8, device=dev)
+    for w in ws:
+        gocr.op_linear(x, w, wk)
+    s = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(reps):
+        for w in ws:
+            gocr.op_linear(x, w, wk)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * len(ws))
+    alg = N * K * es + T * K * es + T * N * 4
+    ach = alg / (ms * 1e-3) / 1e9
+    return {"kernel": "gemm (gate/up, split-K, fused SwiGLU epilogue in the decoder)", "bound": "hbm",
+            "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+            "launch_us": ms * 1e3, "algorithmic_bytes": alg, "shape": [T, N, K]}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,188 @@
+/*
+ * gocr.h - C ABI of the GB300 self-speculative block decoder.
+ *
+ * The library runs the decode round of a decoder trained for both AR and
+ * block-diffusion decoding (GravityOCR, "Diffusion Drafts, AR Verifies"):
+ *
+ *   draft   one forward of [x0, M x B]: the boundary token x0 reads the cache
+ *           causally and yields a0; the B [M] rows read the cache and the whole
+ *           window bidirectionally and yield drafts d1..dB
+ *           (GravityOCR review, §3.2 "Self-Speculative Decoding");
+ *   verify  one token-causal forward of [a0, d1..dB] yields a1..a(B+1) and
+ *           overwrites the draft's KV slots with causal state in place
+ *           (review, Appendix B.2 "Self-Speculative Decoding and KV-Cache Update");
+ *   accept  A = longest prefix with d_j == a_j; commit a0, d1..dA, a(A+1);
+ *           the rejected suffix is rolled back (velog review, inference section).
+ *
+ * Everything runs on one GPU in hand-written sm_103a kernels.  All entry points
+ * return GOCR_OK (0) or a negative GOCR_E* code; nothing throws across the ABI.
+ * A handle is not thread-safe: calls on one handle must not overlap.
+ *
+ * Layouts: every matrix is row-major [out, in] (y = x W^T), elements in the
+ * handle's dtype (fp32, or bf16 as uint16 bit patterns).  Norm gains are fp32.
+ */
+#ifndef GOCR_H
+#define GOCR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define GOCR_OK          0
+#define GOCR_EINVAL     (-1) /* bad argument: null pointer, size out of range   */
+#define GOCR_ECAPACITY  (-2) /* KV capacity, rows or block size over the limit  */
+#define GOCR_ECUDA      (-3) /* a CUDA runtime call failed (see gocr_last_error) */
+#define GOCR_EDEVICE    (-4) /* a kernel raised its error word (NaN logits ...)  */
+#define GOCR_ETIMEOUT   (-5) /* the on-device round loop hit its round limit     */
+#define GOCR_ENOMEM     (-6) /* allocation failed                                */
+#define GOCR_ESTATE     (-7) /* call order: decode before prefill, and the like  */
+
+enum { GOCR_DTYPE_F32 = 0, GOCR_DTYPE_BF16 = 1 };
+/* decode modes: AR greedy (one token per forward) or self-speculative rounds */
+enum { GOCR_MODE_AR = 0, GOCR_MODE_SELFSPEC = 1 };
+/* single-forward kinds for gocr_debug_forward */
+enum { GOCR_FWD_AR = 0, GOCR_FWD_DRAFT = 1, GOCR_FWD_VERIFY = 2 };
+
+#define GOCR_MAX_BLOCK 64      /* largest block size B */
+#define GOCR_LAYER_TENSORS 9   /* wq wk wv wo wg wu wd g_attn g_mlp */
+
+/* Model and capacity.  q_dim = n_q_heads*head_dim and kv_dim =
+ * n_kv_heads*head_dim must be multiples of 128, head_dim 64 or 128, ffn a
+ * multiple of 64, hidden and vocab multiples of 128, n_q_heads a multiple of
+ * n_kv_heads. */
+typedef struct gocr_config {
+  int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  int32_t dtype;          /* GOCR_DTYPE_F32 | GOCR_DTYPE_BF16 */
+  float rms_eps;          /* RMSNorm epsilon (1e-6) */
+  float rope_theta;       /* rotary base (1e4) */
+  int32_t max_ctx;        /* KV positions per request: >= P + max_new + B + 2 */
+  int32_t max_block;      /* largest B the handle will be asked for (<= 64) */
+  int32_t max_requests;   /* request slots (KV caches) */
+  int32_t eos_id;         /* stop token, -1 = none */
+} gocr_config;
+
+/* Device pointers to the weights.  The caller owns them and keeps them alive
+ * until gocr_free; the handle copies the projections it re-packs (QKV fused,
+ * gate/up interleaved) at create time and reads the others in place. */
+typedef struct gocr_weights {
+  const void* embed;        /* [vocab, hidden] dtype */
+  const void* mask_embed;   /* [hidden] dtype: the single [M] row */
+  const void* lm_head;      /* [vocab, hidden] dtype (untied) */
+  const float* g_final;     /* [hidden] fp32 */
+  /* host array of n_layers * GOCR_LAYER_TENSORS device pointers, per layer:
+   * wq [Hq*d, h], wk [Hkv*d, h], wv [Hkv*d, h], wo [h, Hq*d], wg [F, h],
+   * wu [F, h], wd [h, F] (dtype), g_attn [h], g_mlp [h] (fp32) */
+  const void* const* layer;
+} gocr_weights;
+
+/* Decode statistics (review §4.1 eq. 5: TPF = committed / forwards, the
+ * prefill excluded; a round with A accepted drafts commits A + 2 tokens). */
+typedef struct gocr_stats {
+  int64_t rounds;           /* self-spec rounds, or AR steps                  */
+  int64_t forwards;         /* draft + verify forwards (AR: one per token)    */
+  int64_t committed;        /* decode-committed tokens (prefill token not in) */
+  int64_t accepted_drafts;  /* sum of A over rounds                          */
+  int32_t accept_hist[GOCR_MAX_BLOCK + 1]; /* rounds per accepted count A    */
+  double device_ms;         /* device time of the decode call (CUDA events)  */
+} gocr_stats;
+
+/* Optional device allocator (for example backed by PyTorch's caching
+ * allocator).  Must return 256-byte-aligned device memory or NULL. */
+typedef void* (*gocr_alloc_fn)(size_t bytes, void* user);
+typedef void (*gocr_free_fn)(void* ptr, void* user);
+
+typedef struct gocr_handle gocr_handle;
+
+/* Create a decoder on the current CUDA device.
+ *   stream      cudaStream_t every launch goes to (NULL = legacy default).
+ *   alloc/free  device allocator; both NULL = cudaMalloc/cudaFree.
+ * Returns GOCR_EINVAL for an unsupported shape, GOCR_ENOMEM, GOCR_ECUDA. */
+int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream,
+                gocr_alloc_fn alloc, gocr_free_fn free_fn, void* alloc_user,
+                gocr_handle** out);
+
+/* Causal prefill of request slot `req` from P prefix embeddings (the image +
+ * prompt prefix, [P, hidden] in dtype; host or device pointer, copied before
+ * the call returns).  Resets the slot: the argmax of the last row becomes
+ * out[0] and the boundary token x0; the cache holds positions 0..P-1.
+ * GOCR_ECAPACITY if P + 1 > max_ctx. */
+int gocr_prefill(gocr_handle* h, int req, const void* prefix_embeds, int P);
+
+/* Decode request `req` until max_new tokens are in out (out[0], the prefill
+ * token, counts) or eos.  mode GOCR_MODE_AR commits one token per forward;
+ * GOCR_MODE_SELFSPEC runs draft/verify/accept rounds of block size B.  The
+ * whole loop runs on the device (a CUDA graph with a device-side while loop,
+ * no host synchronisation between rounds); the call blocks until it ends and
+ * then copies out_tokens (host, caller-owned, >= max_new entries) and stats
+ * (may be NULL).  GOCR_ECAPACITY if P + max_new + B + 2 > max_ctx. */
+int gocr_decode(gocr_handle* h, int req, int mode, int B, int max_new,
+                int32_t* out_tokens, gocr_stats* stats);
+
+/* Batched decode of n_req prefilled request slots in one round loop: every
+ * forward concatenates the requests' windows (ragged caches, one position
+ * sequence per request).  max_new[i] per request; out_tokens[i] host buffers;
+ * stats: array of n_req or NULL.  Finished requests stop committing while
+ * the others continue. */
+int gocr_decode_batch(gocr_handle* h, int n_req, const int32_t* reqs, int mode, int B,
+                      const int32_t* max_new, int32_t* const* out_tokens, gocr_stats* stats);
+
+/* Forced-acceptance hook for request `req` (host arrays, copied):  in round r
+ * with c tokens committed, drafts become d_j = ref[c+j] for j <= G_r and
+ * d_(G_r+1) = (ref[c+G_r+1] + 1) mod vocab, G_r = schedule[r] (rounds past
+ * n_rounds use G = 0; positions past n_ref keep the model's draft).
+ * n_ref = 0 removes the hook.  Applied between draft and verify. */
+int gocr_set_draft_override(gocr_handle* h, int req, const int32_t* ref_tokens, int n_ref,
+                            const int32_t* schedule, int n_rounds);
+
+/* One forward at the request's current state, for parity checks; nothing is
+ * committed and cache_len is unchanged (KV slots at and after cache_len are
+ * written).  kind AR: tokens = [x], n = 1, at position cache_len.  DRAFT:
+ * tokens[0] = x0 and n = B + 1 (rows 1..B are [M]), positions cache_len.. .
+ * VERIFY: tokens = [a0, d1..dB], n = B + 1, positions cache_len+1.. (call it
+ * after a DRAFT at the same state, which wrote x0's slot).  logits_out: host
+ * [n, vocab] fp32, or NULL. */
+int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens, int n,
+                       float* logits_out);
+
+/* Copy n cached positions from pos0 of layer `layer` to host buffers
+ * k_out/v_out, each [n, n_kv_heads, head_dim] in dtype. */
+int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, void* k_out, void* v_out);
+
+/* Current cache length (position of the boundary token) and boundary token. */
+int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0);
+
+/* Last error message of the handle (or of the library when h is NULL). */
+const char* gocr_last_error(const gocr_handle* h);
+
+void gocr_free(gocr_handle* h);
+
+/* ---- single-kernel entry points (parity tests, device pointers) --------- */
+
+/* y[T, N] (fp32) = x[T, K] w[N, K]^T, the decoder's weight-streaming GEMM with
+ * its fixed split-K reduction (the split count depends on N and K only, so a
+ * row's result does not depend on T).  K % 8 == 0.  workspace: device,
+ * >= gocr_op_linear_workspace(T, N, K) bytes, all zero before the first call
+ * (the kernel leaves it ready for the next call). */
+size_t gocr_op_linear_workspace(int T, int N, int K);
+int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int N, int K,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* y[T, H] (dtype) = x / sqrt(mean(x^2) + eps) * g for x[T, H] fp32. */
+int gocr_op_rmsnorm(int dtype, const float* x, const float* g, void* y, int T, int H, float eps,
+                    void* stream);
+
+/* Grouped-query attention of one request window against a KV cache.
+ * q [T, Hq, d] dtype; kc, vc [Hkv, cap, d] dtype; o [T, Hq, d] dtype;
+ * lim: device int32[T], row t reads keys 0..lim[t] (draft: row 0 = p, rows
+ * 1..B = p+B; verify/AR: the row's own position).  d in {64, 128}. */
+int gocr_op_attention(int dtype, const void* q, const void* kc, const void* vc, void* o,
+                      const int32_t* lim, int T, int Hq, int Hkv, int d, int cap, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GOCR_H */

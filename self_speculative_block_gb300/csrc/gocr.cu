@@ -1,0 +1,707 @@
+// C ABI and round orchestration of the self-speculative block decoder.
+//
+// One handle owns, on one GPU: re-packed projection weights, a contiguous KV
+// cache per request slot ([layer][kv head][position][head_dim]), activation
+// buffers sized for the largest forward, device-resident request state, and a
+// cache of instantiated CUDA graphs.  A decode call launches one graph whose
+// body is a whole round (draft forward, optional forced-acceptance override,
+// verify forward, accept/commit/rollback) inside a device-side while loop; the
+// accept kernel clears the loop condition when every request is done, so no
+// host synchronisation happens between rounds.
+#include "../../include/gocr.h"
+#include "kernels.cuh"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using namespace gocr;
+
+namespace {
+
+thread_local std::string g_lib_error;
+
+struct GraphEntry {
+  int mode, B, n_slots;
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+}  // namespace
+
+struct gocr_handle {
+  gocr_config cfg{};
+  int es = 4;  // element size of dtype
+  int dtype = 0;
+  cudaStream_t hs = nullptr;
+  cudaStream_t user = nullptr;
+  cudaEvent_t ev0 = nullptr, ev1 = nullptr, evu = nullptr;
+  gocr_alloc_fn af = nullptr;
+  gocr_free_fn ff = nullptr;
+  void* au = nullptr;
+  std::vector<void*> allocs;
+
+  const void* embed = nullptr;
+  const void* mask = nullptr;
+  const void* lm = nullptr;
+  const float* gfin = nullptr;
+  std::vector<void*> wqkv, wgu;
+  std::vector<const void*> wo, wd;
+  std::vector<const float*> gattn, gmlp;
+
+  int q_dim = 0, kv_dim = 0, qkv_n = 0, gu_n = 0;
+  int cap = 0, T_max = 0, T_dec = 0, sched_cap = 0;
+  long long layer_stride = 0, req_stride = 0;
+
+  void* kc = nullptr;
+  void* vc = nullptr;
+  float* resid = nullptr;
+  void* xn = nullptr;
+  void* qbuf = nullptr;
+  void* att = nullptr;
+  void* hbuf = nullptr;
+  void* xlog = nullptr;
+  float* logits = nullptr;
+  int* dbuf = nullptr;
+  int* vbuf = nullptr;
+  int* abuf = nullptr;
+  int* am = nullptr;
+  Rows rows{};
+  int* slot_req = nullptr;    // decode slot table
+  int* slot_one = nullptr;    // one-slot table for prefill / debug
+  int* max_new_dev = nullptr;
+  ReqState* st = nullptr;
+  int* out = nullptr;
+  int* ref = nullptr;
+  int* sched = nullptr;
+  int* err = nullptr;
+  int* dbg_toks = nullptr;
+  float2* rope = nullptr;
+  float* ws = nullptr;
+  size_t ws_floats = 0;
+  int* counters = nullptr;
+  float* pmax = nullptr;
+  int* pidx = nullptr;
+  void* prefix_stage = nullptr;
+
+  bool prefilled[MAX_REQ] = {};
+  std::vector<GraphEntry> graphs;
+  std::string msg;
+};
+
+namespace {
+
+int fail(gocr_handle* h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h) h->msg = buf; else g_lib_error = buf;
+  return code;
+}
+
+#define CK(call)                                                                      \
+  do {                                                                                \
+    cudaError_t e_ = (call);                                                          \
+    if (e_ != cudaSuccess)                                                            \
+      return fail(h, GOCR_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_));     \
+  } while (0)
+
+void* dev_alloc(gocr_handle* h, size_t bytes) {
+  if (bytes == 0) bytes = 256;
+  bytes = (bytes + 255) & ~(size_t)255;
+  void* p = nullptr;
+  if (h->af) {
+    p = h->af(bytes, h->au);
+  } else if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    p = nullptr;
+  }
+  if (p) {
+    h->allocs.push_back(p);
+    cudaMemsetAsync(p, 0, bytes, h->hs);
+  }
+  return p;
+}
+
+int n_rows_of(int kind, int n_slots, int B, int P) {
+  if (kind == PLAN_AR) return n_slots;
+  if (kind == PLAN_PREFILL) return P;
+  return n_slots * (B + 1);
+}
+
+GemmArgs gemm_base(gocr_handle* h, const void* x, int ldx, const void* w, int T, int N, int K,
+                   bool single_split) {
+  GemmArgs a{};
+  a.x = x; a.ldx = ldx; a.w = w; a.T = T; a.N = N; a.K = K;
+  if (single_split) {
+    a.kchunk = K; a.splits = 1;
+  } else {
+    a.kchunk = gemm_kchunk(N, K); a.splits = gemm_splits(N, K);
+  }
+  a.ws = h->ws;
+  a.counters = h->counters;
+  a.e.err = h->err;
+  return a;
+}
+
+// Enqueue one decoder forward over the rows the plan kernel has laid out.
+void enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out,
+                     float* logits) {
+  const gocr_config& c = h->cfg;
+  const int T = n_rows_of(kind, n_slots, B, P);
+  const bool single = kind == PLAN_PREFILL;  // prefill keeps its own reduction shape
+  const int H = c.hidden;
+  launch_embed(h->dtype, h->embed, h->mask, h->prefix_stage, h->resid, h->rows, T, H, c.vocab,
+               h->err, h->hs);
+  for (int l = 0; l < c.n_layers; ++l) {
+    launch_rmsnorm(h->dtype, h->resid, H, h->gattn[l], h->xn, H, T, H, c.rms_eps, nullptr, nullptr,
+                   0, h->hs);
+    // QKV projection, RoPE, KV-cache write at each row's position
+    GemmArgs g = gemm_base(h, h->xn, H, h->wqkv[l], T, h->qkv_n, H, single);
+    g.epi = EPI_QKV;
+    g.e.qbuf = h->qbuf;
+    g.e.kc = (char*)h->kc + (size_t)l * h->layer_stride * h->es;
+    g.e.vc = (char*)h->vc + (size_t)l * h->layer_stride * h->es;
+    g.e.req_stride = h->req_stride;
+    g.e.q_dim = h->q_dim; g.e.kv_dim = h->kv_dim; g.e.head_dim = c.head_dim; g.e.cap = h->cap;
+    g.e.rope = h->rope;
+    g.e.row_pos = h->rows.row_pos; g.e.row_slot = h->rows.row_slot; g.e.plan = h->rows.plan;
+    launch_gemm(h->dtype, g, h->hs);
+    // attention with the row key limits of this forward's mask
+    AttnArgs at{};
+    at.q = h->qbuf;
+    at.kc = g.e.kc; at.vc = g.e.vc; at.req_stride = h->req_stride;
+    at.o = h->att; at.row_lim = h->rows.row_lim; at.plan = h->rows.plan;
+    at.T = T; at.Hq = c.n_q_heads; at.Hkv = c.n_kv_heads; at.d = c.head_dim; at.cap = h->cap;
+    at.scale = 1.0f / sqrtf((float)c.head_dim);
+    launch_attention(h->dtype, at, kind == PLAN_PREFILL ? 1 : n_slots,
+                     kind == PLAN_PREFILL ? P : T / n_slots, h->hs);
+    // O projection + residual
+    GemmArgs go = gemm_base(h, h->att, h->q_dim, h->wo[l], T, H, h->q_dim, single);
+    go.epi = EPI_RESID; go.e.y = h->resid; go.e.ldy = H;
+    launch_gemm(h->dtype, go, h->hs);
+    launch_rmsnorm(h->dtype, h->resid, H, h->gmlp[l], h->xn, H, T, H, c.rms_eps, nullptr, nullptr,
+                   0, h->hs);
+    // gate/up (interleaved) + SwiGLU
+    GemmArgs gg = gemm_base(h, h->xn, H, h->wgu[l], T, h->gu_n, H, single);
+    gg.epi = EPI_SWIGLU; gg.e.hbuf = h->hbuf; gg.e.ldh = c.ffn;
+    launch_gemm(h->dtype, gg, h->hs);
+    // down + residual
+    GemmArgs gd = gemm_base(h, h->hbuf, c.ffn, h->wd[l], T, H, c.ffn, single);
+    gd.epi = EPI_RESID; gd.e.y = h->resid; gd.e.ldy = H;
+    launch_gemm(h->dtype, gd, h->hs);
+  }
+  // final norm on the rows that need logits, then LM head + argmax
+  const int n_logit = kind == PLAN_PREFILL ? n_slots : T;
+  launch_rmsnorm(h->dtype, h->resid, H, h->gfin, h->xlog, H, n_logit, H, c.rms_eps,
+                 h->rows.logit_row, nullptr, 0, h->hs);
+  GemmArgs gl = gemm_base(h, h->xlog, H, h->lm, n_logit, c.vocab, H, single);
+  gl.epi = EPI_ARGMAX;
+  gl.e.logits = logits; gl.e.ld_logits = c.vocab;
+  gl.e.pmax = h->pmax; gl.e.pidx = h->pidx; gl.e.am_out = am_out;
+  launch_gemm(h->dtype, gl, h->hs);
+}
+
+// One round (or one AR step) of the decode loop.
+void enqueue_round(gocr_handle* h, int mode, int B, int n_slots, unsigned long long cond,
+                   int use_cond) {
+  const int cap = h->cap;
+  const int out_stride = cap;
+  if (mode == GOCR_MODE_AR) {
+    launch_plan(PLAN_AR, h->rows, h->st, h->slot_req, n_slots, 0, 0, nullptr, nullptr, cap, h->hs);
+    enqueue_forward(h, PLAN_AR, n_slots, 0, 0, h->abuf, nullptr);
+    launch_ar_commit(h->st, h->slot_req, n_slots, h->abuf, h->out, out_stride, h->err, cond,
+                     use_cond, h->hs);
+    return;
+  }
+  launch_plan(PLAN_DRAFT, h->rows, h->st, h->slot_req, n_slots, B, 0, nullptr, nullptr, cap, h->hs);
+  enqueue_forward(h, PLAN_DRAFT, n_slots, B, 0, h->dbuf, nullptr);
+  launch_override(h->st, h->slot_req, n_slots, B, h->dbuf, h->ref, cap, h->sched, h->sched_cap,
+                  h->cfg.vocab, h->hs);
+  launch_plan(PLAN_VERIFY, h->rows, h->st, h->slot_req, n_slots, B, 0, h->dbuf, nullptr, cap, h->hs);
+  enqueue_forward(h, PLAN_VERIFY, n_slots, B, 0, h->vbuf, nullptr);
+  launch_accept(h->st, h->slot_req, n_slots, B, h->dbuf, h->vbuf, h->out, out_stride, h->err, cond,
+                use_cond, h->hs);
+}
+
+int get_graph(gocr_handle* h, int mode, int B, int n_slots, cudaGraphExec_t* exec) {
+  for (auto& g : h->graphs)
+    if (g.mode == mode && g.B == B && g.n_slots == n_slots) { *exec = g.exec; return GOCR_OK; }
+  GraphEntry e{mode, B, n_slots, nullptr, nullptr};
+  CK(cudaGraphCreate(&e.graph, 0));
+  cudaGraphConditionalHandle ch;
+  CK(cudaGraphConditionalHandleCreate(&ch, e.graph, 1, cudaGraphCondAssignDefault));
+  cudaGraphNodeParams np{};
+  np.type = cudaGraphNodeTypeConditional;
+  np.conditional.handle = ch;
+  np.conditional.type = cudaGraphCondTypeWhile;
+  np.conditional.size = 1;
+  cudaGraphNode_t node;
+  CK(cudaGraphAddNode(&node, e.graph, nullptr, nullptr, 0, &np));
+  cudaGraph_t body = np.conditional.phGraph_out[0];
+  CK(cudaStreamBeginCaptureToGraph(h->hs, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
+  enqueue_round(h, mode, B, n_slots, (unsigned long long)ch, 1);
+  cudaError_t le = cudaGetLastError();
+  cudaGraph_t captured = nullptr;
+  cudaError_t ce = cudaStreamEndCapture(h->hs, &captured);
+  if (le != cudaSuccess) return fail(h, GOCR_ECUDA, "launch during capture: %s", cudaGetErrorString(le));
+  if (ce != cudaSuccess) return fail(h, GOCR_ECUDA, "cudaStreamEndCapture: %s", cudaGetErrorString(ce));
+  CK(cudaGraphInstantiate(&e.exec, e.graph, 0));
+  h->graphs.push_back(e);
+  *exec = e.exec;
+  return GOCR_OK;
+}
+
+int check_req(gocr_handle* h, int req) {
+  if (!h) return fail(nullptr, GOCR_EINVAL, "null handle");
+  if (req < 0 || req >= h->cfg.max_requests) return fail(h, GOCR_EINVAL, "request slot %d out of range", req);
+  return GOCR_OK;
+}
+
+// Order the handle's private stream after the caller's stream (NULL = the legacy
+// default stream), so inputs the caller produced there are complete.
+int sync_user(gocr_handle* h) {
+  CK(cudaEventRecord(h->evu, h->user));
+  CK(cudaStreamWaitEvent(h->hs, h->evu, 0));
+  return GOCR_OK;
+}
+
+int read_state(gocr_handle* h, int req, ReqState* out) {
+  CK(cudaMemcpyAsync(out, h->st + req, sizeof(ReqState), cudaMemcpyDeviceToHost, h->hs));
+  CK(cudaStreamSynchronize(h->hs));
+  return GOCR_OK;
+}
+
+int dev_err_code(int e) {
+  if (e == DERR_ROUND_LIMIT) return GOCR_ETIMEOUT;
+  if (e == DERR_CAPACITY) return GOCR_ECAPACITY;
+  return GOCR_EDEVICE;
+}
+
+const char* dev_err_name(int e) {
+  switch (e) {
+    case DERR_NAN_LOGITS: return "NaN in logits";
+    case DERR_CAPACITY: return "KV capacity exceeded on the device";
+    case DERR_ROUND_LIMIT: return "round limit reached";
+    case DERR_BAD_TOKEN: return "token id out of range";
+    default: return "device error";
+  }
+}
+
+int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const int* max_new,
+               int32_t* const* out_tokens, gocr_stats* stats) {
+  const gocr_config& c = h->cfg;
+  if (mode != GOCR_MODE_AR && mode != GOCR_MODE_SELFSPEC) return fail(h, GOCR_EINVAL, "bad mode %d", mode);
+  if (n < 1 || n > c.max_requests) return fail(h, GOCR_EINVAL, "bad request count %d", n);
+  if (mode == GOCR_MODE_SELFSPEC && (B < 1 || B > c.max_block))
+    return fail(h, GOCR_ECAPACITY, "block size %d outside 1..%d", B, c.max_block);
+  if (mode == GOCR_MODE_AR) B = 0;
+  int rows = mode == GOCR_MODE_AR ? n : n * (B + 1);
+  if (rows > h->T_dec) return fail(h, GOCR_ECAPACITY, "%d rows per forward exceed %d", rows, h->T_dec);
+  int bound = 0;
+  for (int i = 0; i < n; ++i) {
+    int r = check_req(h, reqs[i]);
+    if (r) return r;
+    for (int j = 0; j < i; ++j)
+      if (reqs[j] == reqs[i]) return fail(h, GOCR_EINVAL, "request %d listed twice", reqs[i]);
+    if (!h->prefilled[reqs[i]]) return fail(h, GOCR_ESTATE, "request %d has no prefill", reqs[i]);
+    if (!out_tokens || !out_tokens[i]) return fail(h, GOCR_EINVAL, "null out_tokens");
+    if (max_new[i] < 1 || max_new[i] > h->cap) return fail(h, GOCR_EINVAL, "bad max_new %d", max_new[i]);
+    ReqState s;
+    int rc = read_state(h, reqs[i], &s);
+    if (rc) return rc;
+    // prefix length P = cache_len - committed + 1; the last round writes up to P + max_new + B
+    int need = (s.cache_len - s.committed + 1) + max_new[i] + B + 2;
+    if (need > h->cap)
+      return fail(h, GOCR_ECAPACITY, "request %d needs %d KV positions, capacity %d", reqs[i], need, h->cap);
+    if (max_new[i] > bound) bound = max_new[i];
+  }
+  CK(cudaMemcpyAsync(h->slot_req, reqs, sizeof(int) * n, cudaMemcpyHostToDevice, h->hs));
+  CK(cudaMemcpyAsync(h->max_new_dev, max_new, sizeof(int) * n, cudaMemcpyHostToDevice, h->hs));
+  CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
+  launch_begin_decode(h->st, h->slot_req, n, h->max_new_dev, bound + 2, c.eos_id, h->hs);
+  CK(cudaGetLastError());
+  cudaGraphExec_t exec;
+  int rc = get_graph(h, mode, B, n, &exec);
+  if (rc) return rc;
+  CK(cudaEventRecord(h->ev0, h->hs));
+  CK(cudaGraphLaunch(exec, h->hs));
+  CK(cudaEventRecord(h->ev1, h->hs));
+  std::vector<ReqState> sts(n);
+  for (int i = 0; i < n; ++i) {
+    CK(cudaMemcpyAsync(&sts[i], h->st + reqs[i], sizeof(ReqState), cudaMemcpyDeviceToHost, h->hs));
+    CK(cudaMemcpyAsync(out_tokens[i], h->out + (size_t)reqs[i] * h->cap, sizeof(int) * max_new[i],
+                       cudaMemcpyDeviceToHost, h->hs));
+  }
+  CK(cudaStreamSynchronize(h->hs));
+  float ms = 0.f;
+  CK(cudaEventElapsedTime(&ms, h->ev0, h->ev1));
+  int ret = GOCR_OK;
+  for (int i = 0; i < n; ++i) {
+    const ReqState& s = sts[i];
+    if (stats) {
+      gocr_stats& o = stats[i];
+      o.rounds = s.st_rounds; o.forwards = s.st_forwards; o.committed = s.st_committed;
+      o.accepted_drafts = s.st_accepted;
+      for (int k = 0; k <= GOCR_MAX_BLOCK; ++k) o.accept_hist[k] = s.hist[k];
+      o.device_ms = ms;
+    }
+    if (s.error && ret == GOCR_OK)
+      ret = fail(h, dev_err_code(s.error), "request %d: %s", reqs[i], dev_err_name(s.error));
+  }
+  return ret;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, gocr_alloc_fn alloc,
+                gocr_free_fn free_fn, void* alloc_user, gocr_handle** out) {
+  gocr_handle* h = nullptr;
+  if (!cfg || !w || !out) return fail(nullptr, GOCR_EINVAL, "null argument");
+  *out = nullptr;
+  const gocr_config c = *cfg;
+  const int q_dim = c.n_q_heads * c.head_dim, kv_dim = c.n_kv_heads * c.head_dim;
+  if (c.n_layers < 1 || c.hidden < 128 || c.hidden % 128 || c.vocab < 128 || c.vocab % 128 ||
+      (c.head_dim != 64 && c.head_dim != 128) || c.n_kv_heads < 1 || c.n_q_heads % c.n_kv_heads ||
+      q_dim % 128 || kv_dim % 128 || c.ffn < 64 || c.ffn % 64 ||
+      (c.dtype != GOCR_DTYPE_F32 && c.dtype != GOCR_DTYPE_BF16))
+    return fail(nullptr, GOCR_EINVAL, "unsupported model shape");
+  if (c.max_block < 1 || c.max_block > GOCR_MAX_BLOCK || c.max_requests < 1 || c.max_requests > MAX_REQ ||
+      c.max_ctx < c.max_block + 4 || c.max_ctx > (1 << 20) || c.eos_id >= c.vocab)
+    return fail(nullptr, GOCR_EINVAL, "bad capacity settings");
+  if (!w->embed || !w->mask_embed || !w->lm_head || !w->g_final || !w->layer)
+    return fail(nullptr, GOCR_EINVAL, "null weight pointer");
+  for (int i = 0; i < c.n_layers * GOCR_LAYER_TENSORS; ++i)
+    if (!w->layer[i]) return fail(nullptr, GOCR_EINVAL, "null layer tensor %d", i);
+  if ((alloc == nullptr) != (free_fn == nullptr)) return fail(nullptr, GOCR_EINVAL, "alloc and free come together");
+
+  h = new gocr_handle();
+  h->cfg = c;
+  h->dtype = c.dtype;
+  h->es = c.dtype == GOCR_DTYPE_BF16 ? 2 : 4;
+  h->af = alloc; h->ff = free_fn; h->au = alloc_user;
+  h->user = (cudaStream_t)stream;
+  h->q_dim = q_dim; h->kv_dim = kv_dim;
+  h->qkv_n = q_dim + 2 * kv_dim;
+  h->gu_n = 2 * c.ffn;
+  h->cap = c.max_ctx;
+  h->T_dec = c.max_requests * (c.max_block + 1);
+  h->T_max = h->T_dec > c.max_ctx ? h->T_dec : c.max_ctx;
+  h->sched_cap = c.max_ctx;
+  h->layer_stride = (long long)c.n_kv_heads * h->cap * c.head_dim;
+  h->req_stride = h->layer_stride * c.n_layers;
+  *out = h;  // freed by gocr_free on any later failure
+#define CKC(call)                                                                  \
+  do {                                                                             \
+    cudaError_t e_ = (call);                                                       \
+    if (e_ != cudaSuccess) {                                                       \
+      int r_ = fail(h, GOCR_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_)); \
+      g_lib_error = h->msg; gocr_free(h); *out = nullptr; return r_;               \
+    }                                                                              \
+  } while (0)
+  CKC(cudaStreamCreateWithFlags(&h->hs, cudaStreamNonBlocking));
+  CKC(cudaEventCreate(&h->ev0));
+  CKC(cudaEventCreate(&h->ev1));
+  CKC(cudaEventCreateWithFlags(&h->evu, cudaEventDisableTiming));
+  CKC(cudaEventRecord(h->evu, h->user));
+  CKC(cudaStreamWaitEvent(h->hs, h->evu, 0));
+
+  const int H = c.hidden, R = c.max_requests, T = h->T_max;
+  const size_t es = h->es;
+  bool ok = true;
+  auto A = [&](size_t bytes) { void* p = dev_alloc(h, bytes); if (!p) ok = false; return p; };
+  h->embed = w->embed; h->mask = w->mask_embed; h->lm = w->lm_head; h->gfin = w->g_final;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const void* const* L = w->layer + (size_t)l * GOCR_LAYER_TENSORS;
+    void* qkv = A((size_t)h->qkv_n * H * es);
+    void* gu = A((size_t)h->gu_n * H * es);
+    if (!ok) break;
+    CKC(cudaMemcpyAsync(qkv, L[0], (size_t)q_dim * H * es, cudaMemcpyDeviceToDevice, h->hs));
+    CKC(cudaMemcpyAsync((char*)qkv + (size_t)q_dim * H * es, L[1], (size_t)kv_dim * H * es,
+                        cudaMemcpyDeviceToDevice, h->hs));
+    CKC(cudaMemcpyAsync((char*)qkv + (size_t)(q_dim + kv_dim) * H * es, L[2], (size_t)kv_dim * H * es,
+                        cudaMemcpyDeviceToDevice, h->hs));
+    // gate/up interleaved in groups of 64 rows: [g 64 rows][u 64 rows] ...
+    const size_t grp = (size_t)SWIGLU_GROUP * H * es;
+    CKC(cudaMemcpy2DAsync(gu, 2 * grp, L[4], grp, grp, c.ffn / SWIGLU_GROUP, cudaMemcpyDeviceToDevice, h->hs));
+    CKC(cudaMemcpy2DAsync((char*)gu + grp, 2 * grp, L[5], grp, grp, c.ffn / SWIGLU_GROUP,
+                          cudaMemcpyDeviceToDevice, h->hs));
+    h->wqkv.push_back(qkv); h->wgu.push_back(gu);
+    h->wo.push_back(L[3]); h->wd.push_back(L[6]);
+    h->gattn.push_back((const float*)L[7]); h->gmlp.push_back((const float*)L[8]);
+  }
+  const size_t kv_elems = (size_t)h->req_stride * R;
+  h->kc = A(kv_elems * es);
+  h->vc = A(kv_elems * es);
+  h->resid = (float*)A((size_t)T * H * 4);
+  h->xn = A((size_t)T * H * es);
+  h->qbuf = A((size_t)T * q_dim * es);
+  h->att = A((size_t)T * q_dim * es);
+  h->hbuf = A((size_t)T * c.ffn * es);
+  h->xlog = A((size_t)h->T_dec * H * es);
+  h->logits = (float*)A((size_t)h->T_dec * c.vocab * 4);
+  h->dbuf = (int*)A((size_t)h->T_dec * 4);
+  h->vbuf = (int*)A((size_t)h->T_dec * 4);
+  h->abuf = (int*)A((size_t)h->T_dec * 4);
+  h->am = (int*)A((size_t)h->T_dec * 4);
+  h->rows.plan = (Plan*)A(sizeof(Plan));
+  h->rows.row_slot = (int*)A((size_t)T * 4);
+  h->rows.row_pos = (int*)A((size_t)T * 4);
+  h->rows.row_lim = (int*)A((size_t)T * 4);
+  h->rows.row_tok = (int*)A((size_t)T * 4);
+  h->rows.logit_row = (int*)A((size_t)T * 4);
+  h->slot_req = (int*)A(MAX_REQ * 4);
+  h->slot_one = (int*)A(MAX_REQ * 4);
+  h->max_new_dev = (int*)A(MAX_REQ * 4);
+  h->st = (ReqState*)A(sizeof(ReqState) * R);
+  h->out = (int*)A((size_t)R * h->cap * 4);
+  h->ref = (int*)A((size_t)R * h->cap * 4);
+  h->sched = (int*)A((size_t)R * h->sched_cap * 4);
+  h->err = (int*)A(256);
+  h->dbg_toks = (int*)A((size_t)h->T_dec * 4);
+  h->rope = (float2*)A((size_t)h->cap * (c.head_dim / 2) * sizeof(float2));
+  h->prefix_stage = A((size_t)c.max_ctx * H * es);
+  // split-K workspace: decode shapes with their fixed splits, prefill with one split
+  size_t wsf = 0;
+  const int shapes[5][2] = {{h->qkv_n, H}, {H, q_dim}, {h->gu_n, H}, {H, c.ffn}, {c.vocab, H}};
+  int ctr = 0;
+  for (auto& s : shapes) {
+    size_t a = gemm_ws_floats(h->T_dec, s[0], s[1], false);
+    size_t b = gemm_ws_floats(c.max_ctx, s[0], s[1], true);
+    if (a > wsf) wsf = a;
+    if (b > wsf) wsf = b;
+    int ci = gemm_counter_ints(h->T_max, s[0]);
+    if (ci > ctr) ctr = ci;
+  }
+  h->ws_floats = wsf;
+  h->ws = (float*)A(wsf * 4);
+  h->counters = (int*)A((size_t)ctr * 4);
+  const int n_tiles_lm = (c.vocab + NTILE - 1) / NTILE;
+  h->pmax = (float*)A((size_t)n_tiles_lm * h->T_max * 4);
+  h->pidx = (int*)A((size_t)n_tiles_lm * h->T_max * 4);
+  if (!ok) {
+    int r = fail(h, GOCR_ENOMEM, "device allocation failed");
+    g_lib_error = h->msg;
+    gocr_free(h);
+    *out = nullptr;
+    return r;
+  }
+  launch_rope_table(h->rope, h->cap, c.head_dim, c.rope_theta, h->hs);
+  CKC(cudaGetLastError());
+  CKC(cudaStreamSynchronize(h->hs));
+#undef CKC
+  return GOCR_OK;
+}
+
+int gocr_prefill(gocr_handle* h, int req, const void* prefix_embeds, int P) {
+  int r = check_req(h, req);
+  if (r) return r;
+  if (!prefix_embeds) return fail(h, GOCR_EINVAL, "null prefix");
+  if (P < 1) return fail(h, GOCR_EINVAL, "prefix length %d", P);
+  if (P + 1 > h->cap) return fail(h, GOCR_ECAPACITY, "prefix %d exceeds capacity %d", P, h->cap);
+  if ((r = sync_user(h))) return r;
+  CK(cudaMemcpyAsync(h->prefix_stage, prefix_embeds, (size_t)P * h->cfg.hidden * h->es,
+                     cudaMemcpyDefault, h->hs));
+  CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
+  CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
+  launch_plan(PLAN_PREFILL, h->rows, h->st, h->slot_one, 1, 0, P, nullptr, nullptr, h->cap, h->hs);
+  enqueue_forward(h, PLAN_PREFILL, 1, 0, P, h->am, nullptr);
+  launch_prefill_finish(h->st, req, P, h->am, h->out, h->cap, h->hs);
+  CK(cudaGetLastError());
+  int e = 0;
+  CK(cudaMemcpyAsync(&e, h->err, sizeof(int), cudaMemcpyDeviceToHost, h->hs));
+  CK(cudaStreamSynchronize(h->hs));
+  if (e) return fail(h, dev_err_code(e), "prefill: %s", dev_err_name(e));
+  h->prefilled[req] = true;
+  return GOCR_OK;
+}
+
+int gocr_decode(gocr_handle* h, int req, int mode, int B, int max_new, int32_t* out_tokens,
+                gocr_stats* stats) {
+  int r = check_req(h, req);
+  if (r) return r;
+  if ((r = sync_user(h))) return r;
+  int32_t* outs[1] = {out_tokens};
+  return run_decode(h, 1, &req, mode, B, &max_new, outs, stats);
+}
+
+int gocr_decode_batch(gocr_handle* h, int n_req, const int32_t* reqs, int mode, int B,
+                      const int32_t* max_new, int32_t* const* out_tokens, gocr_stats* stats) {
+  if (!h) return fail(nullptr, GOCR_EINVAL, "null handle");
+  if (!reqs || !max_new || !out_tokens) return fail(h, GOCR_EINVAL, "null argument");
+  int r = sync_user(h);
+  if (r) return r;
+  return run_decode(h, n_req, reqs, mode, B, max_new, out_tokens, stats);
+}
+
+int gocr_set_draft_override(gocr_handle* h, int req, const int32_t* ref_tokens, int n_ref,
+                            const int32_t* schedule, int n_rounds) {
+  int r = check_req(h, req);
+  if (r) return r;
+  if (n_ref < 0 || n_ref > h->cap || n_rounds < 0 || n_rounds > h->sched_cap)
+    return fail(h, GOCR_ECAPACITY, "override sizes out of range");
+  if (n_ref > 0 && (!ref_tokens || (n_rounds > 0 && !schedule)))
+    return fail(h, GOCR_EINVAL, "null override array");
+  for (int i = 0; i < n_ref; ++i)
+    if (ref_tokens[i] < 0 || ref_tokens[i] >= h->cfg.vocab) return fail(h, GOCR_EINVAL, "reference token out of range");
+  for (int i = 0; i < n_rounds; ++i)
+    if (schedule[i] < 0) return fail(h, GOCR_EINVAL, "negative schedule entry");
+  if (n_ref > 0) {
+    CK(cudaMemcpyAsync(h->ref + (size_t)req * h->cap, ref_tokens, sizeof(int) * n_ref,
+                       cudaMemcpyHostToDevice, h->hs));
+    if (n_rounds > 0)
+      CK(cudaMemcpyAsync(h->sched + (size_t)req * h->sched_cap, schedule, sizeof(int) * n_rounds,
+                         cudaMemcpyHostToDevice, h->hs));
+  }
+  launch_set_override(h->st, req, n_ref, n_ref > 0 ? n_rounds : 0, h->hs);
+  CK(cudaGetLastError());
+  CK(cudaStreamSynchronize(h->hs));
+  return GOCR_OK;
+}
+
+int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens, int n,
+                       float* logits_out) {
+  int r = check_req(h, req);
+  if (r) return r;
+  if (!h->prefilled[req]) return fail(h, GOCR_ESTATE, "request %d has no prefill", req);
+  if (!tokens) return fail(h, GOCR_EINVAL, "null tokens");
+  int pk, B = 0;
+  if (kind == GOCR_FWD_AR) {
+    if (n != 1) return fail(h, GOCR_EINVAL, "AR forward takes one token");
+    pk = PLAN_AR;
+  } else if (kind == GOCR_FWD_DRAFT || kind == GOCR_FWD_VERIFY) {
+    B = n - 1;
+    if (B < 1 || B > h->cfg.max_block) return fail(h, GOCR_ECAPACITY, "block %d out of range", B);
+    pk = kind == GOCR_FWD_DRAFT ? PLAN_DRAFT : PLAN_VERIFY;
+  } else {
+    return fail(h, GOCR_EINVAL, "bad forward kind %d", kind);
+  }
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return fail(h, GOCR_EINVAL, "token out of range");
+  ReqState s;
+  if ((r = read_state(h, req, &s))) return r;
+  if (s.cache_len + n + 1 > h->cap) return fail(h, GOCR_ECAPACITY, "window exceeds capacity");
+  CK(cudaMemcpyAsync(h->dbg_toks, tokens, sizeof(int) * n, cudaMemcpyHostToDevice, h->hs));
+  CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
+  CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
+  launch_plan(pk, h->rows, h->st, h->slot_one, 1, B, 0, nullptr, h->dbg_toks, h->cap, h->hs);
+  enqueue_forward(h, pk, 1, B, 0, h->am, h->logits);
+  CK(cudaGetLastError());
+  if (logits_out)
+    CK(cudaMemcpyAsync(logits_out, h->logits, sizeof(float) * n * h->cfg.vocab, cudaMemcpyDeviceToHost, h->hs));
+  int e = 0;
+  CK(cudaMemcpyAsync(&e, h->err, sizeof(int), cudaMemcpyDeviceToHost, h->hs));
+  CK(cudaStreamSynchronize(h->hs));
+  if (e) return fail(h, dev_err_code(e), "debug forward: %s", dev_err_name(e));
+  return GOCR_OK;
+}
+
+int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, void* k_out, void* v_out) {
+  int r = check_req(h, req);
+  if (r) return r;
+  const gocr_config& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || pos0 + n > h->cap || !k_out || !v_out)
+    return fail(h, GOCR_EINVAL, "bad KV range");
+  const size_t es = h->es, d = c.head_dim;
+  for (int kvh = 0; kvh < c.n_kv_heads; ++kvh) {
+    size_t off = ((size_t)req * h->req_stride + (size_t)layer * h->layer_stride +
+                  ((size_t)kvh * h->cap + pos0) * d) * es;
+    CK(cudaMemcpy2DAsync((char*)k_out + kvh * d * es, c.n_kv_heads * d * es, (char*)h->kc + off, d * es,
+                         d * es, n, cudaMemcpyDeviceToHost, h->hs));
+    CK(cudaMemcpy2DAsync((char*)v_out + kvh * d * es, c.n_kv_heads * d * es, (char*)h->vc + off, d * es,
+                         d * es, n, cudaMemcpyDeviceToHost, h->hs));
+  }
+  CK(cudaStreamSynchronize(h->hs));
+  return GOCR_OK;
+}
+
+int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0) {
+  int r = check_req(h, req);
+  if (r) return r;
+  ReqState s;
+  if ((r = read_state(h, req, &s))) return r;
+  if (cache_len) *cache_len = s.cache_len;
+  if (x0) *x0 = s.x0;
+  return GOCR_OK;
+}
+
+const char* gocr_last_error(const gocr_handle* h) {
+  return h ? h->msg.c_str() : g_lib_error.c_str();
+}
+
+void gocr_free(gocr_handle* h) {
+  if (!h) return;
+  if (h->hs) cudaStreamSynchronize(h->hs);
+  for (auto& g : h->graphs) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+  }
+  for (void* p : h->allocs) {
+    if (h->ff) h->ff(p, h->au); else cudaFree(p);
+  }
+  if (h->ev0) cudaEventDestroy(h->ev0);
+  if (h->ev1) cudaEventDestroy(h->ev1);
+  if (h->evu) cudaEventDestroy(h->evu);
+  if (h->hs) cudaStreamDestroy(h->hs);
+  delete h;
+}
+
+// ---------------------------------------------------------------- single kernels
+
+size_t gocr_op_linear_workspace(int T, int N, int K) {
+  if (T < 1 || N < 1 || K < 1) return 0;
+  size_t ctr = ((size_t)gemm_counter_ints(T, N) * 4 + 255) & ~(size_t)255;
+  return ctr + gemm_ws_floats(T, N, K, false) * 4;
+}
+
+int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int N, int K,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  gocr_handle* h = nullptr;
+  if (dtype != GOCR_DTYPE_F32 && dtype != GOCR_DTYPE_BF16) return fail(h, GOCR_EINVAL, "bad dtype");
+  if (!x || !w || !y || !workspace) return fail(h, GOCR_EINVAL, "null pointer");
+  if (T < 1 || N < 1 || K < 8 || K % 8) return fail(h, GOCR_EINVAL, "bad shape T=%d N=%d K=%d", T, N, K);
+  if (workspace_bytes < gocr_op_linear_workspace(T, N, K)) return fail(h, GOCR_ECAPACITY, "workspace too small");
+  GemmArgs a{};
+  a.x = x; a.ldx = K; a.w = w; a.T = T; a.N = N; a.K = K;
+  a.kchunk = gemm_kchunk(N, K); a.splits = gemm_splits(N, K);
+  a.counters = (int*)workspace;
+  size_t ctr = ((size_t)gemm_counter_ints(T, N) * 4 + 255) & ~(size_t)255;
+  a.ws = (float*)((char*)workspace + ctr);
+  a.epi = EPI_STORE;
+  a.e.y = y; a.e.ldy = N;
+  launch_gemm(dtype, a, (cudaStream_t)stream);
+  CK(cudaGetLastError());
+  return GOCR_OK;
+}
+
+int gocr_op_rmsnorm(int dtype, const float* x, const float* g, void* y, int T, int H, float eps,
+                    void* stream) {
+  gocr_handle* h = nullptr;
+  if (dtype != GOCR_DTYPE_F32 && dtype != GOCR_DTYPE_BF16) return fail(h, GOCR_EINVAL, "bad dtype");
+  if (!x || !g || !y || T < 1 || H < 1) return fail(h, GOCR_EINVAL, "bad arguments");
+  launch_rmsnorm(dtype, x, H, g, y, H, T, H, eps, nullptr, nullptr, 0, (cudaStream_t)stream);
+  CK(cudaGetLastError());
+  return GOCR_OK;
+}
+
+int gocr_op_attention(int dtype, const void* q, const void* kc, const void* vc, void* o,
+                      const int32_t* lim, int T, int Hq, int Hkv, int d, int cap, void* stream) {
+  gocr_handle* h = nullptr;
+  if (dtype != GOCR_DTYPE_F32 && dtype != GOCR_DTYPE_BF16) return fail(h, GOCR_EINVAL, "bad dtype");
+  if (!q || !kc || !vc || !o || !lim) return fail(h, GOCR_EINVAL, "null pointer");
+  if (T < 1 || Hkv < 1 || Hq % Hkv || (d != 64 && d != 128) || cap < 1)
+    return fail(h, GOCR_EINVAL, "bad shape");
+  AttnArgs a{};
+  a.q = q; a.kc = kc; a.vc = vc; a.req_stride = 0; a.o = o; a.row_lim = lim; a.plan = nullptr;
+  a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.cap = cap; a.scale = 1.0f / sqrtf((float)d);
+  launch_attention(dtype, a, 1, T, (cudaStream_t)stream);
+  CK(cudaGetLastError());
+  return GOCR_OK;
+}
+
+}  // extern "C"

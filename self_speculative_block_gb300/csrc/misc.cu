@@ -1,0 +1,327 @@
+// Row-table, embedding, RMSNorm and round-control kernels.
+//
+// Round control follows GravityOCR's decode round (review §3.2 and
+// Appendix B.2; velog review, inference section):
+//   * the cache holds the causal state of every committed token but the
+//     boundary token x0, which sits at position p = cache_len;
+//   * draft rows [x0, M x B] sit at p..p+B; verify rows [a0, d1..dB] at
+//     p+1..p+B+1;
+//   * A = longest prefix with d_j == a_j; the round commits a0, d1..dA and
+//     a_(A+1) (at most max_new - committed, cut after eos), keeps cache
+//     positions 0..p+A+1 and makes a_(A+1) the next boundary.
+#include "epilogue.cuh"
+
+namespace gocr {
+
+// ---------------------------------------------------------------- RMSNorm
+// y[t] = x[src] / sqrt(mean(x[src]^2) + eps) * g, src = gather ? gather[t] : t.
+// One CTA per row; the sum of squares is reduced in a fixed order.
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, int ldx, const float* g, T* y,
+                                                       int ldy, int T_rows, int H, float eps,
+                                                       const int* gather, const Plan* plan,
+                                                       int which_count) {
+  int t = blockIdx.x;
+  int n = T_rows;
+  if (plan) n = which_count ? plan->n_logit_rows : plan->n_rows;
+  if (t >= n) return;
+  const int src = gather ? gather[t] : t;
+  const float* xr = x + (size_t)src * ldx;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
+  __shared__ float red[32];
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    float v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float rstd = rsqrtf(red[0] / (float)H + eps);
+  T* yr = y + (size_t)t * ldy;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) yr[i] = from_f32<T>(xr[i] * rstd * g[i]);
+}
+
+void launch_rmsnorm(int dtype, const float* x, int ldx, const float* g, void* y, int ldy, int T,
+                    int H, float eps, const int* gather, const Plan* plan, int which_count,
+                    cudaStream_t s) {
+  if (T <= 0) return;
+  if (dtype == 1)
+    rmsnorm_kernel<bf16><<<T, 256, 0, s>>>(x, ldx, g, (bf16*)y, ldy, T, H, eps, gather, plan, which_count);
+  else
+    rmsnorm_kernel<float><<<T, 256, 0, s>>>(x, ldx, g, (float*)y, ldy, T, H, eps, gather, plan, which_count);
+}
+
+// ---------------------------------------------------------------- embedding rows
+template <typename T>
+__global__ void embed_kernel(const T* embed, const T* mask_embed, const T* prefix, float* resid,
+                             Rows r, int H, int vocab, int* err) {
+  const int t = blockIdx.x;
+  if (t >= r.plan->n_rows) return;
+  const int tok = r.row_tok[t];
+  const T* src;
+  if (tok >= 0) {
+    if (tok >= vocab) {
+      if (threadIdx.x == 0) set_err(err, DERR_BAD_TOKEN);
+      return;
+    }
+    src = embed + (size_t)tok * H;
+  } else if (tok == TOK_MASK) {
+    src = mask_embed;
+  } else {
+    src = prefix + (size_t)(-2 - tok) * H;
+  }
+  for (int i = threadIdx.x; i < H; i += blockDim.x) resid[(size_t)t * H + i] = to_f32<T>(src[i]);
+}
+
+void launch_embed(int dtype, const void* embed, const void* mask_embed, const void* prefix,
+                  float* resid, const Rows& r, int T, int H, int vocab, int* err, cudaStream_t s) {
+  if (dtype == 1)
+    embed_kernel<bf16><<<T, 256, 0, s>>>((const bf16*)embed, (const bf16*)mask_embed,
+                                         (const bf16*)prefix, resid, r, H, vocab, err);
+  else
+    embed_kernel<float><<<T, 256, 0, s>>>((const float*)embed, (const float*)mask_embed,
+                                          (const float*)prefix, resid, r, H, vocab, err);
+}
+
+// ---------------------------------------------------------------- rotary table
+// cos/sin of pos * theta^(-2i/d), evaluated in double and rounded once.
+__global__ void rope_table_kernel(float2* tab, int cap, int d, double theta) {
+  const int half = d / 2;
+  size_t n = (size_t)cap * half;
+  for (size_t x = blockIdx.x * (size_t)blockDim.x + threadIdx.x; x < n; x += (size_t)gridDim.x * blockDim.x) {
+    int pos = (int)(x / half), i = (int)(x % half);
+    double inv = pow(theta, -2.0 * i / d);
+    double ang = (double)pos * inv;
+    tab[x] = make_float2((float)cos(ang), (float)sin(ang));
+  }
+}
+
+void launch_rope_table(float2* tab, int cap, int d, float theta, cudaStream_t s) {
+  rope_table_kernel<<<256, 256, 0, s>>>(tab, cap, d, (double)theta);
+}
+
+// ---------------------------------------------------------------- row tables
+// Slot layout: slot s owns rows [s*w, (s+1)*w) with w = 1 (AR), B+1 (draft,
+// verify) or P (prefill, one slot).
+__global__ void plan_kernel(int kind, Rows r, ReqState* st, const int* slot_req, int n_slots, int B,
+                            int prefill_len, const int* dbuf, const int* toks, int cap) {
+  const int w = kind == PLAN_AR ? 1 : (kind == PLAN_PREFILL ? prefill_len : B + 1);
+  const int n_rows = w * n_slots;
+  Plan* pl = r.plan;
+  for (int t = threadIdx.x; t < n_rows; t += blockDim.x) {
+    const int s = t / w, j = t % w;
+    const int req = slot_req[s];
+    const int p = kind == PLAN_PREFILL ? 0 : st[req].cache_len;
+    int pos, lim, tok;
+    switch (kind) {
+      case PLAN_AR:
+        pos = p; lim = p; tok = toks ? toks[t] : st[req].x0;
+        break;
+      case PLAN_DRAFT:
+        pos = p + j; lim = j == 0 ? p : p + B;
+        tok = j == 0 ? (toks ? toks[s * w] : st[req].x0) : TOK_MASK;
+        break;
+      case PLAN_VERIFY:
+        pos = p + 1 + j; lim = pos; tok = toks ? toks[t] : dbuf[t];
+        break;
+      default:  // PLAN_PREFILL
+        pos = j; lim = j; tok = tok_prefix(j);
+        break;
+    }
+    if (pos >= cap) { pos = cap - 1; lim = min(lim, cap - 1); }
+    r.row_slot[t] = s;
+    r.row_pos[t] = pos;
+    r.row_lim[t] = lim;
+    r.row_tok[t] = tok;
+    r.logit_row[t] = kind == PLAN_PREFILL ? (s + 1) * w - 1 : t;
+  }
+  if (threadIdx.x < n_slots) {
+    const int s = threadIdx.x;
+    const int req = slot_req[s];
+    const int p = kind == PLAN_PREFILL ? 0 : st[req].cache_len;
+    pl->slot_req[s] = req;
+    pl->slot_row0[s] = s * w;
+    pl->slot_nrows[s] = w;
+    int ml = kind == PLAN_PREFILL ? w - 1 : (kind == PLAN_AR ? p : (kind == PLAN_DRAFT ? p + B : p + B + 1));
+    pl->slot_maxlim[s] = ml;
+    if (kind != PLAN_PREFILL && p + (kind == PLAN_AR ? 0 : B + 1) >= cap) {
+      st[req].error = DERR_CAPACITY;
+      st[req].done = 1;
+    }
+  }
+  if (threadIdx.x == 0) {
+    pl->n_rows = n_rows;
+    pl->n_slots = n_slots;
+    pl->n_logit_rows = kind == PLAN_PREFILL ? n_slots : n_rows;
+  }
+}
+
+void launch_plan(int kind, const Rows& r, ReqState* st, const int* slot_req, int n_slots, int B,
+                 int prefill_len, const int* dbuf, const int* toks, int cap, cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(kind, r, st, slot_req, n_slots, B, prefill_len, dbuf, toks, cap);
+}
+
+// ---------------------------------------------------------------- commit helpers
+__device__ void finish_round(ReqState& q, int* out_row, const int* commit, int n_commit, int A,
+                             int new_cache_len, int new_x0, int forwards, const int* err) {
+  const int room = q.max_new - q.committed;
+  int n = n_commit < room ? n_commit : room;
+  bool eos = false;
+  if (q.eos_id >= 0) {
+    for (int i = 0; i < n; ++i)
+      if (commit[i] == q.eos_id) { n = i + 1; eos = true; break; }
+  }
+  for (int i = 0; i < n; ++i) out_row[q.committed + i] = commit[i];
+  q.committed += n;
+  q.cache_len = new_cache_len;
+  q.x0 = new_x0;
+  q.st_rounds += 1;
+  q.st_forwards += forwards;
+  q.st_committed += n;
+  q.st_accepted += A;
+  if (A >= 0 && A <= 64) q.hist[A] += 1;
+  q.round += 1;
+  if (err && *err) { q.error = *err; q.done = 1; }
+  if (q.committed >= q.max_new || eos) q.done = 1;
+  if (!q.done && q.round >= q.max_rounds) { q.error = DERR_ROUND_LIMIT; q.done = 1; }
+}
+
+__device__ void set_loop_condition(ReqState* st, const int* slot_req, int n_slots,
+                                   unsigned long long cond, int use_cond) {
+  if (!use_cond) return;
+  int any = 0;
+  for (int s = 0; s < n_slots; ++s) any |= !st[slot_req[s]].done;
+  cudaGraphSetConditional((cudaGraphConditionalHandle)cond, any ? 1u : 0u);
+}
+
+// One thread per slot, one CTA: updates every request, then sets the loop flag.
+__global__ void accept_kernel(ReqState* st, const int* slot_req, int n_slots, int B, const int* dbuf,
+                              const int* vbuf, int* out, int out_stride, const int* err,
+                              unsigned long long cond, int use_cond) {
+  const int s = threadIdx.x;
+  if (s < n_slots) {
+    const int req = slot_req[s];
+    ReqState& q = st[req];
+    if (!q.done) {
+      const int* d = dbuf + s * (B + 1);   // d[0] = a0, d[j] = d_j
+      const int* v = vbuf + s * (B + 1);   // v[j-1] = a_j
+      int A = 0;
+      while (A < B && d[A + 1] == v[A]) ++A;
+      int commit[66];
+      commit[0] = d[0];
+      for (int j = 1; j <= A + 1; ++j) commit[j] = v[j - 1];
+      const int p = q.cache_len;
+      finish_round(q, out + (size_t)req * out_stride, commit, A + 2, A, p + A + 2, v[A], 2, err);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) set_loop_condition(st, slot_req, n_slots, cond, use_cond);
+}
+
+void launch_accept(ReqState* st, const int* slot_req, int n_slots, int B, const int* dbuf,
+                   const int* vbuf, int* out, int out_stride, const int* err,
+                   unsigned long long cond, int use_cond, cudaStream_t s) {
+  accept_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, B, dbuf, vbuf, out, out_stride, err, cond, use_cond);
+}
+
+__global__ void ar_commit_kernel(ReqState* st, const int* slot_req, int n_slots, const int* abuf,
+                                 int* out, int out_stride, const int* err,
+                                 unsigned long long cond, int use_cond) {
+  const int s = threadIdx.x;
+  if (s < n_slots) {
+    const int req = slot_req[s];
+    ReqState& q = st[req];
+    if (!q.done) {
+      int tok = abuf[s];
+      finish_round(q, out + (size_t)req * out_stride, &tok, 1, 0, q.cache_len + 1, tok, 1, err);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) set_loop_condition(st, slot_req, n_slots, cond, use_cond);
+}
+
+void launch_ar_commit(ReqState* st, const int* slot_req, int n_slots, const int* abuf, int* out,
+                      int out_stride, const int* err, unsigned long long cond, int use_cond,
+                      cudaStream_t s) {
+  ar_commit_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, abuf, out, out_stride, err, cond, use_cond);
+}
+
+// Forced-acceptance hook: between draft and verify, per slot.
+__global__ void override_kernel(ReqState* st, const int* slot_req, int n_slots, int B, int* dbuf,
+                                const int* ref, int ref_stride, const int* sched, int sched_stride,
+                                int vocab) {
+  const int s = threadIdx.x;
+  if (s >= n_slots) return;
+  const int req = slot_req[s];
+  const ReqState& q = st[req];
+  if (q.n_ref <= 0 || q.done) return;
+  const int* rr = ref + (size_t)req * ref_stride;
+  const int G = q.round < q.n_sched ? sched[(size_t)req * sched_stride + q.round] : 0;
+  const int c = q.committed;
+  int* d = dbuf + s * (B + 1);
+  for (int j = 1; j <= B && j <= G; ++j)
+    if (c + j < q.n_ref) d[j] = rr[c + j];
+  if (G < B && c + G + 1 < q.n_ref) d[G + 1] = (rr[c + G + 1] + 1) % vocab;
+}
+
+void launch_override(ReqState* st, const int* slot_req, int n_slots, int B, int* dbuf,
+                     const int* ref, int ref_stride, const int* sched, int sched_stride,
+                     int vocab, cudaStream_t s) {
+  override_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, B, dbuf, ref, ref_stride, sched,
+                                   sched_stride, vocab);
+}
+
+__global__ void prefill_finish_kernel(ReqState* st, int req, int P, const int* am, int* out,
+                                      int out_stride) {
+  ReqState& q = st[req];
+  const int t0 = am[0];
+  q.cache_len = P;
+  q.x0 = t0;
+  q.committed = 1;
+  q.done = 0;
+  q.error = 0;
+  q.round = 0;
+  q.st_rounds = q.st_forwards = q.st_committed = q.st_accepted = 0;
+  for (int i = 0; i < 65; ++i) q.hist[i] = 0;
+  out[(size_t)req * out_stride] = t0;
+}
+
+void launch_prefill_finish(ReqState* st, int req, int P, const int* am, int* out, int out_stride,
+                           cudaStream_t s) {
+  prefill_finish_kernel<<<1, 1, 0, s>>>(st, req, P, am, out, out_stride);
+}
+
+__global__ void begin_decode_kernel(ReqState* st, const int* slot_req, int n_slots,
+                                    const int* max_new, int max_rounds, int eos_id) {
+  const int s = threadIdx.x;
+  if (s >= n_slots) return;
+  ReqState& q = st[slot_req[s]];
+  q.max_new = max_new[s];
+  q.max_rounds = max_rounds;
+  q.eos_id = eos_id;
+  q.round = 0;
+  q.error = 0;
+  q.done = q.committed >= q.max_new;
+  q.st_rounds = q.st_forwards = q.st_committed = q.st_accepted = 0;
+  for (int i = 0; i < 65; ++i) q.hist[i] = 0;
+}
+
+void launch_begin_decode(ReqState* st, const int* slot_req, int n_slots, const int* max_new,
+                         int max_rounds, int eos_id, cudaStream_t s) {
+  begin_decode_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, max_new, max_rounds, eos_id);
+}
+
+__global__ void set_override_kernel(ReqState* st, int req, int n_ref, int n_sched) {
+  st[req].n_ref = n_ref;
+  st[req].n_sched = n_sched;
+}
+
+void launch_set_override(ReqState* st, int req, int n_ref, int n_sched, cudaStream_t s) {
+  set_override_kernel<<<1, 1, 0, s>>>(st, req, n_ref, n_sched);
+}
+
+}  // namespace gocr
