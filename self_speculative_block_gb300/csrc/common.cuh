@@ -29,6 +29,7 @@ enum DevErr : int {
   DERR_CAPACITY = 2,
   DERR_ROUND_LIMIT = 3,
   DERR_BAD_TOKEN = 4,
+  DERR_TIMEOUT = 5,     // a bounded wait inside a kernel gave up
 };
 
 constexpr int MAX_REQ = 64;       // request slots per handle (host check)

@@ -10,8 +10,8 @@
 // (AR), B+1 rows (draft / verify) or a batch, which is what makes the GPU's
 // self-speculative output equal its own AR-greedy output token for token.
 //
-// This file is the portable CUDA-core path (fp32 models and the reference
-// implementation of the bf16 path).
+// This file holds the split rule and the CUDA-core kernel of the fp32 models;
+// bf16 models run the tcgen05 kernel of gemm_tc.cu with the same reduction.
 #include "epilogue.cuh"
 
 namespace gocr {
@@ -29,7 +29,7 @@ __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 int gemm_kchunk(int N, int K) {
   const int tiles = cdiv(N, NTILE);
   const int kb = cdiv(K, 64);
-  int want = cdiv(2 * SM_COUNT, tiles);
+  int want = (2 * SM_COUNT) / tiles;  // at most two CTAs per SM in one wave
   int s = want < kb ? want : kb;
   if (s < 1) s = 1;
   return cdiv(kb, s) * 64;
@@ -139,17 +139,11 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
   }
 }
 
-void launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s) {
+bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s) {
+  if (dtype == 1) return launch_gemm_tc(a, s);
   dim3 grid(cdiv(a.N, NTILE), a.splits, cdiv(a.T, TZ));
   size_t smem = sizeof(float) * (NTILE * (KC + 1) + TZ * KC + TZ * YS_LD);
-  if (dtype == 1) {
-    static bool init = false;
-    if (!init) {
-      cudaFuncSetAttribute(gemm_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      init = true;
-    }
-    gemm_simt_kernel<bf16><<<grid, THREADS, smem, s>>>(a);
-  } else {
+  {
     static bool init = false;
     if (!init) {
       cudaFuncSetAttribute(gemm_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -157,6 +151,7 @@ void launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s) {
     }
     gemm_simt_kernel<float><<<grid, THREADS, smem, s>>>(a);
   }
+  return true;
 }
 
 }  // namespace gocr

@@ -148,8 +148,9 @@ GemmArgs gemm_base(gocr_handle* h, const void* x, int ldx, const void* w, int T,
 }
 
 // Enqueue one decoder forward over the rows the plan kernel has laid out.
-void enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out,
+bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out,
                      float* logits) {
+  bool ok = true;
   const gocr_config& c = h->cfg;
   const int T = n_rows_of(kind, n_slots, B, P);
   const bool single = kind == PLAN_PREFILL;  // prefill keeps its own reduction shape
@@ -169,7 +170,7 @@ void enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
     g.e.q_dim = h->q_dim; g.e.kv_dim = h->kv_dim; g.e.head_dim = c.head_dim; g.e.cap = h->cap;
     g.e.rope = h->rope;
     g.e.row_pos = h->rows.row_pos; g.e.row_slot = h->rows.row_slot; g.e.plan = h->rows.plan;
-    launch_gemm(h->dtype, g, h->hs);
+    ok &= launch_gemm(h->dtype, g, h->hs);
     // attention with the row key limits of this forward's mask
     AttnArgs at{};
     at.q = h->qbuf;
@@ -182,17 +183,17 @@ void enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
     // O projection + residual
     GemmArgs go = gemm_base(h, h->att, h->q_dim, h->wo[l], T, H, h->q_dim, single);
     go.epi = EPI_RESID; go.e.y = h->resid; go.e.ldy = H;
-    launch_gemm(h->dtype, go, h->hs);
+    ok &= launch_gemm(h->dtype, go, h->hs);
     launch_rmsnorm(h->dtype, h->resid, H, h->gmlp[l], h->xn, H, T, H, c.rms_eps, nullptr, nullptr,
                    0, h->hs);
     // gate/up (interleaved) + SwiGLU
     GemmArgs gg = gemm_base(h, h->xn, H, h->wgu[l], T, h->gu_n, H, single);
     gg.epi = EPI_SWIGLU; gg.e.hbuf = h->hbuf; gg.e.ldh = c.ffn;
-    launch_gemm(h->dtype, gg, h->hs);
+    ok &= launch_gemm(h->dtype, gg, h->hs);
     // down + residual
     GemmArgs gd = gemm_base(h, h->hbuf, c.ffn, h->wd[l], T, H, c.ffn, single);
     gd.epi = EPI_RESID; gd.e.y = h->resid; gd.e.ldy = H;
-    launch_gemm(h->dtype, gd, h->hs);
+    ok &= launch_gemm(h->dtype, gd, h->hs);
   }
   // final norm on the rows that need logits, then LM head + argmax
   const int n_logit = kind == PLAN_PREFILL ? n_slots : T;
@@ -202,29 +203,32 @@ void enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
   gl.epi = EPI_ARGMAX;
   gl.e.logits = logits; gl.e.ld_logits = c.vocab;
   gl.e.pmax = h->pmax; gl.e.pidx = h->pidx; gl.e.am_out = am_out;
-  launch_gemm(h->dtype, gl, h->hs);
+  ok &= launch_gemm(h->dtype, gl, h->hs);
+  return ok;
 }
 
 // One round (or one AR step) of the decode loop.
-void enqueue_round(gocr_handle* h, int mode, int B, int n_slots, unsigned long long cond,
+bool enqueue_round(gocr_handle* h, int mode, int B, int n_slots, unsigned long long cond,
                    int use_cond) {
+  bool ok = true;
   const int cap = h->cap;
   const int out_stride = cap;
   if (mode == GOCR_MODE_AR) {
     launch_plan(PLAN_AR, h->rows, h->st, h->slot_req, n_slots, 0, 0, nullptr, nullptr, cap, h->hs);
-    enqueue_forward(h, PLAN_AR, n_slots, 0, 0, h->abuf, nullptr);
+    ok &= enqueue_forward(h, PLAN_AR, n_slots, 0, 0, h->abuf, nullptr);
     launch_ar_commit(h->st, h->slot_req, n_slots, h->abuf, h->out, out_stride, h->err, cond,
                      use_cond, h->hs);
-    return;
+    return ok;
   }
   launch_plan(PLAN_DRAFT, h->rows, h->st, h->slot_req, n_slots, B, 0, nullptr, nullptr, cap, h->hs);
-  enqueue_forward(h, PLAN_DRAFT, n_slots, B, 0, h->dbuf, nullptr);
+  ok &= enqueue_forward(h, PLAN_DRAFT, n_slots, B, 0, h->dbuf, nullptr);
   launch_override(h->st, h->slot_req, n_slots, B, h->dbuf, h->ref, cap, h->sched, h->sched_cap,
                   h->cfg.vocab, h->hs);
   launch_plan(PLAN_VERIFY, h->rows, h->st, h->slot_req, n_slots, B, 0, h->dbuf, nullptr, cap, h->hs);
-  enqueue_forward(h, PLAN_VERIFY, n_slots, B, 0, h->vbuf, nullptr);
+  ok &= enqueue_forward(h, PLAN_VERIFY, n_slots, B, 0, h->vbuf, nullptr);
   launch_accept(h->st, h->slot_req, n_slots, B, h->dbuf, h->vbuf, h->out, out_stride, h->err, cond,
                 use_cond, h->hs);
+  return ok;
 }
 
 int get_graph(gocr_handle* h, int mode, int B, int n_slots, cudaGraphExec_t* exec) {
@@ -243,10 +247,11 @@ int get_graph(gocr_handle* h, int mode, int B, int n_slots, cudaGraphExec_t* exe
   CK(cudaGraphAddNode(&node, e.graph, nullptr, nullptr, 0, &np));
   cudaGraph_t body = np.conditional.phGraph_out[0];
   CK(cudaStreamBeginCaptureToGraph(h->hs, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
-  enqueue_round(h, mode, B, n_slots, (unsigned long long)ch, 1);
+  bool enq = enqueue_round(h, mode, B, n_slots, (unsigned long long)ch, 1);
   cudaError_t le = cudaGetLastError();
   cudaGraph_t captured = nullptr;
   cudaError_t ce = cudaStreamEndCapture(h->hs, &captured);
+  if (!enq) return fail(h, GOCR_ECUDA, "TMA descriptor encoding failed");
   if (le != cudaSuccess) return fail(h, GOCR_ECUDA, "launch during capture: %s", cudaGetErrorString(le));
   if (ce != cudaSuccess) return fail(h, GOCR_ECUDA, "cudaStreamEndCapture: %s", cudaGetErrorString(ce));
   CK(cudaGraphInstantiate(&e.exec, e.graph, 0));
@@ -287,6 +292,7 @@ const char* dev_err_name(int e) {
     case DERR_CAPACITY: return "KV capacity exceeded on the device";
     case DERR_ROUND_LIMIT: return "round limit reached";
     case DERR_BAD_TOKEN: return "token id out of range";
+    case DERR_TIMEOUT: return "a bounded wait inside a kernel timed out";
     default: return "device error";
   }
 }
@@ -510,7 +516,8 @@ int gocr_prefill(gocr_handle* h, int req, const void* prefix_embeds, int P) {
   CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
   launch_plan(PLAN_PREFILL, h->rows, h->st, h->slot_one, 1, 0, P, nullptr, nullptr, h->cap, h->hs);
-  enqueue_forward(h, PLAN_PREFILL, 1, 0, P, h->am, nullptr);
+  if (!enqueue_forward(h, PLAN_PREFILL, 1, 0, P, h->am, nullptr))
+    return fail(h, GOCR_ECUDA, "TMA descriptor encoding failed");
   launch_prefill_finish(h->st, req, P, h->am, h->out, h->cap, h->hs);
   CK(cudaGetLastError());
   int e = 0;
@@ -590,7 +597,8 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
   CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
   launch_plan(pk, h->rows, h->st, h->slot_one, 1, B, 0, nullptr, h->dbg_toks, h->cap, h->hs);
-  enqueue_forward(h, pk, 1, B, 0, h->am, h->logits);
+  if (!enqueue_forward(h, pk, 1, B, 0, h->am, h->logits))
+    return fail(h, GOCR_ECUDA, "TMA descriptor encoding failed");
   CK(cudaGetLastError());
   if (logits_out)
     CK(cudaMemcpyAsync(logits_out, h->logits, sizeof(float) * n * h->cfg.vocab, cudaMemcpyDeviceToHost, h->hs));
@@ -674,7 +682,7 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
   a.ws = (float*)((char*)workspace + ctr);
   a.epi = EPI_STORE;
   a.e.y = y; a.e.ldy = N;
-  launch_gemm(dtype, a, (cudaStream_t)stream);
+  if (!launch_gemm(dtype, a, (cudaStream_t)stream)) return fail(h, GOCR_ECUDA, "TMA descriptor encoding failed");
   CK(cudaGetLastError());
   return GOCR_OK;
 }

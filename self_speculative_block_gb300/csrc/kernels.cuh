@@ -45,8 +45,10 @@ struct GemmArgs {
   EpiArgs e;
 };
 
-// Launch of the split-K GEMM with fused epilogue.
-void launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s);
+// Launch of the split-K GEMM with fused epilogue (bf16: tcgen05 + TMA; fp32:
+// CUDA cores).  Returns false when a TMA descriptor cannot be encoded.
+bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s);
+bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s);
 int gemm_splits(int N, int K);
 int gemm_kchunk(int N, int K);
 size_t gemm_ws_floats(int T, int N, int K, bool single_split);
