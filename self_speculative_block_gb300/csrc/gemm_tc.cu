@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     tc::fence_mbar_init();
     s_fail = 0;
   }
+  __syncwarp();
   if (warp == 0) tc::tmem_alloc(tmem_holder, ncols);
   tc::fence_before_sync();
   __syncthreads();
@@ -242,10 +243,11 @@ bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
   if (stages > nkb) stages = nkb;
   if (stages < 1) stages = 1;
   const size_t smem = fixed + (size_t)stages * stage_bytes + (2 * stages + 2) * 8;
-  static int configured = 0;
-  if (!configured) {
-    cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    configured = 1;
+  static size_t configured = 0;
+  if (smem > configured) {
+    if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return false;
+    configured = smem;
   }
   dim3 grid(cdiv_i(a.N, NTILE), a.splits, cdiv_i(a.T, TZ_TC));
   gemm_tc_kernel<<<grid, TC_THREADS, smem, s>>>(tmw, tmx, a, nt, stages);
