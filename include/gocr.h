@@ -149,8 +149,9 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
                        float* logits_out);
 
 /* Copy n cached positions from pos0 of layer `layer` to host buffers
- * k_out/v_out, each [n, n_kv_heads, head_dim] in dtype. */
-int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, void* k_out, void* v_out);
+ * k_out/v_out, each [n, n_kv_heads, head_dim] fp32 (the cache is fp32 for
+ * every model dtype: keys are stored rotated). */
+int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, float* k_out, float* v_out);
 
 /* Current cache length (position of the boundary token) and boundary token. */
 int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0);
@@ -164,22 +165,20 @@ void gocr_free(gocr_handle* h);
 
 /* y[T, N] (fp32) = x[T, K] w[N, K]^T, the decoder's weight-streaming GEMM with
  * its fixed split-K reduction (the split count depends on N and K only, so a
- * row's result does not depend on T).  K % 8 == 0.  workspace: device,
- * >= gocr_op_linear_workspace(T, N, K) bytes, all zero before the first call
- * (the kernel leaves it ready for the next call). */
+ * row's result does not depend on T).  x and w in dtype, K % 8 == 0.
+ * workspace: device, >= gocr_op_linear_workspace(T, N, K) bytes, all zero
+ * before the first call (the kernel leaves it ready for the next call). */
 size_t gocr_op_linear_workspace(int T, int N, int K);
 int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int N, int K,
                    void* workspace, size_t workspace_bytes, void* stream);
 
-/* y[T, H] (dtype) = x / sqrt(mean(x^2) + eps) * g for x[T, H] fp32. */
-int gocr_op_rmsnorm(int dtype, const float* x, const float* g, void* y, int T, int H, float eps,
-                    void* stream);
-
-/* Grouped-query attention of one request window against a KV cache.
- * q [T, Hq, d] dtype; kc, vc [Hkv, cap, d] dtype; o [T, Hq, d] dtype;
- * lim: device int32[T], row t reads keys 0..lim[t] (draft: row 0 = p, rows
- * 1..B = p+B; verify/AR: the row's own position).  d in {64, 128}. */
-int gocr_op_attention(int dtype, const void* q, const void* kc, const void* vc, void* o,
+/* Grouped-query attention of one request window against a KV cache, the
+ * decoder's kernel for that dtype (bf16: tensor cores on hi/lo bf16 splits of
+ * the fp32 inputs; fp32: CUDA cores).  q [T, Hq, d], kc and vc [Hkv, cap, d],
+ * o [T, Hq, d], all fp32 on the device; lim: device int32[T], row t reads keys
+ * 0..lim[t] (draft: row 0 = p, rows 1..B = p+B; verify/AR: the row's own
+ * position).  d in {64, 128}. */
+int gocr_op_attention(int dtype, const float* q, const float* kc, const float* vc, float* o,
                       const int32_t* lim, int T, int Hq, int Hkv, int d, int cap, void* stream);
 
 #ifdef __cplusplus

@@ -11,23 +11,31 @@
 // result does not depend on how many other rows share the launch: the AR step
 // and the verify row at the same position give identical bits.
 //
-// bf16 models: tensor-core kernel.  A cluster of CL CTAs shares one
-// (kv head, 64-query-row group); CTA r visits chunks r, r + CL, ... with an
-// online softmax on mma.sync tiles, then the cluster merges its CL partial
-// (max, sum, output) triples through distributed shared memory in rank order.
+// bf16 models: tensor-core kernel.  q and the KV cache are fp32; they are
+// split on load into bf16 hi + lo terms, QK^T takes qh kh + qh kl + ql kh and
+// PV takes P vh + P vl on mma.sync tiles (P in bf16), accumulating in fp32.
+// A cluster of CL CTAs shares one (kv head, 64-query-row group): CTA r visits
+// chunks r, r + CL, ... with an online softmax, then the cluster merges its CL
+// partial (max, sum, output) triples through distributed shared memory in
+// rank order.  The result is written as the O projection's input planes.
 // fp32 models: CUDA-core kernel with one CTA sweeping every chunk.
 #include <cooperative_groups.h>
 
-#include "kernels.cuh"
+#include "epilogue.cuh"
 
 namespace gocr {
 
 namespace {
-constexpr int ROWS = 128;   // query rows (token, q-head-in-group) per CTA
+constexpr int ROWS = 128;   // CUDA-core kernel: query rows (token, q head) per CTA
 constexpr int CH = 64;      // keys per chunk
-}
+constexpr int CL = 8;       // tensor-core kernel: CTAs per cluster (key-chunk split)
+constexpr int QR = 64;      // tensor-core kernel: query rows per cluster
+constexpr float LOG2E = 1.4426950408889634f;
+}  // namespace
 
-template <typename T, int D>
+// ---------------------------------------------------------------- CUDA-core path (fp32)
+
+template <int D>
 __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
   extern __shared__ float sm[];
   float* Qs = sm;                     // [ROWS][D + 1]
@@ -36,6 +44,7 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
   float* Vs = Ks + CH * D;            // [CH][D]
   __shared__ int s_maxlim;
 
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int G = a.Hq / a.Hkv;
   const int kvh = blockIdx.y;
   const int slot = blockIdx.z;
@@ -48,10 +57,9 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
   const int qr0 = blockIdx.x * ROWS;
   if (qr0 >= nrows * G) return;
 
-  const T* q = reinterpret_cast<const T*>(a.q);
-  const T* kc = reinterpret_cast<const T*>(a.kc) + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
-  const T* vc = reinterpret_cast<const T*>(a.vc) + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
-  T* o = reinterpret_cast<T*>(a.o);
+  const float* kc = a.kc + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
+  const float* vc = a.vc + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
+  float* o = reinterpret_cast<float*>(a.o_hi);
 
   const int i = threadIdx.x;
   const int gi = qr0 + i;
@@ -64,7 +72,7 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
   __syncthreads();
   if (valid) atomicMax(&s_maxlim, lim);
   for (int dd = 0; dd < D; ++dd) {
-    Qs[i * (D + 1) + dd] = valid ? to_f32<T>(q[((size_t)t * a.Hq + hq) * D + dd]) : 0.f;
+    Qs[i * (D + 1) + dd] = valid ? a.q[((size_t)t * a.Hq + hq) * D + dd] : 0.f;
     Os[i * (D + 1) + dd] = 0.f;
   }
   __syncthreads();
@@ -77,8 +85,8 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
     for (int x = i; x < CH * D; x += ROWS) {
       int j = x / D, dd = x % D;
       bool in = kbase + j <= maxlim;
-      Ks[x] = in ? to_f32<T>(kc[(size_t)(kbase + j) * D + dd]) : 0.f;
-      Vs[x] = in ? to_f32<T>(vc[(size_t)(kbase + j) * D + dd]) : 0.f;
+      Ks[x] = in ? kc[(size_t)(kbase + j) * D + dd] : 0.f;
+      Vs[x] = in ? vc[(size_t)(kbase + j) * D + dd] : 0.f;
     }
     __syncthreads();
     float s[CH];
@@ -119,18 +127,11 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
   }
   if (valid) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    for (int dd = 0; dd < D; ++dd)
-      o[((size_t)t * a.Hq + hq) * D + dd] = from_f32<T>(Os[i * (D + 1) + dd] * inv);
+    for (int dd = 0; dd < D; ++dd) o[((size_t)t * a.Hq + hq) * D + dd] = Os[i * (D + 1) + dd] * inv;
   }
 }
 
-// ---------------------------------------------------------------- tensor-core path
-
-namespace {
-constexpr int CL = 8;        // CTAs per cluster (key-chunk split)
-constexpr int QR = 64;       // query rows per cluster
-constexpr float LOG2E = 1.4426950408889634f;
-}
+// ---------------------------------------------------------------- tensor-core path (bf16 models)
 
 __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, const uint32_t* b) {
   asm volatile(
@@ -140,29 +141,53 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, const uint
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// Four 8x8 bf16 matrices, transposed on load: each lane gets the pair
+// (row 2t, col g), (row 2t+1, col g) of the matrix whose row addresses lanes
+// 8i..8i+7 supply, which is the B-fragment layout of m16n8k16.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Split four fp32 values into bf16 hi and lo halves (v = hi + lo + O(2^-17 v)).
+__device__ __forceinline__ void split4(float4 v, bf16* hi, bf16* lo) {
+  const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    bf16 h = __float2bfloat16_rn(x[e]);
+    hi[e] = h;
+    lo[e] = __float2bfloat16_rn(x[e] - __bfloat162float(h));
+  }
+}
+
 template <int D>
-__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_kernel(AttnArgs a, int n_rg) {
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_kernel(AttnArgs a) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
-  constexpr int QLD = D + 8;   // bf16 row stride of Q and K tiles
-  constexpr int VLD = 64 + 8;  // bf16 row stride of the transposed V tile
+  constexpr int QLD = D + 8;   // bf16 row stride of the Q, K and V tiles
   constexpr int OLD = D + 4;   // fp32 row stride of the partial output
   extern __shared__ __align__(16) uint8_t sm_raw[];
-  bf16* Qs = reinterpret_cast<bf16*>(sm_raw);            // [QR][QLD]
-  bf16* Ks = Qs + QR * QLD;                              // [64][QLD]
-  bf16* Vt = Ks + 64 * QLD;                              // [D][VLD]
-  float* Ob = reinterpret_cast<float*>(Vt + D * VLD);    // [QR][OLD]
+  bf16* Qh = reinterpret_cast<bf16*>(sm_raw);            // [QR][QLD]
+  bf16* Ql = Qh + QR * QLD;
+  bf16* Kh = Ql + QR * QLD;                              // [64][QLD]
+  bf16* Kl = Kh + 64 * QLD;
+  bf16* Vh = Kl + 64 * QLD;                              // [64][QLD]
+  bf16* Vl = Vh + 64 * QLD;
+  float* Ob = reinterpret_cast<float*>(Vl + 64 * QLD);   // [QR][OLD]
   float* Ms = Ob + QR * OLD;                             // [QR] running max (log2 units)
   float* Ls = Ms + QR;                                   // [QR] running sum
   int* Lim = reinterpret_cast<int*>(Ls + QR);            // [QR]
   __shared__ int s_maxlim;
 
-  const int rank = blockIdx.x;  // == cluster rank (cluster spans grid x)
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int rank = blockIdx.x;  // == cluster rank (the cluster spans grid x)
   const int kvh = blockIdx.y % a.Hkv;
   const int rg = blockIdx.y / a.Hkv;
   const int slot = blockIdx.z;
@@ -176,25 +201,23 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
   const int nq = nrows * G;
   const int qr0 = rg * QR;
   if (qr0 >= nq) return;  // uniform across the cluster
-  const bf16* q = reinterpret_cast<const bf16*>(a.q);
-  const bf16* kc = reinterpret_cast<const bf16*>(a.kc) + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
-  const bf16* vc = reinterpret_cast<const bf16*>(a.vc) + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
-  bf16* o = reinterpret_cast<bf16*>(a.o);
+  const float* kc = a.kc + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
+  const float* vc = a.vc + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
 
   if (tid == 0) s_maxlim = -1;
   __syncthreads();
-  // stage Q rows (zero for rows past the window) and their key limits
-  for (int x = tid; x < QR * (D / 8); x += 128) {
-    const int r = x / (D / 8), v = x % (D / 8);
+  // stage Q rows as hi/lo (zero past the window) and their key limits
+  for (int x = tid; x < QR * (D / 4); x += 128) {
+    const int r = x / (D / 4), v = x % (D / 4);
     const int gi = qr0 + r;
-    uint4 val = make_uint4(0, 0, 0, 0);
+    float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
     if (gi < nq) {
       const int t = row0 + gi / G, hq = kvh * G + gi % G;
-      val = *reinterpret_cast<const uint4*>(q + ((size_t)t * a.Hq + hq) * D + v * 8);
+      val = *reinterpret_cast<const float4*>(a.q + ((size_t)t * a.Hq + hq) * D + v * 4);
     }
-    *reinterpret_cast<uint4*>(Qs + r * QLD + v * 8) = val;
+    split4(val, Qh + r * QLD + v * 4, Ql + r * QLD + v * 4);
   }
   if (tid < QR) {
     const int gi = qr0 + tid;
@@ -217,17 +240,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
 
   for (int c = rank; c < n_chunks; c += CL) {
     const int kbase = c * 64;
-    for (int x = tid; x < 64 * (D / 8); x += 128) {
-      const int j = x / (D / 8), v = x % (D / 8);
-      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+    for (int x = tid; x < 64 * (D / 4); x += 128) {
+      const int j = x / (D / 4), v = x % (D / 4);
+      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
       if (kbase + j <= maxlim) {
-        kv = *reinterpret_cast<const uint4*>(kc + (size_t)(kbase + j) * D + v * 8);
-        vv = *reinterpret_cast<const uint4*>(vc + (size_t)(kbase + j) * D + v * 8);
+        kv = *reinterpret_cast<const float4*>(kc + (size_t)(kbase + j) * D + v * 4);
+        vv = *reinterpret_cast<const float4*>(vc + (size_t)(kbase + j) * D + v * 4);
       }
-      *reinterpret_cast<uint4*>(Ks + j * QLD + v * 8) = kv;
-      const bf16* ve = reinterpret_cast<const bf16*>(&vv);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) Vt[(v * 8 + e) * VLD + j] = ve[e];
+      split4(kv, Kh + j * QLD + v * 4, Kl + j * QLD + v * 4);
+      split4(vv, Vh + j * QLD + v * 4, Vl + j * QLD + v * 4);
     }
     __syncthreads();
     // S = Q K^T for this warp's 16 rows and the chunk's 64 keys
@@ -236,19 +257,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
     for (int nt = 0; nt < 8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t af[4];
-      const bf16* qa = Qs + (warp * 16 + g) * QLD + ks * 16 + tq * 2;
-      af[0] = *reinterpret_cast<const uint32_t*>(qa);
-      af[1] = *reinterpret_cast<const uint32_t*>(qa + 8 * QLD);
-      af[2] = *reinterpret_cast<const uint32_t*>(qa + 8);
-      af[3] = *reinterpret_cast<const uint32_t*>(qa + 8 * QLD + 8);
+      uint32_t ah[4], al[4];
+      const int qo = (warp * 16 + g) * QLD + ks * 16 + tq * 2;
+      ah[0] = *reinterpret_cast<const uint32_t*>(Qh + qo);
+      ah[1] = *reinterpret_cast<const uint32_t*>(Qh + qo + 8 * QLD);
+      ah[2] = *reinterpret_cast<const uint32_t*>(Qh + qo + 8);
+      ah[3] = *reinterpret_cast<const uint32_t*>(Qh + qo + 8 * QLD + 8);
+      al[0] = *reinterpret_cast<const uint32_t*>(Ql + qo);
+      al[1] = *reinterpret_cast<const uint32_t*>(Ql + qo + 8 * QLD);
+      al[2] = *reinterpret_cast<const uint32_t*>(Ql + qo + 8);
+      al[3] = *reinterpret_cast<const uint32_t*>(Ql + qo + 8 * QLD + 8);
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        uint32_t bfr[2];
-        const bf16* kb = Ks + (nt * 8 + g) * QLD + ks * 16 + tq * 2;
-        bfr[0] = *reinterpret_cast<const uint32_t*>(kb);
-        bfr[1] = *reinterpret_cast<const uint32_t*>(kb + 8);
-        mma16816(sacc[nt], af, bfr);
+        const int ko = (nt * 8 + g) * QLD + ks * 16 + tq * 2;
+        uint32_t bh[2], bl[2];
+        bh[0] = *reinterpret_cast<const uint32_t*>(Kh + ko);
+        bh[1] = *reinterpret_cast<const uint32_t*>(Kh + ko + 8);
+        bl[0] = *reinterpret_cast<const uint32_t*>(Kl + ko);
+        bl[1] = *reinterpret_cast<const uint32_t*>(Kl + ko + 8);
+        mma16816(sacc[nt], al, bh);
+        mma16816(sacc[nt], ah, bl);
+        mma16816(sacc[nt], ah, bh);
       }
     }
     // mask, scale to log2 units, chunk row maxima
@@ -301,17 +330,22 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
       oacc[dn][0] *= corr_lo; oacc[dn][1] *= corr_lo;
       oacc[dn][2] *= corr_hi; oacc[dn][3] *= corr_hi;
     }
-    // O += P V
+    // O += P (V_hi + V_lo); B fragments of two d-tiles per ldmatrix.x4.trans
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int lcol = (lane >> 4) * 8;
 #pragma unroll
     for (int kt = 0; kt < 4; ++kt) {
       uint32_t af[4] = {pf[2 * kt][0], pf[2 * kt][1], pf[2 * kt + 1][0], pf[2 * kt + 1][1]};
 #pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        uint32_t bfr[2];
-        const bf16* vb = Vt + (dn * 8 + g) * VLD + kt * 16 + tq * 2;
-        bfr[0] = *reinterpret_cast<const uint32_t*>(vb);
-        bfr[1] = *reinterpret_cast<const uint32_t*>(vb + 8);
-        mma16816(oacc[dn], af, bfr);
+      for (int dn = 0; dn < D / 8; dn += 2) {
+        const int vo = (kt * 16 + lrow) * QLD + dn * 8 + lcol;
+        uint32_t bh[4], bl[4];
+        ldsm_x4_trans(bh, Vh + vo);
+        ldsm_x4_trans(bl, Vl + vo);
+        mma16816(oacc[dn], af, bl);
+        mma16816(oacc[dn], af, bh);
+        mma16816(oacc[dn + 1], af, bl + 2);
+        mma16816(oacc[dn + 1], af, bh + 2);
       }
     }
     __syncthreads();
@@ -354,48 +388,50 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
       float acc = 0.f;
 #pragma unroll
       for (int c = 0; c < CL; ++c) acc += wv[c] * *cluster.map_shared_rank(Ob + r * OLD + d, c);
-      o[((size_t)t * a.Hq + hq) * D + d] = __float2bfloat16_rn(acc * inv);
+      const size_t idx = ((size_t)t * a.Hq + hq) * D + d;
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, idx, acc * inv);
     }
   }
   cluster.sync();
 }
 
 template <int D>
-static void launch_attn_mma(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s) {
+static bool launch_attn_mma(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
   const int G = a.Hq / a.Hkv;
   const int n_rg = (max_rows * G + QR - 1) / QR;
-  dim3 grid(CL, a.Hkv * n_rg, n_slots);
-  constexpr int QLD = D + 8, VLD = 72, OLD = D + 4;
-  size_t smem = (size_t)(QR * QLD + 64 * QLD + D * VLD) * 2 + (size_t)QR * OLD * 4 + QR * 12;
+  constexpr int QLD = D + 8, OLD = D + 4;
+  const size_t smem = (size_t)(2 * QR * QLD + 4 * 64 * QLD) * 2 + (size_t)QR * OLD * 4 + QR * 12;
   static bool init = false;
   if (!init) {
-    cudaFuncSetAttribute(attention_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaFuncSetAttribute(attention_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return false;
     init = true;
   }
-  attention_mma_kernel<D><<<grid, 128, smem, s>>>(a, n_rg);
+  return launch_k(attention_mma_kernel<D>, dim3(CL, a.Hkv * n_rg, n_slots), dim3(128), smem, s, pdl, a) ==
+         cudaSuccess;
 }
 
-template <typename T, int D>
-static void launch_attn_t(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s) {
+template <int D>
+static bool launch_attn_simt(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
   const int G = a.Hq / a.Hkv;
   dim3 grid((max_rows * G + ROWS - 1) / ROWS, a.Hkv, n_slots);
-  size_t smem = sizeof(float) * (2 * ROWS * (D + 1) + 2 * CH * D);
+  const size_t smem = sizeof(float) * (2 * ROWS * (D + 1) + 2 * CH * D);
   static bool init = false;
   if (!init) {
-    cudaFuncSetAttribute(attention_simt_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaFuncSetAttribute(attention_simt_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return false;
     init = true;
   }
-  attention_simt_kernel<T, D><<<grid, ROWS, smem, s>>>(a);
+  return launch_k(attention_simt_kernel<D>, grid, dim3(ROWS), smem, s, pdl, a) == cudaSuccess;
 }
 
-void launch_attention(int dtype, const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s) {
-  if (dtype == 1) {
-    if (a.d == 128) launch_attn_mma<128>(a, n_slots, max_rows, s);
-    else launch_attn_mma<64>(a, n_slots, max_rows, s);
-  } else {
-    if (a.d == 128) launch_attn_t<float, 128>(a, n_slots, max_rows, s);
-    else launch_attn_t<float, 64>(a, n_slots, max_rows, s);
-  }
+bool launch_attention(int dtype, const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
+  if (dtype == 1) return a.d == 128 ? launch_attn_mma<128>(a, n_slots, max_rows, s, pdl)
+                                    : launch_attn_mma<64>(a, n_slots, max_rows, s, pdl);
+  return a.d == 128 ? launch_attn_simt<128>(a, n_slots, max_rows, s, pdl)
+                    : launch_attn_simt<64>(a, n_slots, max_rows, s, pdl);
 }
 
 }  // namespace gocr

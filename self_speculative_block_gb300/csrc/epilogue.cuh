@@ -1,6 +1,9 @@
-// Fused GEMM epilogues, applied by the CTA that completes a (128-row tile,
-// token slice) after the fixed-order split-K reduction.  The reduced tile sits
-// in shared memory as Ys[tl * ys_ld + c] for token tl < tn and column c < 128.
+// Fused GEMM epilogues, applied by the CTA that owns a finished
+// (128-column tile, token range) after the fixed-order split-K reduction.
+// The reduced tile sits in shared memory as Ys[tl * ys_ld + c] (token tl < tn,
+// column c < 128).  Each warp takes whole tokens; lane l handles columns
+// l, l + 32, l + 64, l + 96, so per-token reductions are warp shuffles in a
+// fixed order and every token's result is independent of the others.
 #pragma once
 #include "kernels.cuh"
 
@@ -15,123 +18,152 @@ __device__ __forceinline__ void argmax_merge(float& v, int& i, float ov, int oi)
   if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
 }
 
+// Order-preserving 64-bit key: larger value wins, then the smaller index.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+  if (v == 0.f) v = 0.f;  // one zero
+  unsigned u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)idx);
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-// Returns true when this CTA must take part in the grid-level argmax finish.
-template <typename T>
-__device__ void apply_epilogue(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0,
-                               int tn) {
+// GEMM-input plane element: bf16 hi + lo, or fp32.
+__device__ __forceinline__ void put_plane(void* hi, void* lo, int bf, size_t idx, float v) {
+  if (bf) {
+    bf16 h = __float2bfloat16_rn(v);
+    reinterpret_cast<bf16*>(hi)[idx] = h;
+    reinterpret_cast<bf16*>(lo)[idx] = __float2bfloat16_rn(v - __bfloat162float(h));
+  } else {
+    reinterpret_cast<float*>(hi)[idx] = v;
+  }
+}
+
+// rs: shared scratch of >= tn floats (row scales of the input norm).
+__device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0, int tn,
+                               float* rs) {
   const EpiArgs& e = a.e;
   const int n0 = tile * NTILE;
-  const int tid = threadIdx.x, nth = blockDim.x;
-  switch (a.epi) {
-    case EPI_STORE:
-      for (int i = tid; i < tn * NTILE; i += nth) {
-        int tl = i / NTILE, c = i % NTILE, n = n0 + c;
-        if (n < a.N) e.y[(size_t)(t0 + tl) * e.ldy + n] = Ys[tl * ys_ld + c];
-      }
-      break;
-    case EPI_RESID:
-      for (int i = tid; i < tn * NTILE; i += nth) {
-        int tl = i / NTILE, c = i % NTILE, n = n0 + c;
-        if (n < a.N) {
-          float* p = e.y + (size_t)(t0 + tl) * e.ldy + n;
-          *p = *p + Ys[tl * ys_ld + c];
-        }
-      }
-      break;
-    case EPI_SWIGLU: {
-      // tile rows [0, 64) are gate rows, [64, 128) the up rows of the same 64 features
-      const int f0 = tile * SWIGLU_GROUP;
-      for (int i = tid; i < tn * SWIGLU_GROUP; i += nth) {
-        int tl = i / SWIGLU_GROUP, j = i % SWIGLU_GROUP;
-        float g = Ys[tl * ys_ld + j], u = Ys[tl * ys_ld + SWIGLU_GROUP + j];
-        T* h = reinterpret_cast<T*>(e.hbuf);
-        h[(size_t)(t0 + tl) * e.ldh + f0 + j] = from_f32<T>(silu_f(g) * u);
-      }
-      break;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
+  if (e.ssq_in) {
+    // rstd = 1 / sqrt(mean(x^2) + eps) from the per-128-column partial sums, in order
+    for (int tl = tid; tl < tn; tl += blockDim.x) {
+      const int row = e.in_rows ? e.in_rows[t0 + tl] : t0 + tl;
+      const float* p = e.ssq_in + (size_t)row * e.n_ssq;
+      float s = 0.f;
+      for (int i = 0; i < e.n_ssq; ++i) s += p[i];
+      rs[tl] = rsqrtf(s / (float)e.norm_H + e.eps);
     }
-    case EPI_QKV: {
-      const int d = e.head_dim, half = d >> 1;
-      T* q = reinterpret_cast<T*>(e.qbuf);
-      T* kc = reinterpret_cast<T*>(e.kc);
-      T* vc = reinterpret_cast<T*>(e.vc);
-      for (int i = tid; i < tn * NTILE; i += nth) {
-        int tl = i / NTILE, c = i % NTILE, n = n0 + c;
-        int t = t0 + tl;
-        int pos = e.row_pos[t];
-        int j = n % d;  // tiles hold whole heads (128 % d == 0)
-        float x = Ys[tl * ys_ld + c];
-        float out = x;
-        if (n < e.q_dim + e.kv_dim) {  // q and k are rotated, v is not
-          int jj = j < half ? j : j - half;
-          float2 cs = e.rope[(size_t)pos * half + jj];
-          float partner = Ys[tl * ys_ld + (j < half ? c + half : c - half)];
-          out = j < half ? (x * cs.x - partner * cs.y) : (x * cs.x + partner * cs.y);
+    __syncthreads();
+  }
+  for (int tl = warp; tl < tn; tl += nwarp) {
+    const int t = t0 + tl;
+    const float r = e.ssq_in ? rs[tl] : 1.f;
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = Ys[tl * ys_ld + lane + 32 * j] * r;
+    switch (a.epi) {
+      case EPI_STORE:
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = n0 + lane + 32 * j;
+          if (n < a.N) e.y[(size_t)t * e.ldy + n] = v[j];
         }
-        if (n < e.q_dim) {
-          q[(size_t)t * e.q_dim + n] = from_f32<T>(out);
-        } else {
-          int slot = e.row_slot[t];
-          int req = e.plan->slot_req[slot];
-          if (pos < 0 || pos >= e.cap) { set_err(e.err, DERR_CAPACITY); continue; }
-          bool is_k = n < e.q_dim + e.kv_dim;
-          int nn = is_k ? n - e.q_dim : n - e.q_dim - e.kv_dim;
-          int kvh = nn / d;
-          size_t off = (size_t)req * e.req_stride + ((size_t)kvh * e.cap + pos) * d + j;
-          (is_k ? kc : vc)[off] = from_f32<T>(out);
+        break;
+      case EPI_RESID: {
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = n0 + lane + 32 * j;
+          float* p = e.resid + (size_t)t * e.H + n;
+          const float x = *p + v[j];
+          *p = x;
+          ss = fmaf(x, x, ss);
+          put_plane(e.pl_hi, e.pl_lo, e.plane_bf16, (size_t)t * e.ld_pl + n, x * e.g_next[n]);
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) e.ssq_out[(size_t)t * (e.H / NTILE) + tile] = ss;
+        break;
       }
-      break;
-    }
-    case EPI_ARGMAX: {
-      const int lane = tid & 31, warp = tid >> 5, nwarp = nth >> 5;
-      for (int tl = warp; tl < tn; tl += nwarp) {
+      case EPI_SWIGLU: {
+        // tile columns [0, 64) are gate rows, [64, 128) the up rows of the same 64 features
+        const int f0 = tile * SWIGLU_GROUP;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          put_plane(e.pl_hi, e.pl_lo, e.plane_bf16, (size_t)t * e.ld_pl + f0 + lane + 32 * j,
+                    silu_f(v[j]) * v[j + 2]);
+        break;
+      }
+      case EPI_QKV: {
+        const int d = e.head_dim, half = d >> 1;
+        const int pos = e.row_pos[t];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = lane + 32 * j, n = n0 + c, jj = n % d;
+          float out = v[j];
+          if (n < e.q_dim + e.kv_dim) {  // q and k are rotated, v is not
+            const float2 cs = e.rope[(size_t)pos * half + (jj < half ? jj : jj - half)];
+            const float partner = Ys[tl * ys_ld + (jj < half ? c + half : c - half)] * r;
+            out = jj < half ? (v[j] * cs.x - partner * cs.y) : (v[j] * cs.x + partner * cs.y);
+          }
+          if (n < e.q_dim) {
+            e.qf[(size_t)t * e.q_dim + n] = out;
+          } else {
+            const int req = e.plan->slot_req[e.row_slot[t]];
+            if (pos < 0 || pos >= e.cap) { set_err(e.err, DERR_CAPACITY); continue; }
+            const bool is_k = n < e.q_dim + e.kv_dim;
+            const int nn = is_k ? n - e.q_dim : n - e.q_dim - e.kv_dim;
+            const size_t off = (size_t)req * e.req_stride + ((size_t)(nn / d) * e.cap + pos) * d + nn % d;
+            (is_k ? e.kc : e.vc)[off] = out;
+          }
+        }
+        break;
+      }
+      case EPI_ARGMAX: {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
         bool nan = false;
-        for (int c = lane; c < NTILE; c += 32) {
-          int n = n0 + c;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = n0 + lane + 32 * j;
           if (n >= a.N) continue;
-          float v = Ys[tl * ys_ld + c];
-          if (v != v) nan = true;
-          if (e.logits) e.logits[(size_t)(t0 + tl) * e.ld_logits + n] = v;
-          argmax_merge(bv, bi, v, n);
+          if (v[j] != v[j]) nan = true;
+          if (e.logits) e.logits[(size_t)t * e.ld_logits + n] = v[j];
+          argmax_merge(bv, bi, v[j], n);
         }
+#pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-          float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
           argmax_merge(bv, bi, ov, oi);
         }
         if (__any_sync(0xffffffffu, nan) && lane == 0) set_err(e.err, DERR_NAN_LOGITS);
-        if (lane == 0) {
-          e.pmax[(size_t)tile * a.T + t0 + tl] = bv;
-          e.pidx[(size_t)tile * a.T + t0 + tl] = bi;
-        }
+        if (lane == 0 && bi != 0x7fffffff) atomicMax(e.amax + t, argmax_key(bv, bi));
+        break;
       }
-      break;
     }
   }
 }
 
-// Grid-level finish of the LM-head argmax: merge every tile's partial maxima.
-__device__ __forceinline__ void argmax_finish(const GemmArgs& a) {
-  const EpiArgs& e = a.e;
-  const int n_tiles = (a.N + NTILE - 1) / NTILE;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
-  for (int t = warp; t < a.T; t += nwarp) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int tile = lane; tile < n_tiles; tile += 32)
-      argmax_merge(bv, bi, __ldcg(e.pmax + (size_t)tile * a.T + t),
-                   __ldcg(e.pidx + (size_t)tile * a.T + t));
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      argmax_merge(bv, bi, ov, oi);
-    }
-    if (lane == 0) e.am_out[t] = (bi == 0x7fffffff) ? 0 : bi;
+// Grid-level end of the LM-head argmax: the last CTA to arrive publishes the
+// indices and clears the keys and the counter for the next launch.
+__device__ __forceinline__ void argmax_grid_finish(const GemmArgs& a, int* s_flag) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int total = (int)(gridDim.x * gridDim.y * gridDim.z);
+    const int prev = atomicAdd(a.e.grid_ctr, 1);
+    *s_flag = (prev == total - 1);
   }
+  __syncthreads();
+  if (!*s_flag) return;
+  __threadfence();
+  for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
+    const unsigned long long k = atomicExch(a.e.amax + t, 0ull);
+    a.e.am_out[t] = k ? (int)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull)) : 0;
+  }
+  if (threadIdx.x == 0) *a.e.grid_ctr = 0;
 }
 
 }  // namespace gocr

@@ -1,17 +1,12 @@
-// Weight-streaming GEMM Y[T, N] = X[T, K] W[N, K]^T with a fixed split-K
-// reduction and fused epilogues (RoPE + KV write, SwiGLU, residual add,
-// LM-head argmax).
+// Weight-streaming GEMM Y[T, N] = X[T, K] W[N, K]^T: the split rule shared by
+// both implementations, and the CUDA-core kernel that fp32 models run.
 //
 // Reduction order is independent of T: the K range is cut into `splits`
-// chunks that depend on (N, K) only; each CTA accumulates its chunk with a
-// sequential fused multiply-add chain per output, writes fp32 partials, and
-// the last CTA of a (tile, token slice) sums the partials in split order.  A
-// row's result is therefore bit-identical whether the forward carries 1 row
-// (AR), B+1 rows (draft / verify) or a batch, which is what makes the GPU's
-// self-speculative output equal its own AR-greedy output token for token.
-//
-// This file holds the split rule and the CUDA-core kernel of the fp32 models;
-// bf16 models run the tcgen05 kernel of gemm_tc.cu with the same reduction.
+// chunks that depend on (N, K) only; each chunk accumulates in a fixed order
+// and the partial sums of a tile are added in split order.  A row's result is
+// therefore bit-identical whether the forward carries 1 row (AR), B+1 rows
+// (draft / verify) or a batch, which is what makes the GPU's self-speculative
+// output equal its own AR-greedy output token for token.
 #include "epilogue.cuh"
 
 namespace gocr {
@@ -21,6 +16,7 @@ constexpr int KC = 32;       // K elements staged per step
 constexpr int TZ = 64;       // tokens per CTA (grid z slices)
 constexpr int THREADS = 256;
 constexpr int SM_COUNT = 152;  // fixed so the split rule is the same on every device
+constexpr int MAX_SPLITS = 8;  // split-K partials are reduced inside one cluster
 constexpr int YS_LD = NTILE + 1;
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
@@ -29,27 +25,25 @@ __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 int gemm_kchunk(int N, int K) {
   const int tiles = cdiv(N, NTILE);
   const int kb = cdiv(K, 64);
-  int want = (2 * SM_COUNT) / tiles;  // at most two CTAs per SM in one wave
-  int s = want < kb ? want : kb;
+  int s = (2 * SM_COUNT) / tiles;  // at most two CTAs per SM in one wave
+  if (s > MAX_SPLITS) s = MAX_SPLITS;
+  if (s > kb) s = kb;
   if (s < 1) s = 1;
   return cdiv(kb, s) * 64;
 }
 
 int gemm_splits(int N, int K) { return cdiv(K, gemm_kchunk(N, K)); }
 
-size_t gemm_ws_floats(int T, int N, int K, bool single_split) {
-  int s = single_split ? 1 : gemm_splits(N, K);
-  return (size_t)s * T * N;
-}
+size_t gemm_ws_floats(int T, int N, int K) { return (size_t)gemm_splits(N, K) * T * N; }
 
 int gemm_counter_ints(int T, int N) { return cdiv(T, TZ) * cdiv(N, NTILE) + 1; }
 
-template <typename T>
 __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
   extern __shared__ float sm[];
   float* Ws = sm;                          // [NTILE][KC + 1]
   float* Xs = Ws + NTILE * (KC + 1);       // [TZ][KC]
   float* Ys = Xs + TZ * KC;                // [TZ][YS_LD]
+  __shared__ float rs[TZ];
   __shared__ int s_last;
 
   const int tile = blockIdx.x, split = blockIdx.y, z = blockIdx.z;
@@ -59,12 +53,13 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
   const int tn = min(TZ, a.T - t0);
   const int k0 = split * a.kchunk;
   const int k1 = min(a.K, k0 + a.kchunk);
-  const T* X = reinterpret_cast<const T*>(a.x);
-  const T* W = reinterpret_cast<const T*>(a.w);
+  const float* X = reinterpret_cast<const float*>(a.x);
+  const float* W = reinterpret_cast<const float*>(a.w);
   const int tid = threadIdx.x;
   const int nl = tid & (NTILE - 1);
   const int tg = tid >> 7;  // 0..1: tokens tg*32 .. tg*32+31 of the slice
 
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   float acc[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) acc[j] = 0.f;
@@ -73,11 +68,11 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
     const int kc = min(KC, k1 - kb);
     for (int i = tid; i < NTILE * KC; i += THREADS) {
       int r = i / KC, c = i % KC, n = n0 + r;
-      Ws[r * (KC + 1) + c] = (n < a.N && c < kc) ? to_f32<T>(W[(size_t)n * a.K + kb + c]) : 0.f;
+      Ws[r * (KC + 1) + c] = (n < a.N && c < kc) ? W[(size_t)n * a.K + kb + c] : 0.f;
     }
     for (int i = tid; i < TZ * KC; i += THREADS) {
       int r = i / KC, c = i % KC;
-      Xs[r * KC + c] = (r < tn && c < kc) ? to_f32<T>(X[(size_t)(t0 + r) * a.ldx + kb + c]) : 0.f;
+      Xs[r * KC + c] = (r < tn && c < kc) ? X[(size_t)(t0 + r) * a.ldx + kb + c] : 0.f;
     }
     __syncthreads();
     for (int c = 0; c < kc; ++c) {
@@ -88,7 +83,7 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
     __syncthreads();
   }
 
-  // partials -> workspace
+  // partials -> workspace; the last CTA of the (tile, token slice) reduces in split order
   const int n = n0 + nl;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
@@ -104,54 +99,54 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
     if (s_last) *ctr = 0;  // ready for the next launch
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // fixed-order reduction over splits
+  if (s_last) {
+    __threadfence();
 #pragma unroll 4
-  for (int j = 0; j < 32; ++j) {
-    int tl = tg * 32 + j;
-    if (tl < tn && n < a.N) {
-      size_t base = (size_t)(t0 + tl) * a.N + n;
-      float v = __ldcg(a.ws + base);
-      for (int s = 1; s < a.splits; ++s) v += __ldcg(a.ws + (size_t)s * a.T * a.N + base);
+    for (int j = 0; j < 32; ++j) {
+      int tl = tg * 32 + j;
+      float v = 0.f;
+      if (tl < tn && n < a.N) {
+        size_t base = (size_t)(t0 + tl) * a.N + n;
+        v = __ldcg(a.ws + base);
+        for (int s = 1; s < a.splits; ++s) v += __ldcg(a.ws + (size_t)s * a.T * a.N + base);
+      }
       Ys[tl * YS_LD + nl] = v;
-    } else if (tl < TZ) {
-      Ys[tl * YS_LD + nl] = 0.f;
     }
+    __syncthreads();
+    apply_epilogue(a, Ys, YS_LD, tile, t0, tn, rs);
   }
-  __syncthreads();
-  apply_epilogue<T>(a, Ys, YS_LD, tile, t0, tn);
-
-  if (a.epi == EPI_ARGMAX) {
+  if (a.epi == EPI_ARGMAX && s_last) {
+    // every (tile, slice) contributes once; the grid counter expects tiles * slices
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-      int* gc = a.counters + gridDim.z * n_tiles;
-      int prev = atomicAdd(gc, 1);
-      s_last = (prev == n_tiles * (int)gridDim.z - 1);
-      if (s_last) *gc = 0;
+      const int total = n_tiles * (int)gridDim.z;
+      const int prev = atomicAdd(a.e.grid_ctr, 1);
+      s_last = (prev == total - 1);
     }
     __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    argmax_finish(a);
+    if (s_last) {
+      __threadfence();
+      for (int t = tid; t < a.T; t += THREADS) {
+        const unsigned long long k = atomicExch(a.e.amax + t, 0ull);
+        a.e.am_out[t] = k ? (int)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull)) : 0;
+      }
+      if (tid == 0) *a.e.grid_ctr = 0;
+    }
   }
 }
 
-bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s) {
-  if (dtype == 1) return launch_gemm_tc(a, s);
+bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s, bool pdl) {
+  if (dtype == 1) return launch_gemm_tc(a, s, pdl);
   dim3 grid(cdiv(a.N, NTILE), a.splits, cdiv(a.T, TZ));
   size_t smem = sizeof(float) * (NTILE * (KC + 1) + TZ * KC + TZ * YS_LD);
-  {
-    static bool init = false;
-    if (!init) {
-      cudaFuncSetAttribute(gemm_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      init = true;
-    }
-    gemm_simt_kernel<float><<<grid, THREADS, smem, s>>>(a);
+  static bool init = false;
+  if (!init) {
+    if (cudaFuncSetAttribute(gemm_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return false;
+    init = true;
   }
-  return true;
+  return launch_k(gemm_simt_kernel, grid, dim3(THREADS), smem, s, pdl, a) == cudaSuccess;
 }
 
 }  // namespace gocr

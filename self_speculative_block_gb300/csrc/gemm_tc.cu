@@ -1,18 +1,26 @@
 // bf16 weight-streaming GEMM on the 5th-generation tensor cores.
 //
 // Y[T, N] = X[T, K] W[N, K]^T with the weights as the 128-row MMA operand
-// ("swap AB"): one CTA owns a 128-row tile of W and one K chunk, so a decode
-// forward with T = B + 1 tokens is an M = 128, N = 16..256 tcgen05.mma with an
-// fp32 accumulator in tensor memory.  TMA streams W tiles (128 x 64, 128-byte
-// swizzle) and the matching X tiles (16-row boxes) through a ring of shared
-// memory stages; one thread issues the TMA loads, one thread issues the MMAs,
-// and the four warps read the accumulator back with tcgen05.ld.
+// ("swap AB"): one CTA owns a 128-row tile of W and one K chunk.  The token
+// side carries both planes of the activation: rows [0, nt) of the B tile are
+// the hi plane and rows [nt, 2 nt) the lo plane of the same tokens, so one
+// M = 128, N = 2 nt tcgen05.mma accumulates W x_hi and W x_lo side by side in
+// tensor memory and the epilogue adds the two columns of each token.
 //
-// The K chunking (split count) depends on (N, K) only and partial sums are
-// added in split order by the last CTA of a tile, exactly as in the CUDA-core
-// path, so a row's bits do not depend on how many rows share the launch.
+// TMA streams W tiles (128 x 64, 128-byte swizzle, evict-first) and X tiles
+// (16-row boxes per plane) through a ring of shared-memory stages; one thread
+// issues the loads, one thread the MMAs.  Under programmatic dependent launch
+// the weight loads of the first stages are issued before griddepcontrol.wait,
+// so they overlap the tail of the kernel that produces X.
+//
+// The K chunks of a tile run on the CTAs of one thread-block cluster (at most
+// 8).  Each CTA parks its fp32 partial tile in shared memory; after a cluster
+// barrier CTA r adds the partials of its token range over distributed shared
+// memory in rank order and runs the epilogue.  The split count depends on
+// (N, K) only, so a row's bits do not depend on how many rows share the launch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cooperative_groups.h>
 
 #include <map>
 #include <mutex>
@@ -25,11 +33,13 @@ namespace gocr {
 
 namespace {
 constexpr int TC_THREADS = 128;
-constexpr int TZ_TC = 256;       // tokens per CTA (MMA N <= 256)
-constexpr int EG = 32;           // tokens per epilogue group
-constexpr int YS_LD_TC = NTILE + 1;
+constexpr int TZ_TC = 128;       // tokens per CTA (two planes: MMA N <= 256)
+constexpr int EG = 32;           // tokens per cluster-reduce group
+constexpr int YLD = NTILE + 1;   // fp32 row stride of the partial tiles
 constexpr int A_BYTES = NTILE * 64 * 2;  // 128 x 64 bf16
-constexpr int SMEM_BUDGET = 200 * 1024;
+constexpr int SMEM_CAP = 200 * 1024;
+constexpr int DECODE_STAGE_CAP = 3;      // decode shapes: keep two CTAs per SM
+constexpr int TAIL_BYTES = TZ_TC * 4 + 16 * 8 + 64;  // row scales, barriers, TMEM holder
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_mu;
@@ -71,36 +81,46 @@ bool tmap_2d(CUtensorMap* out, const void* ptr, int rows, int cols, int box_rows
 __host__ __device__ inline int cdiv_i(int a, int b) { return (a + b - 1) / b; }
 }  // namespace
 
+// ring_bytes >= stages * (A tile + B tile) and >= the partial tile + reduce buffer.
 __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw,
-                                                            const __grid_constant__ CUtensorMap tmx,
-                                                            GemmArgs a, int nt, int stages) {
+                                                            const __grid_constant__ CUtensorMap tmx_hi,
+                                                            const __grid_constant__ CUtensorMap tmx_lo,
+                                                            GemmArgs a, int nt, int two, int stages,
+                                                            int ring_bytes) {
+  namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const int b_bytes = nt * 128;
+  const int b_bytes = (two ? 2 : 1) * nt * 128;
   uint8_t* sA = smem;
   uint8_t* sB = sA + stages * A_BYTES;
-  float* Ys = reinterpret_cast<float*>(sB + stages * b_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(Ys + EG * YS_LD_TC);
+  // after the MMAs the ring is free: the partial tile and the reduce buffer live there
+  float* Yp = reinterpret_cast<float*>(smem);             // [nt][YLD]
+  float* Ys = Yp + nt * YLD;                               // [EG][YLD]
+  uint8_t* tail = smem + ring_bytes;
+  float* rs = reinterpret_cast<float*>(tail);              // [TZ_TC] row scales
+  uint64_t* full = reinterpret_cast<uint64_t*>(rs + TZ_TC);
   uint64_t* empty = full + stages;
   uint64_t* done = empty + stages;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
-  __shared__ int s_last;
   __shared__ int s_fail;
+  __shared__ int s_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile = blockIdx.x, split = blockIdx.y, z = blockIdx.z;
-  const int n_tiles = gridDim.x;
+  const int S = gridDim.y;  // the cluster spans the splits of one tile
   const int n0 = tile * NTILE;
   const int t0 = z * TZ_TC;
   const int tn = min(TZ_TC, a.T - t0);
   const int k0 = split * a.kchunk;
   const int k1 = min(a.K, k0 + a.kchunk);
   const int nkb = cdiv_i(k1 - k0, 64);
-  const uint32_t ncols = nt <= 32 ? 32 : (nt <= 64 ? 64 : (nt <= 128 ? 128 : 256));
+  const int nmma = (two ? 2 : 1) * nt;
+  const uint32_t ncols = nmma <= 32 ? 32 : (nmma <= 64 ? 64 : (nmma <= 128 ? 128 : 256));
 
   if (tid == 0) {
     tc::prefetch_tmap(&tmw);
-    tc::prefetch_tmap(&tmx);
+    tc::prefetch_tmap(&tmx_hi);
+    if (two) tc::prefetch_tmap(&tmx_lo);
     for (int s = 0; s < stages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
@@ -108,6 +128,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     tc::mbar_init(done, 1);
     tc::fence_mbar_init();
     s_fail = 0;
+    tc::grid_dep_launch();
   }
   __syncwarp();
   if (warp == 0) tc::tmem_alloc(tmem_holder, ncols);
@@ -117,25 +138,37 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   const uint32_t tmem = *tmem_holder;
 
   if (tid == 0) {
-    // TMA producer
+    // TMA producer.  Weights do not depend on the previous kernel: the first
+    // stages' weight tiles go out before the grid dependency wait.
     const uint64_t pol = tc::policy_evict_first();
+    const int pre = nkb < stages ? nkb : stages;
+    for (int kb = 0; kb < pre; ++kb) {
+      tc::mbar_expect_tx(&full[kb], A_BYTES + b_bytes);
+      tc::tma_load_2d_hint(sA + kb * A_BYTES, &tmw, k0 + kb * 64, n0, &full[kb], pol);
+    }
+    tc::grid_dep_wait();
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % stages;
       const int use = kb / stages;
-      if (use > 0 && !tc::mbar_wait(&empty[s], (use - 1) & 1)) { s_fail = 1; break; }
-      tc::mbar_expect_tx(&full[s], A_BYTES + b_bytes);
       const int kx = k0 + kb * 64;
-      tc::tma_load_2d_hint(sA + s * A_BYTES, &tmw, kx, n0, &full[s], pol);
-      for (int g = 0; g < nt / 16; ++g) tc::tma_load_2d(sB + s * b_bytes + g * 2048, &tmx, kx, t0 + 16 * g, &full[s]);
+      if (kb >= pre) {
+        if (!tc::mbar_wait(&empty[s], (use - 1) & 1)) { s_fail = 1; break; }
+        tc::mbar_expect_tx(&full[s], A_BYTES + b_bytes);
+        tc::tma_load_2d_hint(sA + s * A_BYTES, &tmw, kx, n0, &full[s], pol);
+      }
+      uint8_t* b = sB + s * b_bytes;
+      for (int g = 0; g < nt / 16; ++g) tc::tma_load_2d(b + g * 2048, &tmx_hi, kx, t0 + 16 * g, &full[s]);
+      if (two)
+        for (int g = 0; g < nt / 16; ++g)
+          tc::tma_load_2d(b + (nt / 16 + g) * 2048, &tmx_lo, kx, t0 + 16 * g, &full[s]);
     }
   } else if (tid == 32) {
     // MMA issuer
-    const uint32_t idesc = tc::idesc_bf16(NTILE, nt);
-    bool ok = true;
-    for (int kb = 0; kb < nkb && ok; ++kb) {
+    const uint32_t idesc = tc::idesc_bf16(NTILE, nmma);
+    for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % stages;
       const int use = kb / stages;
-      if (!tc::mbar_wait(&full[s], use & 1)) { ok = false; s_fail = 1; break; }
+      if (!tc::mbar_wait(&full[s], use & 1)) { s_fail = 1; break; }
       tc::fence_after_sync();
       const uint32_t a_base = tc::smem_u32(sA + s * A_BYTES);
       const uint32_t b_base = tc::smem_u32(sB + s * b_bytes);
@@ -148,110 +181,105 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     tc::mma_commit(done);
   }
   __syncwarp();
+  tc::grid_dep_wait();  // the epilogue reads and writes what earlier kernels touch
   const bool ok_done = tc::mbar_wait(done, 0);
   tc::fence_after_sync();
   __syncthreads();
   const bool failed = !ok_done || s_fail;
-  if (failed) {
-    if (tid == 0) set_err(a.e.err, DERR_TIMEOUT);
-  } else {
-    const int row = warp * 32 + lane;
-    const int n = n0 + row;
-    const int n_groups = cdiv_i(tn, EG);
-    if (a.splits == 1) {
-      for (int g = 0; g < n_groups; ++g) {
-        float v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + g * EG, v);
-        const int gn = min(EG, tn - g * EG);
+  if (failed && tid == 0) set_err(a.e.err, DERR_TIMEOUT);
+
+  // accumulator -> partial tile Yp[token][row]: hi column + lo column of each token
+  const int row = warp * 32 + lane;
+  for (int g = 0; g < nt / 16; ++g) {
+    float vh[16], vl[16];
+    tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + g * 16, vh);
+    if (two) {
+      tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + nt + g * 16, vl);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) Ys[j * YS_LD_TC + row] = j < gn ? v[j] : 0.f;
-        __syncthreads();
-        apply_epilogue<bf16>(a, Ys, YS_LD_TC, tile, t0 + g * EG, gn);
-        __syncthreads();
-      }
-    } else {
-      for (int g = 0; g < n_groups; ++g) {
-        float v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + g * EG, v);
-        const int gn = min(EG, tn - g * EG);
-        if (n < a.N) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < gn) a.ws[((size_t)split * a.T + t0 + g * EG + j) * a.N + n] = v[j];
-        }
-      }
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {
-        int* ctr = a.counters + z * n_tiles + tile;
-        int prev = atomicAdd(ctr, 1);
-        s_last = (prev == a.splits - 1);
-        if (s_last) *ctr = 0;
-      }
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        for (int g = 0; g < n_groups; ++g) {
-          const int gn = min(EG, tn - g * EG);
-          for (int j = 0; j < EG; ++j) {
-            float acc = 0.f;
-            if (j < gn && n < a.N) {
-              const size_t base = (size_t)(t0 + g * EG + j) * a.N + n;
-              acc = __ldcg(a.ws + base);
-              for (int s = 1; s < a.splits; ++s) acc += __ldcg(a.ws + (size_t)s * a.T * a.N + base);
-            }
-            Ys[j * YS_LD_TC + row] = acc;
-          }
-          __syncthreads();
-          apply_epilogue<bf16>(a, Ys, YS_LD_TC, tile, t0 + g * EG, gn);
-          __syncthreads();
-        }
-      }
+      for (int j = 0; j < 16; ++j) vh[j] += vl[j];
     }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) Yp[(g * 16 + j) * YLD + row] = failed ? 0.f : vh[j];
   }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, ncols);
-  if (failed) return;
 
-  if (a.epi == EPI_ARGMAX && (a.splits == 1 || s_last)) {
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      int* gc = a.counters + gridDim.z * n_tiles;
-      int prev = atomicAdd(gc, 1);
-      s_last = (prev == n_tiles * (int)gridDim.z - 1);
-      if (s_last) *gc = 0;
+  if (S == 1) {
+    if (!failed) apply_epilogue(a, Yp, YLD, tile, t0, tn, rs);
+  } else {
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int rank = (int)cluster.block_rank();
+    const int per = cdiv_i(tn, S);
+    const int ta = min(tn, rank * per), tb = min(tn, ta + per);
+    for (int g0 = ta; g0 < tb; g0 += EG) {
+      const int cnt = min(EG, tb - g0);
+      for (int j = 0; j < cnt; ++j) {
+        float acc = 0.f;
+        for (int s = 0; s < S; ++s) acc += *cluster.map_shared_rank(Yp + (g0 + j) * YLD + row, s);
+        Ys[j * YLD + row] = acc;
+      }
+      __syncthreads();
+      if (!failed) apply_epilogue(a, Ys, YLD, tile, t0 + g0, cnt, rs);
+      __syncthreads();
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    argmax_finish(a);
+    cluster.sync();  // peers finished reading this CTA's partial tile
   }
+  if (a.epi == EPI_ARGMAX && !failed) argmax_grid_finish(a, &s_flag);
 }
 
-bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
-  CUtensorMap tmw, tmx;
+bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
+  if (a.splits < 1 || a.splits > 8) return false;
+  CUtensorMap tmw, tmh, tml;
   if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE)) return false;
-  if (!tmap_2d(&tmx, a.x, a.T, a.K, 16)) return false;
+  if (!tmap_2d(&tmh, a.x, a.T, a.K, 16)) return false;
+  const int two = a.x_lo != nullptr;
+  if (two) {
+    if (!tmap_2d(&tml, a.x_lo, a.T, a.K, 16)) return false;
+  } else {
+    tml = tmh;
+  }
   const int nt = ((a.T < TZ_TC ? a.T : TZ_TC) + 15) / 16 * 16;
   const int nkb = cdiv_i(a.kchunk, 64);
-  const int stage_bytes = A_BYTES + nt * 128;
-  const int fixed = 1024 + EG * YS_LD_TC * 4 + 64;
-  int stages = (SMEM_BUDGET - fixed) / stage_bytes;
+  const int stage_bytes = A_BYTES + (two ? 2 : 1) * nt * 128;
+  const int y_bytes = (nt + EG) * YLD * 4;
+  int stages = (SMEM_CAP - 1024 - TAIL_BYTES) / stage_bytes;
   if (stages > 6) stages = 6;
+  if (a.T <= 2 * 64 + 1 && stages > DECODE_STAGE_CAP) stages = DECODE_STAGE_CAP;
   if (stages > nkb) stages = nkb;
   if (stages < 1) stages = 1;
-  const size_t smem = fixed + (size_t)stages * stage_bytes + (2 * stages + 2) * 8;
+  int ring = stages * stage_bytes;
+  if (ring < y_bytes) ring = y_bytes;
+  ring = (ring + 1023) / 1024 * 1024;
+  const size_t smem = 1024 + (size_t)ring + TAIL_BYTES;
+  if (smem > 227 * 1024) return false;
   static size_t configured = 0;
   if (smem > configured) {
     if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return false;
     configured = smem;
   }
-  dim3 grid(cdiv_i(a.N, NTILE), a.splits, cdiv_i(a.T, TZ_TC));
-  gemm_tc_kernel<<<grid, TC_THREADS, smem, s>>>(tmw, tmx, a, nt, stages);
-  return true;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(cdiv_i(a.N, NTILE), a.splits, cdiv_i(a.T, TZ_TC));
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  at[na].id = cudaLaunchAttributeClusterDimension;
+  at[na].val.clusterDim.x = 1;
+  at[na].val.clusterDim.y = a.splits;
+  at[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmw, tmh, tml, a, nt, two, stages, ring) == cudaSuccess;
 }
 
 }  // namespace gocr

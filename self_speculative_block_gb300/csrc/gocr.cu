@@ -55,15 +55,21 @@ struct gocr_handle {
   int cap = 0, T_max = 0, T_dec = 0, sched_cap = 0;
   long long layer_stride = 0, req_stride = 0;
 
-  void* kc = nullptr;
-  void* vc = nullptr;
-  float* resid = nullptr;
-  void* xn = nullptr;
-  void* qbuf = nullptr;
-  void* att = nullptr;
-  void* hbuf = nullptr;
-  void* xlog = nullptr;
+  float* kc = nullptr;        // fp32 KV cache [req][layer][kv head][position][head_dim]
+  float* vc = nullptr;
+  float* resid = nullptr;     // residual stream fp32 [T][H]
+  void* xg_hi = nullptr;      // GEMM-input planes of resid * g (next norm's gain) [T][H]
+  void* xg_lo = nullptr;
+  void* at_hi = nullptr;      // attention output planes [T][q_dim]
+  void* at_lo = nullptr;
+  void* hb_hi = nullptr;      // SwiGLU output planes [T][F]
+  void* hb_lo = nullptr;
+  float* ssq = nullptr;       // per-128-column sums of squares of resid [T][H/128]
+  float* qf = nullptr;        // rotated queries fp32 [T][q_dim]
   float* logits = nullptr;
+  unsigned long long* amax = nullptr;
+  int* grid_ctr = nullptr;
+  bool pdl = true;            // programmatic dependent launch between forward kernels
   int* dbuf = nullptr;
   int* vbuf = nullptr;
   int* abuf = nullptr;
@@ -132,78 +138,95 @@ int n_rows_of(int kind, int n_slots, int B, int P) {
   return n_slots * (B + 1);
 }
 
-GemmArgs gemm_base(gocr_handle* h, const void* x, int ldx, const void* w, int T, int N, int K,
-                   bool single_split) {
+GemmArgs gemm_base(gocr_handle* h, const void* xh, const void* xl, int ldx, const void* w, int T, int N,
+                   int K) {
   GemmArgs a{};
-  a.x = x; a.ldx = ldx; a.w = w; a.T = T; a.N = N; a.K = K;
-  if (single_split) {
-    a.kchunk = K; a.splits = 1;
-  } else {
-    a.kchunk = gemm_kchunk(N, K); a.splits = gemm_splits(N, K);
-  }
+  a.x = xh;
+  a.x_lo = h->dtype == GOCR_DTYPE_BF16 ? xl : nullptr;
+  a.ldx = ldx; a.w = w; a.T = T; a.N = N; a.K = K;
+  a.kchunk = gemm_kchunk(N, K);
+  a.splits = gemm_splits(N, K);
   a.ws = h->ws;
   a.counters = h->counters;
   a.e.err = h->err;
+  a.e.plane_bf16 = h->dtype == GOCR_DTYPE_BF16;
   return a;
 }
 
+void set_norm_in(gocr_handle* h, GemmArgs& a) {
+  a.e.ssq_in = h->ssq;
+  a.e.n_ssq = h->cfg.hidden / NTILE;
+  a.e.norm_H = h->cfg.hidden;
+  a.e.eps = h->cfg.rms_eps;
+}
+
 // Enqueue one decoder forward over the rows the plan kernel has laid out.
+// RMSNorm is folded into the GEMMs: producers write resid * g (the next norm's
+// gain) as planes plus per-tile sums of squares; consumers scale by rstd.
 bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out,
                      float* logits) {
-  bool ok = true;
   const gocr_config& c = h->cfg;
   const int T = n_rows_of(kind, n_slots, B, P);
-  const bool single = kind == PLAN_PREFILL;  // prefill keeps its own reduction shape
   const int H = c.hidden;
-  launch_embed(h->dtype, h->embed, h->mask, h->prefix_stage, h->resid, h->rows, T, H, c.vocab,
-               h->err, h->hs);
+  const bool pdl = h->pdl;
+  bool ok = true;
+  launch_embed(h->dtype, h->embed, h->mask, h->prefix_stage, h->resid, h->gattn[0], h->xg_hi, h->xg_lo,
+               h->ssq, h->rows, T, H, c.vocab, h->err, h->hs, pdl);
   for (int l = 0; l < c.n_layers; ++l) {
-    launch_rmsnorm(h->dtype, h->resid, H, h->gattn[l], h->xn, H, T, H, c.rms_eps, nullptr, nullptr,
-                   0, h->hs);
-    // QKV projection, RoPE, KV-cache write at each row's position
-    GemmArgs g = gemm_base(h, h->xn, H, h->wqkv[l], T, h->qkv_n, H, single);
+    float* kcl = h->kc + (size_t)l * h->layer_stride;
+    float* vcl = h->vc + (size_t)l * h->layer_stride;
+    // QKV projection (input norm), RoPE, KV-cache write at each row's position
+    GemmArgs g = gemm_base(h, h->xg_hi, h->xg_lo, H, h->wqkv[l], T, h->qkv_n, H);
+    set_norm_in(h, g);
     g.epi = EPI_QKV;
-    g.e.qbuf = h->qbuf;
-    g.e.kc = (char*)h->kc + (size_t)l * h->layer_stride * h->es;
-    g.e.vc = (char*)h->vc + (size_t)l * h->layer_stride * h->es;
+    g.e.qf = h->qf;
+    g.e.kc = kcl; g.e.vc = vcl;
     g.e.req_stride = h->req_stride;
     g.e.q_dim = h->q_dim; g.e.kv_dim = h->kv_dim; g.e.head_dim = c.head_dim; g.e.cap = h->cap;
     g.e.rope = h->rope;
     g.e.row_pos = h->rows.row_pos; g.e.row_slot = h->rows.row_slot; g.e.plan = h->rows.plan;
-    ok &= launch_gemm(h->dtype, g, h->hs);
+    ok &= launch_gemm(h->dtype, g, h->hs, pdl);
     // attention with the row key limits of this forward's mask
     AttnArgs at{};
-    at.q = h->qbuf;
-    at.kc = g.e.kc; at.vc = g.e.vc; at.req_stride = h->req_stride;
-    at.o = h->att; at.row_lim = h->rows.row_lim; at.plan = h->rows.plan;
+    at.q = h->qf;
+    at.kc = kcl; at.vc = vcl; at.req_stride = h->req_stride;
+    at.o_hi = h->at_hi; at.o_lo = h->at_lo; at.out_bf16 = h->dtype == GOCR_DTYPE_BF16;
+    at.row_lim = h->rows.row_lim; at.plan = h->rows.plan;
     at.T = T; at.Hq = c.n_q_heads; at.Hkv = c.n_kv_heads; at.d = c.head_dim; at.cap = h->cap;
     at.scale = 1.0f / sqrtf((float)c.head_dim);
-    launch_attention(h->dtype, at, kind == PLAN_PREFILL ? 1 : n_slots,
-                     kind == PLAN_PREFILL ? P : T / n_slots, h->hs);
-    // O projection + residual
-    GemmArgs go = gemm_base(h, h->att, h->q_dim, h->wo[l], T, H, h->q_dim, single);
-    go.epi = EPI_RESID; go.e.y = h->resid; go.e.ldy = H;
-    ok &= launch_gemm(h->dtype, go, h->hs);
-    launch_rmsnorm(h->dtype, h->resid, H, h->gmlp[l], h->xn, H, T, H, c.rms_eps, nullptr, nullptr,
-                   0, h->hs);
-    // gate/up (interleaved) + SwiGLU
-    GemmArgs gg = gemm_base(h, h->xn, H, h->wgu[l], T, h->gu_n, H, single);
-    gg.epi = EPI_SWIGLU; gg.e.hbuf = h->hbuf; gg.e.ldh = c.ffn;
-    ok &= launch_gemm(h->dtype, gg, h->hs);
-    // down + residual
-    GemmArgs gd = gemm_base(h, h->hbuf, c.ffn, h->wd[l], T, H, c.ffn, single);
-    gd.epi = EPI_RESID; gd.e.y = h->resid; gd.e.ldy = H;
-    ok &= launch_gemm(h->dtype, gd, h->hs);
+    ok &= launch_attention(h->dtype, at, kind == PLAN_PREFILL ? 1 : n_slots,
+                           kind == PLAN_PREFILL ? P : T / n_slots, h->hs, pdl);
+    // O projection + residual; planes of resid * g_mlp for the MLP
+    GemmArgs go = gemm_base(h, h->at_hi, h->at_lo, h->q_dim, h->wo[l], T, H, h->q_dim);
+    go.epi = EPI_RESID;
+    go.e.resid = h->resid; go.e.H = H; go.e.g_next = h->gmlp[l]; go.e.ssq_out = h->ssq;
+    go.e.pl_hi = h->xg_hi; go.e.pl_lo = h->xg_lo; go.e.ld_pl = H;
+    ok &= launch_gemm(h->dtype, go, h->hs, pdl);
+    // gate/up (interleaved, input norm) + SwiGLU
+    GemmArgs gg = gemm_base(h, h->xg_hi, h->xg_lo, H, h->wgu[l], T, h->gu_n, H);
+    set_norm_in(h, gg);
+    gg.epi = EPI_SWIGLU;
+    gg.e.pl_hi = h->hb_hi; gg.e.pl_lo = h->hb_lo; gg.e.ld_pl = c.ffn;
+    ok &= launch_gemm(h->dtype, gg, h->hs, pdl);
+    // down + residual; planes of resid * (next layer's g_attn, or the final gain)
+    GemmArgs gd = gemm_base(h, h->hb_hi, h->hb_lo, c.ffn, h->wd[l], T, H, c.ffn);
+    gd.epi = EPI_RESID;
+    gd.e.resid = h->resid; gd.e.H = H; gd.e.ssq_out = h->ssq;
+    gd.e.g_next = l + 1 < c.n_layers ? h->gattn[l + 1] : h->gfin;
+    gd.e.pl_hi = h->xg_hi; gd.e.pl_lo = h->xg_lo; gd.e.ld_pl = H;
+    ok &= launch_gemm(h->dtype, gd, h->hs, pdl);
   }
-  // final norm on the rows that need logits, then LM head + argmax
+  // LM head (input norm) + argmax over the rows that need logits
   const int n_logit = kind == PLAN_PREFILL ? n_slots : T;
-  launch_rmsnorm(h->dtype, h->resid, H, h->gfin, h->xlog, H, n_logit, H, c.rms_eps,
-                 h->rows.logit_row, nullptr, 0, h->hs);
-  GemmArgs gl = gemm_base(h, h->xlog, H, h->lm, n_logit, c.vocab, H, single);
+  const size_t off = kind == PLAN_PREFILL ? (size_t)(P - 1) * H * h->es : 0;
+  GemmArgs gl = gemm_base(h, (char*)h->xg_hi + off, h->xg_lo ? (char*)h->xg_lo + off : nullptr, H, h->lm,
+                          n_logit, c.vocab, H);
+  set_norm_in(h, gl);
+  gl.e.in_rows = kind == PLAN_PREFILL ? h->rows.logit_row : nullptr;
   gl.epi = EPI_ARGMAX;
   gl.e.logits = logits; gl.e.ld_logits = c.vocab;
-  gl.e.pmax = h->pmax; gl.e.pidx = h->pidx; gl.e.am_out = am_out;
-  ok &= launch_gemm(h->dtype, gl, h->hs);
+  gl.e.amax = h->amax; gl.e.am_out = am_out; gl.e.grid_ctr = h->grid_ctr;
+  ok &= launch_gemm(h->dtype, gl, h->hs, pdl);
   return ok;
 }
 
@@ -214,27 +237,24 @@ bool enqueue_round(gocr_handle* h, int mode, int B, int n_slots, unsigned long l
   const int cap = h->cap;
   const int out_stride = cap;
   if (mode == GOCR_MODE_AR) {
-    launch_plan(PLAN_AR, h->rows, h->st, h->slot_req, n_slots, 0, 0, nullptr, nullptr, cap, h->hs);
+    launch_plan(PLAN_AR, h->rows, h->st, h->slot_req, n_slots, 0, 0, nullptr, nullptr, cap, h->hs, h->pdl);
     ok &= enqueue_forward(h, PLAN_AR, n_slots, 0, 0, h->abuf, nullptr);
     launch_ar_commit(h->st, h->slot_req, n_slots, h->abuf, h->out, out_stride, h->err, cond,
-                     use_cond, h->hs);
+                     use_cond, h->hs, h->pdl);
     return ok;
   }
-  launch_plan(PLAN_DRAFT, h->rows, h->st, h->slot_req, n_slots, B, 0, nullptr, nullptr, cap, h->hs);
+  launch_plan(PLAN_DRAFT, h->rows, h->st, h->slot_req, n_slots, B, 0, nullptr, nullptr, cap, h->hs, h->pdl);
   ok &= enqueue_forward(h, PLAN_DRAFT, n_slots, B, 0, h->dbuf, nullptr);
   launch_override(h->st, h->slot_req, n_slots, B, h->dbuf, h->ref, cap, h->sched, h->sched_cap,
-                  h->cfg.vocab, h->hs);
-  launch_plan(PLAN_VERIFY, h->rows, h->st, h->slot_req, n_slots, B, 0, h->dbuf, nullptr, cap, h->hs);
+                  h->cfg.vocab, h->hs, h->pdl);
+  launch_plan(PLAN_VERIFY, h->rows, h->st, h->slot_req, n_slots, B, 0, h->dbuf, nullptr, cap, h->hs, h->pdl);
   ok &= enqueue_forward(h, PLAN_VERIFY, n_slots, B, 0, h->vbuf, nullptr);
   launch_accept(h->st, h->slot_req, n_slots, B, h->dbuf, h->vbuf, h->out, out_stride, h->err, cond,
-                use_cond, h->hs);
+                use_cond, h->hs, h->pdl);
   return ok;
 }
 
-int get_graph(gocr_handle* h, int mode, int B, int n_slots, cudaGraphExec_t* exec) {
-  for (auto& g : h->graphs)
-    if (g.mode == mode && g.B == B && g.n_slots == n_slots) { *exec = g.exec; return GOCR_OK; }
-  GraphEntry e{mode, B, n_slots, nullptr, nullptr};
+int build_graph(gocr_handle* h, GraphEntry& e) {
   CK(cudaGraphCreate(&e.graph, 0));
   cudaGraphConditionalHandle ch;
   CK(cudaGraphConditionalHandleCreate(&ch, e.graph, 1, cudaGraphCondAssignDefault));
@@ -247,14 +267,31 @@ int get_graph(gocr_handle* h, int mode, int B, int n_slots, cudaGraphExec_t* exe
   CK(cudaGraphAddNode(&node, e.graph, nullptr, nullptr, 0, &np));
   cudaGraph_t body = np.conditional.phGraph_out[0];
   CK(cudaStreamBeginCaptureToGraph(h->hs, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
-  bool enq = enqueue_round(h, mode, B, n_slots, (unsigned long long)ch, 1);
+  bool enq = enqueue_round(h, e.mode, e.B, e.n_slots, (unsigned long long)ch, 1);
   cudaError_t le = cudaGetLastError();
   cudaGraph_t captured = nullptr;
   cudaError_t ce = cudaStreamEndCapture(h->hs, &captured);
-  if (!enq) return fail(h, GOCR_ECUDA, "TMA descriptor encoding failed");
+  if (!enq) return fail(h, GOCR_ECUDA, "kernel launch configuration rejected during capture");
   if (le != cudaSuccess) return fail(h, GOCR_ECUDA, "launch during capture: %s", cudaGetErrorString(le));
   if (ce != cudaSuccess) return fail(h, GOCR_ECUDA, "cudaStreamEndCapture: %s", cudaGetErrorString(ce));
   CK(cudaGraphInstantiate(&e.exec, e.graph, 0));
+  return GOCR_OK;
+}
+
+int get_graph(gocr_handle* h, int mode, int B, int n_slots, cudaGraphExec_t* exec) {
+  for (auto& g : h->graphs)
+    if (g.mode == mode && g.B == B && g.n_slots == n_slots) { *exec = g.exec; return GOCR_OK; }
+  GraphEntry e{mode, B, n_slots, nullptr, nullptr};
+  int rc = build_graph(h, e);
+  if (rc != GOCR_OK && h->pdl) {
+    // fall back to plain stream order inside the loop body
+    if (e.graph) cudaGraphDestroy(e.graph);
+    e.graph = nullptr;
+    cudaGetLastError();
+    h->pdl = false;
+    rc = build_graph(h, e);
+  }
+  if (rc != GOCR_OK) return rc;
   h->graphs.push_back(e);
   *exec = e.exec;
   return GOCR_OK;
@@ -442,15 +479,22 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->gattn.push_back((const float*)L[7]); h->gmlp.push_back((const float*)L[8]);
   }
   const size_t kv_elems = (size_t)h->req_stride * R;
-  h->kc = A(kv_elems * es);
-  h->vc = A(kv_elems * es);
+  h->kc = (float*)A(kv_elems * 4);
+  h->vc = (float*)A(kv_elems * 4);
   h->resid = (float*)A((size_t)T * H * 4);
-  h->xn = A((size_t)T * H * es);
-  h->qbuf = A((size_t)T * q_dim * es);
-  h->att = A((size_t)T * q_dim * es);
-  h->hbuf = A((size_t)T * c.ffn * es);
-  h->xlog = A((size_t)h->T_dec * H * es);
+  h->xg_hi = A((size_t)T * H * es);
+  h->at_hi = A((size_t)T * q_dim * es);
+  h->hb_hi = A((size_t)T * c.ffn * es);
+  if (h->dtype == GOCR_DTYPE_BF16) {
+    h->xg_lo = A((size_t)T * H * es);
+    h->at_lo = A((size_t)T * q_dim * es);
+    h->hb_lo = A((size_t)T * c.ffn * es);
+  }
+  h->ssq = (float*)A((size_t)T * (H / NTILE) * 4);
+  h->qf = (float*)A((size_t)T * q_dim * 4);
   h->logits = (float*)A((size_t)h->T_dec * c.vocab * 4);
+  h->amax = (unsigned long long*)A((size_t)T * 8);
+  h->grid_ctr = (int*)A(256);
   h->dbuf = (int*)A((size_t)h->T_dec * 4);
   h->vbuf = (int*)A((size_t)h->T_dec * 4);
   h->abuf = (int*)A((size_t)h->T_dec * 4);
@@ -472,24 +516,21 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
   h->dbg_toks = (int*)A((size_t)h->T_dec * 4);
   h->rope = (float2*)A((size_t)h->cap * (c.head_dim / 2) * sizeof(float2));
   h->prefix_stage = A((size_t)c.max_ctx * H * es);
-  // split-K workspace: decode shapes with their fixed splits, prefill with one split
-  size_t wsf = 0;
-  const int shapes[5][2] = {{h->qkv_n, H}, {H, q_dim}, {h->gu_n, H}, {H, c.ffn}, {c.vocab, H}};
-  int ctr = 0;
-  for (auto& s : shapes) {
-    size_t a = gemm_ws_floats(h->T_dec, s[0], s[1], false);
-    size_t b = gemm_ws_floats(c.max_ctx, s[0], s[1], true);
-    if (a > wsf) wsf = a;
-    if (b > wsf) wsf = b;
-    int ci = gemm_counter_ints(h->T_max, s[0]);
-    if (ci > ctr) ctr = ci;
+  // the CUDA-core GEMM of fp32 models reduces its split-K partials through global memory
+  if (h->dtype == GOCR_DTYPE_F32) {
+    size_t wsf = 0;
+    int ctr = 0;
+    const int shapes[5][2] = {{h->qkv_n, H}, {H, q_dim}, {h->gu_n, H}, {H, c.ffn}, {c.vocab, H}};
+    for (auto& sh : shapes) {
+      size_t a = gemm_ws_floats(T, sh[0], sh[1]);
+      if (a > wsf) wsf = a;
+      int ci = gemm_counter_ints(T, sh[0]);
+      if (ci > ctr) ctr = ci;
+    }
+    h->ws_floats = wsf;
+    h->ws = (float*)A(wsf * 4);
+    h->counters = (int*)A((size_t)ctr * 4);
   }
-  h->ws_floats = wsf;
-  h->ws = (float*)A(wsf * 4);
-  h->counters = (int*)A((size_t)ctr * 4);
-  const int n_tiles_lm = (c.vocab + NTILE - 1) / NTILE;
-  h->pmax = (float*)A((size_t)n_tiles_lm * h->T_max * 4);
-  h->pidx = (int*)A((size_t)n_tiles_lm * h->T_max * 4);
   if (!ok) {
     int r = fail(h, GOCR_ENOMEM, "device allocation failed");
     g_lib_error = h->msg;
@@ -515,9 +556,9 @@ int gocr_prefill(gocr_handle* h, int req, const void* prefix_embeds, int P) {
                      cudaMemcpyDefault, h->hs));
   CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
-  launch_plan(PLAN_PREFILL, h->rows, h->st, h->slot_one, 1, 0, P, nullptr, nullptr, h->cap, h->hs);
+  launch_plan(PLAN_PREFILL, h->rows, h->st, h->slot_one, 1, 0, P, nullptr, nullptr, h->cap, h->hs, false);
   if (!enqueue_forward(h, PLAN_PREFILL, 1, 0, P, h->am, nullptr))
-    return fail(h, GOCR_ECUDA, "TMA descriptor encoding failed");
+    return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   launch_prefill_finish(h->st, req, P, h->am, h->out, h->cap, h->hs);
   CK(cudaGetLastError());
   int e = 0;
@@ -596,9 +637,9 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
   CK(cudaMemcpyAsync(h->dbg_toks, tokens, sizeof(int) * n, cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
-  launch_plan(pk, h->rows, h->st, h->slot_one, 1, B, 0, nullptr, h->dbg_toks, h->cap, h->hs);
+  launch_plan(pk, h->rows, h->st, h->slot_one, 1, B, 0, nullptr, h->dbg_toks, h->cap, h->hs, false);
   if (!enqueue_forward(h, pk, 1, B, 0, h->am, h->logits))
-    return fail(h, GOCR_ECUDA, "TMA descriptor encoding failed");
+    return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   CK(cudaGetLastError());
   if (logits_out)
     CK(cudaMemcpyAsync(logits_out, h->logits, sizeof(float) * n * h->cfg.vocab, cudaMemcpyDeviceToHost, h->hs));
@@ -609,20 +650,19 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
   return GOCR_OK;
 }
 
-int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, void* k_out, void* v_out) {
+int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, float* k_out, float* v_out) {
   int r = check_req(h, req);
   if (r) return r;
   const gocr_config& c = h->cfg;
   if (layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || pos0 + n > h->cap || !k_out || !v_out)
     return fail(h, GOCR_EINVAL, "bad KV range");
-  const size_t es = h->es, d = c.head_dim;
+  const size_t d = c.head_dim;
   for (int kvh = 0; kvh < c.n_kv_heads; ++kvh) {
-    size_t off = ((size_t)req * h->req_stride + (size_t)layer * h->layer_stride +
-                  ((size_t)kvh * h->cap + pos0) * d) * es;
-    CK(cudaMemcpy2DAsync((char*)k_out + kvh * d * es, c.n_kv_heads * d * es, (char*)h->kc + off, d * es,
-                         d * es, n, cudaMemcpyDeviceToHost, h->hs));
-    CK(cudaMemcpy2DAsync((char*)v_out + kvh * d * es, c.n_kv_heads * d * es, (char*)h->vc + off, d * es,
-                         d * es, n, cudaMemcpyDeviceToHost, h->hs));
+    size_t off = (size_t)req * h->req_stride + (size_t)layer * h->layer_stride + ((size_t)kvh * h->cap + pos0) * d;
+    CK(cudaMemcpy2DAsync(k_out + kvh * d, c.n_kv_heads * d * 4, h->kc + off, d * 4, d * 4, n,
+                         cudaMemcpyDeviceToHost, h->hs));
+    CK(cudaMemcpy2DAsync(v_out + kvh * d, c.n_kv_heads * d * 4, h->vc + off, d * 4, d * 4, n,
+                         cudaMemcpyDeviceToHost, h->hs));
   }
   CK(cudaStreamSynchronize(h->hs));
   return GOCR_OK;
@@ -664,7 +704,7 @@ void gocr_free(gocr_handle* h) {
 size_t gocr_op_linear_workspace(int T, int N, int K) {
   if (T < 1 || N < 1 || K < 1) return 0;
   size_t ctr = ((size_t)gemm_counter_ints(T, N) * 4 + 255) & ~(size_t)255;
-  return ctr + gemm_ws_floats(T, N, K, false) * 4;
+  return ctr + gemm_ws_floats(T, N, K) * 4 + 256 + (((size_t)T * 8 + 255) & ~(size_t)255);
 }
 
 int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int N, int K,
@@ -675,29 +715,20 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
   if (T < 1 || N < 1 || K < 8 || K % 8) return fail(h, GOCR_EINVAL, "bad shape T=%d N=%d K=%d", T, N, K);
   if (workspace_bytes < gocr_op_linear_workspace(T, N, K)) return fail(h, GOCR_ECAPACITY, "workspace too small");
   GemmArgs a{};
-  a.x = x; a.ldx = K; a.w = w; a.T = T; a.N = N; a.K = K;
+  a.x = x; a.x_lo = nullptr; a.ldx = K; a.w = w; a.T = T; a.N = N; a.K = K;
   a.kchunk = gemm_kchunk(N, K); a.splits = gemm_splits(N, K);
   a.counters = (int*)workspace;
   size_t ctr = ((size_t)gemm_counter_ints(T, N) * 4 + 255) & ~(size_t)255;
   a.ws = (float*)((char*)workspace + ctr);
   a.epi = EPI_STORE;
   a.e.y = y; a.e.ldy = N;
-  if (!launch_gemm(dtype, a, (cudaStream_t)stream)) return fail(h, GOCR_ECUDA, "TMA descriptor encoding failed");
+  if (!launch_gemm(dtype, a, (cudaStream_t)stream, false))
+    return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   CK(cudaGetLastError());
   return GOCR_OK;
 }
 
-int gocr_op_rmsnorm(int dtype, const float* x, const float* g, void* y, int T, int H, float eps,
-                    void* stream) {
-  gocr_handle* h = nullptr;
-  if (dtype != GOCR_DTYPE_F32 && dtype != GOCR_DTYPE_BF16) return fail(h, GOCR_EINVAL, "bad dtype");
-  if (!x || !g || !y || T < 1 || H < 1) return fail(h, GOCR_EINVAL, "bad arguments");
-  launch_rmsnorm(dtype, x, H, g, y, H, T, H, eps, nullptr, nullptr, 0, (cudaStream_t)stream);
-  CK(cudaGetLastError());
-  return GOCR_OK;
-}
-
-int gocr_op_attention(int dtype, const void* q, const void* kc, const void* vc, void* o,
+int gocr_op_attention(int dtype, const float* q, const float* kc, const float* vc, float* o,
                       const int32_t* lim, int T, int Hq, int Hkv, int d, int cap, void* stream) {
   gocr_handle* h = nullptr;
   if (dtype != GOCR_DTYPE_F32 && dtype != GOCR_DTYPE_BF16) return fail(h, GOCR_EINVAL, "bad dtype");
@@ -705,9 +736,11 @@ int gocr_op_attention(int dtype, const void* q, const void* kc, const void* vc, 
   if (T < 1 || Hkv < 1 || Hq % Hkv || (d != 64 && d != 128) || cap < 1)
     return fail(h, GOCR_EINVAL, "bad shape");
   AttnArgs a{};
-  a.q = q; a.kc = kc; a.vc = vc; a.req_stride = 0; a.o = o; a.row_lim = lim; a.plan = nullptr;
+  a.q = q; a.kc = kc; a.vc = vc; a.req_stride = 0; a.o_hi = o; a.o_lo = nullptr; a.out_bf16 = 0;
+  a.row_lim = lim; a.plan = nullptr;
   a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.cap = cap; a.scale = 1.0f / sqrtf((float)d);
-  launch_attention(dtype, a, 1, T, (cudaStream_t)stream);
+  if (!launch_attention(dtype, a, 1, T, (cudaStream_t)stream, false))
+    return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   CK(cudaGetLastError());
   return GOCR_OK;
 }

@@ -1,4 +1,19 @@
 // Kernel interfaces shared by the host orchestration and the kernel files.
+//
+// Data flow of one decoder forward (T rows):
+//   embed:  resid = E[tok] | [M] | prefix row;  X0 = resid * g_attn[0];  ssq
+//   per layer:
+//     qkv    = rstd * (X W_qkv^T)  -> RoPE; q -> qf, k/v -> fp32 KV cache
+//     attn   = softmax(q K^T / sqrt(d), row key limits) V   -> A planes
+//     resid += A W_o^T             -> X = resid * g_mlp;  ssq
+//     h      = silu(g) * u, [g|u] = rstd * (X W_gu^T)        -> H planes
+//     resid += H W_d^T             -> X = resid * g_next; ssq
+//   logits  = rstd * (X W_lm^T)    -> argmax (lowest index on ties)
+// where rstd = 1/sqrt(mean(resid^2) + eps) is rebuilt by each consumer from
+// per-128-column sums of squares (ssq) in a fixed order, so RMSNorm needs no
+// kernel of its own.  "Planes" are GEMM inputs: for bf16 models two bf16
+// arrays hi + lo with hi = bf16(v), lo = bf16(v - hi) (about 16 significant
+// bits, both fed to the tensor cores); for fp32 models one fp32 array.
 #pragma once
 #include "common.cuh"
 
@@ -18,81 +33,112 @@ struct Rows {
 enum EpiKind : int { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3, EPI_ARGMAX = 4 };
 
 struct EpiArgs {
-  float* y;  int ldy;            // STORE: fp32 [T, N];  RESID: fp32 [T, ldy] +=
-  void* hbuf; int ldh;           // SWIGLU: dtype [T, F]
-  // QKV: q -> qbuf [T, q_dim]; k, v -> cache of the row's request at its position
-  void* qbuf;
-  void* kc; void* vc;            // cache of request 0 at this layer
-  long long req_stride;          // elements between two requests' caches
+  // input normalisation: y *= rstd[row], rstd from ssq_in[row][0..n_ssq)
+  const float* ssq_in; int n_ssq; int norm_H; float eps;
+  const int* in_rows;            // row of ssq_in for output row t (NULL = t)
+  // STORE: fp32 [T, ldy]
+  float* y; int ldy;
+  // RESID: resid[T, H] += y; planes of resid * g_next; ssq_out[T][H/128]
+  float* resid; int H;
+  const float* g_next;
+  float* ssq_out;
+  // planes written by RESID and SWIGLU: bf16 hi/lo (plane_bf16) or one fp32 array in pl_hi
+  void* pl_hi; void* pl_lo; int ld_pl; int plane_bf16;
+  // QKV: q -> qf [T, q_dim] fp32; k, v -> fp32 cache of the row's request at its position
+  float* qf;
+  float* kc; float* vc;          // cache of request 0 at this layer
+  long long req_stride;          // floats between two requests' caches
   int q_dim, kv_dim, head_dim, cap;
   const float2* rope;            // [cap][head_dim/2] (cos, sin)
   const int* row_pos; const int* row_slot; const Plan* plan;
-  // ARGMAX: lowest index among equal maxima
+  // ARGMAX: lowest index among equal maxima via 64-bit atomicMax of
+  // (order-preserving value bits << 32 | ~index); the last CTA publishes.
   float* logits; int ld_logits;  // optional full logits (fp32 [T, N])
-  float* pmax; int* pidx;        // [n_tiles][T] per-tile partial maxima
+  unsigned long long* amax;      // [T], zero between launches
   int* am_out;                   // [T]
+  int* grid_ctr;                 // zero between launches
   int* err;                      // device error word
 };
 
 struct GemmArgs {
-  const void* x; int ldx;        // [T, K] dtype
+  const void* x; const void* x_lo; int ldx;  // [T, K] planes (x_lo NULL: single plane)
   const void* w;                 // [N, K] dtype
   int T, N, K;
   int splits, kchunk;            // K = splits chunks of kchunk (last may be short)
-  float* ws;                     // [splits][T][N] fp32 partials
-  int* counters;                 // [n_tslices * n_tiles + 1], zero between launches
+  float* ws;                     // CUDA-core path: [splits][T][N] fp32 partials
+  int* counters;                 // CUDA-core path: tile counters, zero between launches
   int epi;
   EpiArgs e;
 };
 
-// Launch of the split-K GEMM with fused epilogue (bf16: tcgen05 + TMA; fp32:
-// CUDA cores).  Returns false when a TMA descriptor cannot be encoded.
-bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s);
-bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s);
+// Split-K GEMM with fused epilogue (bf16: tcgen05 + TMA, split-K reduced
+// across a thread-block cluster; fp32: CUDA cores).  pdl: launch with
+// programmatic dependent launch.  Returns false when a TMA descriptor cannot
+// be encoded or the launch configuration is rejected.
+bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s, bool pdl);
+bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl);
 int gemm_splits(int N, int K);
 int gemm_kchunk(int N, int K);
-size_t gemm_ws_floats(int T, int N, int K, bool single_split);
+size_t gemm_ws_floats(int T, int N, int K);
 int gemm_counter_ints(int T, int N);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {
-  const void* q;           // [T, Hq, d]
-  const void* kc; const void* vc;   // request 0's cache at this layer: [Hkv][cap][d]
-  long long req_stride;    // elements between requests' caches
-  void* o;                 // [T, Hq, d]
+  const float* q;          // [T, Hq, d] fp32
+  const float* kc; const float* vc;   // request 0's cache at this layer: [Hkv][cap][d] fp32
+  long long req_stride;    // floats between requests' caches
+  void* o_hi; void* o_lo;  // output planes [T, Hq*d] (bf16 hi/lo, or fp32 in o_hi)
+  int out_bf16;            // planes are bf16 (1) or fp32 (0)
   const int* row_lim;      // [T]
   const Plan* plan;        // slot layout; NULL = one slot of T rows, request 0
   int T, Hq, Hkv, d, cap;
   float scale;
 };
-void launch_attention(int dtype, const AttnArgs& a, int n_slots, int max_rows_per_slot, cudaStream_t s);
+// dtype 1: tensor-core cluster kernel; 0: CUDA-core kernel.
+bool launch_attention(int dtype, const AttnArgs& a, int n_slots, int max_rows_per_slot, cudaStream_t s,
+                      bool pdl);
 
 // ---------------------------------------------------------------- small kernels
-void launch_rmsnorm(int dtype, const float* x, int ldx, const float* g, void* y, int ldy,
-                    int T, int H, float eps, const int* gather, const Plan* plan, int which_count,
-                    cudaStream_t s);
 void launch_embed(int dtype, const void* embed, const void* mask_embed, const void* prefix,
-                  float* resid, const Rows& r, int T, int H, int vocab, int* err, cudaStream_t s);
+                  float* resid, const float* g0, void* pl_hi, void* pl_lo, float* ssq, const Rows& r,
+                  int T, int H, int vocab, int* err, cudaStream_t s, bool pdl);
 void launch_rope_table(float2* tab, int cap, int d, float theta, cudaStream_t s);
 
 enum PlanKind : int { PLAN_AR = 0, PLAN_DRAFT = 1, PLAN_VERIFY = 2, PLAN_PREFILL = 3 };
 // Decode plans read ReqState; `toks` (optional) overrides the row tokens (debug forwards).
 void launch_plan(int kind, const Rows& r, ReqState* st, const int* slot_req, int n_slots, int B,
-                 int prefill_len, const int* dbuf, const int* toks, int cap, cudaStream_t s);
+                 int prefill_len, const int* dbuf, const int* toks, int cap, cudaStream_t s, bool pdl);
 void launch_accept(ReqState* st, const int* slot_req, int n_slots, int B, const int* dbuf,
                    const int* vbuf, int* out, int out_stride, const int* err,
-                   unsigned long long cond, int use_cond, cudaStream_t s);
+                   unsigned long long cond, int use_cond, cudaStream_t s, bool pdl);
 void launch_ar_commit(ReqState* st, const int* slot_req, int n_slots, const int* abuf, int* out,
                       int out_stride, const int* err, unsigned long long cond, int use_cond,
-                      cudaStream_t s);
+                      cudaStream_t s, bool pdl);
 void launch_override(ReqState* st, const int* slot_req, int n_slots, int B, int* dbuf,
                      const int* ref, int ref_stride, const int* sched, int sched_stride,
-                     int vocab, cudaStream_t s);
+                     int vocab, cudaStream_t s, bool pdl);
 void launch_prefill_finish(ReqState* st, int req, int P, const int* am, int* out, int out_stride,
                            cudaStream_t s);
 // Arms request slots for a decode call: max_new, the round bound, eos, stats reset.
 void launch_begin_decode(ReqState* st, const int* slot_req, int n_slots, const int* max_new,
                          int max_rounds, int eos_id, cudaStream_t s);
 void launch_set_override(ReqState* st, int req, int n_ref, int n_sched, cudaStream_t s);
+
+// Launch helper: plain launch, or with the programmatic-dependent-launch attribute.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...);
+}
 
 }  // namespace gocr

@@ -1,4 +1,4 @@
-// Row-table, embedding, RMSNorm and round-control kernels.
+// Row-table, embedding and round-control kernels.
 //
 // Round control follows GravityOCR's decode round (review §3.2 and
 // Appendix B.2; velog review, inference section):
@@ -13,52 +13,16 @@
 
 namespace gocr {
 
-// ---------------------------------------------------------------- RMSNorm
-// y[t] = x[src] / sqrt(mean(x[src]^2) + eps) * g, src = gather ? gather[t] : t.
-// One CTA per row; the sum of squares is reduced in a fixed order.
-template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* x, int ldx, const float* g, T* y,
-                                                       int ldy, int T_rows, int H, float eps,
-                                                       const int* gather, const Plan* plan,
-                                                       int which_count) {
-  int t = blockIdx.x;
-  int n = T_rows;
-  if (plan) n = which_count ? plan->n_logit_rows : plan->n_rows;
-  if (t >= n) return;
-  const int src = gather ? gather[t] : t;
-  const float* xr = x + (size_t)src * ldx;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) ss = fmaf(xr[i], xr[i], ss);
-  __shared__ float red[32];
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = ss;
-  __syncthreads();
-  if (warp == 0) {
-    float v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) red[0] = v;
-  }
-  __syncthreads();
-  const float rstd = rsqrtf(red[0] / (float)H + eps);
-  T* yr = y + (size_t)t * ldy;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) yr[i] = from_f32<T>(xr[i] * rstd * g[i]);
-}
-
-void launch_rmsnorm(int dtype, const float* x, int ldx, const float* g, void* y, int ldy, int T,
-                    int H, float eps, const int* gather, const Plan* plan, int which_count,
-                    cudaStream_t s) {
-  if (T <= 0) return;
-  if (dtype == 1)
-    rmsnorm_kernel<bf16><<<T, 256, 0, s>>>(x, ldx, g, (bf16*)y, ldy, T, H, eps, gather, plan, which_count);
-  else
-    rmsnorm_kernel<float><<<T, 256, 0, s>>>(x, ldx, g, (float*)y, ldy, T, H, eps, gather, plan, which_count);
-}
-
 // ---------------------------------------------------------------- embedding rows
+// resid[t] = E[tok] | [M] | prefix row;  X[t] = resid[t] * g0 as GEMM-input
+// planes;  ssq[t][i] = sum of squares of columns [128 i, 128 i + 128).
+// One CTA per row; warp w takes 128-column groups w, w + 8, ...
 template <typename T>
-__global__ void embed_kernel(const T* embed, const T* mask_embed, const T* prefix, float* resid,
-                             Rows r, int H, int vocab, int* err) {
+__global__ void __launch_bounds__(256) embed_kernel(const T* embed, const T* mask_embed, const T* prefix,
+                                                   float* resid, const float* g0, void* pl_hi, void* pl_lo,
+                                                   float* ssq, Rows r, int H, int vocab, int* err) {
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
   if (t >= r.plan->n_rows) return;
   const int tok = r.row_tok[t];
@@ -74,17 +38,33 @@ __global__ void embed_kernel(const T* embed, const T* mask_embed, const T* prefi
   } else {
     src = prefix + (size_t)(-2 - tok) * H;
   }
-  for (int i = threadIdx.x; i < H; i += blockDim.x) resid[(size_t)t * H + i] = to_f32<T>(src[i]);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int bf = sizeof(T) == 2;
+  for (int grp = warp; grp < H / NTILE; grp += 8) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = grp * NTILE + lane + 32 * j;
+      const float x = to_f32<T>(src[c]);
+      resid[(size_t)t * H + c] = x;
+      put_plane(pl_hi, pl_lo, bf, (size_t)t * H + c, x * g0[c]);
+      ss = fmaf(x, x, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) ssq[(size_t)t * (H / NTILE) + grp] = ss;
+  }
 }
 
 void launch_embed(int dtype, const void* embed, const void* mask_embed, const void* prefix,
-                  float* resid, const Rows& r, int T, int H, int vocab, int* err, cudaStream_t s) {
+                  float* resid, const float* g0, void* pl_hi, void* pl_lo, float* ssq, const Rows& r,
+                  int T, int H, int vocab, int* err, cudaStream_t s, bool pdl) {
   if (dtype == 1)
-    embed_kernel<bf16><<<T, 256, 0, s>>>((const bf16*)embed, (const bf16*)mask_embed,
-                                         (const bf16*)prefix, resid, r, H, vocab, err);
+    launch_k(embed_kernel<bf16>, dim3(T), dim3(256), 0, s, pdl, (const bf16*)embed, (const bf16*)mask_embed,
+             (const bf16*)prefix, resid, g0, pl_hi, pl_lo, ssq, r, H, vocab, err);
   else
-    embed_kernel<float><<<T, 256, 0, s>>>((const float*)embed, (const float*)mask_embed,
-                                          (const float*)prefix, resid, r, H, vocab, err);
+    launch_k(embed_kernel<float>, dim3(T), dim3(256), 0, s, pdl, (const float*)embed, (const float*)mask_embed,
+             (const float*)prefix, resid, g0, pl_hi, pl_lo, ssq, r, H, vocab, err);
 }
 
 // ---------------------------------------------------------------- rotary table
@@ -109,6 +89,8 @@ void launch_rope_table(float2* tab, int cap, int d, float theta, cudaStream_t s)
 // verify) or P (prefill, one slot).
 __global__ void plan_kernel(int kind, Rows r, ReqState* st, const int* slot_req, int n_slots, int B,
                             int prefill_len, const int* dbuf, const int* toks, int cap) {
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int w = kind == PLAN_AR ? 1 : (kind == PLAN_PREFILL ? prefill_len : B + 1);
   const int n_rows = w * n_slots;
   Plan* pl = r.plan;
@@ -161,8 +143,9 @@ __global__ void plan_kernel(int kind, Rows r, ReqState* st, const int* slot_req,
 }
 
 void launch_plan(int kind, const Rows& r, ReqState* st, const int* slot_req, int n_slots, int B,
-                 int prefill_len, const int* dbuf, const int* toks, int cap, cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(kind, r, st, slot_req, n_slots, B, prefill_len, dbuf, toks, cap);
+                 int prefill_len, const int* dbuf, const int* toks, int cap, cudaStream_t s, bool pdl) {
+  launch_k(plan_kernel, dim3(1), dim3(1024), 0, s, pdl, kind, r, st, slot_req, n_slots, B, prefill_len, dbuf,
+           toks, cap);
 }
 
 // ---------------------------------------------------------------- commit helpers
@@ -202,6 +185,7 @@ __device__ void set_loop_condition(ReqState* st, const int* slot_req, int n_slot
 __global__ void accept_kernel(ReqState* st, const int* slot_req, int n_slots, int B, const int* dbuf,
                               const int* vbuf, int* out, int out_stride, const int* err,
                               unsigned long long cond, int use_cond) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int s = threadIdx.x;
   if (s < n_slots) {
     const int req = slot_req[s];
@@ -224,13 +208,15 @@ __global__ void accept_kernel(ReqState* st, const int* slot_req, int n_slots, in
 
 void launch_accept(ReqState* st, const int* slot_req, int n_slots, int B, const int* dbuf,
                    const int* vbuf, int* out, int out_stride, const int* err,
-                   unsigned long long cond, int use_cond, cudaStream_t s) {
-  accept_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, B, dbuf, vbuf, out, out_stride, err, cond, use_cond);
+                   unsigned long long cond, int use_cond, cudaStream_t s, bool pdl) {
+  launch_k(accept_kernel, dim3(1), dim3(64), 0, s, pdl, st, slot_req, n_slots, B, dbuf, vbuf, out, out_stride,
+           err, cond, use_cond);
 }
 
 __global__ void ar_commit_kernel(ReqState* st, const int* slot_req, int n_slots, const int* abuf,
                                  int* out, int out_stride, const int* err,
                                  unsigned long long cond, int use_cond) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int s = threadIdx.x;
   if (s < n_slots) {
     const int req = slot_req[s];
@@ -246,14 +232,17 @@ __global__ void ar_commit_kernel(ReqState* st, const int* slot_req, int n_slots,
 
 void launch_ar_commit(ReqState* st, const int* slot_req, int n_slots, const int* abuf, int* out,
                       int out_stride, const int* err, unsigned long long cond, int use_cond,
-                      cudaStream_t s) {
-  ar_commit_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, abuf, out, out_stride, err, cond, use_cond);
+                      cudaStream_t s, bool pdl) {
+  launch_k(ar_commit_kernel, dim3(1), dim3(64), 0, s, pdl, st, slot_req, n_slots, abuf, out, out_stride, err,
+           cond, use_cond);
 }
 
 // Forced-acceptance hook: between draft and verify, per slot.
 __global__ void override_kernel(ReqState* st, const int* slot_req, int n_slots, int B, int* dbuf,
                                 const int* ref, int ref_stride, const int* sched, int sched_stride,
                                 int vocab) {
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int s = threadIdx.x;
   if (s >= n_slots) return;
   const int req = slot_req[s];
@@ -270,9 +259,9 @@ __global__ void override_kernel(ReqState* st, const int* slot_req, int n_slots, 
 
 void launch_override(ReqState* st, const int* slot_req, int n_slots, int B, int* dbuf,
                      const int* ref, int ref_stride, const int* sched, int sched_stride,
-                     int vocab, cudaStream_t s) {
-  override_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, B, dbuf, ref, ref_stride, sched,
-                                   sched_stride, vocab);
+                     int vocab, cudaStream_t s, bool pdl) {
+  launch_k(override_kernel, dim3(1), dim3(64), 0, s, pdl, st, slot_req, n_slots, B, dbuf, ref, ref_stride, sched,
+           sched_stride, vocab);
 }
 
 __global__ void prefill_finish_kernel(ReqState* st, int req, int P, const int* am, int* out,

@@ -31,7 +31,7 @@ LAYER_TENSORS = 9
 EXPORTS = ("gocr_create", "gocr_prefill", "gocr_decode", "gocr_decode_batch",
            "gocr_set_draft_override", "gocr_debug_forward", "gocr_read_kv", "gocr_get_state",
            "gocr_last_error", "gocr_free", "gocr_op_linear_workspace", "gocr_op_linear",
-           "gocr_op_rmsnorm", "gocr_op_attention")
+           "gocr_op_attention")
 
 
 class GocrError(RuntimeError):
@@ -100,7 +100,6 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gocr_free": (None, [vp]),
         "gocr_op_linear_workspace": (sz, [i32, i32, i32]),
         "gocr_op_linear": (i32, [i32, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
-        "gocr_op_rmsnorm": (i32, [i32, vp, vp, vp, i32, i32, ctypes.c_float, vp]),
         "gocr_op_attention": (i32, [i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     }
     for name, (res, args) in sig.items():
@@ -273,19 +272,12 @@ class Decoder:
         return logits
 
     def read_kv(self, req: int, layer: int, pos0: int, n: int):
-        """Cached K, V of positions pos0..pos0+n-1: two fp32 arrays [n, Hkv, d]
-        (bf16 caches are widened exactly)."""
+        """Cached K (rotated) and V of positions pos0..pos0+n-1: two fp32 arrays [n, Hkv, d]."""
         shape = (n, self.cfg.n_kv_heads, self.cfg.head_dim)
-        if self.cfg.dtype == synth.BF16:
-            k = np.zeros(shape, np.uint16)
-            v = np.zeros(shape, np.uint16)
-        else:
-            k = np.zeros(shape, np.float32)
-            v = np.zeros(shape, np.float32)
+        k = np.zeros(shape, np.float32)
+        v = np.zeros(shape, np.float32)
         _check(self.lib.gocr_read_kv(self.h, req, layer, pos0, n, k.ctypes.data, v.ctypes.data), self.h)
-        if self.cfg.dtype == synth.BF16:
-            return synth.bf16_to_f32(k), synth.bf16_to_f32(v), k, v
-        return k, v, k, v
+        return k, v
 
     def state(self, req: int):
         cl = ctypes.c_int32()
@@ -319,24 +311,15 @@ def op_linear(x, w, workspace=None):
     return y
 
 
-def op_rmsnorm(x, g, eps: float, out_dtype):
-    torch = _torch()
-    lib = load()
-    T, H = x.shape
-    y = torch.empty((T, H), dtype=out_dtype, device=x.device)
-    stream = torch.cuda.current_stream(x.device).cuda_stream
-    _check(lib.gocr_op_rmsnorm(_dt(y), x.data_ptr(), g.data_ptr(), y.data_ptr(), T, H, eps, stream))
-    return y
-
-
-def op_attention(q, kc, vc, lim):
-    """q [T, Hq, d]; kc, vc [Hkv, cap, d]; lim int32 [T] on the device."""
+def op_attention(q, kc, vc, lim, dtype: int):
+    """The decoder's attention kernel for `dtype` (DTYPE_BF16 / DTYPE_F32) on fp32
+    tensors: q [T, Hq, d]; kc, vc [Hkv, cap, d]; lim int32 [T] on the device."""
     torch = _torch()
     lib = load()
     T, Hq, d = q.shape
     Hkv, cap, _ = kc.shape
     o = torch.empty_like(q)
     stream = torch.cuda.current_stream(q.device).cuda_stream
-    _check(lib.gocr_op_attention(_dt(q), q.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(),
+    _check(lib.gocr_op_attention(dtype, q.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(),
                                  lim.data_ptr(), T, Hq, Hkv, d, cap, stream))
     return o

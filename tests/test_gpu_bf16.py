@@ -83,7 +83,7 @@ def test_small_ar_replay_and_kv(small, small_ar):
     dec.prefill(0, small["prefix"])
     dec.decode(0, g.MODE_AR, 0, 200)
     for l in range(small["cfg"].n_layers):
-        k, v, _, _ = dec.read_kv(0, l, 0, P + 199)
+        k, v = dec.read_kv(0, l, 0, P + 199)
         ok, err = close(k, K[l])
         assert ok, err
         ok, err = close(v, V[l])
@@ -100,7 +100,7 @@ def test_small_selfspec_bit_exact(small, small_ar, B):
     dec.prefill(0, small["prefix"])
     dec.decode(0, g.MODE_AR, 0, 200)
     kv_ar = dec.read_kv(0, 1, 0, 100 + 199)
-    assert np.array_equal(kv_ss[2], kv_ar[2]) and np.array_equal(kv_ss[3], kv_ar[3])
+    assert np.array_equal(kv_ss[0], kv_ar[0]) and np.array_equal(kv_ss[1], kv_ar[1])
 
 
 @pytest.mark.parametrize("B,mean", [(8, 4.0), (32, 9.0), (64, 19.0)])

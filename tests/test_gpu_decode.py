@@ -58,7 +58,7 @@ def test_ar_logits_and_kv_match_oracle(env):
     st = oracle.prefill(model, prefix)
     ref, _, _ = oracle.ar_forward(model, st)
     np.testing.assert_allclose(lg, ref, rtol=0, atol=1e-4)
-    k, v, _, _ = dec.read_kv(0, 1, 0, 64)
+    k, v = dec.read_kv(0, 1, 0, 64)
     np.testing.assert_allclose(k, st.cache_k[1], rtol=0, atol=1e-4)
     np.testing.assert_allclose(v, st.cache_v[1], rtol=0, atol=1e-4)
 
@@ -121,8 +121,8 @@ def test_kv_after_selfspec_equals_ar_and_oracle_prefill(env, ar128):
     assert cl == 64 + 127 and x0 == ar[-1]
     _, K, V = oracle.prefill_cache(model, env["prefix"].astype(np.float64), ar[:-1])
     for l in range(env["cfg"].n_layers):
-        k, v, kb, vb = dec.read_kv(0, l, 0, 64 + 127)
-        assert np.array_equal(kb, kv_ar[l][2]) and np.array_equal(vb, kv_ar[l][3])
+        k, v = dec.read_kv(0, l, 0, 64 + 127)
+        assert np.array_equal(k, kv_ar[l][0]) and np.array_equal(v, kv_ar[l][1])
         np.testing.assert_allclose(k, K[l], rtol=0, atol=1e-4)
         np.testing.assert_allclose(v, V[l], rtol=0, atol=1e-4)
 

@@ -1,6 +1,6 @@
 """Kernel-level parity of the CUDA path against the oracle's definitions, through
-the C ABI's single-kernel entry points: the split-K GEMM, RMSNorm and the
-masked GQA attention, at sizes that span several tiles with ragged tails.
+the C ABI's single-kernel entry points: the split-K GEMM and the masked GQA
+attention, at sizes that span several tiles with ragged tails.
 """
 import numpy as np
 import pytest
@@ -57,33 +57,18 @@ def test_linear_row_bits_do_not_depend_on_row_count(g, dt):
         assert torch.equal(part, full[:T]), T
 
 
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
-def test_rmsnorm_matches_oracle(g, dt):
-    rng = np.random.default_rng(9)
-    x = rng.standard_normal((37, 1536)).astype(np.float32) * 3
-    gain = rng.uniform(0.5, 1.5, 1536).astype(np.float32)
-    y = g.op_rmsnorm(torch.from_numpy(x).cuda(), torch.from_numpy(gain).cuda(), 1e-6,
-                     torch.bfloat16 if dt == "bf16" else torch.float32)
-    ref = oracle.rmsnorm(x.astype(np.float64), gain.astype(np.float64), 1e-6)
-    tol = 8e-3 if dt == "bf16" else 2e-6
-    np.testing.assert_allclose(y.float().cpu().numpy(), ref, rtol=tol, atol=tol)
-
-
-def _attn_case(rng, T, Hq, Hkv, d, cap, lims, dt):
-    q = _rounded(rng.standard_normal((T, Hq, d)).astype(np.float32), dt)
-    k = _rounded(rng.standard_normal((Hkv, cap, d)).astype(np.float32), dt)
-    v = _rounded(rng.standard_normal((Hkv, cap, d)).astype(np.float32), dt)
+def _attn_case(rng, T, Hq, Hkv, d, cap, lims, dtype):
+    from self_speculative_block_gb300 import gocr
+    q = rng.standard_normal((T, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((Hkv, cap, d)).astype(np.float32)
+    v = rng.standard_normal((Hkv, cap, d)).astype(np.float32)
     lim = np.asarray(lims, np.int32)
     allowed = np.arange(cap)[None, :] <= lim[:, None]
-    ref = oracle.attention(q, k.transpose(1, 0, 2), v.transpose(1, 0, 2), allowed)
-    o = g_op_attention(q, k, v, lim, dt)
+    ref = oracle.attention(q.astype(np.float64), k.transpose(1, 0, 2).astype(np.float64),
+                           v.transpose(1, 0, 2).astype(np.float64), allowed)
+    t = lambda a: torch.from_numpy(a).cuda()
+    o = gocr.op_attention(t(q), t(k), t(v), t(lim), dtype).cpu().numpy()
     return o, ref
-
-
-def g_op_attention(q, k, v, lim, dt):
-    from self_speculative_block_gb300 import gocr
-    o = gocr.op_attention(_dev(q, dt), _dev(k, dt), _dev(v, dt), torch.from_numpy(lim).cuda())
-    return o.float().cpu().numpy()
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
@@ -92,25 +77,28 @@ def g_op_attention(q, k, v, lim, dt):
 def test_attention_draft_and_verify_masks(g, dt, Hq, Hkv, d, p, B):
     rng = np.random.default_rng(p + B + d)
     cap = p + B + 3
-    tol = 2e-2 if dt == "bf16" else 2e-5
+    dtype = g.DTYPE_BF16 if dt == "bf16" else g.DTYPE_F32
+    # the bf16 kernel runs on hi/lo splits of the fp32 inputs with bf16 probabilities
+    tol = 5e-3 if dt == "bf16" else 2e-5
     # draft: boundary row causal (lim p), [M] rows see the window (lim p+B)
-    o, ref = _attn_case(rng, B + 1, Hq, Hkv, d, cap, [p] + [p + B] * B, dt)
+    o, ref = _attn_case(rng, B + 1, Hq, Hkv, d, cap, [p] + [p + B] * B, dtype)
     np.testing.assert_allclose(o, ref, rtol=tol, atol=tol)
     # verify: row j at p+1+j, token-causal
-    o, ref = _attn_case(rng, B + 1, Hq, Hkv, d, cap, list(range(p + 1, p + B + 2)), dt)
+    o, ref = _attn_case(rng, B + 1, Hq, Hkv, d, cap, list(range(p + 1, p + B + 2)), dtype)
     np.testing.assert_allclose(o, ref, rtol=tol, atol=tol)
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_attention_row_bits_do_not_depend_on_other_rows(g, dt):
-    from self_speculative_block_gb300 import gocr
     rng = np.random.default_rng(3)
+    dtype = g.DTYPE_BF16 if dt == "bf16" else g.DTYPE_F32
     Hq, Hkv, d, cap = 12, 4, 128, 700
-    q = _dev(rng.standard_normal((65, Hq, d)).astype(np.float32), dt)
-    k = _dev(rng.standard_normal((Hkv, cap, d)).astype(np.float32), dt)
-    v = _dev(rng.standard_normal((Hkv, cap, d)).astype(np.float32), dt)
+    t = lambda a: torch.from_numpy(a.astype(np.float32)).cuda()
+    q = t(rng.standard_normal((65, Hq, d)))
+    k = t(rng.standard_normal((Hkv, cap, d)))
+    v = t(rng.standard_normal((Hkv, cap, d)))
     lim = torch.arange(600, 665, dtype=torch.int32, device="cuda")
-    full = gocr.op_attention(q, k, v, lim)
+    full = g.op_attention(q, k, v, lim, dtype)
     for j in (0, 1, 31, 64):
-        one = gocr.op_attention(q[j:j + 1].contiguous(), k, v, lim[j:j + 1].contiguous())
+        one = g.op_attention(q[j:j + 1].contiguous(), k, v, lim[j:j + 1].contiguous(), dtype)
         assert torch.equal(one[0], full[j]), j
