@@ -149,8 +149,8 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
                        float* logits_out);
 
 /* Copy n cached positions from pos0 of layer `layer` to host buffers
- * k_out/v_out, each [n, n_kv_heads, head_dim] fp32 (the cache is fp32 for
- * every model dtype: keys are stored rotated). */
+ * k_out/v_out, each [n, n_kv_heads, head_dim] fp32 (keys are stored rotated;
+ * bf16 models keep the cache as bf16 hi + lo planes, returned as their sum). */
 int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, float* k_out, float* v_out);
 
 /* Current cache length (position of the boundary token) and boundary token. */
@@ -173,13 +173,16 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Grouped-query attention of one request window against a KV cache, the
- * decoder's kernel for that dtype (bf16: tensor cores on hi/lo bf16 splits of
- * the fp32 inputs; fp32: CUDA cores).  q [T, Hq, d], kc and vc [Hkv, cap, d],
- * o [T, Hq, d], all fp32 on the device; lim: device int32[T], row t reads keys
+ * decoder's kernel for that dtype.  Operands are planes, as the decoder keeps
+ * them: for GOCR_DTYPE_BF16, bf16 hi and lo arrays with v = hi + lo (tensor
+ * cores, about 16 significant bits); for GOCR_DTYPE_F32, fp32 arrays in *_hi
+ * with the lo pointers NULL.  q [T, Hq, d], k and v [Hkv, cap, d] (device);
+ * o [T, Hq, d] fp32 (device); lim: device int32[T], row t reads keys
  * 0..lim[t] (draft: row 0 = p, rows 1..B = p+B; verify/AR: the row's own
  * position).  d in {64, 128}. */
-int gocr_op_attention(int dtype, const float* q, const float* kc, const float* vc, float* o,
-                      const int32_t* lim, int T, int Hq, int Hkv, int d, int cap, void* stream);
+int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
+                      const void* v_hi, const void* v_lo, float* o, const int32_t* lim, int T, int Hq, int Hkv,
+                      int d, int cap, void* stream);
 
 #ifdef __cplusplus
 }

@@ -11,13 +11,17 @@
 // result does not depend on how many other rows share the launch: the AR step
 // and the verify row at the same position give identical bits.
 //
-// bf16 models: tensor-core kernel.  q and the KV cache are fp32; they are
-// split on load into bf16 hi + lo terms, QK^T takes qh kh + qh kl + ql kh and
-// PV takes P vh + P vl on mma.sync tiles (P in bf16), accumulating in fp32.
-// A cluster of CL CTAs shares one (kv head, 64-query-row group): CTA r visits
-// chunks r, r + CL, ... with an online softmax, then the cluster merges its CL
-// partial (max, sum, output) triples through distributed shared memory in
-// rank order.  The result is written as the O projection's input planes.
+// bf16 models: tensor-core kernel.  q and the KV cache are stored as bf16
+// hi + lo planes (written once by the QKV epilogue), QK^T takes
+// qh kh + qh kl + ql kh and PV takes P vh + P vl on mma.sync tiles (P in
+// bf16), accumulating in fp32.  A cluster of CL CTAs shares one (kv head,
+// 64-query-row group): CTA r visits chunks r, r + CL, ... with an online
+// softmax, K/V tiles double-buffered through cp.async, then the cluster merges
+// its CL partial (max, sum, output) triples through distributed shared memory
+// in rank order.  Under programmatic dependent launch a CTA fetches its first
+// chunk before the grid-dependency wait when that chunk holds only committed
+// cache positions (below the round-start cache length, which no kernel of the
+// forward writes).  The result is written as the O projection's input planes.
 // fp32 models: CUDA-core kernel with one CTA sweeping every chunk.
 #include <cooperative_groups.h>
 
@@ -57,8 +61,9 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
   const int qr0 = blockIdx.x * ROWS;
   if (qr0 >= nrows * G) return;
 
-  const float* kc = a.kc + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
-  const float* vc = a.vc + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
+  const float* kc = reinterpret_cast<const float*>(a.k_hi) + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
+  const float* vc = reinterpret_cast<const float*>(a.v_hi) + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
+  const float* qf = reinterpret_cast<const float*>(a.q_hi);
   float* o = reinterpret_cast<float*>(a.o_hi);
 
   const int i = threadIdx.x;
@@ -72,7 +77,7 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
   __syncthreads();
   if (valid) atomicMax(&s_maxlim, lim);
   for (int dd = 0; dd < D; ++dd) {
-    Qs[i * (D + 1) + dd] = valid ? a.q[((size_t)t * a.Hq + hq) * D + dd] : 0.f;
+    Qs[i * (D + 1) + dd] = valid ? qf[((size_t)t * a.Hq + hq) * D + dd] : 0.f;
     Os[i * (D + 1) + dd] = 0.f;
   }
   __syncthreads();
@@ -155,16 +160,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Split four fp32 values into bf16 hi and lo halves (v = hi + lo + O(2^-17 v)).
-__device__ __forceinline__ void split4(float4 v, bf16* hi, bf16* lo) {
-  const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    bf16 h = __float2bfloat16_rn(x[e]);
-    hi[e] = h;
-    lo[e] = __float2bfloat16_rn(x[e] - __bfloat162float(h));
-  }
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 fills zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int D>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_kernel(AttnArgs a) {
@@ -172,26 +176,55 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int QLD = D + 8;   // bf16 row stride of the Q, K and V tiles
   constexpr int OLD = D + 4;   // fp32 row stride of the partial output
+  constexpr int TILE = 64 * QLD;
   extern __shared__ __align__(16) uint8_t sm_raw[];
   bf16* Qh = reinterpret_cast<bf16*>(sm_raw);            // [QR][QLD]
   bf16* Ql = Qh + QR * QLD;
-  bf16* Kh = Ql + QR * QLD;                              // [64][QLD]
-  bf16* Kl = Kh + 64 * QLD;
-  bf16* Vh = Kl + 64 * QLD;                              // [64][QLD]
-  bf16* Vl = Vh + 64 * QLD;
-  float* Ob = reinterpret_cast<float*>(Vl + 64 * QLD);   // [QR][OLD]
-  float* Ms = Ob + QR * OLD;                             // [QR] running max (log2 units)
+  bf16* KV = Ql + QR * QLD;                              // 2 stages x {Kh, Kl, Vh, Vl} [64][QLD]
+  float* Ob = reinterpret_cast<float*>(KV);              // [QR][OLD], after the chunk loop
+  float* Ms = reinterpret_cast<float*>(KV + 8 * TILE);   // [QR] running max (log2 units)
   float* Ls = Ms + QR;                                   // [QR] running sum
   int* Lim = reinterpret_cast<int*>(Ls + QR);            // [QR]
   __shared__ int s_maxlim;
 
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int rank = blockIdx.x;  // == cluster rank (the cluster spans grid x)
   const int kvh = blockIdx.y % a.Hkv;
   const int rg = blockIdx.y / a.Hkv;
   const int slot = blockIdx.z;
   const int G = a.Hq / a.Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, tq = lane & 3;
+
+  // issue the cp.async copies of chunk c (keys c*64 .. c*64+63, zero past kmax) into stage st_i
+  auto load_chunk = [&](const bf16* kh, const bf16* kl, const bf16* vh, const bf16* vl, int c, int kmax, int st_i) {
+    bf16* dst = KV + st_i * 4 * TILE;
+    for (int x = tid; x < 4 * 64 * (D / 8); x += 128) {
+      const int pl = x / (64 * (D / 8)), rem = x % (64 * (D / 8));
+      const int j = rem / (D / 8), v = rem % (D / 8);
+      const int key = c * 64 + j;
+      const bf16* base = pl == 0 ? kh : pl == 1 ? kl : pl == 2 ? vh : vl;
+      const bool in = key <= kmax;
+      cp_async16(dst + pl * TILE + j * QLD + v * 8, base + (size_t)(in ? key : 0) * D + v * 8, in ? 16 : 0);
+    }
+  };
+
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // committed cache chunk before the dependency wait (decode launches only)
+  int req_pre = -1, pc = 0;
+  if (a.st && a.slot_req) {
+    req_pre = a.slot_req[slot];
+    pc = a.st[req_pre].cache_len;
+  }
+  const bool pre = req_pre >= 0 && (rank + 1) * 64 <= pc;
+  const size_t kv_off_pre = pre ? (size_t)req_pre * a.req_stride + (size_t)kvh * a.cap * D : 0;
+  if (pre) {
+    load_chunk(reinterpret_cast<const bf16*>(a.k_hi) + kv_off_pre, reinterpret_cast<const bf16*>(a.k_lo) + kv_off_pre,
+               reinterpret_cast<const bf16*>(a.v_hi) + kv_off_pre, reinterpret_cast<const bf16*>(a.v_lo) + kv_off_pre,
+               rank, pc - 1, 0);
+    cp_async_commit();
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   int req = 0, row0 = 0, nrows = a.T;
   if (a.plan) {
     req = a.plan->slot_req[slot];
@@ -200,25 +233,30 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
   }
   const int nq = nrows * G;
   const int qr0 = rg * QR;
-  if (qr0 >= nq) return;  // uniform across the cluster
-  const float* kc = a.kc + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
-  const float* vc = a.vc + (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, tq = lane & 3;
+  if (qr0 >= nq) {  // uniform across the cluster
+    cp_async_wait<0>();
+    return;
+  }
+  const size_t kv_off = (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
+  const bf16* kh = reinterpret_cast<const bf16*>(a.k_hi) + kv_off;
+  const bf16* kl = reinterpret_cast<const bf16*>(a.k_lo) + kv_off;
+  const bf16* vh = reinterpret_cast<const bf16*>(a.v_hi) + kv_off;
+  const bf16* vl = reinterpret_cast<const bf16*>(a.v_lo) + kv_off;
+  const bf16* qh = reinterpret_cast<const bf16*>(a.q_hi);
+  const bf16* ql = reinterpret_cast<const bf16*>(a.q_lo);
 
   if (tid == 0) s_maxlim = -1;
   __syncthreads();
-  // stage Q rows as hi/lo (zero past the window) and their key limits
-  for (int x = tid; x < QR * (D / 4); x += 128) {
-    const int r = x / (D / 4), v = x % (D / 4);
+  // Q planes of this row group (zero past the window) and the rows' key limits
+  for (int x = tid; x < 2 * QR * (D / 8); x += 128) {
+    const int pl = x / (QR * (D / 8)), rem = x % (QR * (D / 8));
+    const int r = rem / (D / 8), v = rem % (D / 8);
     const int gi = qr0 + r;
-    float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (gi < nq) {
-      const int t = row0 + gi / G, hq = kvh * G + gi % G;
-      val = *reinterpret_cast<const float4*>(a.q + ((size_t)t * a.Hq + hq) * D + v * 4);
-    }
-    split4(val, Qh + r * QLD + v * 4, Ql + r * QLD + v * 4);
+    size_t src = 0;
+    if (gi < nq) src = ((size_t)(row0 + gi / G) * a.Hq + kvh * G + gi % G) * D + v * 8;
+    cp_async16((pl ? Ql : Qh) + r * QLD + v * 8, (pl ? ql : qh) + src, gi < nq ? 16 : 0);
   }
+  cp_async_commit();
   if (tid < QR) {
     const int gi = qr0 + tid;
     int lim = -1;
@@ -230,6 +268,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
   const int maxlim = s_maxlim;
   const int n_chunks = maxlim < 0 ? 0 : maxlim / 64 + 1;
   const float sl2 = a.scale * LOG2E;
+  if (!pre && rank < n_chunks) load_chunk(kh, kl, vh, vl, rank, maxlim, 0);
+  cp_async_commit();
 
   const int r_lo = warp * 16 + g, r_hi = r_lo + 8;
   const int lim_lo = Lim[r_lo], lim_hi = Lim[r_hi];
@@ -238,19 +278,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
 
-  for (int c = rank; c < n_chunks; c += CL) {
+  int it = 0;
+  for (int c = rank; c < n_chunks; c += CL, ++it) {
     const int kbase = c * 64;
-    for (int x = tid; x < 64 * (D / 4); x += 128) {
-      const int j = x / (D / 4), v = x % (D / 4);
-      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-      if (kbase + j <= maxlim) {
-        kv = *reinterpret_cast<const float4*>(kc + (size_t)(kbase + j) * D + v * 4);
-        vv = *reinterpret_cast<const float4*>(vc + (size_t)(kbase + j) * D + v * 4);
-      }
-      split4(kv, Kh + j * QLD + v * 4, Kl + j * QLD + v * 4);
-      split4(vv, Vh + j * QLD + v * 4, Vl + j * QLD + v * 4);
-    }
+    const int cur = it & 1;
+    // prefetch the next chunk into the other stage, then wait for this one
+    if (c + CL < n_chunks) load_chunk(kh, kl, vh, vl, c + CL, maxlim, cur ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();
     __syncthreads();
+    const bf16* Kh = KV + cur * 4 * TILE;
+    const bf16* Kl = Kh + TILE;
+    const bf16* Vh = Kl + TILE;
+    const bf16* Vl = Vh + TILE;
     // S = Q K^T for this warp's 16 rows and the chunk's 64 keys
     float sacc[8][4];
 #pragma unroll
@@ -350,6 +390,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
     }
     __syncthreads();
   }
+  cp_async_wait<0>();
+  __syncthreads();
   // publish this CTA's partial (unnormalised output, max, sum)
 #pragma unroll
   for (int dn = 0; dn < D / 8; ++dn) {
@@ -363,34 +405,51 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
     Ms[r_hi] = m_hi; Ls[r_hi] = l_hi;
   }
   cluster.sync();
-  // merge: CTA `rank` finalises rows rank, rank + CL, ... in cluster-rank order
-  for (int r = rank; r < QR; r += CL) {
-    const int gi = qr0 + r;
-    if (gi >= nq) break;
-    float mv[CL], lv[CL];
+  // merge: CTA `rank` finalises rows rank, rank + CL, ... in cluster-rank order.
+  // All (max, sum) pairs of its rows are fetched at once, then each thread
+  // fetches every rank's partial of its (row, column) elements in one batch.
+  constexpr int RPC = QR / CL;               // rows finalised per CTA
+  float* wsm = reinterpret_cast<float*>(Qh);  // [RPC][CL] merge weights (Q tiles are dead)
+  float* isn = wsm + RPC * CL;                // [RPC] 1 / total sum
+  if (tid < RPC * CL) {
+    const int i = tid / CL, c = tid % CL;
+    const int r = rank + i * CL;
+    wsm[tid] = *cluster.map_shared_rank(Ms + r, c);
+    isn[RPC + tid] = *cluster.map_shared_rank(Ls + r, c);  // staged after the weights
+  }
+  __syncthreads();
+  if (tid < RPC) {
     float M = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < CL; ++c) {
-      mv[c] = *cluster.map_shared_rank(Ms + r, c);
-      lv[c] = *cluster.map_shared_rank(Ls + r, c);
-      M = fmaxf(M, mv[c]);
-    }
+    for (int c = 0; c < CL; ++c) M = fmaxf(M, wsm[tid * CL + c]);
     float L = 0.f;
-    float wv[CL];
-#pragma unroll
     for (int c = 0; c < CL; ++c) {
-      wv[c] = mv[c] == -INFINITY ? 0.f : exp2f(mv[c] - M);
-      L += wv[c] * lv[c];
+      const float m = wsm[tid * CL + c];
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+      L += w * isn[RPC + tid * CL + c];
+      wsm[tid * CL + c] = w;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int t = row0 + gi / G, hq = kvh * G + gi % G;
-    for (int d = tid; d < D; d += 128) {
-      float acc = 0.f;
+    isn[tid] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
+  constexpr int PER = RPC * D / 128;  // (row, column) elements per thread
+  float pv[PER][CL];
 #pragma unroll
-      for (int c = 0; c < CL; ++c) acc += wv[c] * *cluster.map_shared_rank(Ob + r * OLD + d, c);
-      const size_t idx = ((size_t)t * a.Hq + hq) * D + d;
-      put_plane(a.o_hi, a.o_lo, a.out_bf16, idx, acc * inv);
-    }
+  for (int e = 0; e < PER; ++e) {
+    const int x = tid + e * 128, i = x / D, d = x % D;
+    const int r = rank + i * CL;
+#pragma unroll
+    for (int c = 0; c < CL; ++c) pv[e][c] = *cluster.map_shared_rank(Ob + r * OLD + d, c);
+  }
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int x = tid + e * 128, i = x / D, d = x % D;
+    const int gi = qr0 + rank + i * CL;
+    if (gi >= nq) continue;
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < CL; ++c) acc += wsm[i * CL + c] * pv[e][c];
+    const int t = row0 + gi / G, hq = kvh * G + gi % G;
+    put_plane(a.o_hi, a.o_lo, a.out_bf16, ((size_t)t * a.Hq + hq) * D + d, acc * isn[i]);
   }
   cluster.sync();
 }
@@ -399,8 +458,8 @@ template <int D>
 static bool launch_attn_mma(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
   const int G = a.Hq / a.Hkv;
   const int n_rg = (max_rows * G + QR - 1) / QR;
-  constexpr int QLD = D + 8, OLD = D + 4;
-  const size_t smem = (size_t)(2 * QR * QLD + 4 * 64 * QLD) * 2 + (size_t)QR * OLD * 4 + QR * 12;
+  constexpr int QLD = D + 8;
+  const size_t smem = (size_t)(2 * QR * QLD + 8 * 64 * QLD) * 2 + QR * 12;
   static bool init = false;
   if (!init) {
     if (cudaFuncSetAttribute(attention_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=

@@ -39,110 +39,137 @@ __device__ __forceinline__ void put_plane(void* hi, void* lo, int bf, size_t idx
   }
 }
 
-// rs: shared scratch of >= tn floats (row scales of the input norm).
+// Shared scratch of one epilogue call, in floats.
+constexpr int EPI_GROUP = 32;                 // tokens per epilogue pass
+constexpr int EPI_MAX_SSQ = 32;               // hidden <= 4096
+constexpr int EPI_SCRATCH_FLOATS = EPI_GROUP + EPI_GROUP * EPI_MAX_SSQ + EPI_GROUP * NTILE;
+
+// Epilogue of tokens t0 .. t0+tn-1.  Every pass first issues all of its
+// global loads (sums of squares, residual rows) into shared memory, so a pass
+// costs one memory round trip rather than one per token.
 __device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0, int tn,
-                               float* rs) {
+                                      float* scratch) {
   const EpiArgs& e = a.e;
   const int n0 = tile * NTILE;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
-  if (e.ssq_in) {
-    // rstd = 1 / sqrt(mean(x^2) + eps) from the per-128-column partial sums, in order
-    for (int tl = tid; tl < tn; tl += blockDim.x) {
-      const int row = e.in_rows ? e.in_rows[t0 + tl] : t0 + tl;
-      const float* p = e.ssq_in + (size_t)row * e.n_ssq;
-      float s = 0.f;
-      for (int i = 0; i < e.n_ssq; ++i) s += p[i];
-      rs[tl] = rsqrtf(s / (float)e.norm_H + e.eps);
+  float* rs = scratch;                                   // [EPI_GROUP] row scales
+  float* sq = rs + EPI_GROUP;                            // [EPI_GROUP][n_ssq]
+  float* rr = sq + EPI_GROUP * EPI_MAX_SSQ;              // [EPI_GROUP][NTILE] residual rows
+  for (int g0 = 0; g0 < tn; g0 += EPI_GROUP) {
+    const int gn = min(EPI_GROUP, tn - g0);
+    const bool norm = e.ssq_in != nullptr;
+    const bool resid = a.epi == EPI_RESID;
+    if (norm)
+      for (int x = tid; x < gn * e.n_ssq; x += blockDim.x) {
+        const int tl = x / e.n_ssq, i = x % e.n_ssq;
+        const int row = e.in_rows ? e.in_rows[t0 + g0 + tl] : t0 + g0 + tl;
+        sq[tl * e.n_ssq + i] = e.ssq_in[(size_t)row * e.n_ssq + i];
+      }
+    if (resid)
+      for (int x = tid; x < gn * NTILE; x += blockDim.x) {
+        const int tl = x / NTILE, c = x % NTILE;
+        rr[x] = e.resid[(size_t)(t0 + g0 + tl) * e.H + n0 + c];
+      }
+    if (norm || resid) __syncthreads();
+    if (norm) {
+      // rstd = 1 / sqrt(mean(x^2) + eps), partial sums added in column order
+      for (int tl = tid; tl < gn; tl += blockDim.x) {
+        float ssum = 0.f;
+        for (int i = 0; i < e.n_ssq; ++i) ssum += sq[tl * e.n_ssq + i];
+        rs[tl] = rsqrtf(ssum / (float)e.norm_H + e.eps);
+      }
+      __syncthreads();
+    }
+    for (int tl = warp; tl < gn; tl += nwarp) {
+      const int t = t0 + g0 + tl;
+      const float r = norm ? rs[tl] : 1.f;
+      const float* yrow = Ys + (size_t)(g0 + tl) * ys_ld;
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = yrow[lane + 32 * j] * r;
+      switch (a.epi) {
+        case EPI_STORE:
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int n = n0 + lane + 32 * j;
+            if (n < a.N) e.y[(size_t)t * e.ldy + n] = v[j];
+          }
+          break;
+        case EPI_RESID: {
+          float ss = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = lane + 32 * j, n = n0 + c;
+            const float x = rr[tl * NTILE + c] + v[j];
+            e.resid[(size_t)t * e.H + n] = x;
+            ss = fmaf(x, x, ss);
+            put_plane(e.pl_hi, e.pl_lo, e.plane_bf16, (size_t)t * e.ld_pl + n, x * e.g_next[n]);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          if (lane == 0) e.ssq_out[(size_t)t * (e.H / NTILE) + tile] = ss;
+          break;
+        }
+        case EPI_SWIGLU: {
+          // tile columns [0, 64) are gate rows, [64, 128) the up rows of the same 64 features
+          const int f0 = tile * SWIGLU_GROUP;
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            put_plane(e.pl_hi, e.pl_lo, e.plane_bf16, (size_t)t * e.ld_pl + f0 + lane + 32 * j,
+                      silu_f(v[j]) * v[j + 2]);
+          break;
+        }
+        case EPI_QKV: {
+          const int d = e.head_dim, half = d >> 1;
+          const int pos = e.row_pos[t];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = lane + 32 * j, n = n0 + c, jj = n % d;
+            float out = v[j];
+            if (n < e.q_dim + e.kv_dim) {  // q and k are rotated, v is not
+              const float2 cs = e.rope[(size_t)pos * half + (jj < half ? jj : jj - half)];
+              const float partner = yrow[jj < half ? c + half : c - half] * r;
+              out = jj < half ? (v[j] * cs.x - partner * cs.y) : (v[j] * cs.x + partner * cs.y);
+            }
+            if (n < e.q_dim) {
+              put_plane(e.q_hi, e.q_lo, e.plane_bf16, (size_t)t * e.q_dim + n, out);
+            } else {
+              const int req = e.plan->slot_req[e.row_slot[t]];
+              if (pos < 0 || pos >= e.cap) { set_err(e.err, DERR_CAPACITY); continue; }
+              const bool is_k = n < e.q_dim + e.kv_dim;
+              const int nn = is_k ? n - e.q_dim : n - e.q_dim - e.kv_dim;
+              const size_t off = (size_t)req * e.req_stride + ((size_t)(nn / d) * e.cap + pos) * d + nn % d;
+              if (is_k) put_plane(e.k_hi, e.k_lo, e.plane_bf16, off, out);
+              else put_plane(e.v_hi, e.v_lo, e.plane_bf16, off, out);
+            }
+          }
+          break;
+        }
+        case EPI_ARGMAX: {
+          float bv = -INFINITY;
+          int bi = 0x7fffffff;
+          bool nan = false;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int n = n0 + lane + 32 * j;
+            if (n >= a.N) continue;
+            if (v[j] != v[j]) nan = true;
+            if (e.logits) e.logits[(size_t)t * e.ld_logits + n] = v[j];
+            argmax_merge(bv, bi, v[j], n);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            argmax_merge(bv, bi, ov, oi);
+          }
+          if (__any_sync(0xffffffffu, nan) && lane == 0) set_err(e.err, DERR_NAN_LOGITS);
+          if (lane == 0 && bi != 0x7fffffff) atomicMax(e.amax + t, argmax_key(bv, bi));
+          break;
+        }
+      }
     }
     __syncthreads();
-  }
-  for (int tl = warp; tl < tn; tl += nwarp) {
-    const int t = t0 + tl;
-    const float r = e.ssq_in ? rs[tl] : 1.f;
-    float v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = Ys[tl * ys_ld + lane + 32 * j] * r;
-    switch (a.epi) {
-      case EPI_STORE:
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int n = n0 + lane + 32 * j;
-          if (n < a.N) e.y[(size_t)t * e.ldy + n] = v[j];
-        }
-        break;
-      case EPI_RESID: {
-        float ss = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int n = n0 + lane + 32 * j;
-          float* p = e.resid + (size_t)t * e.H + n;
-          const float x = *p + v[j];
-          *p = x;
-          ss = fmaf(x, x, ss);
-          put_plane(e.pl_hi, e.pl_lo, e.plane_bf16, (size_t)t * e.ld_pl + n, x * e.g_next[n]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) e.ssq_out[(size_t)t * (e.H / NTILE) + tile] = ss;
-        break;
-      }
-      case EPI_SWIGLU: {
-        // tile columns [0, 64) are gate rows, [64, 128) the up rows of the same 64 features
-        const int f0 = tile * SWIGLU_GROUP;
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-          put_plane(e.pl_hi, e.pl_lo, e.plane_bf16, (size_t)t * e.ld_pl + f0 + lane + 32 * j,
-                    silu_f(v[j]) * v[j + 2]);
-        break;
-      }
-      case EPI_QKV: {
-        const int d = e.head_dim, half = d >> 1;
-        const int pos = e.row_pos[t];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c = lane + 32 * j, n = n0 + c, jj = n % d;
-          float out = v[j];
-          if (n < e.q_dim + e.kv_dim) {  // q and k are rotated, v is not
-            const float2 cs = e.rope[(size_t)pos * half + (jj < half ? jj : jj - half)];
-            const float partner = Ys[tl * ys_ld + (jj < half ? c + half : c - half)] * r;
-            out = jj < half ? (v[j] * cs.x - partner * cs.y) : (v[j] * cs.x + partner * cs.y);
-          }
-          if (n < e.q_dim) {
-            e.qf[(size_t)t * e.q_dim + n] = out;
-          } else {
-            const int req = e.plan->slot_req[e.row_slot[t]];
-            if (pos < 0 || pos >= e.cap) { set_err(e.err, DERR_CAPACITY); continue; }
-            const bool is_k = n < e.q_dim + e.kv_dim;
-            const int nn = is_k ? n - e.q_dim : n - e.q_dim - e.kv_dim;
-            const size_t off = (size_t)req * e.req_stride + ((size_t)(nn / d) * e.cap + pos) * d + nn % d;
-            (is_k ? e.kc : e.vc)[off] = out;
-          }
-        }
-        break;
-      }
-      case EPI_ARGMAX: {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        bool nan = false;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int n = n0 + lane + 32 * j;
-          if (n >= a.N) continue;
-          if (v[j] != v[j]) nan = true;
-          if (e.logits) e.logits[(size_t)t * e.ld_logits + n] = v[j];
-          argmax_merge(bv, bi, v[j], n);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          argmax_merge(bv, bi, ov, oi);
-        }
-        if (__any_sync(0xffffffffu, nan) && lane == 0) set_err(e.err, DERR_NAN_LOGITS);
-        if (lane == 0 && bi != 0x7fffffff) atomicMax(e.amax + t, argmax_key(bv, bi));
-        break;
-      }
-    }
   }
 }
 

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
   float* Ws = sm;                          // [NTILE][KC + 1]
   float* Xs = Ws + NTILE * (KC + 1);       // [TZ][KC]
   float* Ys = Xs + TZ * KC;                // [TZ][YS_LD]
-  __shared__ float rs[TZ];
+  float* scratch = Ys + TZ * YS_LD;        // epilogue scratch
   __shared__ int s_last;
 
   const int tile = blockIdx.x, split = blockIdx.y, z = blockIdx.z;
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
       Ys[tl * YS_LD + nl] = v;
     }
     __syncthreads();
-    apply_epilogue(a, Ys, YS_LD, tile, t0, tn, rs);
+    apply_epilogue(a, Ys, YS_LD, tile, t0, tn, scratch);
   }
   if (a.epi == EPI_ARGMAX && s_last) {
     // every (tile, slice) contributes once; the grid counter expects tiles * slices
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmArgs a) {
 bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (dtype == 1) return launch_gemm_tc(a, s, pdl);
   dim3 grid(cdiv(a.N, NTILE), a.splits, cdiv(a.T, TZ));
-  size_t smem = sizeof(float) * (NTILE * (KC + 1) + TZ * KC + TZ * YS_LD);
+  size_t smem = sizeof(float) * (NTILE * (KC + 1) + TZ * KC + TZ * YS_LD + EPI_SCRATCH_FLOATS);
   static bool init = false;
   if (!init) {
     if (cudaFuncSetAttribute(gemm_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)

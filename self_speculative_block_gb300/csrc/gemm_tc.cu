@@ -39,7 +39,8 @@ constexpr int YLD = NTILE + 1;   // fp32 row stride of the partial tiles
 constexpr int A_BYTES = NTILE * 64 * 2;  // 128 x 64 bf16
 constexpr int SMEM_CAP = 200 * 1024;
 constexpr int DECODE_STAGE_CAP = 3;      // decode shapes: keep two CTAs per SM
-constexpr int TAIL_BYTES = TZ_TC * 4 + 16 * 8 + 64;  // row scales, barriers, TMEM holder
+constexpr int TAIL_BYTES = 16 * 8 + 64;  // barriers, TMEM holder
+constexpr int L2_PREFETCH_BLOCKS = 8;    // weight tiles a CTA brings into L2 ahead of its ring
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_mu;
@@ -81,6 +82,30 @@ bool tmap_2d(CUtensorMap* out, const void* ptr, int rows, int cols, int box_rows
 __host__ __device__ inline int cdiv_i(int a, int b) { return (a + b - 1) / b; }
 }  // namespace
 
+// Ys[j][row] = sum over the S cluster ranks (in rank order) of their partial
+// tiles' token g0 + j: every rank's values of up to 32 / S tokens are in flight
+// at once.
+template <int S>
+__device__ __forceinline__ void gather_splits(cooperative_groups::cluster_group& cluster, float* Yp, float* Ys,
+                                              int g0, int cnt, int row) {
+  constexpr int TB = 32 / S;
+  for (int jb = 0; jb < cnt; jb += TB) {
+    float pv[TB][S];
+#pragma unroll
+    for (int jj = 0; jj < TB; ++jj)
+#pragma unroll
+      for (int sp = 0; sp < S; ++sp)
+        pv[jj][sp] = jb + jj < cnt ? *cluster.map_shared_rank(Yp + (g0 + jb + jj) * YLD + row, sp) : 0.f;
+#pragma unroll
+    for (int jj = 0; jj < TB; ++jj) {
+      float acc = pv[jj][0];
+#pragma unroll
+      for (int sp = 1; sp < S; ++sp) acc += pv[jj][sp];
+      if (jb + jj < cnt) Ys[(jb + jj) * YLD + row] = acc;
+    }
+  }
+}
+
 // ring_bytes >= stages * (A tile + B tile) and >= the partial tile + reduce buffer.
 __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw,
                                                             const __grid_constant__ CUtensorMap tmx_hi,
@@ -93,12 +118,13 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   const int b_bytes = (two ? 2 : 1) * nt * 128;
   uint8_t* sA = smem;
   uint8_t* sB = sA + stages * A_BYTES;
-  // after the MMAs the ring is free: the partial tile and the reduce buffer live there
+  // after the MMAs the ring is free: the partial tile, the reduce buffer and
+  // the epilogue scratch live there
   float* Yp = reinterpret_cast<float*>(smem);             // [nt][YLD]
   float* Ys = Yp + nt * YLD;                               // [EG][YLD]
+  float* scratch = Ys + EG * YLD;                          // epilogue scratch
   uint8_t* tail = smem + ring_bytes;
-  float* rs = reinterpret_cast<float*>(tail);              // [TZ_TC] row scales
-  uint64_t* full = reinterpret_cast<uint64_t*>(rs + TZ_TC);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tail);
   uint64_t* empty = full + stages;
   uint64_t* done = empty + stages;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
@@ -146,6 +172,9 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
       tc::mbar_expect_tx(&full[kb], A_BYTES + b_bytes);
       tc::tma_load_2d_hint(sA + kb * A_BYTES, &tmw, k0 + kb * 64, n0, &full[kb], pol);
     }
+    // the rest of this CTA's weight tiles go to L2 now, so the ring refills
+    // after the dependency wait do not pay a DRAM round trip
+    for (int kb = pre; kb < nkb && kb < pre + L2_PREFETCH_BLOCKS; ++kb) tc::tma_prefetch_2d(&tmw, k0 + kb * 64, n0);
     tc::grid_dep_wait();
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % stages;
@@ -206,7 +235,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   if (warp == 0) tc::tmem_dealloc(tmem, ncols);
 
   if (S == 1) {
-    if (!failed) apply_epilogue(a, Yp, YLD, tile, t0, tn, rs);
+    if (!failed) apply_epilogue(a, Yp, YLD, tile, t0, tn, scratch);
   } else {
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
@@ -215,14 +244,17 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     const int ta = min(tn, rank * per), tb = min(tn, ta + per);
     for (int g0 = ta; g0 < tb; g0 += EG) {
       const int cnt = min(EG, tb - g0);
-      for (int j = 0; j < cnt; ++j) {
-        float acc = 0.f;
-        for (int s = 0; s < S; ++s) acc += *cluster.map_shared_rank(Yp + (g0 + j) * YLD + row, s);
-        Ys[j * YLD + row] = acc;
+      switch (S) {
+        case 2: gather_splits<2>(cluster, Yp, Ys, g0, cnt, row); break;
+        case 3: gather_splits<3>(cluster, Yp, Ys, g0, cnt, row); break;
+        case 4: gather_splits<4>(cluster, Yp, Ys, g0, cnt, row); break;
+        case 5: gather_splits<5>(cluster, Yp, Ys, g0, cnt, row); break;
+        case 6: gather_splits<6>(cluster, Yp, Ys, g0, cnt, row); break;
+        case 7: gather_splits<7>(cluster, Yp, Ys, g0, cnt, row); break;
+        default: gather_splits<8>(cluster, Yp, Ys, g0, cnt, row); break;
       }
       __syncthreads();
-      if (!failed) apply_epilogue(a, Ys, YLD, tile, t0 + g0, cnt, rs);
-      __syncthreads();
+      if (!failed) apply_epilogue(a, Ys, YLD, tile, t0 + g0, cnt, scratch);
     }
     cluster.sync();  // peers finished reading this CTA's partial tile
   }
@@ -243,7 +275,7 @@ bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
   const int nt = ((a.T < TZ_TC ? a.T : TZ_TC) + 15) / 16 * 16;
   const int nkb = cdiv_i(a.kchunk, 64);
   const int stage_bytes = A_BYTES + (two ? 2 : 1) * nt * 128;
-  const int y_bytes = (nt + EG) * YLD * 4;
+  const int y_bytes = ((nt + EG) * YLD + EPI_SCRATCH_FLOATS) * 4;
   int stages = (SMEM_CAP - 1024 - TAIL_BYTES) / stage_bytes;
   if (stages > 6) stages = 6;
   if (a.T <= 2 * 64 + 1 && stages > DECODE_STAGE_CAP) stages = DECODE_STAGE_CAP;

@@ -12,6 +12,7 @@
 #include "kernels.cuh"
 
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -27,6 +28,7 @@ struct GraphEntry {
   int mode, B, n_slots;
   cudaGraph_t graph;
   cudaGraphExec_t exec;
+  bool host_loop;  // body only, no device-side while node
 };
 
 }  // namespace
@@ -55,8 +57,12 @@ struct gocr_handle {
   int cap = 0, T_max = 0, T_dec = 0, sched_cap = 0;
   long long layer_stride = 0, req_stride = 0;
 
-  float* kc = nullptr;        // fp32 KV cache [req][layer][kv head][position][head_dim]
-  float* vc = nullptr;
+  // KV cache [req][layer][kv head][position][head_dim]: bf16 hi/lo planes for
+  // bf16 models, fp32 (in *_hi) for fp32 models; keys are stored rotated
+  void* kc_hi = nullptr;
+  void* kc_lo = nullptr;
+  void* vc_hi = nullptr;
+  void* vc_lo = nullptr;
   float* resid = nullptr;     // residual stream fp32 [T][H]
   void* xg_hi = nullptr;      // GEMM-input planes of resid * g (next norm's gain) [T][H]
   void* xg_lo = nullptr;
@@ -65,11 +71,13 @@ struct gocr_handle {
   void* hb_hi = nullptr;      // SwiGLU output planes [T][F]
   void* hb_lo = nullptr;
   float* ssq = nullptr;       // per-128-column sums of squares of resid [T][H/128]
-  float* qf = nullptr;        // rotated queries fp32 [T][q_dim]
+  void* q_hi = nullptr;       // rotated query planes [T][q_dim]
+  void* q_lo = nullptr;
   float* logits = nullptr;
   unsigned long long* amax = nullptr;
   int* grid_ctr = nullptr;
   bool pdl = true;            // programmatic dependent launch between forward kernels
+  bool host_loop = false;     // GOCR_HOST_LOOP=1: per-round graphs driven by the host
   int* dbuf = nullptr;
   int* vbuf = nullptr;
   int* abuf = nullptr;
@@ -164,7 +172,7 @@ void set_norm_in(gocr_handle* h, GemmArgs& a) {
 // RMSNorm is folded into the GEMMs: producers write resid * g (the next norm's
 // gain) as planes plus per-tile sums of squares; consumers scale by rstd.
 bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out,
-                     float* logits) {
+                     float* logits, const int* slot_tab) {
   const gocr_config& c = h->cfg;
   const int T = n_rows_of(kind, n_slots, B, P);
   const int H = c.hidden;
@@ -172,15 +180,18 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
   bool ok = true;
   launch_embed(h->dtype, h->embed, h->mask, h->prefix_stage, h->resid, h->gattn[0], h->xg_hi, h->xg_lo,
                h->ssq, h->rows, T, H, c.vocab, h->err, h->hs, pdl);
+  const size_t kv_es = h->dtype == GOCR_DTYPE_BF16 ? 2 : 4;
+  auto lay = [&](void* base, int l) -> void* {
+    return base ? (char*)base + (size_t)l * h->layer_stride * kv_es : nullptr;
+  };
   for (int l = 0; l < c.n_layers; ++l) {
-    float* kcl = h->kc + (size_t)l * h->layer_stride;
-    float* vcl = h->vc + (size_t)l * h->layer_stride;
     // QKV projection (input norm), RoPE, KV-cache write at each row's position
     GemmArgs g = gemm_base(h, h->xg_hi, h->xg_lo, H, h->wqkv[l], T, h->qkv_n, H);
     set_norm_in(h, g);
     g.epi = EPI_QKV;
-    g.e.qf = h->qf;
-    g.e.kc = kcl; g.e.vc = vcl;
+    g.e.q_hi = h->q_hi; g.e.q_lo = h->q_lo;
+    g.e.k_hi = lay(h->kc_hi, l); g.e.k_lo = lay(h->kc_lo, l);
+    g.e.v_hi = lay(h->vc_hi, l); g.e.v_lo = lay(h->vc_lo, l);
     g.e.req_stride = h->req_stride;
     g.e.q_dim = h->q_dim; g.e.kv_dim = h->kv_dim; g.e.head_dim = c.head_dim; g.e.cap = h->cap;
     g.e.rope = h->rope;
@@ -188,10 +199,14 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
     ok &= launch_gemm(h->dtype, g, h->hs, pdl);
     // attention with the row key limits of this forward's mask
     AttnArgs at{};
-    at.q = h->qf;
-    at.kc = kcl; at.vc = vcl; at.req_stride = h->req_stride;
+    at.q_hi = h->q_hi; at.q_lo = h->q_lo;
+    at.k_hi = g.e.k_hi; at.k_lo = g.e.k_lo; at.v_hi = g.e.v_hi; at.v_lo = g.e.v_lo;
+    at.req_stride = h->req_stride;
     at.o_hi = h->at_hi; at.o_lo = h->at_lo; at.out_bf16 = h->dtype == GOCR_DTYPE_BF16;
     at.row_lim = h->rows.row_lim; at.plan = h->rows.plan;
+    if (kind != PLAN_PREFILL) {  // committed cache chunks may be fetched before the wait
+      at.slot_req = slot_tab; at.st = h->st;
+    }
     at.T = T; at.Hq = c.n_q_heads; at.Hkv = c.n_kv_heads; at.d = c.head_dim; at.cap = h->cap;
     at.scale = 1.0f / sqrtf((float)c.head_dim);
     ok &= launch_attention(h->dtype, at, kind == PLAN_PREFILL ? 1 : n_slots,
@@ -238,17 +253,17 @@ bool enqueue_round(gocr_handle* h, int mode, int B, int n_slots, unsigned long l
   const int out_stride = cap;
   if (mode == GOCR_MODE_AR) {
     launch_plan(PLAN_AR, h->rows, h->st, h->slot_req, n_slots, 0, 0, nullptr, nullptr, cap, h->hs, h->pdl);
-    ok &= enqueue_forward(h, PLAN_AR, n_slots, 0, 0, h->abuf, nullptr);
+    ok &= enqueue_forward(h, PLAN_AR, n_slots, 0, 0, h->abuf, nullptr, h->slot_req);
     launch_ar_commit(h->st, h->slot_req, n_slots, h->abuf, h->out, out_stride, h->err, cond,
                      use_cond, h->hs, h->pdl);
     return ok;
   }
   launch_plan(PLAN_DRAFT, h->rows, h->st, h->slot_req, n_slots, B, 0, nullptr, nullptr, cap, h->hs, h->pdl);
-  ok &= enqueue_forward(h, PLAN_DRAFT, n_slots, B, 0, h->dbuf, nullptr);
+  ok &= enqueue_forward(h, PLAN_DRAFT, n_slots, B, 0, h->dbuf, nullptr, h->slot_req);
   launch_override(h->st, h->slot_req, n_slots, B, h->dbuf, h->ref, cap, h->sched, h->sched_cap,
                   h->cfg.vocab, h->hs, h->pdl);
   launch_plan(PLAN_VERIFY, h->rows, h->st, h->slot_req, n_slots, B, 0, h->dbuf, nullptr, cap, h->hs, h->pdl);
-  ok &= enqueue_forward(h, PLAN_VERIFY, n_slots, B, 0, h->vbuf, nullptr);
+  ok &= enqueue_forward(h, PLAN_VERIFY, n_slots, B, 0, h->vbuf, nullptr, h->slot_req);
   launch_accept(h->st, h->slot_req, n_slots, B, h->dbuf, h->vbuf, h->out, out_stride, h->err, cond,
                 use_cond, h->hs, h->pdl);
   return ok;
@@ -256,18 +271,21 @@ bool enqueue_round(gocr_handle* h, int mode, int B, int n_slots, unsigned long l
 
 int build_graph(gocr_handle* h, GraphEntry& e) {
   CK(cudaGraphCreate(&e.graph, 0));
-  cudaGraphConditionalHandle ch;
-  CK(cudaGraphConditionalHandleCreate(&ch, e.graph, 1, cudaGraphCondAssignDefault));
-  cudaGraphNodeParams np{};
-  np.type = cudaGraphNodeTypeConditional;
-  np.conditional.handle = ch;
-  np.conditional.type = cudaGraphCondTypeWhile;
-  np.conditional.size = 1;
-  cudaGraphNode_t node;
-  CK(cudaGraphAddNode(&node, e.graph, nullptr, nullptr, 0, &np));
-  cudaGraph_t body = np.conditional.phGraph_out[0];
+  cudaGraph_t body = e.graph;
+  cudaGraphConditionalHandle ch = 0;
+  if (!e.host_loop) {
+    CK(cudaGraphConditionalHandleCreate(&ch, e.graph, 1, cudaGraphCondAssignDefault));
+    cudaGraphNodeParams np{};
+    np.type = cudaGraphNodeTypeConditional;
+    np.conditional.handle = ch;
+    np.conditional.type = cudaGraphCondTypeWhile;
+    np.conditional.size = 1;
+    cudaGraphNode_t node;
+    CK(cudaGraphAddNode(&node, e.graph, nullptr, nullptr, 0, &np));
+    body = np.conditional.phGraph_out[0];
+  }
   CK(cudaStreamBeginCaptureToGraph(h->hs, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal));
-  bool enq = enqueue_round(h, e.mode, e.B, e.n_slots, (unsigned long long)ch, 1);
+  bool enq = enqueue_round(h, e.mode, e.B, e.n_slots, (unsigned long long)ch, e.host_loop ? 0 : 1);
   cudaError_t le = cudaGetLastError();
   cudaGraph_t captured = nullptr;
   cudaError_t ce = cudaStreamEndCapture(h->hs, &captured);
@@ -281,7 +299,7 @@ int build_graph(gocr_handle* h, GraphEntry& e) {
 int get_graph(gocr_handle* h, int mode, int B, int n_slots, cudaGraphExec_t* exec) {
   for (auto& g : h->graphs)
     if (g.mode == mode && g.B == B && g.n_slots == n_slots) { *exec = g.exec; return GOCR_OK; }
-  GraphEntry e{mode, B, n_slots, nullptr, nullptr};
+  GraphEntry e{mode, B, n_slots, nullptr, nullptr, h->host_loop};
   int rc = build_graph(h, e);
   if (rc != GOCR_OK && h->pdl) {
     // fall back to plain stream order inside the loop body
@@ -371,7 +389,22 @@ int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const in
   int rc = get_graph(h, mode, B, n, &exec);
   if (rc) return rc;
   CK(cudaEventRecord(h->ev0, h->hs));
-  CK(cudaGraphLaunch(exec, h->hs));
+  if (!h->host_loop) {
+    CK(cudaGraphLaunch(exec, h->hs));
+  } else {
+    // one graph per round; the host polls the done flags after every round
+    for (int round = 0; round < bound + 2; ++round) {
+      CK(cudaGraphLaunch(exec, h->hs));
+      bool all_done = true;
+      for (int i = 0; i < n; ++i) {
+        int dn = 0;
+        CK(cudaMemcpyAsync(&dn, &h->st[reqs[i]].done, sizeof(int), cudaMemcpyDeviceToHost, h->hs));
+        CK(cudaStreamSynchronize(h->hs));
+        all_done &= dn != 0;
+      }
+      if (all_done) break;
+    }
+  }
   CK(cudaEventRecord(h->ev1, h->hs));
   std::vector<ReqState> sts(n);
   for (int i = 0; i < n; ++i) {
@@ -409,7 +442,7 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
   *out = nullptr;
   const gocr_config c = *cfg;
   const int q_dim = c.n_q_heads * c.head_dim, kv_dim = c.n_kv_heads * c.head_dim;
-  if (c.n_layers < 1 || c.hidden < 128 || c.hidden % 128 || c.vocab < 128 || c.vocab % 128 ||
+  if (c.n_layers < 1 || c.hidden < 128 || c.hidden % 128 || c.hidden > 4096 || c.vocab < 128 || c.vocab % 128 ||
       (c.head_dim != 64 && c.head_dim != 128) || c.n_kv_heads < 1 || c.n_q_heads % c.n_kv_heads ||
       q_dim % 128 || kv_dim % 128 || c.ffn < 64 || c.ffn % 64 ||
       (c.dtype != GOCR_DTYPE_F32 && c.dtype != GOCR_DTYPE_BF16))
@@ -447,6 +480,10 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
       g_lib_error = h->msg; gocr_free(h); *out = nullptr; return r_;               \
     }                                                                              \
   } while (0)
+  {
+    const char* hl = getenv("GOCR_HOST_LOOP");
+    h->host_loop = hl && hl[0] == '1';
+  }
   CKC(cudaStreamCreateWithFlags(&h->hs, cudaStreamNonBlocking));
   CKC(cudaEventCreate(&h->ev0));
   CKC(cudaEventCreate(&h->ev1));
@@ -479,8 +516,15 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->gattn.push_back((const float*)L[7]); h->gmlp.push_back((const float*)L[8]);
   }
   const size_t kv_elems = (size_t)h->req_stride * R;
-  h->kc = (float*)A(kv_elems * 4);
-  h->vc = (float*)A(kv_elems * 4);
+  const size_t kv_es = h->dtype == GOCR_DTYPE_BF16 ? 2 : 4;
+  h->kc_hi = A(kv_elems * kv_es);
+  h->vc_hi = A(kv_elems * kv_es);
+  h->q_hi = A((size_t)T * q_dim * kv_es);
+  if (h->dtype == GOCR_DTYPE_BF16) {
+    h->kc_lo = A(kv_elems * kv_es);
+    h->vc_lo = A(kv_elems * kv_es);
+    h->q_lo = A((size_t)T * q_dim * kv_es);
+  }
   h->resid = (float*)A((size_t)T * H * 4);
   h->xg_hi = A((size_t)T * H * es);
   h->at_hi = A((size_t)T * q_dim * es);
@@ -491,7 +535,6 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->hb_lo = A((size_t)T * c.ffn * es);
   }
   h->ssq = (float*)A((size_t)T * (H / NTILE) * 4);
-  h->qf = (float*)A((size_t)T * q_dim * 4);
   h->logits = (float*)A((size_t)h->T_dec * c.vocab * 4);
   h->amax = (unsigned long long*)A((size_t)T * 8);
   h->grid_ctr = (int*)A(256);
@@ -557,7 +600,7 @@ int gocr_prefill(gocr_handle* h, int req, const void* prefix_embeds, int P) {
   CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
   launch_plan(PLAN_PREFILL, h->rows, h->st, h->slot_one, 1, 0, P, nullptr, nullptr, h->cap, h->hs, false);
-  if (!enqueue_forward(h, PLAN_PREFILL, 1, 0, P, h->am, nullptr))
+  if (!enqueue_forward(h, PLAN_PREFILL, 1, 0, P, h->am, nullptr, h->slot_one))
     return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   launch_prefill_finish(h->st, req, P, h->am, h->out, h->cap, h->hs);
   CK(cudaGetLastError());
@@ -638,7 +681,7 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
   CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
   launch_plan(pk, h->rows, h->st, h->slot_one, 1, B, 0, nullptr, h->dbg_toks, h->cap, h->hs, false);
-  if (!enqueue_forward(h, pk, 1, B, 0, h->am, h->logits))
+  if (!enqueue_forward(h, pk, 1, B, 0, h->am, h->logits, h->slot_one))
     return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   CK(cudaGetLastError());
   if (logits_out)
@@ -656,15 +699,37 @@ int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, float* k_o
   const gocr_config& c = h->cfg;
   if (layer < 0 || layer >= c.n_layers || pos0 < 0 || n < 0 || pos0 + n > h->cap || !k_out || !v_out)
     return fail(h, GOCR_EINVAL, "bad KV range");
-  const size_t d = c.head_dim;
-  for (int kvh = 0; kvh < c.n_kv_heads; ++kvh) {
-    size_t off = (size_t)req * h->req_stride + (size_t)layer * h->layer_stride + ((size_t)kvh * h->cap + pos0) * d;
-    CK(cudaMemcpy2DAsync(k_out + kvh * d, c.n_kv_heads * d * 4, h->kc + off, d * 4, d * 4, n,
-                         cudaMemcpyDeviceToHost, h->hs));
-    CK(cudaMemcpy2DAsync(v_out + kvh * d, c.n_kv_heads * d * 4, h->vc + off, d * 4, d * 4, n,
-                         cudaMemcpyDeviceToHost, h->hs));
+  const size_t d = c.head_dim, Hkv = c.n_kv_heads;
+  const bool bf = h->dtype == GOCR_DTYPE_BF16;
+  const size_t es = bf ? 2 : 4;
+  std::vector<unsigned char> hi(n * Hkv * d * es), lo(bf ? n * Hkv * d * es : 0);
+  void* planes[2][2] = {{h->kc_hi, h->kc_lo}, {h->vc_hi, h->vc_lo}};
+  float* outs[2] = {k_out, v_out};
+  for (int kv = 0; kv < 2; ++kv) {
+    for (int p = 0; p < (bf ? 2 : 1); ++p) {
+      unsigned char* dst = p ? lo.data() : hi.data();
+      for (size_t kvh = 0; kvh < Hkv; ++kvh) {
+        size_t off = (size_t)req * h->req_stride + (size_t)layer * h->layer_stride + (kvh * h->cap + pos0) * d;
+        CK(cudaMemcpy2DAsync(dst + kvh * d * es, Hkv * d * es, (char*)planes[kv][p] + off * es, d * es, d * es, n,
+                             cudaMemcpyDeviceToHost, h->hs));
+      }
+    }
+    CK(cudaStreamSynchronize(h->hs));
+    const size_t m = (size_t)n * Hkv * d;
+    if (bf) {
+      const uint16_t* a = reinterpret_cast<const uint16_t*>(hi.data());
+      const uint16_t* b = reinterpret_cast<const uint16_t*>(lo.data());
+      for (size_t i = 0; i < m; ++i) {
+        uint32_t ua = (uint32_t)a[i] << 16, ub = (uint32_t)b[i] << 16;
+        float fa, fb;
+        memcpy(&fa, &ua, 4);
+        memcpy(&fb, &ub, 4);
+        outs[kv][i] = fa + fb;
+      }
+    } else {
+      memcpy(outs[kv], hi.data(), m * 4);
+    }
   }
-  CK(cudaStreamSynchronize(h->hs));
   return GOCR_OK;
 }
 
@@ -728,15 +793,18 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
   return GOCR_OK;
 }
 
-int gocr_op_attention(int dtype, const float* q, const float* kc, const float* vc, float* o,
-                      const int32_t* lim, int T, int Hq, int Hkv, int d, int cap, void* stream) {
+int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
+                      const void* v_hi, const void* v_lo, float* o, const int32_t* lim, int T, int Hq, int Hkv,
+                      int d, int cap, void* stream) {
   gocr_handle* h = nullptr;
   if (dtype != GOCR_DTYPE_F32 && dtype != GOCR_DTYPE_BF16) return fail(h, GOCR_EINVAL, "bad dtype");
-  if (!q || !kc || !vc || !o || !lim) return fail(h, GOCR_EINVAL, "null pointer");
+  if (!q_hi || !k_hi || !v_hi || !o || !lim) return fail(h, GOCR_EINVAL, "null pointer");
+  if (dtype == GOCR_DTYPE_BF16 && (!q_lo || !k_lo || !v_lo)) return fail(h, GOCR_EINVAL, "missing lo plane");
   if (T < 1 || Hkv < 1 || Hq % Hkv || (d != 64 && d != 128) || cap < 1)
     return fail(h, GOCR_EINVAL, "bad shape");
   AttnArgs a{};
-  a.q = q; a.kc = kc; a.vc = vc; a.req_stride = 0; a.o_hi = o; a.o_lo = nullptr; a.out_bf16 = 0;
+  a.q_hi = q_hi; a.q_lo = q_lo; a.k_hi = k_hi; a.k_lo = k_lo; a.v_hi = v_hi; a.v_lo = v_lo;
+  a.req_stride = 0; a.o_hi = o; a.o_lo = nullptr; a.out_bf16 = 0;
   a.row_lim = lim; a.plan = nullptr;
   a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.cap = cap; a.scale = 1.0f / sqrtf((float)d);
   if (!launch_attention(dtype, a, 1, T, (cudaStream_t)stream, false))

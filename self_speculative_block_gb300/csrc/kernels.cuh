@@ -3,7 +3,7 @@
 // Data flow of one decoder forward (T rows):
 //   embed:  resid = E[tok] | [M] | prefix row;  X0 = resid * g_attn[0];  ssq
 //   per layer:
-//     qkv    = rstd * (X W_qkv^T)  -> RoPE; q -> qf, k/v -> fp32 KV cache
+//     qkv    = rstd * (X W_qkv^T)  -> RoPE; q planes, k/v planes into the KV cache
 //     attn   = softmax(q K^T / sqrt(d), row key limits) V   -> A planes
 //     resid += A W_o^T             -> X = resid * g_mlp;  ssq
 //     h      = silu(g) * u, [g|u] = rstd * (X W_gu^T)        -> H planes
@@ -44,10 +44,11 @@ struct EpiArgs {
   float* ssq_out;
   // planes written by RESID and SWIGLU: bf16 hi/lo (plane_bf16) or one fp32 array in pl_hi
   void* pl_hi; void* pl_lo; int ld_pl; int plane_bf16;
-  // QKV: q -> qf [T, q_dim] fp32; k, v -> fp32 cache of the row's request at its position
-  float* qf;
-  float* kc; float* vc;          // cache of request 0 at this layer
-  long long req_stride;          // floats between two requests' caches
+  // QKV: q -> planes [T, q_dim]; k, v -> cache planes of the row's request at its position
+  // (bf16 hi/lo planes for bf16 models, one fp32 plane for fp32 models)
+  void* q_hi; void* q_lo;
+  void* k_hi; void* k_lo; void* v_hi; void* v_lo;  // cache planes of request 0 at this layer
+  long long req_stride;          // elements between two requests' caches
   int q_dim, kv_dim, head_dim, cap;
   const float2* rope;            // [cap][head_dim/2] (cos, sin)
   const int* row_pos; const int* row_slot; const Plan* plan;
@@ -84,13 +85,18 @@ int gemm_counter_ints(int T, int N);
 
 // ---------------------------------------------------------------- attention
 struct AttnArgs {
-  const float* q;          // [T, Hq, d] fp32
-  const float* kc; const float* vc;   // request 0's cache at this layer: [Hkv][cap][d] fp32
-  long long req_stride;    // floats between requests' caches
+  // q [T, Hq, d] and the KV cache [Hkv][cap][d] of request 0 at this layer, as
+  // planes: bf16 hi + lo (bf16 models) or fp32 in *_hi (fp32 models)
+  const void* q_hi; const void* q_lo;
+  const void* k_hi; const void* k_lo; const void* v_hi; const void* v_lo;
+  long long req_stride;    // elements between requests' caches
   void* o_hi; void* o_lo;  // output planes [T, Hq*d] (bf16 hi/lo, or fp32 in o_hi)
-  int out_bf16;            // planes are bf16 (1) or fp32 (0)
+  int out_bf16;            // output planes are bf16 (1) or fp32 (0)
   const int* row_lim;      // [T]
   const Plan* plan;        // slot layout; NULL = one slot of T rows, request 0
+  // decode launches: the slot table and request states, constant during a
+  // forward, let CTAs fetch committed cache chunks before the dependency wait
+  const int* slot_req; const ReqState* st; int rows_per_slot;
   int T, Hq, Hkv, d, cap;
   float scale;
 };

@@ -66,6 +66,12 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const void* tmap, in
       : "memory");
 }
 
+// Bring a tile of the tensor into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

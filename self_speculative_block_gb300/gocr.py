@@ -100,7 +100,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gocr_free": (None, [vp]),
         "gocr_op_linear_workspace": (sz, [i32, i32, i32]),
         "gocr_op_linear": (i32, [i32, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
-        "gocr_op_attention": (i32, [i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
+        "gocr_op_attention": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -312,14 +312,20 @@ def op_linear(x, w, workspace=None):
 
 
 def op_attention(q, kc, vc, lim, dtype: int):
-    """The decoder's attention kernel for `dtype` (DTYPE_BF16 / DTYPE_F32) on fp32
-    tensors: q [T, Hq, d]; kc, vc [Hkv, cap, d]; lim int32 [T] on the device."""
+    """The decoder's attention kernel for `dtype` (DTYPE_BF16 / DTYPE_F32).
+
+    q [T, Hq, d], kc and vc [Hkv, cap, d]: fp32 tensors for DTYPE_F32, or
+    (hi, lo) pairs of bf16 tensors for DTYPE_BF16; lim int32 [T] on the
+    device.  Returns fp32 [T, Hq, d]."""
     torch = _torch()
     lib = load()
-    T, Hq, d = q.shape
-    Hkv, cap, _ = kc.shape
-    o = torch.empty_like(q)
-    stream = torch.cuda.current_stream(q.device).cuda_stream
-    _check(lib.gocr_op_attention(dtype, q.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(),
+    pair = lambda t: (t[0], t[1]) if isinstance(t, (tuple, list)) else (t, None)
+    (qh, ql), (kh, kl), (vh, vl) = pair(q), pair(kc), pair(vc)
+    T, Hq, d = qh.shape
+    Hkv, cap, _ = kh.shape
+    o = torch.empty((T, Hq, d), dtype=torch.float32, device=qh.device)
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    stream = torch.cuda.current_stream(qh.device).cuda_stream
+    _check(lib.gocr_op_attention(dtype, ptr(qh), ptr(ql), ptr(kh), ptr(kl), ptr(vh), ptr(vl), o.data_ptr(),
                                  lim.data_ptr(), T, Hq, Hkv, d, cap, stream))
     return o

@@ -57,6 +57,17 @@ def test_linear_row_bits_do_not_depend_on_row_count(g, dt):
         assert torch.equal(part, full[:T]), T
 
 
+def _planes(a, dtype):
+    """fp32 array -> the kernel's operand: fp32 tensor, or (hi, lo) bf16 tensors with a = hi + lo."""
+    from self_speculative_block_gb300 import gocr, synth
+    if dtype == gocr.DTYPE_F32:
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+    hi = synth.bf16_bits(a)
+    lo = synth.bf16_bits(a.astype(np.float32) - synth.bf16_to_f32(hi))
+    t = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).cuda().view(torch.bfloat16)
+    return (t(hi), t(lo))
+
+
 def _attn_case(rng, T, Hq, Hkv, d, cap, lims, dtype):
     from self_speculative_block_gb300 import gocr
     q = rng.standard_normal((T, Hq, d)).astype(np.float32)
@@ -66,8 +77,8 @@ def _attn_case(rng, T, Hq, Hkv, d, cap, lims, dtype):
     allowed = np.arange(cap)[None, :] <= lim[:, None]
     ref = oracle.attention(q.astype(np.float64), k.transpose(1, 0, 2).astype(np.float64),
                            v.transpose(1, 0, 2).astype(np.float64), allowed)
-    t = lambda a: torch.from_numpy(a).cuda()
-    o = gocr.op_attention(t(q), t(k), t(v), t(lim), dtype).cpu().numpy()
+    o = gocr.op_attention(_planes(q, dtype), _planes(k, dtype), _planes(v, dtype),
+                          torch.from_numpy(lim).cuda(), dtype).cpu().numpy()
     return o, ref
 
 
@@ -78,7 +89,7 @@ def test_attention_draft_and_verify_masks(g, dt, Hq, Hkv, d, p, B):
     rng = np.random.default_rng(p + B + d)
     cap = p + B + 3
     dtype = g.DTYPE_BF16 if dt == "bf16" else g.DTYPE_F32
-    # the bf16 kernel runs on hi/lo splits of the fp32 inputs with bf16 probabilities
+    # the bf16 kernel takes hi/lo bf16 planes of the fp32 inputs and bf16 probabilities
     tol = 5e-3 if dt == "bf16" else 2e-5
     # draft: boundary row causal (lim p), [M] rows see the window (lim p+B)
     o, ref = _attn_case(rng, B + 1, Hq, Hkv, d, cap, [p] + [p + B] * B, dtype)
@@ -93,12 +104,11 @@ def test_attention_row_bits_do_not_depend_on_other_rows(g, dt):
     rng = np.random.default_rng(3)
     dtype = g.DTYPE_BF16 if dt == "bf16" else g.DTYPE_F32
     Hq, Hkv, d, cap = 12, 4, 128, 700
-    t = lambda a: torch.from_numpy(a.astype(np.float32)).cuda()
-    q = t(rng.standard_normal((65, Hq, d)))
-    k = t(rng.standard_normal((Hkv, cap, d)))
-    v = t(rng.standard_normal((Hkv, cap, d)))
+    qn = rng.standard_normal((65, Hq, d)).astype(np.float32)
+    k = _planes(rng.standard_normal((Hkv, cap, d)).astype(np.float32), dtype)
+    v = _planes(rng.standard_normal((Hkv, cap, d)).astype(np.float32), dtype)
     lim = torch.arange(600, 665, dtype=torch.int32, device="cuda")
-    full = g.op_attention(q, k, v, lim, dtype)
+    full = g.op_attention(_planes(qn, dtype), k, v, lim, dtype)
     for j in (0, 1, 31, 64):
-        one = g.op_attention(q[j:j + 1].contiguous(), k, v, lim[j:j + 1].contiguous(), dtype)
+        one = g.op_attention(_planes(qn[j:j + 1], dtype), k, v, lim[j:j + 1].contiguous(), dtype)
         assert torch.equal(one[0], full[j]), j
