@@ -26,13 +26,13 @@
 #include <cooperative_groups.h>
 
 #include "epilogue.cuh"
+#include "tc.cuh"
 
 namespace gocr {
 
 namespace {
 constexpr int ROWS = 128;   // CUDA-core kernel: query rows (token, q head) per CTA
 constexpr int CH = 64;      // keys per chunk
-constexpr int CL = 8;       // tensor-core kernel: CTAs per cluster (key-chunk split)
 constexpr int QR = 64;      // tensor-core kernel: query rows per cluster
 constexpr float LOG2E = 1.4426950408889634f;
 }  // namespace
@@ -160,6 +160,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Hint a contiguous global range into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, int bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // 16-byte asynchronous global -> shared copy; src_bytes = 0 fills zeros.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
@@ -170,21 +175,38 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int D>
-__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_kernel(AttnArgs a) {
+// Tensor-core kernel: 256 threads, keys in chunks of AC = 32.  Warp w owns
+// query rows 16 (w % 4) .. 16 (w % 4) + 15 of the row group and key half w / 4
+// (keys 16 (w / 4) .. 16 (w / 4) + 15 of every chunk), so each (cluster rank,
+// key half) runs its own online softmax over a fixed set of absolute key
+// positions.  The two halves of a CTA are merged in shared memory (half 0,
+// then half 1), then every CTA pushes its partial rows to the rows' owner CTAs
+// over distributed shared memory (row r belongs to rank r % CL) and, after one
+// cluster barrier, each owner adds the CL partials in rank order.
+constexpr int AC = 32;  // keys per chunk of the tensor-core kernel
+
+template <int D, int CL>
+__global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int QLD = D + 8;   // bf16 row stride of the Q, K and V tiles
-  constexpr int OLD = D + 4;   // fp32 row stride of the partial output
-  constexpr int TILE = 64 * QLD;
+  constexpr int OLD = D + 4;   // fp32 row stride of the half-1 partial
+  constexpr int TILE = AC * QLD;
+  constexpr int RPC = QR / CL; // rows owned per CTA
   extern __shared__ __align__(16) uint8_t sm_raw[];
   bf16* Qh = reinterpret_cast<bf16*>(sm_raw);            // [QR][QLD]
   bf16* Ql = Qh + QR * QLD;
-  bf16* KV = Ql + QR * QLD;                              // 2 stages x {Kh, Kl, Vh, Vl} [64][QLD]
-  float* Ob = reinterpret_cast<float*>(KV);              // [QR][OLD], after the chunk loop
-  float* Ms = reinterpret_cast<float*>(KV + 8 * TILE);   // [QR] running max (log2 units)
-  float* Ls = Ms + QR;                                   // [QR] running sum
-  int* Lim = reinterpret_cast<int*>(Ls + QR);            // [QR]
+  bf16* KV = Ql + QR * QLD;                              // {Kh, Kl, Vh, Vl} [AC][QLD]
+  float* Oh = reinterpret_cast<float*>(Qh);              // [QR][OLD] half-1 partial (Q is dead by then)
+  float* Mh = Oh + QR * OLD;                             // [QR]
+  float* Lh = Mh + QR;                                   // [QR]
+  constexpr int RLD = D + 4;   // fp32 stride of a partial row: D outputs, max, sum, pad
+  float* RX = reinterpret_cast<float*>(KV + 4 * TILE);   // [CL][RPC][RLD] partial rows from each rank
+  float* ST = reinterpret_cast<float*>(KV);              // [CL][RPC][RLD] rows to send, after the loop
+  float* WS = RX + CL * RPC * RLD;                       // [RPC][CL] merge weights
+  float* IL = WS + RPC * CL;                             // [RPC] 1 / total sum
+  int* Lim = reinterpret_cast<int*>(IL + RPC);           // [QR]
+  __shared__ __align__(8) uint64_t rxbar;
   __shared__ int s_maxlim;
 
   const int rank = blockIdx.x;  // == cluster rank (the cluster spans grid x)
@@ -193,40 +215,56 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
   const int slot = blockIdx.z;
   const int G = a.Hq / a.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = warp & 3, kh = warp >> 2;
   const int g = lane >> 2, tq = lane & 3;
 
-  // issue the cp.async copies of chunk c (keys c*64 .. c*64+63, zero past kmax) into stage st_i
-  auto load_chunk = [&](const bf16* kh, const bf16* kl, const bf16* vh, const bf16* vl, int c, int kmax, int st_i) {
-    bf16* dst = KV + st_i * 4 * TILE;
-    for (int x = tid; x < 4 * 64 * (D / 8); x += 128) {
-      const int pl = x / (64 * (D / 8)), rem = x % (64 * (D / 8));
+  // cp.async copies of chunk c (keys c*AC .. c*AC+AC-1, zero past kmax)
+  auto load_chunk = [&](const bf16* k_h, const bf16* k_l, const bf16* v_h, const bf16* v_l, int c, int kmax) {
+    for (int x = tid; x < 4 * AC * (D / 8); x += 256) {
+      const int pl = x / (AC * (D / 8)), rem = x % (AC * (D / 8));
       const int j = rem / (D / 8), v = rem % (D / 8);
-      const int key = c * 64 + j;
-      const bf16* base = pl == 0 ? kh : pl == 1 ? kl : pl == 2 ? vh : vl;
+      const int key = c * AC + j;
+      const bf16* base = pl == 0 ? k_h : pl == 1 ? k_l : pl == 2 ? v_h : v_l;
       const bool in = key <= kmax;
-      cp_async16(dst + pl * TILE + j * QLD + v * 8, base + (size_t)(in ? key : 0) * D + v * 8, in ? 16 : 0);
+      cp_async16(KV + pl * TILE + j * QLD + v * 8, base + (size_t)(in ? key : 0) * D + v * 8, in ? 16 : 0);
     }
   };
 
-  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // committed cache chunk before the dependency wait (decode launches only)
+  if (tid == 0) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    tc::mbar_init(&rxbar, 1);
+    tc::fence_mbar_init();
+    tc::mbar_expect_tx(&rxbar, (uint32_t)(CL * RPC * RLD * 4));  // one block of rows from every rank
+  }
+  cluster.sync();  // every receive barrier is armed before any rank sends
+  // committed cache before the dependency wait (decode launches only): the
+  // first chunk into shared memory, the CTA's later committed chunks into L2
   int req_pre = -1, pc = 0;
   if (a.st && a.slot_req) {
     req_pre = a.slot_req[slot];
     pc = a.st[req_pre].cache_len;
   }
-  const bool pre = req_pre >= 0 && (rank + 1) * 64 <= pc;
-  const size_t kv_off_pre = pre ? (size_t)req_pre * a.req_stride + (size_t)kvh * a.cap * D : 0;
+  const bool pre = req_pre >= 0 && (rank + 1) * AC <= pc;
   if (pre) {
-    load_chunk(reinterpret_cast<const bf16*>(a.k_hi) + kv_off_pre, reinterpret_cast<const bf16*>(a.k_lo) + kv_off_pre,
-               reinterpret_cast<const bf16*>(a.v_hi) + kv_off_pre, reinterpret_cast<const bf16*>(a.v_lo) + kv_off_pre,
-               rank, pc - 1, 0);
+    const size_t o = (size_t)req_pre * a.req_stride + (size_t)kvh * a.cap * D;
+    const bf16* pk[4] = {reinterpret_cast<const bf16*>(a.k_hi) + o, reinterpret_cast<const bf16*>(a.k_lo) + o,
+                         reinterpret_cast<const bf16*>(a.v_hi) + o, reinterpret_cast<const bf16*>(a.v_lo) + o};
+    load_chunk(pk[0], pk[1], pk[2], pk[3], rank, pc - 1);
     cp_async_commit();
+    // later committed chunks of this CTA: rank + CL, rank + 2 CL, ... (4 planes each)
+    for (int i = tid; i < 4 * 8; i += 256) {
+      const int c = rank + (1 + i / 4) * CL;
+      if ((c + 1) * AC <= pc) prefetch_l2(pk[i % 4] + (size_t)c * AC * D, AC * D * 2);
+    }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   int req = 0, row0 = 0, nrows = a.T;
-  if (a.plan) {
+  if (a.rows_per_slot > 0) {
+    req = a.slot_req[slot];
+    row0 = slot * a.rows_per_slot;
+    nrows = a.rows_per_slot;
+  } else if (a.plan) {
     req = a.plan->slot_req[slot];
     row0 = a.plan->slot_row0[slot];
     nrows = a.plan->slot_nrows[slot];
@@ -238,17 +276,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
     return;
   }
   const size_t kv_off = (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
-  const bf16* kh = reinterpret_cast<const bf16*>(a.k_hi) + kv_off;
-  const bf16* kl = reinterpret_cast<const bf16*>(a.k_lo) + kv_off;
-  const bf16* vh = reinterpret_cast<const bf16*>(a.v_hi) + kv_off;
-  const bf16* vl = reinterpret_cast<const bf16*>(a.v_lo) + kv_off;
+  const bf16* k_h = reinterpret_cast<const bf16*>(a.k_hi) + kv_off;
+  const bf16* k_l = reinterpret_cast<const bf16*>(a.k_lo) + kv_off;
+  const bf16* v_h = reinterpret_cast<const bf16*>(a.v_hi) + kv_off;
+  const bf16* v_l = reinterpret_cast<const bf16*>(a.v_lo) + kv_off;
   const bf16* qh = reinterpret_cast<const bf16*>(a.q_hi);
   const bf16* ql = reinterpret_cast<const bf16*>(a.q_lo);
 
   if (tid == 0) s_maxlim = -1;
   __syncthreads();
   // Q planes of this row group (zero past the window) and the rows' key limits
-  for (int x = tid; x < 2 * QR * (D / 8); x += 128) {
+  for (int x = tid; x < 2 * QR * (D / 8); x += 256) {
     const int pl = x / (QR * (D / 8)), rem = x % (QR * (D / 8));
     const int r = rem / (D / 8), v = rem % (D / 8);
     const int gi = qr0 + r;
@@ -266,39 +304,37 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
   }
   __syncthreads();
   const int maxlim = s_maxlim;
-  const int n_chunks = maxlim < 0 ? 0 : maxlim / 64 + 1;
+  const int n_chunks = maxlim < 0 ? 0 : maxlim / AC + 1;
   const float sl2 = a.scale * LOG2E;
-  if (!pre && rank < n_chunks) load_chunk(kh, kl, vh, vl, rank, maxlim, 0);
-  cp_async_commit();
 
-  const int r_lo = warp * 16 + g, r_hi = r_lo + 8;
+  const int r_lo = mt * 16 + g, r_hi = r_lo + 8;
   const int lim_lo = Lim[r_lo], lim_hi = Lim[r_hi];
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
   float oacc[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int lcol = (lane >> 4) * 8;
+  const bf16* Kh = KV + kh * 16 * QLD;  // this warp's 16 keys of the chunk
+  const bf16* Kl = Kh + TILE;
+  const bf16* Vh = Kl + TILE;
+  const bf16* Vl = Vh + TILE;
 
   int it = 0;
   for (int c = rank; c < n_chunks; c += CL, ++it) {
-    const int kbase = c * 64;
-    const int cur = it & 1;
-    // prefetch the next chunk into the other stage, then wait for this one
-    if (c + CL < n_chunks) load_chunk(kh, kl, vh, vl, c + CL, maxlim, cur ^ 1);
+    const int kbase = c * AC + kh * 16;
+    if (it > 0 || !pre) load_chunk(k_h, k_l, v_h, v_l, c, maxlim);
     cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<0>();
     __syncthreads();
-    const bf16* Kh = KV + cur * 4 * TILE;
-    const bf16* Kl = Kh + TILE;
-    const bf16* Vh = Kl + TILE;
-    const bf16* Vl = Vh + TILE;
-    // S = Q K^T for this warp's 16 rows and the chunk's 64 keys
-    float sacc[8][4];
+    // S = Q K^T for this warp's 16 rows and 16 keys
+    float sacc[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       uint32_t ah[4], al[4];
-      const int qo = (warp * 16 + g) * QLD + ks * 16 + tq * 2;
+      const int qo = (mt * 16 + g) * QLD + ks * 16 + tq * 2;
       ah[0] = *reinterpret_cast<const uint32_t*>(Qh + qo);
       ah[1] = *reinterpret_cast<const uint32_t*>(Qh + qo + 8 * QLD);
       ah[2] = *reinterpret_cast<const uint32_t*>(Qh + qo + 8);
@@ -308,7 +344,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
       al[2] = *reinterpret_cast<const uint32_t*>(Ql + qo + 8);
       al[3] = *reinterpret_cast<const uint32_t*>(Ql + qo + 8 * QLD + 8);
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < 2; ++nt) {
         const int ko = (nt * 8 + g) * QLD + ks * 16 + tq * 2;
         uint32_t bh[2], bl[2];
         bh[0] = *reinterpret_cast<const uint32_t*>(Kh + ko);
@@ -320,10 +356,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
         mma16816(sacc[nt], ah, bh);
       }
     }
-    // mask, scale to log2 units, chunk row maxima
+    // mask, scale to log2 units, row maxima over the 16 keys
     float mc_lo = -INFINITY, mc_hi = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = kbase + nt * 8 + tq * 2 + e;
@@ -344,9 +380,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
     const float corr_lo = mn_lo == -INFINITY ? 1.f : (m_lo == -INFINITY ? 0.f : exp2f(m_lo - mn_lo));
     const float corr_hi = mn_hi == -INFINITY ? 1.f : (m_hi == -INFINITY ? 0.f : exp2f(m_hi - mn_hi));
     float ps_lo = 0.f, ps_hi = 0.f;
-    uint32_t pf[8][2];
+    uint32_t pf[2][2];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
       float p0 = sacc[nt][0] == -INFINITY ? 0.f : exp2f(sacc[nt][0] - mn_lo);
       float p1 = sacc[nt][1] == -INFINITY ? 0.f : exp2f(sacc[nt][1] - mn_lo);
       float p2 = sacc[nt][2] == -INFINITY ? 0.f : exp2f(sacc[nt][2] - mn_hi);
@@ -371,103 +407,175 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(128) attention_mma_
       oacc[dn][2] *= corr_hi; oacc[dn][3] *= corr_hi;
     }
     // O += P (V_hi + V_lo); B fragments of two d-tiles per ldmatrix.x4.trans
-    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int lcol = (lane >> 4) * 8;
+    uint32_t af[4] = {pf[0][0], pf[0][1], pf[1][0], pf[1][1]};
 #pragma unroll
-    for (int kt = 0; kt < 4; ++kt) {
-      uint32_t af[4] = {pf[2 * kt][0], pf[2 * kt][1], pf[2 * kt + 1][0], pf[2 * kt + 1][1]};
-#pragma unroll
-      for (int dn = 0; dn < D / 8; dn += 2) {
-        const int vo = (kt * 16 + lrow) * QLD + dn * 8 + lcol;
-        uint32_t bh[4], bl[4];
-        ldsm_x4_trans(bh, Vh + vo);
-        ldsm_x4_trans(bl, Vl + vo);
-        mma16816(oacc[dn], af, bl);
-        mma16816(oacc[dn], af, bh);
-        mma16816(oacc[dn + 1], af, bl + 2);
-        mma16816(oacc[dn + 1], af, bh + 2);
-      }
+    for (int dn = 0; dn < D / 8; dn += 2) {
+      const int vo = lrow * QLD + dn * 8 + lcol;
+      uint32_t bh[4], bl[4];
+      ldsm_x4_trans(bh, Vh + vo);
+      ldsm_x4_trans(bl, Vl + vo);
+      mma16816(oacc[dn], af, bl);
+      mma16816(oacc[dn], af, bh);
+      mma16816(oacc[dn + 1], af, bl + 2);
+      mma16816(oacc[dn + 1], af, bh + 2);
     }
     __syncthreads();
   }
   cp_async_wait<0>();
   __syncthreads();
-  // publish this CTA's partial (unnormalised output, max, sum)
+  // merge the two key halves of this CTA: half 0 + half 1, in that order
+  if (kh == 1) {
 #pragma unroll
-  for (int dn = 0; dn < D / 8; ++dn) {
-    Ob[r_lo * OLD + dn * 8 + tq * 2] = oacc[dn][0];
-    Ob[r_lo * OLD + dn * 8 + tq * 2 + 1] = oacc[dn][1];
-    Ob[r_hi * OLD + dn * 8 + tq * 2] = oacc[dn][2];
-    Ob[r_hi * OLD + dn * 8 + tq * 2 + 1] = oacc[dn][3];
-  }
-  if (tq == 0) {
-    Ms[r_lo] = m_lo; Ls[r_lo] = l_lo;
-    Ms[r_hi] = m_hi; Ls[r_hi] = l_hi;
-  }
-  cluster.sync();
-  // merge: CTA `rank` finalises rows rank, rank + CL, ... in cluster-rank order.
-  // All (max, sum) pairs of its rows are fetched at once, then each thread
-  // fetches every rank's partial of its (row, column) elements in one batch.
-  constexpr int RPC = QR / CL;               // rows finalised per CTA
-  float* wsm = reinterpret_cast<float*>(Qh);  // [RPC][CL] merge weights (Q tiles are dead)
-  float* isn = wsm + RPC * CL;                // [RPC] 1 / total sum
-  if (tid < RPC * CL) {
-    const int i = tid / CL, c = tid % CL;
-    const int r = rank + i * CL;
-    wsm[tid] = *cluster.map_shared_rank(Ms + r, c);
-    isn[RPC + tid] = *cluster.map_shared_rank(Ls + r, c);  // staged after the weights
+    for (int dn = 0; dn < D / 8; ++dn) {
+      Oh[r_lo * OLD + dn * 8 + tq * 2] = oacc[dn][0];
+      Oh[r_lo * OLD + dn * 8 + tq * 2 + 1] = oacc[dn][1];
+      Oh[r_hi * OLD + dn * 8 + tq * 2] = oacc[dn][2];
+      Oh[r_hi * OLD + dn * 8 + tq * 2 + 1] = oacc[dn][3];
+    }
+    if (tq == 0) {
+      Mh[r_lo] = m_lo; Lh[r_lo] = l_lo;
+      Mh[r_hi] = m_hi; Lh[r_hi] = l_hi;
+    }
   }
   __syncthreads();
+  if (kh == 0) {
+    const float m1_lo = Mh[r_lo], m1_hi = Mh[r_hi];
+    const float M_lo = fmaxf(m_lo, m1_lo), M_hi = fmaxf(m_hi, m1_hi);
+    const float w0_lo = m_lo == -INFINITY ? 0.f : exp2f(m_lo - M_lo);
+    const float w1_lo = m1_lo == -INFINITY ? 0.f : exp2f(m1_lo - M_lo);
+    const float w0_hi = m_hi == -INFINITY ? 0.f : exp2f(m_hi - M_hi);
+    const float w1_hi = m1_hi == -INFINITY ? 0.f : exp2f(m1_hi - M_hi);
+    const float L_lo = w0_lo * l_lo + w1_lo * Lh[r_lo];
+    const float L_hi = w0_hi * l_hi + w1_hi * Lh[r_hi];
+    // stage this CTA's partial rows by owner: row r -> rank r % CL, slot r / CL
+    float* st_lo = ST + ((r_lo % CL) * RPC + r_lo / CL) * RLD;
+    float* st_hi = ST + ((r_hi % CL) * RPC + r_hi / CL) * RLD;
+    float o1[D / 8][4];
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      const int col = dn * 8 + tq * 2;
+      o1[dn][0] = Oh[r_lo * OLD + col];
+      o1[dn][1] = Oh[r_lo * OLD + col + 1];
+      o1[dn][2] = Oh[r_hi * OLD + col];
+      o1[dn][3] = Oh[r_hi * OLD + col + 1];
+    }
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      const int col = dn * 8 + tq * 2;
+      st_lo[col] = w0_lo * oacc[dn][0] + w1_lo * o1[dn][0];
+      st_lo[col + 1] = w0_lo * oacc[dn][1] + w1_lo * o1[dn][1];
+      st_hi[col] = w0_hi * oacc[dn][2] + w1_hi * o1[dn][2];
+      st_hi[col + 1] = w0_hi * oacc[dn][3] + w1_hi * o1[dn][3];
+    }
+    if (tq == 0) {
+      st_lo[D] = M_lo; st_lo[D + 1] = L_lo;
+      st_hi[D] = M_hi; st_hi[D + 1] = L_hi;
+    }
+  }
+  tc::fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    // one bulk copy per owner: this CTA's rows of that owner -> its RX[rank]
+    for (int r = 0; r < CL; ++r)
+      tc::bulk_s2s(tc::mapa(tc::smem_u32(RX + (size_t)rank * RPC * RLD), r), ST + (size_t)r * RPC * RLD,
+                   (uint32_t)(RPC * RLD * 4), tc::mapa(tc::smem_u32(&rxbar), r));
+    tc::bulk_commit();
+  }
+  const bool rx_ok = tc::mbar_wait(&rxbar, 0);
+  // owner: rows rank + i * CL, partials of ranks 0 .. CL-1 added in rank order
   if (tid < RPC) {
     float M = -INFINITY;
-    for (int c = 0; c < CL; ++c) M = fmaxf(M, wsm[tid * CL + c]);
+    for (int c = 0; c < CL; ++c) M = fmaxf(M, RX[(c * RPC + tid) * RLD + D]);
     float L = 0.f;
     for (int c = 0; c < CL; ++c) {
-      const float m = wsm[tid * CL + c];
+      const float m = RX[(c * RPC + tid) * RLD + D];
       const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-      L += w * isn[RPC + tid * CL + c];
-      wsm[tid * CL + c] = w;
+      WS[tid * CL + c] = w;
+      L += w * RX[(c * RPC + tid) * RLD + D + 1];
     }
-    isn[tid] = L > 0.f ? 1.f / L : 0.f;
+    IL[tid] = L > 0.f ? 1.f / L : 0.f;
   }
   __syncthreads();
-  constexpr int PER = RPC * D / 128;  // (row, column) elements per thread
-  float pv[PER][CL];
+  if (rx_ok) {
+    for (int x = tid; x < RPC * D; x += 256) {
+      const int i = x / D, d = x % D;
+      const int gi = qr0 + rank + i * CL;
+      if (gi >= nq) continue;
+      float acc = 0.f;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const int x = tid + e * 128, i = x / D, d = x % D;
-    const int r = rank + i * CL;
-#pragma unroll
-    for (int c = 0; c < CL; ++c) pv[e][c] = *cluster.map_shared_rank(Ob + r * OLD + d, c);
+      for (int c = 0; c < CL; ++c) acc += WS[i * CL + c] * RX[(c * RPC + i) * RLD + d];
+      const int t = row0 + gi / G, hq = kvh * G + gi % G;
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, ((size_t)t * a.Hq + hq) * D + d, acc * IL[i]);
+    }
   }
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    const int x = tid + e * 128, i = x / D, d = x % D;
-    const int gi = qr0 + rank + i * CL;
-    if (gi >= nq) continue;
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < CL; ++c) acc += wsm[i * CL + c] * pv[e][c];
-    const int t = row0 + gi / G, hq = kvh * G + gi % G;
-    put_plane(a.o_hi, a.o_lo, a.out_bf16, ((size_t)t * a.Hq + hq) * D + d, acc * isn[i]);
+  if (tid == 0) tc::bulk_wait_read();  // the copies have read this CTA's staged rows
+}
+
+template <int D, int CL>
+static size_t attn_mma_smem() {
+  constexpr int QLD = D + 8, RPC = QR / CL, RLD = D + 4;
+  return (size_t)(2 * QR * QLD + 4 * AC * QLD) * 2 + ((size_t)CL * RPC * RLD + RPC * CL + RPC) * 4 + QR * 4;
+}
+
+template <int D, int CL>
+static cudaError_t launch_attn_cl(const AttnArgs& a, dim3 grid, cudaStream_t s, bool pdl) {
+  const size_t smem = attn_mma_smem<D, CL>();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, attention_mma_kernel<D, CL>, a);
+}
+
+// Cluster width: 16 CTAs when the device schedules such clusters, else 8.
+template <int D>
+static int attn_cluster_width() {
+  static int width = 0;
+  if (width) return width;
+  width = 8;
+  const size_t smem16 = attn_mma_smem<D, 16>();
+  if (cudaFuncSetAttribute(attention_mma_kernel<D, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+          cudaSuccess &&
+      cudaFuncSetAttribute(attention_mma_kernel<D, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem16) ==
+          cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(16, 1, 1);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem16;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 16;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attention_mma_kernel<D, 16>, &cfg) == cudaSuccess && n >= 4) width = 16;
   }
-  cluster.sync();
+  cudaGetLastError();
+  if (width == 8)
+    cudaFuncSetAttribute(attention_mma_kernel<D, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)attn_mma_smem<D, 8>());
+  return width;
 }
 
 template <int D>
 static bool launch_attn_mma(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
   const int G = a.Hq / a.Hkv;
   const int n_rg = (max_rows * G + QR - 1) / QR;
-  constexpr int QLD = D + 8;
-  const size_t smem = (size_t)(2 * QR * QLD + 8 * 64 * QLD) * 2 + QR * 12;
-  static bool init = false;
-  if (!init) {
-    if (cudaFuncSetAttribute(attention_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return false;
-    init = true;
-  }
-  return launch_k(attention_mma_kernel<D>, dim3(CL, a.Hkv * n_rg, n_slots), dim3(128), smem, s, pdl, a) ==
+  const int cl = attn_cluster_width<D>();
+  const dim3 grid(cl, a.Hkv * n_rg, n_slots);
+  return (cl == 16 ? launch_attn_cl<D, 16>(a, grid, s, pdl) : launch_attn_cl<D, 8>(a, grid, s, pdl)) ==
          cudaSuccess;
 }
 

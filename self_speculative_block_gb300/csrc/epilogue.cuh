@@ -39,6 +39,19 @@ __device__ __forceinline__ void put_plane(void* hi, void* lo, int bf, size_t idx
   }
 }
 
+// rstd of one row from its per-128-column sums of squares, added in column order.
+__device__ __forceinline__ float row_rstd(const EpiArgs& e, int row) {
+  const float* p = e.ssq_in + (size_t)row * e.n_ssq;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = i < e.n_ssq ? p[i] : 0.f;
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i < e.n_ssq) s += v[i];
+  return rsqrtf(s / (float)e.norm_H + e.eps);
+}
+
 // Shared scratch of one epilogue call, in floats.
 constexpr int EPI_GROUP = 32;                 // tokens per epilogue pass
 constexpr int EPI_MAX_SSQ = 32;               // hidden <= 4096
@@ -46,40 +59,46 @@ constexpr int EPI_SCRATCH_FLOATS = EPI_GROUP + EPI_GROUP * EPI_MAX_SSQ + EPI_GRO
 
 // Epilogue of tokens t0 .. t0+tn-1.  Every pass first issues all of its
 // global loads (sums of squares, residual rows) into shared memory, so a pass
-// costs one memory round trip rather than one per token.
+// costs one memory round trip rather than one per token.  rs_in (row scales
+// of tokens t0 .. t0+tn-1) and rr_in (residual rows of tokens t0 .. t0+tn-1
+// for this tile, tn <= EPI_GROUP) may be supplied already loaded.
 __device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0, int tn,
-                                      float* scratch) {
+                                      float* scratch, const float* rs_in = nullptr, const float* rr_in = nullptr) {
   const EpiArgs& e = a.e;
   const int n0 = tile * NTILE;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
-  float* rs = scratch;                                   // [EPI_GROUP] row scales
-  float* sq = rs + EPI_GROUP;                            // [EPI_GROUP][n_ssq]
-  float* rr = sq + EPI_GROUP * EPI_MAX_SSQ;              // [EPI_GROUP][NTILE] residual rows
+  float* rs_s = scratch;                                 // [EPI_GROUP] row scales
+  float* sq = rs_s + EPI_GROUP;                          // [EPI_GROUP][n_ssq]
+  float* rr_s = sq + EPI_GROUP * EPI_MAX_SSQ;            // [EPI_GROUP][NTILE] residual rows
   for (int g0 = 0; g0 < tn; g0 += EPI_GROUP) {
     const int gn = min(EPI_GROUP, tn - g0);
     const bool norm = e.ssq_in != nullptr;
     const bool resid = a.epi == EPI_RESID;
-    if (norm)
+    const bool load_rs = norm && !rs_in;
+    const bool load_rr = resid && !rr_in;
+    if (load_rs)
       for (int x = tid; x < gn * e.n_ssq; x += blockDim.x) {
         const int tl = x / e.n_ssq, i = x % e.n_ssq;
         const int row = e.in_rows ? e.in_rows[t0 + g0 + tl] : t0 + g0 + tl;
         sq[tl * e.n_ssq + i] = e.ssq_in[(size_t)row * e.n_ssq + i];
       }
-    if (resid)
+    if (load_rr)
       for (int x = tid; x < gn * NTILE; x += blockDim.x) {
         const int tl = x / NTILE, c = x % NTILE;
-        rr[x] = e.resid[(size_t)(t0 + g0 + tl) * e.H + n0 + c];
+        rr_s[x] = e.resid[(size_t)(t0 + g0 + tl) * e.H + n0 + c];
       }
-    if (norm || resid) __syncthreads();
-    if (norm) {
+    if (load_rs || load_rr) __syncthreads();
+    if (load_rs) {
       // rstd = 1 / sqrt(mean(x^2) + eps), partial sums added in column order
       for (int tl = tid; tl < gn; tl += blockDim.x) {
         float ssum = 0.f;
         for (int i = 0; i < e.n_ssq; ++i) ssum += sq[tl * e.n_ssq + i];
-        rs[tl] = rsqrtf(ssum / (float)e.norm_H + e.eps);
+        rs_s[tl] = rsqrtf(ssum / (float)e.norm_H + e.eps);
       }
       __syncthreads();
     }
+    const float* rs = rs_in ? rs_in + g0 : rs_s;
+    const float* rr = rr_in ? rr_in + (size_t)g0 * NTILE : rr_s;
     for (int tl = warp; tl < gn; tl += nwarp) {
       const int t = t0 + g0 + tl;
       const float r = norm ? rs[tl] : 1.f;

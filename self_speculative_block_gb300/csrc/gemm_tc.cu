@@ -35,11 +35,13 @@ namespace {
 constexpr int TC_THREADS = 128;
 constexpr int TZ_TC = 128;       // tokens per CTA (two planes: MMA N <= 256)
 constexpr int EG = 32;           // tokens per cluster-reduce group
-constexpr int YLD = NTILE + 1;   // fp32 row stride of the partial tiles
+constexpr int YLD = NTILE + 4;   // fp32 row stride of the partial tiles (16-byte multiple)
 constexpr int A_BYTES = NTILE * 64 * 2;  // 128 x 64 bf16
 constexpr int SMEM_CAP = 200 * 1024;
 constexpr int DECODE_STAGE_CAP = 3;      // decode shapes: keep two CTAs per SM
-constexpr int TAIL_BYTES = 16 * 8 + 64;  // barriers, TMEM holder
+// outside the ring: row scales of the z-slice, residual rows of the first
+// epilogue group, barriers, TMEM holder
+constexpr int TAIL_BYTES = TZ_TC * 4 + EG * NTILE * 4 + 16 * 8 + 64;
 constexpr int L2_PREFETCH_BLOCKS = 8;    // weight tiles a CTA brings into L2 ahead of its ring
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -82,52 +84,32 @@ bool tmap_2d(CUtensorMap* out, const void* ptr, int rows, int cols, int box_rows
 __host__ __device__ inline int cdiv_i(int a, int b) { return (a + b - 1) / b; }
 }  // namespace
 
-// Ys[j][row] = sum over the S cluster ranks (in rank order) of their partial
-// tiles' token g0 + j: every rank's values of up to 32 / S tokens are in flight
-// at once.
-template <int S>
-__device__ __forceinline__ void gather_splits(cooperative_groups::cluster_group& cluster, float* Yp, float* Ys,
-                                              int g0, int cnt, int row) {
-  constexpr int TB = 32 / S;
-  for (int jb = 0; jb < cnt; jb += TB) {
-    float pv[TB][S];
-#pragma unroll
-    for (int jj = 0; jj < TB; ++jj)
-#pragma unroll
-      for (int sp = 0; sp < S; ++sp)
-        pv[jj][sp] = jb + jj < cnt ? *cluster.map_shared_rank(Yp + (g0 + jb + jj) * YLD + row, sp) : 0.f;
-#pragma unroll
-    for (int jj = 0; jj < TB; ++jj) {
-      float acc = pv[jj][0];
-#pragma unroll
-      for (int sp = 1; sp < S; ++sp) acc += pv[jj][sp];
-      if (jb + jj < cnt) Ys[(jb + jj) * YLD + row] = acc;
-    }
-  }
-}
-
 // ring_bytes >= stages * (A tile + B tile) and >= the partial tile + reduce buffer.
 __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw,
                                                             const __grid_constant__ CUtensorMap tmx_hi,
                                                             const __grid_constant__ CUtensorMap tmx_lo,
                                                             GemmArgs a, int nt, int two, int stages,
-                                                            int ring_bytes) {
+                                                            int ring_bytes, int per) {
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int b_bytes = (two ? 2 : 1) * nt * 128;
   uint8_t* sA = smem;
   uint8_t* sB = sA + stages * A_BYTES;
-  // after the MMAs the ring is free: the partial tile, the reduce buffer and
-  // the epilogue scratch live there
+  // after the MMAs the ring is free: the partial tile, the partial rows the
+  // cluster peers send, the reduced rows and the epilogue scratch live there
   float* Yp = reinterpret_cast<float*>(smem);             // [nt][YLD]
-  float* Ys = Yp + nt * YLD;                               // [EG][YLD]
+  float* RX = Yp + nt * YLD;                               // [S][per][YLD] peers' partial rows
+  float* Ys = RX + (size_t)gridDim.y * per * YLD;          // [EG][YLD]
   float* scratch = Ys + EG * YLD;                          // epilogue scratch
   uint8_t* tail = smem + ring_bytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(tail);
+  float* rs_all = reinterpret_cast<float*>(tail);          // [TZ_TC] rstd of the slice's tokens
+  float* rr_pre = rs_all + TZ_TC;                          // [EG][NTILE] residual rows
+  uint64_t* full = reinterpret_cast<uint64_t*>(rr_pre + EG * NTILE);
   uint64_t* empty = full + stages;
   uint64_t* done = empty + stages;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* rxbar = done + 1;   // peers' partial rows landed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(rxbar + 1);
   __shared__ int s_fail;
   __shared__ int s_flag;
 
@@ -152,6 +134,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
       tc::mbar_init(&empty[s], 1);
     }
     tc::mbar_init(done, 1);
+    tc::mbar_init(rxbar, 1);
     tc::fence_mbar_init();
     s_fail = 0;
     tc::grid_dep_launch();
@@ -186,10 +169,8 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
         tc::tma_load_2d_hint(sA + s * A_BYTES, &tmw, kx, n0, &full[s], pol);
       }
       uint8_t* b = sB + s * b_bytes;
-      for (int g = 0; g < nt / 16; ++g) tc::tma_load_2d(b + g * 2048, &tmx_hi, kx, t0 + 16 * g, &full[s]);
-      if (two)
-        for (int g = 0; g < nt / 16; ++g)
-          tc::tma_load_2d(b + (nt / 16 + g) * 2048, &tmx_lo, kx, t0 + 16 * g, &full[s]);
+      tc::tma_load_2d(b, &tmx_hi, kx, t0, &full[s]);
+      if (two) tc::tma_load_2d(b + nt * 128, &tmx_lo, kx, t0, &full[s]);
     }
   } else if (tid == 32) {
     // MMA issuer
@@ -211,6 +192,20 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   }
   __syncwarp();
   tc::grid_dep_wait();  // the epilogue reads and writes what earlier kernels touch
+  // epilogue token range of this CTA: the whole slice, or its share of the cluster
+  const int ea = S == 1 ? 0 : min(tn, split * per);
+  const int eb = S == 1 ? tn : min(tn, ea + per);
+  const int pre_n = min(EG, eb - ea);
+  if (warp >= 2) {
+    // warps 2 and 3 have no mainloop role: fetch the epilogue's inputs now
+    const int it = tid - 64;
+    if (a.e.ssq_in)
+      for (int tl = it; tl < tn; tl += 64)
+        rs_all[tl] = row_rstd(a.e, a.e.in_rows ? a.e.in_rows[t0 + tl] : t0 + tl);
+    if (a.epi == EPI_RESID)
+      for (int x = it; x < pre_n * NTILE; x += 64)
+        rr_pre[x] = a.e.resid[(size_t)(t0 + ea + x / NTILE) * a.e.H + n0 + x % NTILE];
+  }
   const bool ok_done = tc::mbar_wait(done, 0);
   tc::fence_after_sync();
   __syncthreads();
@@ -235,28 +230,51 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   if (warp == 0) tc::tmem_dealloc(tmem, ncols);
 
   if (S == 1) {
-    if (!failed) apply_epilogue(a, Yp, YLD, tile, t0, tn, scratch);
+    if (!failed) {
+      for (int g0 = 0; g0 < tn; g0 += EG) {
+        const int cnt = min(EG, tn - g0);
+        apply_epilogue(a, Yp + g0 * YLD, YLD, tile, t0 + g0, cnt, scratch, a.e.ssq_in ? rs_all + g0 : nullptr,
+                       g0 == 0 ? rr_pre : nullptr);
+      }
+    }
   } else {
+    // split-K reduction: every CTA sends the rows of each peer's token range
+    // to that peer with one bulk shared-memory copy; the owner adds the
+    // partials in rank order
     cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
     const int rank = (int)cluster.block_rank();
-    const int per = cdiv_i(tn, S);
     const int ta = min(tn, rank * per), tb = min(tn, ta + per);
+    if (tid == 0) tc::mbar_expect_tx(rxbar, (uint32_t)((S - 1) * (tb - ta) * YLD * 4));
+    tc::fence_proxy_async_smem();
+    cluster.sync();  // every partial tile is written and every receive barrier armed
+    if (tid == 0) {
+      for (int r = 0; r < S; ++r) {
+        const int ra = min(tn, r * per), rb = min(tn, ra + per);
+        if (r == rank || rb <= ra) continue;
+        tc::bulk_s2s(tc::mapa(tc::smem_u32(RX + (size_t)rank * per * YLD), r), Yp + (size_t)ra * YLD,
+                     (uint32_t)((rb - ra) * YLD * 4), tc::mapa(tc::smem_u32(rxbar), r));
+      }
+      tc::bulk_commit();
+    }
+    const bool rx_ok = tc::mbar_wait(rxbar, 0);
+    if (!rx_ok && tid == 0) set_err(a.e.err, DERR_TIMEOUT);
     for (int g0 = ta; g0 < tb; g0 += EG) {
       const int cnt = min(EG, tb - g0);
-      switch (S) {
-        case 2: gather_splits<2>(cluster, Yp, Ys, g0, cnt, row); break;
-        case 3: gather_splits<3>(cluster, Yp, Ys, g0, cnt, row); break;
-        case 4: gather_splits<4>(cluster, Yp, Ys, g0, cnt, row); break;
-        case 5: gather_splits<5>(cluster, Yp, Ys, g0, cnt, row); break;
-        case 6: gather_splits<6>(cluster, Yp, Ys, g0, cnt, row); break;
-        case 7: gather_splits<7>(cluster, Yp, Ys, g0, cnt, row); break;
-        default: gather_splits<8>(cluster, Yp, Ys, g0, cnt, row); break;
+      for (int j = 0; j < cnt; ++j) {
+        float acc = 0.f;
+        for (int sp = 0; sp < S; ++sp) {
+          const float v = sp == rank ? Yp[(size_t)(g0 + j) * YLD + row]
+                                     : RX[((size_t)sp * per + (g0 - ta) + j) * YLD + row];
+          acc = sp == 0 ? v : acc + v;
+        }
+        Ys[j * YLD + row] = acc;
       }
       __syncthreads();
-      if (!failed) apply_epilogue(a, Ys, YLD, tile, t0 + g0, cnt, scratch);
+      if (!failed && rx_ok)
+        apply_epilogue(a, Ys, YLD, tile, t0 + g0, cnt, scratch, a.e.ssq_in ? rs_all + g0 : nullptr,
+                       g0 == ta ? rr_pre : nullptr);
     }
-    cluster.sync();  // peers finished reading this CTA's partial tile
+    if (tid == 0) tc::bulk_wait_read();  // the copies have read this CTA's partial tile
   }
   if (a.epi == EPI_ARGMAX && !failed) argmax_grid_finish(a, &s_flag);
 }
@@ -265,17 +283,18 @@ bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (a.splits < 1 || a.splits > 8) return false;
   CUtensorMap tmw, tmh, tml;
   if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE)) return false;
-  if (!tmap_2d(&tmh, a.x, a.T, a.K, 16)) return false;
+  const int nt = ((a.T < TZ_TC ? a.T : TZ_TC) + 15) / 16 * 16;
+  if (!tmap_2d(&tmh, a.x, a.T, a.K, nt)) return false;
   const int two = a.x_lo != nullptr;
   if (two) {
-    if (!tmap_2d(&tml, a.x_lo, a.T, a.K, 16)) return false;
+    if (!tmap_2d(&tml, a.x_lo, a.T, a.K, nt)) return false;
   } else {
     tml = tmh;
   }
-  const int nt = ((a.T < TZ_TC ? a.T : TZ_TC) + 15) / 16 * 16;
   const int nkb = cdiv_i(a.kchunk, 64);
   const int stage_bytes = A_BYTES + (two ? 2 : 1) * nt * 128;
-  const int y_bytes = ((nt + EG) * YLD + EPI_SCRATCH_FLOATS) * 4;
+  const int per = cdiv_i(a.T < TZ_TC ? a.T : TZ_TC, a.splits);  // tokens each cluster rank reduces
+  const int y_bytes = ((nt + a.splits * per + EG) * YLD + EPI_SCRATCH_FLOATS) * 4;
   int stages = (SMEM_CAP - 1024 - TAIL_BYTES) / stage_bytes;
   if (stages > 6) stages = 6;
   if (a.T <= 2 * 64 + 1 && stages > DECODE_STAGE_CAP) stages = DECODE_STAGE_CAP;
@@ -311,7 +330,7 @@ bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmw, tmh, tml, a, nt, two, stages, ring) == cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmw, tmh, tml, a, nt, two, stages, ring, per) == cudaSuccess;
 }
 
 }  // namespace gocr

@@ -204,9 +204,11 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
     at.req_stride = h->req_stride;
     at.o_hi = h->at_hi; at.o_lo = h->at_lo; at.out_bf16 = h->dtype == GOCR_DTYPE_BF16;
     at.row_lim = h->rows.row_lim; at.plan = h->rows.plan;
-    if (kind != PLAN_PREFILL) {  // committed cache chunks may be fetched before the wait
-      at.slot_req = slot_tab; at.st = h->st;
-    }
+    // slot geometry is static for a forward; outside prefill (which rewrites the
+    // cache from position 0) committed cache chunks may be fetched before the wait
+    at.slot_req = slot_tab;
+    at.rows_per_slot = kind == PLAN_PREFILL ? P : T / n_slots;
+    if (kind != PLAN_PREFILL) at.st = h->st;
     at.T = T; at.Hq = c.n_q_heads; at.Hkv = c.n_kv_heads; at.d = c.head_dim; at.cap = h->cap;
     at.scale = 1.0f / sqrtf((float)c.head_dim);
     ok &= launch_attention(h->dtype, at, kind == PLAN_PREFILL ? 1 : n_slots,
