@@ -16,7 +16,7 @@ constexpr int KC = 32;       // K elements staged per step
 constexpr int TZ = 64;       // tokens per CTA (grid z slices)
 constexpr int THREADS = 256;
 constexpr int SM_COUNT = 152;  // fixed so the split rule is the same on every device
-constexpr int MAX_SPLITS = 8;  // split-K partials are reduced inside one cluster
+constexpr int MAX_SPLITS = 12;  // split-K partials are reduced inside one cluster (non-portable size)
 constexpr int YS_LD = NTILE + 1;
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }

@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
 }
 
 bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
-  if (a.splits < 1 || a.splits > 8) return false;
+  if (a.splits < 1 || a.splits > 16) return false;
   CUtensorMap tmw, tmh, tml;
   if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE)) return false;
   const int nt = ((a.T < TZ_TC ? a.T : TZ_TC) + 15) / 16 * 16;
@@ -308,6 +308,9 @@ bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
   static size_t configured = 0;
   if (smem > configured) {
     if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return false;
+    if (configured == 0 &&
+        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return false;
     configured = smem;
   }
