@@ -184,6 +184,32 @@ int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void*
                       const void* v_hi, const void* v_lo, float* o, const int32_t* lim, int T, int Hq, int Hkv,
                       int d, int cap, void* stream);
 
+/* ---- allocation-free GEMM ------------------------------------------------ */
+
+/* Bytes of the device scratch array behind gocr_op_linear_static (per GPU). */
+#define GOCR_STATIC_SCRATCH_BYTES (16u << 20)
+
+/* gocr_op_linear for callers that cannot allocate device memory: a plug-in
+ * whose host application owns every allocation, a real-time loop that may not
+ * enter the allocator, a sandbox that forbids cudaMalloc.  Same arguments,
+ * layouts and results as gocr_op_linear, but no workspace: the split-K partial
+ * sums and tile counters live in one file-scope device array of
+ * GOCR_STATIC_SCRATCH_BYTES that every GPU loading this library keeps until
+ * the process exits.  The paper has no counterpart: this is a deployment
+ * convenience of this library.
+ *   - Calls nothing that allocates (no cudaMalloc/cudaFree, no library
+ *     allocator): it clears the counters with cudaMemsetAsync and launches.
+ *   - GOCR_ECAPACITY when gocr_op_linear_workspace(T, N, K) exceeds
+ *     GOCR_STATIC_SCRATCH_BYTES (message in gocr_last_error(NULL)).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents: calls that overlap on the GPU (other streams, other threads)
+ *     race; order them on one stream. */
+int gocr_op_linear_static(int dtype, const void* x, const void* w, float* y, int T, int N, int K,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,6 +33,8 @@ struct GraphEntry {
 
 }  // namespace
 
+void gocr::set_lib_error(const char* msg) { g_lib_error = msg; }
+
 struct gocr_handle {
   gocr_config cfg{};
   int es = 4;  // element size of dtype

@@ -130,6 +130,9 @@ void launch_begin_decode(ReqState* st, const int* slot_req, int n_slots, const i
                          int max_rounds, int eos_id, cudaStream_t s);
 void launch_set_override(ReqState* st, int req, int n_ref, int n_sched, cudaStream_t s);
 
+// Library-level error message returned by gocr_last_error(NULL).
+void set_lib_error(const char* msg);
+
 // Launch helper: plain launch, or with the programmatic-dependent-launch attribute.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,

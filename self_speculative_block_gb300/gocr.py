@@ -31,7 +31,7 @@ LAYER_TENSORS = 9
 EXPORTS = ("gocr_create", "gocr_prefill", "gocr_decode", "gocr_decode_batch",
            "gocr_set_draft_override", "gocr_debug_forward", "gocr_read_kv", "gocr_get_state",
            "gocr_last_error", "gocr_free", "gocr_op_linear_workspace", "gocr_op_linear",
-           "gocr_op_attention")
+           "gocr_op_attention", "gocr_op_linear_static")
 
 
 class GocrError(RuntimeError):
@@ -101,6 +101,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gocr_op_linear_workspace": (sz, [i32, i32, i32]),
         "gocr_op_linear": (i32, [i32, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
         "gocr_op_attention": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
+        "gocr_op_linear_static": (i32, [i32, vp, vp, vp, i32, i32, i32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -308,6 +309,19 @@ def op_linear(x, w, workspace=None):
     stream = torch.cuda.current_stream(x.device).cuda_stream
     _check(lib.gocr_op_linear(_dt(x), x.data_ptr(), w.data_ptr(), y.data_ptr(), T, N, K,
                               workspace.data_ptr(), workspace.numel(), stream))
+    return y
+
+
+def op_linear_static(x, w):
+    """op_linear without a workspace: the library's static device scratch array
+    (for callers that cannot allocate device memory)."""
+    torch = _torch()
+    lib = load()
+    T, K = x.shape
+    N = w.shape[0]
+    y = torch.empty((T, N), dtype=torch.float32, device=x.device)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    _check(lib.gocr_op_linear_static(_dt(x), x.data_ptr(), w.data_ptr(), y.data_ptr(), T, N, K, stream))
     return y
 
 
