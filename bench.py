@@ -202,23 +202,64 @@ def main():
     torch.cuda.set_device(dev)
     cfg = wl.model
     W = synth.make_weights(cfg)
-    prefix = synth.make_prefix(cfg, wl.prefix_len)
-    prefix_bits = np.ascontiguousarray(synth.bf16_bits(prefix) if cfg.dtype == synth.BF16 else prefix)
+    hbm, peak_kind = peaks()
     B = wl.block
-    max_ctx = wl.prefix_len + wl.max_new + B + 8
-    dec = gocr.Decoder(cfg, W, max_ctx=max_ctx, max_block=B, device=str(dev))
-    del W
-    prefix_dev = torch.from_numpy(prefix_bits.view(np.int16) if cfg.dtype == synth.BF16 else prefix_bits).to(dev)
+    kind = args.workload
+    if kind == "batch":
+        prefix_lens, new_lens = synth.batch_lengths(wl.n_requests)
+        max_ctx = max(prefix_lens) + max(new_lens) + B + 8
+        n_req = wl.n_requests
+    elif kind == "sweep":
+        max_ctx = wl.prefix_len + wl.max_new + max(synth.SWEEP_BLOCKS) + 8
+        prefix_lens, new_lens, n_req = [wl.prefix_len], [wl.max_new], 1
+    else:
+        max_ctx = wl.prefix_len + wl.max_new + B + 8
+        prefix_lens, new_lens, n_req = [wl.prefix_len], [wl.max_new], 1
+    dec = gocr.Decoder(cfg, W, max_ctx=max_ctx, max_block=max(B, max(synth.SWEEP_BLOCKS) if kind == "sweep" else B),
+                       max_requests=n_req, device=str(dev))
+    prefixes = []
+    for r in range(n_req):
+        seed = synth.REQUEST_PREFIX_SEED0 + r if kind == "batch" else synth.PREFIX_SEED
+        pb = synth.make_prefix(cfg, prefix_lens[r], seed=seed)
+        bits = np.ascontiguousarray(synth.bf16_bits(pb) if cfg.dtype == synth.BF16 else pb)
+        prefixes.append((bits, torch.from_numpy(bits.view(np.int16) if cfg.dtype == synth.BF16 else bits).to(dev)))
+    refs = []
     if wl.forced_mean is not None:
-        dec.prefill(0, prefix_dev)
-        ref, _ = dec.decode(0, gocr.MODE_AR, 0, wl.max_new)
-        sched = synth.accept_schedule(wl.forced_mean, wl.max_new)
-        dec.set_draft_override(0, ref, sched)
+        # the AR-greedy continuation each forced draft copies (setup, not timed)
+        for r in range(n_req):
+            dec.prefill(r, prefixes[r][1])
+            ref, _ = dec.decode(r, gocr.MODE_AR, 0, new_lens[r])
+            refs.append(ref)
 
-    def step():
-        dec.prefill(0, prefix_dev)
-        out, st = dec.decode(0, gocr.MODE_SELFSPEC, B, wl.max_new)
-        return out, st
+    def arm(mean, seed_off=0):
+        for r in range(n_req):
+            dec.set_draft_override(r, refs[r], synth.accept_schedule(mean, new_lens[r], seed=synth.SCHEDULE_SEED + r + seed_off))
+
+    def step(Bv=B):
+        for r in range(n_req):
+            dec.prefill(r, prefixes[r][1])
+        if n_req == 1:
+            out, st = dec.decode(0, gocr.MODE_SELFSPEC, Bv, new_lens[0])
+            return st["device_ms"], st["committed"], st["rounds"]
+        outs, sts = dec.decode_batch(list(range(n_req)), gocr.MODE_SELFSPEC, Bv, new_lens)
+        return sts[0]["device_ms"], sum(x["committed"] for x in sts), max(x["rounds"] for x in sts)
+
+    sweep = None
+    if kind == "sweep":
+        sweep = []
+        for Bv in synth.SWEEP_BLOCKS:
+            for mean in synth.SWEEP_MEANS:
+                arm(mean)
+                for _ in range(2):
+                    step(Bv)
+                ms_l, tok_l, rd_l = [], 0, 0
+                for _ in range(3):
+                    ms, tk, rd = step(Bv)
+                    ms_l.append(ms); tok_l += tk; rd_l += rd
+                sweep.append({"B": Bv, "mean_accepted": mean, "round_us": 1e3 * sum(ms_l) / rd_l,
+                              "tokens_per_s": tok_l / (sum(ms_l) / 1e3), "tpf": tok_l / (2 * rd_l)})
+    if wl.forced_mean is not None:
+        arm(wl.forced_mean)
 
     for _ in range(args.warmup):
         step()
@@ -228,10 +269,10 @@ def main():
     dev_ms, tokens, rounds = [], 0, 0
     with ClockSampler(local) as clk:
         for _ in range(args.steps):
-            out, st = step()
-            dev_ms.append(st["device_ms"])
-            tokens += st["committed"]
-            rounds += st["rounds"]
+            ms, tk, rd = step()
+            dev_ms.append(ms)
+            tokens += tk
+            rounds += rd
     torch.cuda.synchronize()
     total_s = sum(dev_ms) / 1e3
     if world > 1:
@@ -243,45 +284,54 @@ def main():
     value = tokens / total_s
     ms_per_step = sum(dev_ms) / len(dev_ms)
     round_us = 1e3 * sum(dev_ms) / rounds
-    hbm, peak_kind = peaks()
     # round roofline: algorithmic bytes of an average round at the mean cache length
-    p_mid = wl.prefix_len + wl.max_new // 2
+    p_mid = int(np.mean(prefix_lens) + np.mean(new_lens) / 2)
     rb = round_bytes(cfg, p_mid, B)
+    if n_req > 1:  # weights once per forward, every request's KV
+        rb = 2 * cfg.weight_bytes_per_forward() + n_req * (round_bytes(cfg, p_mid, B) - 2 * cfg.weight_bytes_per_forward())
     round_frac = (rb / (hbm * 1e9)) / (round_us * 1e-6)
 
-    # dominant kernel: the gate/up GEMM of the draft/verify forwards, timed live on
-    # the stream it is launched on, sweeping all layers' weights (> L2) like a forward
-    kern = kernel_roofline(dec, cfg, B, hbm, dev)
+    # dominant kernel: the split-K GEMM on one forward's weight matrices, timed live
+    kern = kernel_roofline(dec, cfg, None, B, hbm, dev)
 
-    # end to end through the C ABI with host buffers: H2D prefix, prefill, decode, D2H tokens
-    pinned = torch.from_numpy(prefix_bits.view(np.int16) if cfg.dtype == synth.BF16 else prefix_bits).pin_memory()
+    # end to end through the C ABI with host buffers: H2D prefixes, prefill, decode, D2H tokens
+    pinned = [torch.from_numpy(b.view(np.int16) if cfg.dtype == synth.BF16 else b).pin_memory() for b, _ in prefixes]
     e2e_tok, e2e_s = 0, 0.0
     for _ in range(max(1, args.steps)):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        dec.prefill(0, pinned)
-        out, st = dec.decode(0, gocr.MODE_SELFSPEC, B, wl.max_new)
+        for r in range(n_req):
+            dec.prefill(r, pinned[r])
+        if n_req == 1:
+            out, st = dec.decode(0, gocr.MODE_SELFSPEC, B, new_lens[0])
+            e2e_tok += st["committed"]
+        else:
+            outs, sts = dec.decode_batch(list(range(n_req)), gocr.MODE_SELFSPEC, B, new_lens)
+            e2e_tok += sum(x["committed"] for x in sts)
         e2e_s += time.perf_counter() - t0
-        e2e_tok += st["committed"]
-    h2d = int(prefix_bits.nbytes)
-    d2h = wl.max_new * 4
+    h2d = int(sum(b.nbytes for b, _ in prefixes))
+    d2h = int(sum(new_lens) * 4)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and n_req == 1:
         dec.close()
+        del W
         torch.cuda.empty_cache()
         cpu = OracleArm(wl).sample(seconds=args.cpu_seconds)
     launches = rounds * (2 * kernels_per_forward(cfg) + 4) + args.steps
     if rank == 0:
+        config = {"workload": wl.name, "prefix": prefix_lens if n_req > 1 else prefix_lens[0], "B": B,
+                  "max_new": new_lens if n_req > 1 else new_lens[0], "batch": n_req,
+                  "parallelism": "replicas" if world > 1 else "single-gpu",
+                  "l2": "inputs larger than L2 (1.0 GB of weights per forward)",
+                  "drafts": "natural" if wl.forced_mean is None else f"forced, geometric mean {wl.forced_mean}"}
         line = {
             "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if cfg.dtype == synth.BF16 else "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "prefix": wl.prefix_len, "B": B, "max_new": wl.max_new,
-                       "batch": 1, "parallelism": "replicas" if world > 1 else "single-gpu",
-                       "l2": "inputs larger than L2 (1.0 GB of weights per forward)",
-                       "drafts": "natural" if wl.forced_mean is None else f"forced mean {wl.forced_mean}"},
+            "config": config,
             "round_us": round_us, "rounds_per_step": rounds / args.steps,
+            "tpf": tokens / (2 * rounds),
             "round_roofline": {"bytes": rb, "peak_gbs": hbm, "frac": round_frac, "peak": peak_kind},
             "roofline": kern,
             "cpu_baseline": cpu,
@@ -290,41 +340,56 @@ def main():
             "gpu_launches": launches,
             "clocks": clk.summary(),
         }
+        if sweep is not None:
+            line["sweep"] = sweep
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def kernel_roofline(dec, cfg, B, hbm, dev):
-    """gate/up GEMM with the decode launch shape (B + 1 rows), all layers' packed
-    weights in turn so every launch streams from HBM; CUDA events on its stream."""
+def kernel_roofline(dec, cfg, W, B, hbm, dev):
+    """The split-K GEMM kernel on one forward's weight matrices (every layer's
+    QKV, O, gate/up and down shapes, then the LM head), with the decode launch
+    shape: B + 1 tokens, hi and lo planes stacked as 2 (B + 1) rows.  Timed with
+    CUDA events on the stream it is launched on; the matrices total ~1 GB, more
+    than L2, so every launch streams its weights from HBM."""
     import torch
     from self_speculative_block_gb300 import gocr
-    T, N, K = B + 1, 2 * cfg.ffn, cfg.hidden
     es = 2 if cfg.dtype == synth.BF16 else 4
     tdt = torch.bfloat16 if es == 2 else torch.float32
-    x = torch.randn(T, K, device=dev).to(tdt)
-    ws = [torch.randn(N, K, device=dev).to(tdt) for _ in range(8)]  # 8 x 25 MB > L2
-    need = dec.lib.gocr_op_linear_workspace(T, N, K)
+    T = 2 * (B + 1)
+    h, f = cfg.hidden, cfg.ffn
+    shapes = []
+    for _ in range(cfg.n_layers):
+        shapes += [(cfg.q_dim + 2 * cfg.kv_dim, h), (h, cfg.q_dim), (2 * f, h), (h, f)]
+    shapes.append((cfg.vocab, h))
+    ws = [torch.empty((n, k), dtype=tdt, device=dev).normal_(0, 0.02) for n, k in shapes]
+    xs = {k: torch.randn(T, k, device=dev).to(tdt) for k in {k for _, k in shapes}}
+    need = max(dec.lib.gocr_op_linear_workspace(T, n, k) for n, k in shapes)
     wk = torch.zeros(need, dtype=torch.uint8, device=dev)
-    for w in ws:
-        gocr.op_linear(x, w, wk)
+
+    def sweep():
+        for (n, k), w in zip(shapes, ws):
+            gocr.op_linear(xs[k], w, wk)
+
+    sweep()
     s = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 5
+    reps = 3
     torch.cuda.synchronize()
     e0.record(s)
     for _ in range(reps):
-        for w in ws:
-            gocr.op_linear(x, w, wk)
+        sweep()
     e1.record(s)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / (reps * len(ws))
-    alg = N * K * es + T * K * es + T * N * 4
+    ms = e0.elapsed_time(e1) / (reps * len(shapes))
+    alg = sum(n * k * es + T * k * es + T * n * 4 for n, k in shapes) / len(shapes)
     ach = alg / (ms * 1e-3) / 1e9
-    return {"kernel": "gemm (gate/up, split-K, fused SwiGLU epilogue in the decoder)", "bound": "hbm",
-            "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
-            "launch_us": ms * 1e3, "algorithmic_bytes": alg, "shape": [T, N, K]}
+    del ws
+    return {"kernel": "gemm_tc_kernel (tcgen05 split-K GEMM), one forward's 81 weight matrices",
+            "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+            "traffic": None, "launch_us": ms * 1e3, "algorithmic_bytes": alg, "rows": T,
+            "launches": len(shapes)}
 
 
 if __name__ == "__main__":

@@ -93,6 +93,11 @@ WORKLOADS: Dict[str, Workload] = {
     # table-region decode: 872 tokens (the pages' table mean), forced mean 9
     "table": Workload("table-region-bf16-0.5B-prefix2048-B32-new872-forced9", BASE, 2048, 32, 872,
                       forced_mean=9.0),
+    # block-size sweep: B in SWEEP_BLOCKS x forced means SWEEP_MEANS, 512 tokens (headline B=32, mean 9)
+    "sweep": Workload("block-sweep-bf16-0.5B-prefix2048-new512", BASE, 2048, 32, 512, forced_mean=9.0),
+    # page-level batch: 16 ragged requests, B=32, per-request forced mean 9
+    "batch": Workload("page-batch-bf16-0.5B-16req-ragged-B32-forced9", BASE, 0, 32, 0, forced_mean=9.0,
+                      n_requests=16),
 }
 SWEEP_BLOCKS = (8, 16, 32, 64)
 SWEEP_MEANS = (4.0, 9.0, 19.0)
