@@ -107,8 +107,13 @@ def round_bytes(cfg: synth.ModelConfig, p: int, B: int) -> int:
 
 
 def kernels_per_forward(cfg: synth.ModelConfig) -> int:
-    # embed + per layer (norm, qkv, attention, o, norm, gate/up, down) + final norm + LM head
-    return 1 + 7 * cfg.n_layers + 2
+    # embed + per layer (qkv, attention, o, gate/up, down) + LM head; RMSNorm is folded into the GEMMs
+    return 1 + 5 * cfg.n_layers + 1
+
+
+def kernels_per_round(cfg: synth.ModelConfig) -> int:
+    # plan, draft forward, override, plan, verify forward, accept
+    return 2 * kernels_per_forward(cfg) + 4
 
 
 # --------------------------------------------------------------------------- CPU oracle arm
@@ -116,26 +121,53 @@ def kernels_per_forward(cfg: synth.ModelConfig) -> int:
 class OracleArm:
     """The CPU oracle on a bounded sample of the workload: one untimed prefill,
     then each sample runs self-speculative rounds from a copy of that state
-    until ~`seconds` of round time or the end of the workload."""
+    until ~`seconds` of round time or the end of the workload.
 
-    def __init__(self, wl):
+    The 16-request page batch is sampled on its first request (the oracle
+    decodes requests one after another, so its rate is per request).  Forced
+    workloads first decode, untimed, an AR-greedy continuation of at most
+    `ref_seconds` of oracle time; the forced drafts copy it, and a sample stops
+    where it runs out."""
+
+    def __init__(self, wl, ref_seconds: float = 20.0):
         import oracle
         self.oracle = oracle
         self.wl = wl
         cfg = wl.model
+        if wl.n_requests > 1:
+            prefix_lens, new_lens = synth.batch_lengths(wl.n_requests)
+            self.P, self.max_new, seed = prefix_lens[0], new_lens[0], synth.REQUEST_PREFIX_SEED0
+        else:
+            self.P, self.max_new, seed = wl.prefix_len, wl.max_new, synth.PREFIX_SEED
         W = synth.make_weights(cfg)
         self.model = oracle.Model(W, cfg)
         del W
-        prefix = synth.make_prefix(cfg, wl.prefix_len).astype(np.float64)
+        prefix = synth.make_prefix(cfg, self.P, seed=seed).astype(np.float64)
         self.st0 = oracle.prefill(self.model, prefix)
+        self.ref, self.override = None, None
+        if wl.forced_mean is not None:
+            st = self._copy()
+            t0 = time.perf_counter()
+            while len(st.out) < self.max_new and time.perf_counter() - t0 < ref_seconds:
+                oracle.ar_step(self.model, st)
+            self.ref = list(st.out)
+            sched = synth.accept_schedule(wl.forced_mean, self.max_new, seed=synth.SCHEDULE_SEED)
+            self.override = oracle.forced_override(self.ref, sched, cfg.vocab)
+
+    def _copy(self):
+        s = self.st0
+        return self.oracle.State(list(s.cache_k), list(s.cache_v), s.x0, list(s.out))
 
     def sample(self, seconds: float):
         o, wl = self.oracle, self.wl
-        st = o.State(list(self.st0.cache_k), list(self.st0.cache_v), self.st0.x0, list(self.st0.out))
+        st = self._copy()
         committed, rounds, t_total = 0, 0, 0.0
-        while len(st.out) < wl.max_new and t_total < seconds:
+        while len(st.out) < self.max_new and t_total < seconds:
+            if self.ref is not None and len(self.ref) < self.max_new and len(st.out) + wl.block + 2 > len(self.ref):
+                break
             t0 = time.perf_counter()
-            log = o.selfspec_round(self.model, st, wl.block, wl.max_new)
+            log = o.selfspec_round(self.model, st, wl.block, self.max_new, override=self.override,
+                                   round_index=rounds)
             t_total += time.perf_counter() - t0
             committed += len(log.committed)
             rounds += 1
@@ -144,9 +176,11 @@ class OracleArm:
             cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [os.cpu_count() or 1])
         except Exception:
             cores = os.cpu_count() or 1
-        return {"value": committed / t_total, "unit": "tokens/s", "cores": int(cores), "kind": "oracle",
-                "sample": f"{rounds} self-speculative rounds (B={wl.block}, fp64 NumPy) after an untimed "
-                          f"{wl.prefix_len}-row prefill of {wl.name}; {committed} tokens in {t_total:.1f} s"}
+        what = "natural drafts" if self.ref is None else f"forced drafts, geometric mean {wl.forced_mean}"
+        req = f"request 0 ({self.P}-row prefix) of " if wl.n_requests > 1 else f"{self.P}-row prefill of "
+        return {"value": committed / max(t_total, 1e-9), "unit": "tokens/s", "cores": int(cores), "kind": "oracle",
+                "sample": f"{rounds} self-speculative rounds (B={wl.block}, fp64 NumPy, {what}) after an untimed "
+                          f"{req}{wl.name}; {committed} tokens in {t_total:.1f} s"}
 
 
 # --------------------------------------------------------------------------- main
@@ -171,22 +205,25 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        vals = []
-        samples = []
+        vals, secs, samples = [], [], []
         arm = OracleArm(wl)
         for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
             s = arm.sample(seconds=max(2.0, args.cpu_seconds / max(1, args.steps)))
             if i >= args.warmup:
                 vals.append(s["value"])
+                secs.append(time.perf_counter() - t0)
                 samples.append(s)
         v = statistics.median(vals)
         cb = dict(samples[-1])
         cb["value"] = v
-        line = {"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": 0,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": wl.name, "prefix": wl.prefix_len, "B": wl.block,
-                           "max_new": wl.max_new, "batch": 1},
+        config = {"workload": wl.name, "prefix": arm.P, "B": wl.block, "max_new": arm.max_new,
+                  "batch": 1, "parallelism": "host cores",
+                  "drafts": "natural" if wl.forced_mean is None else f"forced, geometric mean {wl.forced_mean}"}
+        line = {"impl": "reference", "metric": metric, "value": v, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
                 "cpu_baseline": cb, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                                             "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
@@ -292,7 +329,7 @@ def main():
     round_frac = (rb / (hbm * 1e9)) / (round_us * 1e-6)
 
     # dominant kernel: the split-K GEMM on one forward's weight matrices, timed live
-    kern = kernel_roofline(dec, cfg, None, B, hbm, dev)
+    kern = kernel_roofline(cfg, B, hbm, dev)
 
     # end to end through the C ABI with host buffers: H2D prefixes, prefill, decode, D2H tokens
     pinned = [torch.from_numpy(b.view(np.int16) if cfg.dtype == synth.BF16 else b).pin_memory() for b, _ in prefixes]
@@ -313,12 +350,12 @@ def main():
     d2h = int(sum(new_lens) * 4)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and n_req == 1:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dec.close()
         del W
         torch.cuda.empty_cache()
         cpu = OracleArm(wl).sample(seconds=args.cpu_seconds)
-    launches = rounds * (2 * kernels_per_forward(cfg) + 4) + args.steps
+    launches = rounds * kernels_per_round(cfg) + args.steps  # + one begin-decode kernel per call
     if rank == 0:
         config = {"workload": wl.name, "prefix": prefix_lens if n_req > 1 else prefix_lens[0], "B": B,
                   "max_new": new_lens if n_req > 1 else new_lens[0], "batch": n_req,
@@ -347,49 +384,62 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-def kernel_roofline(dec, cfg, W, B, hbm, dev):
-    """The split-K GEMM kernel on one forward's weight matrices (every layer's
-    QKV, O, gate/up and down shapes, then the LM head), with the decode launch
-    shape: B + 1 tokens, hi and lo planes stacked as 2 (B + 1) rows.  Timed with
-    CUDA events on the stream it is launched on; the matrices total ~1 GB, more
-    than L2, so every launch streams its weights from HBM."""
+GEMM_SOURCES = ("gemm_tc.cu", "gemm.cu", "epilogue.cuh", "tc.cuh", "kernels.cuh", "common.cuh")
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "gemm_tc_decode_sweep.md")
+
+
+def gemm_sources_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "self_speculative_block_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the GEMM sweep from the committed ncu summary,
+    or None when the kernel sources changed since that capture."""
+    try:
+        kv = dict(line.split(":", 1) for line in open(GEMM_PROFILE).read().splitlines()
+                  if line.startswith(("traffic_bytes_per_launch:", "gemm_sources_digest:")))
+    except (OSError, ValueError):
+        return None
+    if kv.get("gemm_sources_digest", "").strip() != gemm_sources_digest():
+        return None
+    return float(kv["traffic_bytes_per_launch"])
+
+
+def kernel_roofline(cfg, B, hbm, dev):
+    """The split-K GEMM kernel on one forward's 65 weight launches (every
+    layer's packed QKV, O, packed gate/up and down, then the LM head) at the
+    decode launch shape: B + 1 tokens, hi and lo planes stacked as 2 (B + 1)
+    rows.  Timed with CUDA events on the stream it is launched on; the
+    matrices total ~1 GB, more than L2, so every launch streams its weights
+    from HBM."""
     import torch
-    from self_speculative_block_gb300 import gocr
-    es = 2 if cfg.dtype == synth.BF16 else 4
-    tdt = torch.bfloat16 if es == 2 else torch.float32
-    T = 2 * (B + 1)
-    h, f = cfg.hidden, cfg.ffn
-    shapes = []
-    for _ in range(cfg.n_layers):
-        shapes += [(cfg.q_dim + 2 * cfg.kv_dim, h), (h, cfg.q_dim), (2 * f, h), (h, f)]
-    shapes.append((cfg.vocab, h))
-    ws = [torch.empty((n, k), dtype=tdt, device=dev).normal_(0, 0.02) for n, k in shapes]
-    xs = {k: torch.randn(T, k, device=dev).to(tdt) for k in {k for _, k in shapes}}
-    need = max(dec.lib.gocr_op_linear_workspace(T, n, k) for n, k in shapes)
-    wk = torch.zeros(need, dtype=torch.uint8, device=dev)
-
-    def sweep():
-        for (n, k), w in zip(shapes, ws):
-            gocr.op_linear(xs[k], w, wk)
-
-    sweep()
+    from self_speculative_block_gb300.profile_cases import GemmSweep
+    sw = GemmSweep(cfg, 2 * (B + 1), dev)
+    g = sw.graph()
+    g.replay()
     s = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 3
+    reps = 5
     torch.cuda.synchronize()
     e0.record(s)
     for _ in range(reps):
-        sweep()
+        g.replay()
     e1.record(s)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / (reps * len(shapes))
-    alg = sum(n * k * es + T * k * es + T * n * 4 for n, k in shapes) / len(shapes)
+    ms = e0.elapsed_time(e1) / (reps * len(sw.shapes))
+    alg = sw.algorithmic_bytes()
     ach = alg / (ms * 1e-3) / 1e9
-    del ws
-    return {"kernel": "gemm_tc_kernel (tcgen05 split-K GEMM), one forward's 81 weight matrices",
+    n = len(sw.shapes)
+    del sw
+    return {"kernel": f"gemm_tc_kernel (tcgen05 split-K GEMM), one forward's {n} weight launches",
             "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-            "traffic": None, "launch_us": ms * 1e3, "algorithmic_bytes": alg, "rows": T,
-            "launches": len(shapes)}
+            "traffic": profiled_traffic(), "launch_us": ms * 1e3, "algorithmic_bytes": alg,
+            "rows": 2 * (B + 1), "launches": n}
 
 
 if __name__ == "__main__":

@@ -537,12 +537,18 @@ static cudaError_t launch_attn_cl(const AttnArgs& a, dim3 grid, cudaStream_t s, 
   return cudaLaunchKernelEx(&cfg, attention_mma_kernel<D, CL>, a);
 }
 
-// Cluster width: 16 CTAs when the device schedules such clusters, else 8.
+// Cluster width: 16 CTAs when the device keeps the eight 16-CTA clusters of
+// a 33-row decode window (4 kv heads x 2 row groups) resident at once, else
+// 8.  The width fixes which rank reads which key chunk and the order of the
+// merge, so it is chosen once per process: every launch, AR or
+// self-speculative, adds the same partials in the same order.
 template <int D>
 static int attn_cluster_width() {
   static int width = 0;
   if (width) return width;
   width = 8;
+  prefer_shared(reinterpret_cast<const void*>(attention_mma_kernel<D, 16>));
+  prefer_shared(reinterpret_cast<const void*>(attention_mma_kernel<D, 8>));
   const size_t smem16 = attn_mma_smem<D, 16>();
   if (cudaFuncSetAttribute(attention_mma_kernel<D, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
           cudaSuccess &&
@@ -560,7 +566,7 @@ static int attn_cluster_width() {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attention_mma_kernel<D, 16>, &cfg) == cudaSuccess && n >= 4) width = 16;
+    if (cudaOccupancyMaxActiveClusters(&n, attention_mma_kernel<D, 16>, &cfg) == cudaSuccess && n >= 8) width = 16;
   }
   cudaGetLastError();
   if (width == 8)

@@ -57,23 +57,38 @@ constexpr int EPI_GROUP = 32;                 // tokens per epilogue pass
 constexpr int EPI_MAX_SSQ = 32;               // hidden <= 4096
 constexpr int EPI_SCRATCH_FLOATS = EPI_GROUP + EPI_GROUP * EPI_MAX_SSQ + EPI_GROUP * NTILE;
 
-// Epilogue of tokens t0 .. t0+tn-1.  Every pass first issues all of its
+// Epilogue inputs a GEMM kernel fetched ahead of time into shared memory,
+// for the tokens t0 .. t0+tn-1 of one epilogue call (tn <= EPI_GROUP); a null
+// pointer means "read it from global memory now".
+struct EpiPre {
+  const float* rs = nullptr;     // [tn] row scales
+  const float* rr = nullptr;     // [tn][NTILE] residual rows of this tile (RESID)
+  const float* gn = nullptr;     // [NTILE] next-norm gain of this tile's columns (RESID)
+  const int* pos = nullptr;      // [tn] row positions (QKV)
+  const int* req = nullptr;      // [tn] request of each row (QKV)
+  const float2* rope = nullptr;  // [tn][head_dim / 2] (cos, sin) at each row's position (QKV)
+};
+
+// Epilogue EPI of tokens t0 .. t0+tn-1.  Every pass first issues all of its
 // global loads (sums of squares, residual rows) into shared memory, so a pass
-// costs one memory round trip rather than one per token.  rs_in (row scales
-// of tokens t0 .. t0+tn-1) and rr_in (residual rows of tokens t0 .. t0+tn-1
-// for this tile, tn <= EPI_GROUP) may be supplied already loaded.
-__device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0, int tn,
-                                      float* scratch, const float* rs_in = nullptr, const float* rr_in = nullptr) {
+// costs one memory round trip rather than one per token; inputs in `pre`
+// (tn <= EPI_GROUP) are not fetched again.  The kind is a template argument
+// so that a kernel carries only its own epilogue code.
+template <int EPI>
+__device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0, int tn,
+                                        float* scratch, const EpiPre& pre = EpiPre()) {
   const EpiArgs& e = a.e;
   const int n0 = tile * NTILE;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   float* rs_s = scratch;                                 // [EPI_GROUP] row scales
   float* sq = rs_s + EPI_GROUP;                          // [EPI_GROUP][n_ssq]
   float* rr_s = sq + EPI_GROUP * EPI_MAX_SSQ;            // [EPI_GROUP][NTILE] residual rows
+  const float* rs_in = pre.rs;
+  const float* rr_in = pre.rr;
   for (int g0 = 0; g0 < tn; g0 += EPI_GROUP) {
     const int gn = min(EPI_GROUP, tn - g0);
     const bool norm = e.ssq_in != nullptr;
-    const bool resid = a.epi == EPI_RESID;
+    const bool resid = EPI == EPI_RESID;
     const bool load_rs = norm && !rs_in;
     const bool load_rr = resid && !rr_in;
     if (load_rs)
@@ -97,6 +112,7 @@ __device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys
       }
       __syncthreads();
     }
+    const bool first = g0 == 0;
     const float* rs = rs_in ? rs_in + g0 : rs_s;
     const float* rr = rr_in ? rr_in + (size_t)g0 * NTILE : rr_s;
     for (int tl = warp; tl < gn; tl += nwarp) {
@@ -106,7 +122,7 @@ __device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys
       float v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = yrow[lane + 32 * j] * r;
-      switch (a.epi) {
+      switch (EPI) {
         case EPI_STORE:
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -122,7 +138,7 @@ __device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys
             const float x = rr[tl * NTILE + c] + v[j];
             e.resid[(size_t)t * e.H + n] = x;
             ss = fmaf(x, x, ss);
-            put_plane(e.pl_hi, e.pl_lo, e.plane_bf16, (size_t)t * e.ld_pl + n, x * e.g_next[n]);
+            put_plane(e.pl_hi, e.pl_lo, e.plane_bf16, (size_t)t * e.ld_pl + n, x * (pre.gn ? pre.gn[c] : e.g_next[n]));
           }
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -140,20 +156,22 @@ __device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys
         }
         case EPI_QKV: {
           const int d = e.head_dim, half = d >> 1;
-          const int pos = e.row_pos[t];
+          const bool pq = first && pre.pos;
+          const int pos = pq ? pre.pos[tl] : e.row_pos[t];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int c = lane + 32 * j, n = n0 + c, jj = n % d;
             float out = v[j];
             if (n < e.q_dim + e.kv_dim) {  // q and k are rotated, v is not
-              const float2 cs = e.rope[(size_t)pos * half + (jj < half ? jj : jj - half)];
+              const int ri = jj < half ? jj : jj - half;
+              const float2 cs = (first && pre.rope) ? pre.rope[tl * half + ri] : e.rope[(size_t)pos * half + ri];
               const float partner = yrow[jj < half ? c + half : c - half] * r;
               out = jj < half ? (v[j] * cs.x - partner * cs.y) : (v[j] * cs.x + partner * cs.y);
             }
             if (n < e.q_dim) {
               put_plane(e.q_hi, e.q_lo, e.plane_bf16, (size_t)t * e.q_dim + n, out);
             } else {
-              const int req = e.plan->slot_req[e.row_slot[t]];
+              const int req = (first && pre.req) ? pre.req[tl] : e.plan->slot_req[e.row_slot[t]];
               if (pos < 0 || pos >= e.cap) { set_err(e.err, DERR_CAPACITY); continue; }
               const bool is_k = n < e.q_dim + e.kv_dim;
               const int nn = is_k ? n - e.q_dim : n - e.q_dim - e.kv_dim;
@@ -189,6 +207,18 @@ __device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys
       }
     }
     __syncthreads();
+  }
+}
+
+// Epilogue with the kind taken from the launch arguments.
+__device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0, int tn,
+                                      float* scratch) {
+  switch (a.epi) {
+    case EPI_STORE: apply_epilogue_k<EPI_STORE>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
+    case EPI_RESID: apply_epilogue_k<EPI_RESID>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
+    case EPI_QKV: apply_epilogue_k<EPI_QKV>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
+    case EPI_SWIGLU: apply_epilogue_k<EPI_SWIGLU>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
+    case EPI_ARGMAX: apply_epilogue_k<EPI_ARGMAX>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
   }
 }
 

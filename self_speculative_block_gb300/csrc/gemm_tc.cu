@@ -39,10 +39,12 @@ constexpr int YLD = NTILE + 4;   // fp32 row stride of the partial tiles (16-byt
 constexpr int A_BYTES = NTILE * 64 * 2;  // 128 x 64 bf16
 constexpr int SMEM_CAP = 200 * 1024;
 constexpr int DECODE_STAGE_CAP = 3;      // decode shapes: keep two CTAs per SM
-// outside the ring: row scales of the z-slice, residual rows of the first
-// epilogue group, barriers, TMEM holder
-constexpr int TAIL_BYTES = TZ_TC * 4 + EG * NTILE * 4 + 16 * 8 + 64;
+// outside the ring: row scales of the z-slice; the first epilogue group's
+// residual rows (RESID) or RoPE rows (QKV); the tile's next-norm gains; the
+// first group's positions and requests; barriers; TMEM holder
+constexpr int TAIL_BYTES = TZ_TC * 4 + EG * NTILE * 4 + NTILE * 4 + 2 * EG * 4 + 16 * 8 + 64;
 constexpr int L2_PREFETCH_BLOCKS = 8;    // weight tiles a CTA brings into L2 ahead of its ring
+constexpr int MAX_CLUSTER = 16;          // split-K ranks of one tile
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_mu;
@@ -85,6 +87,8 @@ __host__ __device__ inline int cdiv_i(int a, int b) { return (a + b - 1) / b; }
 }  // namespace
 
 // ring_bytes >= stages * (A tile + B tile) and >= the partial tile + reduce buffer.
+// EPI: the fused epilogue (a.epi), one instantiation per kind.
+template <int EPI>
 __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw,
                                                             const __grid_constant__ CUtensorMap tmx_hi,
                                                             const __grid_constant__ CUtensorMap tmx_lo,
@@ -92,7 +96,9 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
                                                             int ring_bytes, int per) {
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  // 1024-byte alignment for the 128-byte-swizzled tiles, by pointer arithmetic
+  // on the shared array so that the compiler keeps shared-memory addressing
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int b_bytes = (two ? 2 : 1) * nt * 128;
   uint8_t* sA = smem;
   uint8_t* sB = sA + stages * A_BYTES;
@@ -104,8 +110,12 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   float* scratch = Ys + EG * YLD;                          // epilogue scratch
   uint8_t* tail = smem + ring_bytes;
   float* rs_all = reinterpret_cast<float*>(tail);          // [TZ_TC] rstd of the slice's tokens
-  float* rr_pre = rs_all + TZ_TC;                          // [EG][NTILE] residual rows
-  uint64_t* full = reinterpret_cast<uint64_t*>(rr_pre + EG * NTILE);
+  float* rr_pre = rs_all + TZ_TC;                          // [EG][NTILE] residual rows, or
+  float2* rope_pre = reinterpret_cast<float2*>(rr_pre);    //   [EG][head_dim / 2] RoPE rows
+  float* gn_pre = rr_pre + EG * NTILE;                     // [NTILE] next-norm gains
+  int* pos_pre = reinterpret_cast<int*>(gn_pre + NTILE);   // [EG] row positions
+  int* req_pre = pos_pre + EG;                             // [EG] row requests
+  uint64_t* full = reinterpret_cast<uint64_t*>(req_pre + EG);
   uint64_t* empty = full + stages;
   uint64_t* done = empty + stages;
   uint64_t* rxbar = done + 1;   // peers' partial rows landed
@@ -191,20 +201,40 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     tc::mma_commit(done);
   }
   __syncwarp();
+  // the norm gains are weights: fetched before the dependency wait
+  if (EPI == EPI_RESID && warp >= 2)
+    for (int c = tid - 64; c < NTILE; c += 64) gn_pre[c] = n0 + c < a.e.H ? a.e.g_next[n0 + c] : 0.f;
   tc::grid_dep_wait();  // the epilogue reads and writes what earlier kernels touch
   // epilogue token range of this CTA: the whole slice, or its share of the cluster
   const int ea = S == 1 ? 0 : min(tn, split * per);
   const int eb = S == 1 ? tn : min(tn, ea + per);
   const int pre_n = min(EG, eb - ea);
+  const bool pre_rope = EPI == EPI_QKV && a.e.head_dim <= NTILE;  // [EG][head_dim / 2] float2 fits rr_pre
   if (warp >= 2) {
     // warps 2 and 3 have no mainloop role: fetch the epilogue's inputs now
     const int it = tid - 64;
     if (a.e.ssq_in)
       for (int tl = it; tl < tn; tl += 64)
         rs_all[tl] = row_rstd(a.e, a.e.in_rows ? a.e.in_rows[t0 + tl] : t0 + tl);
-    if (a.epi == EPI_RESID)
+    if (EPI == EPI_RESID)
       for (int x = it; x < pre_n * NTILE; x += 64)
         rr_pre[x] = a.e.resid[(size_t)(t0 + ea + x / NTILE) * a.e.H + n0 + x % NTILE];
+    if (EPI == EPI_QKV) {
+      if (it < pre_n) {
+        const int t = t0 + ea + it;
+        pos_pre[it] = a.e.row_pos[t];
+        req_pre[it] = a.e.plan->slot_req[a.e.row_slot[t]];
+      }
+      asm volatile("bar.sync 1, 64;" ::: "memory");  // warps 2 and 3 only
+      if (pre_rope) {
+        const int half = a.e.head_dim / 2;
+        for (int x = it; x < pre_n * half; x += 64) {
+          const int tl = x / half;
+          const int pc = min(max(pos_pre[tl], 0), a.e.cap - 1);  // a bad position is flagged by the epilogue
+          rope_pre[x] = a.e.rope[(size_t)pc * half + x % half];
+        }
+      }
+    }
   }
   const bool ok_done = tc::mbar_wait(done, 0);
   tc::fence_after_sync();
@@ -233,8 +263,18 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     if (!failed) {
       for (int g0 = 0; g0 < tn; g0 += EG) {
         const int cnt = min(EG, tn - g0);
-        apply_epilogue(a, Yp + g0 * YLD, YLD, tile, t0 + g0, cnt, scratch, a.e.ssq_in ? rs_all + g0 : nullptr,
-                       g0 == 0 ? rr_pre : nullptr);
+        EpiPre pre;
+        pre.rs = a.e.ssq_in ? rs_all + g0 : nullptr;
+        if (EPI == EPI_RESID) pre.gn = gn_pre;
+        if (g0 == 0) {
+          if (EPI == EPI_RESID) pre.rr = rr_pre;
+          if (EPI == EPI_QKV) {
+            pre.pos = pos_pre;
+            pre.req = req_pre;
+            if (pre_rope) pre.rope = rope_pre;
+          }
+        }
+        apply_epilogue_k<EPI>(a, Yp + g0 * YLD, YLD, tile, t0 + g0, cnt, scratch, pre);
       }
     }
   } else {
@@ -260,27 +300,52 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     if (!rx_ok && tid == 0) set_err(a.e.err, DERR_TIMEOUT);
     for (int g0 = ta; g0 < tb; g0 += EG) {
       const int cnt = min(EG, tb - g0);
-      for (int j = 0; j < cnt; ++j) {
-        float acc = 0.f;
-        for (int sp = 0; sp < S; ++sp) {
-          const float v = sp == rank ? Yp[(size_t)(g0 + j) * YLD + row]
-                                     : RX[((size_t)sp * per + (g0 - ta) + j) * YLD + row];
-          acc = sp == 0 ? v : acc + v;
-        }
-        Ys[j * YLD + row] = acc;
+      // thread x: token x / 32, columns 4 (x % 32) .. +3; every partial is
+      // loaded first, then they are added in rank order
+      for (int x = tid; x < cnt * (NTILE / 4); x += TC_THREADS) {
+        const int j = x / (NTILE / 4), c4 = (x % (NTILE / 4)) * 4;
+        float4 v[MAX_CLUSTER];
+#pragma unroll
+        for (int sp = 0; sp < MAX_CLUSTER; ++sp)
+          if (sp < S) {
+            const float* src = sp == rank ? Yp + (size_t)(g0 + j) * YLD : RX + ((size_t)sp * per + (g0 - ta) + j) * YLD;
+            v[sp] = *reinterpret_cast<const float4*>(src + c4);
+          }
+        float4 acc = v[0];
+#pragma unroll
+        for (int sp = 1; sp < MAX_CLUSTER; ++sp)
+          if (sp < S) {
+            acc.x += v[sp].x;
+            acc.y += v[sp].y;
+            acc.z += v[sp].z;
+            acc.w += v[sp].w;
+          }
+        *reinterpret_cast<float4*>(Ys + (size_t)j * YLD + c4) = acc;
       }
       __syncthreads();
-      if (!failed && rx_ok)
-        apply_epilogue(a, Ys, YLD, tile, t0 + g0, cnt, scratch, a.e.ssq_in ? rs_all + g0 : nullptr,
-                       g0 == ta ? rr_pre : nullptr);
+      if (!failed && rx_ok) {
+        EpiPre pre;
+        pre.rs = a.e.ssq_in ? rs_all + g0 : nullptr;
+        if (EPI == EPI_RESID) pre.gn = gn_pre;
+        if (g0 == ta) {
+          if (EPI == EPI_RESID) pre.rr = rr_pre;
+          if (EPI == EPI_QKV) {
+            pre.pos = pos_pre;
+            pre.req = req_pre;
+            if (pre_rope) pre.rope = rope_pre;
+          }
+        }
+        apply_epilogue_k<EPI>(a, Ys, YLD, tile, t0 + g0, cnt, scratch, pre);
+      }
     }
     if (tid == 0) tc::bulk_wait_read();  // the copies have read this CTA's partial tile
   }
-  if (a.epi == EPI_ARGMAX && !failed) argmax_grid_finish(a, &s_flag);
+  if (EPI == EPI_ARGMAX && !failed) argmax_grid_finish(a, &s_flag);
 }
 
-bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
-  if (a.splits < 1 || a.splits > 16) return false;
+template <int EPI>
+static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
+  if (a.splits < 1 || a.splits > MAX_CLUSTER) return false;
   CUtensorMap tmw, tmh, tml;
   if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE)) return false;
   const int nt = ((a.T < TZ_TC ? a.T : TZ_TC) + 15) / 16 * 16;
@@ -307,13 +372,15 @@ bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (smem > 227 * 1024) return false;
   static size_t configured = 0;
   if (smem > configured) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
       return false;
     if (configured == 0 &&
-        cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return false;
     configured = smem;
   }
+  prefer_shared(reinterpret_cast<const void*>(gemm_tc_kernel<EPI>));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(cdiv_i(a.N, NTILE), a.splits, cdiv_i(a.T, TZ_TC));
   cfg.blockDim = dim3(TC_THREADS);
@@ -333,7 +400,18 @@ bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tmw, tmh, tml, a, nt, two, stages, ring, per) == cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, tmw, tmh, tml, a, nt, two, stages, ring, per) == cudaSuccess;
+}
+
+bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {
+  switch (a.epi) {
+    case EPI_STORE: return launch_gemm_tc_k<EPI_STORE>(a, s, pdl);
+    case EPI_RESID: return launch_gemm_tc_k<EPI_RESID>(a, s, pdl);
+    case EPI_QKV: return launch_gemm_tc_k<EPI_QKV>(a, s, pdl);
+    case EPI_SWIGLU: return launch_gemm_tc_k<EPI_SWIGLU>(a, s, pdl);
+    case EPI_ARGMAX: return launch_gemm_tc_k<EPI_ARGMAX>(a, s, pdl);
+  }
+  return false;
 }
 
 }  // namespace gocr

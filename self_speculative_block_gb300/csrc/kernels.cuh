@@ -133,10 +133,18 @@ void launch_set_override(ReqState* st, int req, int n_ref, int n_sched, cudaStre
 // Library-level error message returned by gocr_last_error(NULL).
 void set_lib_error(const char* msg);
 
+// Ask for the largest shared-memory carveout for kernel `fn` on the current
+// device (once).  Every kernel of the decode path runs with the same SM
+// configuration, so a kernel launched early under programmatic dependent
+// launch can share SMs with the one before it, and two 104 KB CTAs fit on an
+// SM.
+void prefer_shared(const void* fn);
+
 // Launch helper: plain launch, or with the programmatic-dependent-launch attribute.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                             bool pdl, Args... args) {
+  prefer_shared(reinterpret_cast<const void*>(k));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = block;

@@ -11,7 +11,23 @@
 //     positions 0..p+A+1 and makes a_(A+1) the next boundary.
 #include "epilogue.cuh"
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 namespace gocr {
+
+void prefer_shared(const void* fn) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!done.insert({dev, fn}).second) return;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+      cudaSuccess)
+    cudaGetLastError();  // a hint only: the launch still works without it
+}
 
 // ---------------------------------------------------------------- embedding rows
 // resid[t] = E[tok] | [M] | prefix row;  X[t] = resid[t] * g0 as GEMM-input

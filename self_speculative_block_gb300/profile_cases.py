@@ -1,0 +1,120 @@
+"""Small, self-contained launches of the hot kernels for capture under a profiler.
+
+    python -m self_speculative_block_gb300.profile_cases draft
+        0.5B-class bf16 decoder, 1024-row synthetic prefill, then two draft
+        forwards (B = 32, 33 rows).  The prefill launches gemm_tc_kernel 65
+        times and attention_mma_kernel 16 times, so the first draft forward's
+        QKV / O / gate-up / down GEMMs are gemm_tc launches 65..68 and its first
+        attention is attention_mma launch 16.
+    python -m self_speculative_block_gb300.profile_cases sweep
+        The split-K GEMM over one forward's 65 weight matrices (16 x packed
+        QKV, O, packed gate/up, down, then the LM head) at the decode launch
+        shape: 33 tokens as hi and lo planes, 66 rows.  Runs the sweep once, then
+        once more as a CUDA graph (gemm_tc launches 65..129 are the graph's).
+
+Both hold about 2 GB on the device.  The sweep's shapes and inputs are the ones
+bench.py times for its kernel roofline.
+"""
+from __future__ import annotations
+
+import sys
+
+from . import synth
+
+
+def forward_gemm_shapes(cfg: synth.ModelConfig):
+    """(N, K) of every GEMM launch in one decoder forward, in launch order."""
+    h, f = cfg.hidden, cfg.ffn
+    shapes = []
+    for _ in range(cfg.n_layers):
+        shapes += [(cfg.q_dim + 2 * cfg.kv_dim, h), (h, cfg.q_dim), (2 * f, h), (h, f)]
+    shapes.append((cfg.vocab, h))
+    return shapes
+
+
+class GemmSweep:
+    """Device weights, inputs and outputs for the forward's GEMMs at `rows` rows."""
+
+    def __init__(self, cfg: synth.ModelConfig, rows: int, device, seed: int = 0):
+        import torch
+        from . import gocr
+        self.lib = gocr.load()
+        self.es = 2 if cfg.dtype == synth.BF16 else 4
+        self.dtype = gocr.DTYPE_BF16 if self.es == 2 else gocr.DTYPE_F32
+        tdt = torch.bfloat16 if self.es == 2 else torch.float32
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.device = device
+        self.rows = rows
+        self.shapes = forward_gemm_shapes(cfg)
+        self.ws = [(0.02 * torch.randn((n, k), generator=g, device=device)).to(tdt) for n, k in self.shapes]
+        self.xs = {k: torch.randn((rows, k), generator=g, device=device).to(tdt)
+                   for k in sorted({k for _, k in self.shapes})}
+        self.ys = [torch.empty((rows, n), dtype=torch.float32, device=device) for n, _ in self.shapes]
+        need = max(self.lib.gocr_op_linear_workspace(rows, n, k) for n, k in self.shapes)
+        self.workspace = torch.zeros(need, dtype=torch.uint8, device=device)
+
+    def run(self):
+        """Enqueue the forward's GEMM launches on the current stream."""
+        import torch
+        from . import gocr
+        stream = torch.cuda.current_stream(self.device).cuda_stream
+        for (n, k), w, y in zip(self.shapes, self.ws, self.ys):
+            rc = self.lib.gocr_op_linear(self.dtype, self.xs[k].data_ptr(), w.data_ptr(), y.data_ptr(), self.rows,
+                                         n, k, self.workspace.data_ptr(), self.workspace.numel(), stream)
+            if rc != gocr.GOCR_OK:
+                raise gocr.GocrError(rc, gocr.last_error(None))
+
+    def graph(self):
+        """The launches captured in one CUDA graph, so that timing them
+        measures the GPU and not the host's launch rate."""
+        import torch
+        self.run()  # tensor maps and kernel attributes are set up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        return g
+
+    def algorithmic_bytes(self) -> float:
+        """Mean bytes per launch: weights, input, fp32 output."""
+        T, es = self.rows, self.es
+        return sum(n * k * es + T * k * es + T * n * 4 for n, k in self.shapes) / len(self.shapes)
+
+
+def draft_case():
+    from . import gocr
+    cfg = synth.BASE
+    W = synth.make_weights(cfg)
+    dec = gocr.Decoder(cfg, W, max_ctx=1024 + 80, max_block=32)
+    del W
+    dec.prefill(0, synth.make_prefix(cfg, 1024))
+    _, x0 = dec.state(0)
+    for _ in range(2):
+        dec.debug_forward(0, gocr.FWD_DRAFT, [x0] + [0] * 32)
+    dec.close()
+
+
+def sweep_case():
+    import torch
+    sw = GemmSweep(synth.BASE, 2 * 33, torch.device("cuda:0"))
+    g = sw.graph()
+    g.replay()
+    torch.cuda.synchronize()
+
+
+def main(argv):
+    what = argv[1] if len(argv) > 1 else ""
+    if what == "draft":
+        draft_case()
+    elif what == "sweep":
+        sweep_case()
+    else:
+        print(__doc__)
+        return 2
+    print("ok")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main(sys.argv))
