@@ -218,6 +218,18 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
   const int mt = warp & 3, kh = warp >> 2;
   const int g = lane >> 2, tq = lane & 3;
 
+  // cp.async copies of the two planes of K (tile 0) or V (tile 2) of chunk c
+  // (keys c*AC .. c*AC+AC-1, zero past kmax)
+  auto load_part = [&](const bf16* p_h, const bf16* p_l, int tile0, int c, int kmax) {
+    for (int x = tid; x < 2 * AC * (D / 8); x += 256) {
+      const int pl = x / (AC * (D / 8)), rem = x % (AC * (D / 8));
+      const int j = rem / (D / 8), v = rem % (D / 8);
+      const int key = c * AC + j;
+      const bf16* base = pl == 0 ? p_h : p_l;
+      const bool in = key <= kmax;
+      cp_async16(KV + (tile0 + pl) * TILE + j * QLD + v * 8, base + (size_t)(in ? key : 0) * D + v * 8, in ? 16 : 0);
+    }
+  };
   // cp.async copies of chunk c (keys c*AC .. c*AC+AC-1, zero past kmax)
   auto load_chunk = [&](const bf16* k_h, const bf16* k_l, const bf16* v_h, const bf16* v_l, int c, int kmax) {
     for (int x = tid; x < 4 * AC * (D / 8); x += 256) {
@@ -261,7 +273,7 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
 
   int req = 0, row0 = 0, nrows = a.T;
   if (a.rows_per_slot > 0) {
-    req = a.slot_req[slot];
+    req = req_pre >= 0 ? req_pre : a.slot_req[slot];  // the slot table is constant during a decode
     row0 = slot * a.rows_per_slot;
     nrows = a.rows_per_slot;
   } else if (a.plan) {
@@ -320,12 +332,20 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
   const bf16* Vh = Kl + TILE;
   const bf16* Vl = Vh + TILE;
 
+  // K and V of a chunk are separate cp.async groups: K of the next chunk
+  // streams in while this chunk's softmax and PV run, V of the next chunk
+  // while the next QK^T runs.  Group order: [K+V of the first chunk] (issued
+  // before the wait when it is committed cache), Q, then K, V per chunk.
+  if (!pre && rank < n_chunks) {
+    load_part(k_h, k_l, 0, rank, maxlim);
+    load_part(v_h, v_l, 2, rank, maxlim);
+  }
+  cp_async_commit();
   int it = 0;
   for (int c = rank; c < n_chunks; c += CL, ++it) {
     const int kbase = c * AC + kh * 16;
-    if (it > 0 || !pre) load_chunk(k_h, k_l, v_h, v_l, c, maxlim);
-    cp_async_commit();
-    cp_async_wait<0>();
+    const bool next = c + CL < n_chunks;
+    if (it == 0) cp_async_wait<0>(); else cp_async_wait<1>();  // this chunk's K (and Q, first chunk)
     __syncthreads();
     // S = Q K^T for this warp's 16 rows and 16 keys
     float sacc[2][4];
@@ -356,6 +376,9 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
         mma16816(sacc[nt], ah, bh);
       }
     }
+    __syncthreads();  // every warp is done with this chunk's K
+    if (next) load_part(k_h, k_l, 0, c + CL, maxlim);
+    cp_async_commit();
     // mask, scale to log2 units, row maxima over the 16 keys
     float mc_lo = -INFINITY, mc_hi = -INFINITY;
 #pragma unroll
@@ -406,6 +429,10 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
       oacc[dn][0] *= corr_lo; oacc[dn][1] *= corr_lo;
       oacc[dn][2] *= corr_hi; oacc[dn][3] *= corr_hi;
     }
+    if (it > 0) {
+      cp_async_wait<1>();  // this chunk's V (the next chunk's K may still be in flight)
+      __syncthreads();
+    }
     // O += P (V_hi + V_lo); B fragments of two d-tiles per ldmatrix.x4.trans
     uint32_t af[4] = {pf[0][0], pf[0][1], pf[1][0], pf[1][1]};
 #pragma unroll
@@ -419,7 +446,9 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
       mma16816(oacc[dn + 1], af, bl + 2);
       mma16816(oacc[dn + 1], af, bh + 2);
     }
-    __syncthreads();
+    __syncthreads();  // every warp is done with this chunk's V
+    if (next) load_part(v_h, v_l, 2, c + CL, maxlim);
+    cp_async_commit();
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -482,30 +511,49 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
     tc::bulk_commit();
   }
   const bool rx_ok = tc::mbar_wait(&rxbar, 0);
-  // owner: rows rank + i * CL, partials of ranks 0 .. CL-1 added in rank order
-  if (tid < RPC) {
-    float M = -INFINITY;
-    for (int c = 0; c < CL; ++c) M = fmaxf(M, RX[(c * RPC + tid) * RLD + D]);
-    float L = 0.f;
-    for (int c = 0; c < CL; ++c) {
-      const float m = RX[(c * RPC + tid) * RLD + D];
-      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-      WS[tid * CL + c] = w;
-      L += w * RX[(c * RPC + tid) * RLD + D + 1];
-    }
-    IL[tid] = L > 0.f ? 1.f / L : 0.f;
+  // owner: rows rank + i * CL.  Warp i computes the merge weights of row i,
+  // lane c holding rank c's (max, sum); the butterfly order is fixed
+  if (warp < RPC) {
+    const int i = warp;
+    const float m = lane < CL ? RX[(lane * RPC + i) * RLD + D] : -INFINITY;
+    const float l = lane < CL ? RX[(lane * RPC + i) * RLD + D + 1] : 0.f;
+    float M = m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+    float L = w * l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane < CL) WS[i * CL + lane] = w;
+    if (lane == 0) IL[i] = L > 0.f ? 1.f / L : 0.f;
   }
   __syncthreads();
   if (rx_ok) {
-    for (int x = tid; x < RPC * D; x += 256) {
-      const int i = x / D, d = x % D;
+    // thread x: row x / (D / 4), outputs 4 (x % (D / 4)) .. +3; all CL partials
+    // are loaded first, then weighted and added in rank order
+    for (int x = tid; x < RPC * (D / 4); x += 256) {
+      const int i = x / (D / 4), d4 = (x % (D / 4)) * 4;
       const int gi = qr0 + rank + i * CL;
       if (gi >= nq) continue;
-      float acc = 0.f;
+      float4 pv[CL];
 #pragma unroll
-      for (int c = 0; c < CL; ++c) acc += WS[i * CL + c] * RX[(c * RPC + i) * RLD + d];
+      for (int c = 0; c < CL; ++c) pv[c] = *reinterpret_cast<const float4*>(RX + (c * RPC + i) * RLD + d4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < CL; ++c) {
+        const float w = WS[i * CL + c];
+        acc.x += w * pv[c].x;
+        acc.y += w * pv[c].y;
+        acc.z += w * pv[c].z;
+        acc.w += w * pv[c].w;
+      }
+      const float il = IL[i];
       const int t = row0 + gi / G, hq = kvh * G + gi % G;
-      put_plane(a.o_hi, a.o_lo, a.out_bf16, ((size_t)t * a.Hq + hq) * D + d, acc * IL[i]);
+      const size_t o = ((size_t)t * a.Hq + hq) * D + d4;
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o, acc.x * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 1, acc.y * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 2, acc.z * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 3, acc.w * il);
     }
   }
   if (tid == 0) tc::bulk_wait_read();  // the copies have read this CTA's staged rows
