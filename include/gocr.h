@@ -156,6 +156,46 @@ int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, float* k_o
 /* Current cache length (position of the boundary token) and boundary token. */
 int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0);
 
+/* Handle options.
+ *   GOCR_OPT_FORWARD  which kernels run a decode forward (draft, verify, AR
+ *                     step, debug forward) of a bf16 model with head_dim 128
+ *                     and at most 128 rows per forward:
+ *     GOCR_FORWARD_OPS (default)  one kernel per operation, chained by
+ *       programmatic dependent launch;
+ *     GOCR_FORWARD_PERSISTENT  one persistent kernel per forward, one CTA per
+ *       SM: every layer's GEMMs, attention and epilogues and the LM head, with
+ *       device counters in place of kernel boundaries.
+ *   Both give bit-identical results (the same reductions in the same order).
+ *   Prefill, fp32 models and larger forwards always run one kernel per
+ *   operation.  The environment variable GOCR_FORWARD=persistent selects
+ *   PERSISTENT at create time.  Changing the option drops the handle's
+ *   captured graphs.
+ * GOCR_EINVAL for an unknown option or value. */
+/*   GOCR_OPT_PERSISTENT_FORWARDS  (get only) forwards the persistent kernel
+ *                     completed in the last decode or debug-forward call of
+ *                     the handle, read from the device (0 when none ran). */
+/*   GOCR_OPT_TRACE_RECORDS (get only) event records per writer of the
+ *                     persistent forward's trace (0 = tracing off; the
+ *                     environment variable GOCR_MK_TRACE=<records> at create
+ *                     time turns it on).
+ *   GOCR_OPT_GRID_CTAS (get only) CTAs of the persistent forward (SM count). */
+enum { GOCR_OPT_FORWARD = 1, GOCR_OPT_PERSISTENT_FORWARDS = 2, GOCR_OPT_TRACE_RECORDS = 3,
+       GOCR_OPT_GRID_CTAS = 4 };
+enum { GOCR_FORWARD_PERSISTENT = 0, GOCR_FORWARD_OPS = 1 };
+int gocr_set_option(gocr_handle* h, int option, int value);
+int gocr_get_option(const gocr_handle* h, int option, int* value);
+
+/* Event trace of the last persistent forward (a profiling aid; tracing must
+ * be on, see GOCR_OPT_TRACE_RECORDS).  out: host, n_words >= CTAs * 2 *
+ * records * 2 words, laid out [CTA][writer][record][2]: writer 0 is the
+ * activation producer, writer 1 the compute group; a record is (globaltimer
+ * ns, phase << 8 | event), zero past the last record.  Phases: layer l has
+ * QKV, attention, O, gate/up, down at 5 l + 0..4, the LM head is 5 L.
+ * Events: 0 start, 1 input ready, 2 accumulator ready, 3 partial tile
+ * written, 4 tile finished, 5 attention inputs ready, 6 attention partial
+ * rows written, 7 attention rows merged, 8 end.  GOCR_ESTATE when off. */
+int gocr_read_trace(gocr_handle* h, uint64_t* out, size_t n_words);
+
 /* Last error message of the handle (or of the library when h is NULL). */
 const char* gocr_last_error(const gocr_handle* h);
 

@@ -1,0 +1,437 @@
+// Tensor-core attention of one (request, kv head, 64-query-row group) tile
+// over a fixed subset of key chunks, and the fixed-order merge of the
+// partial results of the CL tiles that share those query rows.
+//
+// The per-forward attention kernel (one CTA per tile, a thread-block
+// cluster of CL tiles merging over distributed shared memory) and the
+// persistent decode kernel (tiles as work items, merging through global
+// memory) both run these functions, so a row's attention output has the
+// same bits whichever kernel computes it.
+//
+// Layout of the work: keys sit in chunks of AC = 32 at absolute positions;
+// tile `rank` of the CL tiles visits chunks rank, rank + CL, ...  In a tile,
+// warp w owns query rows 16 (w % 4) .. +15 and key half w / 4 (keys
+// 16 (w / 4) .. +15 of every chunk), so each (rank, key half) runs its own
+// online softmax over a fixed set of key positions.  A chunk with no key
+// visible to a row leaves that row's running (max, sum, output) bit for bit
+// unchanged, so a row's result does not depend on the other rows.  q and the
+// KV cache are bf16 hi + lo planes: QK^T takes qh kh + qh kl + ql kh and PV
+// takes P vh + P vl on mma.sync tiles (P in bf16), accumulating in fp32.
+#pragma once
+#include "epilogue.cuh"
+
+namespace gocr {
+namespace attn {
+
+constexpr int QR = 64;      // query rows (token, q head) per tile
+constexpr int AC = 32;      // keys per chunk
+constexpr float LOG2E = 1.4426950408889634f;
+
+template <int D> struct Geo {
+  static constexpr int QLD = D + 8;    // bf16 row stride of the Q, K and V tiles
+  static constexpr int OLD = D + 4;    // fp32 row stride of the half-1 partial
+  static constexpr int TILE = AC * QLD;
+  static constexpr int RLD = D + 4;    // fp32 stride of a partial row: D outputs, max, sum, pad
+  // shared memory of one tile: Q planes, the four K/V chunk planes, row limits
+  static constexpr size_t Q_BYTES = (size_t)2 * QR * QLD * 2;
+  static constexpr size_t KV_BYTES = (size_t)4 * TILE * 2;
+  static constexpr size_t LIM_BYTES = QR * 4;
+  static constexpr size_t TILE_SMEM = Q_BYTES + KV_BYTES + LIM_BYTES + 16;
+  // the staged partial rows (CL x RPC = QR rows) live where K/V were
+  static_assert((size_t)QR * RLD * 4 <= KV_BYTES, "staged rows fit the K/V region");
+  static_assert((size_t)QR * OLD * 4 + 2 * QR * 4 <= Q_BYTES, "half-1 partial fits the Q region");
+};
+
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Four 8x8 bf16 matrices, transposed on load: each lane gets the pair
+// (row 2t, col g), (row 2t+1, col g) of the matrix whose row addresses lanes
+// 8i..8i+7 supply, which is the B-fragment layout of m16n8k16.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Hint a contiguous global range into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, int bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 fills zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Cache planes of one (request, kv head): K hi, K lo, V hi, V lo.
+struct KvPlanes {
+  const bf16* p[4];
+};
+
+__device__ __forceinline__ KvPlanes kv_planes(const AttnArgs& a, int req, int kvh, int D) {
+  const size_t o = (size_t)req * a.req_stride + (size_t)kvh * a.cap * D;
+  KvPlanes k;
+  k.p[0] = reinterpret_cast<const bf16*>(a.k_hi) + o;
+  k.p[1] = reinterpret_cast<const bf16*>(a.k_lo) + o;
+  k.p[2] = reinterpret_cast<const bf16*>(a.v_hi) + o;
+  k.p[3] = reinterpret_cast<const bf16*>(a.v_lo) + o;
+  return k;
+}
+
+// cp.async copies of planes [pl0, pl0 + npl) of chunk c (keys c*AC .. c*AC+AC-1,
+// zero past kmax) into the tile's K/V region, by the group's 256 threads.
+template <int D>
+__device__ __forceinline__ void load_planes(bf16* KV, const KvPlanes& kv, int pl0, int npl, int c, int kmax,
+                                            int tid) {
+  using G = Geo<D>;
+  for (int x = tid; x < npl * AC * (D / 8); x += 256) {
+    const int pl = pl0 + x / (AC * (D / 8)), rem = x % (AC * (D / 8));
+    const int j = rem / (D / 8), v = rem % (D / 8);
+    const int key = c * AC + j;
+    const bool in = key <= kmax;
+    cp_async16(KV + pl * G::TILE + j * G::QLD + v * 8, kv.p[pl] + (size_t)(in ? key : 0) * D + v * 8, in ? 16 : 0);
+  }
+}
+
+// Work a tile may start before the rows' q and the window's K/V exist: when
+// its first chunk holds only committed cache positions (below the round-start
+// cache length pc, which no kernel of the forward writes), that chunk goes to
+// shared memory as one committed cp.async group and the tile's later
+// committed chunks into L2.  Returns whether the first chunk was issued.
+template <int D, int CL>
+__device__ __forceinline__ bool tile_prefetch(uint8_t* sm, const KvPlanes& kv, int rank, int pc, int tid) {
+  bf16* KV = reinterpret_cast<bf16*>(sm + Geo<D>::Q_BYTES);
+  const bool pre = (rank + 1) * AC <= pc;
+  if (pre) {
+    load_planes<D>(KV, kv, 0, 4, rank, pc - 1, tid);
+    cp_async_commit();
+    for (int i = tid; i < 4 * 8; i += 256) {
+      const int c = rank + (1 + i / 4) * CL;
+      if ((c + 1) * AC <= pc) prefetch_l2(kv.p[i % 4] + (size_t)c * AC * D, AC * D * 2);
+    }
+  }
+  return pre;
+}
+
+// One tile: query rows qr0 .. qr0+63 of the (row, q head) list of a request
+// window (rows row0 .. row0+nrows-1, G = Hq / Hkv heads per kv head), keys
+// of chunks rank, rank + CL, ...  `pre`: tile_prefetch issued the first chunk.
+// On return the tile's partial rows (D outputs, max, sum) sit in shared
+// memory, staged by owner: row r at (r % CL) * (QR / CL) + r / CL, stride RLD,
+// starting at staged_rows(sm).  Every thread of the 256-thread group calls it.
+template <int D>
+__device__ __forceinline__ float* staged_rows(uint8_t* sm) {
+  return reinterpret_cast<float*>(sm + Geo<D>::Q_BYTES);
+}
+
+template <int D, int CL>
+__device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, const KvPlanes& kv, int rank, int kvh,
+                             int qr0, int row0, int nrows, bool pre, int* s_maxlim) {
+  using Gm = Geo<D>;
+  constexpr int QLD = Gm::QLD, OLD = Gm::OLD, TILE = Gm::TILE, RLD = Gm::RLD;
+  constexpr int RPC = QR / CL;
+  bf16* Qh = reinterpret_cast<bf16*>(sm);               // [QR][QLD]
+  bf16* Ql = Qh + QR * QLD;
+  bf16* KV = Ql + QR * QLD;                             // {Kh, Kl, Vh, Vl} [AC][QLD]
+  int* Lim = reinterpret_cast<int*>(sm + Gm::Q_BYTES + Gm::KV_BYTES);  // [QR]
+  float* Oh = reinterpret_cast<float*>(Qh);             // [QR][OLD] half-1 partial (Q is dead by then)
+  float* Mh = Oh + QR * OLD;                            // [QR]
+  float* Lh = Mh + QR;                                  // [QR]
+  float* ST = reinterpret_cast<float*>(KV);             // [CL][RPC][RLD] staged rows
+
+  const int G = a.Hq / a.Hkv;
+  const int tid = grp.tid, warp = tid >> 5, lane = tid & 31;
+  const int mt = warp & 3, kh = warp >> 2;
+  const int g = lane >> 2, tq = lane & 3;
+  const int nq = nrows * G;
+  const bf16* qh = reinterpret_cast<const bf16*>(a.q_hi);
+  const bf16* ql = reinterpret_cast<const bf16*>(a.q_lo);
+
+  if (tid == 0) *s_maxlim = -1;
+  grp.sync();
+  // Q planes of this row group (zero past the window) and the rows' key limits
+  for (int x = tid; x < 2 * QR * (D / 8); x += 256) {
+    const int pl = x / (QR * (D / 8)), rem = x % (QR * (D / 8));
+    const int r = rem / (D / 8), v = rem % (D / 8);
+    const int gi = qr0 + r;
+    size_t src = 0;
+    if (gi < nq) src = ((size_t)(row0 + gi / G) * a.Hq + kvh * G + gi % G) * D + v * 8;
+    cp_async16((pl ? Ql : Qh) + r * QLD + v * 8, (pl ? ql : qh) + src, gi < nq ? 16 : 0);
+  }
+  cp_async_commit();
+  if (tid < QR) {
+    const int gi = qr0 + tid;
+    int lim = -1;
+    if (gi < nq) lim = min(a.row_lim[row0 + gi / G], a.cap - 1);
+    Lim[tid] = lim;
+    if (lim >= 0) atomicMax(s_maxlim, lim);
+  }
+  grp.sync();
+  const int maxlim = *s_maxlim;
+  const int n_chunks = maxlim < 0 ? 0 : maxlim / AC + 1;
+  const float sl2 = a.scale * LOG2E;
+
+  const int r_lo = mt * 16 + g, r_hi = r_lo + 8;
+  const int lim_lo = Lim[r_lo], lim_hi = Lim[r_hi];
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  float oacc[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
+  const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int lcol = (lane >> 4) * 8;
+  const bf16* Kh = KV + kh * 16 * QLD;  // this warp's 16 keys of the chunk
+  const bf16* Kl = Kh + TILE;
+  const bf16* Vh = Kl + TILE;
+  const bf16* Vl = Vh + TILE;
+
+  // K and V of a chunk are separate cp.async groups: K of the next chunk
+  // streams in while this chunk's softmax and PV run, V of the next chunk
+  // while the next QK^T runs.  Group order: [K+V of the first chunk] (issued
+  // early when it is committed cache), Q, then K, V per chunk.
+  if (!pre && rank < n_chunks) {
+    load_planes<D>(KV, kv, 0, 2, rank, maxlim, tid);
+    load_planes<D>(KV, kv, 2, 2, rank, maxlim, tid);
+  }
+  cp_async_commit();
+  int it = 0;
+  for (int c = rank; c < n_chunks; c += CL, ++it) {
+    const int kbase = c * AC + kh * 16;
+    const bool next = c + CL < n_chunks;
+    if (it == 0) cp_async_wait<0>(); else cp_async_wait<1>();  // this chunk's K (and Q, first chunk)
+    grp.sync();
+    // S = Q K^T for this warp's 16 rows and 16 keys
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t ah[4], al[4];
+      const int qo = (mt * 16 + g) * QLD + ks * 16 + tq * 2;
+      ah[0] = *reinterpret_cast<const uint32_t*>(Qh + qo);
+      ah[1] = *reinterpret_cast<const uint32_t*>(Qh + qo + 8 * QLD);
+      ah[2] = *reinterpret_cast<const uint32_t*>(Qh + qo + 8);
+      ah[3] = *reinterpret_cast<const uint32_t*>(Qh + qo + 8 * QLD + 8);
+      al[0] = *reinterpret_cast<const uint32_t*>(Ql + qo);
+      al[1] = *reinterpret_cast<const uint32_t*>(Ql + qo + 8 * QLD);
+      al[2] = *reinterpret_cast<const uint32_t*>(Ql + qo + 8);
+      al[3] = *reinterpret_cast<const uint32_t*>(Ql + qo + 8 * QLD + 8);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int ko = (nt * 8 + g) * QLD + ks * 16 + tq * 2;
+        uint32_t bh[2], bl[2];
+        bh[0] = *reinterpret_cast<const uint32_t*>(Kh + ko);
+        bh[1] = *reinterpret_cast<const uint32_t*>(Kh + ko + 8);
+        bl[0] = *reinterpret_cast<const uint32_t*>(Kl + ko);
+        bl[1] = *reinterpret_cast<const uint32_t*>(Kl + ko + 8);
+        mma16816(sacc[nt], al, bh);
+        mma16816(sacc[nt], ah, bl);
+        mma16816(sacc[nt], ah, bh);
+      }
+    }
+    grp.sync();  // every warp is done with this chunk's K
+    if (next) load_planes<D>(KV, kv, 0, 2, c + CL, maxlim, tid);
+    cp_async_commit();
+    // mask, scale to log2 units, row maxima over the 16 keys
+    float mc_lo = -INFINITY, mc_hi = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = kbase + nt * 8 + tq * 2 + e;
+        float s0 = key <= lim_lo ? sacc[nt][e] * sl2 : -INFINITY;
+        float s1 = key <= lim_hi ? sacc[nt][2 + e] * sl2 : -INFINITY;
+        sacc[nt][e] = s0;
+        sacc[nt][2 + e] = s1;
+        mc_lo = fmaxf(mc_lo, s0);
+        mc_hi = fmaxf(mc_hi, s1);
+      }
+    }
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      mc_lo = fmaxf(mc_lo, __shfl_xor_sync(0xffffffffu, mc_lo, off));
+      mc_hi = fmaxf(mc_hi, __shfl_xor_sync(0xffffffffu, mc_hi, off));
+    }
+    const float mn_lo = fmaxf(m_lo, mc_lo), mn_hi = fmaxf(m_hi, mc_hi);
+    const float corr_lo = mn_lo == -INFINITY ? 1.f : (m_lo == -INFINITY ? 0.f : exp2f(m_lo - mn_lo));
+    const float corr_hi = mn_hi == -INFINITY ? 1.f : (m_hi == -INFINITY ? 0.f : exp2f(m_hi - mn_hi));
+    float ps_lo = 0.f, ps_hi = 0.f;
+    uint32_t pf[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      float p0 = sacc[nt][0] == -INFINITY ? 0.f : exp2f(sacc[nt][0] - mn_lo);
+      float p1 = sacc[nt][1] == -INFINITY ? 0.f : exp2f(sacc[nt][1] - mn_lo);
+      float p2 = sacc[nt][2] == -INFINITY ? 0.f : exp2f(sacc[nt][2] - mn_hi);
+      float p3 = sacc[nt][3] == -INFINITY ? 0.f : exp2f(sacc[nt][3] - mn_hi);
+      ps_lo += p0 + p1;
+      ps_hi += p2 + p3;
+      pf[nt][0] = pack_bf16(p0, p1);
+      pf[nt][1] = pack_bf16(p2, p3);
+    }
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      ps_lo += __shfl_xor_sync(0xffffffffu, ps_lo, off);
+      ps_hi += __shfl_xor_sync(0xffffffffu, ps_hi, off);
+    }
+    l_lo = l_lo * corr_lo + ps_lo;
+    l_hi = l_hi * corr_hi + ps_hi;
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      oacc[dn][0] *= corr_lo; oacc[dn][1] *= corr_lo;
+      oacc[dn][2] *= corr_hi; oacc[dn][3] *= corr_hi;
+    }
+    if (it > 0) {
+      cp_async_wait<1>();  // this chunk's V (the next chunk's K may still be in flight)
+      grp.sync();
+    }
+    // O += P (V_hi + V_lo); B fragments of two d-tiles per ldmatrix.x4.trans
+    uint32_t af[4] = {pf[0][0], pf[0][1], pf[1][0], pf[1][1]};
+#pragma unroll
+    for (int dn = 0; dn < D / 8; dn += 2) {
+      const int vo = lrow * QLD + dn * 8 + lcol;
+      uint32_t bh[4], bl[4];
+      ldsm_x4_trans(bh, Vh + vo);
+      ldsm_x4_trans(bl, Vl + vo);
+      mma16816(oacc[dn], af, bl);
+      mma16816(oacc[dn], af, bh);
+      mma16816(oacc[dn + 1], af, bl + 2);
+      mma16816(oacc[dn + 1], af, bh + 2);
+    }
+    grp.sync();  // every warp is done with this chunk's V
+    if (next) load_planes<D>(KV, kv, 2, 2, c + CL, maxlim, tid);
+    cp_async_commit();
+  }
+  cp_async_wait<0>();
+  grp.sync();
+  // merge the two key halves of this tile: half 0 + half 1, in that order
+  if (kh == 1) {
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      Oh[r_lo * OLD + dn * 8 + tq * 2] = oacc[dn][0];
+      Oh[r_lo * OLD + dn * 8 + tq * 2 + 1] = oacc[dn][1];
+      Oh[r_hi * OLD + dn * 8 + tq * 2] = oacc[dn][2];
+      Oh[r_hi * OLD + dn * 8 + tq * 2 + 1] = oacc[dn][3];
+    }
+    if (tq == 0) {
+      Mh[r_lo] = m_lo; Lh[r_lo] = l_lo;
+      Mh[r_hi] = m_hi; Lh[r_hi] = l_hi;
+    }
+  }
+  grp.sync();
+  if (kh == 0) {
+    const float m1_lo = Mh[r_lo], m1_hi = Mh[r_hi];
+    const float M_lo = fmaxf(m_lo, m1_lo), M_hi = fmaxf(m_hi, m1_hi);
+    const float w0_lo = m_lo == -INFINITY ? 0.f : exp2f(m_lo - M_lo);
+    const float w1_lo = m1_lo == -INFINITY ? 0.f : exp2f(m1_lo - M_lo);
+    const float w0_hi = m_hi == -INFINITY ? 0.f : exp2f(m_hi - M_hi);
+    const float w1_hi = m1_hi == -INFINITY ? 0.f : exp2f(m1_hi - M_hi);
+    const float L_lo = w0_lo * l_lo + w1_lo * Lh[r_lo];
+    const float L_hi = w0_hi * l_hi + w1_hi * Lh[r_hi];
+    // stage this tile's partial rows by owner: row r -> rank r % CL, slot r / CL
+    float* st_lo = ST + ((r_lo % CL) * RPC + r_lo / CL) * RLD;
+    float* st_hi = ST + ((r_hi % CL) * RPC + r_hi / CL) * RLD;
+    float o1[D / 8][4];
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      const int col = dn * 8 + tq * 2;
+      o1[dn][0] = Oh[r_lo * OLD + col];
+      o1[dn][1] = Oh[r_lo * OLD + col + 1];
+      o1[dn][2] = Oh[r_hi * OLD + col];
+      o1[dn][3] = Oh[r_hi * OLD + col + 1];
+    }
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      const int col = dn * 8 + tq * 2;
+      st_lo[col] = w0_lo * oacc[dn][0] + w1_lo * o1[dn][0];
+      st_lo[col + 1] = w0_lo * oacc[dn][1] + w1_lo * o1[dn][1];
+      st_hi[col] = w0_hi * oacc[dn][2] + w1_hi * o1[dn][2];
+      st_hi[col + 1] = w0_hi * oacc[dn][3] + w1_hi * o1[dn][3];
+    }
+    if (tq == 0) {
+      st_lo[D] = M_lo; st_lo[D + 1] = L_lo;
+      st_hi[D] = M_hi; st_hi[D + 1] = L_hi;
+    }
+  }
+  grp.sync();
+}
+
+// Merge of the RPC rows that tile `owner` owns (rows owner + i * CL of the
+// row group) from the CL tiles' partial rows, row(c, i) -> D outputs, max,
+// sum of tile c's partial of owned row i.  Warp i computes the merge weights
+// of row i with lane c holding tile c's (max, sum) and a fixed butterfly
+// order; then all CL partials of an output quad are loaded and added in tile
+// order.  Writes the rows' attention output planes.  WS: [RPC][CL] and IL:
+// [RPC] shared scratch.  GLOBAL: the partial rows are in global memory,
+// written by other CTAs of a running kernel (read through L2, not L1).
+template <int D, int CL, class Row, bool GLOBAL = false>
+__device__ void merge_owned(const AttnArgs& a, const Grp& grp, const Row& row, float* WS, float* IL, int owner,
+                            int kvh, int qr0, int row0, int nrows, bool ok) {
+  constexpr int RPC = QR / CL;
+  const int tid = grp.tid, warp = tid >> 5, lane = tid & 31;
+  const int G = a.Hq / a.Hkv;
+  const int nq = nrows * G;
+  if (warp < RPC) {
+    const int i = warp;
+    const float m = lane < CL ? (GLOBAL ? __ldcg(row(lane, i) + D) : row(lane, i)[D]) : -INFINITY;
+    const float l = lane < CL ? (GLOBAL ? __ldcg(row(lane, i) + D + 1) : row(lane, i)[D + 1]) : 0.f;
+    float M = m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+    float L = w * l;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane < CL) WS[i * CL + lane] = w;
+    if (lane == 0) IL[i] = L > 0.f ? 1.f / L : 0.f;
+  }
+  grp.sync();
+  if (ok) {
+    for (int x = tid; x < RPC * (D / 4); x += grp.n) {
+      const int i = x / (D / 4), d4 = (x % (D / 4)) * 4;
+      const int gi = qr0 + owner + i * CL;
+      if (gi >= nq) continue;
+      float4 pv[CL];
+#pragma unroll
+      for (int c = 0; c < CL; ++c)
+        pv[c] = GLOBAL ? __ldcg(reinterpret_cast<const float4*>(row(c, i) + d4))
+                       : *reinterpret_cast<const float4*>(row(c, i) + d4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < CL; ++c) {
+        const float w = WS[i * CL + c];
+        acc.x += w * pv[c].x;
+        acc.y += w * pv[c].y;
+        acc.z += w * pv[c].z;
+        acc.w += w * pv[c].w;
+      }
+      const float il = IL[i];
+      const int t = row0 + gi / G, hq = kvh * G + gi % G;
+      const size_t o = ((size_t)t * a.Hq + hq) * D + d4;
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o, acc.x * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 1, acc.y * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 2, acc.z * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 3, acc.w * il);
+    }
+  }
+}
+
+}  // namespace attn
+
+}  // namespace gocr

@@ -13,6 +13,20 @@ __device__ __forceinline__ void set_err(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// The threads that run an epilogue: the whole CTA (barrier 0), or a set of
+// whole warps that synchronise on a named barrier of their own while the
+// CTA's other warps keep producing.
+struct Grp {
+  int tid;   // thread index within the group
+  int n;     // threads in the group (a multiple of 32)
+  int bar;   // 0: __syncthreads; else the named barrier id
+  __device__ static Grp block() { return Grp{(int)threadIdx.x, (int)blockDim.x, 0}; }
+  __device__ __forceinline__ void sync() const {
+    if (bar == 0) __syncthreads();
+    else asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(n) : "memory");
+  }
+};
+
 // (value, index) maximum with the lowest index among equal values.
 __device__ __forceinline__ void argmax_merge(float& v, int& i, float ov, int oi) {
   if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
@@ -44,7 +58,7 @@ __device__ __forceinline__ float row_rstd(const EpiArgs& e, int row) {
   const float* p = e.ssq_in + (size_t)row * e.n_ssq;
   float v[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = i < e.n_ssq ? p[i] : 0.f;
+  for (int i = 0; i < 32; ++i) v[i] = i < e.n_ssq ? __ldcg(p + i) : 0.f;
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < 32; ++i)
@@ -72,14 +86,16 @@ struct EpiPre {
 // Epilogue EPI of tokens t0 .. t0+tn-1.  Every pass first issues all of its
 // global loads (sums of squares, residual rows) into shared memory, so a pass
 // costs one memory round trip rather than one per token; inputs in `pre`
-// (tn <= EPI_GROUP) are not fetched again.  The kind is a template argument
+// (tn <= EPI_GROUP) are not fetched again.  Those loads bypass L1: inside a
+// persistent kernel other CTAs rewrite the residual and the sums between two
+// epilogues that run on one SM.  The kind is a template argument
 // so that a kernel carries only its own epilogue code.
 template <int EPI>
 __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0, int tn,
-                                        float* scratch, const EpiPre& pre = EpiPre()) {
+                                        float* scratch, const EpiPre& pre, const Grp& grp) {
   const EpiArgs& e = a.e;
   const int n0 = tile * NTILE;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
+  const int tid = grp.tid, lane = tid & 31, warp = tid >> 5, nwarp = grp.n >> 5;
   float* rs_s = scratch;                                 // [EPI_GROUP] row scales
   float* sq = rs_s + EPI_GROUP;                          // [EPI_GROUP][n_ssq]
   float* rr_s = sq + EPI_GROUP * EPI_MAX_SSQ;            // [EPI_GROUP][NTILE] residual rows
@@ -92,25 +108,25 @@ __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int 
     const bool load_rs = norm && !rs_in;
     const bool load_rr = resid && !rr_in;
     if (load_rs)
-      for (int x = tid; x < gn * e.n_ssq; x += blockDim.x) {
+      for (int x = tid; x < gn * e.n_ssq; x += grp.n) {
         const int tl = x / e.n_ssq, i = x % e.n_ssq;
         const int row = e.in_rows ? e.in_rows[t0 + g0 + tl] : t0 + g0 + tl;
-        sq[tl * e.n_ssq + i] = e.ssq_in[(size_t)row * e.n_ssq + i];
+        sq[tl * e.n_ssq + i] = __ldcg(e.ssq_in + (size_t)row * e.n_ssq + i);
       }
     if (load_rr)
-      for (int x = tid; x < gn * NTILE; x += blockDim.x) {
+      for (int x = tid; x < gn * NTILE; x += grp.n) {
         const int tl = x / NTILE, c = x % NTILE;
-        rr_s[x] = e.resid[(size_t)(t0 + g0 + tl) * e.H + n0 + c];
+        rr_s[x] = __ldcg(e.resid + (size_t)(t0 + g0 + tl) * e.H + n0 + c);
       }
-    if (load_rs || load_rr) __syncthreads();
+    if (load_rs || load_rr) grp.sync();
     if (load_rs) {
       // rstd = 1 / sqrt(mean(x^2) + eps), partial sums added in column order
-      for (int tl = tid; tl < gn; tl += blockDim.x) {
+      for (int tl = tid; tl < gn; tl += grp.n) {
         float ssum = 0.f;
         for (int i = 0; i < e.n_ssq; ++i) ssum += sq[tl * e.n_ssq + i];
         rs_s[tl] = rsqrtf(ssum / (float)e.norm_H + e.eps);
       }
-      __syncthreads();
+      grp.sync();
     }
     const bool first = g0 == 0;
     const float* rs = rs_in ? rs_in + g0 : rs_s;
@@ -206,7 +222,7 @@ __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int 
         }
       }
     }
-    __syncthreads();
+    grp.sync();
   }
 }
 
@@ -214,11 +230,11 @@ __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int 
 __device__ inline void apply_epilogue(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0, int tn,
                                       float* scratch) {
   switch (a.epi) {
-    case EPI_STORE: apply_epilogue_k<EPI_STORE>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
-    case EPI_RESID: apply_epilogue_k<EPI_RESID>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
-    case EPI_QKV: apply_epilogue_k<EPI_QKV>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
-    case EPI_SWIGLU: apply_epilogue_k<EPI_SWIGLU>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
-    case EPI_ARGMAX: apply_epilogue_k<EPI_ARGMAX>(a, Ys, ys_ld, tile, t0, tn, scratch); break;
+    case EPI_STORE: apply_epilogue_k<EPI_STORE>(a, Ys, ys_ld, tile, t0, tn, scratch, EpiPre(), Grp::block()); break;
+    case EPI_RESID: apply_epilogue_k<EPI_RESID>(a, Ys, ys_ld, tile, t0, tn, scratch, EpiPre(), Grp::block()); break;
+    case EPI_QKV: apply_epilogue_k<EPI_QKV>(a, Ys, ys_ld, tile, t0, tn, scratch, EpiPre(), Grp::block()); break;
+    case EPI_SWIGLU: apply_epilogue_k<EPI_SWIGLU>(a, Ys, ys_ld, tile, t0, tn, scratch, EpiPre(), Grp::block()); break;
+    case EPI_ARGMAX: apply_epilogue_k<EPI_ARGMAX>(a, Ys, ys_ld, tile, t0, tn, scratch, EpiPre(), Grp::block()); break;
   }
 }
 

@@ -9,6 +9,9 @@
 // output equal its own AR-greedy output token for token.
 #include "epilogue.cuh"
 
+#include <cstdlib>
+#include <cstring>
+
 namespace gocr {
 
 namespace {
@@ -22,11 +25,34 @@ constexpr int YS_LD = NTILE + 1;
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 }  // namespace
 
+// Split rule, fixed for the process (GOCR_SPLIT_K: "wave", the default, or
+// the largest K chunk in elements).
+//   wave:  enough splits to fill two CTAs per SM in one wave (at most 12), so
+//          that every SM streams an equal share of a matrix's weights: one
+//          SM's TMA ring sustains only about 1/150 of HBM bandwidth.
+//   chunk: K is cut into ceil(K / chunk) equal splits (fewer reductions,
+//          fewer SMs per matrix).
+static int split_chunk_limit() {
+  static int lim = -1;
+  if (lim < 0) {
+    const char* v = getenv("GOCR_SPLIT_K");
+    lim = 0;
+    if (v && strcmp(v, "wave") != 0 && atoi(v) >= 64) lim = atoi(v) / 64 * 64;
+  }
+  return lim;
+}
+
 int gemm_kchunk(int N, int K) {
   const int tiles = cdiv(N, NTILE);
   const int kb = cdiv(K, 64);
-  int s = (2 * SM_COUNT) / tiles;  // at most two CTAs per SM in one wave
-  if (s > MAX_SPLITS) s = MAX_SPLITS;
+  const int lim = split_chunk_limit();
+  int s;
+  if (lim > 0) {
+    s = cdiv(kb, lim / 64);
+  } else {
+    s = (2 * SM_COUNT) / tiles;  // at most two CTAs per SM in one wave
+    if (s > MAX_SPLITS) s = MAX_SPLITS;
+  }
   if (s > kb) s = kb;
   if (s < 1) s = 1;
   return cdiv(kb, s) * 64;

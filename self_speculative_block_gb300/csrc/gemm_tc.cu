@@ -86,6 +86,10 @@ bool tmap_2d(CUtensorMap* out, const void* ptr, int rows, int cols, int box_rows
 __host__ __device__ inline int cdiv_i(int a, int b) { return (a + b - 1) / b; }
 }  // namespace
 
+bool encode_tmap_bf16(void* out, const void* ptr, int rows, int cols, int box_rows) {
+  return tmap_2d(reinterpret_cast<CUtensorMap*>(out), ptr, rows, cols, box_rows);
+}
+
 // ring_bytes >= stages * (A tile + B tile) and >= the partial tile + reduce buffer.
 // EPI: the fused epilogue (a.epi), one instantiation per kind.
 template <int EPI>
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
             if (pre_rope) pre.rope = rope_pre;
           }
         }
-        apply_epilogue_k<EPI>(a, Yp + g0 * YLD, YLD, tile, t0 + g0, cnt, scratch, pre);
+        apply_epilogue_k<EPI>(a, Yp + g0 * YLD, YLD, tile, t0 + g0, cnt, scratch, pre, Grp::block());
       }
     }
   } else {
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
             if (pre_rope) pre.rope = rope_pre;
           }
         }
-        apply_epilogue_k<EPI>(a, Ys, YLD, tile, t0 + g0, cnt, scratch, pre);
+        apply_epilogue_k<EPI>(a, Ys, YLD, tile, t0 + g0, cnt, scratch, pre, Grp::block());
       }
     }
     if (tid == 0) tc::bulk_wait_read();  // the copies have read this CTA's partial tile

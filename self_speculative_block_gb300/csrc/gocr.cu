@@ -31,6 +31,23 @@ struct GraphEntry {
   bool host_loop;  // body only, no device-side while node
 };
 
+// Argument table of the persistent forward for one forward shape.
+struct MkEntry {
+  int kind, n_slots, B;
+  const int* am_out;
+  const float* logits;
+  const int* slot_tab;
+  MkArgs args;
+};
+
+// Every kernel argument of one decoder forward: per layer the QKV, O,
+// gate/up and down GEMMs, then the LM head; per layer the attention.
+struct FwdArgs {
+  int T = 0;
+  std::vector<GemmArgs> g;
+  std::vector<AttnArgs> at;
+};
+
 }  // namespace
 
 void gocr::set_lib_error(const char* msg) { g_lib_error = msg; }
@@ -102,6 +119,21 @@ struct gocr_handle {
   int* pidx = nullptr;
   void* prefix_stage = nullptr;
 
+  // persistent decode forward (bf16 models): counters, split-K partials,
+  // attention partial rows, and per-forward-shape argument tables
+  bool mk_enabled = false;
+  unsigned* mk_ctr = nullptr;
+  size_t mk_ctr_bytes = 0;
+  float* mk_part = nullptr;
+  float* mk_att = nullptr;
+  int mk_T_max = 0;
+  int mk_att_items = 0;
+  int mk_G = 0;
+  int mk_pf = 16;
+  unsigned long long* mk_trace = nullptr;
+  int mk_trace_cap = 0;
+  std::vector<MkEntry> mk_tables;
+
   bool prefilled[MAX_REQ] = {};
   std::vector<GraphEntry> graphs;
   std::string msg;
@@ -170,18 +202,17 @@ void set_norm_in(gocr_handle* h, GemmArgs& a) {
   a.e.eps = h->cfg.rms_eps;
 }
 
-// Enqueue one decoder forward over the rows the plan kernel has laid out.
-// RMSNorm is folded into the GEMMs: producers write resid * g (the next norm's
-// gain) as planes plus per-tile sums of squares; consumers scale by rstd.
-bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out,
-                     float* logits, const int* slot_tab) {
+// Kernel arguments of one decoder forward over the rows the plan kernel lays
+// out.  RMSNorm is folded into the GEMMs: producers write resid * g (the next
+// norm's gain) as planes plus per-tile sums of squares; consumers scale by rstd.
+void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out, float* logits,
+                  const int* slot_tab, FwdArgs& f) {
   const gocr_config& c = h->cfg;
   const int T = n_rows_of(kind, n_slots, B, P);
   const int H = c.hidden;
-  const bool pdl = h->pdl;
-  bool ok = true;
-  launch_embed(h->dtype, h->embed, h->mask, h->prefix_stage, h->resid, h->gattn[0], h->xg_hi, h->xg_lo,
-               h->ssq, h->rows, T, H, c.vocab, h->err, h->hs, pdl);
+  f.T = T;
+  f.g.clear();
+  f.at.clear();
   const size_t kv_es = h->dtype == GOCR_DTYPE_BF16 ? 2 : 4;
   auto lay = [&](void* base, int l) -> void* {
     return base ? (char*)base + (size_t)l * h->layer_stride * kv_es : nullptr;
@@ -198,7 +229,7 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
     g.e.q_dim = h->q_dim; g.e.kv_dim = h->kv_dim; g.e.head_dim = c.head_dim; g.e.cap = h->cap;
     g.e.rope = h->rope;
     g.e.row_pos = h->rows.row_pos; g.e.row_slot = h->rows.row_slot; g.e.plan = h->rows.plan;
-    ok &= launch_gemm(h->dtype, g, h->hs, pdl);
+    f.g.push_back(g);
     // attention with the row key limits of this forward's mask
     AttnArgs at{};
     at.q_hi = h->q_hi; at.q_lo = h->q_lo;
@@ -213,27 +244,26 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
     if (kind != PLAN_PREFILL) at.st = h->st;
     at.T = T; at.Hq = c.n_q_heads; at.Hkv = c.n_kv_heads; at.d = c.head_dim; at.cap = h->cap;
     at.scale = 1.0f / sqrtf((float)c.head_dim);
-    ok &= launch_attention(h->dtype, at, kind == PLAN_PREFILL ? 1 : n_slots,
-                           kind == PLAN_PREFILL ? P : T / n_slots, h->hs, pdl);
+    f.at.push_back(at);
     // O projection + residual; planes of resid * g_mlp for the MLP
     GemmArgs go = gemm_base(h, h->at_hi, h->at_lo, h->q_dim, h->wo[l], T, H, h->q_dim);
     go.epi = EPI_RESID;
     go.e.resid = h->resid; go.e.H = H; go.e.g_next = h->gmlp[l]; go.e.ssq_out = h->ssq;
     go.e.pl_hi = h->xg_hi; go.e.pl_lo = h->xg_lo; go.e.ld_pl = H;
-    ok &= launch_gemm(h->dtype, go, h->hs, pdl);
+    f.g.push_back(go);
     // gate/up (interleaved, input norm) + SwiGLU
     GemmArgs gg = gemm_base(h, h->xg_hi, h->xg_lo, H, h->wgu[l], T, h->gu_n, H);
     set_norm_in(h, gg);
     gg.epi = EPI_SWIGLU;
     gg.e.pl_hi = h->hb_hi; gg.e.pl_lo = h->hb_lo; gg.e.ld_pl = c.ffn;
-    ok &= launch_gemm(h->dtype, gg, h->hs, pdl);
+    f.g.push_back(gg);
     // down + residual; planes of resid * (next layer's g_attn, or the final gain)
     GemmArgs gd = gemm_base(h, h->hb_hi, h->hb_lo, c.ffn, h->wd[l], T, H, c.ffn);
     gd.epi = EPI_RESID;
     gd.e.resid = h->resid; gd.e.H = H; gd.e.ssq_out = h->ssq;
     gd.e.g_next = l + 1 < c.n_layers ? h->gattn[l + 1] : h->gfin;
     gd.e.pl_hi = h->xg_hi; gd.e.pl_lo = h->xg_lo; gd.e.ld_pl = H;
-    ok &= launch_gemm(h->dtype, gd, h->hs, pdl);
+    f.g.push_back(gd);
   }
   // LM head (input norm) + argmax over the rows that need logits
   const int n_logit = kind == PLAN_PREFILL ? n_slots : T;
@@ -245,7 +275,155 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
   gl.epi = EPI_ARGMAX;
   gl.e.logits = logits; gl.e.ld_logits = c.vocab;
   gl.e.amax = h->amax; gl.e.am_out = am_out; gl.e.grid_ctr = h->grid_ctr;
-  ok &= launch_gemm(h->dtype, gl, h->hs, pdl);
+  f.g.push_back(gl);
+}
+
+// Whether the persistent kernel runs this forward, and its launch arguments
+// (without the device tables).
+bool mk_shape(gocr_handle* h, int kind, int n_slots, int B, MkArgs& a) {
+  const gocr_config& c = h->cfg;
+  if (!h->mk_enabled || h->dtype != GOCR_DTYPE_BF16 || kind == PLAN_PREFILL) return false;
+  const int T = n_rows_of(kind, n_slots, B, 0);
+  if (T < 1 || T > h->mk_T_max || T % n_slots) return false;
+  const int CL = attention_cluster_width(c.head_dim);
+  if (!forward_mk_fits(c.head_dim, CL)) return false;
+  a = MkArgs{};
+  a.L = c.n_layers;
+  a.T = T;
+  a.nt = (T + 15) / 16 * 16;
+  a.n_slots = n_slots;
+  a.rows_per_slot = T / n_slots;
+  const int G = c.n_q_heads / c.n_kv_heads;
+  a.n_rg = (a.rows_per_slot * G + 63) / 64;
+  a.Hkv = c.n_kv_heads;
+  a.CL = CL;
+  a.G = h->mk_G;
+  const int NK[5][2] = {{h->qkv_n, c.hidden}, {c.hidden, h->q_dim}, {h->gu_n, c.hidden}, {c.hidden, c.ffn},
+                        {c.vocab, c.hidden}};
+  for (int k = 0; k < 5; ++k) {
+    a.N[k] = NK[k][0];
+    a.K[k] = NK[k][1];
+    if (a.N[k] % NTILE || a.K[k] % 64) return false;
+    a.tiles[k] = a.N[k] / NTILE;
+    a.splits[k] = gemm_splits(a.N[k], a.K[k]);
+    a.kchunk[k] = gemm_kchunk(a.N[k], a.K[k]);
+    // split tiles need a completion counter each
+    if (a.splits[k] > 16 || ((k < 4 || a.splits[k] > 1) && a.tiles[k] > mk::MAXT)) return false;
+  }
+  a.n_items[0] = a.tiles[0] * a.splits[0];
+  a.n_items[1] = n_slots * a.Hkv * a.n_rg * CL;
+  a.n_items[2] = a.tiles[1] * a.splits[1];
+  a.n_items[3] = a.tiles[2] * a.splits[2];
+  a.n_items[4] = a.tiles[3] * a.splits[3];
+  if (a.n_items[1] > h->mk_att_items || a.n_items[1] / CL > mk::MAXT) return false;
+  int acc = 0;
+  for (int k = 0; k < 5; ++k) {
+    a.prefix[k] = acc;
+    acc += a.n_items[k];
+  }
+  a.per_layer = acc;
+  // ring depths: as many weight stages as fit next to the activation stages
+  const int ast = 2 * a.nt * 128;
+  // (2 KB of the 227 KB per CTA stay for the kernel's static shared memory)
+  const size_t cap = 227 * 1024 - 2048;
+  int ws = 0;
+  for (a.as_stages = a.nt <= 64 ? 6 : 3; a.as_stages >= 2; --a.as_stages) {
+    const size_t fixed = forward_mk_smem(a.nt, 0, a.as_stages);
+    ws = fixed < cap ? (int)((cap - fixed) / (NTILE * 64 * 2 + 16)) : 0;
+    if (ws >= 4) break;
+  }
+  if (ws < 2) return false;
+  if (ws > 12) ws = 12;
+  a.ws_stages = ws;
+  (void)ast;
+  a.pf_blocks = h->mk_pf;
+  a.trace = h->mk_trace;
+  a.trace_cap = h->mk_trace_cap;
+  a.ctr = h->mk_ctr;
+  a.part = h->mk_part;
+  a.att_part = h->mk_att;
+  a.err = h->err;
+  return forward_mk_smem(a.nt, a.ws_stages, a.as_stages) <= cap;
+}
+
+MkEntry* mk_find(gocr_handle* h, int kind, int n_slots, int B, const int* am_out, const float* logits,
+                 const int* slot_tab) {
+  for (auto& e : h->mk_tables)
+    if (e.kind == kind && e.n_slots == n_slots && e.B == B && e.am_out == am_out && e.logits == logits &&
+        e.slot_tab == slot_tab)
+      return &e;
+  return nullptr;
+}
+
+// Builds (once) the device tables of the persistent forward for this shape.
+// Not during stream capture: it allocates and copies synchronously.
+int mk_prepare(gocr_handle* h, int kind, int n_slots, int B, int* am_out, float* logits, const int* slot_tab) {
+  MkArgs a;
+  if (!mk_shape(h, kind, n_slots, B, a)) return GOCR_OK;
+  if (mk_find(h, kind, n_slots, B, am_out, logits, slot_tab)) return GOCR_OK;
+  FwdArgs f;
+  forward_args(h, kind, n_slots, B, 0, am_out, logits, slot_tab, f);
+  const int L = h->cfg.n_layers;
+  const size_t n_maps = 4 * (size_t)L + 1 + 6;
+  const size_t off_g = 0;
+  const size_t off_a = (off_g + f.g.size() * sizeof(GemmArgs) + 255) & ~(size_t)255;
+  const size_t off_m = (off_a + f.at.size() * sizeof(AttnArgs) + 255) & ~(size_t)255;
+  const size_t bytes = off_m + n_maps * 128;
+  std::vector<unsigned char> blob(bytes, 0);
+  memcpy(blob.data() + off_g, f.g.data(), f.g.size() * sizeof(GemmArgs));
+  memcpy(blob.data() + off_a, f.at.data(), f.at.size() * sizeof(AttnArgs));
+  unsigned char* maps = blob.data() + off_m;
+  bool ok = true;
+  for (int l = 0; l <= L; ++l) {
+    for (int k = 0; k < (l < L ? 4 : 1); ++k) {
+      const GemmArgs& g = f.g[(size_t)l * 4 + k];
+      ok &= encode_tmap_bf16(maps + ((size_t)l * 4 + k) * 128, g.w, g.N, g.K, NTILE);
+    }
+  }
+  const gocr_config& c = h->cfg;
+  const void* act[6] = {h->xg_hi, h->xg_lo, h->at_hi, h->at_lo, h->hb_hi, h->hb_lo};
+  const int cols[3] = {c.hidden, h->q_dim, c.ffn};
+  for (int i = 0; i < 6; ++i)
+    ok &= encode_tmap_bf16(maps + (4 * (size_t)L + 1 + i) * 128, act[i], a.T, cols[i / 2], a.nt);
+  if (!ok) return GOCR_OK;  // no TMA descriptor: the per-operation kernels run this shape
+  void* dev = dev_alloc(h, bytes);
+  if (!dev) return fail(h, GOCR_ENOMEM, "device allocation failed");
+  CK(cudaMemcpyAsync(dev, blob.data(), bytes, cudaMemcpyHostToDevice, h->hs));
+  CK(cudaStreamSynchronize(h->hs));
+  a.gemm = reinterpret_cast<const GemmArgs*>((char*)dev + off_g);
+  a.att = reinterpret_cast<const AttnArgs*>((char*)dev + off_a);
+  a.maps = (char*)dev + off_m;
+  MkEntry e{kind, n_slots, B, am_out, logits, slot_tab, a};
+  h->mk_tables.push_back(e);
+  return GOCR_OK;
+}
+
+// Enqueue one decoder forward over the rows the plan kernel has laid out:
+// the embedding rows, then either the persistent forward (decode shapes of
+// bf16 models whose tables mk_prepare built) or one kernel per operation.
+bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out,
+                     float* logits, const int* slot_tab) {
+  const gocr_config& c = h->cfg;
+  const int T = n_rows_of(kind, n_slots, B, P);
+  const int H = c.hidden;
+  const bool pdl = h->pdl;
+  bool ok = true;
+  launch_embed(h->dtype, h->embed, h->mask, h->prefix_stage, h->resid, h->gattn[0], h->xg_hi, h->xg_lo,
+               h->ssq, h->rows, T, H, c.vocab, h->err, h->hs, pdl);
+  if (h->mk_enabled)
+    if (const MkEntry* e = mk_find(h, kind, n_slots, B, am_out, logits, slot_tab))
+      return launch_forward_mk(e->args, c.head_dim, h->hs, pdl);
+  FwdArgs f;
+  forward_args(h, kind, n_slots, B, P, am_out, logits, slot_tab, f);
+  for (int l = 0; l < c.n_layers; ++l) {
+    ok &= launch_gemm(h->dtype, f.g[(size_t)l * 4 + 0], h->hs, pdl);
+    ok &= launch_attention(h->dtype, f.at[l], kind == PLAN_PREFILL ? 1 : n_slots,
+                           kind == PLAN_PREFILL ? P : T / n_slots, h->hs, pdl);
+    ok &= launch_gemm(h->dtype, f.g[(size_t)l * 4 + 1], h->hs, pdl);
+    ok &= launch_gemm(h->dtype, f.g[(size_t)l * 4 + 2], h->hs, pdl);
+    ok &= launch_gemm(h->dtype, f.g[(size_t)l * 4 + 3], h->hs, pdl);
+  }
+  ok &= launch_gemm(h->dtype, f.g[(size_t)c.n_layers * 4], h->hs, pdl);
   return ok;
 }
 
@@ -389,8 +567,18 @@ int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const in
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
   launch_begin_decode(h->st, h->slot_req, n, h->max_new_dev, bound + 2, c.eos_id, h->hs);
   CK(cudaGetLastError());
+  int rc = GOCR_OK;
+  if (mode == GOCR_MODE_AR) {
+    rc = mk_prepare(h, PLAN_AR, n, 0, h->abuf, nullptr, h->slot_req);
+  } else {
+    rc = mk_prepare(h, PLAN_DRAFT, n, B, h->dbuf, nullptr, h->slot_req);
+    if (!rc) rc = mk_prepare(h, PLAN_VERIFY, n, B, h->vbuf, nullptr, h->slot_req);
+  }
+  if (rc) return rc;
+  if (h->mk_ctr) CK(cudaMemsetAsync(h->mk_ctr, 0, h->mk_ctr_bytes, h->hs));
+  if (h->mk_trace) CK(cudaMemsetAsync(h->mk_trace, 0, (size_t)h->mk_G * 2 * h->mk_trace_cap * 16, h->hs));
   cudaGraphExec_t exec;
-  int rc = get_graph(h, mode, B, n, &exec);
+  rc = get_graph(h, mode, B, n, &exec);
   if (rc) return rc;
   CK(cudaEventRecord(h->ev0, h->hs));
   if (!h->host_loop) {
@@ -578,6 +766,34 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->ws = (float*)A(wsf * 4);
     h->counters = (int*)A((size_t)ctr * 4);
   }
+  if (h->dtype == GOCR_DTYPE_BF16) {
+    // persistent decode forward: decode shapes of up to 128 rows
+    const char* fw = getenv("GOCR_FORWARD");
+    h->mk_enabled = fw && strcmp(fw, "persistent") == 0;
+    const char* pf = getenv("GOCR_MK_PREFETCH");
+    if (pf) h->mk_pf = atoi(pf) < 0 ? 0 : atoi(pf);
+    int dev = 0;
+    CKC(cudaGetDevice(&dev));
+    CKC(cudaDeviceGetAttribute(&h->mk_G, cudaDevAttrMultiProcessorCount, dev));
+    h->mk_T_max = h->T_dec < 128 ? h->T_dec : 128;
+    const int NK[5][2] = {{h->qkv_n, H}, {H, q_dim}, {h->gu_n, H}, {H, c.ffn}, {c.vocab, H}};
+    size_t part = 0;
+    for (auto& nk : NK) {
+      const int sp = gemm_splits(nk[0], nk[1]);
+      const size_t f = sp > 1 ? (size_t)sp * nk[0] : 0;  // partial tiles of split GEMMs only
+      if (f > part) part = f;
+    }
+    h->mk_part = (float*)A(part * h->mk_T_max * 4);
+    h->mk_att_items = 1024;
+    h->mk_att = (float*)A((size_t)h->mk_att_items * 64 * (c.head_dim + 4) * 4);
+    h->mk_ctr_bytes = mk::ctr_words(c.n_layers) * 4;
+    h->mk_ctr = (unsigned*)A(h->mk_ctr_bytes);
+    const char* tr = getenv("GOCR_MK_TRACE");
+    if (tr && atoi(tr) > 0) {
+      h->mk_trace_cap = atoi(tr) > 4096 ? 4096 : atoi(tr);
+      h->mk_trace = (unsigned long long*)A((size_t)h->mk_G * 2 * h->mk_trace_cap * 16);
+    }
+  }
   if (!ok) {
     int r = fail(h, GOCR_ENOMEM, "device allocation failed");
     g_lib_error = h->msg;
@@ -684,6 +900,9 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
   CK(cudaMemcpyAsync(h->dbg_toks, tokens, sizeof(int) * n, cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
+  if ((r = mk_prepare(h, pk, 1, B, h->am, h->logits, h->slot_one))) return r;
+  if (h->mk_ctr) CK(cudaMemsetAsync(h->mk_ctr, 0, h->mk_ctr_bytes, h->hs));
+  if (h->mk_trace) CK(cudaMemsetAsync(h->mk_trace, 0, (size_t)h->mk_G * 2 * h->mk_trace_cap * 16, h->hs));
   launch_plan(pk, h->rows, h->st, h->slot_one, 1, B, 0, nullptr, h->dbg_toks, h->cap, h->hs, false);
   if (!enqueue_forward(h, pk, 1, B, 0, h->am, h->logits, h->slot_one))
     return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
@@ -744,6 +963,59 @@ int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0) {
   if ((r = read_state(h, req, &s))) return r;
   if (cache_len) *cache_len = s.cache_len;
   if (x0) *x0 = s.x0;
+  return GOCR_OK;
+}
+
+int gocr_set_option(gocr_handle* h, int option, int value) {
+  if (!h) return fail(nullptr, GOCR_EINVAL, "null handle");
+  if (option != GOCR_OPT_FORWARD) return fail(h, GOCR_EINVAL, "unknown option %d", option);
+  if (value != GOCR_FORWARD_PERSISTENT && value != GOCR_FORWARD_OPS) return fail(h, GOCR_EINVAL, "bad value %d", value);
+  const bool en = value == GOCR_FORWARD_PERSISTENT && h->mk_ctr != nullptr;
+  if (en == h->mk_enabled) return GOCR_OK;
+  CK(cudaStreamSynchronize(h->hs));
+  for (auto& g : h->graphs) {
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+  }
+  h->graphs.clear();
+  h->mk_enabled = en;
+  return GOCR_OK;
+}
+
+int gocr_get_option(const gocr_handle* h, int option, int* value) {
+  if (!h || !value) return fail(nullptr, GOCR_EINVAL, "null argument");
+  if (option == GOCR_OPT_FORWARD) {
+    *value = h->mk_enabled ? GOCR_FORWARD_PERSISTENT : GOCR_FORWARD_OPS;
+    return GOCR_OK;
+  }
+  if (option == GOCR_OPT_PERSISTENT_FORWARDS) {
+    unsigned e = 0;
+    if (h->mk_ctr) {
+      if (cudaStreamSynchronize(h->hs) != cudaSuccess ||
+          cudaMemcpy(&e, h->mk_ctr + mk::CTR_EPOCH, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GOCR_ECUDA;
+    }
+    *value = (int)e;
+    return GOCR_OK;
+  }
+  if (option == GOCR_OPT_TRACE_RECORDS) {
+    *value = h->mk_trace ? h->mk_trace_cap : 0;
+    return GOCR_OK;
+  }
+  if (option == GOCR_OPT_GRID_CTAS) {
+    *value = h->mk_G;
+    return GOCR_OK;
+  }
+  return GOCR_EINVAL;
+}
+
+int gocr_read_trace(gocr_handle* h, uint64_t* out, size_t n_words) {
+  if (!h || !out) return fail(h, GOCR_EINVAL, "null argument");
+  if (!h->mk_trace) return fail(h, GOCR_ESTATE, "tracing is off (GOCR_MK_TRACE)");
+  const size_t words = (size_t)h->mk_G * 2 * h->mk_trace_cap * 2;
+  if (n_words < words) return fail(h, GOCR_ECAPACITY, "trace needs %zu words", words);
+  CK(cudaStreamSynchronize(h->hs));
+  CK(cudaMemcpy(out, h->mk_trace, words * 8, cudaMemcpyDeviceToHost));
   return GOCR_OK;
 }
 

@@ -61,7 +61,7 @@ struct EpiArgs {
   int* err;                      // device error word
 };
 
-struct GemmArgs {
+struct alignas(16) GemmArgs {  // 16-byte aligned: tables of them are copied by 16-byte loads
   const void* x; const void* x_lo; int ldx;  // [T, K] planes (x_lo NULL: single plane)
   const void* w;                 // [N, K] dtype
   int T, N, K;
@@ -79,12 +79,15 @@ struct GemmArgs {
 bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s, bool pdl);
 bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl);
 int gemm_splits(int N, int K);
+// 128-byte-swizzled TMA descriptor (CUtensorMap, 128 bytes at `out`) of a
+// row-major bf16 matrix [rows, cols] with boxes of 64 columns x box_rows.
+bool encode_tmap_bf16(void* out, const void* ptr, int rows, int cols, int box_rows);
 int gemm_kchunk(int N, int K);
 size_t gemm_ws_floats(int T, int N, int K);
 int gemm_counter_ints(int T, int N);
 
 // ---------------------------------------------------------------- attention
-struct AttnArgs {
+struct alignas(16) AttnArgs {
   // q [T, Hq, d] and the KV cache [Hkv][cap][d] of request 0 at this layer, as
   // planes: bf16 hi + lo (bf16 models) or fp32 in *_hi (fp32 models)
   const void* q_hi; const void* q_lo;
@@ -100,9 +103,56 @@ struct AttnArgs {
   int T, Hq, Hkv, d, cap;
   float scale;
 };
+// Cluster width of the tensor-core attention kernel for head dim d (16 or 8),
+// fixed once per process: it decides which tile reads which key chunk and the
+// order of the merge.
+int attention_cluster_width(int d);
 // dtype 1: tensor-core cluster kernel; 0: CUDA-core kernel.
 bool launch_attention(int dtype, const AttnArgs& a, int n_slots, int max_rows_per_slot, cudaStream_t s,
                       bool pdl);
+
+// ---------------------------------------------------------------- persistent decode forward
+// One kernel runs a whole decode forward (every layer's QKV, attention, O,
+// gate/up, down, then the LM head) on one CTA per SM, with the same
+// arithmetic as the per-operation kernels above (forward_mk.cu).
+namespace mk {
+constexpr int MAXT = 128;        // tile counters per phase
+constexpr int CTR_EPOCH = 0, CTR_DONE = 1, CTR_ABORT = 2, CTR_PHASE = 4;
+// phases: layer l has QKV, ATT, O, GU, DN at 5 l + 0..4; the LM head is 5 L
+__host__ __device__ inline int tile_ctr_base(int L) { return ((CTR_PHASE + 5 * L + 1 + 31) / 32) * 32; }
+__host__ __device__ inline size_t ctr_words(int L) { return (size_t)tile_ctr_base(L) + (size_t)(5 * L + 1) * MAXT; }
+}  // namespace mk
+
+struct MkArgs {
+  const GemmArgs* gemm;    // device [4 L + 1]: per layer QKV, O, GU, DN; then the LM head
+  const AttnArgs* att;     // device [L]
+  const void* maps;        // device CUtensorMap [4 L + 1] weights (same order), then 6 activation maps:
+                           // GEMM-input planes hi/lo, attention-output planes hi/lo, SwiGLU planes hi/lo
+  unsigned* ctr;           // device counters, mk::ctr_words(L) words, zero at the first forward
+  float* part;             // split-K partial tiles [S][T][N] of the running phase
+  float* att_part;         // attention partial rows [group][CL][64][D + 4]
+  int* err;
+  int L, T, nt, n_slots, rows_per_slot, n_rg, Hkv, CL;
+  int G;                   // CTAs (one per SM)
+  int ws_stages, as_stages, pf_blocks;
+  int N[5], K[5], tiles[5], splits[5], kchunk[5];  // per GEMM kind: QKV, O, GU, DN, LM
+  int n_items[5];          // per phase kind: QKV, ATT, O, GU, DN
+  int prefix[5];           // items of the earlier phase kinds of a layer
+  int per_layer;           // items of one layer
+  // optional event trace: [G][2 writers][trace_cap] records of two words
+  // (globaltimer ns, phase << 8 | event); NULL = off
+  unsigned long long* trace;
+  int trace_cap;
+};
+namespace mk {
+// trace events
+enum : int { EV_START = 0, EV_DEP = 1, EV_ACC = 2, EV_DRAINED = 3, EV_FIXED = 4, EV_ATT_READY = 5,
+             EV_ATT_PART = 6, EV_ATT_MERGED = 7, EV_END = 8 };
+}
+// Shared-memory bytes and launch check; false when the shapes do not fit.
+size_t forward_mk_smem(int nt, int ws_stages, int as_stages);
+bool forward_mk_fits(int head_dim, int CL);
+bool launch_forward_mk(const MkArgs& a, int head_dim, cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------- small kernels
 void launch_embed(int dtype, const void* embed, const void* mask_embed, const void* prefix,

@@ -24,13 +24,15 @@ ERRORS = {-1: "EINVAL", -2: "ECAPACITY", -3: "ECUDA", -4: "EDEVICE", -5: "ETIMEO
 DTYPE_F32, DTYPE_BF16 = 0, 1
 MODE_AR, MODE_SELFSPEC = 0, 1
 FWD_AR, FWD_DRAFT, FWD_VERIFY = 0, 1, 2
+OPT_FORWARD, OPT_PERSISTENT_FORWARDS, OPT_TRACE_RECORDS, OPT_GRID_CTAS = 1, 2, 3, 4
+FORWARD_PERSISTENT, FORWARD_OPS = 0, 1
 MAX_BLOCK = 64
 LAYER_TENSORS = 9
 
 # every symbol include/gocr.h declares
 EXPORTS = ("gocr_create", "gocr_prefill", "gocr_decode", "gocr_decode_batch",
            "gocr_set_draft_override", "gocr_debug_forward", "gocr_read_kv", "gocr_get_state",
-           "gocr_last_error", "gocr_free", "gocr_op_linear_workspace", "gocr_op_linear",
+           "gocr_set_option", "gocr_get_option", "gocr_read_trace", "gocr_last_error", "gocr_free", "gocr_op_linear_workspace", "gocr_op_linear",
            "gocr_op_attention", "gocr_op_linear_static")
 
 
@@ -96,6 +98,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gocr_debug_forward": (i32, [vp, i32, i32, P32, i32, ctypes.POINTER(ctypes.c_float)]),
         "gocr_read_kv": (i32, [vp, i32, i32, i32, i32, vp, vp]),
         "gocr_get_state": (i32, [vp, i32, P32, P32]),
+        "gocr_set_option": (i32, [vp, i32, i32]),
+        "gocr_read_trace": (i32, [vp, vp, sz]),
+        "gocr_get_option": (i32, [vp, i32, P32]),
         "gocr_last_error": (ctypes.c_char_p, [vp]),
         "gocr_free": (None, [vp]),
         "gocr_op_linear_workspace": (sz, [i32, i32, i32]),
@@ -279,6 +284,34 @@ class Decoder:
         v = np.zeros(shape, np.float32)
         _check(self.lib.gocr_read_kv(self.h, req, layer, pos0, n, k.ctypes.data, v.ctypes.data), self.h)
         return k, v
+
+    def set_forward_path(self, path: int) -> None:
+        """FORWARD_PERSISTENT (one kernel per decode forward) or FORWARD_OPS."""
+        _check(self.lib.gocr_set_option(self.h, OPT_FORWARD, path), self.h)
+
+    def forward_path(self) -> int:
+        v = ctypes.c_int32()
+        _check(self.lib.gocr_get_option(self.h, OPT_FORWARD, ctypes.byref(v)), self.h)
+        return v.value
+
+    def persistent_forwards(self) -> int:
+        """Forwards the persistent kernel completed in the last decode or debug forward."""
+        v = ctypes.c_int32()
+        _check(self.lib.gocr_get_option(self.h, OPT_PERSISTENT_FORWARDS, ctypes.byref(v)), self.h)
+        return v.value
+
+    def _option(self, opt: int) -> int:
+        v = ctypes.c_int32()
+        _check(self.lib.gocr_get_option(self.h, opt, ctypes.byref(v)), self.h)
+        return v.value
+
+    def read_trace(self) -> np.ndarray:
+        """Event trace of the last persistent forward: uint64 [CTAs, 2, records, 2]
+        (writer 0: activation producer, 1: compute group; (ns, phase << 8 | event))."""
+        G, cap = self._option(OPT_GRID_CTAS), self._option(OPT_TRACE_RECORDS)
+        out = np.zeros((G, 2, cap, 2), np.uint64)
+        _check(self.lib.gocr_read_trace(self.h, out.ctypes.data, out.size), self.h)
+        return out
 
     def state(self, req: int):
         cl = ctypes.c_int32()
