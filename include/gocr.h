@@ -185,16 +185,27 @@ enum { GOCR_FORWARD_PERSISTENT = 0, GOCR_FORWARD_OPS = 1 };
 int gocr_set_option(gocr_handle* h, int option, int value);
 int gocr_get_option(const gocr_handle* h, int option, int* value);
 
-/* Event trace of the last persistent forward (a profiling aid; tracing must
- * be on, see GOCR_OPT_TRACE_RECORDS).  out: host, n_words >= CTAs * 2 *
- * records * 2 words, laid out [CTA][writer][record][2]: writer 0 is the
- * activation producer, writer 1 the compute group; a record is (globaltimer
- * ns, phase << 8 | event), zero past the last record.  Phases: layer l has
- * QKV, attention, O, gate/up, down at 5 l + 0..4, the LM head is 5 L.
- * Events: 0 start, 1 input ready, 2 accumulator ready, 3 partial tile
- * written, 4 tile finished, 5 attention inputs ready, 6 attention partial
- * rows written, 7 attention rows merged, 8 end.  GOCR_ESTATE when off. */
-int gocr_read_trace(gocr_handle* h, uint64_t* out, size_t n_words);
+/* Timelines of the last debug forward (profiling aids; GOCR_ESTATE when the
+ * trace is off).  out: host, at least n_words words.
+ *   GOCR_TRACE_PERSISTENT  events of the persistent forward (on when the
+ *     environment variable GOCR_MK_TRACE=<records> is set at create time):
+ *     n_words >= CTAs * 2 * records * 2, laid out [CTA][writer][record][2];
+ *     writer 0 is the activation producer, writer 1 the compute group; a
+ *     record is (globaltimer ns, phase << 8 | event), zero past the last
+ *     record.  Phases: layer l has QKV, attention, O, gate/up, down at
+ *     5 l + 0..4, the LM head is 5 L.  Events: 0 start, 1 input ready,
+ *     2 accumulator ready, 3 partial tile written, 4 tile finished,
+ *     5 attention inputs ready, 6 attention partial rows written,
+ *     7 attention rows merged, 8 end.
+ *   GOCR_TRACE_KERNELS  one record per launch of a debug forward run with
+ *     one kernel per operation (on with GOCR_OP_TRACE=1): n_words >=
+ *     8 * (5 * n_layers + 1), laid out [launch][8] in forward order (per
+ *     layer QKV, attention, O, gate/up, down; then the LM head); a record is
+ *     (first CTA start, first and last release from the dependency wait,
+ *     last CTA end, last mainloop end, last split-K exchange end, 0, 0),
+ *     globaltimer ns (the last two marks for GEMMs only). */
+enum { GOCR_TRACE_PERSISTENT = 0, GOCR_TRACE_KERNELS = 1 };
+int gocr_read_trace(gocr_handle* h, int which, uint64_t* out, size_t n_words);
 
 /* Last error message of the handle (or of the library when h is NULL). */
 const char* gocr_last_error(const gocr_handle* h);

@@ -138,8 +138,12 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
 
 // One CTA per (cluster rank, kv head x row group, slot) tile; the cluster's
 // CL tiles split the key chunks and merge over distributed shared memory.
-template <int D, int CL>
-__global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
+// At most 128 registers a thread: one attention CTA (32 K registers) and two
+// GEMM CTAs of the next kernels then fit one SM's register file together, so
+// under programmatic dependent launch those CTAs become resident, and start
+// their weight loads, while attention still runs.
+template <int D, int CL, bool TRACE>
+__global__ void __launch_bounds__(256, 2) attention_mma_kernel(AttnArgs a) {
   namespace cg = cooperative_groups;
   using Gm = attn::Geo<D>;
   constexpr int RLD = Gm::RLD;
@@ -161,6 +165,7 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
   const int tid = threadIdx.x;
 
   if (tid == 0) {
+    if (TRACE) trace_mark(a.trace, 0);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     tc::mbar_init(&rxbar, 1);
     tc::fence_mbar_init();
@@ -176,6 +181,7 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
                                      tid);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (TRACE && tid == 0) trace_mark(a.trace, 1);
 
   int req = 0, row0 = 0, nrows = a.T;
   if (a.rows_per_slot > 0) {
@@ -192,8 +198,8 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
     attn::cp_async_wait<0>();
     return;
   }
-  attn::tile_partial<D, CL>(a, sm_raw, grp, attn::kv_planes(a, req, kvh, D), rank, kvh, qr0, row0, nrows, pre,
-                            &s_maxlim);
+  attn::tile_partial<D, CL, TRACE>(a, sm_raw, grp, attn::kv_planes(a, req, kvh, D), rank, kvh, qr0, row0, nrows,
+                                   pre, &s_maxlim);
   float* ST = attn::staged_rows<D>(sm_raw);
   tc::fence_proxy_async_smem();
   __syncthreads();
@@ -205,9 +211,11 @@ __global__ void __launch_bounds__(256) attention_mma_kernel(AttnArgs a) {
     tc::bulk_commit();
   }
   const bool rx_ok = tc::mbar_wait(&rxbar, 0);
+  if (TRACE && tid == 0) trace_mark(a.trace, 6);
   auto row = [&](int c, int i) -> const float* { return RX + (c * RPC + i) * RLD; };
   attn::merge_owned<D, CL>(a, grp, row, WS, IL, rank, kvh, qr0, row0, nrows, rx_ok);
   if (tid == 0) tc::bulk_wait_read();  // the copies have read this CTA's staged rows
+  if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 
 template <int D, int CL>
@@ -216,7 +224,7 @@ static size_t attn_mma_smem() {
   return attn::Geo<D>::TILE_SMEM + ((size_t)CL * RPC * RLD + RPC * CL + RPC) * 4;
 }
 
-template <int D, int CL>
+template <int D, int CL, bool TRACE>
 static cudaError_t launch_attn_cl(const AttnArgs& a, dim3 grid, cudaStream_t s, bool pdl) {
   const size_t smem = attn_mma_smem<D, CL>();
   cudaLaunchConfig_t cfg{};
@@ -233,7 +241,21 @@ static cudaError_t launch_attn_cl(const AttnArgs& a, dim3 grid, cudaStream_t s, 
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, attention_mma_kernel<D, CL>, a);
+  return cudaLaunchKernelEx(&cfg, attention_mma_kernel<D, CL, TRACE>, a);
+}
+
+// Kernel attributes of one cluster width (both trace instantiations).
+template <int D, int CL>
+static bool attn_configure() {
+  const int smem = (int)attn_mma_smem<D, CL>();
+  bool ok = true;
+  for (const void* fn : {reinterpret_cast<const void*>(attention_mma_kernel<D, CL, false>),
+                         reinterpret_cast<const void*>(attention_mma_kernel<D, CL, true>)}) {
+    prefer_shared(fn);
+    if (CL > 8) ok &= cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    ok &= cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
+  }
+  return ok;
 }
 
 // Cluster width: 16 CTAs when the device keeps the eight 16-CTA clusters of
@@ -246,17 +268,11 @@ static int attn_cluster_width() {
   static int width = 0;
   if (width) return width;
   width = 8;
-  prefer_shared(reinterpret_cast<const void*>(attention_mma_kernel<D, 16>));
-  prefer_shared(reinterpret_cast<const void*>(attention_mma_kernel<D, 8>));
-  const size_t smem16 = attn_mma_smem<D, 16>();
-  if (cudaFuncSetAttribute(attention_mma_kernel<D, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-          cudaSuccess &&
-      cudaFuncSetAttribute(attention_mma_kernel<D, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem16) ==
-          cudaSuccess) {
+  if (attn_configure<D, 16>()) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(16, 1, 1);
     cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = smem16;
+    cfg.dynamicSmemBytes = attn_mma_smem<D, 16>();
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 16;
@@ -265,12 +281,11 @@ static int attn_cluster_width() {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attention_mma_kernel<D, 16>, &cfg) == cudaSuccess && n >= 8) width = 16;
+    if (cudaOccupancyMaxActiveClusters(&n, attention_mma_kernel<D, 16, false>, &cfg) == cudaSuccess && n >= 8)
+      width = 16;
   }
   cudaGetLastError();
-  if (width == 8)
-    cudaFuncSetAttribute(attention_mma_kernel<D, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)attn_mma_smem<D, 8>());
+  if (width == 8) attn_configure<D, 8>();
   return width;
 }
 
@@ -282,8 +297,12 @@ static bool launch_attn_mma(const AttnArgs& a, int n_slots, int max_rows, cudaSt
   const int n_rg = (max_rows * G + attn::QR - 1) / attn::QR;
   const int cl = attn_cluster_width<D>();
   const dim3 grid(cl, a.Hkv * n_rg, n_slots);
-  return (cl == 16 ? launch_attn_cl<D, 16>(a, grid, s, pdl) : launch_attn_cl<D, 8>(a, grid, s, pdl)) ==
-         cudaSuccess;
+  cudaError_t e;
+  if (a.trace)
+    e = cl == 16 ? launch_attn_cl<D, 16, true>(a, grid, s, pdl) : launch_attn_cl<D, 8, true>(a, grid, s, pdl);
+  else
+    e = cl == 16 ? launch_attn_cl<D, 16, false>(a, grid, s, pdl) : launch_attn_cl<D, 8, false>(a, grid, s, pdl);
+  return e == cudaSuccess;
 }
 
 template <int D>

@@ -140,7 +140,8 @@ __device__ __forceinline__ float* staged_rows(uint8_t* sm) {
   return reinterpret_cast<float*>(sm + Geo<D>::Q_BYTES);
 }
 
-template <int D, int CL>
+// TRACE: record timeline marks in a.trace (first chunk ready, loop done).
+template <int D, int CL, bool TRACE = false>
 __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, const KvPlanes& kv, int rank, int kvh,
                              int qr0, int row0, int nrows, bool pre, int* s_maxlim) {
   using Gm = Geo<D>;
@@ -215,6 +216,7 @@ __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, con
     const bool next = c + CL < n_chunks;
     if (it == 0) cp_async_wait<0>(); else cp_async_wait<1>();  // this chunk's K (and Q, first chunk)
     grp.sync();
+    if (TRACE && it == 0 && tid == 0) trace_mark(a.trace, 4);
     // S = Q K^T for this warp's 16 rows and 16 keys
     float sacc[2][4];
 #pragma unroll
@@ -320,6 +322,7 @@ __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, con
   }
   cp_async_wait<0>();
   grp.sync();
+  if (TRACE && tid == 0) trace_mark(a.trace, 5);
   // merge the two key halves of this tile: half 0 + half 1, in that order
   if (kh == 1) {
 #pragma unroll

@@ -58,7 +58,7 @@ __device__ __forceinline__ float row_rstd(const EpiArgs& e, int row) {
   const float* p = e.ssq_in + (size_t)row * e.n_ssq;
   float v[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = i < e.n_ssq ? __ldcg(p + i) : 0.f;
+  for (int i = 0; i < 32; ++i) v[i] = i < e.n_ssq ? p[i] : 0.f;
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < 32; ++i)
@@ -86,9 +86,9 @@ struct EpiPre {
 // Epilogue EPI of tokens t0 .. t0+tn-1.  Every pass first issues all of its
 // global loads (sums of squares, residual rows) into shared memory, so a pass
 // costs one memory round trip rather than one per token; inputs in `pre`
-// (tn <= EPI_GROUP) are not fetched again.  Those loads bypass L1: inside a
-// persistent kernel other CTAs rewrite the residual and the sums between two
-// epilogues that run on one SM.  The kind is a template argument
+// (tn <= EPI_GROUP) are not fetched again.  The loads here are plain (L1
+// cached): a kernel that runs an epilogue on data other CTAs of the same
+// kernel wrote must pass those inputs in `pre`.  The kind is a template argument
 // so that a kernel carries only its own epilogue code.
 template <int EPI>
 __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int ys_ld, int tile, int t0, int tn,
@@ -111,12 +111,12 @@ __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int 
       for (int x = tid; x < gn * e.n_ssq; x += grp.n) {
         const int tl = x / e.n_ssq, i = x % e.n_ssq;
         const int row = e.in_rows ? e.in_rows[t0 + g0 + tl] : t0 + g0 + tl;
-        sq[tl * e.n_ssq + i] = __ldcg(e.ssq_in + (size_t)row * e.n_ssq + i);
+        sq[tl * e.n_ssq + i] = e.ssq_in[(size_t)row * e.n_ssq + i];
       }
     if (load_rr)
       for (int x = tid; x < gn * NTILE; x += grp.n) {
         const int tl = x / NTILE, c = x % NTILE;
-        rr_s[x] = __ldcg(e.resid + (size_t)(t0 + g0 + tl) * e.H + n0 + c);
+        rr_s[x] = e.resid[(size_t)(t0 + g0 + tl) * e.H + n0 + c];
       }
     if (load_rs || load_rr) grp.sync();
     if (load_rs) {

@@ -46,7 +46,6 @@ constexpr int THREADS = 384;
 constexpr int W_BYTES = NTILE * 64 * 2;     // one 128 x 64 bf16 weight tile
 constexpr int EG = 32;                      // tokens per epilogue pass
 constexpr int YLD = NTILE + 4;              // fp32 row stride of reduced rows
-constexpr int MAX_SPLIT = 16;
 constexpr int D = 128;                      // head dim of the attention tiles
 constexpr unsigned long long WAIT_NS = 200ull * 1000 * 1000;
 constexpr int GRP_BAR = 1;                  // named barrier of the compute group
@@ -496,10 +495,19 @@ __device__ void fixup_tile(const Ctx& c, const Geo& g, int t0, int t1) {
 template <int EPI>
 __device__ void direct_tile(const Ctx& c, const Geo& g, uint32_t taddr, int half, int row) {
   const MkArgs& a = *c.a;
+  const EpiArgs& e = c.sGA->e;
   float* Ys = reinterpret_cast<float*>(c.sC);
   float* scratch = Ys + EG * YLD;
+  float* pf_rr = scratch + EPI_SCRATCH_FLOATS + EG + EG * EPI_MAX_SSQ;  // [EG][NTILE] residual rows
+  float* pf_gn = pf_rr + EG * NTILE;                                     // [NTILE]
   for (int g0 = 0; g0 < a.T; g0 += EG) {
     const int cnt = min(EG, a.T - g0);
+    if (EPI == EPI_RESID) {
+      // residual rows written by other CTAs of this kernel: through L2
+      for (int x = c.grp.tid; x < cnt * NTILE; x += c.grp.n)
+        pf_rr[x] = __ldcg(e.resid + (size_t)(g0 + x / NTILE) * e.H + g.n0 + x % NTILE);
+      for (int x = c.grp.tid; x < NTILE; x += c.grp.n) pf_gn[x] = e.g_next[g.n0 + x];
+    }
     const int g16 = g0 / 16 + half;
     if (g16 * 16 < a.nt) {  // warp-uniform
       float vh[16], vl[16];
@@ -510,7 +518,11 @@ __device__ void direct_tile(const Ctx& c, const Geo& g, uint32_t taddr, int half
     }
     c.grp.sync();
     EpiPre pre;
-    if (c.sGA->e.ssq_in) pre.rs = c.s_rs + g0;
+    if (e.ssq_in) pre.rs = c.s_rs + g0;
+    if (EPI == EPI_RESID) {
+      pre.rr = pf_rr;
+      pre.gn = pf_gn;
+    }
     if (EPI == EPI_QKV) {
       pre.pos = c.s_pos + g0;
       pre.req = c.s_req + g0;
@@ -714,7 +726,13 @@ __device__ void compute_group(const Ctx& c) {
       load_gemm_args(c, g0, ga_loaded);
       const EpiArgs& e = c.sGA->e;
       if (e.ssq_in)
-        for (int t = c.grp.tid; t < a.T; t += c.grp.n) c.s_rs[t] = row_rstd(e, e.in_rows ? e.in_rows[t] : t);
+        for (int t = c.grp.tid; t < a.T; t += c.grp.n) {
+          // row_rstd's sum in column order, through L2 (other CTAs wrote the sums)
+          const float* p = e.ssq_in + (size_t)(e.in_rows ? e.in_rows[t] : t) * e.n_ssq;
+          float ssum = 0.f;
+          for (int i = 0; i < e.n_ssq; ++i) ssum += __ldcg(p + i);
+          c.s_rs[t] = rsqrtf(ssum / (float)e.norm_H + e.eps);
+        }
       c.grp.sync();
     }
     Item it;

@@ -37,9 +37,19 @@ static int split_chunk_limit() {
   if (lim < 0) {
     const char* v = getenv("GOCR_SPLIT_K");
     lim = 0;
-    if (v && strcmp(v, "wave") != 0 && atoi(v) >= 64) lim = atoi(v) / 64 * 64;
+    if (v && strncmp(v, "wave", 4) != 0 && atoi(v) >= 64) lim = atoi(v) / 64 * 64;
   }
   return lim;
+}
+
+// CTAs per SM the wave rule fills (GOCR_SPLIT_K=wave1 or wave2).
+static int wave_ctas_per_sm() {
+  static int w = 0;
+  if (!w) {
+    const char* v = getenv("GOCR_SPLIT_K");
+    w = (v && strcmp(v, "wave1") == 0) ? 1 : 2;
+  }
+  return w;
 }
 
 int gemm_kchunk(int N, int K) {
@@ -50,7 +60,7 @@ int gemm_kchunk(int N, int K) {
   if (lim > 0) {
     s = cdiv(kb, lim / 64);
   } else {
-    s = (2 * SM_COUNT) / tiles;  // at most two CTAs per SM in one wave
+    s = (wave_ctas_per_sm() * SM_COUNT) / tiles;  // CTAs per SM in one wave
     if (s > MAX_SPLITS) s = MAX_SPLITS;
   }
   if (s > kb) s = kb;

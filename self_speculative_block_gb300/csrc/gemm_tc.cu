@@ -91,8 +91,10 @@ bool encode_tmap_bf16(void* out, const void* ptr, int rows, int cols, int box_ro
 }
 
 // ring_bytes >= stages * (A tile + B tile) and >= the partial tile + reduce buffer.
-// EPI: the fused epilogue (a.epi), one instantiation per kind.
-template <int EPI>
+// EPI: the fused epilogue (a.epi), one instantiation per kind.  TRACE: the
+// instantiation that records the launch timeline (a.trace), launched only
+// when a record is attached, so that the other carries no trace code.
+template <int EPI, bool TRACE>
 __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw,
                                                             const __grid_constant__ CUtensorMap tmx_hi,
                                                             const __grid_constant__ CUtensorMap tmx_lo,
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   const uint32_t ncols = nmma <= 32 ? 32 : (nmma <= 64 ? 64 : (nmma <= 128 ? 128 : 256));
 
   if (tid == 0) {
+    if (TRACE) trace_mark(a.trace, 0);
     tc::prefetch_tmap(&tmw);
     tc::prefetch_tmap(&tmx_hi);
     if (two) tc::prefetch_tmap(&tmx_lo);
@@ -173,6 +176,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     // after the dependency wait do not pay a DRAM round trip
     for (int kb = pre; kb < nkb && kb < pre + L2_PREFETCH_BLOCKS; ++kb) tc::tma_prefetch_2d(&tmw, k0 + kb * 64, n0);
     tc::grid_dep_wait();
+    if (TRACE) trace_mark(a.trace, 1);
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % stages;
       const int use = kb / stages;
@@ -241,6 +245,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     }
   }
   const bool ok_done = tc::mbar_wait(done, 0);
+  if (TRACE && tid == 0) trace_mark(a.trace, 4);
   tc::fence_after_sync();
   __syncthreads();
   const bool failed = !ok_done || s_fail;
@@ -301,6 +306,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
       tc::bulk_commit();
     }
     const bool rx_ok = tc::mbar_wait(rxbar, 0);
+    if (TRACE && tid == 0) trace_mark(a.trace, 5);
     if (!rx_ok && tid == 0) set_err(a.e.err, DERR_TIMEOUT);
     for (int g0 = ta; g0 < tb; g0 += EG) {
       const int cnt = min(EG, tb - g0);
@@ -345,10 +351,11 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     if (tid == 0) tc::bulk_wait_read();  // the copies have read this CTA's partial tile
   }
   if (EPI == EPI_ARGMAX && !failed) argmax_grid_finish(a, &s_flag);
+  if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 
-template <int EPI>
-static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
+template <int EPI, bool TRACE>
+static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (a.splits < 1 || a.splits > MAX_CLUSTER) return false;
   CUtensorMap tmw, tmh, tml;
   if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE)) return false;
@@ -376,15 +383,15 @@ static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (smem > 227 * 1024) return false;
   static size_t configured = 0;
   if (smem > configured) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(gemm_tc_kernel<EPI, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return false;
     if (configured == 0 &&
-        cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        cudaFuncSetAttribute(gemm_tc_kernel<EPI, TRACE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return false;
     configured = smem;
   }
-  prefer_shared(reinterpret_cast<const void*>(gemm_tc_kernel<EPI>));
+  prefer_shared(reinterpret_cast<const void*>(gemm_tc_kernel<EPI, TRACE>));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(cdiv_i(a.N, NTILE), a.splits, cdiv_i(a.T, TZ_TC));
   cfg.blockDim = dim3(TC_THREADS);
@@ -404,7 +411,13 @@ static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI>, tmw, tmh, tml, a, nt, two, stages, ring, per) == cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, TRACE>, tmw, tmh, tml, a, nt, two, stages, ring, per) ==
+         cudaSuccess;
+}
+
+template <int EPI>
+static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
+  return a.trace ? launch_gemm_tc_kt<EPI, true>(a, s, pdl) : launch_gemm_tc_kt<EPI, false>(a, s, pdl);
 }
 
 bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {

@@ -132,6 +132,9 @@ struct gocr_handle {
   int mk_pf = 16;
   unsigned long long* mk_trace = nullptr;
   int mk_trace_cap = 0;
+  // per-launch timeline of debug forwards run with one kernel per operation
+  unsigned long long* op_trace = nullptr;
+  bool op_trace_next = false;
   std::vector<MkEntry> mk_tables;
 
   bool prefilled[MAX_REQ] = {};
@@ -415,6 +418,14 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
       return launch_forward_mk(e->args, c.head_dim, h->hs, pdl);
   FwdArgs f;
   forward_args(h, kind, n_slots, B, P, am_out, logits, slot_tab, f);
+  if (h->op_trace_next) {
+    // launch records in forward order: per layer QKV, attention, O, gate/up, down; then the LM head
+    for (int l = 0; l < c.n_layers; ++l) {
+      for (int k = 0; k < 4; ++k) f.g[(size_t)l * 4 + k].trace = h->op_trace + TRACE_WORDS * (5 * l + (k == 0 ? 0 : k + 1));
+      f.at[l].trace = h->op_trace + TRACE_WORDS * (5 * l + 1);
+    }
+    f.g[(size_t)c.n_layers * 4].trace = h->op_trace + TRACE_WORDS * (5 * c.n_layers);
+  }
   for (int l = 0; l < c.n_layers; ++l) {
     ok &= launch_gemm(h->dtype, f.g[(size_t)l * 4 + 0], h->hs, pdl);
     ok &= launch_attention(h->dtype, f.at[l], kind == PLAN_PREFILL ? 1 : n_slots,
@@ -788,6 +799,8 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->mk_att = (float*)A((size_t)h->mk_att_items * 64 * (c.head_dim + 4) * 4);
     h->mk_ctr_bytes = mk::ctr_words(c.n_layers) * 4;
     h->mk_ctr = (unsigned*)A(h->mk_ctr_bytes);
+    const char* ot = getenv("GOCR_OP_TRACE");
+    if (ot && ot[0] == '1') h->op_trace = (unsigned long long*)A((size_t)TRACE_WORDS * (5 * c.n_layers + 1) * 8);
     const char* tr = getenv("GOCR_MK_TRACE");
     if (tr && atoi(tr) > 0) {
       h->mk_trace_cap = atoi(tr) > 4096 ? 4096 : atoi(tr);
@@ -903,9 +916,16 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
   if ((r = mk_prepare(h, pk, 1, B, h->am, h->logits, h->slot_one))) return r;
   if (h->mk_ctr) CK(cudaMemsetAsync(h->mk_ctr, 0, h->mk_ctr_bytes, h->hs));
   if (h->mk_trace) CK(cudaMemsetAsync(h->mk_trace, 0, (size_t)h->mk_G * 2 * h->mk_trace_cap * 16, h->hs));
+  if (h->op_trace) {
+    std::vector<unsigned long long> init((size_t)TRACE_WORDS * (5 * h->cfg.n_layers + 1));
+    for (size_t i = 0; i < init.size(); ++i) init[i] = (i % TRACE_WORDS) < 2 ? ~0ull : 0ull;
+    CK(cudaMemcpy(h->op_trace, init.data(), init.size() * 8, cudaMemcpyHostToDevice));
+    h->op_trace_next = true;
+  }
   launch_plan(pk, h->rows, h->st, h->slot_one, 1, B, 0, nullptr, h->dbg_toks, h->cap, h->hs, false);
-  if (!enqueue_forward(h, pk, 1, B, 0, h->am, h->logits, h->slot_one))
-    return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
+  const bool enq = enqueue_forward(h, pk, 1, B, 0, h->am, h->logits, h->slot_one);
+  h->op_trace_next = false;
+  if (!enq) return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   CK(cudaGetLastError());
   if (logits_out)
     CK(cudaMemcpyAsync(logits_out, h->logits, sizeof(float) * n * h->cfg.vocab, cudaMemcpyDeviceToHost, h->hs));
@@ -1009,8 +1029,17 @@ int gocr_get_option(const gocr_handle* h, int option, int* value) {
   return GOCR_EINVAL;
 }
 
-int gocr_read_trace(gocr_handle* h, uint64_t* out, size_t n_words) {
+int gocr_read_trace(gocr_handle* h, int which, uint64_t* out, size_t n_words) {
   if (!h || !out) return fail(h, GOCR_EINVAL, "null argument");
+  if (which == GOCR_TRACE_KERNELS) {
+    if (!h->op_trace) return fail(h, GOCR_ESTATE, "kernel tracing is off (GOCR_OP_TRACE)");
+    const size_t words = (size_t)TRACE_WORDS * (5 * h->cfg.n_layers + 1);
+    if (n_words < words) return fail(h, GOCR_ECAPACITY, "trace needs %zu words", words);
+    CK(cudaStreamSynchronize(h->hs));
+    CK(cudaMemcpy(out, h->op_trace, words * 8, cudaMemcpyDeviceToHost));
+    return GOCR_OK;
+  }
+  if (which != GOCR_TRACE_PERSISTENT) return fail(h, GOCR_EINVAL, "bad trace kind %d", which);
   if (!h->mk_trace) return fail(h, GOCR_ESTATE, "tracing is off (GOCR_MK_TRACE)");
   const size_t words = (size_t)h->mk_G * 2 * h->mk_trace_cap * 2;
   if (n_words < words) return fail(h, GOCR_ECAPACITY, "trace needs %zu words", words);

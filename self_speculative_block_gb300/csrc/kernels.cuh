@@ -70,6 +70,9 @@ struct alignas(16) GemmArgs {  // 16-byte aligned: tables of them are copied by 
   int* counters;                 // CUDA-core path: tile counters, zero between launches
   int epi;
   EpiArgs e;
+  // optional launch timeline record (4 words: first CTA start, first and last
+  // release from the dependency wait, last CTA end; globaltimer ns)
+  unsigned long long* trace;
 };
 
 // Split-K GEMM with fused epilogue (bf16: tcgen05 + TMA, split-K reduced
@@ -102,6 +105,7 @@ struct alignas(16) AttnArgs {
   const int* slot_req; const ReqState* st; int rows_per_slot;
   int T, Hq, Hkv, d, cap;
   float scale;
+  unsigned long long* trace;  // launch timeline record, as GemmArgs::trace
 };
 // Cluster width of the tensor-core attention kernel for head dim d (16 or 8),
 // fixed once per process: it decides which tile reads which key chunk and the
@@ -179,6 +183,25 @@ void launch_prefill_finish(ReqState* st, int req, int P, const int* am, int* out
 void launch_begin_decode(ReqState* st, const int* slot_req, int n_slots, const int* max_new,
                          int max_rounds, int eos_id, cudaStream_t s);
 void launch_set_override(ReqState* st, int req, int n_ref, int n_sched, cudaStream_t s);
+
+// Launch timeline records (GemmArgs::trace, TRACE_WORDS words): word 0 min of
+// CTA start times, 1 and 2 min / max of dependency-release times, 3 max of
+// CTA end times; GEMMs also 4 max of mainloop-done times, 5 max of split-K
+// exchange-done times; attention 4 max of first-chunk-ready times, 5 max of
+// chunk-loop-done times, 6 max of merge-exchange-done times.
+constexpr int TRACE_WORDS = 8;
+__device__ __forceinline__ unsigned long long trace_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void trace_mark(unsigned long long* r, int word) {
+  if (!r) return;
+  const unsigned long long t = trace_now();
+  if (word == 0 || word == 1) atomicMin(r + word, t);
+  else atomicMax(r + word, t);
+  if (word == 1) atomicMax(r + 2, t);
+}
 
 // Library-level error message returned by gocr_last_error(NULL).
 void set_lib_error(const char* msg);

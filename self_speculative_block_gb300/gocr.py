@@ -99,7 +99,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gocr_read_kv": (i32, [vp, i32, i32, i32, i32, vp, vp]),
         "gocr_get_state": (i32, [vp, i32, P32, P32]),
         "gocr_set_option": (i32, [vp, i32, i32]),
-        "gocr_read_trace": (i32, [vp, vp, sz]),
+        "gocr_read_trace": (i32, [vp, i32, vp, sz]),
         "gocr_get_option": (i32, [vp, i32, P32]),
         "gocr_last_error": (ctypes.c_char_p, [vp]),
         "gocr_free": (None, [vp]),
@@ -310,7 +310,15 @@ class Decoder:
         (writer 0: activation producer, 1: compute group; (ns, phase << 8 | event))."""
         G, cap = self._option(OPT_GRID_CTAS), self._option(OPT_TRACE_RECORDS)
         out = np.zeros((G, 2, cap, 2), np.uint64)
-        _check(self.lib.gocr_read_trace(self.h, out.ctypes.data, out.size), self.h)
+        _check(self.lib.gocr_read_trace(self.h, 0, out.ctypes.data, out.size), self.h)
+        return out
+
+    def read_kernel_trace(self) -> np.ndarray:
+        """Per-launch timeline of the last debug forward run with one kernel per
+        operation: uint64 [5 L + 1, 8] (first start, first and last dependency
+        release, last end, last mainloop end, last split-K exchange end; ns)."""
+        out = np.zeros((5 * self.cfg.n_layers + 1, 8), np.uint64)
+        _check(self.lib.gocr_read_trace(self.h, 1, out.ctypes.data, out.size), self.h)
         return out
 
     def state(self, req: int):
