@@ -230,7 +230,9 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
  * with the lo pointers NULL.  q [T, Hq, d], k and v [Hkv, cap, d] (device);
  * o [T, Hq, d] fp32 (device); lim: device int32[T], row t reads keys
  * 0..lim[t] (draft: row 0 = p, rows 1..B = p+B; verify/AR: the row's own
- * position).  d in {64, 128}. */
+ * position).  d in {64, 128}.  GOCR_DTYPE_BF16 keeps its partial rows in a
+ * device scratch buffer of the library (one per device, allocated or grown
+ * by the first call that needs more): calls that overlap on the GPU race. */
 int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
                       const void* v_hi, const void* v_lo, float* o, const int32_t* lim, int T, int Hq, int Hkv,
                       int d, int cap, void* stream);

@@ -5,25 +5,27 @@
 //          lim = p + B (the cache plus the whole window, bidirectional);
 //   verify / AR / prefill: lim = the row's own position (token-causal).
 //
-// Keys are visited in fixed 64-key chunks at absolute positions.  A chunk with
-// no key visible to a row leaves that row's running (max, sum, output)
-// bit-for-bit unchanged (scale exp(0) = 1, zero contributions), so a row's
-// result does not depend on how many other rows share the launch: the AR step
-// and the verify row at the same position give identical bits.
+// Keys are visited in fixed chunks at absolute positions (64 keys for the
+// CUDA-core kernel, 32 for the tensor-core one).  A chunk with no key visible
+// to a row leaves that row's running (max, sum, output) bit-for-bit unchanged
+// (scale exp(0) = 1, zero contributions), so a row's result does not depend
+// on how many other rows share the launch: the AR step and the verify row at
+// the same position give identical bits.
 //
-// bf16 models: tensor-core kernel.  q and the KV cache are stored as bf16
+// bf16 models: tensor-core kernels.  q and the KV cache are stored as bf16
 // hi + lo planes (written once by the QKV epilogue), QK^T takes
 // qh kh + qh kl + ql kh and PV takes P vh + P vl on mma.sync tiles (P in
-// bf16), accumulating in fp32.  A cluster of CL CTAs shares one (kv head,
-// 64-query-row group): CTA r visits chunks r, r + CL, ... with an online
-// softmax, K/V tiles double-buffered through cp.async, then the cluster merges
-// its CL partial (max, sum, output) triples through distributed shared memory
-// in rank order.  Under programmatic dependent launch a CTA fetches its first
+// bf16), accumulating in fp32.  The ATTN_RANKS CTAs of one (kv head,
+// 64-query-row group) split the chunks, rank r visiting chunks r, r + R, ...
+// with an online softmax, and write partial (max, sum, output) rows to global
+// memory; a merge kernel adds them in rank order.  There is no thread-block
+// cluster: most decode contexts give each rank one chunk, and the CTAs need no
+// co-scheduling.  Under programmatic dependent launch a CTA fetches its first
 // chunk before the grid-dependency wait when that chunk holds only committed
 // cache positions (below the round-start cache length, which no kernel of the
 // forward writes).  The result is written as the O projection's input planes.
 // fp32 models: CUDA-core kernel with one CTA sweeping every chunk.
-#include <cooperative_groups.h>
+#include <cstdlib>
 
 #include "attn_core.cuh"
 #include "tc.cuh"
@@ -136,49 +138,35 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
 
 // ---------------------------------------------------------------- tensor-core path (bf16 models)
 
-// One CTA per (cluster rank, kv head x row group, slot) tile; the cluster's
-// CL tiles split the key chunks and merge over distributed shared memory.
-// At most 128 registers a thread: one attention CTA (32 K registers) and two
-// GEMM CTAs of the next kernels then fit one SM's register file together, so
-// under programmatic dependent launch those CTAs become resident, and start
-// their weight loads, while attention still runs.
-template <int D, int CL, bool TRACE>
-__global__ void __launch_bounds__(256, 2) attention_mma_kernel(AttnArgs a) {
-  namespace cg = cooperative_groups;
+// Partial kernel: one CTA per (kv head x row group, rank, slot) tile; the
+// rank is the second grid dimension so that low ranks, which hold chunks at
+// every context length, dispatch first.  Ranks whose first chunk lies past
+// the group's last visible key exit after the row limits are read; the others
+// write their partial rows to a.part.
+template <int D, bool TRACE>
+__global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
   using Gm = attn::Geo<D>;
   constexpr int RLD = Gm::RLD;
-  constexpr int RPC = attn::QR / CL; // rows owned per CTA
-  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(16) uint8_t sm_raw[];
-  float* RX = reinterpret_cast<float*>(sm_raw + Gm::TILE_SMEM);  // [CL][RPC][RLD] partial rows from each rank
-  float* WS = RX + CL * RPC * RLD;                               // [RPC][CL] merge weights
-  float* IL = WS + RPC * CL;                                     // [RPC] 1 / total sum
-  __shared__ __align__(8) uint64_t rxbar;
   __shared__ int s_maxlim;
   const Grp grp = Grp::block();
-
-  const int rank = blockIdx.x;  // == cluster rank (the cluster spans grid x)
-  const int kvh = blockIdx.y % a.Hkv;
-  const int rg = blockIdx.y / a.Hkv;
+  const int group = blockIdx.x, rank = blockIdx.y, R = gridDim.y;
   const int slot = blockIdx.z;
+  const int kvh = group % a.Hkv, rg = group / a.Hkv;
   const int G = a.Hq / a.Hkv;
   const int tid = threadIdx.x;
 
   if (tid == 0) {
     if (TRACE) trace_mark(a.trace, 0);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    tc::mbar_init(&rxbar, 1);
-    tc::fence_mbar_init();
-    tc::mbar_expect_tx(&rxbar, (uint32_t)(CL * RPC * RLD * 4));  // one block of rows from every rank
   }
-  cluster.sync();  // every receive barrier is armed before any rank sends
   // committed cache before the dependency wait (decode launches only)
   int req_pre = -1;
   bool pre = false;
   if (a.st && a.slot_req) {
     req_pre = a.slot_req[slot];
-    pre = attn::tile_prefetch<D, CL>(sm_raw, attn::kv_planes(a, req_pre, kvh, D), rank, a.st[req_pre].cache_len,
-                                     tid);
+    pre = attn::tile_prefetch<D>(sm_raw, attn::kv_planes(a, req_pre, kvh, D), rank, R, a.st[req_pre].cache_len,
+                                 tid);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (TRACE && tid == 0) trace_mark(a.trace, 1);
@@ -194,115 +182,94 @@ __global__ void __launch_bounds__(256, 2) attention_mma_kernel(AttnArgs a) {
     nrows = a.plan->slot_nrows[slot];
   }
   const int qr0 = rg * attn::QR;
-  if (qr0 >= nrows * G) {  // uniform across the cluster
+  if (qr0 >= nrows * G) {  // uniform: a row group past the window
     attn::cp_async_wait<0>();
     return;
   }
-  attn::tile_partial<D, CL, TRACE>(a, sm_raw, grp, attn::kv_planes(a, req, kvh, D), rank, kvh, qr0, row0, nrows,
-                                   pre, &s_maxlim);
-  float* ST = attn::staged_rows<D>(sm_raw);
-  tc::fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) {
-    // one bulk copy per owner: this CTA's rows of that owner -> its RX[rank]
-    for (int r = 0; r < CL; ++r)
-      tc::bulk_s2s(tc::mapa(tc::smem_u32(RX + (size_t)rank * RPC * RLD), r), ST + (size_t)r * RPC * RLD,
-                   (uint32_t)(RPC * RLD * 4), tc::mapa(tc::smem_u32(&rxbar), r));
-    tc::bulk_commit();
-  }
-  const bool rx_ok = tc::mbar_wait(&rxbar, 0);
-  if (TRACE && tid == 0) trace_mark(a.trace, 6);
-  auto row = [&](int c, int i) -> const float* { return RX + (c * RPC + i) * RLD; };
-  attn::merge_owned<D, CL>(a, grp, row, WS, IL, rank, kvh, qr0, row0, nrows, rx_ok);
-  if (tid == 0) tc::bulk_wait_read();  // the copies have read this CTA's staged rows
+  const int n_chunks = attn::tile_partial<D, TRACE>(a, sm_raw, grp, attn::kv_planes(a, req, kvh, D), rank, R, kvh,
+                                                    qr0, row0, nrows, pre, &s_maxlim);
+  if (rank == 0 && tid == 0) a.part_chunks[(size_t)slot * gridDim.x + group] = n_chunks;
+  if (rank >= n_chunks) return;
+  const float4* src = reinterpret_cast<const float4*>(attn::staged_rows<D>(sm_raw));
+  float4* dst = reinterpret_cast<float4*>(
+      a.part + (((size_t)slot * gridDim.x + group) * R + rank) * attn::QR * RLD);
+  for (int x = tid; x < attn::QR * RLD / 4; x += 256) dst[x] = src[x];
   if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 
-template <int D, int CL>
-static size_t attn_mma_smem() {
-  constexpr int RPC = attn::QR / CL, RLD = attn::Geo<D>::RLD;
-  return attn::Geo<D>::TILE_SMEM + ((size_t)CL * RPC * RLD + RPC * CL + RPC) * 4;
+// Merge kernel: one CTA per (pair of rows, kv head x row group, slot).
+template <int D, bool TRACE>
+__global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R) {
+  constexpr int RLD = attn::Geo<D>::RLD;
+  __shared__ float WS[2 * 64];
+  __shared__ float IL[2];
+  __shared__ float4 AC[4 * 64];
+  const Grp grp = Grp::block();
+  const int pair = blockIdx.x, group = blockIdx.y, slot = blockIdx.z;
+  const int kvh = group % a.Hkv, rg = group / a.Hkv;
+  const int G = a.Hq / a.Hkv;
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (TRACE && threadIdx.x == 0) trace_mark(a.trace, 6);
+  int row0 = 0, nrows = a.T;
+  if (a.rows_per_slot > 0) {
+    row0 = slot * a.rows_per_slot;
+    nrows = a.rows_per_slot;
+  } else if (a.plan) {
+    row0 = a.plan->slot_row0[slot];
+    nrows = a.plan->slot_nrows[slot];
+  }
+  const int qr0 = rg * attn::QR;
+  if (qr0 + 2 * pair >= nrows * G) return;
+  const int n_chunks = a.part_chunks[(size_t)slot * gridDim.y + group];
+  const int n_ranks = n_chunks < R ? n_chunks : R;
+  const float* base = a.part + ((size_t)slot * gridDim.y + group) * R * attn::QR * RLD;
+  auto part = [&](int c, int i) -> const float* { return base + ((size_t)c * attn::QR + i) * RLD; };
+  attn::merge_rows<D, false>(a, grp, part, WS, IL, AC, n_ranks, R, 2 * pair, 1, 2, kvh, qr0, row0, nrows);
+  if (TRACE && threadIdx.x == 0) trace_mark(a.trace, 3);
 }
 
-template <int D, int CL, bool TRACE>
-static cudaError_t launch_attn_cl(const AttnArgs& a, dim3 grid, cudaStream_t s, bool pdl) {
-  const size_t smem = attn_mma_smem<D, CL>();
+size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d) {
+  const int G = Hq / Hkv;
+  const size_t groups = (size_t)Hkv * ((max_rows * G + attn::QR - 1) / attn::QR);
+  return (size_t)n_slots * groups * ATTN_RANKS * attn::QR * (d + 4);
+}
+
+template <int D, bool TRACE>
+static bool launch_attn_mma_t(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
+  const int G = a.Hq / a.Hkv;
+  const int n_rg = (max_rows * G + attn::QR - 1) / attn::QR;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(attention_part_kernel<D, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)attn::Geo<D>::TILE_SMEM) != cudaSuccess)
+      return false;
+    prefer_shared(reinterpret_cast<const void*>(attention_part_kernel<D, TRACE>));
+    configured = true;
+  }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
+  const int R = attention_ranks(a.cap);
+  cfg.gridDim = dim3(a.Hkv * n_rg, R, n_slots);
   cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = attn::Geo<D>::TILE_SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute at[2];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = CL;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, attention_mma_kernel<D, CL, TRACE>, a);
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, attention_part_kernel<D, TRACE>, a) != cudaSuccess) return false;
+  // the merge reads every rank's rows: always ordered after the partial kernel
+  cfg.gridDim = dim3(attn::QR / 2, a.Hkv * n_rg, n_slots);
+  cfg.dynamicSmemBytes = 0;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attention_merge_kernel<D, TRACE>, a, R) == cudaSuccess;
 }
-
-// Kernel attributes of one cluster width (both trace instantiations).
-template <int D, int CL>
-static bool attn_configure() {
-  const int smem = (int)attn_mma_smem<D, CL>();
-  bool ok = true;
-  for (const void* fn : {reinterpret_cast<const void*>(attention_mma_kernel<D, CL, false>),
-                         reinterpret_cast<const void*>(attention_mma_kernel<D, CL, true>)}) {
-    prefer_shared(fn);
-    if (CL > 8) ok &= cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-    ok &= cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
-  }
-  return ok;
-}
-
-// Cluster width: 16 CTAs when the device keeps the eight 16-CTA clusters of
-// a 33-row decode window (4 kv heads x 2 row groups) resident at once, else
-// 8.  The width fixes which rank reads which key chunk and the order of the
-// merge, so it is chosen once per process: every launch, AR or
-// self-speculative, adds the same partials in the same order.
-template <int D>
-static int attn_cluster_width() {
-  static int width = 0;
-  if (width) return width;
-  width = 8;
-  if (attn_configure<D, 16>()) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(16, 1, 1);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = attn_mma_smem<D, 16>();
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 16;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attention_mma_kernel<D, 16, false>, &cfg) == cudaSuccess && n >= 8)
-      width = 16;
-  }
-  cudaGetLastError();
-  if (width == 8) attn_configure<D, 8>();
-  return width;
-}
-
-int attention_cluster_width(int d) { return d == 128 ? attn_cluster_width<128>() : attn_cluster_width<64>(); }
 
 template <int D>
 static bool launch_attn_mma(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
-  const int G = a.Hq / a.Hkv;
-  const int n_rg = (max_rows * G + attn::QR - 1) / attn::QR;
-  const int cl = attn_cluster_width<D>();
-  const dim3 grid(cl, a.Hkv * n_rg, n_slots);
-  cudaError_t e;
-  if (a.trace)
-    e = cl == 16 ? launch_attn_cl<D, 16, true>(a, grid, s, pdl) : launch_attn_cl<D, 8, true>(a, grid, s, pdl);
-  else
-    e = cl == 16 ? launch_attn_cl<D, 16, false>(a, grid, s, pdl) : launch_attn_cl<D, 8, false>(a, grid, s, pdl);
-  return e == cudaSuccess;
+  return a.trace ? launch_attn_mma_t<D, true>(a, n_slots, max_rows, s, pdl)
+                 : launch_attn_mma_t<D, false>(a, n_slots, max_rows, s, pdl);
 }
 
 template <int D>

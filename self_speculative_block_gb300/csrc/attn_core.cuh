@@ -1,15 +1,14 @@
 // Tensor-core attention of one (request, kv head, 64-query-row group) tile
 // over a fixed subset of key chunks, and the fixed-order merge of the
-// partial results of the CL tiles that share those query rows.
+// partial results of the R tiles ("ranks") that share those query rows.
 //
-// The per-forward attention kernel (one CTA per tile, a thread-block
-// cluster of CL tiles merging over distributed shared memory) and the
-// persistent decode kernel (tiles as work items, merging through global
-// memory) both run these functions, so a row's attention output has the
-// same bits whichever kernel computes it.
+// The per-operation attention (a partial kernel, one CTA per tile, then a
+// merge kernel) and the persistent decode kernel (tiles and merges as work
+// items) both run these functions, so a row's attention output has the same
+// bits whichever kernel computes it.
 //
 // Layout of the work: keys sit in chunks of AC = 32 at absolute positions;
-// tile `rank` of the CL tiles visits chunks rank, rank + CL, ...  In a tile,
+// rank r of the R ranks visits chunks r, r + R, ...  In a tile,
 // warp w owns query rows 16 (w % 4) .. +15 and key half w / 4 (keys
 // 16 (w / 4) .. +15 of every chunk), so each (rank, key half) runs its own
 // online softmax over a fixed set of key positions.  A chunk with no key
@@ -113,16 +112,18 @@ __device__ __forceinline__ void load_planes(bf16* KV, const KvPlanes& kv, int pl
 // its first chunk holds only committed cache positions (below the round-start
 // cache length pc, which no kernel of the forward writes), that chunk goes to
 // shared memory as one committed cp.async group and the tile's later
-// committed chunks into L2.  Returns whether the first chunk was issued.
-template <int D, int CL>
-__device__ __forceinline__ bool tile_prefetch(uint8_t* sm, const KvPlanes& kv, int rank, int pc, int tid) {
+// committed chunks (rank + stride, ...) into L2.  Returns whether the first
+// chunk was issued.
+template <int D>
+__device__ __forceinline__ bool tile_prefetch(uint8_t* sm, const KvPlanes& kv, int rank, int stride, int pc,
+                                              int tid) {
   bf16* KV = reinterpret_cast<bf16*>(sm + Geo<D>::Q_BYTES);
   const bool pre = (rank + 1) * AC <= pc;
   if (pre) {
     load_planes<D>(KV, kv, 0, 4, rank, pc - 1, tid);
     cp_async_commit();
     for (int i = tid; i < 4 * 8; i += 256) {
-      const int c = rank + (1 + i / 4) * CL;
+      const int c = rank + (1 + i / 4) * stride;
       if ((c + 1) * AC <= pc) prefetch_l2(kv.p[i % 4] + (size_t)c * AC * D, AC * D * 2);
     }
   }
@@ -131,22 +132,23 @@ __device__ __forceinline__ bool tile_prefetch(uint8_t* sm, const KvPlanes& kv, i
 
 // One tile: query rows qr0 .. qr0+63 of the (row, q head) list of a request
 // window (rows row0 .. row0+nrows-1, G = Hq / Hkv heads per kv head), keys
-// of chunks rank, rank + CL, ...  `pre`: tile_prefetch issued the first chunk.
-// On return the tile's partial rows (D outputs, max, sum) sit in shared
-// memory, staged by owner: row r at (r % CL) * (QR / CL) + r / CL, stride RLD,
-// starting at staged_rows(sm).  Every thread of the 256-thread group calls it.
+// of chunks rank, rank + stride, ...  `pre`: tile_prefetch issued the first
+// chunk.  Returns the number of chunks the rows read (the last visible key
+// of any row, over AC).  When rank < that number the tile's partial rows (D
+// outputs, max, sum; stride RLD, row r at r * RLD) sit in shared memory at
+// staged_rows(sm) on return; otherwise nothing is staged (the rank holds
+// no chunk).  Every thread of the 256-thread group calls it.
 template <int D>
 __device__ __forceinline__ float* staged_rows(uint8_t* sm) {
   return reinterpret_cast<float*>(sm + Geo<D>::Q_BYTES);
 }
 
 // TRACE: record timeline marks in a.trace (first chunk ready, loop done).
-template <int D, int CL, bool TRACE = false>
-__device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, const KvPlanes& kv, int rank, int kvh,
-                             int qr0, int row0, int nrows, bool pre, int* s_maxlim) {
+template <int D, bool TRACE = false>
+__device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, const KvPlanes& kv, int rank,
+                            int stride, int kvh, int qr0, int row0, int nrows, bool pre, int* s_maxlim) {
   using Gm = Geo<D>;
   constexpr int QLD = Gm::QLD, OLD = Gm::OLD, TILE = Gm::TILE, RLD = Gm::RLD;
-  constexpr int RPC = QR / CL;
   bf16* Qh = reinterpret_cast<bf16*>(sm);               // [QR][QLD]
   bf16* Ql = Qh + QR * QLD;
   bf16* KV = Ql + QR * QLD;                             // {Kh, Kl, Vh, Vl} [AC][QLD]
@@ -154,7 +156,7 @@ __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, con
   float* Oh = reinterpret_cast<float*>(Qh);             // [QR][OLD] half-1 partial (Q is dead by then)
   float* Mh = Oh + QR * OLD;                            // [QR]
   float* Lh = Mh + QR;                                  // [QR]
-  float* ST = reinterpret_cast<float*>(KV);             // [CL][RPC][RLD] staged rows
+  float* ST = reinterpret_cast<float*>(KV);             // [QR][RLD] staged rows
 
   const int G = a.Hq / a.Hkv;
   const int tid = grp.tid, warp = tid >> 5, lane = tid & 31;
@@ -186,6 +188,10 @@ __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, con
   grp.sync();
   const int maxlim = *s_maxlim;
   const int n_chunks = maxlim < 0 ? 0 : maxlim / AC + 1;
+  if (rank >= n_chunks) {  // uniform: this rank holds no chunk
+    cp_async_wait<0>();
+    return n_chunks;
+  }
   const float sl2 = a.scale * LOG2E;
 
   const int r_lo = mt * 16 + g, r_hi = r_lo + 8;
@@ -211,9 +217,9 @@ __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, con
   }
   cp_async_commit();
   int it = 0;
-  for (int c = rank; c < n_chunks; c += CL, ++it) {
+  for (int c = rank; c < n_chunks; c += stride, ++it) {
     const int kbase = c * AC + kh * 16;
-    const bool next = c + CL < n_chunks;
+    const bool next = c + stride < n_chunks;
     if (it == 0) cp_async_wait<0>(); else cp_async_wait<1>();  // this chunk's K (and Q, first chunk)
     grp.sync();
     if (TRACE && it == 0 && tid == 0) trace_mark(a.trace, 4);
@@ -247,7 +253,7 @@ __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, con
       }
     }
     grp.sync();  // every warp is done with this chunk's K
-    if (next) load_planes<D>(KV, kv, 0, 2, c + CL, maxlim, tid);
+    if (next) load_planes<D>(KV, kv, 0, 2, c + stride, maxlim, tid);
     cp_async_commit();
     // mask, scale to log2 units, row maxima over the 16 keys
     float mc_lo = -INFINITY, mc_hi = -INFINITY;
@@ -317,7 +323,7 @@ __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, con
       mma16816(oacc[dn + 1], af, bh + 2);
     }
     grp.sync();  // every warp is done with this chunk's V
-    if (next) load_planes<D>(KV, kv, 2, 2, c + CL, maxlim, tid);
+    if (next) load_planes<D>(KV, kv, 2, 2, c + stride, maxlim, tid);
     cp_async_commit();
   }
   cp_async_wait<0>();
@@ -347,9 +353,9 @@ __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, con
     const float w1_hi = m1_hi == -INFINITY ? 0.f : exp2f(m1_hi - M_hi);
     const float L_lo = w0_lo * l_lo + w1_lo * Lh[r_lo];
     const float L_hi = w0_hi * l_hi + w1_hi * Lh[r_hi];
-    // stage this tile's partial rows by owner: row r -> rank r % CL, slot r / CL
-    float* st_lo = ST + ((r_lo % CL) * RPC + r_lo / CL) * RLD;
-    float* st_hi = ST + ((r_hi % CL) * RPC + r_hi / CL) * RLD;
+    // stage this tile's partial rows
+    float* st_lo = ST + r_lo * RLD;
+    float* st_hi = ST + r_hi * RLD;
     float o1[D / 8][4];
 #pragma unroll
     for (int dn = 0; dn < D / 8; ++dn) {
@@ -373,66 +379,121 @@ __device__ void tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, con
     }
   }
   grp.sync();
+  return n_chunks;
 }
 
-// Merge of the RPC rows that tile `owner` owns (rows owner + i * CL of the
-// row group) from the CL tiles' partial rows, row(c, i) -> D outputs, max,
-// sum of tile c's partial of owned row i.  Warp i computes the merge weights
-// of row i with lane c holding tile c's (max, sum) and a fixed butterfly
-// order; then all CL partials of an output quad are loaded and added in tile
-// order.  Writes the rows' attention output planes.  WS: [RPC][CL] and IL:
-// [RPC] shared scratch.  GLOBAL: the partial rows are in global memory,
-// written by other CTAs of a running kernel (read through L2, not L1).
-template <int D, int CL, class Row, bool GLOBAL = false>
-__device__ void merge_owned(const AttnArgs& a, const Grp& grp, const Row& row, float* WS, float* IL, int owner,
-                            int kvh, int qr0, int row0, int nrows, bool ok) {
-  constexpr int RPC = QR / CL;
+// Chunks of a (request, kv head, row group) tile set: the last key any of
+// its 64 rows reads decides how many ranks hold partial rows.  All 64 rows'
+// limits are read, by the group's first 64 threads; s_maxlim is shared.
+__device__ __forceinline__ int tile_chunks(const AttnArgs& a, const Grp& grp, int qr0, int row0, int nrows,
+                                           int* s_maxlim) {
+  const int G = a.Hq / a.Hkv;
+  if (grp.tid == 0) *s_maxlim = -1;
+  grp.sync();
+  if (grp.tid < QR) {
+    const int gi = qr0 + grp.tid;
+    if (gi < nrows * G) {
+      const int lim = min(a.row_lim[row0 + gi / G], a.cap - 1);
+      if (lim >= 0) atomicMax(s_maxlim, lim);
+    }
+  }
+  grp.sync();
+  const int maxlim = *s_maxlim;
+  grp.sync();
+  return maxlim < 0 ? 0 : maxlim / AC + 1;
+}
+
+// Merge of tile rows i0 and i0 + step (cnt = 1 or 2 of them, < QR) from the
+// partial rows of ranks 0 .. n_ranks-1 (n_ranks <= r_all <= 64, r_all the
+// rank slots part() may address): part(c, i) -> D
+// outputs, max, sum of rank c's partial of row i.  Ranks whose chunks a row
+// cannot see hold (-inf, 0, 0) and add exact zeros, so the result does not
+// depend on n_ranks beyond the row's own chunks.  Fixed order: warp k reduces
+// row k's maxima and weighted sums over lanes (lane l holds ranks l and
+// l + 32, added in that order, then a fixed butterfly); the outputs are four
+// sums over the ranks of each residue mod 4 (in rank order), added as
+// ((s0 + s1) + s2) + s3.  The group has 256 threads.  WS: [2][64], IL: [2]
+// and AC: [4][64] float4 shared scratch; writes the rows' output planes.
+template <int D, bool GLOBAL, class Part>
+__device__ void merge_rows(const AttnArgs& a, const Grp& grp, const Part& part, float* WS, float* IL, float4* AC,
+                           int n_ranks, int r_all, int i0, int step, int cnt, int kvh, int qr0, int row0,
+                           int nrows) {
+  static_assert(D <= 128 && D % 4 == 0, "two rows of output quads per 64 threads");
   const int tid = grp.tid, warp = tid >> 5, lane = tid & 31;
   const int G = a.Hq / a.Hkv;
   const int nq = nrows * G;
-  if (warp < RPC) {
-    const int i = warp;
-    const float m = lane < CL ? (GLOBAL ? __ldcg(row(lane, i) + D) : row(lane, i)[D]) : -INFINITY;
-    const float l = lane < CL ? (GLOBAL ? __ldcg(row(lane, i) + D + 1) : row(lane, i)[D + 1]) : 0.f;
-    float M = m;
+  auto ld = [&](const float* p) -> float { return GLOBAL ? __ldcg(p) : *p; };
+  if (warp < cnt) {
+    const int k = warp;
+    const int i = i0 + k * step;
+    // every rank slot's (max, sum) is read before n_ranks is used, so the
+    // loads share one round trip with the caller's; slots past n_ranks hold
+    // stale values and are masked
+    const float lm0 = lane < r_all ? ld(part(lane, i) + D) : 0.f;
+    const float lm1 = lane + 32 < r_all ? ld(part(lane + 32, i) + D) : 0.f;
+    const float ll0 = lane < r_all ? ld(part(lane, i) + D + 1) : 0.f;
+    const float ll1 = lane + 32 < r_all ? ld(part(lane + 32, i) + D + 1) : 0.f;
+    const float m0 = lane < n_ranks ? lm0 : -INFINITY;
+    const float m1 = lane + 32 < n_ranks ? lm1 : -INFINITY;
+    float M = fmaxf(m0, m1);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-    float L = w * l;
+    const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+    const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+    float L = w0 * (lane < n_ranks ? ll0 : 0.f);
+    L += w1 * (lane + 32 < n_ranks ? ll1 : 0.f);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (lane < CL) WS[i * CL + lane] = w;
-    if (lane == 0) IL[i] = L > 0.f ? 1.f / L : 0.f;
+    WS[k * 64 + lane] = w0;
+    WS[k * 64 + lane + 32] = w1;
+    if (lane == 0) IL[k] = L > 0.f ? 1.f / L : 0.f;
   }
   grp.sync();
-  if (ok) {
-    for (int x = tid; x < RPC * (D / 4); x += grp.n) {
-      const int i = x / (D / 4), d4 = (x % (D / 4)) * 4;
-      const int gi = qr0 + owner + i * CL;
-      if (gi >= nq) continue;
-      float4 pv[CL];
+  // thread: residue q = tid / 64 of the ranks, output quad (row k, d4) = tid % 64
+  const int q = tid >> 6, slot = tid & 63, k = slot / (D / 4), d4 = (slot % (D / 4)) * 4;
+  if (k < cnt) {
+    const int i = i0 + k * step;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // the (at most 16) partials of this residue load together, then add in rank order
+    float4 v[16];
 #pragma unroll
-      for (int c = 0; c < CL; ++c)
-        pv[c] = GLOBAL ? __ldcg(reinterpret_cast<const float4*>(row(c, i) + d4))
-                       : *reinterpret_cast<const float4*>(row(c, i) + d4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < 16; ++u) {
+      const int c = q + 4 * u;
+      if (c < n_ranks)
+        v[u] = GLOBAL ? __ldcg(reinterpret_cast<const float4*>(part(c, i) + d4))
+                      : *reinterpret_cast<const float4*>(part(c, i) + d4);
+    }
 #pragma unroll
-      for (int c = 0; c < CL; ++c) {
-        const float w = WS[i * CL + c];
-        acc.x += w * pv[c].x;
-        acc.y += w * pv[c].y;
-        acc.z += w * pv[c].z;
-        acc.w += w * pv[c].w;
+    for (int u = 0; u < 16; ++u) {
+      const int c = q + 4 * u;
+      if (c < n_ranks) {
+        const float w = WS[k * 64 + c];
+        acc.x += w * v[u].x;
+        acc.y += w * v[u].y;
+        acc.z += w * v[u].z;
+        acc.w += w * v[u].w;
       }
-      const float il = IL[i];
+    }
+    AC[q * 64 + slot] = acc;
+  }
+  grp.sync();
+  if (q == 0 && k < cnt) {
+    const int i = i0 + k * step;
+    const int gi = qr0 + i;
+    if (gi < nq) {
+      const float4 s0 = AC[slot], s1 = AC[64 + slot], s2 = AC[128 + slot], s3 = AC[192 + slot];
+      const float il = IL[k];
+      const float ox = ((s0.x + s1.x) + s2.x) + s3.x, oy = ((s0.y + s1.y) + s2.y) + s3.y;
+      const float oz = ((s0.z + s1.z) + s2.z) + s3.z, ow = ((s0.w + s1.w) + s2.w) + s3.w;
       const int t = row0 + gi / G, hq = kvh * G + gi % G;
       const size_t o = ((size_t)t * a.Hq + hq) * D + d4;
-      put_plane(a.o_hi, a.o_lo, a.out_bf16, o, acc.x * il);
-      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 1, acc.y * il);
-      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 2, acc.z * il);
-      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 3, acc.w * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o, ox * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 1, oy * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 2, oz * il);
+      put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 3, ow * il);
     }
   }
+  grp.sync();
 }
 
 }  // namespace attn

@@ -52,7 +52,7 @@ constexpr int GRP_BAR = 1;                  // named barrier of the compute grou
 
 constexpr size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 constexpr size_t EPI_BYTES = (size_t)EG * YLD * 4 + (size_t)EPI_SCRATCH_FLOATS * 4;
-constexpr size_t ATT_BYTES = attn::Geo<D>::TILE_SMEM + (size_t)(attn::QR + attn::QR) * 4;  // + merge weights
+constexpr size_t ATT_BYTES = attn::Geo<D>::TILE_SMEM + (size_t)(2 * 64 + 4) * 4 + 4 * 64 * 16;  // + merge scratch
 // fixup inputs fetched with the partial sums: row scales, sums of squares,
 // then residual rows (RESID) or RoPE rows (QKV), and the next-norm gains
 constexpr size_t PF_FLOATS = EG + EG * EPI_MAX_SSQ + EG * NTILE + NTILE;
@@ -642,13 +642,13 @@ __device__ bool gemm_fixup(const Ctx& c, const Item& it, int& ga_loaded) {
 }
 
 // The attention items of one layer: first every tile's partial rows (which
-// wait only for the QKV phase), then every owned-row merge (which waits for
-// the CL tiles of its group).  False on abort.
-template <int CL>
+// wait only for the QKV phase), then every rank's row merges (which wait for
+// the R ranks of its group).  Rank r merges rows r, r + R, ...  False on abort.
 __device__ bool attention_phase(const Ctx& c, int ph) {
   const MkArgs& a = *c.a;
   using Gm = attn::Geo<D>;
-  constexpr int RLD = Gm::RLD, RPC = attn::QR / CL, QR = attn::QR;
+  constexpr int RLD = Gm::RLD, QR = attn::QR;
+  const int R = a.ranks;
   const int l = ph / 5;
   const int n = a.n_items[1];
   const int j0 = first_item(a, ph, blockIdx.x);
@@ -657,18 +657,20 @@ __device__ bool attention_phase(const Ctx& c, int ph) {
   c.grp.sync();
   const AttnArgs& at = *c.sAA;
   const int per_slot = a.Hkv * a.n_rg;
+  const int G = at.Hq / at.Hkv;
   unsigned* tctr = a.ctr + tile_ctr_base(a.L) + (size_t)ph * MAXT;
-  float* WSm = reinterpret_cast<float*>(c.sC + Gm::TILE_SMEM);
-  float* ILm = WSm + QR;
+  float* WSm = reinterpret_cast<float*>(c.sC + Gm::TILE_SMEM);  // [2][64]
+  float* ILm = WSm + 2 * 64;                                      // [2] (+ pad)
+  float4* ACm = reinterpret_cast<float4*>(ILm + 4);               // [4][64]
   const unsigned qkv_target = c.e1 * (unsigned)n_done(a, ph - 1);
   bool qkv_ready = false;
   for (int j = j0; j < n; j += a.G) {
-    const int rank = j % CL, grp_id = j / CL;
+    const int rank = j % R, grp_id = j / R;
     const int y = grp_id % per_slot, slot = grp_id / per_slot;
     const int kvh = y % a.Hkv, rg = y / a.Hkv;
     const int req = at.slot_req[slot];
     const attn::KvPlanes kv = attn::kv_planes(at, req, kvh, D);
-    const bool pre = attn::tile_prefetch<D, CL>(c.sC, kv, rank, at.st[req].cache_len, c.grp.tid);
+    const bool pre = attn::tile_prefetch<D>(c.sC, kv, rank, R, at.st[req].cache_len, c.grp.tid);
     if (!qkv_ready) {
       if (!grp_wait_ctr(c, a.ctr + CTR_PHASE + ph - 1, qkv_target)) {
         attn::cp_async_wait<0>();
@@ -677,23 +679,36 @@ __device__ bool attention_phase(const Ctx& c, int ph) {
       qkv_ready = true;
       c.ev(ph, EV_ATT_READY);
     }
-    attn::tile_partial<D, CL>(at, c.sC, c.grp, kv, rank, kvh, rg * QR, slot * a.rows_per_slot, a.rows_per_slot,
-                              pre, c.s_maxlim);
-    const float4* src = reinterpret_cast<const float4*>(attn::staged_rows<D>(c.sC));
-    float4* dst = reinterpret_cast<float4*>(a.att_part + ((size_t)grp_id * CL + rank) * QR * RLD);
-    for (int x = c.grp.tid; x < QR * RLD / 4; x += c.grp.n) __stcg(dst + x, src[x]);
+    const int row0 = slot * a.rows_per_slot, nrows = a.rows_per_slot, qr0 = rg * QR;
+    const bool rows = qr0 < nrows * G;
+    const int n_chunks =
+        rows ? attn::tile_partial<D>(at, c.sC, c.grp, kv, rank, R, kvh, qr0, row0, nrows, pre, c.s_maxlim) : 0;
+    if (rows && rank < n_chunks) {
+      const float4* src = reinterpret_cast<const float4*>(attn::staged_rows<D>(c.sC));
+      float4* dst = reinterpret_cast<float4*>(at.part + ((size_t)grp_id * R + rank) * QR * RLD);
+      for (int x = c.grp.tid; x < QR * RLD / 4; x += c.grp.n) __stcg(dst + x, src[x]);
+    } else {
+      attn::cp_async_wait<0>();
+    }
     grp_publish(c, tctr + grp_id, false);
     c.ev(ph, EV_ATT_PART);
   }
   for (int j = j0; j < n; j += a.G) {
-    const int rank = j % CL, grp_id = j / CL;
+    const int rank = j % R, grp_id = j / R;
     const int y = grp_id % per_slot, slot = grp_id / per_slot;
     const int kvh = y % a.Hkv, rg = y / a.Hkv;
-    if (!grp_wait_ctr(c, tctr + grp_id, c.e1 * (unsigned)CL)) return false;
-    const float* base = a.att_part + (size_t)grp_id * CL * QR * RLD + (size_t)rank * RPC * RLD;
-    auto row = [&](int src, int i) -> const float* { return base + ((size_t)src * QR + i) * RLD; };
-    attn::merge_owned<D, CL, decltype(row), true>(at, c.grp, row, WSm, ILm, rank, kvh, rg * QR,
-                                                  slot * a.rows_per_slot, a.rows_per_slot, true);
+    if (!grp_wait_ctr(c, tctr + grp_id, c.e1 * (unsigned)R)) return false;
+    const int row0 = slot * a.rows_per_slot, nrows = a.rows_per_slot, qr0 = rg * QR;
+    if (qr0 < nrows * G && rank < QR) {
+      const int n_chunks = attn::tile_chunks(at, c.grp, qr0, row0, nrows, c.s_maxlim);
+      const int n_ranks = n_chunks < R ? n_chunks : R;
+      const float* base = at.part + (size_t)grp_id * R * QR * RLD;
+      auto part = [&](int src, int i) -> const float* { return base + ((size_t)src * QR + i) * RLD; };
+      const int cnt = (QR - rank + R - 1) / R;  // rows rank, rank + R, ... of the 64
+      for (int k0 = 0; k0 < cnt; k0 += 2)
+        attn::merge_rows<D, true>(at, c.grp, part, WSm, ILm, ACm, n_ranks, R, rank + k0 * R, R,
+                                  cnt - k0 < 2 ? cnt - k0 : 2, kvh, qr0, row0, nrows);
+    }
     grp_publish(c, a.ctr + CTR_PHASE + ph, true);
     c.ev(ph, EV_ATT_MERGED);
   }
@@ -703,13 +718,12 @@ __device__ bool attention_phase(const Ctx& c, int ph) {
 // Phase by phase: attention items, or every GEMM item's drain and then every
 // split item's fixup.  Drains wait only for the previous phase, so no CTA
 // waits on a tile whose partials sit behind its own pending fixup.
-template <int CL>
 __device__ void compute_group(const Ctx& c) {
   const MkArgs& a = *c.a;
   int gi = 0, ga_loaded = -1;
   for (int ph = 0; ph <= 5 * a.L; ++ph) {
     if (is_att(a, ph)) {
-      if (!attention_phase<CL>(c, ph)) return;
+      if (!attention_phase(c, ph)) return;
       continue;
     }
     const int n = n_items(a, ph);
@@ -752,7 +766,6 @@ __device__ void compute_group(const Ctx& c) {
 
 // ---------------------------------------------------------------- kernel
 
-template <int CL>
 __global__ void __launch_bounds__(THREADS, 1) forward_mk_kernel(const MkArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -846,7 +859,7 @@ __global__ void __launch_bounds__(THREADS, 1) forward_mk_kernel(const MkArgs a) 
     c.s_req = s_req;
     c.s_rs = s_rs;
     c.ev(0, EV_START);
-    compute_group<CL>(c);
+    compute_group(c);
     c.ev(5 * a.L, EV_END);
     attn::cp_async_wait<0>();
   }
@@ -871,30 +884,28 @@ size_t forward_mk_smem(int nt, int ws_stages, int as_stages) {
          mk::AA_BYTES + (size_t)(2 * ws_stages + 2 * as_stages + 5) * 8;
 }
 
-template <int CL>
 static bool mk_configure(size_t smem) {
   static size_t configured = 0;
   if (smem <= configured) return true;
-  if (cudaFuncSetAttribute(mk::forward_mk_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+  if (cudaFuncSetAttribute(mk::forward_mk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return false;
-  prefer_shared(reinterpret_cast<const void*>(mk::forward_mk_kernel<CL>));
+  prefer_shared(reinterpret_cast<const void*>(mk::forward_mk_kernel));
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mk::forward_mk_kernel<CL>, mk::THREADS, smem) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mk::forward_mk_kernel, mk::THREADS, smem) != cudaSuccess ||
       n < 1)
     return false;
   configured = smem;
   return true;
 }
 
-bool forward_mk_fits(int head_dim, int CL) { return head_dim == mk::D && (CL == 8 || CL == 16); }
+bool forward_mk_fits(int head_dim) { return head_dim == mk::D; }
 
 bool launch_forward_mk(const MkArgs& a, int head_dim, cudaStream_t s, bool pdl) {
-  if (!forward_mk_fits(head_dim, a.CL)) return false;
+  if (!forward_mk_fits(head_dim) || a.ranks < 1 || a.ranks > 64) return false;
   const size_t smem = forward_mk_smem(a.nt, a.ws_stages, a.as_stages);
   if (smem > 227 * 1024) return false;
-  const bool ok = a.CL == 16 ? mk_configure<16>(smem) : mk_configure<8>(smem);
-  if (!ok) return false;
+  if (!mk_configure(smem)) return false;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.G);
   cfg.blockDim = dim3(mk::THREADS);
@@ -905,9 +916,7 @@ bool launch_forward_mk(const MkArgs& a, int head_dim, cudaStream_t s, bool pdl) 
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  const cudaError_t e = a.CL == 16 ? cudaLaunchKernelEx(&cfg, mk::forward_mk_kernel<16>, a)
-                                   : cudaLaunchKernelEx(&cfg, mk::forward_mk_kernel<8>, a);
-  return e == cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, mk::forward_mk_kernel, a) == cudaSuccess;
 }
 
 }  // namespace gocr

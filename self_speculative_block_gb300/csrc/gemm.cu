@@ -42,14 +42,22 @@ static int split_chunk_limit() {
   return lim;
 }
 
-// CTAs per SM the wave rule fills (GOCR_SPLIT_K=wave1 or wave2).
-static int wave_ctas_per_sm() {
-  static int w = 0;
+// CTAs per SM the wave rule fills and its split cap
+// (GOCR_SPLIT_K=wave<ctas per SM>[:<max splits>], default wave2:12).
+static void wave_params(int* ctas, int* cap) {
+  static int w = 0, c = 0;
   if (!w) {
+    w = 2;
+    c = MAX_SPLITS;
     const char* v = getenv("GOCR_SPLIT_K");
-    w = (v && strcmp(v, "wave1") == 0) ? 1 : 2;
+    if (v && strncmp(v, "wave", 4) == 0) {
+      if (v[4] >= '1' && v[4] <= '4') w = v[4] - '0';
+      const char* colon = strchr(v, ':');
+      if (colon && atoi(colon + 1) >= 1 && atoi(colon + 1) <= 16) c = atoi(colon + 1);
+    }
   }
-  return w;
+  *ctas = w;
+  *cap = c;
 }
 
 int gemm_kchunk(int N, int K) {
@@ -60,8 +68,10 @@ int gemm_kchunk(int N, int K) {
   if (lim > 0) {
     s = cdiv(kb, lim / 64);
   } else {
-    s = (wave_ctas_per_sm() * SM_COUNT) / tiles;  // CTAs per SM in one wave
-    if (s > MAX_SPLITS) s = MAX_SPLITS;
+    int w, cap;
+    wave_params(&w, &cap);
+    s = (w * SM_COUNT) / tiles;  // CTAs per SM in one wave
+    if (s > cap) s = cap;
   }
   if (s > kb) s = kb;
   if (s < 1) s = 1;

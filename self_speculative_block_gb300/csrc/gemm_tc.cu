@@ -156,6 +156,19 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     s_fail = 0;
     tc::grid_dep_launch();
   }
+  if (tid == 96 && a.pf_next) {
+    // this CTA's share of the next GEMM's weights into L2, in 32 KB pieces
+    const unsigned n_cta = gridDim.x * gridDim.y * gridDim.z;
+    const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const size_t piece = 32768, pieces = (a.pf_bytes + piece - 1) / piece;
+    for (size_t i = cta; i < pieces; i += n_cta) {
+      const size_t off = i * piece;
+      const size_t len = a.pf_bytes - off < piece ? a.pf_bytes - off : piece;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((const char*)a.pf_next + off),
+                   "r"((unsigned)(len & ~(size_t)15))
+                   : "memory");
+    }
+  }
   __syncwarp();
   if (warp == 0) tc::tmem_alloc(tmem_holder, ncols);
   tc::fence_before_sync();

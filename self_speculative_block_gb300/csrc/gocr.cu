@@ -15,6 +15,7 @@
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -93,9 +94,12 @@ struct gocr_handle {
   void* q_hi = nullptr;       // rotated query planes [T][q_dim]
   void* q_lo = nullptr;
   float* logits = nullptr;
+  float* att_part = nullptr;  // attention partial rows of the key-chunk ranks (bf16 models)
+  int* att_chunks = nullptr;  // chunks per (slot, kv head x row group) of the last attention
   unsigned long long* amax = nullptr;
   int* grid_ctr = nullptr;
   bool pdl = true;            // programmatic dependent launch between forward kernels
+  bool l2_prefetch = true;    // GEMMs prefetch the next GEMM's weights into L2 (GOCR_L2_PREFETCH=0: off)
   bool host_loop = false;     // GOCR_HOST_LOOP=1: per-round graphs driven by the host
   int* dbuf = nullptr;
   int* vbuf = nullptr;
@@ -125,9 +129,7 @@ struct gocr_handle {
   unsigned* mk_ctr = nullptr;
   size_t mk_ctr_bytes = 0;
   float* mk_part = nullptr;
-  float* mk_att = nullptr;
   int mk_T_max = 0;
-  int mk_att_items = 0;
   int mk_G = 0;
   int mk_pf = 16;
   unsigned long long* mk_trace = nullptr;
@@ -247,6 +249,8 @@ void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_o
     if (kind != PLAN_PREFILL) at.st = h->st;
     at.T = T; at.Hq = c.n_q_heads; at.Hkv = c.n_kv_heads; at.d = c.head_dim; at.cap = h->cap;
     at.scale = 1.0f / sqrtf((float)c.head_dim);
+    at.part = h->att_part;
+    at.part_chunks = h->att_chunks;
     f.at.push_back(at);
     // O projection + residual; planes of resid * g_mlp for the MLP
     GemmArgs go = gemm_base(h, h->at_hi, h->at_lo, h->q_dim, h->wo[l], T, H, h->q_dim);
@@ -279,6 +283,14 @@ void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_o
   gl.e.logits = logits; gl.e.ld_logits = c.vocab;
   gl.e.amax = h->amax; gl.e.am_out = am_out; gl.e.grid_ctr = h->grid_ctr;
   f.g.push_back(gl);
+  // each GEMM brings the next GEMM's weights into L2 (at most 48 MB of them)
+  if (h->l2_prefetch)
+    for (size_t i = 0; i + 1 < f.g.size(); ++i) {
+      const GemmArgs& nx = f.g[i + 1];
+      const size_t bytes = (size_t)nx.N * nx.K * h->es;
+      f.g[i].pf_next = nx.w;
+      f.g[i].pf_bytes = bytes < ((size_t)48 << 20) ? bytes : ((size_t)48 << 20);
+    }
 }
 
 // Whether the persistent kernel runs this forward, and its launch arguments
@@ -288,8 +300,7 @@ bool mk_shape(gocr_handle* h, int kind, int n_slots, int B, MkArgs& a) {
   if (!h->mk_enabled || h->dtype != GOCR_DTYPE_BF16 || kind == PLAN_PREFILL) return false;
   const int T = n_rows_of(kind, n_slots, B, 0);
   if (T < 1 || T > h->mk_T_max || T % n_slots) return false;
-  const int CL = attention_cluster_width(c.head_dim);
-  if (!forward_mk_fits(c.head_dim, CL)) return false;
+  if (!forward_mk_fits(c.head_dim)) return false;
   a = MkArgs{};
   a.L = c.n_layers;
   a.T = T;
@@ -299,7 +310,7 @@ bool mk_shape(gocr_handle* h, int kind, int n_slots, int B, MkArgs& a) {
   const int G = c.n_q_heads / c.n_kv_heads;
   a.n_rg = (a.rows_per_slot * G + 63) / 64;
   a.Hkv = c.n_kv_heads;
-  a.CL = CL;
+  a.ranks = attention_ranks(h->cap);
   a.G = h->mk_G;
   const int NK[5][2] = {{h->qkv_n, c.hidden}, {c.hidden, h->q_dim}, {h->gu_n, c.hidden}, {c.hidden, c.ffn},
                         {c.vocab, c.hidden}};
@@ -314,11 +325,11 @@ bool mk_shape(gocr_handle* h, int kind, int n_slots, int B, MkArgs& a) {
     if (a.splits[k] > 16 || ((k < 4 || a.splits[k] > 1) && a.tiles[k] > mk::MAXT)) return false;
   }
   a.n_items[0] = a.tiles[0] * a.splits[0];
-  a.n_items[1] = n_slots * a.Hkv * a.n_rg * CL;
+  a.n_items[1] = n_slots * a.Hkv * a.n_rg * a.ranks;
   a.n_items[2] = a.tiles[1] * a.splits[1];
   a.n_items[3] = a.tiles[2] * a.splits[2];
   a.n_items[4] = a.tiles[3] * a.splits[3];
-  if (a.n_items[1] > h->mk_att_items || a.n_items[1] / CL > mk::MAXT) return false;
+  if (a.n_items[1] / a.ranks > mk::MAXT) return false;
   int acc = 0;
   for (int k = 0; k < 5; ++k) {
     a.prefix[k] = acc;
@@ -344,7 +355,6 @@ bool mk_shape(gocr_handle* h, int kind, int n_slots, int B, MkArgs& a) {
   a.trace_cap = h->mk_trace_cap;
   a.ctr = h->mk_ctr;
   a.part = h->mk_part;
-  a.att_part = h->mk_att;
   a.err = h->err;
   return forward_mk_smem(a.nt, a.ws_stages, a.as_stages) <= cap;
 }
@@ -686,6 +696,8 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
   {
     const char* hl = getenv("GOCR_HOST_LOOP");
     h->host_loop = hl && hl[0] == '1';
+    const char* lp = getenv("GOCR_L2_PREFETCH");
+    h->l2_prefetch = !(lp && lp[0] == '0');
   }
   CKC(cudaStreamCreateWithFlags(&h->hs, cudaStreamNonBlocking));
   CKC(cudaEventCreate(&h->ev0));
@@ -739,6 +751,16 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
   }
   h->ssq = (float*)A((size_t)T * (H / NTILE) * 4);
   h->logits = (float*)A((size_t)h->T_dec * c.vocab * 4);
+  if (h->dtype == GOCR_DTYPE_BF16) {
+    // partial rows of the attention ranks: a prefill (one slot of up to
+    // max_ctx rows) or a decode forward (max_requests slots of max_block + 1 rows)
+    const size_t pf = attention_part_floats(1, c.max_ctx, c.n_q_heads, c.n_kv_heads, c.head_dim);
+    const size_t df = attention_part_floats(R, c.max_block + 1, c.n_q_heads, c.n_kv_heads, c.head_dim);
+    h->att_part = (float*)A((pf > df ? pf : df) * 4);
+    const size_t pg = (size_t)c.n_kv_heads * ((c.max_ctx * (c.n_q_heads / c.n_kv_heads) + 63) / 64);
+    const size_t dg = (size_t)R * c.n_kv_heads * (((c.max_block + 1) * (c.n_q_heads / c.n_kv_heads) + 63) / 64);
+    h->att_chunks = (int*)A((pg > dg ? pg : dg) * 4);
+  }
   h->amax = (unsigned long long*)A((size_t)T * 8);
   h->grid_ctr = (int*)A(256);
   h->dbuf = (int*)A((size_t)h->T_dec * 4);
@@ -795,8 +817,6 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
       if (f > part) part = f;
     }
     h->mk_part = (float*)A(part * h->mk_T_max * 4);
-    h->mk_att_items = 1024;
-    h->mk_att = (float*)A((size_t)h->mk_att_items * 64 * (c.head_dim + 4) * 4);
     h->mk_ctr_bytes = mk::ctr_words(c.n_layers) * 4;
     h->mk_ctr = (unsigned*)A(h->mk_ctr_bytes);
     const char* ot = getenv("GOCR_OP_TRACE");
@@ -922,9 +942,30 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
     CK(cudaMemcpy(h->op_trace, init.data(), init.size() * 8, cudaMemcpyHostToDevice));
     h->op_trace_next = true;
   }
+  // GOCR_DEBUG_GRAPH=1: run the forward from a captured graph, as a decode
+  // round runs it (a profiling aid: launch timing differs from eager launches)
+  const char* dg = getenv("GOCR_DEBUG_GRAPH");
+  const bool as_graph = dg && dg[0] == '1';
+  cudaGraph_t graph = nullptr;
+  if (as_graph) CK(cudaStreamBeginCapture(h->hs, cudaStreamCaptureModeThreadLocal));
   launch_plan(pk, h->rows, h->st, h->slot_one, 1, B, 0, nullptr, h->dbg_toks, h->cap, h->hs, false);
   const bool enq = enqueue_forward(h, pk, 1, B, 0, h->am, h->logits, h->slot_one);
   h->op_trace_next = false;
+  if (as_graph) {
+    const cudaError_t ce = cudaStreamEndCapture(h->hs, &graph);
+    if (!enq || ce != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      return fail(h, GOCR_ECUDA, "debug forward capture failed");
+    }
+    cudaGraphExec_t ge = nullptr;
+    const cudaError_t ie = cudaGraphInstantiate(&ge, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) return fail(h, GOCR_ECUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(ie));
+    const cudaError_t le = cudaGraphLaunch(ge, h->hs);
+    cudaStreamSynchronize(h->hs);
+    cudaGraphExecDestroy(ge);
+    if (le != cudaSuccess) return fail(h, GOCR_ECUDA, "cudaGraphLaunch: %s", cudaGetErrorString(le));
+  }
   if (!enq) return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   CK(cudaGetLastError());
   if (logits_out)
@@ -1112,6 +1153,31 @@ int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void*
   a.req_stride = 0; a.o_hi = o; a.o_lo = nullptr; a.out_bf16 = 0;
   a.row_lim = lim; a.plan = nullptr;
   a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.cap = cap; a.scale = 1.0f / sqrtf((float)d);
+  if (dtype == GOCR_DTYPE_BF16) {
+    // partial rows of the attention ranks: a process-wide scratch buffer per
+    // device, grown on demand (calls must not overlap on the GPU)
+    static std::mutex mu;
+    static std::vector<std::pair<void*, size_t>> bufs(64, {nullptr, 0});
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return fail(h, GOCR_ECUDA, "device index %d", dev);
+    const size_t groups = (size_t)Hkv * ((T * (Hq / Hkv) + 63) / 64);
+    const size_t part_bytes = (attention_part_floats(1, T, Hq, Hkv, d) * 4 + 255) & ~(size_t)255;
+    const size_t need = part_bytes + groups * 4;
+    std::lock_guard<std::mutex> lk(mu);
+    if (bufs[dev].second < need) {
+      if (bufs[dev].first) {
+        CK(cudaStreamSynchronize((cudaStream_t)stream));
+        cudaFree(bufs[dev].first);
+      }
+      bufs[dev] = {nullptr, 0};
+      void* p = nullptr;
+      if (cudaMalloc(&p, need) != cudaSuccess) return fail(h, GOCR_ENOMEM, "attention scratch allocation failed");
+      bufs[dev] = {p, need};
+    }
+    a.part = (float*)bufs[dev].first;
+    a.part_chunks = (int*)((char*)bufs[dev].first + part_bytes);
+  }
   if (!launch_attention(dtype, a, 1, T, (cudaStream_t)stream, false))
     return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   CK(cudaGetLastError());

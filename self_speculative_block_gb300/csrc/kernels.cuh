@@ -70,6 +70,11 @@ struct alignas(16) GemmArgs {  // 16-byte aligned: tables of them are copied by 
   int* counters;                 // CUDA-core path: tile counters, zero between launches
   int epi;
   EpiArgs e;
+  // weights of the forward's next GEMM: the launch's CTAs bring pf_bytes of
+  // them into L2 at their start (NULL = none), so that the next kernel's
+  // weight loads hit L2 (the forward is a fixed sequence of matrices)
+  const void* pf_next;
+  size_t pf_bytes;
   // optional launch timeline record (4 words: first CTA start, first and last
   // release from the dependency wait, last CTA end; globaltimer ns)
   unsigned long long* trace;
@@ -105,12 +110,22 @@ struct alignas(16) AttnArgs {
   const int* slot_req; const ReqState* st; int rows_per_slot;
   int T, Hq, Hkv, d, cap;
   float scale;
+  // tensor-core path: partial rows of the ranks, [slot][kv head x row group][rank][64][d + 4] fp32
+  float* part;
+  int* part_chunks;           // [slot][kv head x row group] chunks the group's rows read
   unsigned long long* trace;  // launch timeline record, as GemmArgs::trace
 };
-// Cluster width of the tensor-core attention kernel for head dim d (16 or 8),
-// fixed once per process: it decides which tile reads which key chunk and the
-// order of the merge.
-int attention_cluster_width(int d);
+// Key-chunk ranks of the tensor-core attention: rank r reads chunks r, r + R, ...
+// R = attention_ranks(cap): at most ATTN_RANKS, and no more than a KV
+// capacity of cap keys has chunks of 32.  R is fixed by the capacity, so every
+// forward of a handle splits a row's keys the same way.
+constexpr int ATTN_RANKS = 48;
+inline int attention_ranks(int cap) {
+  const int c = (cap + 31) / 32;
+  return c < 1 ? 1 : (c < ATTN_RANKS ? c : ATTN_RANKS);
+}
+// fp32 words of the tensor-core attention's partial rows for n_slots slots of up to max_rows rows
+size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d);
 // dtype 1: tensor-core cluster kernel; 0: CUDA-core kernel.
 bool launch_attention(int dtype, const AttnArgs& a, int n_slots, int max_rows_per_slot, cudaStream_t s,
                       bool pdl);
@@ -134,9 +149,9 @@ struct MkArgs {
                            // GEMM-input planes hi/lo, attention-output planes hi/lo, SwiGLU planes hi/lo
   unsigned* ctr;           // device counters, mk::ctr_words(L) words, zero at the first forward
   float* part;             // split-K partial tiles [S][T][N] of the running phase
-  float* att_part;         // attention partial rows [group][CL][64][D + 4]
   int* err;
-  int L, T, nt, n_slots, rows_per_slot, n_rg, Hkv, CL;
+  int L, T, nt, n_slots, rows_per_slot, n_rg, Hkv;
+  int ranks;               // attention key-chunk ranks (ATTN_RANKS); partial rows in AttnArgs::part
   int G;                   // CTAs (one per SM)
   int ws_stages, as_stages, pf_blocks;
   int N[5], K[5], tiles[5], splits[5], kchunk[5];  // per GEMM kind: QKV, O, GU, DN, LM
@@ -155,7 +170,7 @@ enum : int { EV_START = 0, EV_DEP = 1, EV_ACC = 2, EV_DRAINED = 3, EV_FIXED = 4,
 }
 // Shared-memory bytes and launch check; false when the shapes do not fit.
 size_t forward_mk_smem(int nt, int ws_stages, int as_stages);
-bool forward_mk_fits(int head_dim, int CL);
+bool forward_mk_fits(int head_dim);
 bool launch_forward_mk(const MkArgs& a, int head_dim, cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------- small kernels
