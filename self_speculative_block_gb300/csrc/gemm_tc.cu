@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, ncols);
+  if (TRACE && tid == 0) trace_mark(a.trace, 7);
 
   if (S == 1) {
     if (!failed) {
@@ -309,6 +310,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     if (tid == 0) tc::mbar_expect_tx(rxbar, (uint32_t)((S - 1) * (tb - ta) * YLD * 4));
     tc::fence_proxy_async_smem();
     cluster.sync();  // every partial tile is written and every receive barrier armed
+    if (TRACE && tid == 0) trace_mark(a.trace, 6);
     if (tid == 0) {
       for (int r = 0; r < S; ++r) {
         const int ra = min(tn, r * per), rb = min(tn, ra + per);

@@ -202,7 +202,8 @@ void launch_set_override(ReqState* st, int req, int n_ref, int n_sched, cudaStre
 // Launch timeline records (GemmArgs::trace, TRACE_WORDS words): word 0 min of
 // CTA start times, 1 and 2 min / max of dependency-release times, 3 max of
 // CTA end times; GEMMs also 4 max of mainloop-done times, 5 max of split-K
-// exchange-done times; attention 4 max of first-chunk-ready times, 5 max of
+// exchange-done times, 6 max of cluster-barrier-passed times, 7 max of
+// accumulator-drained times; attention 4 max of first-chunk-ready times, 5 max of
 // chunk-loop-done times, 6 max of merge-exchange-done times.
 constexpr int TRACE_WORDS = 8;
 __device__ __forceinline__ unsigned long long trace_now() {
