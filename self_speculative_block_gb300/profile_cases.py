@@ -3,9 +3,10 @@
     python -m self_speculative_block_gb300.profile_cases draft
         0.5B-class bf16 decoder, 1024-row synthetic prefill, then two draft
         forwards (B = 32, 33 rows).  The prefill launches gemm_tc_kernel 65
-        times and attention_mma_kernel 16 times, so the first draft forward's
-        QKV / O / gate-up / down GEMMs are gemm_tc launches 65..68 and its first
-        attention is attention_mma launch 16.
+        times and attention_part_kernel / attention_merge_kernel 16 times
+        each, so the first draft forward's QKV / O / gate-up / down GEMMs are
+        gemm_tc launches 65..68 and its first attention is attention_part and
+        attention_merge launch 16.
     python -m self_speculative_block_gb300.profile_cases sweep
         The split-K GEMM over one forward's 65 weight matrices (16 x packed
         QKV, O, packed gate/up, down, then the LM head) at the decode launch
