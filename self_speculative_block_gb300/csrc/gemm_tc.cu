@@ -369,6 +369,212 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 
+// Many-slice variant (more than two 128-token slices, e.g. prefill and the
+// batched round): one CTA per (128-row weight tile, token slice) runs the S
+// K chunks of the split rule one after another.  Each chunk's MMAs start a
+// fresh accumulator (two in TMEM, so the next chunk's MMAs overlap this
+// chunk's drain), and four drain warps add the chunk sums into a shared-memory
+// running sum in chunk order: p0 + p1 + ... + p(S-1), the clustered kernel's
+// reduction, so a token's bits do not depend on which kernel ran it.  Warp 0:
+// TMA producer; warp 1: MMA issuer; warps 4-7: drain; all eight warps run the
+// epilogue.
+constexpr int SEQ_THREADS = 256;
+
+template <int EPI, bool TRACE>
+__global__ void __launch_bounds__(SEQ_THREADS) gemm_tc_seq_kernel(const __grid_constant__ CUtensorMap tmw,
+                                                                 const __grid_constant__ CUtensorMap tmx_hi,
+                                                                 const __grid_constant__ CUtensorMap tmx_lo,
+                                                                 GemmArgs a, int nt, int two, int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int b_bytes = (two ? 2 : 1) * nt * 128;
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + stages * A_BYTES;
+  float* Ysum = reinterpret_cast<float*>(sB + stages * b_bytes);  // [nt][YLD] running sum over chunks
+  float* scratch = Ysum + (size_t)nt * YLD;                       // epilogue scratch
+  uint64_t* full = reinterpret_cast<uint64_t*>(scratch + EPI_SCRATCH_FLOATS);
+  uint64_t* empty = full + stages;
+  uint64_t* accf = empty + stages;  // [2] chunk accumulator ready
+  uint64_t* acce = accf + 2;        // [2] chunk accumulator drained
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acce + 2);
+  __shared__ int s_fail;
+  __shared__ int s_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile = blockIdx.x, z = blockIdx.z;
+  const int n0 = tile * NTILE;
+  const int t0 = z * TZ_TC;
+  const int tn = min(TZ_TC, a.T - t0);
+  const int S = a.splits, kpc = a.kchunk / 64, nkb_all = cdiv_i(a.K, 64);
+  const int nmma = (two ? 2 : 1) * nt;
+  const uint32_t bufcols = nmma <= 32 ? 32 : (nmma <= 64 ? 64 : (nmma <= 128 ? 128 : 256));
+
+  if (tid == 0) {
+    if (TRACE) trace_mark(a.trace, 0);
+    tc::prefetch_tmap(&tmw);
+    tc::prefetch_tmap(&tmx_hi);
+    if (two) tc::prefetch_tmap(&tmx_lo);
+    for (int st = 0; st < stages; ++st) {
+      tc::mbar_init(&full[st], 1);
+      tc::mbar_init(&empty[st], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 1);
+      tc::mbar_init(&acce[b], 4);  // one arrival per drain warp
+    }
+    tc::fence_mbar_init();
+    s_fail = 0;
+    tc::grid_dep_launch();
+  }
+  __syncwarp();
+  if (warp == 0) tc::tmem_alloc(tmem_holder, 2 * bufcols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  if (tid == 0) {
+    // TMA producer: every k block of the tile, chunk after chunk; the first
+    // stages' weight tiles go out before the grid dependency wait
+    const uint64_t pol = tc::policy_evict_first();
+    const int pre = nkb_all < stages ? nkb_all : stages;
+    for (int kb = 0; kb < pre; ++kb) {
+      tc::mbar_expect_tx(&full[kb], A_BYTES + b_bytes);
+      tc::tma_load_2d_hint(sA + kb * A_BYTES, &tmw, kb * 64, n0, &full[kb], pol);
+    }
+    for (int kb = pre; kb < nkb_all && kb < pre + L2_PREFETCH_BLOCKS; ++kb) tc::tma_prefetch_2d(&tmw, kb * 64, n0);
+    tc::grid_dep_wait();
+    if (TRACE) trace_mark(a.trace, 1);
+    for (int kb = 0; kb < nkb_all; ++kb) {
+      const int st = kb % stages;
+      const int use = kb / stages;
+      if (kb >= pre) {
+        if (!tc::mbar_wait(&empty[st], (use - 1) & 1)) { s_fail = 1; break; }
+        tc::mbar_expect_tx(&full[st], A_BYTES + b_bytes);
+        tc::tma_load_2d_hint(sA + st * A_BYTES, &tmw, kb * 64, n0, &full[st], pol);
+        if (kb + L2_PREFETCH_BLOCKS < nkb_all) tc::tma_prefetch_2d(&tmw, (kb + L2_PREFETCH_BLOCKS) * 64, n0);
+      }
+      uint8_t* b = sB + st * b_bytes;
+      tc::tma_load_2d(b, &tmx_hi, kb * 64, t0, &full[st]);
+      if (two) tc::tma_load_2d(b + nt * 128, &tmx_lo, kb * 64, t0, &full[st]);
+    }
+  } else if (tid == 32) {
+    // MMA issuer: chunk c accumulates into TMEM buffer c & 1
+    const uint32_t idesc = tc::idesc_bf16(NTILE, nmma);
+    int kb = 0;
+    for (int c = 0; c < S && !s_fail; ++c) {
+      const int b = c & 1;
+      if (c >= 2 && !tc::mbar_wait(&acce[b], ((c >> 1) - 1) & 1)) { s_fail = 1; break; }
+      tc::fence_after_sync();
+      const uint32_t d = tmem + (uint32_t)b * bufcols;
+      const int kend = min(nkb_all, (c + 1) * kpc);
+      for (int k0 = kb; kb < kend; ++kb) {
+        const int st = kb % stages;
+        if (!tc::mbar_wait(&full[st], (kb / stages) & 1)) { s_fail = 1; break; }
+        tc::fence_after_sync();
+        const uint32_t a_base = tc::smem_u32(sA + st * A_BYTES);
+        const uint32_t b_base = tc::smem_u32(sB + st * b_bytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16(d, tc::sdesc_sw128(a_base + kk * 32), tc::sdesc_sw128(b_base + kk * 32), idesc,
+                       (kb > k0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(&empty[st]);
+      }
+      tc::mma_commit(&accf[b]);
+    }
+  } else if (warp >= 4) {
+    // drain: chunk sums into Ysum[token][row], added in chunk order
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    for (int c = 0; c < S; ++c) {
+      const int b = c & 1;
+      if (!tc::mbar_wait(&accf[b], (c >> 1) & 1)) {
+        s_fail = 1;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t taddr = tmem + (uint32_t)b * bufcols + ((uint32_t)(q * 32) << 16);
+      for (int g = 0; g < nt / 16; ++g) {
+        float vh[16], vl[16];
+        tc::tmem_ld16(taddr + g * 16, vh);
+        if (two) {
+          tc::tmem_ld16(taddr + nt + g * 16, vl);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) vh[j] += vl[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float* y = Ysum + (size_t)(g * 16 + j) * YLD + row;
+          *y = c == 0 ? vh[j] : *y + vh[j];
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acce[b]);
+    }
+  }
+  __syncwarp();
+  tc::grid_dep_wait();  // the epilogue reads and writes what earlier kernels touch
+  tc::fence_before_sync();
+  __syncthreads();
+  if (TRACE && tid == 0) trace_mark(a.trace, 4);
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 2 * bufcols);
+  }
+  const bool failed = s_fail != 0;
+  if (failed) {
+    if (tid == 0) set_err(a.e.err, DERR_TIMEOUT);
+    return;
+  }
+  for (int g0 = 0; g0 < tn; g0 += EG) {
+    const int cnt = min(EG, tn - g0);
+    apply_epilogue_k<EPI>(a, Ysum + (size_t)g0 * YLD, YLD, tile, t0 + g0, cnt, scratch, EpiPre(), Grp::block());
+  }
+  if (EPI == EPI_ARGMAX) argmax_grid_finish(a, &s_flag);
+  if (TRACE && tid == 0) trace_mark(a.trace, 3);
+}
+
+template <int EPI, bool TRACE>
+static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
+  CUtensorMap tmw, tmh, tml;
+  if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE)) return false;
+  const int nt = TZ_TC;  // several full slices
+  if (!tmap_2d(&tmh, a.x, a.T, a.K, nt)) return false;
+  const int two = a.x_lo != nullptr;
+  if (two) {
+    if (!tmap_2d(&tml, a.x_lo, a.T, a.K, nt)) return false;
+  } else {
+    tml = tmh;
+  }
+  const int stage_bytes = A_BYTES + (two ? 2 : 1) * nt * 128;
+  const size_t fixed = 1024 + (size_t)nt * YLD * 4 + (size_t)EPI_SCRATCH_FLOATS * 4 + 16 * 8 + 64;
+  int stages = (int)((227 * 1024 - 2048 - fixed) / stage_bytes);
+  if (stages > 4) stages = 4;
+  if (stages < 2) return false;
+  const size_t smem = fixed + (size_t)stages * stage_bytes;
+  static size_t configured = 0;
+  if (smem > configured) {
+    if (cudaFuncSetAttribute(gemm_tc_seq_kernel<EPI, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return false;
+    configured = smem;
+  }
+  prefer_shared(reinterpret_cast<const void*>(gemm_tc_seq_kernel<EPI, TRACE>));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(cdiv_i(a.N, NTILE), 1, cdiv_i(a.T, TZ_TC));
+  cfg.blockDim = dim3(SEQ_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_seq_kernel<EPI, TRACE>, tmw, tmh, tml, a, nt, two, stages) ==
+         cudaSuccess;
+}
+
 template <int EPI, bool TRACE>
 static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (a.splits < 1 || a.splits > MAX_CLUSTER) return false;
@@ -430,8 +636,13 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
          cudaSuccess;
 }
 
+// Launches of more than two 128-token slices run the K chunks in one CTA
+// (gemm_tc_seq_kernel); the others split them over a cluster.  Both add the
+// chunk sums in chunk order.
 template <int EPI>
 static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
+  if (cdiv_i(a.T, TZ_TC) > 2)
+    return a.trace ? launch_gemm_tc_seq<EPI, true>(a, s, pdl) : launch_gemm_tc_seq<EPI, false>(a, s, pdl);
   return a.trace ? launch_gemm_tc_kt<EPI, true>(a, s, pdl) : launch_gemm_tc_kt<EPI, false>(a, s, pdl);
 }
 

@@ -13,7 +13,15 @@
         shape: 33 tokens as hi and lo planes, 66 rows.  Runs the sweep once, then
         once more as a CUDA graph (gemm_tc launches 65..129 are the graph's).
 
-Both hold about 2 GB on the device.  The sweep's shapes and inputs are the ones
+    python -m self_speculative_block_gb300.profile_cases batch
+        The 16-request page batch: 16 ragged prefills (each one plan, one
+        embed, 65 gemm_tc, 16 attention_part, 16 attention_merge and one
+        finishing launch: 100 launches), then one batched self-speculative
+        round (B = 32, 16 x 33 = 528 rows per forward).  Run it with
+        GOCR_HOST_LOOP=1 so that the round's kernels are profilable: they
+        start at launch 1600.
+
+All hold a few GB on the device.  The sweep's shapes and inputs are the ones
 bench.py times for its kernel roofline.
 """
 from __future__ import annotations
@@ -104,12 +112,29 @@ def sweep_case():
     torch.cuda.synchronize()
 
 
+def batch_case():
+    from . import gocr
+    cfg = synth.BASE
+    wl = synth.WORKLOADS["batch"]
+    prefix_lens, new_lens = synth.batch_lengths(wl.n_requests)
+    W = synth.make_weights(cfg)
+    dec = gocr.Decoder(cfg, W, max_ctx=max(prefix_lens) + max(new_lens) + wl.block + 8, max_block=wl.block,
+                       max_requests=wl.n_requests)
+    del W
+    for r in range(wl.n_requests):
+        dec.prefill(r, synth.make_prefix(cfg, prefix_lens[r], seed=synth.REQUEST_PREFIX_SEED0 + r))
+    dec.decode_batch(list(range(wl.n_requests)), gocr.MODE_SELFSPEC, wl.block, [3] * wl.n_requests)
+    dec.close()
+
+
 def main(argv):
     what = argv[1] if len(argv) > 1 else ""
     if what == "draft":
         draft_case()
     elif what == "sweep":
         sweep_case()
+    elif what == "batch":
+        batch_case()
     else:
         print(__doc__)
         return 2
