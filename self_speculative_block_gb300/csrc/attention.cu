@@ -15,12 +15,13 @@
 // bf16 models: tensor-core kernels.  q and the KV cache are stored as bf16
 // hi + lo planes (written once by the QKV epilogue), QK^T takes
 // qh kh + qh kl + ql kh and PV takes P vh + P vl on mma.sync tiles (P in
-// bf16), accumulating in fp32.  The ATTN_RANKS CTAs of one (kv head,
-// 64-query-row group) split the chunks, rank r visiting chunks r, r + R, ...
-// with an online softmax, and write partial (max, sum, output) rows to global
-// memory; a merge kernel adds them in rank order.  There is no thread-block
-// cluster: most decode contexts give each rank one chunk, and the CTAs need no
-// co-scheduling.  Under programmatic dependent launch a CTA fetches its first
+// bf16), accumulating in fp32.  The R CTAs of one (kv head, 64-query-row
+// group) split the chunks, rank r visiting chunks r, r + R, ... with an online
+// softmax, and write the group's valid partial (max, sum, output) rows to
+// global memory; a merge kernel adds them in rank order.  R is fixed per
+// handle (attention_ranks: 48 for one request, fewer for a batch).  There is
+// no thread-block cluster: most single-request decode contexts give each rank
+// one chunk, and the CTAs need no co-scheduling.  Under programmatic dependent launch a CTA fetches its first
 // chunk before the grid-dependency wait when that chunk holds only committed
 // cache positions (below the round-start cache length, which no kernel of the
 // forward writes).  The result is written as the O projection's input planes.
@@ -190,10 +191,12 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
                                                     qr0, row0, nrows, pre, &s_maxlim);
   if (rank == 0 && tid == 0) a.part_chunks[(size_t)slot * gridDim.x + group] = n_chunks;
   if (rank >= n_chunks) return;
+  // the group's valid rows only: the merge writes no output for the others
+  const int vrows = min(attn::QR, nrows * G - qr0);
   const float4* src = reinterpret_cast<const float4*>(attn::staged_rows<D>(sm_raw));
   float4* dst = reinterpret_cast<float4*>(
       a.part + (((size_t)slot * gridDim.x + group) * R + rank) * attn::QR * RLD);
-  for (int x = tid; x < attn::QR * RLD / 4; x += 256) dst[x] = src[x];
+  for (int x = tid; x < vrows * RLD / 4; x += 256) dst[x] = src[x];
   if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 
@@ -229,10 +232,10 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R)
   if (TRACE && threadIdx.x == 0) trace_mark(a.trace, 3);
 }
 
-size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d) {
+size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, int R) {
   const int G = Hq / Hkv;
   const size_t groups = (size_t)Hkv * ((max_rows * G + attn::QR - 1) / attn::QR);
-  return (size_t)n_slots * groups * ATTN_RANKS * attn::QR * (d + 4);
+  return (size_t)n_slots * groups * R * attn::QR * (d + 4);
 }
 
 template <int D, bool TRACE>
@@ -248,7 +251,7 @@ static bool launch_attn_mma_t(const AttnArgs& a, int n_slots, int max_rows, cuda
     configured = true;
   }
   cudaLaunchConfig_t cfg{};
-  const int R = attention_ranks(a.cap);
+  const int R = a.ranks > 0 ? a.ranks : attention_ranks(a.cap, 1);
   cfg.gridDim = dim3(a.Hkv * n_rg, R, n_slots);
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = attn::Geo<D>::TILE_SMEM;

@@ -75,6 +75,7 @@ struct gocr_handle {
 
   int q_dim = 0, kv_dim = 0, qkv_n = 0, gu_n = 0;
   int cap = 0, T_max = 0, T_dec = 0, sched_cap = 0;
+  int attn_ranks = 1;  // key-chunk ranks of the tensor-core attention, fixed for the handle
   long long layer_stride = 0, req_stride = 0;
 
   // KV cache [req][layer][kv head][position][head_dim]: bf16 hi/lo planes for
@@ -251,6 +252,7 @@ void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_o
     at.scale = 1.0f / sqrtf((float)c.head_dim);
     at.part = h->att_part;
     at.part_chunks = h->att_chunks;
+    at.ranks = h->attn_ranks;
     f.at.push_back(at);
     // O projection + residual; planes of resid * g_mlp for the MLP
     GemmArgs go = gemm_base(h, h->at_hi, h->at_lo, h->q_dim, h->wo[l], T, H, h->q_dim);
@@ -310,7 +312,7 @@ bool mk_shape(gocr_handle* h, int kind, int n_slots, int B, MkArgs& a) {
   const int G = c.n_q_heads / c.n_kv_heads;
   a.n_rg = (a.rows_per_slot * G + 63) / 64;
   a.Hkv = c.n_kv_heads;
-  a.ranks = attention_ranks(h->cap);
+  a.ranks = h->attn_ranks;
   a.G = h->mk_G;
   const int NK[5][2] = {{h->qkv_n, c.hidden}, {c.hidden, h->q_dim}, {h->gu_n, c.hidden}, {c.hidden, c.ffn},
                         {c.vocab, c.hidden}};
@@ -698,6 +700,10 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->host_loop = hl && hl[0] == '1';
     const char* lp = getenv("GOCR_L2_PREFETCH");
     h->l2_prefetch = !(lp && lp[0] == '0');
+    // GOCR_ATTN_RANKS=<n>: rank count for this handle instead of the rule
+    h->attn_ranks = attention_ranks(h->cap, c.max_requests);
+    const char* ar = getenv("GOCR_ATTN_RANKS");
+    if (ar && atoi(ar) >= 1 && atoi(ar) <= 64) h->attn_ranks = atoi(ar) < (h->cap + 31) / 32 ? atoi(ar) : (h->cap + 31) / 32;
   }
   CKC(cudaStreamCreateWithFlags(&h->hs, cudaStreamNonBlocking));
   CKC(cudaEventCreate(&h->ev0));
@@ -754,8 +760,9 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
   if (h->dtype == GOCR_DTYPE_BF16) {
     // partial rows of the attention ranks: a prefill (one slot of up to
     // max_ctx rows) or a decode forward (max_requests slots of max_block + 1 rows)
-    const size_t pf = attention_part_floats(1, c.max_ctx, c.n_q_heads, c.n_kv_heads, c.head_dim);
-    const size_t df = attention_part_floats(R, c.max_block + 1, c.n_q_heads, c.n_kv_heads, c.head_dim);
+    const int AR = h->attn_ranks;
+    const size_t pf = attention_part_floats(1, c.max_ctx, c.n_q_heads, c.n_kv_heads, c.head_dim, AR);
+    const size_t df = attention_part_floats(R, c.max_block + 1, c.n_q_heads, c.n_kv_heads, c.head_dim, AR);
     h->att_part = (float*)A((pf > df ? pf : df) * 4);
     const size_t pg = (size_t)c.n_kv_heads * ((c.max_ctx * (c.n_q_heads / c.n_kv_heads) + 63) / 64);
     const size_t dg = (size_t)R * c.n_kv_heads * (((c.max_block + 1) * (c.n_q_heads / c.n_kv_heads) + 63) / 64);
@@ -1162,7 +1169,8 @@ int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void*
     CK(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return fail(h, GOCR_ECUDA, "device index %d", dev);
     const size_t groups = (size_t)Hkv * ((T * (Hq / Hkv) + 63) / 64);
-    const size_t part_bytes = (attention_part_floats(1, T, Hq, Hkv, d) * 4 + 255) & ~(size_t)255;
+    const size_t part_bytes =
+        (attention_part_floats(1, T, Hq, Hkv, d, attention_ranks(cap, 1)) * 4 + 255) & ~(size_t)255;
     const size_t need = part_bytes + groups * 4;
     std::lock_guard<std::mutex> lk(mu);
     if (bufs[dev].second < need) {

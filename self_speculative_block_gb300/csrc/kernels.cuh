@@ -113,19 +113,26 @@ struct alignas(16) AttnArgs {
   // tensor-core path: partial rows of the ranks, [slot][kv head x row group][rank][64][d + 4] fp32
   float* part;
   int* part_chunks;           // [slot][kv head x row group] chunks the group's rows read
+  int ranks;                  // key-chunk ranks R (attention_ranks); 0: attention_ranks(cap, 1)
   unsigned long long* trace;  // launch timeline record, as GemmArgs::trace
 };
 // Key-chunk ranks of the tensor-core attention: rank r reads chunks r, r + R, ...
-// R = attention_ranks(cap): at most ATTN_RANKS, and no more than a KV
-// capacity of cap keys has chunks of 32.  R is fixed by the capacity, so every
-// forward of a handle splits a row's keys the same way.
+// R = attention_ranks(cap, n_req): ATTN_RANKS for one request, fewer (at
+// least ATTN_RANKS_MIN) when a forward carries up to n_req requests, so that
+// a full batch keeps about as many partial tiles as one request and each
+// tile reads more chunks; never more than a KV capacity of cap keys has chunks
+// of 32.  A handle fixes R at creation, so every forward of a handle (one row
+// or B + 1, one request or a batch) splits a row's keys the same way.
 constexpr int ATTN_RANKS = 48;
-inline int attention_ranks(int cap) {
+constexpr int ATTN_RANKS_MIN = 8;
+inline int attention_ranks(int cap, int n_req) {
   const int c = (cap + 31) / 32;
-  return c < 1 ? 1 : (c < ATTN_RANKS ? c : ATTN_RANKS);
+  int r = ATTN_RANKS / (n_req < 1 ? 1 : n_req);
+  if (r < ATTN_RANKS_MIN) r = ATTN_RANKS_MIN;
+  return c < 1 ? 1 : (c < r ? c : r);
 }
-// fp32 words of the tensor-core attention's partial rows for n_slots slots of up to max_rows rows
-size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d);
+// fp32 words of the tensor-core attention's partial rows for n_slots slots of up to max_rows rows, R ranks
+size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, int R);
 // dtype 1: tensor-core cluster kernel; 0: CUDA-core kernel.
 bool launch_attention(int dtype, const AttnArgs& a, int n_slots, int max_rows_per_slot, cudaStream_t s,
                       bool pdl);
