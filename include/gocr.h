@@ -223,6 +223,18 @@ size_t gocr_op_linear_workspace(int T, int N, int K);
 int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int N, int K,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* y[T, N] (fp32) = (x_hi + x_lo)[T, K] w[N, K]^T with bf16 planes x_hi,
+ * x_lo and bf16 w: the decoder's GEMM on the hi + lo activation planes its
+ * epilogues write (each K chunk takes the hi and the lo products as separate
+ * tensor-core accumulators, adds them, and the chunk sums are added in chunk
+ * order).  Up to two 128-row token slices split each tile's K chunks over a
+ * thread-block cluster; more slices run them in one CTA.  Either way a row's
+ * bits depend on neither T nor the kernel that ran it.  K % 8 == 0; x_hi, x_lo,
+ * w 16-byte aligned.  workspace: as gocr_op_linear.  Errors: GOCR_EINVAL
+ * (null pointer, shape), GOCR_ECAPACITY (workspace), GOCR_ECUDA (launch). */
+int gocr_op_linear_planes(const void* x_hi, const void* x_lo, const void* w, float* y, int T, int N, int K,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
 /* Grouped-query attention of one request window against a KV cache, the
  * decoder's kernel for that dtype.  Operands are planes, as the decoder keeps
  * them: for GOCR_DTYPE_BF16, bf16 hi and lo arrays with v = hi + lo (tensor

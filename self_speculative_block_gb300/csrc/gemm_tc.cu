@@ -45,6 +45,18 @@ constexpr int DECODE_STAGE_CAP = 3;      // decode shapes: keep two CTAs per SM
 constexpr int TAIL_BYTES = TZ_TC * 4 + EG * NTILE * 4 + NTILE * 4 + 2 * EG * 4 + 16 * 8 + 64;
 constexpr int L2_PREFETCH_BLOCKS = 8;    // weight tiles a CTA brings into L2 ahead of its ring
 constexpr int MAX_CLUSTER = 16;          // split-K ranks of one tile
+constexpr size_t TWO_CTA_SMEM = 113 * 1024;  // dynamic shared memory of each of two CTAs on one SM
+
+// fp32 words over the ring after the mainloop (gemm_tc_kernel's layout):
+// the partial tile [nt], the peers' rows [S x per] and, after them, the
+// reduced rows [min(per, EG)] and the epilogue scratch, which with one
+// epilogue pass (per <= EG) reuses the space of the first two instead.
+inline int gemm_y_floats(int nt, int S, int per) {
+  if (S == 1) return nt * YLD + EPI_SCRATCH_FLOATS;
+  const int xs = (nt + S * per) * YLD;
+  if (per <= EG) return (xs > EPI_SCRATCH_FLOATS ? xs : EPI_SCRATCH_FLOATS) + per * YLD;
+  return xs + EG * YLD + EPI_SCRATCH_FLOATS;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::mutex g_mu;
@@ -110,10 +122,16 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   uint8_t* sB = sA + stages * A_BYTES;
   // after the MMAs the ring is free: the partial tile, the partial rows the
   // cluster peers send, the reduced rows and the epilogue scratch live there
+  // (gemm_y_floats).  With one epilogue pass (per <= EG) the scratch takes the
+  // place of the partial tile and the peers' rows, which are dead by then.
+  const bool alias = gridDim.y > 1 && per <= EG;
   float* Yp = reinterpret_cast<float*>(smem);             // [nt][YLD]
   float* RX = Yp + nt * YLD;                               // [S][per][YLD] peers' partial rows
-  float* Ys = RX + (size_t)gridDim.y * per * YLD;          // [EG][YLD]
-  float* scratch = Ys + EG * YLD;                          // epilogue scratch
+  const int ys_off = gridDim.y == 1 ? nt * YLD
+                     : alias ? max((nt + (int)gridDim.y * per) * YLD, EPI_SCRATCH_FLOATS)
+                             : (nt + (int)gridDim.y * per) * YLD;
+  float* Ys = Yp + ys_off;                                 // [min(per, EG)][YLD] (unused when S = 1)
+  float* scratch = gridDim.y == 1 ? Ys : alias ? Yp : Ys + EG * YLD;  // epilogue scratch
   uint8_t* tail = smem + ring_bytes;
   float* rs_all = reinterpret_cast<float*>(tail);          // [TZ_TC] rstd of the slice's tokens
   float* rr_pre = rs_all + TZ_TC;                          // [EG][NTILE] residual rows, or
@@ -347,6 +365,9 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
           }
         *reinterpret_cast<float4*>(Ys + (size_t)j * YLD + c4) = acc;
       }
+      // an aliased scratch overwrites the partial tile: the copies to the
+      // peers must have read it
+      if (alias && tid == 0) tc::bulk_wait_read();
       __syncthreads();
       if (!failed && rx_ok) {
         EpiPre pre;
@@ -373,41 +394,52 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
 // batched round): one CTA per (128-row weight tile, token slice) runs the S
 // K chunks of the split rule one after another.  Each chunk's MMAs start a
 // fresh accumulator (two in TMEM, so the next chunk's MMAs overlap this
-// chunk's drain), and four drain warps add the chunk sums into a shared-memory
-// running sum in chunk order: p0 + p1 + ... + p(S-1), the clustered kernel's
-// reduction, so a token's bits do not depend on which kernel ran it.  Warp 0:
-// TMA producer; warp 1: MMA issuer; warps 4-7: drain; all eight warps run the
-// epilogue.
+// chunk's drain), and four drain warps add the chunk sums into running sums
+// held in registers (thread = weight row, one register per token), in chunk
+// order: p0 + p1 + ... + p(S-1), the clustered kernel's reduction, so a
+// token's bits do not depend on which kernel ran it.  After the last chunk
+// the sums go to shared memory over the then idle operand ring, where all
+// eight warps run the epilogue.  Warp 0: TMA producer; warp 1: MMA issuer;
+// warps 4-7: drain.  Inputs are bf16 hi + lo planes (single-plane launches
+// take the clustered kernel).
 constexpr int SEQ_THREADS = 256;
+constexpr int SEQ_NT = TZ_TC;    // tokens per slice
+constexpr int SEQ_STAGES = 4;    // operand ring depth (48 KB per stage with both planes)
 
 template <int EPI, bool TRACE>
-__global__ void __launch_bounds__(SEQ_THREADS) gemm_tc_seq_kernel(const __grid_constant__ CUtensorMap tmw,
-                                                                 const __grid_constant__ CUtensorMap tmx_hi,
-                                                                 const __grid_constant__ CUtensorMap tmx_lo,
-                                                                 GemmArgs a, int nt, int two, int stages) {
+__global__ void __launch_bounds__(SEQ_THREADS, 1) gemm_tc_seq_kernel(const __grid_constant__ CUtensorMap tmw,
+                                                                    const __grid_constant__ CUtensorMap tmx_hi,
+                                                                    const __grid_constant__ CUtensorMap tmx_lo,
+                                                                    GemmArgs a, int stages) {
+  constexpr int nt = SEQ_NT;
+  constexpr int two = 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const int b_bytes = (two ? 2 : 1) * nt * 128;
   uint8_t* sA = smem;
   uint8_t* sB = sA + stages * A_BYTES;
-  float* Ysum = reinterpret_cast<float*>(sB + stages * b_bytes);  // [nt][YLD] running sum over chunks
-  float* scratch = Ysum + (size_t)nt * YLD;                       // epilogue scratch
-  uint64_t* full = reinterpret_cast<uint64_t*>(scratch + EPI_SCRATCH_FLOATS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + stages * b_bytes);
   uint64_t* empty = full + stages;
   uint64_t* accf = empty + stages;  // [2] chunk accumulator ready
   uint64_t* acce = accf + 2;        // [2] chunk accumulator drained
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acce + 2);
+  // after the mainloop: the reduced tile and the epilogue scratch over the ring
+  float* Ysum = reinterpret_cast<float*>(smem);                   // [nt][YLD]
+  float* scratch = Ysum + (size_t)nt * YLD;
   __shared__ int s_fail;
   __shared__ int s_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, z = blockIdx.z;
+  // the slices of one weight tile are adjacent in launch order, so the tile
+  // comes from HBM once and from L2 for the other slices
+  const int nz = cdiv_i(a.T, TZ_TC);
+  const int tile = blockIdx.x / nz, z = blockIdx.x % nz;
   const int n0 = tile * NTILE;
   const int t0 = z * TZ_TC;
   const int tn = min(TZ_TC, a.T - t0);
   const int S = a.splits, kpc = a.kchunk / 64, nkb_all = cdiv_i(a.K, 64);
   const int nmma = (two ? 2 : 1) * nt;
-  const uint32_t bufcols = nmma <= 32 ? 32 : (nmma <= 64 ? 64 : (nmma <= 128 ? 128 : 256));
+  const uint32_t bufcols = two ? 256u : 128u;
 
   if (tid == 0) {
     if (TRACE) trace_mark(a.trace, 0);
@@ -482,10 +514,11 @@ __global__ void __launch_bounds__(SEQ_THREADS) gemm_tc_seq_kernel(const __grid_c
       }
       tc::mma_commit(&accf[b]);
     }
-  } else if (warp >= 4) {
-    // drain: chunk sums into Ysum[token][row], added in chunk order
+  }
+  float acc[nt];  // drain warps: running sums of weight row q*32 + lane, one per token
+  if (warp >= 4) {
+    // drain: chunk sums (hi + lo products) added to the running sums in chunk order
     const int q = warp & 3;
-    const int row = q * 32 + lane;
     for (int c = 0; c < S; ++c) {
       const int b = c & 1;
       if (!tc::mbar_wait(&accf[b], (c >> 1) & 1)) {
@@ -494,18 +527,14 @@ __global__ void __launch_bounds__(SEQ_THREADS) gemm_tc_seq_kernel(const __grid_c
       }
       tc::fence_after_sync();
       const uint32_t taddr = tmem + (uint32_t)b * bufcols + ((uint32_t)(q * 32) << 16);
+#pragma unroll
       for (int g = 0; g < nt / 16; ++g) {
         float vh[16], vl[16];
-        tc::tmem_ld16(taddr + g * 16, vh);
-        if (two) {
-          tc::tmem_ld16(taddr + nt + g * 16, vl);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) vh[j] += vl[j];
-        }
+        tc::tmem_ld16x2(taddr + g * 16, taddr + nt + g * 16, vh, vl);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          float* y = Ysum + (size_t)(g * 16 + j) * YLD + row;
-          *y = c == 0 ? vh[j] : *y + vh[j];
+          const float v = vh[j] + vl[j];
+          acc[g * 16 + j] = c == 0 ? v : acc[g * 16 + j] + v;
         }
       }
       tc::fence_before_sync();
@@ -516,7 +545,7 @@ __global__ void __launch_bounds__(SEQ_THREADS) gemm_tc_seq_kernel(const __grid_c
   __syncwarp();
   tc::grid_dep_wait();  // the epilogue reads and writes what earlier kernels touch
   tc::fence_before_sync();
-  __syncthreads();
+  __syncthreads();  // every chunk drained: the MMAs, and so the ring's TMA writes, are complete
   if (TRACE && tid == 0) trace_mark(a.trace, 4);
   if (warp == 0) {
     tc::fence_after_sync();
@@ -527,6 +556,12 @@ __global__ void __launch_bounds__(SEQ_THREADS) gemm_tc_seq_kernel(const __grid_c
     if (tid == 0) set_err(a.e.err, DERR_TIMEOUT);
     return;
   }
+  if (warp >= 4) {
+    const int row = (warp & 3) * 32 + lane;
+#pragma unroll
+    for (int t = 0; t < nt; ++t) Ysum[(size_t)t * YLD + row] = acc[t];
+  }
+  __syncthreads();
   for (int g0 = 0; g0 < tn; g0 += EG) {
     const int cnt = min(EG, tn - g0);
     apply_epilogue_k<EPI>(a, Ysum + (size_t)g0 * YLD, YLD, tile, t0 + g0, cnt, scratch, EpiPre(), Grp::block());
@@ -539,20 +574,15 @@ template <int EPI, bool TRACE>
 static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
   CUtensorMap tmw, tmh, tml;
   if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE)) return false;
-  const int nt = TZ_TC;  // several full slices
-  if (!tmap_2d(&tmh, a.x, a.T, a.K, nt)) return false;
-  const int two = a.x_lo != nullptr;
-  if (two) {
-    if (!tmap_2d(&tml, a.x_lo, a.T, a.K, nt)) return false;
-  } else {
-    tml = tmh;
-  }
-  const int stage_bytes = A_BYTES + (two ? 2 : 1) * nt * 128;
-  const size_t fixed = 1024 + (size_t)nt * YLD * 4 + (size_t)EPI_SCRATCH_FLOATS * 4 + 16 * 8 + 64;
-  int stages = (int)((227 * 1024 - 2048 - fixed) / stage_bytes);
-  if (stages > 4) stages = 4;
-  if (stages < 2) return false;
-  const size_t smem = fixed + (size_t)stages * stage_bytes;
+  const int nt = SEQ_NT;
+  if (!a.x_lo || !tmap_2d(&tmh, a.x, a.T, a.K, nt) || !tmap_2d(&tml, a.x_lo, a.T, a.K, nt)) return false;
+  const int stage_bytes = A_BYTES + 2 * nt * 128;
+  const int stages = SEQ_STAGES;
+  const size_t ring = (size_t)stages * stage_bytes;
+  const size_t epi = ((size_t)nt * YLD + EPI_SCRATCH_FLOATS) * 4;  // aliases the ring after the mainloop
+  if (epi > ring) return false;
+  const size_t smem = 1024 + ring + (2 * stages + 4) * 8 + 16;
+  if (smem > 227 * 1024) return false;
   static size_t configured = 0;
   if (smem > configured) {
     if (cudaFuncSetAttribute(gemm_tc_seq_kernel<EPI, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -562,7 +592,7 @@ static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
   }
   prefer_shared(reinterpret_cast<const void*>(gemm_tc_seq_kernel<EPI, TRACE>));
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(cdiv_i(a.N, NTILE), 1, cdiv_i(a.T, TZ_TC));
+  cfg.gridDim = dim3(cdiv_i(a.N, NTILE) * cdiv_i(a.T, TZ_TC));
   cfg.blockDim = dim3(SEQ_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -571,8 +601,7 @@ static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_seq_kernel<EPI, TRACE>, tmw, tmh, tml, a, nt, two, stages) ==
-         cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_seq_kernel<EPI, TRACE>, tmw, tmh, tml, a, stages) == cudaSuccess;
 }
 
 template <int EPI, bool TRACE>
@@ -591,16 +620,25 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   const int nkb = cdiv_i(a.kchunk, 64);
   const int stage_bytes = A_BYTES + (two ? 2 : 1) * nt * 128;
   const int per = cdiv_i(a.T < TZ_TC ? a.T : TZ_TC, a.splits);  // tokens each cluster rank reduces
-  const int y_bytes = ((nt + a.splits * per + EG) * YLD + EPI_SCRATCH_FLOATS) * 4;
+  const int y_bytes = gemm_y_floats(nt, a.splits, per) * 4;
+  auto smem_of = [&](int st) {
+    int ring = st * stage_bytes;
+    if (ring < y_bytes) ring = y_bytes;
+    ring = (ring + 1023) / 1024 * 1024;
+    return std::make_pair((size_t)1024 + ring + TAIL_BYTES, ring);
+  };
   int stages = (SMEM_CAP - 1024 - TAIL_BYTES) / stage_bytes;
   if (stages > 6) stages = 6;
-  if (a.T <= 2 * 64 + 1 && stages > DECODE_STAGE_CAP) stages = DECODE_STAGE_CAP;
+  if (a.T <= 2 * 64 + 1) {
+    // decode shapes: the deepest ring (at most DECODE_STAGE_CAP, at least
+    // two stages) that keeps two CTAs per SM
+    if (stages > DECODE_STAGE_CAP) stages = DECODE_STAGE_CAP;
+    while (stages > 2 && smem_of(stages).first > TWO_CTA_SMEM) --stages;
+  }
   if (stages > nkb) stages = nkb;
   if (stages < 1) stages = 1;
-  int ring = stages * stage_bytes;
-  if (ring < y_bytes) ring = y_bytes;
-  ring = (ring + 1023) / 1024 * 1024;
-  const size_t smem = 1024 + (size_t)ring + TAIL_BYTES;
+  const int ring = smem_of(stages).second;
+  const size_t smem = smem_of(stages).first;
   if (smem > 227 * 1024) return false;
   static size_t configured = 0;
   if (smem > configured) {
@@ -636,12 +674,12 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
          cudaSuccess;
 }
 
-// Launches of more than two 128-token slices run the K chunks in one CTA
-// (gemm_tc_seq_kernel); the others split them over a cluster.  Both add the
-// chunk sums in chunk order.
+// Launches of more than two 128-token slices of hi + lo planes run the K
+// chunks in one CTA (gemm_tc_seq_kernel); the others split them over a
+// cluster.  Both add the chunk sums in chunk order.
 template <int EPI>
 static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
-  if (cdiv_i(a.T, TZ_TC) > 2)
+  if (cdiv_i(a.T, TZ_TC) > 2 && a.x_lo)
     return a.trace ? launch_gemm_tc_seq<EPI, true>(a, s, pdl) : launch_gemm_tc_seq<EPI, false>(a, s, pdl);
   return a.trace ? launch_gemm_tc_kt<EPI, true>(a, s, pdl) : launch_gemm_tc_kt<EPI, false>(a, s, pdl);
 }

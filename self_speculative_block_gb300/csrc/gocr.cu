@@ -1146,6 +1146,27 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
   return GOCR_OK;
 }
 
+int gocr_op_linear_planes(const void* x_hi, const void* x_lo, const void* w, float* y, int T, int N, int K,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  gocr_handle* h = nullptr;
+  if (!x_hi || !x_lo || !w || !y || !workspace) return fail(h, GOCR_EINVAL, "null pointer");
+  if (T < 1 || N < 1 || K < 8 || K % 8) return fail(h, GOCR_EINVAL, "bad shape T=%d N=%d K=%d", T, N, K);
+  if (((uintptr_t)x_hi | (uintptr_t)x_lo | (uintptr_t)w) & 15) return fail(h, GOCR_EINVAL, "operand not 16-byte aligned");
+  if (workspace_bytes < gocr_op_linear_workspace(T, N, K)) return fail(h, GOCR_ECAPACITY, "workspace too small");
+  GemmArgs a{};
+  a.x = x_hi; a.x_lo = x_lo; a.ldx = K; a.w = w; a.T = T; a.N = N; a.K = K;
+  a.kchunk = gemm_kchunk(N, K); a.splits = gemm_splits(N, K);
+  a.counters = (int*)workspace;
+  size_t ctr = ((size_t)gemm_counter_ints(T, N) * 4 + 255) & ~(size_t)255;
+  a.ws = (float*)((char*)workspace + ctr);
+  a.epi = EPI_STORE;
+  a.e.y = y; a.e.ldy = N;
+  if (!launch_gemm(GOCR_DTYPE_BF16, a, (cudaStream_t)stream, false))
+    return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
+  CK(cudaGetLastError());
+  return GOCR_OK;
+}
+
 int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
                       const void* v_hi, const void* v_lo, float* o, const int32_t* lim, int T, int Hq, int Hkv,
                       int d, int cap, void* stream) {

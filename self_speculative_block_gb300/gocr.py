@@ -32,7 +32,7 @@ LAYER_TENSORS = 9
 # every symbol include/gocr.h declares
 EXPORTS = ("gocr_create", "gocr_prefill", "gocr_decode", "gocr_decode_batch",
            "gocr_set_draft_override", "gocr_debug_forward", "gocr_read_kv", "gocr_get_state",
-           "gocr_set_option", "gocr_get_option", "gocr_read_trace", "gocr_last_error", "gocr_free", "gocr_op_linear_workspace", "gocr_op_linear",
+           "gocr_set_option", "gocr_get_option", "gocr_read_trace", "gocr_last_error", "gocr_free", "gocr_op_linear_workspace", "gocr_op_linear", "gocr_op_linear_planes",
            "gocr_op_attention", "gocr_op_linear_static")
 
 
@@ -105,6 +105,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gocr_free": (None, [vp]),
         "gocr_op_linear_workspace": (sz, [i32, i32, i32]),
         "gocr_op_linear": (i32, [i32, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
+        "gocr_op_linear_planes": (i32, [vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
         "gocr_op_attention": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gocr_op_linear_static": (i32, [i32, vp, vp, vp, i32, i32, i32, vp]),
     }
@@ -350,6 +351,25 @@ def op_linear(x, w, workspace=None):
     stream = torch.cuda.current_stream(x.device).cuda_stream
     _check(lib.gocr_op_linear(_dt(x), x.data_ptr(), w.data_ptr(), y.data_ptr(), T, N, K,
                               workspace.data_ptr(), workspace.numel(), stream))
+    return y
+
+
+def op_linear_planes(x_hi, x_lo, w, workspace=None):
+    """y[T, N] fp32 = (x_hi + x_lo)[T, K] w[N, K]^T on bf16 planes, the
+    decoder's GEMM on its activation planes."""
+    torch = _torch()
+    lib = load()
+    T, K = x_hi.shape
+    N = w.shape[0]
+    if x_lo.shape != x_hi.shape or not (x_hi.dtype == x_lo.dtype == w.dtype == torch.bfloat16):
+        raise ValueError("op_linear_planes takes bf16 planes of one shape and bf16 weights")
+    y = torch.empty((T, N), dtype=torch.float32, device=x_hi.device)
+    need = lib.gocr_op_linear_workspace(T, N, K)
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=x_hi.device)
+    stream = torch.cuda.current_stream(x_hi.device).cuda_stream
+    _check(lib.gocr_op_linear_planes(x_hi.data_ptr(), x_lo.data_ptr(), w.data_ptr(), y.data_ptr(), T, N, K,
+                                     workspace.data_ptr(), workspace.numel(), stream))
     return y
 
 

@@ -1,12 +1,15 @@
 """Small, self-contained launches of the hot kernels for capture under a profiler.
 
-    python -m self_speculative_block_gb300.profile_cases draft
+    python -m self_speculative_block_gb300.profile_cases draft [B]
         0.5B-class bf16 decoder, 1024-row synthetic prefill, then two draft
-        forwards (B = 32, 33 rows).  The prefill launches gemm_tc_kernel 65
-        times and attention_part_kernel / attention_merge_kernel 16 times
-        each, so the first draft forward's QKV / O / gate-up / down GEMMs are
-        gemm_tc launches 65..68 and its first attention is attention_part and
-        attention_merge launch 16.
+        forwards (B = 32 unless given: B + 1 rows).  The prefill (1024 rows,
+        eight token slices) launches gemm_tc_seq_kernel 65 times and
+        attention_part_kernel / attention_merge_kernel 16 times each; the
+        draft forwards launch gemm_tc_kernel (65 per forward), so the first
+        draft forward's QKV / O / gate-up / down GEMMs are launches 0..3 of
+        `-k regex:gemm_tc_kernel` (65..68 of `-k regex:gemm_tc`, which also
+        matches the prefill's kernel) and its first attention is
+        attention_part and attention_merge launch 16.
     python -m self_speculative_block_gb300.profile_cases sweep
         The split-K GEMM over one forward's 65 weight matrices (16 x packed
         QKV, O, packed gate/up, down, then the LM head) at the decode launch
@@ -91,16 +94,16 @@ class GemmSweep:
         return sum(n * k * es + T * k * es + T * n * 4 for n, k in self.shapes) / len(self.shapes)
 
 
-def draft_case():
+def draft_case(B: int = 32):
     from . import gocr
     cfg = synth.BASE
     W = synth.make_weights(cfg)
-    dec = gocr.Decoder(cfg, W, max_ctx=1024 + 80, max_block=32)
+    dec = gocr.Decoder(cfg, W, max_ctx=1024 + 2 * B + 16, max_block=B)
     del W
     dec.prefill(0, synth.make_prefix(cfg, 1024))
     _, x0 = dec.state(0)
     for _ in range(2):
-        dec.debug_forward(0, gocr.FWD_DRAFT, [x0] + [0] * 32)
+        dec.debug_forward(0, gocr.FWD_DRAFT, [x0] + [0] * B)
     dec.close()
 
 
@@ -130,7 +133,7 @@ def batch_case():
 def main(argv):
     what = argv[1] if len(argv) > 1 else ""
     if what == "draft":
-        draft_case()
+        draft_case(int(argv[2]) if len(argv) > 2 else 32)
     elif what == "sweep":
         sweep_case()
     elif what == "batch":

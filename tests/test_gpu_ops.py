@@ -57,6 +57,40 @@ def test_linear_row_bits_do_not_depend_on_row_count(g, dt):
         assert torch.equal(part, full[:T]), T
 
 
+def _bf16_planes_of(a):
+    """fp32 array -> (hi, lo) bf16 tensors with a = hi + lo, and hi + lo in fp64."""
+    from self_speculative_block_gb300 import synth
+    hi = synth.bf16_bits(a)
+    lo = synth.bf16_bits(a.astype(np.float32) - synth.bf16_to_f32(hi))
+    t = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).cuda().view(torch.bfloat16)
+    return t(hi), t(lo), synth.bf16_to_f32(hi).astype(np.float64) + synth.bf16_to_f32(lo).astype(np.float64)
+
+
+# up to two 128-row slices: K chunks over a cluster; three or more: one CTA
+# runs every K chunk (ragged last slices: 300 = 2 x 128 + 44, 528 = 4 x 128 + 16)
+@pytest.mark.parametrize("T,N,K", [(1, 128, 64), (33, 2560, 1536), (256, 384, 704), (300, 384, 704),
+                                   (528, 1536, 4096), (1000, 256, 1536)])
+def test_linear_planes_matches_oracle_matmul(g, T, N, K):
+    from self_speculative_block_gb300 import synth
+    rng = np.random.default_rng(T * 11 + N + K)
+    xh, xl, x = _bf16_planes_of(rng.standard_normal((T, K)).astype(np.float32))
+    w = _rounded((0.02 * rng.standard_normal((N, K))).astype(np.float32), "bf16")
+    y = g.op_linear_planes(xh, xl, _dev(w, "bf16")).cpu().numpy()
+    ref = x @ w.T  # fp64 on the kernel's exact operands
+    np.testing.assert_allclose(y, ref, rtol=1e-4, atol=2e-5 * np.sqrt(K / 64))
+
+
+def test_linear_planes_row_bits_do_not_depend_on_row_count_or_kernel(g):
+    rng = np.random.default_rng(9)
+    N, K = 1536, 4096
+    xh, xl, _ = _bf16_planes_of(rng.standard_normal((528, K)).astype(np.float32))
+    w = _dev((0.02 * rng.standard_normal((N, K))).astype(np.float32), "bf16")
+    full = g.op_linear_planes(xh, xl, w)  # five slices: one CTA per (tile, slice)
+    for T in (1, 33, 65, 200, 256, 300):  # T <= 256: the clustered kernel
+        part = g.op_linear_planes(xh[:T].contiguous(), xl[:T].contiguous(), w)
+        assert torch.equal(part, full[:T]), T
+
+
 def _planes(a, dtype):
     """fp32 array -> the kernel's operand: fp32 tensor, or (hi, lo) bf16 tensors with a = hi + lo."""
     from self_speculative_block_gb300 import gocr, synth
