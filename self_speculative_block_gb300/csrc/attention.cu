@@ -17,8 +17,8 @@
 // qh kh + qh kl + ql kh and PV takes P vh + P vl on mma.sync tiles (P in
 // bf16), accumulating in fp32.  The R CTAs of one (kv head, 64-query-row
 // group) split the chunks, rank r visiting chunks r, r + R, ... with an online
-// softmax, and write the group's valid partial (max, sum, output) rows to
-// global memory; a merge kernel adds them in rank order.  R is fixed per
+// softmax, and write partial (max, sum, output) rows to global memory; a
+// merge kernel adds them in rank order.  R is fixed per
 // handle (attention_ranks: 48 for one request, fewer for a batch).  There is
 // no thread-block cluster: most single-request decode contexts give each rank
 // one chunk, and the CTAs need no co-scheduling.  Under programmatic dependent launch a CTA fetches its first
@@ -191,12 +191,12 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
                                                     qr0, row0, nrows, pre, &s_maxlim);
   if (rank == 0 && tid == 0) a.part_chunks[(size_t)slot * gridDim.x + group] = n_chunks;
   if (rank >= n_chunks) return;
-  // the group's valid rows only: the merge writes no output for the others
-  const int vrows = min(attn::QR, nrows * G - qr0);
+  // all 64 rows, also those past the window (which the merge reads but does
+  // not output): a fixed trip count measured faster than writing fewer rows
   const float4* src = reinterpret_cast<const float4*>(attn::staged_rows<D>(sm_raw));
   float4* dst = reinterpret_cast<float4*>(
       a.part + (((size_t)slot * gridDim.x + group) * R + rank) * attn::QR * RLD);
-  for (int x = tid; x < vrows * RLD / 4; x += 256) dst[x] = src[x];
+  for (int x = tid; x < attn::QR * RLD / 4; x += 256) dst[x] = src[x];
   if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 

@@ -47,15 +47,23 @@ constexpr int L2_PREFETCH_BLOCKS = 8;    // weight tiles a CTA brings into L2 ah
 constexpr int MAX_CLUSTER = 16;          // split-K ranks of one tile
 constexpr size_t TWO_CTA_SMEM = 113 * 1024;  // dynamic shared memory of each of two CTAs on one SM
 
-// fp32 words over the ring after the mainloop (gemm_tc_kernel's layout):
+// Layout over the ring after the mainloop (gemm_tc_kernel):
 // the partial tile [nt], the peers' rows [S x per] and, after them, the
-// reduced rows [min(per, EG)] and the epilogue scratch, which with one
-// epilogue pass (per <= EG) reuses the space of the first two instead.
-inline int gemm_y_floats(int nt, int S, int per) {
-  if (S == 1) return nt * YLD + EPI_SCRATCH_FLOATS;
-  const int xs = (nt + S * per) * YLD;
-  if (per <= EG) return (xs > EPI_SCRATCH_FLOATS ? xs : EPI_SCRATCH_FLOATS) + per * YLD;
-  return xs + EG * YLD + EPI_SCRATCH_FLOATS;
+// reduced rows [EG] and the epilogue scratch.  The compact layout (one
+// epilogue pass: per <= EG; or S = 1) keeps [min(per, EG)] reduced rows and
+// puts the scratch over the peers' rows, which are dead by then.  It is taken
+// only where it is what lets two CTAs share an SM: measured at 33 tokens, the
+// smaller footprint alone made the decode round slower (its CTAs and the next
+// kernel's share SMs differently under programmatic dependent launch).
+struct YLayout {
+  int ys, scratch, floats;  // offsets of the reduced rows and the scratch; total fp32 words
+};
+inline YLayout gemm_y_layout(int nt, int S, int per, bool compact) {
+  const int rx = S * per * YLD;
+  if (!compact) return {nt * YLD + rx, nt * YLD + rx + EG * YLD, nt * YLD + rx + EG * YLD + EPI_SCRATCH_FLOATS};
+  if (S == 1) return {nt * YLD, nt * YLD, nt * YLD + EPI_SCRATCH_FLOATS};
+  const int ys = nt * YLD + (rx > EPI_SCRATCH_FLOATS ? rx : EPI_SCRATCH_FLOATS);
+  return {ys, nt * YLD, ys + per * YLD};
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -111,7 +119,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
                                                             const __grid_constant__ CUtensorMap tmx_hi,
                                                             const __grid_constant__ CUtensorMap tmx_lo,
                                                             GemmArgs a, int nt, int two, int stages,
-                                                            int ring_bytes, int per) {
+                                                            int ring_bytes, int per, int ys_off, int scr_off) {
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzled tiles, by pointer arithmetic
@@ -122,16 +130,11 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   uint8_t* sB = sA + stages * A_BYTES;
   // after the MMAs the ring is free: the partial tile, the partial rows the
   // cluster peers send, the reduced rows and the epilogue scratch live there
-  // (gemm_y_floats).  With one epilogue pass (per <= EG) the scratch takes the
-  // place of the partial tile and the peers' rows, which are dead by then.
-  const bool alias = gridDim.y > 1 && per <= EG;
+  // at the offsets of gemm_y_layout
   float* Yp = reinterpret_cast<float*>(smem);             // [nt][YLD]
   float* RX = Yp + nt * YLD;                               // [S][per][YLD] peers' partial rows
-  const int ys_off = gridDim.y == 1 ? nt * YLD
-                     : alias ? max((nt + (int)gridDim.y * per) * YLD, EPI_SCRATCH_FLOATS)
-                             : (nt + (int)gridDim.y * per) * YLD;
-  float* Ys = Yp + ys_off;                                 // [min(per, EG)][YLD] (unused when S = 1)
-  float* scratch = gridDim.y == 1 ? Ys : alias ? Yp : Ys + EG * YLD;  // epilogue scratch
+  float* Ys = Yp + ys_off;                                 // reduced rows (unused when S = 1)
+  float* scratch = Yp + scr_off;                           // epilogue scratch
   uint8_t* tail = smem + ring_bytes;
   float* rs_all = reinterpret_cast<float*>(tail);          // [TZ_TC] rstd of the slice's tokens
   float* rr_pre = rs_all + TZ_TC;                          // [EG][NTILE] residual rows, or
@@ -365,9 +368,6 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
           }
         *reinterpret_cast<float4*>(Ys + (size_t)j * YLD + c4) = acc;
       }
-      // an aliased scratch overwrites the partial tile: the copies to the
-      // peers must have read it
-      if (alias && tid == 0) tc::bulk_wait_read();
       __syncthreads();
       if (!failed && rx_ok) {
         EpiPre pre;
@@ -620,9 +620,10 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   const int nkb = cdiv_i(a.kchunk, 64);
   const int stage_bytes = A_BYTES + (two ? 2 : 1) * nt * 128;
   const int per = cdiv_i(a.T < TZ_TC ? a.T : TZ_TC, a.splits);  // tokens each cluster rank reduces
-  const int y_bytes = gemm_y_floats(nt, a.splits, per) * 4;
+  bool compact = false;
   auto smem_of = [&](int st) {
     int ring = st * stage_bytes;
+    const int y_bytes = gemm_y_layout(nt, a.splits, per, compact).floats * 4;
     if (ring < y_bytes) ring = y_bytes;
     ring = (ring + 1023) / 1024 * 1024;
     return std::make_pair((size_t)1024 + ring + TAIL_BYTES, ring);
@@ -631,14 +632,22 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (stages > 6) stages = 6;
   if (a.T <= 2 * 64 + 1) {
     // decode shapes: the deepest ring (at most DECODE_STAGE_CAP, at least
-    // two stages) that keeps two CTAs per SM
+    // two stages) that keeps two CTAs per SM, in the compact layout if the
+    // regular one does not allow that
     if (stages > DECODE_STAGE_CAP) stages = DECODE_STAGE_CAP;
+    if (stages > nkb) stages = nkb;
     while (stages > 2 && smem_of(stages).first > TWO_CTA_SMEM) --stages;
+    if (smem_of(stages).first > TWO_CTA_SMEM && (a.splits == 1 || per <= EG)) {
+      compact = true;
+      stages = DECODE_STAGE_CAP;
+      while (stages > 2 && smem_of(stages).first > TWO_CTA_SMEM) --stages;
+    }
   }
   if (stages > nkb) stages = nkb;
   if (stages < 1) stages = 1;
   const int ring = smem_of(stages).second;
   const size_t smem = smem_of(stages).first;
+  const YLayout yl = gemm_y_layout(nt, a.splits, per, compact);
   if (smem > 227 * 1024) return false;
   static size_t configured = 0;
   if (smem > configured) {
@@ -670,7 +679,7 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, TRACE>, tmw, tmh, tml, a, nt, two, stages, ring, per) ==
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, TRACE>, tmw, tmh, tml, a, nt, two, stages, ring, per, yl.ys, yl.scratch) ==
          cudaSuccess;
 }
 
