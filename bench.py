@@ -413,13 +413,14 @@ def profiled_traffic():
 def kernel_roofline(cfg, B, hbm, dev):
     """The split-K GEMM kernel on one forward's 65 weight launches (every
     layer's packed QKV, O, packed gate/up and down, then the LM head) at the
-    decode launch shape: B + 1 tokens, hi and lo planes stacked as 2 (B + 1)
-    rows.  Timed with CUDA events on the stream it is launched on; the
-    matrices total ~1 GB, more than L2, so every launch streams its weights
-    from HBM."""
+    decode launch shape: B + 1 tokens as bf16 hi and lo planes, each launch
+    with programmatic dependent launch, as the forward launches them (the
+    forward's fused epilogues are a plain fp32 store here).  Timed with CUDA
+    events on the stream it is launched on; the matrices total ~1 GB, more
+    than L2, so every launch streams its weights from HBM."""
     import torch
     from self_speculative_block_gb300.profile_cases import GemmSweep
-    sw = GemmSweep(cfg, 2 * (B + 1), dev)
+    sw = GemmSweep(cfg, B + 1, dev)
     g = sw.graph()
     g.replay()
     s = torch.cuda.current_stream(dev)
@@ -439,7 +440,7 @@ def kernel_roofline(cfg, B, hbm, dev):
     return {"kernel": f"gemm_tc_kernel (tcgen05 split-K GEMM), one forward's {n} weight launches",
             "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
             "traffic": profiled_traffic(), "launch_us": ms * 1e3, "algorithmic_bytes": alg,
-            "rows": 2 * (B + 1), "launches": n}
+            "tokens": B + 1, "planes": 2, "launches": n}
 
 
 if __name__ == "__main__":

@@ -230,10 +230,16 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
  * order).  Up to two 128-row token slices split each tile's K chunks over a
  * thread-block cluster; more slices run them in one CTA.  Either way a row's
  * bits depend on neither T nor the kernel that ran it.  K % 8 == 0; x_hi, x_lo,
- * w 16-byte aligned.  workspace: as gocr_op_linear.  Errors: GOCR_EINVAL
- * (null pointer, shape), GOCR_ECAPACITY (workspace), GOCR_ECUDA (launch). */
+ * w 16-byte aligned.  workspace: as gocr_op_linear.
+ * flags: 0, or GOCR_OP_OVERLAP: launched as the decoder launches it, with
+ * programmatic dependent launch, so that it may start while the stream's
+ * previous kernel finishes.  It then fetches w before that kernel has
+ * completed (x_hi, x_lo and y only after): w must not be written by it.
+ * Errors: GOCR_EINVAL (null pointer, shape, flags), GOCR_ECAPACITY
+ * (workspace), GOCR_ECUDA (launch). */
+#define GOCR_OP_OVERLAP 1u
 int gocr_op_linear_planes(const void* x_hi, const void* x_lo, const void* w, float* y, int T, int N, int K,
-                          void* workspace, size_t workspace_bytes, void* stream);
+                          void* workspace, size_t workspace_bytes, unsigned flags, void* stream);
 
 /* Grouped-query attention of one request window against a KV cache, the
  * decoder's kernel for that dtype.  Operands are planes, as the decoder keeps

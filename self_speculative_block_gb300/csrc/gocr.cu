@@ -1147,9 +1147,10 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
 }
 
 int gocr_op_linear_planes(const void* x_hi, const void* x_lo, const void* w, float* y, int T, int N, int K,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+                          void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
   gocr_handle* h = nullptr;
   if (!x_hi || !x_lo || !w || !y || !workspace) return fail(h, GOCR_EINVAL, "null pointer");
+  if (flags & ~GOCR_OP_OVERLAP) return fail(h, GOCR_EINVAL, "unknown flags 0x%x", flags);
   if (T < 1 || N < 1 || K < 8 || K % 8) return fail(h, GOCR_EINVAL, "bad shape T=%d N=%d K=%d", T, N, K);
   if (((uintptr_t)x_hi | (uintptr_t)x_lo | (uintptr_t)w) & 15) return fail(h, GOCR_EINVAL, "operand not 16-byte aligned");
   if (workspace_bytes < gocr_op_linear_workspace(T, N, K)) return fail(h, GOCR_ECAPACITY, "workspace too small");
@@ -1161,7 +1162,7 @@ int gocr_op_linear_planes(const void* x_hi, const void* x_lo, const void* w, flo
   a.ws = (float*)((char*)workspace + ctr);
   a.epi = EPI_STORE;
   a.e.y = y; a.e.ldy = N;
-  if (!launch_gemm(GOCR_DTYPE_BF16, a, (cudaStream_t)stream, false))
+  if (!launch_gemm(GOCR_DTYPE_BF16, a, (cudaStream_t)stream, (flags & GOCR_OP_OVERLAP) != 0))
     return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   CK(cudaGetLastError());
   return GOCR_OK;

@@ -105,7 +105,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gocr_free": (None, [vp]),
         "gocr_op_linear_workspace": (sz, [i32, i32, i32]),
         "gocr_op_linear": (i32, [i32, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
-        "gocr_op_linear_planes": (i32, [vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
+        "gocr_op_linear_planes": (i32, [vp, vp, vp, vp, i32, i32, i32, vp, sz, ctypes.c_uint, vp]),
         "gocr_op_attention": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gocr_op_linear_static": (i32, [i32, vp, vp, vp, i32, i32, i32, vp]),
     }
@@ -354,9 +354,14 @@ def op_linear(x, w, workspace=None):
     return y
 
 
-def op_linear_planes(x_hi, x_lo, w, workspace=None):
+OP_OVERLAP = 1
+
+
+def op_linear_planes(x_hi, x_lo, w, workspace=None, flags: int = 0):
     """y[T, N] fp32 = (x_hi + x_lo)[T, K] w[N, K]^T on bf16 planes, the
-    decoder's GEMM on its activation planes."""
+    decoder's GEMM on its activation planes.  flags=OP_OVERLAP launches it as
+    the decoder does (programmatic dependent launch; w must not be written by
+    the stream's previous kernel)."""
     torch = _torch()
     lib = load()
     T, K = x_hi.shape
@@ -369,7 +374,7 @@ def op_linear_planes(x_hi, x_lo, w, workspace=None):
         workspace = torch.zeros(need, dtype=torch.uint8, device=x_hi.device)
     stream = torch.cuda.current_stream(x_hi.device).cuda_stream
     _check(lib.gocr_op_linear_planes(x_hi.data_ptr(), x_lo.data_ptr(), w.data_ptr(), y.data_ptr(), T, N, K,
-                                     workspace.data_ptr(), workspace.numel(), stream))
+                                     workspace.data_ptr(), workspace.numel(), flags, stream))
     return y
 
 

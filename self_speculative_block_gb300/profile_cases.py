@@ -13,8 +13,10 @@
     python -m self_speculative_block_gb300.profile_cases sweep
         The split-K GEMM over one forward's 65 weight matrices (16 x packed
         QKV, O, packed gate/up, down, then the LM head) at the decode launch
-        shape: 33 tokens as hi and lo planes, 66 rows.  Runs the sweep once, then
-        once more as a CUDA graph (gemm_tc launches 65..129 are the graph's).
+        shape: 33 tokens as bf16 hi and lo planes, launched with programmatic
+        dependent launch as the forward launches them.  Runs the sweep once,
+        then once more as a CUDA graph (gemm_tc launches 65..129 are the
+        graph's).
 
     python -m self_speculative_block_gb300.profile_cases batch
         The 16-request page batch: 16 ragged prefills (each one plan, one
@@ -45,25 +47,31 @@ def forward_gemm_shapes(cfg: synth.ModelConfig):
 
 
 class GemmSweep:
-    """Device weights, inputs and outputs for the forward's GEMMs at `rows` rows."""
+    """Device weights, hi + lo input planes and outputs for the forward's GEMMs
+    at `tokens` tokens (bf16 models), launched as the decoder launches them:
+    the two-plane tcgen05 kernel, each launch with programmatic dependent
+    launch so that it may start while the previous one finishes."""
 
-    def __init__(self, cfg: synth.ModelConfig, rows: int, device, seed: int = 0):
+    def __init__(self, cfg: synth.ModelConfig, tokens: int, device, seed: int = 0):
         import torch
         from . import gocr
+        if cfg.dtype != synth.BF16:
+            raise ValueError("the GEMM sweep runs the bf16 decoder's kernel")
         self.lib = gocr.load()
-        self.es = 2 if cfg.dtype == synth.BF16 else 4
-        self.dtype = gocr.DTYPE_BF16 if self.es == 2 else gocr.DTYPE_F32
-        tdt = torch.bfloat16 if self.es == 2 else torch.float32
         g = torch.Generator(device=device)
         g.manual_seed(seed)
         self.device = device
-        self.rows = rows
+        self.tokens = tokens
         self.shapes = forward_gemm_shapes(cfg)
-        self.ws = [(0.02 * torch.randn((n, k), generator=g, device=device)).to(tdt) for n, k in self.shapes]
-        self.xs = {k: torch.randn((rows, k), generator=g, device=device).to(tdt)
-                   for k in sorted({k for _, k in self.shapes})}
-        self.ys = [torch.empty((rows, n), dtype=torch.float32, device=device) for n, _ in self.shapes]
-        need = max(self.lib.gocr_op_linear_workspace(rows, n, k) for n, k in self.shapes)
+        self.ws = [(0.02 * torch.randn((n, k), generator=g, device=device)).to(torch.bfloat16)
+                   for n, k in self.shapes]
+        self.xs = {}
+        for k in sorted({k for _, k in self.shapes}):
+            x = torch.randn((tokens, k), generator=g, device=device)
+            hi = x.to(torch.bfloat16)
+            self.xs[k] = (hi, (x - hi.float()).to(torch.bfloat16))
+        self.ys = [torch.empty((tokens, n), dtype=torch.float32, device=device) for n, _ in self.shapes]
+        need = max(self.lib.gocr_op_linear_workspace(tokens, n, k) for n, k in self.shapes)
         self.workspace = torch.zeros(need, dtype=torch.uint8, device=device)
 
     def run(self):
@@ -72,8 +80,10 @@ class GemmSweep:
         from . import gocr
         stream = torch.cuda.current_stream(self.device).cuda_stream
         for (n, k), w, y in zip(self.shapes, self.ws, self.ys):
-            rc = self.lib.gocr_op_linear(self.dtype, self.xs[k].data_ptr(), w.data_ptr(), y.data_ptr(), self.rows,
-                                         n, k, self.workspace.data_ptr(), self.workspace.numel(), stream)
+            xh, xl = self.xs[k]
+            rc = self.lib.gocr_op_linear_planes(xh.data_ptr(), xl.data_ptr(), w.data_ptr(), y.data_ptr(),
+                                                self.tokens, n, k, self.workspace.data_ptr(),
+                                                self.workspace.numel(), gocr.OP_OVERLAP, stream)
             if rc != gocr.GOCR_OK:
                 raise gocr.GocrError(rc, gocr.last_error(None))
 
@@ -89,9 +99,9 @@ class GemmSweep:
         return g
 
     def algorithmic_bytes(self) -> float:
-        """Mean bytes per launch: weights, input, fp32 output."""
-        T, es = self.rows, self.es
-        return sum(n * k * es + T * k * es + T * n * 4 for n, k in self.shapes) / len(self.shapes)
+        """Mean bytes per launch: weights, both input planes, fp32 output."""
+        T = self.tokens
+        return sum(n * k * 2 + 2 * T * k * 2 + T * n * 4 for n, k in self.shapes) / len(self.shapes)
 
 
 def draft_case(B: int = 32):
@@ -109,7 +119,7 @@ def draft_case(B: int = 32):
 
 def sweep_case():
     import torch
-    sw = GemmSweep(synth.BASE, 2 * 33, torch.device("cuda:0"))
+    sw = GemmSweep(synth.BASE, 33, torch.device("cuda:0"))
     g = sw.graph()
     g.replay()
     torch.cuda.synchronize()

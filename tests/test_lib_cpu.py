@@ -60,10 +60,12 @@ def test_op_entry_points_validate_arguments(lib):
     assert lib.gocr_op_linear_workspace(0, 128, 128) == 0
     assert lib.gocr_op_linear_workspace(33, 256, 1536) > 0
     assert lib.gocr_op_linear(0, None, None, None, 1, 1, 8, None, 0, None) == -1
-    assert lib.gocr_op_linear_planes(None, None, None, None, 1, 1, 8, None, 0, None) == -1
+    assert lib.gocr_op_linear_planes(None, None, None, None, 1, 1, 8, None, 0, 0, None) == -1
     one = ctypes.c_void_p(16)
-    assert lib.gocr_op_linear_planes(one, ctypes.c_void_p(18), one, one, 1, 1, 8, one, 1 << 20, None) == -1
+    assert lib.gocr_op_linear_planes(one, ctypes.c_void_p(18), one, one, 1, 1, 8, one, 1 << 20, 0, None) == -1
     assert b"aligned" in lib.gocr_last_error(None)
+    assert lib.gocr_op_linear_planes(one, one, one, one, 1, 1, 8, one, 1 << 20, 6, None) == -1
+    assert b"flags" in lib.gocr_last_error(None)
     assert lib.gocr_op_attention(1, None, None, None, None, None, None, None, None, 1, 4, 2, 64, 16, None) == -1
 
 
