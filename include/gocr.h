@@ -164,12 +164,22 @@ int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0);
  *       programmatic dependent launch;
  *     GOCR_FORWARD_PERSISTENT  one persistent kernel per forward, one CTA per
  *       SM: every layer's GEMMs, attention and epilogues and the LM head, with
- *       device counters in place of kernel boundaries.
+ *       device counters in place of kernel boundaries.  Only for handles
+ *       created with the mma.sync attention (GOCR_ATTN_MMA_SYNC, the default),
+ *       whose tile code it shares; GOCR_ESTATE otherwise.
  *   Both give bit-identical results (the same reductions in the same order).
  *   Prefill, fp32 models and larger forwards always run one kernel per
  *   operation.  The environment variable GOCR_FORWARD=persistent selects
  *   PERSISTENT at create time.  Changing the option drops the handle's
  *   captured graphs.
+ *   GOCR_OPT_ATTENTION (get only) the tensor-core attention kernels of a bf16
+ *                     handle, fixed at create time:
+ *     GOCR_ATTN_MMA_SYNC (default)  64-row tiles on mma.sync;
+ *     GOCR_ATTN_TCGEN05  128-row tiles with both contractions on tcgen05 and
+ *       their accumulators in tensor memory (GOCR_ATTN=tc in the environment
+ *       at create time; gocr_op_attention reads it per call).
+ *   The two round differently; each is bit-consistent across its own
+ *   forwards.
  * GOCR_EINVAL for an unknown option or value. */
 /*   GOCR_OPT_PERSISTENT_FORWARDS  (get only) forwards the persistent kernel
  *                     completed in the last decode or debug-forward call of
@@ -180,8 +190,9 @@ int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0);
  *                     time turns it on).
  *   GOCR_OPT_GRID_CTAS (get only) CTAs of the persistent forward (SM count). */
 enum { GOCR_OPT_FORWARD = 1, GOCR_OPT_PERSISTENT_FORWARDS = 2, GOCR_OPT_TRACE_RECORDS = 3,
-       GOCR_OPT_GRID_CTAS = 4 };
+       GOCR_OPT_GRID_CTAS = 4, GOCR_OPT_ATTENTION = 5 };
 enum { GOCR_FORWARD_PERSISTENT = 0, GOCR_FORWARD_OPS = 1 };
+enum { GOCR_ATTN_TCGEN05 = 0, GOCR_ATTN_MMA_SYNC = 1 };
 int gocr_set_option(gocr_handle* h, int option, int value);
 int gocr_get_option(const gocr_handle* h, int option, int* value);
 

@@ -29,6 +29,7 @@
 #include <cstdlib>
 
 #include "attn_core.cuh"
+#include "attn_tc.cuh"
 #include "tc.cuh"
 
 namespace gocr {
@@ -200,15 +201,16 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
   if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 
-// Merge kernel: one CTA per (pair of rows, kv head x row group, slot).
-template <int D, bool TRACE>
-__global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R) {
+// Merge kernel: one CTA per (ppc pairs of rows, kv head x row group, slot);
+// tiles of TQR rows.
+template <int D, int TQR, bool TRACE>
+__global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R, int ppc) {
   constexpr int RLD = attn::Geo<D>::RLD;
   __shared__ float WS[2 * 64];
   __shared__ float IL[2];
   __shared__ float4 AC[4 * 64];
   const Grp grp = Grp::block();
-  const int pair = blockIdx.x, group = blockIdx.y, slot = blockIdx.z;
+  const int group = blockIdx.y, slot = blockIdx.z;
   const int kvh = group % a.Hkv, rg = group / a.Hkv;
   const int G = a.Hq / a.Hkv;
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -222,20 +224,74 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R)
     row0 = a.plan->slot_row0[slot];
     nrows = a.plan->slot_nrows[slot];
   }
-  const int qr0 = rg * attn::QR;
-  if (qr0 + 2 * pair >= nrows * G) return;
+  const int qr0 = rg * TQR;
+  if (qr0 + 2 * blockIdx.x * ppc >= nrows * G) return;
   const int n_chunks = a.part_chunks[(size_t)slot * gridDim.y + group];
   const int n_ranks = n_chunks < R ? n_chunks : R;
-  const float* base = a.part + ((size_t)slot * gridDim.y + group) * R * attn::QR * RLD;
-  auto part = [&](int c, int i) -> const float* { return base + ((size_t)c * attn::QR + i) * RLD; };
-  attn::merge_rows<D, false>(a, grp, part, WS, IL, AC, n_ranks, R, 2 * pair, 1, 2, kvh, qr0, row0, nrows);
+  const float* base = a.part + ((size_t)slot * gridDim.y + group) * R * TQR * RLD;
+  auto part = [&](int c, int i) -> const float* { return base + ((size_t)c * TQR + i) * RLD; };
+  for (int k = 0; k < ppc; ++k) {
+    const int pair = blockIdx.x * ppc + k;
+    if (qr0 + 2 * pair >= nrows * G) break;  // uniform over the CTA
+    attn::merge_rows<D, false>(a, grp, part, WS, IL, AC, n_ranks, R, 2 * pair, 1, 2, kvh, qr0, row0, nrows);
+  }
   if (TRACE && threadIdx.x == 0) trace_mark(a.trace, 3);
 }
 
 size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, int R) {
   const int G = Hq / Hkv;
-  const size_t groups = (size_t)Hkv * ((max_rows * G + attn::QR - 1) / attn::QR);
-  return (size_t)n_slots * groups * R * attn::QR * (d + 4);
+  size_t best = 0;
+  for (int qr : {attn::QR, attn_tc::QR}) {
+    const size_t groups = (size_t)Hkv * ((max_rows * G + qr - 1) / qr);
+    const size_t f = (size_t)n_slots * groups * R * qr * (d + 4);
+    if (f > best) best = f;
+  }
+  return best;
+}
+
+// The merge after a partial kernel of TQR-row tiles (always ordered after it).
+template <int D, int TQR, bool TRACE>
+static bool launch_attn_merge(const AttnArgs& a, int R, int n_groups, int n_slots, cudaStream_t s) {
+  // with few ranks a row pair is little work: four pairs per CTA then
+  const int ppc = R <= 16 ? 4 : 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(TQR / 2 / ppc, n_groups, n_slots);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attention_merge_kernel<D, TQR, TRACE>, a, R, ppc) == cudaSuccess;
+}
+
+template <int D, bool TRACE>
+static bool launch_attn_tc_t(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
+  using Gm = attn_tc::Geo<D>;
+  const int G = a.Hq / a.Hkv;
+  const int n_rg = (max_rows * G + attn_tc::QR - 1) / attn_tc::QR;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(attention_tc_part_kernel<D, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Gm::SMEM) != cudaSuccess)
+      return false;
+    prefer_shared(reinterpret_cast<const void*>(attention_tc_part_kernel<D, TRACE>));
+    configured = true;
+  }
+  const int R = a.ranks > 0 ? a.ranks : attention_ranks(a.cap, 1);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.Hkv * n_rg, R, n_slots);
+  cfg.blockDim = dim3(attn_tc::THREADS);
+  cfg.dynamicSmemBytes = Gm::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, attention_tc_part_kernel<D, TRACE>, a) != cudaSuccess) return false;
+  return launch_attn_merge<D, attn_tc::QR, TRACE>(a, R, a.Hkv * n_rg, n_slots, s);
 }
 
 template <int D, bool TRACE>
@@ -262,15 +318,14 @@ static bool launch_attn_mma_t(const AttnArgs& a, int n_slots, int max_rows, cuda
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, attention_part_kernel<D, TRACE>, a) != cudaSuccess) return false;
-  // the merge reads every rank's rows: always ordered after the partial kernel
-  cfg.gridDim = dim3(attn::QR / 2, a.Hkv * n_rg, n_slots);
-  cfg.dynamicSmemBytes = 0;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attention_merge_kernel<D, TRACE>, a, R) == cudaSuccess;
+  return launch_attn_merge<D, attn::QR, TRACE>(a, R, a.Hkv * n_rg, n_slots, s);
 }
 
 template <int D>
 static bool launch_attn_mma(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
+  if (a.kind == ATTN_TCGEN05)
+    return a.trace ? launch_attn_tc_t<D, true>(a, n_slots, max_rows, s, pdl)
+                   : launch_attn_tc_t<D, false>(a, n_slots, max_rows, s, pdl);
   return a.trace ? launch_attn_mma_t<D, true>(a, n_slots, max_rows, s, pdl)
                  : launch_attn_mma_t<D, false>(a, n_slots, max_rows, s, pdl);
 }

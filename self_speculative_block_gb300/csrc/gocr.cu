@@ -76,6 +76,7 @@ struct gocr_handle {
   int q_dim = 0, kv_dim = 0, qkv_n = 0, gu_n = 0;
   int cap = 0, T_max = 0, T_dec = 0, sched_cap = 0;
   int attn_ranks = 1;  // key-chunk ranks of the tensor-core attention, fixed for the handle
+  int attn_kind = ATTN_MMA_SYNC;  // tensor-core attention kernels, fixed for the handle
   long long layer_stride = 0, req_stride = 0;
 
   // KV cache [req][layer][kv head][position][head_dim]: bf16 hi/lo planes for
@@ -253,6 +254,8 @@ void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_o
     at.part = h->att_part;
     at.part_chunks = h->att_chunks;
     at.ranks = h->attn_ranks;
+    at.kind = h->attn_kind;
+    at.err = h->err;
     f.at.push_back(at);
     // O projection + residual; planes of resid * g_mlp for the MLP
     GemmArgs go = gemm_base(h, h->at_hi, h->at_lo, h->q_dim, h->wo[l], T, H, h->q_dim);
@@ -704,6 +707,10 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->attn_ranks = attention_ranks(h->cap, c.max_requests);
     const char* ar = getenv("GOCR_ATTN_RANKS");
     if (ar && atoi(ar) >= 1 && atoi(ar) <= 64) h->attn_ranks = atoi(ar) < (h->cap + 31) / 32 ? atoi(ar) : (h->cap + 31) / 32;
+    // GOCR_ATTN=tc: the tcgen05 attention (measured slower at the decode
+    // shapes, where a tile holds one or two chunks; see attn_tc.cuh)
+    const char* ak = getenv("GOCR_ATTN");
+    h->attn_kind = ak && strcmp(ak, "tc") == 0 ? ATTN_TCGEN05 : ATTN_MMA_SYNC;
   }
   CKC(cudaStreamCreateWithFlags(&h->hs, cudaStreamNonBlocking));
   CKC(cudaEventCreate(&h->ev0));
@@ -809,7 +816,7 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
   if (h->dtype == GOCR_DTYPE_BF16) {
     // persistent decode forward: decode shapes of up to 128 rows
     const char* fw = getenv("GOCR_FORWARD");
-    h->mk_enabled = fw && strcmp(fw, "persistent") == 0;
+    h->mk_enabled = fw && strcmp(fw, "persistent") == 0 && h->attn_kind == ATTN_MMA_SYNC;
     const char* pf = getenv("GOCR_MK_PREFETCH");
     if (pf) h->mk_pf = atoi(pf) < 0 ? 0 : atoi(pf);
     int dev = 0;
@@ -1038,6 +1045,8 @@ int gocr_set_option(gocr_handle* h, int option, int value) {
   if (!h) return fail(nullptr, GOCR_EINVAL, "null handle");
   if (option != GOCR_OPT_FORWARD) return fail(h, GOCR_EINVAL, "unknown option %d", option);
   if (value != GOCR_FORWARD_PERSISTENT && value != GOCR_FORWARD_OPS) return fail(h, GOCR_EINVAL, "bad value %d", value);
+  if (value == GOCR_FORWARD_PERSISTENT && h->attn_kind != ATTN_MMA_SYNC)
+    return fail(h, GOCR_ESTATE, "the persistent forward needs the mma.sync attention (the default)");
   const bool en = value == GOCR_FORWARD_PERSISTENT && h->mk_ctr != nullptr;
   if (en == h->mk_enabled) return GOCR_OK;
   CK(cudaStreamSynchronize(h->hs));
@@ -1072,6 +1081,10 @@ int gocr_get_option(const gocr_handle* h, int option, int* value) {
   }
   if (option == GOCR_OPT_GRID_CTAS) {
     *value = h->mk_G;
+    return GOCR_OK;
+  }
+  if (option == GOCR_OPT_ATTENTION) {
+    *value = h->attn_kind == ATTN_MMA_SYNC ? GOCR_ATTN_MMA_SYNC : GOCR_ATTN_TCGEN05;
     return GOCR_OK;
   }
   return GOCR_EINVAL;
@@ -1182,6 +1195,10 @@ int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void*
   a.req_stride = 0; a.o_hi = o; a.o_lo = nullptr; a.out_bf16 = 0;
   a.row_lim = lim; a.plan = nullptr;
   a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.cap = cap; a.scale = 1.0f / sqrtf((float)d);
+  {
+    const char* ak = getenv("GOCR_ATTN");
+    a.kind = ak && strcmp(ak, "tc") == 0 ? ATTN_TCGEN05 : ATTN_MMA_SYNC;
+  }
   if (dtype == GOCR_DTYPE_BF16) {
     // partial rows of the attention ranks: a process-wide scratch buffer per
     // device, grown on demand (calls must not overlap on the GPU)

@@ -114,8 +114,16 @@ struct alignas(16) AttnArgs {
   float* part;
   int* part_chunks;           // [slot][kv head x row group] chunks the group's rows read
   int ranks;                  // key-chunk ranks R (attention_ranks); 0: attention_ranks(cap, 1)
+  int kind;                   // bf16 models: ATTN_TCGEN05 or ATTN_MMA_SYNC
+  int* err;                   // device error word (bounded waits), or NULL
   unsigned long long* trace;  // launch timeline record, as GemmArgs::trace
 };
+// Tensor-core attention kernels of bf16 models.  ATTN_MMA_SYNC (default):
+// 64-row tiles on mma.sync, the tile code the persistent forward shares.
+// ATTN_TCGEN05: 128-row tiles, both contractions on tcgen05 with accumulators
+// in tensor memory.  The two give different bits; a handle fixes one at
+// creation.
+enum { ATTN_TCGEN05 = 0, ATTN_MMA_SYNC = 1 };
 // Key-chunk ranks of the tensor-core attention: rank r reads chunks r, r + R, ...
 // R = attention_ranks(cap, n_req): ATTN_RANKS for one request, fewer (at
 // least ATTN_RANKS_MIN) when a forward carries up to n_req requests, so that
@@ -132,6 +140,7 @@ inline int attention_ranks(int cap, int n_req) {
   return c < 1 ? 1 : (c < r ? c : r);
 }
 // fp32 words of the tensor-core attention's partial rows for n_slots slots of up to max_rows rows, R ranks
+// (enough for either kind)
 size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, int R);
 // dtype 1: tensor-core cluster kernel; 0: CUDA-core kernel.
 bool launch_attention(int dtype, const AttnArgs& a, int n_slots, int max_rows_per_slot, cudaStream_t s,

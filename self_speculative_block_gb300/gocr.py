@@ -24,8 +24,9 @@ ERRORS = {-1: "EINVAL", -2: "ECAPACITY", -3: "ECUDA", -4: "EDEVICE", -5: "ETIMEO
 DTYPE_F32, DTYPE_BF16 = 0, 1
 MODE_AR, MODE_SELFSPEC = 0, 1
 FWD_AR, FWD_DRAFT, FWD_VERIFY = 0, 1, 2
-OPT_FORWARD, OPT_PERSISTENT_FORWARDS, OPT_TRACE_RECORDS, OPT_GRID_CTAS = 1, 2, 3, 4
+OPT_FORWARD, OPT_PERSISTENT_FORWARDS, OPT_TRACE_RECORDS, OPT_GRID_CTAS, OPT_ATTENTION = 1, 2, 3, 4, 5
 FORWARD_PERSISTENT, FORWARD_OPS = 0, 1
+ATTN_TCGEN05, ATTN_MMA_SYNC = 0, 1
 MAX_BLOCK = 64
 LAYER_TENSORS = 9
 
@@ -300,6 +301,10 @@ class Decoder:
         v = ctypes.c_int32()
         _check(self.lib.gocr_get_option(self.h, OPT_PERSISTENT_FORWARDS, ctypes.byref(v)), self.h)
         return v.value
+
+    def attention_kind(self) -> int:
+        """ATTN_TCGEN05 or ATTN_MMA_SYNC (GOCR_ATTN=mma at create time)."""
+        return self._option(OPT_ATTENTION)
 
     def _option(self, opt: int) -> int:
         v = ctypes.c_int32()

@@ -1,4 +1,4 @@
-"""bf16 decode path (tcgen05 GEMM + tensor-core cluster attention) through the C ABI.
+"""bf16 decode path (tcgen05 GEMMs + tensor-core split-KV attention) through the C ABI.
 
 * a small bf16 decoder with the 0.5B model's head geometry (GQA 3:1, head_dim
   128): draft / verify / AR logits vs the oracle within max-abs 3e-2 /
@@ -138,6 +138,52 @@ def test_small_batched_ragged_equals_single_ar(small):
             assert sts[r]["committed"] == news[r] - 1
 
 
+def test_small_tcgen05_attention_handle(small, monkeypatch):
+    """A handle with the tcgen05 attention: draft and verify logits against the
+    oracle, and its self-speculative output (single and batched) equal to its
+    own AR-greedy output bit for bit."""
+    g, synth, cfg, model = small["g"], small["synth"], small["cfg"], small["model"]
+    monkeypatch.setenv("GOCR_ATTN", "tc")
+    dec = g.Decoder(cfg, small["W"], max_ctx=100 + 200 + 64 + 8, max_block=64, max_requests=4)
+    monkeypatch.delenv("GOCR_ATTN")
+    try:
+        assert dec.attention_kind() == g.ATTN_TCGEN05
+        prefix = small["prefix"].astype(np.float64)
+        for B in (1, 32, 64):
+            dec.prefill(0, small["prefix"])
+            cl, x0 = dec.state(0)
+            lg_d = dec.debug_forward(0, g.FWD_DRAFT, [x0] + [0] * B)
+            st = oracle.prefill(model, prefix)
+            ref_d, kd, vd = oracle.draft_forward(model, st, B)
+            ok, err = close(lg_d, ref_d)
+            assert ok, (B, err)
+            a0 = int(np.argmax(lg_d[0]))
+            drafts = [int(t) for t in np.random.default_rng(B).integers(0, cfg.vocab, B)]
+            lg_v = dec.debug_forward(0, g.FWD_VERIFY, [a0] + drafts)
+            st.append([k[:1] for k in kd], [v[:1] for v in vd])
+            ref_v, _, _ = oracle.verify_forward(model, st, a0, drafts)
+            ok, err = close(lg_v, ref_v)
+            assert ok, (B, err)
+        dec.prefill(0, small["prefix"])
+        ar, _ = dec.decode(0, g.MODE_AR, 0, 200)
+        for B in (8, 32, 64):
+            dec.prefill(0, small["prefix"])
+            ss, _ = dec.decode(0, g.MODE_SELFSPEC, B, 200)
+            assert list(ss) == list(ar), B
+        lens, news = [37, 100, 64, 129], [40, 120, 7, 90]
+        prefixes = [synth.make_prefix(cfg, n, seed=1000 + r) for r, n in enumerate(lens)]
+        refs = []
+        for r in range(4):
+            dec.prefill(r, prefixes[r])
+            refs.append(list(dec.decode(r, g.MODE_AR, 0, news[r])[0]))
+        for r in range(4):
+            dec.prefill(r, prefixes[r])
+        outs, _ = dec.decode_batch([0, 1, 2, 3], g.MODE_SELFSPEC, 32, news)
+        assert [list(o) for o in outs] == refs
+    finally:
+        dec.close()
+
+
 # ------------------------------------------------------------------ 0.5B-class decoder
 
 @pytest.fixture(scope="module")
@@ -214,10 +260,13 @@ def test_base_sampled_logits_vs_oracle(base):
 def test_base_persistent_forward_equals_per_operation(base):
     """The persistent decode forward and the per-operation kernels give the
     same bits on the 0.5B-class decoder: draft logits and the text-region
-    self-speculative token stream."""
-    dec, g, synth = base["dec"], base["g"], base["synth"]
+    self-speculative token stream (a handle of its own: the mma.sync attention,
+    whose tile code the persistent kernel shares, and no captured graphs)."""
+    g, synth = base["g"], base["synth"]
     wl = synth.WORKLOADS["text"]
     prefix = synth.make_prefix(wl.model, wl.prefix_len)
+    dec = g.Decoder(base["cfg"], base["W"], max_ctx=wl.prefix_len + wl.max_new + 64 + 8, max_block=wl.block)
+    assert dec.attention_kind() == g.ATTN_MMA_SYNC
 
     def run():
         dec.prefill(0, prefix)
@@ -227,13 +276,12 @@ def test_base_persistent_forward_equals_per_operation(base):
         ss, _ = dec.decode(0, g.MODE_SELFSPEC, wl.block, wl.max_new)
         return lg, list(ss)
 
-    dec.set_forward_path(g.FORWARD_OPS)
-    lg_ops, ss_ops = run()
-    dec.set_forward_path(g.FORWARD_PERSISTENT)
     try:
+        lg_ops, ss_ops = run()
+        dec.set_forward_path(g.FORWARD_PERSISTENT)
         lg_p, ss_p = run()
         assert dec.persistent_forwards() > 0
     finally:
-        dec.set_forward_path(g.FORWARD_OPS)
+        dec.close()
     assert np.array_equal(lg_ops.view(np.uint32), lg_p.view(np.uint32))
     assert ss_ops == ss_p

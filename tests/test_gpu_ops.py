@@ -116,15 +116,24 @@ def _attn_case(rng, T, Hq, Hkv, d, cap, lims, dtype):
     return o, ref
 
 
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def _attn_kind(monkeypatch, dt):
+    """bf16: the mma.sync kernel (default); bf16-tc: the tcgen05 kernel."""
+    if dt == "bf16-tc":
+        monkeypatch.setenv("GOCR_ATTN", "tc")
+    else:
+        monkeypatch.delenv("GOCR_ATTN", raising=False)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16", "bf16-tc"])
 @pytest.mark.parametrize("Hq,Hkv,d", [(4, 2, 64), (12, 4, 128)])
-@pytest.mark.parametrize("p,B", [(0, 1), (5, 4), (130, 8), (1000, 32)])
-def test_attention_draft_and_verify_masks(g, dt, Hq, Hkv, d, p, B):
+@pytest.mark.parametrize("p,B", [(0, 1), (5, 4), (130, 8), (1000, 32), (300, 64)])
+def test_attention_draft_and_verify_masks(g, monkeypatch, dt, Hq, Hkv, d, p, B):
+    _attn_kind(monkeypatch, dt)
     rng = np.random.default_rng(p + B + d)
     cap = p + B + 3
-    dtype = g.DTYPE_BF16 if dt == "bf16" else g.DTYPE_F32
+    dtype = g.DTYPE_F32 if dt == "f32" else g.DTYPE_BF16
     # the bf16 kernel takes hi/lo bf16 planes of the fp32 inputs and bf16 probabilities
-    tol = 5e-3 if dt == "bf16" else 2e-5
+    tol = 2e-5 if dt == "f32" else 5e-3
     # draft: boundary row causal (lim p), [M] rows see the window (lim p+B)
     o, ref = _attn_case(rng, B + 1, Hq, Hkv, d, cap, [p] + [p + B] * B, dtype)
     np.testing.assert_allclose(o, ref, rtol=tol, atol=tol)
@@ -133,10 +142,11 @@ def test_attention_draft_and_verify_masks(g, dt, Hq, Hkv, d, p, B):
     np.testing.assert_allclose(o, ref, rtol=tol, atol=tol)
 
 
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
-def test_attention_row_bits_do_not_depend_on_other_rows(g, dt):
+@pytest.mark.parametrize("dt", ["f32", "bf16", "bf16-tc"])
+def test_attention_row_bits_do_not_depend_on_other_rows(g, monkeypatch, dt):
+    _attn_kind(monkeypatch, dt)
     rng = np.random.default_rng(3)
-    dtype = g.DTYPE_BF16 if dt == "bf16" else g.DTYPE_F32
+    dtype = g.DTYPE_F32 if dt == "f32" else g.DTYPE_BF16
     Hq, Hkv, d, cap = 12, 4, 128, 700
     qn = rng.standard_normal((65, Hq, d)).astype(np.float32)
     k = _planes(rng.standard_normal((Hkv, cap, d)).astype(np.float32), dtype)

@@ -1,5 +1,7 @@
 """The persistent decode forward (one kernel per forward, one CTA per SM)
-against the per-operation forward (one kernel per GEMM and attention).
+against the per-operation forward (one kernel per GEMM and attention), on a
+handle with the mma.sync attention, whose tile code the persistent kernel
+shares.
 
 Both run the same reductions in the same order, so every result must be
 bit-identical: draft, verify and AR logits, the KV cache rows the forward
@@ -19,13 +21,17 @@ torch = pytest.importorskip("torch")
 def small():
     if not torch.cuda.is_available():
         pytest.fail("gpu tests need a CUDA device")
+    import os
     from self_speculative_block_gb300 import build, gocr, synth
     build.build()
     cfg = synth.ModelConfig(n_layers=2, hidden=512, n_q_heads=6, n_kv_heads=2, head_dim=128, ffn=1024,
                             vocab=2048, dtype=synth.BF16)
     W = synth.make_weights(cfg, seed=31)
     prefix = synth.make_prefix(cfg, 150, seed=32)
+    # the persistent forward shares the mma.sync attention's tile code (the default)
+    assert os.environ.get("GOCR_ATTN") is None
     dec = gocr.Decoder(cfg, W, max_ctx=150 + 200 + 64 + 8, max_block=64, max_requests=4)
+    assert dec.attention_kind() == gocr.ATTN_MMA_SYNC
     assert dec.forward_path() == gocr.FORWARD_OPS
     yield dict(g=gocr, synth=synth, cfg=cfg, prefix=prefix, dec=dec)
     dec.close()
@@ -132,6 +138,21 @@ def test_batched_ragged_bit_identical(small):
     ops, pers = both_paths(dec, g, run)
     assert ops == pers
     assert pers[0] == pers[1] == pers[2]
+
+
+def test_persistent_forward_needs_the_mma_sync_attention(small, monkeypatch):
+    g, synth, cfg = small["g"], small["synth"], small["cfg"]
+    W = synth.make_weights(cfg, seed=31)
+    monkeypatch.setenv("GOCR_ATTN", "tc")
+    dec = g.Decoder(cfg, W, max_ctx=256, max_block=8)
+    monkeypatch.delenv("GOCR_ATTN")
+    try:
+        assert dec.attention_kind() == g.ATTN_TCGEN05
+        with pytest.raises(g.GocrError):
+            dec.set_forward_path(g.FORWARD_PERSISTENT)
+        assert dec.forward_path() == g.FORWARD_OPS
+    finally:
+        dec.close()
 
 
 def test_option_round_trip(small):
