@@ -201,10 +201,10 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
   if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 
-// Merge kernel: one CTA per (ppc pairs of rows, kv head x row group, slot);
+// Merge kernel: one CTA per (PPC pairs of rows, kv head x row group, slot);
 // tiles of TQR rows.
-template <int D, int TQR, bool TRACE>
-__global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R, int ppc) {
+template <int D, int TQR, int PPC, bool TRACE>
+__global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R) {
   constexpr int RLD = attn::Geo<D>::RLD;
   __shared__ float WS[2 * 64];
   __shared__ float IL[2];
@@ -225,13 +225,14 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R,
     nrows = a.plan->slot_nrows[slot];
   }
   const int qr0 = rg * TQR;
-  if (qr0 + 2 * blockIdx.x * ppc >= nrows * G) return;
+  if (qr0 + 2 * blockIdx.x * PPC >= nrows * G) return;
   const int n_chunks = a.part_chunks[(size_t)slot * gridDim.y + group];
   const int n_ranks = n_chunks < R ? n_chunks : R;
   const float* base = a.part + ((size_t)slot * gridDim.y + group) * R * TQR * RLD;
   auto part = [&](int c, int i) -> const float* { return base + ((size_t)c * TQR + i) * RLD; };
-  for (int k = 0; k < ppc; ++k) {
-    const int pair = blockIdx.x * ppc + k;
+#pragma unroll
+  for (int k = 0; k < PPC; ++k) {
+    const int pair = blockIdx.x * PPC + k;
     if (qr0 + 2 * pair >= nrows * G) break;  // uniform over the CTA
     attn::merge_rows<D, false>(a, grp, part, WS, IL, AC, n_ranks, R, 2 * pair, 1, 2, kvh, qr0, row0, nrows);
   }
@@ -263,7 +264,8 @@ static bool launch_attn_merge(const AttnArgs& a, int R, int n_groups, int n_slot
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attention_merge_kernel<D, TQR, TRACE>, a, R, ppc) == cudaSuccess;
+  return (ppc == 4 ? cudaLaunchKernelEx(&cfg, attention_merge_kernel<D, TQR, 4, TRACE>, a, R)
+                   : cudaLaunchKernelEx(&cfg, attention_merge_kernel<D, TQR, 1, TRACE>, a, R)) == cudaSuccess;
 }
 
 template <int D, bool TRACE>
