@@ -163,12 +163,14 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
   // committed cache before the dependency wait (decode launches only)
-  int req_pre = -1;
+  int req_pre = -1, kv_kmax = -1;
   bool pre = false;
   if (a.st && a.slot_req) {
     req_pre = a.slot_req[slot];
-    pre = attn::tile_prefetch<D>(sm_raw, attn::kv_planes(a, req_pre, kvh, D), rank, R, a.st[req_pre].cache_len,
-                                 tid);
+    const int pc = a.st[req_pre].cache_len;
+    pre = attn::tile_prefetch<D>(sm_raw, attn::kv_planes(a, req_pre, kvh, D), rank, R, pc, tid);
+    // no row of this forward reads past the round-start length plus its rows
+    kv_kmax = min(a.cap - 1, pc + a.rows_per_slot);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (TRACE && tid == 0) trace_mark(a.trace, 1);
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
     return;
   }
   const int n_chunks = attn::tile_partial<D, TRACE>(a, sm_raw, grp, attn::kv_planes(a, req, kvh, D), rank, R, kvh,
-                                                    qr0, row0, nrows, pre, &s_maxlim);
+                                                    qr0, row0, nrows, pre, &s_maxlim, kv_kmax);
   if (rank == 0 && tid == 0) a.part_chunks[(size_t)slot * gridDim.x + group] = n_chunks;
   if (rank >= n_chunks) return;
   // all 64 rows, also those past the window (which the merge reads but does

@@ -144,9 +144,16 @@ __device__ __forceinline__ float* staged_rows(uint8_t* sm) {
 }
 
 // TRACE: record timeline marks in a.trace (first chunk ready, loop done).
+// kv_kmax >= 0 (decode launches): every cache position up to kv_kmax holds a
+// finite value (the cache is zeroed at allocation and only ever written with
+// finite k, v), so a first chunk that tile_prefetch did not fetch is loaded
+// up to kv_kmax right away, together with Q, instead of after the rows' key
+// limits are known.  Keys past a row's limit contribute exact zeros either
+// way.
 template <int D, bool TRACE = false>
 __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, const KvPlanes& kv, int rank,
-                            int stride, int kvh, int qr0, int row0, int nrows, bool pre, int* s_maxlim) {
+                            int stride, int kvh, int qr0, int row0, int nrows, bool pre, int* s_maxlim,
+                            int kv_kmax = -1) {
   using Gm = Geo<D>;
   constexpr int QLD = Gm::QLD, OLD = Gm::OLD, TILE = Gm::TILE, RLD = Gm::RLD;
   bf16* Qh = reinterpret_cast<bf16*>(sm);               // [QR][QLD]
@@ -168,6 +175,11 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
 
   if (tid == 0) *s_maxlim = -1;
   grp.sync();
+  const bool early = !pre && kv_kmax >= 0 && rank * AC <= kv_kmax;
+  if (early) {
+    load_planes<D>(KV, kv, 0, 2, rank, kv_kmax, tid);
+    load_planes<D>(KV, kv, 2, 2, rank, kv_kmax, tid);
+  }
   // Q planes of this row group (zero past the window) and the rows' key limits
   for (int x = tid; x < 2 * QR * (D / 8); x += 256) {
     const int pl = x / (QR * (D / 8)), rem = x % (QR * (D / 8));
@@ -211,7 +223,7 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   // streams in while this chunk's softmax and PV run, V of the next chunk
   // while the next QK^T runs.  Group order: [K+V of the first chunk] (issued
   // early when it is committed cache), Q, then K, V per chunk.
-  if (!pre && rank < n_chunks) {
+  if (!pre && !early && rank < n_chunks) {
     load_planes<D>(KV, kv, 0, 2, rank, maxlim, tid);
     load_planes<D>(KV, kv, 2, 2, rank, maxlim, tid);
   }
