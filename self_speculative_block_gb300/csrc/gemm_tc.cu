@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
 }
 
 // Many-slice variant (more than two 128-token slices, e.g. prefill and the
-// batched round): one CTA per (128-row weight tile, token slice) runs the S
+// batched round): one CTA per (128-row weight tile, NT-token slice) runs the S
 // K chunks of the split rule one after another.  Each chunk's MMAs start a
 // fresh accumulator (two in TMEM, so the next chunk's MMAs overlap this
 // chunk's drain), and four drain warps add the chunk sums into running sums
@@ -402,16 +402,17 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
 // eight warps run the epilogue.  Warp 0: TMA producer; warp 1: MMA issuer;
 // warps 4-7: drain.  Inputs are bf16 hi + lo planes (single-plane launches
 // take the clustered kernel).
+// NT = 128: one CTA per SM, four 48 KB stages.  NT = 64: two CTAs per SM,
+// three 32 KB stages, twice the work units, so that narrow matrices (few
+// weight tiles) still occupy every SM.
 constexpr int SEQ_THREADS = 256;
-constexpr int SEQ_NT = TZ_TC;    // tokens per slice
-constexpr int SEQ_STAGES = 4;    // operand ring depth (48 KB per stage with both planes)
 
-template <int EPI, bool TRACE>
-__global__ void __launch_bounds__(SEQ_THREADS, 1) gemm_tc_seq_kernel(const __grid_constant__ CUtensorMap tmw,
-                                                                    const __grid_constant__ CUtensorMap tmx_hi,
-                                                                    const __grid_constant__ CUtensorMap tmx_lo,
-                                                                    GemmArgs a, int stages) {
-  constexpr int nt = SEQ_NT;
+template <int EPI, bool TRACE, int NT>
+__global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
+    gemm_tc_seq_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx_hi,
+                       const __grid_constant__ CUtensorMap tmx_lo, GemmArgs a, int stages) {
+  static_assert(NT == 64 || NT == 128, "token slice of 64 or 128");
+  constexpr int nt = NT;
   constexpr int two = 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -432,14 +433,14 @@ __global__ void __launch_bounds__(SEQ_THREADS, 1) gemm_tc_seq_kernel(const __gri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the slices of one weight tile are adjacent in launch order, so the tile
   // comes from HBM once and from L2 for the other slices
-  const int nz = cdiv_i(a.T, TZ_TC);
+  const int nz = cdiv_i(a.T, NT);
   const int tile = blockIdx.x / nz, z = blockIdx.x % nz;
   const int n0 = tile * NTILE;
-  const int t0 = z * TZ_TC;
-  const int tn = min(TZ_TC, a.T - t0);
+  const int t0 = z * NT;
+  const int tn = min(NT, a.T - t0);
   const int S = a.splits, kpc = a.kchunk / 64, nkb_all = cdiv_i(a.K, 64);
   const int nmma = (two ? 2 : 1) * nt;
-  const uint32_t bufcols = two ? 256u : 128u;
+  constexpr uint32_t bufcols = 2 * NT;
 
   if (tid == 0) {
     if (TRACE) trace_mark(a.trace, 0);
@@ -570,14 +571,24 @@ __global__ void __launch_bounds__(SEQ_THREADS, 1) gemm_tc_seq_kernel(const __gri
   if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 
-template <int EPI, bool TRACE>
+template <int EPI, bool TRACE, int NT>
 static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
   CUtensorMap tmw, tmh, tml;
   if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE)) return false;
-  const int nt = SEQ_NT;
+  const int nt = NT;
   if (!a.x_lo || !tmap_2d(&tmh, a.x, a.T, a.K, nt) || !tmap_2d(&tml, a.x_lo, a.T, a.K, nt)) return false;
   const int stage_bytes = A_BYTES + 2 * nt * 128;
-  const int stages = SEQ_STAGES;
+  // 64-token slices: three stages keep two CTAs per SM; a grid that fits one
+  // CTA per SM (narrow matrices) takes a six-stage ring instead, since each
+  // CTA's k loop is bound by the stages it has in flight
+  static int n_sm = 0;
+  if (!n_sm) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n_sm = 1;
+  }
+  const int ctas = cdiv_i(a.N, NTILE) * cdiv_i(a.T, NT);
+  const int stages = NT == 128 ? 4 : (ctas <= n_sm ? 6 : 3);
   const size_t ring = (size_t)stages * stage_bytes;
   const size_t epi = ((size_t)nt * YLD + EPI_SCRATCH_FLOATS) * 4;  // aliases the ring after the mainloop
   if (epi > ring) return false;
@@ -585,14 +596,14 @@ static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (smem > 227 * 1024) return false;
   static size_t configured = 0;
   if (smem > configured) {
-    if (cudaFuncSetAttribute(gemm_tc_seq_kernel<EPI, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_tc_seq_kernel<EPI, TRACE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return false;
     configured = smem;
   }
-  prefer_shared(reinterpret_cast<const void*>(gemm_tc_seq_kernel<EPI, TRACE>));
+  prefer_shared(reinterpret_cast<const void*>(gemm_tc_seq_kernel<EPI, TRACE, NT>));
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(cdiv_i(a.N, NTILE) * cdiv_i(a.T, TZ_TC));
+  cfg.gridDim = dim3(cdiv_i(a.N, NTILE) * cdiv_i(a.T, NT));
   cfg.blockDim = dim3(SEQ_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -601,7 +612,7 @@ static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_seq_kernel<EPI, TRACE>, tmw, tmh, tml, a, stages) == cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_seq_kernel<EPI, TRACE, NT>, tmw, tmh, tml, a, stages) == cudaSuccess;
 }
 
 template <int EPI, bool TRACE>
@@ -686,10 +697,22 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
 // Launches of more than two 128-token slices of hi + lo planes run the K
 // chunks in one CTA (gemm_tc_seq_kernel); the others split them over a
 // cluster.  Both add the chunk sums in chunk order.
+static int seq_slice_tokens() {
+  static int nt = 0;
+  if (!nt) {
+    const char* v = getenv("GOCR_SEQ_NT");
+    nt = v && atoi(v) == 128 ? 128 : 64;
+  }
+  return nt;
+}
+
 template <int EPI>
 static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
-  if (cdiv_i(a.T, TZ_TC) > 2 && a.x_lo)
-    return a.trace ? launch_gemm_tc_seq<EPI, true>(a, s, pdl) : launch_gemm_tc_seq<EPI, false>(a, s, pdl);
+  if (cdiv_i(a.T, TZ_TC) > 2 && a.x_lo) {
+    if (seq_slice_tokens() == 128)
+      return a.trace ? launch_gemm_tc_seq<EPI, true, 128>(a, s, pdl) : launch_gemm_tc_seq<EPI, false, 128>(a, s, pdl);
+    return a.trace ? launch_gemm_tc_seq<EPI, true, 64>(a, s, pdl) : launch_gemm_tc_seq<EPI, false, 64>(a, s, pdl);
+  }
   return a.trace ? launch_gemm_tc_kt<EPI, true>(a, s, pdl) : launch_gemm_tc_kt<EPI, false>(a, s, pdl);
 }
 
