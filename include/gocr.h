@@ -165,8 +165,8 @@ int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0);
  *     GOCR_FORWARD_PERSISTENT  one persistent kernel per forward, one CTA per
  *       SM: every layer's GEMMs, attention and epilogues and the LM head, with
  *       device counters in place of kernel boundaries.  Only for handles
- *       created with the mma.sync attention (GOCR_ATTN_MMA_SYNC, the default),
- *       whose tile code it shares; GOCR_ESTATE otherwise.
+ *       with the mma.sync attention (GOCR_ATTN_MMA_SYNC), whose tile code it
+ *       shares; GOCR_ESTATE otherwise.
  *   Both give bit-identical results (the same reductions in the same order).
  *   Prefill, fp32 models and larger forwards always run one kernel per
  *   operation.  The environment variable GOCR_FORWARD=persistent selects
@@ -174,10 +174,13 @@ int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0);
  *   captured graphs.
  *   GOCR_OPT_ATTENTION (get only) the tensor-core attention kernels of a bf16
  *                     handle, fixed at create time:
- *     GOCR_ATTN_MMA_SYNC (default)  64-row tiles on mma.sync;
+ *     GOCR_ATTN_MMA_SYNC  64-row tiles on mma.sync;
  *     GOCR_ATTN_TCGEN05  128-row tiles with both contractions on tcgen05 and
- *       their accumulators in tensor memory (GOCR_ATTN=tc in the environment
- *       at create time; gocr_op_attention reads it per call).
+ *       their accumulators in tensor memory.
+ *   A handle takes TCGEN05 when its key-chunk ranks average at least four
+ *   32-key chunks at full capacity (batched handles), MMA_SYNC otherwise;
+ *   GOCR_ATTN=tc or GOCR_ATTN=mma in the environment at create time
+ *   overrides (gocr_op_attention reads it per call; MMA_SYNC by default).
  *   The two round differently; each is bit-consistent across its own
  *   forwards.
  * GOCR_EINVAL for an unknown option or value. */

@@ -707,10 +707,14 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->attn_ranks = attention_ranks(h->cap, c.max_requests);
     const char* ar = getenv("GOCR_ATTN_RANKS");
     if (ar && atoi(ar) >= 1 && atoi(ar) <= 64) h->attn_ranks = atoi(ar) < (h->cap + 31) / 32 ? atoi(ar) : (h->cap + 31) / 32;
-    // GOCR_ATTN=tc: the tcgen05 attention (measured slower at the decode
-    // shapes, where a tile holds one or two chunks; see attn_tc.cuh)
+    // attention kernels: tcgen05 when a rank averages at least four chunks at
+    // full capacity (its heavier tile setup is then amortised: measured 2.8%
+    // faster on the 16-request batch), mma.sync otherwise (faster at one or
+    // two chunks per rank); GOCR_ATTN=tc | mma overrides
+    h->attn_kind = (h->cap + 31) / 32 >= 4 * h->attn_ranks ? ATTN_TCGEN05 : ATTN_MMA_SYNC;
     const char* ak = getenv("GOCR_ATTN");
-    h->attn_kind = ak && strcmp(ak, "tc") == 0 ? ATTN_TCGEN05 : ATTN_MMA_SYNC;
+    if (ak && strcmp(ak, "tc") == 0) h->attn_kind = ATTN_TCGEN05;
+    if (ak && strcmp(ak, "mma") == 0) h->attn_kind = ATTN_MMA_SYNC;
   }
   CKC(cudaStreamCreateWithFlags(&h->hs, cudaStreamNonBlocking));
   CKC(cudaEventCreate(&h->ev0));
@@ -1046,7 +1050,7 @@ int gocr_set_option(gocr_handle* h, int option, int value) {
   if (option != GOCR_OPT_FORWARD) return fail(h, GOCR_EINVAL, "unknown option %d", option);
   if (value != GOCR_FORWARD_PERSISTENT && value != GOCR_FORWARD_OPS) return fail(h, GOCR_EINVAL, "bad value %d", value);
   if (value == GOCR_FORWARD_PERSISTENT && h->attn_kind != ATTN_MMA_SYNC)
-    return fail(h, GOCR_ESTATE, "the persistent forward needs the mma.sync attention (the default)");
+    return fail(h, GOCR_ESTATE, "the persistent forward needs the mma.sync attention (GOCR_ATTN=mma at create)");
   const bool en = value == GOCR_FORWARD_PERSISTENT && h->mk_ctr != nullptr;
   if (en == h->mk_enabled) return GOCR_OK;
   CK(cudaStreamSynchronize(h->hs));

@@ -118,11 +118,11 @@ struct alignas(16) AttnArgs {
   int* err;                   // device error word (bounded waits), or NULL
   unsigned long long* trace;  // launch timeline record, as GemmArgs::trace
 };
-// Tensor-core attention kernels of bf16 models.  ATTN_MMA_SYNC (default):
-// 64-row tiles on mma.sync, the tile code the persistent forward shares.
-// ATTN_TCGEN05: 128-row tiles, both contractions on tcgen05 with accumulators
-// in tensor memory.  The two give different bits; a handle fixes one at
-// creation.
+// Tensor-core attention kernels of bf16 models.  ATTN_MMA_SYNC: 64-row tiles
+// on mma.sync, the tile code the persistent forward shares.  ATTN_TCGEN05:
+// 128-row tiles, both contractions on tcgen05 with accumulators in tensor
+// memory.  The two give different bits; a handle fixes one at creation (by
+// the chunks per rank at full capacity, or GOCR_ATTN).
 enum { ATTN_TCGEN05 = 0, ATTN_MMA_SYNC = 1 };
 // Key-chunk ranks of the tensor-core attention: rank r reads chunks r, r + R, ...
 // R = attention_ranks(cap, n_req): ATTN_RANKS for one request, fewer (at

@@ -155,6 +155,25 @@ def test_persistent_forward_needs_the_mma_sync_attention(small, monkeypatch):
         dec.close()
 
 
+def test_attention_kernel_follows_chunks_per_rank(small, monkeypatch):
+    """A handle whose ranks average at least four chunks at full capacity
+    (here 16 requests: 8 ranks over 64 chunks) takes the tcgen05 attention;
+    GOCR_ATTN=mma overrides, and one request at the same capacity (48 ranks)
+    keeps mma.sync."""
+    g, synth, cfg = small["g"], small["synth"], small["cfg"]
+    W = synth.make_weights(cfg, seed=31)
+    monkeypatch.delenv("GOCR_ATTN", raising=False)
+    for env, n_req, want in ((None, 16, g.ATTN_TCGEN05), ("mma", 16, g.ATTN_MMA_SYNC), (None, 1, g.ATTN_MMA_SYNC)):
+        if env:
+            monkeypatch.setenv("GOCR_ATTN", env)
+        dec = g.Decoder(cfg, W, max_ctx=2048, max_block=8, max_requests=n_req)
+        monkeypatch.delenv("GOCR_ATTN", raising=False)
+        try:
+            assert dec.attention_kind() == want, (env, n_req)
+        finally:
+            dec.close()
+
+
 def test_option_round_trip(small):
     dec, g = small["dec"], small["g"]
     dec.set_forward_path(g.FORWARD_PERSISTENT)
