@@ -13,7 +13,9 @@
 // softmax with one thread per query row (a row's 32 scores come from its own
 // TMEM lane, so no cross-thread reduction); all eight warps fold each chunk's
 // PV into the running output, O = O * corr + PV (warp w: rows 32 (w % 4) ..
-// +31, output columns (w / 4) d/2 .. +d/2).
+// +31, output columns (w / 4) d/2 .. +d/2).  Two score buffers let the next
+// chunk's QK^T run under this chunk's softmax; K/V are fetched two chunks
+// ahead.
 //
 // A chunk with no key visible to a row leaves that row's (max, sum, output)
 // bit for bit unchanged (corr = 1, P = 0), so a row's result does not depend
@@ -30,7 +32,7 @@ namespace attn_tc {
 constexpr int QR = 128;       // query rows per tile (MMA M)
 constexpr int AC = attn::AC;  // keys per chunk: the rank split is shared with every other path
 constexpr int THREADS = 256;
-constexpr uint32_t S_COL = 0;     // TMEM columns of the score accumulator [QR x AC]
+constexpr uint32_t S_COL = 0;     // TMEM columns of the two score accumulators [2][QR x AC]
 constexpr uint32_t PV_COL = 128;  // TMEM columns of the chunk's P V accumulator [QR x d]
 constexpr uint32_t TMEM_COLS = 256;
 
@@ -50,7 +52,7 @@ template <int D> struct Geo {
   static constexpr int OFF_V = OFF_P + P_BYTES;              // [stage][hi, lo]
   static constexpr int OFF_LIM = OFF_V + 4 * V_PLANE;        // int [QR]
   static constexpr int OFF_CORR = OFF_LIM + QR * 4;          // float [QR]
-  static constexpr int OFF_BAR = OFF_CORR + QR * 4;          // two mbarriers, the TMEM address
+  static constexpr int OFF_BAR = OFF_CORR + QR * 4;          // three mbarriers, the TMEM address
   static constexpr int SMEM = OFF_BAR + 32 + 1024;           // + slack for the 1024-byte alignment
   static constexpr int RLD = D + 4;                          // fp32 stride of a staged partial row
   static_assert(QR * RLD * 4 <= OFF_VT, "staged partial rows fit over Q and K");
@@ -122,8 +124,8 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   int* Lim = reinterpret_cast<int*>(sm + Gm::OFF_LIM);
   float* Corr = reinterpret_cast<float*>(sm + Gm::OFF_CORR);
-  uint64_t* s_full = reinterpret_cast<uint64_t*>(sm + Gm::OFF_BAR);
-  uint64_t* pv_full = s_full + 1;
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(sm + Gm::OFF_BAR);  // [2] score buffers
+  uint64_t* pv_full = s_full + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(pv_full + 1);
   __shared__ int s_maxlim;
   __shared__ int s_fail;
@@ -137,6 +139,7 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
     if (TRACE) trace_mark(a.trace, 0);
     tc::grid_dep_launch();
     tc::mbar_init(s_full, 1);
+    tc::mbar_init(s_full + 1, 1);
     tc::mbar_init(pv_full, 1);
     tc::fence_mbar_init();
     s_maxlim = -1;
@@ -210,8 +213,14 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
     if (rank == 0 && tid == 0) a.part_chunks[(size_t)slot * gridDim.x + group] = n_chunks;
     if (rank < n_chunks) {  // uniform
       const attn::KvPlanes kv = attn::kv_planes(a, req, kvh, D);
+      // a rank's chunks: c_it = rank + it * R, it = 0 .. n_it - 1; chunk c_it
+      // sits in stage it & 1 (K swizzled, V row-major), its scores in S buffer
+      // it & 1
+      const int n_it = (n_chunks - rank + R - 1) / R;
       if (!pre) load_kv<D>(sm, kv, 0, rank, maxlim, tid);
-      attn::cp_async_commit();
+      attn::cp_async_commit();  // Q (and chunk 0)
+      if (n_it > 1) load_kv<D>(sm, kv, 1, rank + R, maxlim, tid);
+      attn::cp_async_commit();  // chunk 1
       const float sl2 = a.scale * attn::LOG2E;
       const int q4 = warp & 3, h = warp >> 2;
       const int r = q4 * 32 + lane;  // this thread's tile row
@@ -227,45 +236,55 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
       const uint32_t q_hi = tc::smem_u32(sm + Gm::OFF_Q), q_lo = q_hi + Gm::Q_PLANE;
       const uint32_t vt_hi = tc::smem_u32(sm + Gm::OFF_VT), vt_lo = vt_hi + Gm::VT_PLANE;
       const uint32_t p_s = tc::smem_u32(sm + Gm::OFF_P);
-      int it = 0;
-      for (int c = rank; c < n_chunks; c += R, ++it) {
+      // S(it) = Qh Kh^T, += Qh Kl^T, += Ql Kh^T over d in 16-element steps (one thread)
+      auto issue_qk = [&](int it) {
         const int st = it & 1;
-        const bool next = c + R < n_chunks;
+        const uint32_t k_hi = tc::smem_u32(sm + Gm::OFF_K + (st * 2) * Gm::K_PLANE), k_lo = k_hi + Gm::K_PLANE;
+        const uint32_t as[3] = {q_hi, q_hi, q_lo}, bs[3] = {k_hi, k_lo, k_hi};
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t ao = (ks >> 2) * (QR * 128) + (ks & 3) * 32;
+            const uint32_t bo = (ks >> 2) * (AC * 128) + (ks & 3) * 32;
+            tc::mma_bf16(tmem + S_COL + st * AC, tc::sdesc_sw128(as[t] + ao), tc::sdesc_sw128(bs[t] + bo), idesc_s,
+                         (t > 0 || ks > 0) ? 1u : 0u);
+          }
+        tc::mma_commit(s_full + st);
+      };
+      // prologue: Q and chunk 0 in shared memory, its scores on the way
+      if (n_it > 1) attn::cp_async_wait<1>(); else attn::cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc::fence_after_sync();
+        issue_qk(0);
+      }
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it & 1, c = rank + it * R;
+        // chunk it + 1 landed; V of chunk it transposed (the last P V has completed)
         attn::cp_async_wait<0>();
-        __syncthreads();  // chunk c's K and V (and Q) landed; VT, P and the accumulators are free
         transpose_v<D>(sm, st, warp, lane);
         tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
         __syncthreads();
         if (TRACE && it == 0 && tid == 0) trace_mark(a.trace, 4);
-        if (tid == 0) {
+        // the next chunk's scores while this chunk's softmax runs
+        if (tid == 0 && it + 1 < n_it) {
           tc::fence_after_sync();
-          const uint32_t k_hi = tc::smem_u32(sm + Gm::OFF_K + (st * 2) * Gm::K_PLANE), k_lo = k_hi + Gm::K_PLANE;
-          // S = Qh Kh^T, += Qh Kl^T, += Ql Kh^T; each over d in 16-element steps
-          const uint32_t as[3] = {q_hi, q_hi, q_lo}, bs[3] = {k_hi, k_lo, k_hi};
-#pragma unroll
-          for (int t = 0; t < 3; ++t)
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t ao = (ks >> 2) * (QR * 128) + (ks & 3) * 32;
-              const uint32_t bo = (ks >> 2) * (AC * 128) + (ks & 3) * 32;
-              tc::mma_bf16(tmem + S_COL, tc::sdesc_sw128(as[t] + ao), tc::sdesc_sw128(bs[t] + bo), idesc_s,
-                           (t > 0 || ks > 0) ? 1u : 0u);
-            }
-          tc::mma_commit(s_full);
+          issue_qk(it + 1);
         }
-        if (next) load_kv<D>(sm, kv, st ^ 1, c + R, maxlim, tid);
-        attn::cp_async_commit();
         if (warp >= 4) {
           // online softmax of row r over the chunk's 32 keys
-          if (!tc::mbar_wait(s_full, it & 1)) s_fail = 1;
+          if (!tc::mbar_wait(s_full + st, (it >> 1) & 1)) s_fail = 1;
           tc::fence_after_sync();
-          float s[AC];
-          tc::tmem_ld32(lane_base + S_COL, s);
+          float sv[AC];
+          tc::tmem_ld32(lane_base + S_COL + st * AC, sv);
           float mc = -INFINITY;
 #pragma unroll
           for (int j = 0; j < AC; ++j) {
-            const float v = c * AC + j <= lim_r ? s[j] * sl2 : -INFINITY;
-            s[j] = v;
+            const float v = c * AC + j <= lim_r ? sv[j] * sl2 : -INFINITY;
+            sv[j] = v;
             mc = fmaxf(mc, v);
           }
           const float mn = fmaxf(m, mc);
@@ -274,8 +293,8 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
           uint32_t pk[AC / 2];
 #pragma unroll
           for (int j = 0; j < AC; j += 2) {
-            const float p0 = s[j] == -INFINITY ? 0.f : exp2f(s[j] - mn);
-            const float p1 = s[j + 1] == -INFINITY ? 0.f : exp2f(s[j + 1] - mn);
+            const float p0 = sv[j] == -INFINITY ? 0.f : exp2f(sv[j] - mn);
+            const float p1 = sv[j + 1] == -INFINITY ? 0.f : exp2f(sv[j + 1] - mn);
             ps += p0;
             ps += p1;
             pk[j / 2] = attn::pack_bf16(p0, p1);
@@ -291,7 +310,7 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
           tc::fence_proxy_async_smem();
         }
         tc::fence_before_sync();
-        __syncthreads();  // P and the corrections are in shared memory
+        __syncthreads();  // P and the corrections are in shared memory; S(it) and K(it) are consumed
         if (tid == 0) {
           tc::fence_after_sync();
           // PV = P Vh, += P Vl; over the chunk's keys in 16-element steps
@@ -303,6 +322,9 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
                            tc::sdesc_sw128((t ? vt_lo : vt_hi) + ks * 32), idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
           tc::mma_commit(pv_full);
         }
+        // chunk it + 2 into this chunk's stage
+        if (it + 2 < n_it) load_kv<D>(sm, kv, st, c + 2 * R, maxlim, tid);
+        attn::cp_async_commit();
         // O = O * corr + PV for this warp's rows and output columns
         if (!tc::mbar_wait(pv_full, it & 1)) s_fail = 1;
         tc::fence_after_sync();
