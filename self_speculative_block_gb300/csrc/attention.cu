@@ -13,18 +13,23 @@
 // the same position give identical bits.
 //
 // bf16 models: tensor-core kernels.  q and the KV cache are stored as bf16
-// hi + lo planes (written once by the QKV epilogue), QK^T takes
-// qh kh + qh kl + ql kh and PV takes P vh + P vl on mma.sync tiles (P in
-// bf16), accumulating in fp32.  The R CTAs of one (kv head, 64-query-row
-// group) split the chunks, rank r visiting chunks r, r + R, ... with an online
-// softmax, and write partial (max, sum, output) rows to global memory; a
-// merge kernel adds them in rank order.  R is fixed per
-// handle (attention_ranks: 48 for one request, fewer for a batch).  There is
-// no thread-block cluster: most single-request decode contexts give each rank
-// one chunk, and the CTAs need no co-scheduling.  Under programmatic dependent launch a CTA fetches its first
-// chunk before the grid-dependency wait when that chunk holds only committed
-// cache positions (below the round-start cache length, which no kernel of the
-// forward writes).  The result is written as the O projection's input planes.
+// hi + lo planes (written once by the QKV epilogue); QK^T takes qh kh + qh kl
+// + ql kh and PV takes P vh + P vl (P in bf16), accumulating in fp32.  The R
+// CTAs of one (kv head, query-row group) split the chunks, rank r visiting
+// chunks r, r + R, ... with an online softmax, and write partial (max, sum,
+// output) rows to global memory; a merge kernel adds them in rank order.  R
+// is fixed per handle (attention_ranks: 48 for one request, fewer for a
+// batch).  Two partial kernels, one per handle:
+//   attention_part_kernel: 64-row groups on mma.sync tiles (this file and
+//     attn_core.cuh), the lighter footprint that wins when a rank reads one
+//     or two chunks;
+//   attention_tc_part_kernel: 128-row groups on tcgen05 (attn_tc.cuh), for
+//     handles whose ranks average at least four chunks.
+// There is no thread-block cluster: the CTAs need no co-scheduling.  Under
+// programmatic dependent launch a CTA fetches its first chunk before the
+// grid-dependency wait when that chunk holds only committed cache positions
+// (below the round-start cache length, which no kernel of the forward
+// writes).  The result is written as the O projection's input planes.
 // fp32 models: CUDA-core kernel with one CTA sweeping every chunk.
 #include <cstdlib>
 
