@@ -422,7 +422,7 @@ template <int EPI>
 __device__ void fixup_tile(const Ctx& c, const Geo& g, int t0, int t1) {
   const MkArgs& a = *c.a;
   const EpiArgs& e = c.sGA->e;
-  const int T = a.T, N = a.N[g.gk], S = a.splits[g.gk];
+  const int T = a.T, N = a.N[g.gk], S = a.splits[g.gk], gs = a.kgroup[g.gk];
   float* Ys = reinterpret_cast<float*>(c.sC);
   float* scratch = Ys + EG * YLD;
   float* pf_rs = scratch + EPI_SCRATCH_FLOATS;  // [EG]
@@ -437,15 +437,30 @@ __device__ void fixup_tile(const Ctx& c, const Geo& g, int t0, int t1) {
     for (int x = c.grp.tid; x < cnt * (NTILE / 4); x += c.grp.n) {
       const int j = x / (NTILE / 4), c4 = (x % (NTILE / 4)) * 4;
       const float* src = a.part + ((size_t)g0 + j) * N + g.n0 + c4;
-      // acc = p0 + p1 + ... in split order; the unrolled loads go out together
-      float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
+      // chunk sums added in split order within each reduction group of gs
+      // splits, the group sums in group order; the unrolled loads go out together
+      float4 acc = __ldcg(reinterpret_cast<const float4*>(src)), gsum = acc;
 #pragma unroll 12
       for (int sp = 1; sp < S; ++sp) {
         const float4 v = __ldcg(reinterpret_cast<const float4*>(src + sp * sstride));
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+        if (sp % gs == 0) {
+          gsum = v;
+        } else {
+          gsum.x += v.x;
+          gsum.y += v.y;
+          gsum.z += v.z;
+          gsum.w += v.w;
+        }
+        if (sp % gs == gs - 1 || sp == S - 1) {
+          if (sp < gs) {
+            acc = gsum;
+          } else {
+            acc.x += gsum.x;
+            acc.y += gsum.y;
+            acc.z += gsum.z;
+            acc.w += gsum.w;
+          }
+        }
       }
       *reinterpret_cast<float4*>(Ys + (size_t)j * YLD + c4) = acc;
     }

@@ -80,6 +80,19 @@ int gemm_kchunk(int N, int K) {
 
 int gemm_splits(int N, int K) { return cdiv(K, gemm_kchunk(N, K)); }
 
+// Chunks per reduction group.  A tile's split-K sum is taken as group sums
+// (the group's chunk sums added in chunk order) added in group order.  With
+// two_groups (handles that batch requests), narrow matrices (at most 16
+// weight tiles) with four or more chunks use two groups, so that the
+// many-slice GEMM can give each group a CTA of its own; otherwise one group,
+// the plain chunk-order sum.  A handle fixes the choice, so its results
+// depend on (N, K) only.  The kernels take at most two groups.
+int gemm_kgroup(int N, int K, bool two_groups) {
+  const int S = gemm_splits(N, K);
+  if (two_groups && cdiv(N, NTILE) <= 16 && S >= 4) return cdiv(S, 2);
+  return S;
+}
+
 size_t gemm_ws_floats(int T, int N, int K) { return (size_t)gemm_splits(N, K) * T * N; }
 
 int gemm_counter_ints(int T, int N) { return cdiv(T, TZ) * cdiv(N, NTILE) + 1; }

@@ -114,7 +114,7 @@ bool encode_tmap_bf16(void* out, const void* ptr, int rows, int cols, int box_ro
 // EPI: the fused epilogue (a.epi), one instantiation per kind.  TRACE: the
 // instantiation that records the launch timeline (a.trace), launched only
 // when a record is attached, so that the other carries no trace code.
-template <int EPI, bool TRACE>
+template <int EPI, bool TRACE, bool TWO>
 __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmw,
                                                             const __grid_constant__ CUtensorMap tmx_hi,
                                                             const __grid_constant__ CUtensorMap tmx_lo,
@@ -347,7 +347,9 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     for (int g0 = ta; g0 < tb; g0 += EG) {
       const int cnt = min(EG, tb - g0);
       // thread x: token x / 32, columns 4 (x % 32) .. +3; every partial is
-      // loaded first, then they are added in rank order
+      // loaded first, then they are added in rank (chunk) order within each
+      // reduction group of kgroup ranks, and the group sums in group order
+      const int gs = TWO ? a.kgroup : S;
       for (int x = tid; x < cnt * (NTILE / 4); x += TC_THREADS) {
         const int j = x / (NTILE / 4), c4 = (x % (NTILE / 4)) * 4;
         float4 v[MAX_CLUSTER];
@@ -358,14 +360,40 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
             v[sp] = *reinterpret_cast<const float4*>(src + c4);
           }
         float4 acc = v[0];
+        if (!TWO) {
 #pragma unroll
-        for (int sp = 1; sp < MAX_CLUSTER; ++sp)
-          if (sp < S) {
-            acc.x += v[sp].x;
-            acc.y += v[sp].y;
-            acc.z += v[sp].z;
-            acc.w += v[sp].w;
-          }
+          for (int sp = 1; sp < MAX_CLUSTER; ++sp)
+            if (sp < S) {
+              acc.x += v[sp].x;
+              acc.y += v[sp].y;
+              acc.z += v[sp].z;
+              acc.w += v[sp].w;
+            }
+        } else {
+          // two groups (gemm_kgroup): ranks [0, gs) and [gs, S)
+          float4 g1 = v[0];
+#pragma unroll
+          for (int sp = 1; sp < MAX_CLUSTER; ++sp)
+            if (sp < S) {
+              if (sp < gs) {
+                acc.x += v[sp].x;
+                acc.y += v[sp].y;
+                acc.z += v[sp].z;
+                acc.w += v[sp].w;
+              } else if (sp == gs) {
+                g1 = v[sp];
+              } else {
+                g1.x += v[sp].x;
+                g1.y += v[sp].y;
+                g1.z += v[sp].z;
+                g1.w += v[sp].w;
+              }
+            }
+          acc.x += g1.x;
+          acc.y += g1.y;
+          acc.z += g1.z;
+          acc.w += g1.w;
+        }
         *reinterpret_cast<float4*>(Ys + (size_t)j * YLD + c4) = acc;
       }
       __syncthreads();
@@ -404,7 +432,12 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
 // take the clustered kernel).
 // NT = 128: one CTA per SM, four 48 KB stages.  NT = 64: two CTAs per SM,
 // three 32 KB stages, twice the work units, so that narrow matrices (few
-// weight tiles) still occupy every SM.
+// weight tiles) still occupy every SM.  A matrix with several reduction
+// groups (gemm_kgroup) gives each group a CTA of a cluster: CTA g sums its
+// group's chunks in order, then each CTA adds the group sums in group order
+// for its share of the slice's tokens (read from the peers' shared memory)
+// and runs their epilogue; the clustered kernel adds its ranks' partials in
+// the same two levels.
 constexpr int SEQ_THREADS = 256;
 
 template <int EPI, bool TRACE, int NT>
@@ -424,21 +457,32 @@ __global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
   uint64_t* accf = empty + stages;  // [2] chunk accumulator ready
   uint64_t* acce = accf + 2;        // [2] chunk accumulator drained
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acce + 2);
-  // after the mainloop: the reduced tile and the epilogue scratch over the ring
-  float* Ysum = reinterpret_cast<float*>(smem);                   // [nt][YLD]
-  float* scratch = Ysum + (size_t)nt * YLD;
   __shared__ int s_fail;
   __shared__ int s_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // reduction groups of the tile: CTA grp of a cluster of P takes chunks
+  // [grp * gs, (grp + 1) * gs)
+  const int S = a.splits, kpc = a.kchunk / 64, nkb_all = cdiv_i(a.K, 64);
+  const int gs = a.kgroup > 0 ? a.kgroup : S;
+  const int P = cdiv_i(S, gs);
+  const int unit = blockIdx.x / P, grp = blockIdx.x % P;
+  const int c_beg = grp * gs, c_end = min(S, c_beg + gs);
+  const int kb_beg = min(nkb_all, c_beg * kpc), kb_end = min(nkb_all, c_end * kpc);
+  const int nkb = kb_end - kb_beg;
+  // after the mainloop, over the ring: the group sum [nt], the reduced rows of
+  // this CTA's tokens [per] (clusters only) and the epilogue scratch
+  const int per = cdiv_i(NT, P);
+  float* Ysum = reinterpret_cast<float*>(smem);                   // [nt][YLD]
+  float* Yred = Ysum + (size_t)nt * YLD;                          // [per][YLD]
+  float* scratch = P > 1 ? Yred + (size_t)per * YLD : Yred;
   // the slices of one weight tile are adjacent in launch order, so the tile
   // comes from HBM once and from L2 for the other slices
   const int nz = cdiv_i(a.T, NT);
-  const int tile = blockIdx.x / nz, z = blockIdx.x % nz;
+  const int tile = unit / nz, z = unit % nz;
   const int n0 = tile * NTILE;
   const int t0 = z * NT;
   const int tn = min(NT, a.T - t0);
-  const int S = a.splits, kpc = a.kchunk / 64, nkb_all = cdiv_i(a.K, 64);
   const int nmma = (two ? 2 : 1) * nt;
   constexpr uint32_t bufcols = 2 * NT;
 
@@ -466,41 +510,44 @@ __global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
 
+  const int nc = c_end - c_beg;  // this CTA's chunks
   if (tid == 0) {
-    // TMA producer: every k block of the tile, chunk after chunk; the first
-    // stages' weight tiles go out before the grid dependency wait
+    // TMA producer: every k block of the CTA's chunks, chunk after chunk; the
+    // first stages' weight tiles go out before the grid dependency wait
     const uint64_t pol = tc::policy_evict_first();
-    const int pre = nkb_all < stages ? nkb_all : stages;
+    const int pre = nkb < stages ? nkb : stages;
     for (int kb = 0; kb < pre; ++kb) {
       tc::mbar_expect_tx(&full[kb], A_BYTES + b_bytes);
-      tc::tma_load_2d_hint(sA + kb * A_BYTES, &tmw, kb * 64, n0, &full[kb], pol);
+      tc::tma_load_2d_hint(sA + kb * A_BYTES, &tmw, (kb_beg + kb) * 64, n0, &full[kb], pol);
     }
-    for (int kb = pre; kb < nkb_all && kb < pre + L2_PREFETCH_BLOCKS; ++kb) tc::tma_prefetch_2d(&tmw, kb * 64, n0);
+    for (int kb = pre; kb < nkb && kb < pre + L2_PREFETCH_BLOCKS; ++kb)
+      tc::tma_prefetch_2d(&tmw, (kb_beg + kb) * 64, n0);
     tc::grid_dep_wait();
     if (TRACE) trace_mark(a.trace, 1);
-    for (int kb = 0; kb < nkb_all; ++kb) {
+    for (int kb = 0; kb < nkb; ++kb) {
       const int st = kb % stages;
       const int use = kb / stages;
+      const int kx = (kb_beg + kb) * 64;
       if (kb >= pre) {
         if (!tc::mbar_wait(&empty[st], (use - 1) & 1)) { s_fail = 1; break; }
         tc::mbar_expect_tx(&full[st], A_BYTES + b_bytes);
-        tc::tma_load_2d_hint(sA + st * A_BYTES, &tmw, kb * 64, n0, &full[st], pol);
-        if (kb + L2_PREFETCH_BLOCKS < nkb_all) tc::tma_prefetch_2d(&tmw, (kb + L2_PREFETCH_BLOCKS) * 64, n0);
+        tc::tma_load_2d_hint(sA + st * A_BYTES, &tmw, kx, n0, &full[st], pol);
+        if (kb + L2_PREFETCH_BLOCKS < nkb) tc::tma_prefetch_2d(&tmw, kx + L2_PREFETCH_BLOCKS * 64, n0);
       }
       uint8_t* b = sB + st * b_bytes;
-      tc::tma_load_2d(b, &tmx_hi, kb * 64, t0, &full[st]);
-      if (two) tc::tma_load_2d(b + nt * 128, &tmx_lo, kb * 64, t0, &full[st]);
+      tc::tma_load_2d(b, &tmx_hi, kx, t0, &full[st]);
+      if (two) tc::tma_load_2d(b + nt * 128, &tmx_lo, kx, t0, &full[st]);
     }
   } else if (tid == 32) {
-    // MMA issuer: chunk c accumulates into TMEM buffer c & 1
+    // MMA issuer: the CTA's lc-th chunk accumulates into TMEM buffer lc & 1
     const uint32_t idesc = tc::idesc_bf16(NTILE, nmma);
     int kb = 0;
-    for (int c = 0; c < S && !s_fail; ++c) {
-      const int b = c & 1;
-      if (c >= 2 && !tc::mbar_wait(&acce[b], ((c >> 1) - 1) & 1)) { s_fail = 1; break; }
+    for (int lc = 0; lc < nc && !s_fail; ++lc) {
+      const int b = lc & 1;
+      if (lc >= 2 && !tc::mbar_wait(&acce[b], ((lc >> 1) - 1) & 1)) { s_fail = 1; break; }
       tc::fence_after_sync();
       const uint32_t d = tmem + (uint32_t)b * bufcols;
-      const int kend = min(nkb_all, (c + 1) * kpc);
+      const int kend = min(nkb_all, (c_beg + lc + 1) * kpc) - kb_beg;
       for (int k0 = kb; kb < kend; ++kb) {
         const int st = kb % stages;
         if (!tc::mbar_wait(&full[st], (kb / stages) & 1)) { s_fail = 1; break; }
@@ -520,7 +567,7 @@ __global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
   if (warp >= 4) {
     // drain: chunk sums (hi + lo products) added to the running sums in chunk order
     const int q = warp & 3;
-    for (int c = 0; c < S; ++c) {
+    for (int c = 0; c < nc; ++c) {
       const int b = c & 1;
       if (!tc::mbar_wait(&accf[b], (c >> 1) & 1)) {
         s_fail = 1;
@@ -553,21 +600,54 @@ __global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
     tc::tmem_dealloc(tmem, 2 * bufcols);
   }
   const bool failed = s_fail != 0;
-  if (failed) {
-    if (tid == 0) set_err(a.e.err, DERR_TIMEOUT);
-    return;
-  }
-  if (warp >= 4) {
-    const int row = (warp & 3) * 32 + lane;
+  if (failed && tid == 0) set_err(a.e.err, DERR_TIMEOUT);
+  if (P == 1) {
+    if (failed) return;
+    if (warp >= 4) {
+      const int row = (warp & 3) * 32 + lane;
 #pragma unroll
-    for (int t = 0; t < nt; ++t) Ysum[(size_t)t * YLD + row] = acc[t];
+      for (int t = 0; t < nt; ++t) Ysum[(size_t)t * YLD + row] = acc[t];
+    }
+    __syncthreads();
+    for (int g0 = 0; g0 < tn; g0 += EG) {
+      const int cnt = min(EG, tn - g0);
+      apply_epilogue_k<EPI>(a, Ysum + (size_t)g0 * YLD, YLD, tile, t0 + g0, cnt, scratch, EpiPre(), Grp::block());
+    }
+    if (EPI == EPI_ARGMAX) argmax_grid_finish(a, &s_flag);
+  } else {
+    // every CTA of the cluster passes both cluster barriers, failed or not
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    if (warp >= 4) {
+      const int row = (warp & 3) * 32 + lane;
+#pragma unroll
+      for (int t = 0; t < nt; ++t) Ysum[(size_t)t * YLD + row] = acc[t];
+    }
+    cluster.sync();  // every group sum of the slice is in its CTA's shared memory
+    // this CTA's tokens: the group sums added in group order
+    const int ta = min(tn, grp * per), tb = min(tn, ta + per);
+    for (int x = tid; x < (tb - ta) * (NTILE / 4); x += SEQ_THREADS) {
+      const int j = x / (NTILE / 4), c4 = (x % (NTILE / 4)) * 4;
+      const size_t off = (size_t)(ta + j) * YLD + c4;
+      float4 r = *reinterpret_cast<const float4*>(cluster.map_shared_rank(Ysum, 0) + off);
+      for (int g = 1; g < P; ++g) {
+        const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(Ysum, g) + off);
+        r.x += v.x;
+        r.y += v.y;
+        r.z += v.z;
+        r.w += v.w;
+      }
+      *reinterpret_cast<float4*>(Yred + (size_t)j * YLD + c4) = r;
+    }
+    __syncthreads();
+    if (!failed)
+      for (int g0 = ta; g0 < tb; g0 += EG) {
+        const int cnt = min(EG, tb - g0);
+        apply_epilogue_k<EPI>(a, Yred + (size_t)(g0 - ta) * YLD, YLD, tile, t0 + g0, cnt, scratch, EpiPre(),
+                              Grp::block());
+      }
+    cluster.sync();  // the peers have read this CTA's group sums
   }
-  __syncthreads();
-  for (int g0 = 0; g0 < tn; g0 += EG) {
-    const int cnt = min(EG, tn - g0);
-    apply_epilogue_k<EPI>(a, Ysum + (size_t)g0 * YLD, YLD, tile, t0 + g0, cnt, scratch, EpiPre(), Grp::block());
-  }
-  if (EPI == EPI_ARGMAX) argmax_grid_finish(a, &s_flag);
   if (TRACE && tid == 0) trace_mark(a.trace, 3);
 }
 
@@ -587,10 +667,14 @@ static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       n_sm = 1;
   }
-  const int ctas = cdiv_i(a.N, NTILE) * cdiv_i(a.T, NT);
+  const int ctas = cdiv_i(a.N, NTILE) * cdiv_i(a.T, NT) * cdiv_i(a.splits, a.kgroup > 0 ? a.kgroup : a.splits);
   const int stages = NT == 128 ? 4 : (ctas <= n_sm ? 6 : 3);
+  const int gsz = a.kgroup > 0 ? a.kgroup : a.splits;
+  const int P = cdiv_i(a.splits, gsz);  // reduction groups: CTAs per cluster
+  if (P > 8) return false;
   const size_t ring = (size_t)stages * stage_bytes;
-  const size_t epi = ((size_t)nt * YLD + EPI_SCRATCH_FLOATS) * 4;  // aliases the ring after the mainloop
+  // aliases the ring after the mainloop: group sum, reduced rows, scratch
+  const size_t epi = ((size_t)(nt + (P > 1 ? cdiv_i(nt, P) : 0)) * YLD + EPI_SCRATCH_FLOATS) * 4;
   if (epi > ring) return false;
   const size_t smem = 1024 + ring + (2 * stages + 4) * 8 + 16;
   if (smem > 227 * 1024) return false;
@@ -603,19 +687,30 @@ static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
   }
   prefer_shared(reinterpret_cast<const void*>(gemm_tc_seq_kernel<EPI, TRACE, NT>));
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(cdiv_i(a.N, NTILE) * cdiv_i(a.T, NT));
+  cfg.gridDim = dim3(cdiv_i(a.N, NTILE) * cdiv_i(a.T, NT) * P);
   cfg.blockDim = dim3(SEQ_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (P > 1) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = P;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = at;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, gemm_tc_seq_kernel<EPI, TRACE, NT>, tmw, tmh, tml, a, stages) == cudaSuccess;
 }
 
-template <int EPI, bool TRACE>
+template <int EPI, bool TRACE, bool TWO>
 static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (a.splits < 1 || a.splits > MAX_CLUSTER) return false;
   CUtensorMap tmw, tmh, tml;
@@ -662,15 +757,15 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (smem > 227 * 1024) return false;
   static size_t configured = 0;
   if (smem > configured) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<EPI, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(gemm_tc_kernel<EPI, TRACE, TWO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return false;
     if (configured == 0 &&
-        cudaFuncSetAttribute(gemm_tc_kernel<EPI, TRACE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        cudaFuncSetAttribute(gemm_tc_kernel<EPI, TRACE, TWO>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return false;
     configured = smem;
   }
-  prefer_shared(reinterpret_cast<const void*>(gemm_tc_kernel<EPI, TRACE>));
+  prefer_shared(reinterpret_cast<const void*>(gemm_tc_kernel<EPI, TRACE, TWO>));
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(cdiv_i(a.N, NTILE), a.splits, cdiv_i(a.T, TZ_TC));
   cfg.blockDim = dim3(TC_THREADS);
@@ -690,7 +785,7 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, TRACE>, tmw, tmh, tml, a, nt, two, stages, ring, per, yl.ys, yl.scratch) ==
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, TRACE, TWO>, tmw, tmh, tml, a, nt, two, stages, ring, per, yl.ys, yl.scratch) ==
          cudaSuccess;
 }
 
@@ -713,7 +808,14 @@ static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
       return a.trace ? launch_gemm_tc_seq<EPI, true, 128>(a, s, pdl) : launch_gemm_tc_seq<EPI, false, 128>(a, s, pdl);
     return a.trace ? launch_gemm_tc_seq<EPI, true, 64>(a, s, pdl) : launch_gemm_tc_seq<EPI, false, 64>(a, s, pdl);
   }
-  return a.trace ? launch_gemm_tc_kt<EPI, true>(a, s, pdl) : launch_gemm_tc_kt<EPI, false>(a, s, pdl);
+  // a separate instantiation for two reduction groups, so that the common
+  // one-group kernel keeps its code (its timing under programmatic dependent
+  // launch is sensitive to register allocation)
+  if (a.kgroup > 0 && a.kgroup < a.splits) {
+    if (2 * a.kgroup < a.splits) return false;  // at most two groups
+    return a.trace ? launch_gemm_tc_kt<EPI, true, true>(a, s, pdl) : launch_gemm_tc_kt<EPI, false, true>(a, s, pdl);
+  }
+  return a.trace ? launch_gemm_tc_kt<EPI, true, false>(a, s, pdl) : launch_gemm_tc_kt<EPI, false, false>(a, s, pdl);
 }
 
 bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl) {

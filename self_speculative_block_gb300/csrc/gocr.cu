@@ -77,6 +77,7 @@ struct gocr_handle {
   int cap = 0, T_max = 0, T_dec = 0, sched_cap = 0;
   int attn_ranks = 1;  // key-chunk ranks of the tensor-core attention, fixed for the handle
   int attn_kind = ATTN_MMA_SYNC;  // tensor-core attention kernels, fixed for the handle
+  bool two_groups = false;        // split-K sums of narrow matrices in two groups (gemm_kgroup)
   long long layer_stride = 0, req_stride = 0;
 
   // KV cache [req][layer][kv head][position][head_dim]: bf16 hi/lo planes for
@@ -195,6 +196,7 @@ GemmArgs gemm_base(gocr_handle* h, const void* xh, const void* xl, int ldx, cons
   a.ldx = ldx; a.w = w; a.T = T; a.N = N; a.K = K;
   a.kchunk = gemm_kchunk(N, K);
   a.splits = gemm_splits(N, K);
+  a.kgroup = gemm_kgroup(N, K, h->two_groups);
   a.ws = h->ws;
   a.counters = h->counters;
   a.e.err = h->err;
@@ -326,6 +328,7 @@ bool mk_shape(gocr_handle* h, int kind, int n_slots, int B, MkArgs& a) {
     a.tiles[k] = a.N[k] / NTILE;
     a.splits[k] = gemm_splits(a.N[k], a.K[k]);
     a.kchunk[k] = gemm_kchunk(a.N[k], a.K[k]);
+    a.kgroup[k] = gemm_kgroup(a.N[k], a.K[k], h->two_groups);
     // split tiles need a completion counter each
     if (a.splits[k] > 16 || ((k < 4 || a.splits[k] > 1) && a.tiles[k] > mk::MAXT)) return false;
   }
@@ -705,6 +708,9 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->l2_prefetch = !(lp && lp[0] == '0');
     // GOCR_ATTN_RANKS=<n>: rank count for this handle instead of the rule
     h->attn_ranks = attention_ranks(h->cap, c.max_requests);
+    // handles that batch requests run their batched GEMMs on the many-slice
+    // kernel, which splits narrow matrices over two CTAs per slice
+    h->two_groups = c.max_requests > 1;
     const char* ar = getenv("GOCR_ATTN_RANKS");
     if (ar && atoi(ar) >= 1 && atoi(ar) <= 64) h->attn_ranks = atoi(ar) < (h->cap + 31) / 32 ? atoi(ar) : (h->cap + 31) / 32;
     // attention kernels: tcgen05 when a rank averages at least four chunks at
@@ -1151,7 +1157,7 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
   if (workspace_bytes < gocr_op_linear_workspace(T, N, K)) return fail(h, GOCR_ECAPACITY, "workspace too small");
   GemmArgs a{};
   a.x = x; a.x_lo = nullptr; a.ldx = K; a.w = w; a.T = T; a.N = N; a.K = K;
-  a.kchunk = gemm_kchunk(N, K); a.splits = gemm_splits(N, K);
+  a.kchunk = gemm_kchunk(N, K); a.splits = gemm_splits(N, K); a.kgroup = gemm_kgroup(N, K, false);
   a.counters = (int*)workspace;
   size_t ctr = ((size_t)gemm_counter_ints(T, N) * 4 + 255) & ~(size_t)255;
   a.ws = (float*)((char*)workspace + ctr);
@@ -1173,7 +1179,7 @@ int gocr_op_linear_planes(const void* x_hi, const void* x_lo, const void* w, flo
   if (workspace_bytes < gocr_op_linear_workspace(T, N, K)) return fail(h, GOCR_ECAPACITY, "workspace too small");
   GemmArgs a{};
   a.x = x_hi; a.x_lo = x_lo; a.ldx = K; a.w = w; a.T = T; a.N = N; a.K = K;
-  a.kchunk = gemm_kchunk(N, K); a.splits = gemm_splits(N, K);
+  a.kchunk = gemm_kchunk(N, K); a.splits = gemm_splits(N, K); a.kgroup = gemm_kgroup(N, K, false);
   a.counters = (int*)workspace;
   size_t ctr = ((size_t)gemm_counter_ints(T, N) * 4 + 255) & ~(size_t)255;
   a.ws = (float*)((char*)workspace + ctr);

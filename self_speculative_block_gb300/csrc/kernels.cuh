@@ -66,6 +66,7 @@ struct alignas(16) GemmArgs {  // 16-byte aligned: tables of them are copied by 
   const void* w;                 // [N, K] dtype
   int T, N, K;
   int splits, kchunk;            // K = splits chunks of kchunk (last may be short)
+  int kgroup;                    // tcgen05 kernels: chunks per reduction group (gemm_kgroup)
   float* ws;                     // CUDA-core path: [splits][T][N] fp32 partials
   int* counters;                 // CUDA-core path: tile counters, zero between launches
   int epi;
@@ -87,6 +88,7 @@ struct alignas(16) GemmArgs {  // 16-byte aligned: tables of them are copied by 
 bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s, bool pdl);
 bool launch_gemm_tc(const GemmArgs& a, cudaStream_t s, bool pdl);
 int gemm_splits(int N, int K);
+int gemm_kgroup(int N, int K, bool two_groups);
 // 128-byte-swizzled TMA descriptor (CUtensorMap, 128 bytes at `out`) of a
 // row-major bf16 matrix [rows, cols] with boxes of 64 columns x box_rows.
 bool encode_tmap_bf16(void* out, const void* ptr, int rows, int cols, int box_rows);
@@ -170,7 +172,7 @@ struct MkArgs {
   int ranks;               // attention key-chunk ranks (ATTN_RANKS); partial rows in AttnArgs::part
   int G;                   // CTAs (one per SM)
   int ws_stages, as_stages, pf_blocks;
-  int N[5], K[5], tiles[5], splits[5], kchunk[5];  // per GEMM kind: QKV, O, GU, DN, LM
+  int N[5], K[5], tiles[5], splits[5], kchunk[5], kgroup[5];  // per GEMM kind: QKV, O, GU, DN, LM
   int n_items[5];          // per phase kind: QKV, ATT, O, GU, DN
   int prefix[5];           // items of the earlier phase kinds of a layer
   int per_layer;           // items of one layer

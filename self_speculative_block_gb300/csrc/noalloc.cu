@@ -77,6 +77,7 @@ int gocr_op_linear_static(int dtype, const void* x, const void* w, float* y, int
   a.x = x; a.x_lo = nullptr; a.ldx = K; a.w = w; a.T = T; a.N = N; a.K = K;
   a.kchunk = gemm_kchunk(N, K);
   a.splits = gemm_splits(N, K);
+  a.kgroup = gemm_kgroup(N, K, false);
   a.counters = (int*)scratch;
   a.ws = (float*)((char*)scratch + ctr);
   a.epi = EPI_STORE;
