@@ -242,8 +242,8 @@ int gocr_op_linear(int dtype, const void* x, const void* w, float* y, int T, int
  * epilogues write (each K chunk takes the hi and the lo products as separate
  * tensor-core accumulators, adds them, and the chunk sums are added in chunk
  * order).  Up to two 128-row token slices split each tile's K chunks over a
- * thread-block cluster; more slices run them in one CTA.  Either way a row's
- * bits depend on neither T nor the kernel that ran it.  K % 8 == 0; x_hi, x_lo,
+ * thread-block cluster; more rows run them in one CTA per 64-token slice.
+ * Either way a row's bits depend on neither T nor the kernel that ran it.  K % 8 == 0; x_hi, x_lo,
  * w 16-byte aligned.  workspace: as gocr_op_linear.
  * flags: 0, or GOCR_OP_OVERLAP: launched as the decoder launches it, with
  * programmatic dependent launch, so that it may start while the stream's

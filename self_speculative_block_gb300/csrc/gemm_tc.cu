@@ -646,6 +646,7 @@ __global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
         apply_epilogue_k<EPI>(a, Yred + (size_t)(g0 - ta) * YLD, YLD, tile, t0 + g0, cnt, scratch, EpiPre(),
                               Grp::block());
       }
+    if (EPI == EPI_ARGMAX) argmax_grid_finish(a, &s_flag);  // every CTA of the grid counts itself
     cluster.sync();  // the peers have read this CTA's group sums
   }
   if (TRACE && tid == 0) trace_mark(a.trace, 3);

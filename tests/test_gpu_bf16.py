@@ -129,7 +129,11 @@ def test_small_batched_ragged_equals_single_ar(small):
         dec.prefill(r, prefixes[r])
         out, _ = dec.decode(r, g.MODE_AR, 0, news[r])
         refs.append(list(out))
-    for mode, B in ((g.MODE_SELFSPEC, 8), (g.MODE_AR, 0), (g.MODE_SELFSPEC, 32)):
+    # B = 64: 4 x 65 = 260 rows, past two 128-token slices, so the batched
+    # forwards run the many-slice GEMM; on this batching handle the O and down
+    # projections (4 weight tiles, 8 chunks) sum in two groups on two-CTA
+    # clusters, which must reproduce the clustered kernel's bits for AR
+    for mode, B in ((g.MODE_SELFSPEC, 8), (g.MODE_AR, 0), (g.MODE_SELFSPEC, 32), (g.MODE_SELFSPEC, 64)):
         for r in range(4):
             dec.prefill(r, prefixes[r])
         outs, sts = dec.decode_batch([0, 1, 2, 3], mode, B, news)
