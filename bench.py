@@ -313,11 +313,7 @@ def main():
     torch.cuda.synchronize()
     total_s = sum(dev_ms) / 1e3
     if world > 1:
-        t = torch.tensor([total_s, tokens], dtype=torch.float64, device=dev)
-        tt = [torch.zeros_like(t) for _ in range(world)]
-        torch.distributed.all_gather(tt, t)
-        total_s = max(float(x[0]) for x in tt)
-        tokens = sum(int(x[1]) for x in tt)
+        total_s, tokens = replica_totals(total_s, tokens, dev)
     value = tokens / total_s
     ms_per_step = sum(dev_ms) / len(dev_ms)
     round_us = 1e3 * sum(dev_ms) / rounds
@@ -386,6 +382,18 @@ def main():
 
 GEMM_SOURCES = ("gemm_tc.cu", "gemm.cu", "epilogue.cuh", "tc.cuh", "kernels.cuh", "common.cuh")
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "gemm_tc_decode_sweep.md")
+
+
+def replica_totals(total_s: float, tokens: int, device) -> tuple[float, int]:
+    """N replicas (one process per GPU, an initialised process group): the
+    slowest rank's timed seconds and the tokens all ranks committed, so that
+    the whole-job rate is tokens / seconds."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(total_s), float(tokens)], dtype=torch.float64, device=device)
+    tt = [torch.zeros_like(t) for _ in range(dist.get_world_size())]
+    dist.all_gather(tt, t)
+    return max(float(x[0]) for x in tt), sum(int(round(float(x[1]))) for x in tt)
 
 
 def gemm_sources_digest() -> str:
