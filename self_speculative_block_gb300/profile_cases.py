@@ -2,14 +2,15 @@
 
     python -m self_speculative_block_gb300.profile_cases draft [B]
         0.5B-class bf16 decoder, 1024-row synthetic prefill, then two draft
-        forwards (B = 32 unless given: B + 1 rows).  The prefill (1024 rows,
-        eight token slices) launches gemm_tc_seq_kernel 65 times and
-        attention_part_kernel / attention_merge_kernel 16 times each; the
-        draft forwards launch gemm_tc_kernel (65 per forward), so the first
-        draft forward's QKV / O / gate-up / down GEMMs are launches 0..3 of
-        `-k regex:gemm_tc_kernel` (65..68 of `-k regex:gemm_tc`, which also
-        matches the prefill's kernel) and its first attention is
-        attention_part and attention_merge launch 16.
+        forwards (B = 32 unless given: B + 1 rows).  The prefill (1024 rows)
+        launches gemm_tc_seq_kernel 64 times, gemm_tc_kernel once (the LM
+        head of its last row) and attention_part_kernel /
+        attention_merge_kernel 16 times each; the draft forwards launch
+        gemm_tc_kernel (65 per forward), so the first draft forward's QKV /
+        O / gate-up / down GEMMs are launches 1..4 of `-k regex:gemm_tc_kernel`
+        (65..68 of `-k regex:gemm_tc`, which also matches the prefill's
+        kernel) and its first attention is attention_part and
+        attention_merge launch 16.
     python -m self_speculative_block_gb300.profile_cases sweep
         The split-K GEMM over one forward's 65 weight matrices (16 x packed
         QKV, O, packed gate/up, down, then the LM head) at the decode launch
@@ -20,7 +21,7 @@
 
     python -m self_speculative_block_gb300.profile_cases batch
         The 16-request page batch: 16 ragged prefills (each one plan, one
-        embed, 65 gemm_tc, 16 attention_part, 16 attention_merge and one
+        embed, 65 GEMM, 16 attention partial, 16 attention merge and one
         finishing launch: 100 launches), then one batched self-speculative
         round (B = 32, 16 x 33 = 528 rows per forward).  Run it with
         GOCR_HOST_LOOP=1 so that the round's kernels are profilable: they
