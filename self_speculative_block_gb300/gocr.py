@@ -303,7 +303,7 @@ class Decoder:
         return v.value
 
     def attention_kind(self) -> int:
-        """ATTN_TCGEN05 or ATTN_MMA_SYNC (GOCR_ATTN=mma at create time)."""
+        """ATTN_TCGEN05 or ATTN_MMA_SYNC, fixed at create time (by chunks per rank, or GOCR_ATTN=tc | mma)."""
         return self._option(OPT_ATTENTION)
 
     def _option(self, opt: int) -> int:
