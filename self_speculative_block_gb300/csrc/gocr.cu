@@ -708,6 +708,18 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->l2_prefetch = !(lp && lp[0] == '0');
     // GOCR_ATTN_RANKS=<n>: rank count for this handle instead of the rule
     h->attn_ranks = attention_ranks(h->cap, c.max_requests);
+    if (c.max_requests <= 1) {
+      // one request: no more ranks than fill two CTAs per SM in one wave for
+      // the (kv head, 64-row group) tiles of a B + 1 = 33-row forward (or of
+      // the handle's largest forward when that is smaller); measured on the
+      // table region (2,992 positions, B = 32): 38 ranks 1,641 us per round
+      // against 48 ranks 1,785 us
+      const int fw_rows = (c.max_block < 32 ? c.max_block : 32) + 1;
+      const int fw_groups = c.n_kv_heads * ((fw_rows * (c.n_q_heads / c.n_kv_heads) + 63) / 64);
+      const int wave = 2 * 152 / (fw_groups > 0 ? fw_groups : 1);
+      const int cap_r = wave < ATTN_RANKS_MIN ? ATTN_RANKS_MIN : wave;
+      if (h->attn_ranks > cap_r) h->attn_ranks = cap_r;
+    }
     // handles that batch requests run their batched GEMMs on the many-slice
     // kernel, which splits narrow matrices over two CTAs per slice
     h->two_groups = c.max_requests > 1;
