@@ -6,6 +6,9 @@ calls it and shares no code with it (the seeded input generators, which hold
 none of the method's arithmetic, are the only thing both sides consume).
 
 Plain NumPy in float64 by default, with explicit dense mask matrices.
+model.py: the decoder and the masks; decode.py: AR greedy and the
+self-speculative round; diffusion.py: direct block-diffusion decoding and
+rounds with refined drafts.
 
 Parity notes: the pages print no worked numeric example (their B = 4 example
 and their Figure 4 are images missing from the text), so no function here is
@@ -20,6 +23,9 @@ from .model import (Model, argmax_lowest, attention, causal_mask, draft_mask, fo
 from .decode import (RoundLog, State, accept_length, ar_decode, ar_forward, ar_step,
                      draft_forward, forced_override, prefill, round_stats, selfspec_decode,
                      selfspec_round, tokens_per_forward, verify_forward)
+from .diffusion import (BlockLog, RefinedRoundLog, StepLog, choose_slots, confidence,
+                        diffusion_block, diffusion_decode, diffusion_stats, refined_decode,
+                        refined_round, refined_stats, window_forward)
 
 __all__ = [
     "Model", "argmax_lowest", "attention", "causal_mask", "draft_mask", "forward",
@@ -27,4 +33,7 @@ __all__ = [
     "verify_mask", "RoundLog", "State", "accept_length", "ar_decode", "ar_forward", "ar_step",
     "draft_forward", "forced_override", "prefill", "round_stats", "selfspec_decode",
     "selfspec_round", "tokens_per_forward", "verify_forward",
+    "BlockLog", "RefinedRoundLog", "StepLog", "choose_slots", "confidence", "diffusion_block",
+    "diffusion_decode", "diffusion_stats", "refined_decode", "refined_round", "refined_stats",
+    "window_forward",
 ]
