@@ -148,6 +148,15 @@ int gocr_set_draft_override(gocr_handle* h, int req, const int32_t* ref_tokens, 
 int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens, int n,
                        float* logits_out);
 
+/* gocr_debug_forward over n_req prefilled request slots in one batched
+ * forward, as gocr_decode_batch runs its rounds: request i's window is rows
+ * [i n, (i + 1) n) with tokens[i n .. (i + 1) n) (same per-kind meaning as
+ * above, each at its own request's cache length), and logits_out (host, or
+ * NULL) receives [n_req n, vocab] fp32 in that row order.  The requests are
+ * distinct; GOCR_ECAPACITY when a window does not fit its cache. */
+int gocr_debug_forward_batch(gocr_handle* h, int n_req, const int32_t* reqs, int kind, const int32_t* tokens,
+                             int n, float* logits_out);
+
 /* Copy n cached positions from pos0 of layer `layer` to host buffers
  * k_out/v_out, each [n, n_kv_heads, head_dim] fp32 (keys are stored rotated;
  * bf16 models keep the cache as bf16 hi + lo planes, returned as their sum). */
@@ -156,24 +165,9 @@ int gocr_read_kv(gocr_handle* h, int req, int layer, int pos0, int n, float* k_o
 /* Current cache length (position of the boundary token) and boundary token. */
 int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0);
 
-/* Handle options.
- *   GOCR_OPT_FORWARD  which kernels run a decode forward (draft, verify, AR
- *                     step, debug forward) of a bf16 model with head_dim 128
- *                     and at most 128 rows per forward:
- *     GOCR_FORWARD_OPS (default)  one kernel per operation, chained by
- *       programmatic dependent launch;
- *     GOCR_FORWARD_PERSISTENT  one persistent kernel per forward, one CTA per
- *       SM: every layer's GEMMs, attention and epilogues and the LM head, with
- *       device counters in place of kernel boundaries.  Only for handles
- *       with the mma.sync attention (GOCR_ATTN_MMA_SYNC), whose tile code it
- *       shares; GOCR_ESTATE otherwise.
- *   Both give bit-identical results (the same reductions in the same order).
- *   Prefill, fp32 models and larger forwards always run one kernel per
- *   operation.  The environment variable GOCR_FORWARD=persistent selects
- *   PERSISTENT at create time.  Changing the option drops the handle's
- *   captured graphs.
- *   GOCR_OPT_ATTENTION (get only) the tensor-core attention kernels of a bf16
- *                     handle, fixed at create time:
+/* Read-only handle properties.
+ *   GOCR_OPT_ATTENTION  the tensor-core attention kernels of a bf16 handle,
+ *                     fixed at create time:
  *     GOCR_ATTN_MMA_SYNC  64-row tiles on mma.sync;
  *     GOCR_ATTN_TCGEN05  128-row tiles with both contractions on tcgen05 and
  *       their accumulators in tensor memory.
@@ -183,42 +177,23 @@ int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0);
  *   overrides (gocr_op_attention reads it per call; MMA_SYNC by default).
  *   The two round differently; each is bit-consistent across its own
  *   forwards.
- * GOCR_EINVAL for an unknown option or value. */
-/*   GOCR_OPT_PERSISTENT_FORWARDS  (get only) forwards the persistent kernel
- *                     completed in the last decode or debug-forward call of
- *                     the handle, read from the device (0 when none ran). */
-/*   GOCR_OPT_TRACE_RECORDS (get only) event records per writer of the
- *                     persistent forward's trace (0 = tracing off; the
- *                     environment variable GOCR_MK_TRACE=<records> at create
- *                     time turns it on).
- *   GOCR_OPT_GRID_CTAS (get only) CTAs of the persistent forward (SM count). */
-enum { GOCR_OPT_FORWARD = 1, GOCR_OPT_PERSISTENT_FORWARDS = 2, GOCR_OPT_TRACE_RECORDS = 3,
-       GOCR_OPT_GRID_CTAS = 4, GOCR_OPT_ATTENTION = 5 };
-enum { GOCR_FORWARD_PERSISTENT = 0, GOCR_FORWARD_OPS = 1 };
+ *   GOCR_OPT_ATTN_RANKS  key-chunk ranks of the handle's attention (the
+ *                     split of a row's keys, fixed at create time).
+ * GOCR_EINVAL for an unknown option. */
+enum { GOCR_OPT_ATTENTION = 5, GOCR_OPT_ATTN_RANKS = 6 };
 enum { GOCR_ATTN_TCGEN05 = 0, GOCR_ATTN_MMA_SYNC = 1 };
-int gocr_set_option(gocr_handle* h, int option, int value);
 int gocr_get_option(const gocr_handle* h, int option, int* value);
 
-/* Timelines of the last debug forward (profiling aids; GOCR_ESTATE when the
+/* Timeline of the last debug forward (a profiling aid; GOCR_ESTATE when the
  * trace is off).  out: host, at least n_words words.
- *   GOCR_TRACE_PERSISTENT  events of the persistent forward (on when the
- *     environment variable GOCR_MK_TRACE=<records> is set at create time):
- *     n_words >= CTAs * 2 * records * 2, laid out [CTA][writer][record][2];
- *     writer 0 is the activation producer, writer 1 the compute group; a
- *     record is (globaltimer ns, phase << 8 | event), zero past the last
- *     record.  Phases: layer l has QKV, attention, O, gate/up, down at
- *     5 l + 0..4, the LM head is 5 L.  Events: 0 start, 1 input ready,
- *     2 accumulator ready, 3 partial tile written, 4 tile finished,
- *     5 attention inputs ready, 6 attention partial rows written,
- *     7 attention rows merged, 8 end.
- *   GOCR_TRACE_KERNELS  one record per launch of a debug forward run with
- *     one kernel per operation (on with GOCR_OP_TRACE=1): n_words >=
+ *   GOCR_TRACE_KERNELS  one record per launch of a debug forward (on with
+ *     GOCR_OP_TRACE=1 in the environment at create time): n_words >=
  *     8 * (5 * n_layers + 1), laid out [launch][8] in forward order (per
  *     layer QKV, attention, O, gate/up, down; then the LM head); a record is
  *     (first CTA start, first and last release from the dependency wait,
  *     last CTA end, last mainloop end, last split-K exchange end, 0, 0),
  *     globaltimer ns (the last two marks for GEMMs only). */
-enum { GOCR_TRACE_PERSISTENT = 0, GOCR_TRACE_KERNELS = 1 };
+enum { GOCR_TRACE_KERNELS = 1 };
 int gocr_read_trace(gocr_handle* h, int which, uint64_t* out, size_t n_words);
 
 /* Last error message of the handle (or of the library when h is NULL). */
@@ -288,7 +263,11 @@ int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void*
  *     GOCR_STATIC_SCRATCH_BYTES (message in gocr_last_error(NULL)).
  *   - The first call on a device looks up the array's device address with
  *     that device current and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  Under lazy module loading (the CUDA default) that
+ *     first call is also where the driver reserves the array on the device,
+ *     and it fails with GOCR_ECUDA if the device has no room for it; from
+ *     the second call on, nothing is reserved.
+ *   - `stream` must belong to the current device (GOCR_EINVAL otherwise).
  *   - All calls on a device share the array and it keeps the last call's
  *     contents: calls that overlap on the GPU (other streams, other threads)
  *     race; order them on one stream. */

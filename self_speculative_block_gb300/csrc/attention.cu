@@ -280,14 +280,8 @@ static bool launch_attn_tc_t(const AttnArgs& a, int n_slots, int max_rows, cudaS
   using Gm = attn_tc::Geo<D>;
   const int G = a.Hq / a.Hkv;
   const int n_rg = (max_rows * G + attn_tc::QR - 1) / attn_tc::QR;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(attention_tc_part_kernel<D, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Gm::SMEM) != cudaSuccess)
-      return false;
-    prefer_shared(reinterpret_cast<const void*>(attention_tc_part_kernel<D, TRACE>));
-    configured = true;
-  }
+  if (!kernel_smem_at_least(reinterpret_cast<const void*>(attention_tc_part_kernel<D, TRACE>), Gm::SMEM))
+    return false;
   const int R = a.ranks > 0 ? a.ranks : attention_ranks(a.cap, 1);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.Hkv * n_rg, R, n_slots);
@@ -307,14 +301,9 @@ template <int D, bool TRACE>
 static bool launch_attn_mma_t(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
   const int G = a.Hq / a.Hkv;
   const int n_rg = (max_rows * G + attn::QR - 1) / attn::QR;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(attention_part_kernel<D, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attn::Geo<D>::TILE_SMEM) != cudaSuccess)
-      return false;
-    prefer_shared(reinterpret_cast<const void*>(attention_part_kernel<D, TRACE>));
-    configured = true;
-  }
+  if (!kernel_smem_at_least(reinterpret_cast<const void*>(attention_part_kernel<D, TRACE>),
+                            attn::Geo<D>::TILE_SMEM))
+    return false;
   cudaLaunchConfig_t cfg{};
   const int R = a.ranks > 0 ? a.ranks : attention_ranks(a.cap, 1);
   cfg.gridDim = dim3(a.Hkv * n_rg, R, n_slots);
@@ -344,13 +333,7 @@ static bool launch_attn_simt(const AttnArgs& a, int n_slots, int max_rows, cudaS
   const int G = a.Hq / a.Hkv;
   dim3 grid((max_rows * G + ROWS - 1) / ROWS, a.Hkv, n_slots);
   const size_t smem = sizeof(float) * (2 * ROWS * (D + 1) + 2 * CH * D);
-  static bool init = false;
-  if (!init) {
-    if (cudaFuncSetAttribute(attention_simt_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return false;
-    init = true;
-  }
+  if (!kernel_smem_at_least(reinterpret_cast<const void*>(attention_simt_kernel<D>), smem)) return false;
   return launch_k(attention_simt_kernel<D>, grid, dim3(ROWS), smem, s, pdl, a) == cudaSuccess;
 }
 

@@ -2,10 +2,8 @@
 // over a fixed subset of key chunks, and the fixed-order merge of the
 // partial results of the R tiles ("ranks") that share those query rows.
 //
-// The per-operation attention (a partial kernel, one CTA per tile, then a
-// merge kernel) and the persistent decode kernel (tiles and merges as work
-// items) both run these functions, so a row's attention output has the same
-// bits whichever kernel computes it.
+// The attention partial kernel runs one tile per CTA; the merge adds the
+// ranks' partial rows in rank order.
 //
 // Layout of the work: keys sit in chunks of AC = 32 at absolute positions;
 // rank r of the R ranks visits chunks r, r + R, ...  In a tile,

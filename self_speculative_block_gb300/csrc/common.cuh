@@ -34,6 +34,10 @@ enum DevErr : int {
 
 constexpr int MAX_REQ = 64;       // request slots per handle (host check)
 constexpr int NTILE = 128;        // GEMM rows of W per CTA tile
+// SMs of a GB300.  Work splits that change results (GEMM split-K counts,
+// attention ranks) are sized against this constant rather than the device's
+// SM count, so that a result's bits are the same on every device.
+constexpr int SM_COUNT = 152;
 constexpr int SWIGLU_GROUP = 64;  // gate/up interleave granularity (rows)
 
 // Per-request decode state, resident on the device for the whole decode.

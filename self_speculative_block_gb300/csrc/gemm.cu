@@ -18,7 +18,6 @@ namespace {
 constexpr int KC = 32;       // K elements staged per step
 constexpr int TZ = 64;       // tokens per CTA (grid z slices)
 constexpr int THREADS = 256;
-constexpr int SM_COUNT = 152;  // fixed so the split rule is the same on every device
 constexpr int MAX_SPLITS = 12;  // split-K partials are reduced inside one cluster (non-portable size)
 constexpr int YS_LD = NTILE + 1;
 
@@ -199,12 +198,7 @@ bool launch_gemm(int dtype, const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (dtype == 1) return launch_gemm_tc(a, s, pdl);
   dim3 grid(cdiv(a.N, NTILE), a.splits, cdiv(a.T, TZ));
   size_t smem = sizeof(float) * (NTILE * (KC + 1) + TZ * KC + TZ * YS_LD + EPI_SCRATCH_FLOATS);
-  static bool init = false;
-  if (!init) {
-    if (cudaFuncSetAttribute(gemm_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return false;
-    init = true;
-  }
+  if (!kernel_smem_at_least(reinterpret_cast<const void*>(gemm_simt_kernel), smem)) return false;
   return launch_k(gemm_simt_kernel, grid, dim3(THREADS), smem, s, pdl, a) == cudaSuccess;
 }
 

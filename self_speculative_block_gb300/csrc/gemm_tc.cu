@@ -679,14 +679,7 @@ static bool launch_gemm_tc_seq(const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (epi > ring) return false;
   const size_t smem = 1024 + ring + (2 * stages + 4) * 8 + 16;
   if (smem > 227 * 1024) return false;
-  static size_t configured = 0;
-  if (smem > configured) {
-    if (cudaFuncSetAttribute(gemm_tc_seq_kernel<EPI, TRACE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return false;
-    configured = smem;
-  }
-  prefer_shared(reinterpret_cast<const void*>(gemm_tc_seq_kernel<EPI, TRACE, NT>));
+  if (!kernel_smem_at_least(reinterpret_cast<const void*>(gemm_tc_seq_kernel<EPI, TRACE, NT>), smem)) return false;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(cdiv_i(a.N, NTILE) * cdiv_i(a.T, NT) * P);
   cfg.blockDim = dim3(SEQ_THREADS);
@@ -756,17 +749,7 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   const size_t smem = smem_of(stages).first;
   const YLayout yl = gemm_y_layout(nt, a.splits, per, compact);
   if (smem > 227 * 1024) return false;
-  static size_t configured = 0;
-  if (smem > configured) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<EPI, TRACE, TWO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return false;
-    if (configured == 0 &&
-        cudaFuncSetAttribute(gemm_tc_kernel<EPI, TRACE, TWO>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return false;
-    configured = smem;
-  }
-  prefer_shared(reinterpret_cast<const void*>(gemm_tc_kernel<EPI, TRACE, TWO>));
+  if (!kernel_smem_at_least(reinterpret_cast<const void*>(gemm_tc_kernel<EPI, TRACE, TWO>), smem, true)) return false;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(cdiv_i(a.N, NTILE), a.splits, cdiv_i(a.T, TZ_TC));
   cfg.blockDim = dim3(TC_THREADS);

@@ -32,15 +32,6 @@ struct GraphEntry {
   bool host_loop;  // body only, no device-side while node
 };
 
-// Argument table of the persistent forward for one forward shape.
-struct MkEntry {
-  int kind, n_slots, B;
-  const int* am_out;
-  const float* logits;
-  const int* slot_tab;
-  MkArgs args;
-};
-
 // Every kernel argument of one decoder forward: per layer the QKV, O,
 // gate/up and down GEMMs, then the LM head; per layer the attention.
 struct FwdArgs {
@@ -126,21 +117,9 @@ struct gocr_handle {
   int* pidx = nullptr;
   void* prefix_stage = nullptr;
 
-  // persistent decode forward (bf16 models): counters, split-K partials,
-  // attention partial rows, and per-forward-shape argument tables
-  bool mk_enabled = false;
-  unsigned* mk_ctr = nullptr;
-  size_t mk_ctr_bytes = 0;
-  float* mk_part = nullptr;
-  int mk_T_max = 0;
-  int mk_G = 0;
-  int mk_pf = 16;
-  unsigned long long* mk_trace = nullptr;
-  int mk_trace_cap = 0;
   // per-launch timeline of debug forwards run with one kernel per operation
   unsigned long long* op_trace = nullptr;
   bool op_trace_next = false;
-  std::vector<MkEntry> mk_tables;
 
   bool prefilled[MAX_REQ] = {};
   std::vector<GraphEntry> graphs;
@@ -300,128 +279,8 @@ void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_o
     }
 }
 
-// Whether the persistent kernel runs this forward, and its launch arguments
-// (without the device tables).
-bool mk_shape(gocr_handle* h, int kind, int n_slots, int B, MkArgs& a) {
-  const gocr_config& c = h->cfg;
-  if (!h->mk_enabled || h->dtype != GOCR_DTYPE_BF16 || kind == PLAN_PREFILL) return false;
-  const int T = n_rows_of(kind, n_slots, B, 0);
-  if (T < 1 || T > h->mk_T_max || T % n_slots) return false;
-  if (!forward_mk_fits(c.head_dim)) return false;
-  a = MkArgs{};
-  a.L = c.n_layers;
-  a.T = T;
-  a.nt = (T + 15) / 16 * 16;
-  a.n_slots = n_slots;
-  a.rows_per_slot = T / n_slots;
-  const int G = c.n_q_heads / c.n_kv_heads;
-  a.n_rg = (a.rows_per_slot * G + 63) / 64;
-  a.Hkv = c.n_kv_heads;
-  a.ranks = h->attn_ranks;
-  a.G = h->mk_G;
-  const int NK[5][2] = {{h->qkv_n, c.hidden}, {c.hidden, h->q_dim}, {h->gu_n, c.hidden}, {c.hidden, c.ffn},
-                        {c.vocab, c.hidden}};
-  for (int k = 0; k < 5; ++k) {
-    a.N[k] = NK[k][0];
-    a.K[k] = NK[k][1];
-    if (a.N[k] % NTILE || a.K[k] % 64) return false;
-    a.tiles[k] = a.N[k] / NTILE;
-    a.splits[k] = gemm_splits(a.N[k], a.K[k]);
-    a.kchunk[k] = gemm_kchunk(a.N[k], a.K[k]);
-    a.kgroup[k] = gemm_kgroup(a.N[k], a.K[k], h->two_groups);
-    // split tiles need a completion counter each
-    if (a.splits[k] > 16 || ((k < 4 || a.splits[k] > 1) && a.tiles[k] > mk::MAXT)) return false;
-  }
-  a.n_items[0] = a.tiles[0] * a.splits[0];
-  a.n_items[1] = n_slots * a.Hkv * a.n_rg * a.ranks;
-  a.n_items[2] = a.tiles[1] * a.splits[1];
-  a.n_items[3] = a.tiles[2] * a.splits[2];
-  a.n_items[4] = a.tiles[3] * a.splits[3];
-  if (a.n_items[1] / a.ranks > mk::MAXT) return false;
-  int acc = 0;
-  for (int k = 0; k < 5; ++k) {
-    a.prefix[k] = acc;
-    acc += a.n_items[k];
-  }
-  a.per_layer = acc;
-  // ring depths: as many weight stages as fit next to the activation stages
-  const int ast = 2 * a.nt * 128;
-  // (2 KB of the 227 KB per CTA stay for the kernel's static shared memory)
-  const size_t cap = 227 * 1024 - 2048;
-  int ws = 0;
-  for (a.as_stages = a.nt <= 64 ? 6 : 3; a.as_stages >= 2; --a.as_stages) {
-    const size_t fixed = forward_mk_smem(a.nt, 0, a.as_stages);
-    ws = fixed < cap ? (int)((cap - fixed) / (NTILE * 64 * 2 + 16)) : 0;
-    if (ws >= 4) break;
-  }
-  if (ws < 2) return false;
-  if (ws > 12) ws = 12;
-  a.ws_stages = ws;
-  (void)ast;
-  a.pf_blocks = h->mk_pf;
-  a.trace = h->mk_trace;
-  a.trace_cap = h->mk_trace_cap;
-  a.ctr = h->mk_ctr;
-  a.part = h->mk_part;
-  a.err = h->err;
-  return forward_mk_smem(a.nt, a.ws_stages, a.as_stages) <= cap;
-}
-
-MkEntry* mk_find(gocr_handle* h, int kind, int n_slots, int B, const int* am_out, const float* logits,
-                 const int* slot_tab) {
-  for (auto& e : h->mk_tables)
-    if (e.kind == kind && e.n_slots == n_slots && e.B == B && e.am_out == am_out && e.logits == logits &&
-        e.slot_tab == slot_tab)
-      return &e;
-  return nullptr;
-}
-
-// Builds (once) the device tables of the persistent forward for this shape.
-// Not during stream capture: it allocates and copies synchronously.
-int mk_prepare(gocr_handle* h, int kind, int n_slots, int B, int* am_out, float* logits, const int* slot_tab) {
-  MkArgs a;
-  if (!mk_shape(h, kind, n_slots, B, a)) return GOCR_OK;
-  if (mk_find(h, kind, n_slots, B, am_out, logits, slot_tab)) return GOCR_OK;
-  FwdArgs f;
-  forward_args(h, kind, n_slots, B, 0, am_out, logits, slot_tab, f);
-  const int L = h->cfg.n_layers;
-  const size_t n_maps = 4 * (size_t)L + 1 + 6;
-  const size_t off_g = 0;
-  const size_t off_a = (off_g + f.g.size() * sizeof(GemmArgs) + 255) & ~(size_t)255;
-  const size_t off_m = (off_a + f.at.size() * sizeof(AttnArgs) + 255) & ~(size_t)255;
-  const size_t bytes = off_m + n_maps * 128;
-  std::vector<unsigned char> blob(bytes, 0);
-  memcpy(blob.data() + off_g, f.g.data(), f.g.size() * sizeof(GemmArgs));
-  memcpy(blob.data() + off_a, f.at.data(), f.at.size() * sizeof(AttnArgs));
-  unsigned char* maps = blob.data() + off_m;
-  bool ok = true;
-  for (int l = 0; l <= L; ++l) {
-    for (int k = 0; k < (l < L ? 4 : 1); ++k) {
-      const GemmArgs& g = f.g[(size_t)l * 4 + k];
-      ok &= encode_tmap_bf16(maps + ((size_t)l * 4 + k) * 128, g.w, g.N, g.K, NTILE);
-    }
-  }
-  const gocr_config& c = h->cfg;
-  const void* act[6] = {h->xg_hi, h->xg_lo, h->at_hi, h->at_lo, h->hb_hi, h->hb_lo};
-  const int cols[3] = {c.hidden, h->q_dim, c.ffn};
-  for (int i = 0; i < 6; ++i)
-    ok &= encode_tmap_bf16(maps + (4 * (size_t)L + 1 + i) * 128, act[i], a.T, cols[i / 2], a.nt);
-  if (!ok) return GOCR_OK;  // no TMA descriptor: the per-operation kernels run this shape
-  void* dev = dev_alloc(h, bytes);
-  if (!dev) return fail(h, GOCR_ENOMEM, "device allocation failed");
-  CK(cudaMemcpyAsync(dev, blob.data(), bytes, cudaMemcpyHostToDevice, h->hs));
-  CK(cudaStreamSynchronize(h->hs));
-  a.gemm = reinterpret_cast<const GemmArgs*>((char*)dev + off_g);
-  a.att = reinterpret_cast<const AttnArgs*>((char*)dev + off_a);
-  a.maps = (char*)dev + off_m;
-  MkEntry e{kind, n_slots, B, am_out, logits, slot_tab, a};
-  h->mk_tables.push_back(e);
-  return GOCR_OK;
-}
-
 // Enqueue one decoder forward over the rows the plan kernel has laid out:
-// the embedding rows, then either the persistent forward (decode shapes of
-// bf16 models whose tables mk_prepare built) or one kernel per operation.
+// the embedding rows, then one kernel per operation.
 bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out,
                      float* logits, const int* slot_tab) {
   const gocr_config& c = h->cfg;
@@ -431,9 +290,6 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
   bool ok = true;
   launch_embed(h->dtype, h->embed, h->mask, h->prefix_stage, h->resid, h->gattn[0], h->xg_hi, h->xg_lo,
                h->ssq, h->rows, T, H, c.vocab, h->err, h->hs, pdl);
-  if (h->mk_enabled)
-    if (const MkEntry* e = mk_find(h, kind, n_slots, B, am_out, logits, slot_tab))
-      return launch_forward_mk(e->args, c.head_dim, h->hs, pdl);
   FwdArgs f;
   forward_args(h, kind, n_slots, B, P, am_out, logits, slot_tab, f);
   if (h->op_trace_next) {
@@ -596,18 +452,8 @@ int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const in
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
   launch_begin_decode(h->st, h->slot_req, n, h->max_new_dev, bound + 2, c.eos_id, h->hs);
   CK(cudaGetLastError());
-  int rc = GOCR_OK;
-  if (mode == GOCR_MODE_AR) {
-    rc = mk_prepare(h, PLAN_AR, n, 0, h->abuf, nullptr, h->slot_req);
-  } else {
-    rc = mk_prepare(h, PLAN_DRAFT, n, B, h->dbuf, nullptr, h->slot_req);
-    if (!rc) rc = mk_prepare(h, PLAN_VERIFY, n, B, h->vbuf, nullptr, h->slot_req);
-  }
-  if (rc) return rc;
-  if (h->mk_ctr) CK(cudaMemsetAsync(h->mk_ctr, 0, h->mk_ctr_bytes, h->hs));
-  if (h->mk_trace) CK(cudaMemsetAsync(h->mk_trace, 0, (size_t)h->mk_G * 2 * h->mk_trace_cap * 16, h->hs));
   cudaGraphExec_t exec;
-  rc = get_graph(h, mode, B, n, &exec);
+  int rc = get_graph(h, mode, B, n, &exec);
   if (rc) return rc;
   CK(cudaEventRecord(h->ev0, h->hs));
   if (!h->host_loop) {
@@ -706,25 +552,11 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->host_loop = hl && hl[0] == '1';
     const char* lp = getenv("GOCR_L2_PREFETCH");
     h->l2_prefetch = !(lp && lp[0] == '0');
-    // GOCR_ATTN_RANKS=<n>: rank count for this handle instead of the rule
+    // key-chunk ranks by the rule; GOCR_ATTN_RANKS=<n> replaces the rule's count
     h->attn_ranks = attention_ranks(h->cap, c.max_requests);
-    if (c.max_requests <= 1) {
-      // one request: no more ranks than fill two CTAs per SM in one wave for
-      // the (kv head, 64-row group) tiles of a B + 1 = 33-row forward (or of
-      // the handle's largest forward when that is smaller); measured on the
-      // table region (2,992 positions, B = 32): 38 ranks 1,641 us per round
-      // against 48 ranks 1,785 us
-      const int fw_rows = (c.max_block < 32 ? c.max_block : 32) + 1;
-      const int fw_groups = c.n_kv_heads * ((fw_rows * (c.n_q_heads / c.n_kv_heads) + 63) / 64);
-      const int wave = 2 * 152 / (fw_groups > 0 ? fw_groups : 1);
-      const int cap_r = wave < ATTN_RANKS_MIN ? ATTN_RANKS_MIN : wave;
-      if (h->attn_ranks > cap_r) h->attn_ranks = cap_r;
-    }
     // handles that batch requests run their batched GEMMs on the many-slice
     // kernel, which splits narrow matrices over two CTAs per slice
     h->two_groups = c.max_requests > 1;
-    const char* ar = getenv("GOCR_ATTN_RANKS");
-    if (ar && atoi(ar) >= 1 && atoi(ar) <= 64) h->attn_ranks = atoi(ar) < (h->cap + 31) / 32 ? atoi(ar) : (h->cap + 31) / 32;
     // attention kernels: tcgen05 when a rank averages at least four chunks at
     // full capacity (its heavier tile setup is then amortised: measured 2.8%
     // faster on the 16-request batch), mma.sync otherwise (faster at one or
@@ -733,6 +565,21 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     const char* ak = getenv("GOCR_ATTN");
     if (ak && strcmp(ak, "tc") == 0) h->attn_kind = ATTN_TCGEN05;
     if (ak && strcmp(ak, "mma") == 0) h->attn_kind = ATTN_MMA_SYNC;
+    if (c.max_requests <= 1 && h->attn_kind == ATTN_MMA_SYNC) {
+      // one request on the mma.sync kernel (64-row tiles, two CTAs per SM):
+      // no more ranks than fill two CTAs per SM in one wave for the (kv head,
+      // 64-row group) tiles of a B + 1 = 33-row forward (or of the handle's
+      // largest forward when that is smaller); measured on the table region
+      // (2,992 positions, B = 32): 38 ranks 1,641 us per round against 48
+      // ranks 1,785 us
+      const int fw_rows = (c.max_block < 32 ? c.max_block : 32) + 1;
+      const int fw_groups = c.n_kv_heads * ((fw_rows * (c.n_q_heads / c.n_kv_heads) + 63) / 64);
+      const int wave = 2 * SM_COUNT / (fw_groups > 0 ? fw_groups : 1);
+      const int cap_r = wave < ATTN_RANKS_MIN ? ATTN_RANKS_MIN : wave;
+      if (h->attn_ranks > cap_r) h->attn_ranks = cap_r;
+    }
+    const char* ar = getenv("GOCR_ATTN_RANKS");
+    if (ar && atoi(ar) >= 1 && atoi(ar) <= 64) h->attn_ranks = atoi(ar) < (h->cap + 31) / 32 ? atoi(ar) : (h->cap + 31) / 32;
   }
   CKC(cudaStreamCreateWithFlags(&h->hs, cudaStreamNonBlocking));
   CKC(cudaEventCreate(&h->ev0));
@@ -836,32 +683,8 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->counters = (int*)A((size_t)ctr * 4);
   }
   if (h->dtype == GOCR_DTYPE_BF16) {
-    // persistent decode forward: decode shapes of up to 128 rows
-    const char* fw = getenv("GOCR_FORWARD");
-    h->mk_enabled = fw && strcmp(fw, "persistent") == 0 && h->attn_kind == ATTN_MMA_SYNC;
-    const char* pf = getenv("GOCR_MK_PREFETCH");
-    if (pf) h->mk_pf = atoi(pf) < 0 ? 0 : atoi(pf);
-    int dev = 0;
-    CKC(cudaGetDevice(&dev));
-    CKC(cudaDeviceGetAttribute(&h->mk_G, cudaDevAttrMultiProcessorCount, dev));
-    h->mk_T_max = h->T_dec < 128 ? h->T_dec : 128;
-    const int NK[5][2] = {{h->qkv_n, H}, {H, q_dim}, {h->gu_n, H}, {H, c.ffn}, {c.vocab, H}};
-    size_t part = 0;
-    for (auto& nk : NK) {
-      const int sp = gemm_splits(nk[0], nk[1]);
-      const size_t f = sp > 1 ? (size_t)sp * nk[0] : 0;  // partial tiles of split GEMMs only
-      if (f > part) part = f;
-    }
-    h->mk_part = (float*)A(part * h->mk_T_max * 4);
-    h->mk_ctr_bytes = mk::ctr_words(c.n_layers) * 4;
-    h->mk_ctr = (unsigned*)A(h->mk_ctr_bytes);
     const char* ot = getenv("GOCR_OP_TRACE");
     if (ot && ot[0] == '1') h->op_trace = (unsigned long long*)A((size_t)TRACE_WORDS * (5 * c.n_layers + 1) * 8);
-    const char* tr = getenv("GOCR_MK_TRACE");
-    if (tr && atoi(tr) > 0) {
-      h->mk_trace_cap = atoi(tr) > 4096 ? 4096 : atoi(tr);
-      h->mk_trace = (unsigned long long*)A((size_t)h->mk_G * 2 * h->mk_trace_cap * 16);
-    }
   }
   if (!ok) {
     int r = fail(h, GOCR_ENOMEM, "device allocation failed");
@@ -946,10 +769,14 @@ int gocr_set_draft_override(gocr_handle* h, int req, const int32_t* ref_tokens, 
 
 int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens, int n,
                        float* logits_out) {
-  int r = check_req(h, req);
-  if (r) return r;
-  if (!h->prefilled[req]) return fail(h, GOCR_ESTATE, "request %d has no prefill", req);
-  if (!tokens) return fail(h, GOCR_EINVAL, "null tokens");
+  return gocr_debug_forward_batch(h, 1, &req, kind, tokens, n, logits_out);
+}
+
+int gocr_debug_forward_batch(gocr_handle* h, int n_req, const int32_t* reqs, int kind, const int32_t* tokens,
+                             int n, float* logits_out) {
+  if (!h) return fail(nullptr, GOCR_EINVAL, "null handle");
+  if (!reqs || !tokens) return fail(h, GOCR_EINVAL, "null argument");
+  if (n_req < 1 || n_req > h->cfg.max_requests) return fail(h, GOCR_EINVAL, "bad request count %d", n_req);
   int pk, B = 0;
   if (kind == GOCR_FWD_AR) {
     if (n != 1) return fail(h, GOCR_EINVAL, "AR forward takes one token");
@@ -961,17 +788,22 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
   } else {
     return fail(h, GOCR_EINVAL, "bad forward kind %d", kind);
   }
-  for (int i = 0; i < n; ++i)
+  for (int i = 0; i < n * n_req; ++i)
     if (tokens[i] < 0 || tokens[i] >= h->cfg.vocab) return fail(h, GOCR_EINVAL, "token out of range");
-  ReqState s;
-  if ((r = read_state(h, req, &s))) return r;
-  if (s.cache_len + n + 1 > h->cap) return fail(h, GOCR_ECAPACITY, "window exceeds capacity");
-  CK(cudaMemcpyAsync(h->dbg_toks, tokens, sizeof(int) * n, cudaMemcpyHostToDevice, h->hs));
-  CK(cudaMemcpyAsync(h->slot_one, &req, sizeof(int), cudaMemcpyHostToDevice, h->hs));
+  int r = GOCR_OK;
+  for (int i = 0; i < n_req; ++i) {
+    if ((r = check_req(h, reqs[i]))) return r;
+    for (int j = 0; j < i; ++j)
+      if (reqs[j] == reqs[i]) return fail(h, GOCR_EINVAL, "request %d listed twice", reqs[i]);
+    if (!h->prefilled[reqs[i]]) return fail(h, GOCR_ESTATE, "request %d has no prefill", reqs[i]);
+    ReqState s;
+    if ((r = read_state(h, reqs[i], &s))) return r;
+    if (s.cache_len + n + 1 > h->cap) return fail(h, GOCR_ECAPACITY, "window exceeds capacity");
+  }
+  const int n_slots = n_req;
+  CK(cudaMemcpyAsync(h->dbg_toks, tokens, sizeof(int) * n * n_req, cudaMemcpyHostToDevice, h->hs));
+  CK(cudaMemcpyAsync(h->slot_one, reqs, sizeof(int) * n_req, cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
-  if ((r = mk_prepare(h, pk, 1, B, h->am, h->logits, h->slot_one))) return r;
-  if (h->mk_ctr) CK(cudaMemsetAsync(h->mk_ctr, 0, h->mk_ctr_bytes, h->hs));
-  if (h->mk_trace) CK(cudaMemsetAsync(h->mk_trace, 0, (size_t)h->mk_G * 2 * h->mk_trace_cap * 16, h->hs));
   if (h->op_trace) {
     std::vector<unsigned long long> init((size_t)TRACE_WORDS * (5 * h->cfg.n_layers + 1));
     for (size_t i = 0; i < init.size(); ++i) init[i] = (i % TRACE_WORDS) < 2 ? ~0ull : 0ull;
@@ -984,8 +816,8 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
   const bool as_graph = dg && dg[0] == '1';
   cudaGraph_t graph = nullptr;
   if (as_graph) CK(cudaStreamBeginCapture(h->hs, cudaStreamCaptureModeThreadLocal));
-  launch_plan(pk, h->rows, h->st, h->slot_one, 1, B, 0, nullptr, h->dbg_toks, h->cap, h->hs, false);
-  const bool enq = enqueue_forward(h, pk, 1, B, 0, h->am, h->logits, h->slot_one);
+  launch_plan(pk, h->rows, h->st, h->slot_one, n_slots, B, 0, nullptr, h->dbg_toks, h->cap, h->hs, false);
+  const bool enq = enqueue_forward(h, pk, n_slots, B, 0, h->am, h->logits, h->slot_one);
   h->op_trace_next = false;
   if (as_graph) {
     const cudaError_t ce = cudaStreamEndCapture(h->hs, &graph);
@@ -1005,7 +837,8 @@ int gocr_debug_forward(gocr_handle* h, int req, int kind, const int32_t* tokens,
   if (!enq) return fail(h, GOCR_ECUDA, "kernel launch configuration rejected");
   CK(cudaGetLastError());
   if (logits_out)
-    CK(cudaMemcpyAsync(logits_out, h->logits, sizeof(float) * n * h->cfg.vocab, cudaMemcpyDeviceToHost, h->hs));
+    CK(cudaMemcpyAsync(logits_out, h->logits, sizeof(float) * n * n_req * h->cfg.vocab, cudaMemcpyDeviceToHost,
+                       h->hs));
   int e = 0;
   CK(cudaMemcpyAsync(&e, h->err, sizeof(int), cudaMemcpyDeviceToHost, h->hs));
   CK(cudaStreamSynchronize(h->hs));
@@ -1063,50 +896,14 @@ int gocr_get_state(gocr_handle* h, int req, int32_t* cache_len, int32_t* x0) {
   return GOCR_OK;
 }
 
-int gocr_set_option(gocr_handle* h, int option, int value) {
-  if (!h) return fail(nullptr, GOCR_EINVAL, "null handle");
-  if (option != GOCR_OPT_FORWARD) return fail(h, GOCR_EINVAL, "unknown option %d", option);
-  if (value != GOCR_FORWARD_PERSISTENT && value != GOCR_FORWARD_OPS) return fail(h, GOCR_EINVAL, "bad value %d", value);
-  if (value == GOCR_FORWARD_PERSISTENT && h->attn_kind != ATTN_MMA_SYNC)
-    return fail(h, GOCR_ESTATE, "the persistent forward needs the mma.sync attention (GOCR_ATTN=mma at create)");
-  const bool en = value == GOCR_FORWARD_PERSISTENT && h->mk_ctr != nullptr;
-  if (en == h->mk_enabled) return GOCR_OK;
-  CK(cudaStreamSynchronize(h->hs));
-  for (auto& g : h->graphs) {
-    if (g.exec) cudaGraphExecDestroy(g.exec);
-    if (g.graph) cudaGraphDestroy(g.graph);
-  }
-  h->graphs.clear();
-  h->mk_enabled = en;
-  return GOCR_OK;
-}
-
 int gocr_get_option(const gocr_handle* h, int option, int* value) {
   if (!h || !value) return fail(nullptr, GOCR_EINVAL, "null argument");
-  if (option == GOCR_OPT_FORWARD) {
-    *value = h->mk_enabled ? GOCR_FORWARD_PERSISTENT : GOCR_FORWARD_OPS;
-    return GOCR_OK;
-  }
-  if (option == GOCR_OPT_PERSISTENT_FORWARDS) {
-    unsigned e = 0;
-    if (h->mk_ctr) {
-      if (cudaStreamSynchronize(h->hs) != cudaSuccess ||
-          cudaMemcpy(&e, h->mk_ctr + mk::CTR_EPOCH, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess)
-        return GOCR_ECUDA;
-    }
-    *value = (int)e;
-    return GOCR_OK;
-  }
-  if (option == GOCR_OPT_TRACE_RECORDS) {
-    *value = h->mk_trace ? h->mk_trace_cap : 0;
-    return GOCR_OK;
-  }
-  if (option == GOCR_OPT_GRID_CTAS) {
-    *value = h->mk_G;
-    return GOCR_OK;
-  }
   if (option == GOCR_OPT_ATTENTION) {
     *value = h->attn_kind == ATTN_MMA_SYNC ? GOCR_ATTN_MMA_SYNC : GOCR_ATTN_TCGEN05;
+    return GOCR_OK;
+  }
+  if (option == GOCR_OPT_ATTN_RANKS) {
+    *value = h->attn_ranks;
     return GOCR_OK;
   }
   return GOCR_EINVAL;
@@ -1114,20 +911,12 @@ int gocr_get_option(const gocr_handle* h, int option, int* value) {
 
 int gocr_read_trace(gocr_handle* h, int which, uint64_t* out, size_t n_words) {
   if (!h || !out) return fail(h, GOCR_EINVAL, "null argument");
-  if (which == GOCR_TRACE_KERNELS) {
-    if (!h->op_trace) return fail(h, GOCR_ESTATE, "kernel tracing is off (GOCR_OP_TRACE)");
-    const size_t words = (size_t)TRACE_WORDS * (5 * h->cfg.n_layers + 1);
-    if (n_words < words) return fail(h, GOCR_ECAPACITY, "trace needs %zu words", words);
-    CK(cudaStreamSynchronize(h->hs));
-    CK(cudaMemcpy(out, h->op_trace, words * 8, cudaMemcpyDeviceToHost));
-    return GOCR_OK;
-  }
-  if (which != GOCR_TRACE_PERSISTENT) return fail(h, GOCR_EINVAL, "bad trace kind %d", which);
-  if (!h->mk_trace) return fail(h, GOCR_ESTATE, "tracing is off (GOCR_MK_TRACE)");
-  const size_t words = (size_t)h->mk_G * 2 * h->mk_trace_cap * 2;
+  if (which != GOCR_TRACE_KERNELS) return fail(h, GOCR_EINVAL, "bad trace kind %d", which);
+  if (!h->op_trace) return fail(h, GOCR_ESTATE, "kernel tracing is off (GOCR_OP_TRACE)");
+  const size_t words = (size_t)TRACE_WORDS * (5 * h->cfg.n_layers + 1);
   if (n_words < words) return fail(h, GOCR_ECAPACITY, "trace needs %zu words", words);
   CK(cudaStreamSynchronize(h->hs));
-  CK(cudaMemcpy(out, h->mk_trace, words * 8, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(out, h->op_trace, words * 8, cudaMemcpyDeviceToHost));
   return GOCR_OK;
 }
 

@@ -121,7 +121,7 @@ struct alignas(16) AttnArgs {
   unsigned long long* trace;  // launch timeline record, as GemmArgs::trace
 };
 // Tensor-core attention kernels of bf16 models.  ATTN_MMA_SYNC: 64-row tiles
-// on mma.sync, the tile code the persistent forward shares.  ATTN_TCGEN05:
+// on mma.sync.  ATTN_TCGEN05:
 // 128-row tiles, both contractions on tcgen05 with accumulators in tensor
 // memory.  The two give different bits; a handle fixes one at creation (by
 // the chunks per rank at full capacity, or GOCR_ATTN).
@@ -147,49 +147,6 @@ size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, 
 // dtype 1: tensor-core cluster kernel; 0: CUDA-core kernel.
 bool launch_attention(int dtype, const AttnArgs& a, int n_slots, int max_rows_per_slot, cudaStream_t s,
                       bool pdl);
-
-// ---------------------------------------------------------------- persistent decode forward
-// One kernel runs a whole decode forward (every layer's QKV, attention, O,
-// gate/up, down, then the LM head) on one CTA per SM, with the same
-// arithmetic as the per-operation kernels above (forward_mk.cu).
-namespace mk {
-constexpr int MAXT = 128;        // tile counters per phase
-constexpr int CTR_EPOCH = 0, CTR_DONE = 1, CTR_ABORT = 2, CTR_PHASE = 4;
-// phases: layer l has QKV, ATT, O, GU, DN at 5 l + 0..4; the LM head is 5 L
-__host__ __device__ inline int tile_ctr_base(int L) { return ((CTR_PHASE + 5 * L + 1 + 31) / 32) * 32; }
-__host__ __device__ inline size_t ctr_words(int L) { return (size_t)tile_ctr_base(L) + (size_t)(5 * L + 1) * MAXT; }
-}  // namespace mk
-
-struct MkArgs {
-  const GemmArgs* gemm;    // device [4 L + 1]: per layer QKV, O, GU, DN; then the LM head
-  const AttnArgs* att;     // device [L]
-  const void* maps;        // device CUtensorMap [4 L + 1] weights (same order), then 6 activation maps:
-                           // GEMM-input planes hi/lo, attention-output planes hi/lo, SwiGLU planes hi/lo
-  unsigned* ctr;           // device counters, mk::ctr_words(L) words, zero at the first forward
-  float* part;             // split-K partial tiles [S][T][N] of the running phase
-  int* err;
-  int L, T, nt, n_slots, rows_per_slot, n_rg, Hkv;
-  int ranks;               // attention key-chunk ranks (ATTN_RANKS); partial rows in AttnArgs::part
-  int G;                   // CTAs (one per SM)
-  int ws_stages, as_stages, pf_blocks;
-  int N[5], K[5], tiles[5], splits[5], kchunk[5], kgroup[5];  // per GEMM kind: QKV, O, GU, DN, LM
-  int n_items[5];          // per phase kind: QKV, ATT, O, GU, DN
-  int prefix[5];           // items of the earlier phase kinds of a layer
-  int per_layer;           // items of one layer
-  // optional event trace: [G][2 writers][trace_cap] records of two words
-  // (globaltimer ns, phase << 8 | event); NULL = off
-  unsigned long long* trace;
-  int trace_cap;
-};
-namespace mk {
-// trace events
-enum : int { EV_START = 0, EV_DEP = 1, EV_ACC = 2, EV_DRAINED = 3, EV_FIXED = 4, EV_ATT_READY = 5,
-             EV_ATT_PART = 6, EV_ATT_MERGED = 7, EV_END = 8 };
-}
-// Shared-memory bytes and launch check; false when the shapes do not fit.
-size_t forward_mk_smem(int nt, int ws_stages, int as_stages);
-bool forward_mk_fits(int head_dim);
-bool launch_forward_mk(const MkArgs& a, int head_dim, cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------- small kernels
 void launch_embed(int dtype, const void* embed, const void* mask_embed, const void* prefix,
@@ -246,6 +203,12 @@ void set_lib_error(const char* msg);
 // launch can share SMs with the one before it, and two 104 KB CTAs fit on an
 // SM.
 void prefer_shared(const void* fn);
+// Raises kernel fn's dynamic shared-memory limit on the current device to at
+// least `bytes` (and allows non-portable cluster sizes when asked), then
+// prefer_shared(fn).  Kept per (device, kernel) under a lock, so handles on
+// several devices or threads each configure their device.  False when the
+// runtime rejects the attribute.
+bool kernel_smem_at_least(const void* fn, size_t bytes, bool nonportable_cluster = false);
 
 // Launch helper: plain launch, or with the programmatic-dependent-launch attribute.
 template <typename... KArgs, typename... Args>

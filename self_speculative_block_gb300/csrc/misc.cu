@@ -12,6 +12,7 @@
 #include "epilogue.cuh"
 
 #include <mutex>
+#include <map>
 #include <set>
 #include <utility>
 
@@ -27,6 +28,27 @@ void prefer_shared(const void* fn) {
   if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
       cudaSuccess)
     cudaGetLastError();  // a hint only: the launch still works without it
+}
+
+bool kernel_smem_at_least(const void* fn, size_t bytes, bool nonportable_cluster) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = done.find({dev, fn});
+    if (it == done.end() || it->second < bytes) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return false;
+      if (nonportable_cluster &&
+          cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return false;
+      done[{dev, fn}] = bytes;
+    }
+  }
+  prefer_shared(fn);
+  return true;
 }
 
 // ---------------------------------------------------------------- embedding rows

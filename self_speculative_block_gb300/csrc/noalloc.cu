@@ -31,7 +31,10 @@ int set_error(int code, const char* msg) {
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// once per device (with that device current) and cached.  With lazy module
+// loading (the CUDA default) this first lookup is also where the driver loads
+// the module and reserves the array on that device, so it can fail there for
+// lack of device memory (GOCR_ECUDA).
 int scratch_on_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
@@ -66,12 +69,17 @@ int gocr_op_linear_static(int dtype, const void* x, const void* w, float* y, int
              need, STATIC_SCRATCH_BYTES);
     return set_error(GOCR_ECAPACITY, m);
   }
+  cudaStream_t s = (cudaStream_t)stream;
+  // the scratch address below is the current device's: the stream must belong to it
+  int cur = 0, sdev = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(s, &sdev) != cudaSuccess)
+    return set_error(GOCR_ECUDA, "cannot read the current or the stream's device");
+  if (cur != sdev) return set_error(GOCR_EINVAL, "the stream belongs to another device than the current one");
   void* scratch = nullptr;
   int rc = scratch_on_current_device(&scratch);
   if (rc != GOCR_OK) return rc;
   // the array keeps the previous call's contents: the tile counters must start at zero
   const size_t ctr = ((size_t)gemm_counter_ints(T, N) * 4 + 255) & ~(size_t)255;
-  cudaStream_t s = (cudaStream_t)stream;
   if (cudaMemsetAsync(scratch, 0, ctr, s) != cudaSuccess) return set_error(GOCR_ECUDA, "cudaMemsetAsync failed");
   GemmArgs a{};
   a.x = x; a.x_lo = nullptr; a.ldx = K; a.w = w; a.T = T; a.N = N; a.K = K;

@@ -24,17 +24,18 @@ ERRORS = {-1: "EINVAL", -2: "ECAPACITY", -3: "ECUDA", -4: "EDEVICE", -5: "ETIMEO
 DTYPE_F32, DTYPE_BF16 = 0, 1
 MODE_AR, MODE_SELFSPEC = 0, 1
 FWD_AR, FWD_DRAFT, FWD_VERIFY = 0, 1, 2
-OPT_FORWARD, OPT_PERSISTENT_FORWARDS, OPT_TRACE_RECORDS, OPT_GRID_CTAS, OPT_ATTENTION = 1, 2, 3, 4, 5
-FORWARD_PERSISTENT, FORWARD_OPS = 0, 1
+OPT_ATTENTION, OPT_ATTN_RANKS = 5, 6
+TRACE_KERNELS = 1
 ATTN_TCGEN05, ATTN_MMA_SYNC = 0, 1
 MAX_BLOCK = 64
 LAYER_TENSORS = 9
 
 # every symbol include/gocr.h declares
 EXPORTS = ("gocr_create", "gocr_prefill", "gocr_decode", "gocr_decode_batch",
-           "gocr_set_draft_override", "gocr_debug_forward", "gocr_read_kv", "gocr_get_state",
-           "gocr_set_option", "gocr_get_option", "gocr_read_trace", "gocr_last_error", "gocr_free", "gocr_op_linear_workspace", "gocr_op_linear", "gocr_op_linear_planes",
-           "gocr_op_attention", "gocr_op_linear_static")
+           "gocr_set_draft_override", "gocr_debug_forward", "gocr_debug_forward_batch", "gocr_read_kv", "gocr_get_state",
+           "gocr_get_option", "gocr_read_trace", "gocr_last_error", "gocr_free",
+           "gocr_op_linear_workspace", "gocr_op_linear", "gocr_op_linear_planes", "gocr_op_attention",
+           "gocr_op_linear_static")
 
 
 class GocrError(RuntimeError):
@@ -97,9 +98,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                     ctypes.POINTER(Stats)]),
         "gocr_set_draft_override": (i32, [vp, i32, P32, i32, P32, i32]),
         "gocr_debug_forward": (i32, [vp, i32, i32, P32, i32, ctypes.POINTER(ctypes.c_float)]),
+        "gocr_debug_forward_batch": (i32, [vp, i32, P32, i32, P32, i32, ctypes.POINTER(ctypes.c_float)]),
         "gocr_read_kv": (i32, [vp, i32, i32, i32, i32, vp, vp]),
         "gocr_get_state": (i32, [vp, i32, P32, P32]),
-        "gocr_set_option": (i32, [vp, i32, i32]),
         "gocr_read_trace": (i32, [vp, i32, vp, sz]),
         "gocr_get_option": (i32, [vp, i32, P32]),
         "gocr_last_error": (ctypes.c_char_p, [vp]),
@@ -279,6 +280,16 @@ class Decoder:
                self.h)
         return logits
 
+    def debug_forward_batch(self, reqs: Sequence[int], kind: int, tokens) -> np.ndarray:
+        """One batched forward over several requests; tokens [n_req, n]; logits [n_req, n, vocab]."""
+        r = _i32(reqs)
+        t = _i32(tokens)
+        n_req, n = t.shape
+        logits = np.zeros((n_req, n, self.cfg.vocab), np.float32)
+        _check(self.lib.gocr_debug_forward_batch(self.h, n_req, _p32(r), kind, _p32(t.reshape(-1)), n,
+                                                 logits.ctypes.data_as(ctypes.POINTER(ctypes.c_float))), self.h)
+        return logits
+
     def read_kv(self, req: int, layer: int, pos0: int, n: int):
         """Cached K (rotated) and V of positions pos0..pos0+n-1: two fp32 arrays [n, Hkv, d]."""
         shape = (n, self.cfg.n_kv_heads, self.cfg.head_dim)
@@ -287,44 +298,25 @@ class Decoder:
         _check(self.lib.gocr_read_kv(self.h, req, layer, pos0, n, k.ctypes.data, v.ctypes.data), self.h)
         return k, v
 
-    def set_forward_path(self, path: int) -> None:
-        """FORWARD_PERSISTENT (one kernel per decode forward) or FORWARD_OPS."""
-        _check(self.lib.gocr_set_option(self.h, OPT_FORWARD, path), self.h)
-
-    def forward_path(self) -> int:
-        v = ctypes.c_int32()
-        _check(self.lib.gocr_get_option(self.h, OPT_FORWARD, ctypes.byref(v)), self.h)
-        return v.value
-
-    def persistent_forwards(self) -> int:
-        """Forwards the persistent kernel completed in the last decode or debug forward."""
-        v = ctypes.c_int32()
-        _check(self.lib.gocr_get_option(self.h, OPT_PERSISTENT_FORWARDS, ctypes.byref(v)), self.h)
-        return v.value
-
     def attention_kind(self) -> int:
         """ATTN_TCGEN05 or ATTN_MMA_SYNC, fixed at create time (by chunks per rank, or GOCR_ATTN=tc | mma)."""
         return self._option(OPT_ATTENTION)
+
+    def attention_ranks(self) -> int:
+        """Key-chunk ranks of the handle's attention (fixed at create time)."""
+        return self._option(OPT_ATTN_RANKS)
 
     def _option(self, opt: int) -> int:
         v = ctypes.c_int32()
         _check(self.lib.gocr_get_option(self.h, opt, ctypes.byref(v)), self.h)
         return v.value
 
-    def read_trace(self) -> np.ndarray:
-        """Event trace of the last persistent forward: uint64 [CTAs, 2, records, 2]
-        (writer 0: activation producer, 1: compute group; (ns, phase << 8 | event))."""
-        G, cap = self._option(OPT_GRID_CTAS), self._option(OPT_TRACE_RECORDS)
-        out = np.zeros((G, 2, cap, 2), np.uint64)
-        _check(self.lib.gocr_read_trace(self.h, 0, out.ctypes.data, out.size), self.h)
-        return out
-
     def read_kernel_trace(self) -> np.ndarray:
         """Per-launch timeline of the last debug forward run with one kernel per
         operation: uint64 [5 L + 1, 8] (first start, first and last dependency
         release, last end, last mainloop end, last split-K exchange end; ns)."""
         out = np.zeros((5 * self.cfg.n_layers + 1, 8), np.uint64)
-        _check(self.lib.gocr_read_trace(self.h, 1, out.ctypes.data, out.size), self.h)
+        _check(self.lib.gocr_read_trace(self.h, TRACE_KERNELS, out.ctypes.data, out.size), self.h)
         return out
 
     def state(self, req: int):
@@ -391,8 +383,9 @@ def op_linear_static(x, w):
     T, K = x.shape
     N = w.shape[0]
     y = torch.empty((T, N), dtype=torch.float32, device=x.device)
-    stream = torch.cuda.current_stream(x.device).cuda_stream
-    _check(lib.gocr_op_linear_static(_dt(x), x.data_ptr(), w.data_ptr(), y.data_ptr(), T, N, K, stream))
+    with torch.cuda.device(x.device):  # the library takes the scratch address of the current device
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+        _check(lib.gocr_op_linear_static(_dt(x), x.data_ptr(), w.data_ptr(), y.data_ptr(), T, N, K, stream))
     return y
 
 

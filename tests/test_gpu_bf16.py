@@ -259,33 +259,3 @@ def test_base_sampled_logits_vs_oracle(base):
     assert ok, err
     agree = float(np.mean(np.argmax(lg_v, -1) == np.argmax(ref_v, -1)))
     print(f"0.5B verify-row argmax agreement with the oracle: {agree:.3f}")
-
-
-def test_base_persistent_forward_equals_per_operation(base):
-    """The persistent decode forward and the per-operation kernels give the
-    same bits on the 0.5B-class decoder: draft logits and the text-region
-    self-speculative token stream (a handle of its own: the mma.sync attention,
-    whose tile code the persistent kernel shares, and no captured graphs)."""
-    g, synth = base["g"], base["synth"]
-    wl = synth.WORKLOADS["text"]
-    prefix = synth.make_prefix(wl.model, wl.prefix_len)
-    dec = g.Decoder(base["cfg"], base["W"], max_ctx=wl.prefix_len + wl.max_new + 64 + 8, max_block=wl.block)
-    assert dec.attention_kind() == g.ATTN_MMA_SYNC
-
-    def run():
-        dec.prefill(0, prefix)
-        _, x0 = dec.state(0)
-        lg = dec.debug_forward(0, g.FWD_DRAFT, [x0] + [0] * wl.block)
-        dec.prefill(0, prefix)
-        ss, _ = dec.decode(0, g.MODE_SELFSPEC, wl.block, wl.max_new)
-        return lg, list(ss)
-
-    try:
-        lg_ops, ss_ops = run()
-        dec.set_forward_path(g.FORWARD_PERSISTENT)
-        lg_p, ss_p = run()
-        assert dec.persistent_forwards() > 0
-    finally:
-        dec.close()
-    assert np.array_equal(lg_ops.view(np.uint32), lg_p.view(np.uint32))
-    assert ss_ops == ss_p
