@@ -42,8 +42,10 @@ extern "C" {
 #define GOCR_ESTATE     (-7) /* call order: decode before prefill, and the like  */
 
 enum { GOCR_DTYPE_F32 = 0, GOCR_DTYPE_BF16 = 1 };
-/* decode modes: AR greedy (one token per forward) or self-speculative rounds */
-enum { GOCR_MODE_AR = 0, GOCR_MODE_SELFSPEC = 1 };
+/* decode modes: AR greedy (one token per forward), self-speculative rounds,
+ * and (gocr_decode_ex) direct block diffusion and self-speculative rounds
+ * with a refined draft */
+enum { GOCR_MODE_AR = 0, GOCR_MODE_SELFSPEC = 1, GOCR_MODE_DIFFUSION = 2, GOCR_MODE_REFINED = 3 };
 /* single-forward kinds for gocr_debug_forward */
 enum { GOCR_FWD_AR = 0, GOCR_FWD_DRAFT = 1, GOCR_FWD_VERIFY = 2 };
 
@@ -129,6 +131,47 @@ int gocr_decode(gocr_handle* h, int req, int mode, int B, int max_new,
  * the others continue. */
 int gocr_decode_batch(gocr_handle* h, int n_req, const int32_t* reqs, int mode, int B,
                       const int32_t* max_new, int32_t* const* out_tokens, gocr_stats* stats);
+
+/* Options of the block-step decodes. */
+typedef struct gocr_decode_opts {
+  float tau;            /* DIFFUSION: the confidence threshold tau_c; REFINED: the
+                           draft-side threshold.  Confidence = the largest softmax
+                           probability of a row; a value equal to tau passes. */
+  int32_t draft_steps;  /* REFINED: draft forwards per round at most, 1..64 */
+} gocr_decode_opts;
+
+/* gocr_decode_batch with every mode, one forward per device-loop iteration
+ * for the two block-step modes (opts required for them, ignored otherwise):
+ *
+ *   GOCR_MODE_DIFFUSION  direct block-diffusion decoding (GravityOCR review,
+ *     §2 "Block Diffusion" and Appendix B.1 "Direct Block-Diffusion
+ *     Decoding"): a block of B slots at positions p+1..p+B starts as [M];
+ *     each denoising step forwards the draft window [x0, slots] (x0 causal,
+ *     the slots reading the cache and the whole window) and fixes every masked
+ *     slot whose confidence reaches tau (slot s takes the argmax of the row at
+ *     position p+s-1, the shift-by-one convention), or else the single most
+ *     confident masked slot (the lowest slot among equals).  A finished block
+ *     commits its B tokens (cut at max_new and after the first eos); unless
+ *     decoding stops there, a token-causal cache-write forward of [x0,
+ *     y_1..y_B] at p..p+B follows, the cache keeps positions 0..p+B-1 and
+ *     y_B becomes the boundary.  Stats: rounds = blocks, forwards = denoising
+ *     steps + cache writes, accept_hist[k] = blocks finished in k steps,
+ *     accepted_drafts = 0.
+ *   GOCR_MODE_REFINED  self-speculative rounds whose draft runs up to
+ *     draft_steps denoising forwards (review Appendix D, "Draft Schedule"):
+ *     each step fixes slots by the rule above with the draft-side threshold;
+ *     after the last step (or when every slot is fixed) the verify window is
+ *     [slot 1..slot B, the last step's prediction at position p+B+1], unfixed
+ *     slots taking the last step's predictions; verify, accept and rollback
+ *     are those of GOCR_MODE_SELFSPEC, so the output equals AR greedy.
+ *     draft_steps = 1 is the one-shot round (the same tokens, stats and bits
+ *     as GOCR_MODE_SELFSPEC).  Stats: forwards = draft steps + verifies.
+ *
+ * No forced-acceptance override applies to the block-step modes.
+ * Errors as gocr_decode_batch; GOCR_EINVAL for a NaN threshold or
+ * draft_steps out of range. */
+int gocr_decode_ex(gocr_handle* h, int n_req, const int32_t* reqs, int mode, int B, const gocr_decode_opts* opts,
+                   const int32_t* max_new, int32_t* const* out_tokens, gocr_stats* stats);
 
 /* Forced-acceptance hook for request `req` (host arrays, copied):  in round r
  * with c tokens committed, drafts become d_j = ref[c+j] for j <= G_r and

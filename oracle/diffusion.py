@@ -50,7 +50,7 @@ from typing import List, Optional, Sequence, Tuple
 import numpy as np
 
 from .decode import State, _stopped, accept_length, prefill, verify_forward
-from .model import Model, argmax_lowest, causal_mask, draft_mask, forward, token_rows
+from .model import Model, argmax_lowest, causal_mask, draft_mask, forward, token_rows, top2_margin
 
 
 def confidence(logits: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
@@ -94,6 +94,7 @@ class StepLog:
     fixed: List[int]          # slot indices (0-based: slot s+1) fixed by this step
     tokens: List[int]         # the B slot predictions of the step (rows 0..B-1)
     conf: List[float]         # their confidences
+    margin: List[float]       # top-two logit margin of every row of the window (diagnostic)
 
 
 @dataclasses.dataclass
@@ -128,7 +129,8 @@ def diffusion_block(model: Model, st: State, B: int, tau: float, max_new: int,
         fixed = choose_slots(conf, masked, tau)
         for s in fixed:
             slots[s] = int(tok[s])
-        steps.append(StepLog(fixed=fixed, tokens=[int(t) for t in tok], conf=[float(x) for x in conf]))
+        steps.append(StepLog(fixed=fixed, tokens=[int(t) for t in tok], conf=[float(x) for x in conf],
+                             margin=[top2_margin(r) for r in logits]))
     commit = list(slots)[: max_new - c]
     if eos_id >= 0 and eos_id in commit:
         commit = commit[: commit.index(eos_id) + 1]
@@ -206,7 +208,8 @@ def refined_round(model: Model, st: State, B: int, tau_d: float, n_steps: int, m
         fixed = choose_slots(conf[:B], masked, tau_d)
         for s in fixed:
             slots[s] = last[s]
-        steps.append(StepLog(fixed=fixed, tokens=last[:B], conf=[float(x) for x in conf[:B]]))
+        steps.append(StepLog(fixed=fixed, tokens=last[:B], conf=[float(x) for x in conf[:B]],
+                             margin=[top2_margin(r) for r in logits]))
         if all(s >= 0 for s in slots):
             break
     window = [slots[s] if slots[s] >= 0 else last[s] for s in range(B)] + [last[B]]

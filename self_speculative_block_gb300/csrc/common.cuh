@@ -56,7 +56,16 @@ struct ReqState {
   int pad_;
   long long st_rounds, st_forwards, st_committed, st_accepted;
   int hist[65];
+  // block-step decodes (direct block diffusion, refined drafts): one forward
+  // per loop iteration, its kind chosen from `phase`
+  int phase;           // PHASE_STEP, PHASE_WRITE (diffusion) or PHASE_VERIFY (refined)
+  int steps;           // denoising steps run in the current block or draft
+  int n_steps;         // refined drafts: draft forwards per round at most
+  float tau;           // confidence threshold (tau_c, or the draft-side tau_d)
+  int blk[64];         // slot tokens of the window, -1 = [M] (slot s at position cache_len + 1 + s)
+  int win[65];         // refined drafts: the verify window [a0, d1..dB] of the last draft step
 };
+enum BlockPhase : int { PHASE_STEP = 0, PHASE_WRITE = 1, PHASE_VERIFY = 2 };
 
 // Row table of one forward (built on the device from ReqState by plan kernels).
 struct Plan {

@@ -218,6 +218,16 @@ __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int 
           }
           if (__any_sync(0xffffffffu, nan) && lane == 0) set_err(e.err, DERR_NAN_LOGITS);
           if (lane == 0 && bi != 0x7fffffff) atomicMax(e.amax + t, argmax_key(bv, bi));
+          if (e.conf_part) {
+            // every lane holds the tile maximum bv; lane 0's sum takes one fixed order
+            float se = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (n0 + lane + 32 * j < a.N) se += expf(v[j] - bv);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+            if (lane == 0) e.conf_part[(size_t)t * (a.N / NTILE) + tile] = make_float2(bv, se);
+          }
           break;
         }
       }

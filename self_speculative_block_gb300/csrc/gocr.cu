@@ -88,6 +88,7 @@ struct gocr_handle {
   void* q_hi = nullptr;       // rotated query planes [T][q_dim]
   void* q_lo = nullptr;
   float* logits = nullptr;
+  float2* conf_part = nullptr;  // LM-head softmax partials [T_dec][vocab / 128] (block-step decodes)
   float* att_part = nullptr;  // attention partial rows of the key-chunk ranks (bf16 models)
   int* att_chunks = nullptr;  // chunks per (slot, kv head x row group) of the last attention
   unsigned long long* amax = nullptr;
@@ -194,7 +195,7 @@ void set_norm_in(gocr_handle* h, GemmArgs& a) {
 // out.  RMSNorm is folded into the GEMMs: producers write resid * g (the next
 // norm's gain) as planes plus per-tile sums of squares; consumers scale by rstd.
 void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out, float* logits,
-                  const int* slot_tab, FwdArgs& f) {
+                  const int* slot_tab, FwdArgs& f, float2* conf_part = nullptr) {
   const gocr_config& c = h->cfg;
   const int T = n_rows_of(kind, n_slots, B, P);
   const int H = c.hidden;
@@ -267,6 +268,7 @@ void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_o
   gl.e.in_rows = kind == PLAN_PREFILL ? h->rows.logit_row : nullptr;
   gl.epi = EPI_ARGMAX;
   gl.e.logits = logits; gl.e.ld_logits = c.vocab;
+  gl.e.conf_part = conf_part;
   gl.e.amax = h->amax; gl.e.am_out = am_out; gl.e.grid_ctr = h->grid_ctr;
   f.g.push_back(gl);
   // each GEMM brings the next GEMM's weights into L2 (at most 48 MB of them)
@@ -282,7 +284,7 @@ void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_o
 // Enqueue one decoder forward over the rows the plan kernel has laid out:
 // the embedding rows, then one kernel per operation.
 bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_out,
-                     float* logits, const int* slot_tab) {
+                     float* logits, const int* slot_tab, float2* conf_part = nullptr) {
   const gocr_config& c = h->cfg;
   const int T = n_rows_of(kind, n_slots, B, P);
   const int H = c.hidden;
@@ -291,7 +293,7 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
   launch_embed(h->dtype, h->embed, h->mask, h->prefix_stage, h->resid, h->gattn[0], h->xg_hi, h->xg_lo,
                h->ssq, h->rows, T, H, c.vocab, h->err, h->hs, pdl);
   FwdArgs f;
-  forward_args(h, kind, n_slots, B, P, am_out, logits, slot_tab, f);
+  forward_args(h, kind, n_slots, B, P, am_out, logits, slot_tab, f, conf_part);
   if (h->op_trace_next) {
     // launch records in forward order: per layer QKV, attention, O, gate/up, down; then the LM head
     for (int l = 0; l < c.n_layers; ++l) {
@@ -318,6 +320,14 @@ bool enqueue_round(gocr_handle* h, int mode, int B, int n_slots, unsigned long l
   bool ok = true;
   const int cap = h->cap;
   const int out_stride = cap;
+  if (mode == GOCR_MODE_DIFFUSION || mode == GOCR_MODE_REFINED) {
+    // one forward per iteration; its rows follow each request's phase
+    launch_plan(PLAN_BLOCK, h->rows, h->st, h->slot_req, n_slots, B, 0, nullptr, nullptr, cap, h->hs, h->pdl);
+    ok &= enqueue_forward(h, PLAN_DRAFT, n_slots, B, 0, h->dbuf, nullptr, h->slot_req, h->conf_part);
+    launch_block_step(mode == GOCR_MODE_REFINED, h->st, h->slot_req, n_slots, B, h->dbuf, h->conf_part,
+                      h->cfg.vocab / NTILE, h->out, out_stride, h->err, cond, use_cond, h->hs, h->pdl);
+    return ok;
+  }
   if (mode == GOCR_MODE_AR) {
     launch_plan(PLAN_AR, h->rows, h->st, h->slot_req, n_slots, 0, 0, nullptr, nullptr, cap, h->hs, h->pdl);
     ok &= enqueue_forward(h, PLAN_AR, n_slots, 0, 0, h->abuf, nullptr, h->slot_req);
@@ -420,12 +430,19 @@ const char* dev_err_name(int e) {
 }
 
 int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const int* max_new,
-               int32_t* const* out_tokens, gocr_stats* stats) {
+               int32_t* const* out_tokens, gocr_stats* stats, float tau = 0.f, int draft_steps = 1) {
   const gocr_config& c = h->cfg;
-  if (mode != GOCR_MODE_AR && mode != GOCR_MODE_SELFSPEC) return fail(h, GOCR_EINVAL, "bad mode %d", mode);
+  if (mode != GOCR_MODE_AR && mode != GOCR_MODE_SELFSPEC && mode != GOCR_MODE_DIFFUSION &&
+      mode != GOCR_MODE_REFINED)
+    return fail(h, GOCR_EINVAL, "bad mode %d", mode);
   if (n < 1 || n > c.max_requests) return fail(h, GOCR_EINVAL, "bad request count %d", n);
-  if (mode == GOCR_MODE_SELFSPEC && (B < 1 || B > c.max_block))
+  if (mode != GOCR_MODE_AR && (B < 1 || B > c.max_block))
     return fail(h, GOCR_ECAPACITY, "block size %d outside 1..%d", B, c.max_block);
+  if (mode == GOCR_MODE_DIFFUSION || mode == GOCR_MODE_REFINED) {
+    if (!(tau == tau)) return fail(h, GOCR_EINVAL, "threshold is NaN");
+    if (mode == GOCR_MODE_REFINED && (draft_steps < 1 || draft_steps > GOCR_MAX_BLOCK))
+      return fail(h, GOCR_EINVAL, "draft steps %d outside 1..%d", draft_steps, GOCR_MAX_BLOCK);
+  }
   if (mode == GOCR_MODE_AR) B = 0;
   int rows = mode == GOCR_MODE_AR ? n : n * (B + 1);
   if (rows > h->T_dec) return fail(h, GOCR_ECAPACITY, "%d rows per forward exceed %d", rows, h->T_dec);
@@ -450,7 +467,16 @@ int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const in
   CK(cudaMemcpyAsync(h->slot_req, reqs, sizeof(int) * n, cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemcpyAsync(h->max_new_dev, max_new, sizeof(int) * n, cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
-  launch_begin_decode(h->st, h->slot_req, n, h->max_new_dev, bound + 2, c.eos_id, h->hs);
+  // device-side loop bound: rounds (AR steps) for the two-forward loops;
+  // loop iterations (one forward each) for the block-step decodes: at most
+  // B denoising steps and one cache write per block of B tokens, or
+  // draft_steps draft forwards and one verify per round
+  long long iters = bound + 2;
+  if (mode == GOCR_MODE_DIFFUSION) iters = (long long)(B + 1) * ((bound + B - 1) / B) + 2;
+  if (mode == GOCR_MODE_REFINED) iters = (long long)(draft_steps + 1) * (bound + 2);
+  if (iters > (1 << 30)) iters = 1 << 30;
+  launch_begin_decode(h->st, h->slot_req, n, h->max_new_dev, (int)iters, c.eos_id, tau,
+                      mode == GOCR_MODE_REFINED ? draft_steps : 1, h->hs);
   CK(cudaGetLastError());
   cudaGraphExec_t exec;
   int rc = get_graph(h, mode, B, n, &exec);
@@ -460,7 +486,7 @@ int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const in
     CK(cudaGraphLaunch(exec, h->hs));
   } else {
     // one graph per round; the host polls the done flags after every round
-    for (int round = 0; round < bound + 2; ++round) {
+    for (long long round = 0; round < iters; ++round) {
       CK(cudaGraphLaunch(exec, h->hs));
       bool all_done = true;
       for (int i = 0; i < n; ++i) {
@@ -633,6 +659,7 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
   }
   h->ssq = (float*)A((size_t)T * (H / NTILE) * 4);
   h->logits = (float*)A((size_t)h->T_dec * c.vocab * 4);
+  h->conf_part = (float2*)A((size_t)h->T_dec * (c.vocab / NTILE) * sizeof(float2));
   if (h->dtype == GOCR_DTYPE_BF16) {
     // partial rows of the attention ranks: a prefill (one slot of up to
     // max_ctx rows) or a decode forward (max_requests slots of max_block + 1 rows)
@@ -740,6 +767,18 @@ int gocr_decode_batch(gocr_handle* h, int n_req, const int32_t* reqs, int mode, 
   int r = sync_user(h);
   if (r) return r;
   return run_decode(h, n_req, reqs, mode, B, max_new, out_tokens, stats);
+}
+
+int gocr_decode_ex(gocr_handle* h, int n_req, const int32_t* reqs, int mode, int B, const gocr_decode_opts* opts,
+                   const int32_t* max_new, int32_t* const* out_tokens, gocr_stats* stats) {
+  if (!h) return fail(nullptr, GOCR_EINVAL, "null handle");
+  if (!reqs || !max_new || !out_tokens) return fail(h, GOCR_EINVAL, "null argument");
+  if ((mode == GOCR_MODE_DIFFUSION || mode == GOCR_MODE_REFINED) && !opts)
+    return fail(h, GOCR_EINVAL, "mode %d needs options", mode);
+  int r = sync_user(h);
+  if (r) return r;
+  return run_decode(h, n_req, reqs, mode, B, max_new, out_tokens, stats, opts ? opts->tau : 0.f,
+                    opts ? opts->draft_steps : 1);
 }
 
 int gocr_set_draft_override(gocr_handle* h, int req, const int32_t* ref_tokens, int n_ref,

@@ -55,6 +55,10 @@ struct EpiArgs {
   // ARGMAX: lowest index among equal maxima via 64-bit atomicMax of
   // (order-preserving value bits << 32 | ~index); the last CTA publishes.
   float* logits; int ld_logits;  // optional full logits (fp32 [T, N])
+  // optional per-(row, 128-column tile) softmax partials (tile max m, sum of
+  // exp(l - m) over the tile's columns), [T][N / 128]: the confidence of a
+  // row is 1 / sum_tiles s exp(m - max m), combined in tile order
+  float2* conf_part;
   unsigned long long* amax;      // [T], zero between launches
   int* am_out;                   // [T]
   int* grid_ctr;                 // zero between launches
@@ -154,7 +158,10 @@ void launch_embed(int dtype, const void* embed, const void* mask_embed, const vo
                   int T, int H, int vocab, int* err, cudaStream_t s, bool pdl);
 void launch_rope_table(float2* tab, int cap, int d, float theta, cudaStream_t s);
 
-enum PlanKind : int { PLAN_AR = 0, PLAN_DRAFT = 1, PLAN_VERIFY = 2, PLAN_PREFILL = 3 };
+// PLAN_BLOCK: block-step decodes; each slot's rows follow its ReqState::phase
+// (the draft window with the slots' tokens, the causal cache write, or the
+// refined round's verify window), B + 1 rows per slot.
+enum PlanKind : int { PLAN_AR = 0, PLAN_DRAFT = 1, PLAN_VERIFY = 2, PLAN_PREFILL = 3, PLAN_BLOCK = 4 };
 // Decode plans read ReqState; `toks` (optional) overrides the row tokens (debug forwards).
 void launch_plan(int kind, const Rows& r, ReqState* st, const int* slot_req, int n_slots, int B,
                  int prefill_len, const int* dbuf, const int* toks, int cap, cudaStream_t s, bool pdl);
@@ -169,9 +176,16 @@ void launch_override(ReqState* st, const int* slot_req, int n_slots, int B, int*
                      int vocab, cudaStream_t s, bool pdl);
 void launch_prefill_finish(ReqState* st, int req, int P, const int* am, int* out, int out_stride,
                            cudaStream_t s);
-// Arms request slots for a decode call: max_new, the round bound, eos, stats reset.
+// Arms request slots for a decode call: max_new, the loop bound, eos, stats
+// reset, and the block-step state (threshold, draft steps, masked slots).
 void launch_begin_decode(ReqState* st, const int* slot_req, int n_slots, const int* max_new,
-                         int max_rounds, int eos_id, cudaStream_t s);
+                         int max_rounds, int eos_id, float tau, int n_steps, cudaStream_t s);
+// The step kernel of a block-step decode (refined = 0: direct block
+// diffusion; 1: self-speculative rounds with refined drafts), after the
+// forward whose LM head wrote argmaxes `am` and confidence partials.
+void launch_block_step(int refined, ReqState* st, const int* slot_req, int n_slots, int B, const int* am,
+                       const float2* conf_part, int n_tiles, int* out, int out_stride, const int* err,
+                       unsigned long long cond, int use_cond, cudaStream_t s, bool pdl);
 void launch_set_override(ReqState* st, int req, int n_ref, int n_sched, cudaStream_t s);
 
 // Launch timeline records (GemmArgs::trace, TRACE_WORDS words): word 0 min of

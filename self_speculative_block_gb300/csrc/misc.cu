@@ -148,6 +148,19 @@ __global__ void plan_kernel(int kind, Rows r, ReqState* st, const int* slot_req,
       case PLAN_VERIFY:
         pos = p + 1 + j; lim = pos; tok = toks ? toks[t] : dbuf[t];
         break;
+      case PLAN_BLOCK: {
+        const ReqState& q = st[req];
+        if (q.phase == PHASE_STEP) {          // [x0, slots] under the draft mask
+          pos = p + j; lim = j == 0 ? p : p + B;
+          tok = j == 0 ? q.x0 : (q.blk[j - 1] >= 0 ? q.blk[j - 1] : TOK_MASK);
+        } else if (q.phase == PHASE_WRITE) {  // [x0, y_1..y_B], token-causal
+          pos = p + j; lim = pos;
+          tok = j == 0 ? q.x0 : q.blk[j - 1];
+        } else {                              // PHASE_VERIFY: [a0, d_1..d_B] at p+1.., token-causal
+          pos = p + 1 + j; lim = pos; tok = q.win[j];
+        }
+        break;
+      }
       default:  // PLAN_PREFILL
         pos = j; lim = j; tok = tok_prefix(j);
         break;
@@ -167,6 +180,7 @@ __global__ void plan_kernel(int kind, Rows r, ReqState* st, const int* slot_req,
     pl->slot_row0[s] = s * w;
     pl->slot_nrows[s] = w;
     int ml = kind == PLAN_PREFILL ? w - 1 : (kind == PLAN_AR ? p : (kind == PLAN_DRAFT ? p + B : p + B + 1));
+    if (kind == PLAN_BLOCK) ml = st[req].phase == PHASE_VERIFY ? p + B + 1 : p + B;
     pl->slot_maxlim[s] = ml;
     if (kind != PLAN_PREFILL && p + (kind == PLAN_AR ? 0 : B + 1) >= cap) {
       st[req].error = DERR_CAPACITY;
@@ -302,6 +316,183 @@ void launch_override(ReqState* st, const int* slot_req, int n_slots, int B, int*
            sched_stride, vocab);
 }
 
+// ---------------------------------------------------------------- block-step decodes
+// Confidence of one LM-head row from its per-tile partials (tile max m_k,
+// sum of exp(l - m_k) over the tile): 1 / sum_k s_k exp(m_k - m), m = max_k m_k.
+// Lane l folds tiles l, l + 32, ... in order, then the lanes combine in a
+// fixed butterfly; lane 0's value is the result.
+__device__ float row_confidence(const float2* part, int n_tiles) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY, s = 0.f;
+  for (int k = lane; k < n_tiles; k += 32) {
+    const float2 pk = part[k];
+    if (pk.x > m) {
+      s = s * expf(m - pk.x) + pk.y;
+      m = pk.x;
+    } else {
+      s += pk.y * expf(pk.x - m);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const float os = __shfl_xor_sync(0xffffffffu, s, o);
+    const float mm = fmaxf(m, om);
+    s = (m == -INFINITY ? 0.f : s * expf(m - mm)) + (om == -INFINITY ? 0.f : os * expf(om - mm));
+    m = mm;
+  }
+  return 1.f / s;
+}
+
+// Confidences of every still-masked slot's row (slot r is predicted by row r
+// of the request's window), one warp per row, into conf[slot][64].
+__device__ void masked_slot_confidences(const ReqState* st, const int* slot_req, int n_slots, int B,
+                                        const float2* conf_part, int n_tiles, float* conf) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int x = warp; x < n_slots * B; x += nw) {
+    const int i = x / B, r = x % B;
+    const ReqState& q = st[slot_req[i]];
+    if (q.done || q.phase != PHASE_STEP || q.blk[r] >= 0) continue;
+    const float c = row_confidence(conf_part + (size_t)(i * (B + 1) + r) * n_tiles, n_tiles);
+    if ((threadIdx.x & 31) == 0) conf[i * 64 + r] = c;
+  }
+}
+
+// One denoising step's threshold rule (GravityOCR review, Appendix B.1): every
+// masked slot whose confidence reaches tau gets its row's argmax; if none
+// does, the most confident masked slot alone (the lowest slot among equals).
+// Returns whether every slot is fixed.
+__device__ bool fix_slots(ReqState& q, const float* conf, const int* pred, int B) {
+  int n_pass = 0, best = -1;
+  float bc = 0.f;
+  for (int r = 0; r < B; ++r) {
+    if (q.blk[r] >= 0) continue;
+    if (conf[r] >= q.tau) ++n_pass;
+    if (best < 0 || conf[r] > bc) { best = r; bc = conf[r]; }
+  }
+  bool all = true;
+  for (int r = 0; r < B; ++r) {
+    if (q.blk[r] >= 0) continue;
+    if (n_pass ? conf[r] >= q.tau : r == best) q.blk[r] = pred[r];
+    else all = false;
+  }
+  return all;
+}
+
+__device__ void end_iteration(ReqState& q, const int* err) {
+  if (err && *err) { q.error = *err; q.done = 1; }
+  if (!q.done && q.round >= q.max_rounds) { q.error = DERR_ROUND_LIMIT; q.done = 1; }
+}
+
+// Direct block-diffusion decoding, one forward per loop iteration.
+//   PHASE_STEP: fix slots by the threshold rule; a finished block commits
+//   y_1..y_B (cut at max_new and after the first EOS) and, unless decoding
+//   stops, moves to PHASE_WRITE.
+//   PHASE_WRITE (the causal cache-write forward has run): positions
+//   p..p+B-1 now hold causal state, y_B becomes the boundary, a new block of
+//   masks starts.
+// Stats: rounds = blocks, forwards = steps + cache writes, hist[steps of a block].
+__global__ void diffusion_step_kernel(ReqState* st, const int* slot_req, int n_slots, int B, const int* am,
+                                      const float2* conf_part, int n_tiles, int* out, int out_stride,
+                                      const int* err, unsigned long long cond, int use_cond) {
+  __shared__ float conf[MAX_REQ * 64];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  masked_slot_confidences(st, slot_req, n_slots, B, conf_part, n_tiles, conf);
+  __syncthreads();
+  const int i = threadIdx.x;
+  if (i < n_slots) {
+    const int req = slot_req[i];
+    ReqState& q = st[req];
+    if (!q.done) {
+      q.round += 1;
+      q.st_forwards += 1;
+      if (q.phase == PHASE_STEP) {
+        q.steps += 1;
+        if (fix_slots(q, conf + i * 64, am + i * (B + 1), B)) {
+          const int room = q.max_new - q.committed;
+          int n = B < room ? B : room;
+          bool eos = false;
+          if (q.eos_id >= 0)
+            for (int r = 0; r < n; ++r)
+              if (q.blk[r] == q.eos_id) { n = r + 1; eos = true; break; }
+          int* o = out + (size_t)req * out_stride;
+          for (int r = 0; r < n; ++r) o[q.committed + r] = q.blk[r];
+          q.committed += n;
+          q.st_committed += n;
+          q.st_rounds += 1;
+          q.hist[q.steps < 64 ? q.steps : 64] += 1;
+          if (q.committed >= q.max_new || eos) q.done = 1;
+          else q.phase = PHASE_WRITE;
+        }
+      } else {
+        q.cache_len += B;
+        q.x0 = q.blk[B - 1];
+        for (int r = 0; r < B; ++r) q.blk[r] = -1;
+        q.steps = 0;
+        q.phase = PHASE_STEP;
+      }
+      end_iteration(q, err);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) set_loop_condition(st, slot_req, n_slots, cond, use_cond);
+}
+
+// Self-speculative rounds with a refined draft (GravityOCR review, Appendix D),
+// one forward per loop iteration.
+//   PHASE_STEP: a draft forward; fix slots by the draft-side threshold; the
+//   verify window becomes [slot 1..B (fixed, else this step's prediction),
+//   row B's prediction]; after n_steps draft forwards, or when every slot is
+//   fixed, move to PHASE_VERIFY.
+//   PHASE_VERIFY: accept, commit and roll back as the one-shot round does.
+__global__ void refine_step_kernel(ReqState* st, const int* slot_req, int n_slots, int B, const int* am,
+                                   const float2* conf_part, int n_tiles, int* out, int out_stride,
+                                   const int* err, unsigned long long cond, int use_cond) {
+  __shared__ float conf[MAX_REQ * 64];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  masked_slot_confidences(st, slot_req, n_slots, B, conf_part, n_tiles, conf);
+  __syncthreads();
+  const int i = threadIdx.x;
+  if (i < n_slots) {
+    const int req = slot_req[i];
+    ReqState& q = st[req];
+    if (!q.done) {
+      const int* a = am + i * (B + 1);
+      if (q.phase == PHASE_STEP) {
+        q.round += 1;
+        q.st_forwards += 1;
+        q.steps += 1;
+        const bool all = fix_slots(q, conf + i * 64, a, B);
+        for (int r = 0; r < B; ++r) q.win[r] = q.blk[r] >= 0 ? q.blk[r] : a[r];
+        q.win[B] = a[B];
+        if (all || q.steps >= q.n_steps) q.phase = PHASE_VERIFY;
+        end_iteration(q, err);
+      } else {
+        // a holds a_1..a_(B+1); the drafts d_j = win[j]
+        int A = 0;
+        while (A < B && q.win[A + 1] == a[A]) ++A;
+        int commit[66];
+        commit[0] = q.win[0];
+        for (int j = 1; j <= A + 1; ++j) commit[j] = a[j - 1];
+        const int p = q.cache_len;
+        finish_round(q, out + (size_t)req * out_stride, commit, A + 2, A, p + A + 2, a[A], 1, err);
+        for (int r = 0; r < B; ++r) q.blk[r] = -1;
+        q.steps = 0;
+        q.phase = PHASE_STEP;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) set_loop_condition(st, slot_req, n_slots, cond, use_cond);
+}
+
+void launch_block_step(int refined, ReqState* st, const int* slot_req, int n_slots, int B, const int* am,
+                       const float2* conf_part, int n_tiles, int* out, int out_stride, const int* err,
+                       unsigned long long cond, int use_cond, cudaStream_t s, bool pdl) {
+  launch_k(refined ? refine_step_kernel : diffusion_step_kernel, dim3(1), dim3(1024), 0, s, pdl, st, slot_req,
+           n_slots, B, am, conf_part, n_tiles, out, out_stride, err, cond, use_cond);
+}
+
 __global__ void prefill_finish_kernel(ReqState* st, int req, int P, const int* am, int* out,
                                       int out_stride) {
   ReqState& q = st[req];
@@ -323,7 +514,7 @@ void launch_prefill_finish(ReqState* st, int req, int P, const int* am, int* out
 }
 
 __global__ void begin_decode_kernel(ReqState* st, const int* slot_req, int n_slots,
-                                    const int* max_new, int max_rounds, int eos_id) {
+                                    const int* max_new, int max_rounds, int eos_id, float tau, int n_steps) {
   const int s = threadIdx.x;
   if (s >= n_slots) return;
   ReqState& q = st[slot_req[s]];
@@ -335,11 +526,17 @@ __global__ void begin_decode_kernel(ReqState* st, const int* slot_req, int n_slo
   q.done = q.committed >= q.max_new;
   q.st_rounds = q.st_forwards = q.st_committed = q.st_accepted = 0;
   for (int i = 0; i < 65; ++i) q.hist[i] = 0;
+  q.phase = PHASE_STEP;
+  q.steps = 0;
+  q.n_steps = n_steps;
+  q.tau = tau;
+  for (int i = 0; i < 64; ++i) q.blk[i] = -1;
+  for (int i = 0; i < 65; ++i) q.win[i] = q.x0;
 }
 
 void launch_begin_decode(ReqState* st, const int* slot_req, int n_slots, const int* max_new,
-                         int max_rounds, int eos_id, cudaStream_t s) {
-  begin_decode_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, max_new, max_rounds, eos_id);
+                         int max_rounds, int eos_id, float tau, int n_steps, cudaStream_t s) {
+  begin_decode_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, max_new, max_rounds, eos_id, tau, n_steps);
 }
 
 __global__ void set_override_kernel(ReqState* st, int req, int n_ref, int n_sched) {

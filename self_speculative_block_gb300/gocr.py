@@ -22,7 +22,7 @@ GOCR_OK = 0
 ERRORS = {-1: "EINVAL", -2: "ECAPACITY", -3: "ECUDA", -4: "EDEVICE", -5: "ETIMEOUT",
           -6: "ENOMEM", -7: "ESTATE"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
-MODE_AR, MODE_SELFSPEC = 0, 1
+MODE_AR, MODE_SELFSPEC, MODE_DIFFUSION, MODE_REFINED = 0, 1, 2, 3
 FWD_AR, FWD_DRAFT, FWD_VERIFY = 0, 1, 2
 OPT_ATTENTION, OPT_ATTN_RANKS = 5, 6
 TRACE_KERNELS = 1
@@ -31,7 +31,7 @@ MAX_BLOCK = 64
 LAYER_TENSORS = 9
 
 # every symbol include/gocr.h declares
-EXPORTS = ("gocr_create", "gocr_prefill", "gocr_decode", "gocr_decode_batch",
+EXPORTS = ("gocr_create", "gocr_prefill", "gocr_decode", "gocr_decode_batch", "gocr_decode_ex",
            "gocr_set_draft_override", "gocr_debug_forward", "gocr_debug_forward_batch", "gocr_read_kv", "gocr_get_state",
            "gocr_get_option", "gocr_read_trace", "gocr_last_error", "gocr_free",
            "gocr_op_linear_workspace", "gocr_op_linear", "gocr_op_linear_planes", "gocr_op_attention",
@@ -73,6 +73,10 @@ class Stats(ctypes.Structure):
         return d
 
 
+class DecodeOpts(ctypes.Structure):
+    _fields_ = [("tau", ctypes.c_float), ("draft_steps", ctypes.c_int32)]
+
+
 ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p)
 FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p)
 
@@ -96,6 +100,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gocr_decode": (i32, [vp, i32, i32, i32, i32, P32, ctypes.POINTER(Stats)]),
         "gocr_decode_batch": (i32, [vp, i32, P32, i32, i32, P32, ctypes.POINTER(P32),
                                     ctypes.POINTER(Stats)]),
+        "gocr_decode_ex": (i32, [vp, i32, P32, i32, i32, ctypes.POINTER(DecodeOpts), P32, ctypes.POINTER(P32),
+                                 ctypes.POINTER(Stats)]),
         "gocr_set_draft_override": (i32, [vp, i32, P32, i32, P32, i32]),
         "gocr_debug_forward": (i32, [vp, i32, i32, P32, i32, ctypes.POINTER(ctypes.c_float)]),
         "gocr_debug_forward_batch": (i32, [vp, i32, P32, i32, P32, i32, ctypes.POINTER(ctypes.c_float)]),
@@ -260,6 +266,22 @@ class Decoder:
         optr = (ctypes.POINTER(ctypes.c_int32) * n)(*[_p32(o) for o in outs])
         sts = (Stats * n)()
         _check(self.lib.gocr_decode_batch(self.h, n, _p32(r), mode, B, _p32(mn), optr, sts), self.h)
+        return outs, [s.as_dict() for s in sts]
+
+    def decode_ex(self, reqs: Sequence[int], mode: int, B: int, max_new: Sequence[int], tau: float = 0.0,
+                  draft_steps: int = 1):
+        """Any decode mode over several requests; MODE_DIFFUSION takes the
+        confidence threshold tau, MODE_REFINED the draft-side threshold tau and
+        at most draft_steps draft forwards per round."""
+        n = len(reqs)
+        r = _i32(reqs)
+        mn = _i32(max_new)
+        outs = [np.zeros(int(m), np.int32) for m in max_new]
+        optr = (ctypes.POINTER(ctypes.c_int32) * n)(*[_p32(o) for o in outs])
+        sts = (Stats * n)()
+        opts = DecodeOpts(float(tau), int(draft_steps))
+        _check(self.lib.gocr_decode_ex(self.h, n, _p32(r), mode, B, ctypes.byref(opts), _p32(mn), optr, sts),
+               self.h)
         return outs, [s.as_dict() for s in sts]
 
     def set_draft_override(self, req: int, ref: Sequence[int], schedule: Sequence[int]):
