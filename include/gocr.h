@@ -236,7 +236,15 @@ int gocr_get_option(const gocr_handle* h, int option, int* value);
  *     (first CTA start, first and last release from the dependency wait,
  *     last CTA end, last mainloop end, last split-K exchange end, 0, 0),
  *     globaltimer ns (the last two marks for GEMMs only). */
-enum { GOCR_TRACE_KERNELS = 1 };
+/*   GOCR_TRACE_CTAS  the same launches with one record per CTA (on with
+ *     GOCR_OP_TRACE=2): n_words >= 8 * 2048 * (5 * n_layers + 1), laid out
+ *     [launch][CTA slot][8]; CTA c of a kernel (linear block index) fills slot
+ *     c, the attention merge kernel's CTAs slots 1024 + c; a record is (start,
+ *     release from the dependency wait, GEMM epilogue start, end, then as the
+ *     launch records: mainloop end, split-K exchange end, cluster barrier
+ *     passed, accumulator drained; attention: first chunk ready, chunk loop
+ *     done, merge start), zero where a CTA did not reach a mark. */
+enum { GOCR_TRACE_KERNELS = 1, GOCR_TRACE_CTAS = 2 };
 int gocr_read_trace(gocr_handle* h, int which, uint64_t* out, size_t n_words);
 
 /* Last error message of the handle (or of the library when h is NULL). */

@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
   const int tid = threadIdx.x;
 
   if (tid == 0) {
-    if (TRACE) trace_mark(a.trace, 0);
+    if (TRACE) trace_at(a, 0);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
   // committed cache before the dependency wait (decode launches only)
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
     kv_kmax = min(a.cap - 1, pc + a.rows_per_slot);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (TRACE && tid == 0) trace_mark(a.trace, 1);
+  if (TRACE && tid == 0) trace_at(a, 1);
 
   int req = 0, row0 = 0, nrows = a.T;
   if (a.rows_per_slot > 0) {
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
   float4* dst = reinterpret_cast<float4*>(
       a.part + (((size_t)slot * gridDim.x + group) * R + rank) * attn::QR * RLD);
   for (int x = tid; x < attn::QR * RLD / 4; x += 256) dst[x] = src[x];
-  if (TRACE && tid == 0) trace_mark(a.trace, 3);
+  if (TRACE && tid == 0) trace_at(a, 3);
 }
 
 // Merge kernel: one CTA per (PPC pairs of rows, kv head x row group, slot);
@@ -221,8 +221,10 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R)
   const int kvh = group % a.Hkv, rg = group / a.Hkv;
   const int G = a.Hq / a.Hkv;
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (TRACE && a.trace_cta && threadIdx.x == 0) trace_at(a, 0, TRACE_MERGE_SLOT);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (TRACE && threadIdx.x == 0) trace_mark(a.trace, 6);
+  if (TRACE && a.trace_cta && threadIdx.x == 0) trace_at(a, 1, TRACE_MERGE_SLOT);
+  if (TRACE && threadIdx.x == 0) trace_at(a, 6, TRACE_MERGE_SLOT);
   int row0 = 0, nrows = a.T;
   if (a.rows_per_slot > 0) {
     row0 = slot * a.rows_per_slot;
@@ -243,7 +245,7 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R)
     if (qr0 + 2 * pair >= nrows * G) break;  // uniform over the CTA
     attn::merge_rows<D, false>(a, grp, part, WS, IL, AC, n_ranks, R, 2 * pair, 1, 2, kvh, qr0, row0, nrows);
   }
-  if (TRACE && threadIdx.x == 0) trace_mark(a.trace, 3);
+  if (TRACE && threadIdx.x == 0) trace_at(a, 3, TRACE_MERGE_SLOT);
 }
 
 size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, int R) {

@@ -232,7 +232,7 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
     const bool next = c + stride < n_chunks;
     if (it == 0) cp_async_wait<0>(); else cp_async_wait<1>();  // this chunk's K (and Q, first chunk)
     grp.sync();
-    if (TRACE && it == 0 && tid == 0) trace_mark(a.trace, 4);
+    if (TRACE && it == 0 && tid == 0) trace_at(a, 4);
     // S = Q K^T for this warp's 16 rows and 16 keys
     float sacc[2][4];
 #pragma unroll
@@ -338,7 +338,7 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   }
   cp_async_wait<0>();
   grp.sync();
-  if (TRACE && tid == 0) trace_mark(a.trace, 5);
+  if (TRACE && tid == 0) trace_at(a, 5);
   // merge the two key halves of this tile: half 0 + half 1, in that order
   if (kh == 1) {
 #pragma unroll

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
   const int G = a.Hq / a.Hkv;
 
   if (tid == 0) {
-    if (TRACE) trace_mark(a.trace, 0);
+    if (TRACE) trace_at(a, 0);
     tc::grid_dep_launch();
     tc::mbar_init(s_full, 1);
     tc::mbar_init(s_full + 1, 1);
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
   tc::grid_dep_wait();
-  if (TRACE && tid == 0) trace_mark(a.trace, 1);
+  if (TRACE && tid == 0) trace_at(a, 1);
 
   int req = 0, row0 = 0, nrows = a.T;
   if (a.rows_per_slot > 0) {
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        if (TRACE && it == 0 && tid == 0) trace_mark(a.trace, 4);
+        if (TRACE && it == 0 && tid == 0) trace_at(a, 4);
         // the next chunk's scores while this chunk's softmax runs
         if (tid == 0 && it + 1 < n_it) {
           tc::fence_after_sync();
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
         }
         tc::fence_before_sync();
       }
-      if (TRACE && tid == 0) trace_mark(a.trace, 5);
+      if (TRACE && tid == 0) trace_at(a, 5);
       __syncthreads();  // every MMA is complete: Q and K are dead
       float* ST = reinterpret_cast<float*>(sm);  // [QR][RLD] staged partial rows
 #pragma unroll
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
       float4* dst = reinterpret_cast<float4*>(a.part + (((size_t)slot * gridDim.x + group) * R + rank) * QR * Gm::RLD);
       for (int x = tid; x < QR * Gm::RLD / 4; x += THREADS) dst[x] = src[x];
       if (s_fail && tid == 0) set_err(a.err, DERR_TIMEOUT);
-      if (TRACE && tid == 0) trace_mark(a.trace, 3);
+      if (TRACE && tid == 0) trace_at(a, 3);
     }
   }
   attn::cp_async_wait<0>();

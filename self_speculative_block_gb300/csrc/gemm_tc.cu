@@ -14,14 +14,19 @@
 // so they overlap the tail of the kernel that produces X.
 //
 // The K chunks of a tile run on the CTAs of one thread-block cluster (at most
-// 8).  Each CTA parks its fp32 partial tile in shared memory; after a cluster
-// barrier CTA r adds the partials of its token range over distributed shared
-// memory in rank order and runs the epilogue.  The split count depends on
-// (N, K) only, so a row's bits do not depend on how many rows share the launch.
+// 16).  Each CTA parks its fp32 partial tile in shared memory and sends the
+// rows of each peer's token range to that peer by a bulk shared-to-cluster
+// copy; CTA r adds the partials of its token range in rank order and runs the
+// epilogue.  At decode shapes the receive buffers sit past the operand ring
+// and are armed at the kernel's start ("early exchange"), so a CTA sends as
+// soon as its own accumulator is drained instead of after a cluster barrier
+// that waits for every peer's mainloop.  The split count depends on (N, K)
+// only, so a row's bits do not depend on how many rows share the launch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cooperative_groups.h>
 
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -104,13 +109,22 @@ bool tmap_2d(CUtensorMap* out, const void* ptr, int rows, int cols, int box_rows
 }
 
 __host__ __device__ inline int cdiv_i(int a, int b) { return (a + b - 1) / b; }
+
+// An environment switch (1 = set).
+bool getenv_flag(const char* name) {
+  const char* v = getenv(name);
+  return v && v[0] == '1';
+}
 }  // namespace
 
 bool encode_tmap_bf16(void* out, const void* ptr, int rows, int cols, int box_rows) {
   return tmap_2d(reinterpret_cast<CUtensorMap*>(out), ptr, rows, cols, box_rows);
 }
 
-// ring_bytes >= stages * (A tile + B tile) and >= the partial tile + reduce buffer.
+// Shared memory: the ring (>= stages * (A tile + B tile), and, after the
+// mainloop, the partial tile, the reduced rows and the epilogue scratch at
+// the offsets of gemm_y_layout), in the early exchange layout the peers'
+// partial rows past it (rx_off, in floats), then the tail at tail_off bytes.
 // EPI: the fused epilogue (a.epi), one instantiation per kind.  TRACE: the
 // instantiation that records the launch timeline (a.trace), launched only
 // when a record is attached, so that the other carries no trace code.
@@ -119,7 +133,8 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
                                                             const __grid_constant__ CUtensorMap tmx_hi,
                                                             const __grid_constant__ CUtensorMap tmx_lo,
                                                             GemmArgs a, int nt, int two, int stages,
-                                                            int ring_bytes, int per, int ys_off, int scr_off) {
+                                                            int tail_off, int per, int ys_off, int scr_off,
+                                                            int rx_off, int pre_rows) {
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzled tiles, by pointer arithmetic
@@ -131,15 +146,18 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   // after the MMAs the ring is free: the partial tile, the partial rows the
   // cluster peers send, the reduced rows and the epilogue scratch live there
   // at the offsets of gemm_y_layout
+  // the peers' partial rows: in the ring (rx_off < 0), or, in the early
+  // exchange layout, in a region of their own past the ring that peers may
+  // fill while this CTA's mainloop still uses the ring
   float* Yp = reinterpret_cast<float*>(smem);             // [nt][YLD]
-  float* RX = Yp + nt * YLD;                               // [S][per][YLD] peers' partial rows
+  float* RX = rx_off >= 0 ? Yp + rx_off : Yp + nt * YLD;   // [S][per][YLD] peers' partial rows
   float* Ys = Yp + ys_off;                                 // reduced rows (unused when S = 1)
   float* scratch = Yp + scr_off;                           // epilogue scratch
-  uint8_t* tail = smem + ring_bytes;
+  uint8_t* tail = smem + tail_off;
   float* rs_all = reinterpret_cast<float*>(tail);          // [TZ_TC] rstd of the slice's tokens
-  float* rr_pre = rs_all + TZ_TC;                          // [EG][NTILE] residual rows, or
-  float2* rope_pre = reinterpret_cast<float2*>(rr_pre);    //   [EG][head_dim / 2] RoPE rows
-  float* gn_pre = rr_pre + EG * NTILE;                     // [NTILE] next-norm gains
+  float* rr_pre = rs_all + TZ_TC;                          // [pre_rows][NTILE] residual rows, or
+  float2* rope_pre = reinterpret_cast<float2*>(rr_pre);    //   [pre_rows][head_dim / 2] RoPE rows
+  float* gn_pre = rr_pre + pre_rows * NTILE;               // [NTILE] next-norm gains
   int* pos_pre = reinterpret_cast<int*>(gn_pre + NTILE);   // [EG] row positions
   int* req_pre = pos_pre + EG;                             // [EG] row requests
   uint64_t* full = reinterpret_cast<uint64_t*>(req_pre + EG);
@@ -161,9 +179,14 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   const int nkb = cdiv_i(k1 - k0, 64);
   const int nmma = (two ? 2 : 1) * nt;
   const uint32_t ncols = nmma <= 32 ? 32 : (nmma <= 64 ? 64 : (nmma <= 128 ? 128 : 256));
+  // early exchange: every CTA arms its receive barrier and arrives on the
+  // cluster barrier at its start, so that after the mainloop a peer only has
+  // to wait for that barrier (long complete by then), not for every peer's
+  // mainloop, before sending its partial rows
+  const bool early = S > 1 && rx_off >= 0;
 
   if (tid == 0) {
-    if (TRACE) trace_mark(a.trace, 0);
+    if (TRACE) trace_at(a, 0);
     tc::prefetch_tmap(&tmw);
     tc::prefetch_tmap(&tmx_hi);
     if (two) tc::prefetch_tmap(&tmx_lo);
@@ -173,6 +196,10 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     }
     tc::mbar_init(done, 1);
     tc::mbar_init(rxbar, 1);
+    if (early) {
+      const int ta = min(tn, split * per), tb = min(tn, ta + per);
+      tc::mbar_expect_tx(rxbar, (uint32_t)((S - 1) * (tb - ta) * YLD * 4));
+    }
     tc::fence_mbar_init();
     s_fail = 0;
     tc::grid_dep_launch();
@@ -196,6 +223,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_holder;
+  if (early) tc::cluster_arrive_release();  // this CTA's receive barrier is armed
 
   if (tid == 0) {
     // TMA producer.  Weights do not depend on the previous kernel: the first
@@ -210,7 +238,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     // after the dependency wait do not pay a DRAM round trip
     for (int kb = pre; kb < nkb && kb < pre + L2_PREFETCH_BLOCKS; ++kb) tc::tma_prefetch_2d(&tmw, k0 + kb * 64, n0);
     tc::grid_dep_wait();
-    if (TRACE) trace_mark(a.trace, 1);
+    if (TRACE) trace_at(a, 1);
     for (int kb = 0; kb < nkb; ++kb) {
       const int s = kb % stages;
       const int use = kb / stages;
@@ -279,7 +307,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     }
   }
   const bool ok_done = tc::mbar_wait(done, 0);
-  if (TRACE && tid == 0) trace_mark(a.trace, 4);
+  if (TRACE && tid == 0) trace_at(a, 4);
   tc::fence_after_sync();
   __syncthreads();
   const bool failed = !ok_done || s_fail;
@@ -298,10 +326,11 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
 #pragma unroll
     for (int j = 0; j < 16; ++j) Yp[(g * 16 + j) * YLD + row] = failed ? 0.f : vh[j];
   }
+  if (early) tc::fence_proxy_async_smem();  // the partial tile is read by bulk copies
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, ncols);
-  if (TRACE && tid == 0) trace_mark(a.trace, 7);
+  if (TRACE && tid == 0) trace_at(a, 7);
 
   if (S == 1) {
     if (!failed) {
@@ -328,10 +357,14 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int ta = min(tn, rank * per), tb = min(tn, ta + per);
-    if (tid == 0) tc::mbar_expect_tx(rxbar, (uint32_t)((S - 1) * (tb - ta) * YLD * 4));
-    tc::fence_proxy_async_smem();
-    cluster.sync();  // every partial tile is written and every receive barrier armed
-    if (TRACE && tid == 0) trace_mark(a.trace, 6);
+    if (early) {
+      tc::cluster_wait_acquire();  // every peer's receive barrier is armed (at its start)
+    } else {
+      if (tid == 0) tc::mbar_expect_tx(rxbar, (uint32_t)((S - 1) * (tb - ta) * YLD * 4));
+      tc::fence_proxy_async_smem();
+      cluster.sync();  // every partial tile is written and every receive barrier armed
+    }
+    if (TRACE && tid == 0) trace_at(a, 6);
     if (tid == 0) {
       for (int r = 0; r < S; ++r) {
         const int ra = min(tn, r * per), rb = min(tn, ra + per);
@@ -342,7 +375,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
       tc::bulk_commit();
     }
     const bool rx_ok = tc::mbar_wait(rxbar, 0);
-    if (TRACE && tid == 0) trace_mark(a.trace, 5);
+    if (TRACE && tid == 0) trace_at(a, 5);
     if (!rx_ok && tid == 0) set_err(a.e.err, DERR_TIMEOUT);
     for (int g0 = ta; g0 < tb; g0 += EG) {
       const int cnt = min(EG, tb - g0);
@@ -397,6 +430,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
         *reinterpret_cast<float4*>(Ys + (size_t)j * YLD + c4) = acc;
       }
       __syncthreads();
+      if (TRACE && tid == 0 && g0 == ta) trace_at(a, 2);
       if (!failed && rx_ok) {
         EpiPre pre;
         pre.rs = a.e.ssq_in ? rs_all + g0 : nullptr;
@@ -415,7 +449,7 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     if (tid == 0) tc::bulk_wait_read();  // the copies have read this CTA's partial tile
   }
   if (EPI == EPI_ARGMAX && !failed) argmax_grid_finish(a, &s_flag);
-  if (TRACE && tid == 0) trace_mark(a.trace, 3);
+  if (TRACE && tid == 0) trace_at(a, 3);
 }
 
 // Many-slice variant (more than two 128-token slices, e.g. prefill and the
@@ -487,7 +521,7 @@ __global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
   constexpr uint32_t bufcols = 2 * NT;
 
   if (tid == 0) {
-    if (TRACE) trace_mark(a.trace, 0);
+    if (TRACE) trace_at(a, 0);
     tc::prefetch_tmap(&tmw);
     tc::prefetch_tmap(&tmx_hi);
     if (two) tc::prefetch_tmap(&tmx_lo);
@@ -523,7 +557,7 @@ __global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
     for (int kb = pre; kb < nkb && kb < pre + L2_PREFETCH_BLOCKS; ++kb)
       tc::tma_prefetch_2d(&tmw, (kb_beg + kb) * 64, n0);
     tc::grid_dep_wait();
-    if (TRACE) trace_mark(a.trace, 1);
+    if (TRACE) trace_at(a, 1);
     for (int kb = 0; kb < nkb; ++kb) {
       const int st = kb % stages;
       const int use = kb / stages;
@@ -594,7 +628,7 @@ __global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
   tc::grid_dep_wait();  // the epilogue reads and writes what earlier kernels touch
   tc::fence_before_sync();
   __syncthreads();  // every chunk drained: the MMAs, and so the ring's TMA writes, are complete
-  if (TRACE && tid == 0) trace_mark(a.trace, 4);
+  if (TRACE && tid == 0) trace_at(a, 4);
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 2 * bufcols);
@@ -649,7 +683,7 @@ __global__ void __launch_bounds__(SEQ_THREADS, NT == 64 ? 2 : 1)
     if (EPI == EPI_ARGMAX) argmax_grid_finish(a, &s_flag);  // every CTA of the grid counts itself
     cluster.sync();  // the peers have read this CTA's group sums
   }
-  if (TRACE && tid == 0) trace_mark(a.trace, 3);
+  if (TRACE && tid == 0) trace_at(a, 3);
 }
 
 template <int EPI, bool TRACE, int NT>
@@ -728,6 +762,53 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
     ring = (ring + 1023) / 1024 * 1024;
     return std::make_pair((size_t)1024 + ring + TAIL_BYTES, ring);
   };
+  // early exchange layout (decode shapes with split K): the peers' partial
+  // rows in a region past the ring, the epilogue scratch in the ring after
+  // the partial tile and this CTA's reduced rows, and the tail's prefetch
+  // rows sized to the tokens this CTA reduces
+  const int pre_rows_e = per < EG ? per : EG;
+  const int rx_bytes = a.splits * per * YLD * 4;
+  const int tail_e = TZ_TC * 4 + pre_rows_e * NTILE * 4 + NTILE * 4 + 2 * EG * 4 + 16 * 8 + 64;
+  auto early_of = [&](int st) {  // (total bytes, ring bytes)
+    int ring = st * stage_bytes;
+    const int y_bytes = ((nt + per) * YLD + EPI_SCRATCH_FLOATS) * 4;
+    if (ring < y_bytes) ring = y_bytes;
+    ring = (ring + 1023) / 1024 * 1024;
+    return std::make_pair((size_t)1024 + ring + rx_bytes + tail_e, ring);
+  };
+  if (a.splits > 1 && a.T <= 2 * 64 + 1 && !getenv_flag("GOCR_LATE_EXCHANGE")) {
+    int st = DECODE_STAGE_CAP < nkb ? DECODE_STAGE_CAP : nkb;
+    while (st > 2 && early_of(st).first > TWO_CTA_SMEM) --st;
+    if (st < 1) st = 1;
+    if (early_of(st).first <= TWO_CTA_SMEM) {
+      const int ring = early_of(st).second;
+      const size_t smem = early_of(st).first;
+      if (!kernel_smem_at_least(reinterpret_cast<const void*>(gemm_tc_kernel<EPI, TRACE, TWO>), smem, true))
+        return false;
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(cdiv_i(a.N, NTILE), a.splits, cdiv_i(a.T, TZ_TC));
+      cfg.blockDim = dim3(TC_THREADS);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = s;
+      cudaLaunchAttribute at[2];
+      int na = 0;
+      at[na].id = cudaLaunchAttributeClusterDimension;
+      at[na].val.clusterDim.x = 1;
+      at[na].val.clusterDim.y = a.splits;
+      at[na].val.clusterDim.z = 1;
+      ++na;
+      if (pdl) {
+        at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+      }
+      cfg.attrs = at;
+      cfg.numAttrs = na;
+      const int ys = nt * YLD, scr = (nt + per) * YLD, rx = ring / 4;
+      return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, TRACE, TWO>, tmw, tmh, tml, a, nt, two, st,
+                                ring + rx_bytes, per, ys, scr, rx, pre_rows_e) == cudaSuccess;
+    }
+  }
   int stages = (SMEM_CAP - 1024 - TAIL_BYTES) / stage_bytes;
   if (stages > 6) stages = 6;
   if (a.T <= 2 * 64 + 1) {
@@ -769,8 +850,8 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, TRACE, TWO>, tmw, tmh, tml, a, nt, two, stages, ring, per, yl.ys, yl.scratch) ==
-         cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<EPI, TRACE, TWO>, tmw, tmh, tml, a, nt, two, stages, ring, per,
+                            yl.ys, yl.scratch, -1, EG) == cudaSuccess;
 }
 
 // Launches of more than two 128-token slices of hi + lo planes run the K

@@ -120,6 +120,7 @@ struct gocr_handle {
 
   // per-launch timeline of debug forwards run with one kernel per operation
   unsigned long long* op_trace = nullptr;
+  bool op_trace_cta = false;  // GOCR_OP_TRACE=2: one record per CTA
   bool op_trace_next = false;
 
   bool prefilled[MAX_REQ] = {};
@@ -128,6 +129,11 @@ struct gocr_handle {
 };
 
 namespace {
+
+// Words of the kernel timelines: one record per launch, or per CTA of a launch.
+size_t op_trace_words(const gocr_handle* h) {
+  return (size_t)TRACE_WORDS * (h->op_trace_cta ? TRACE_CTA_SLOTS : 1) * (5 * h->cfg.n_layers + 1);
+}
 
 int fail(gocr_handle* h, int code, const char* fmt, ...) {
   char buf[512];
@@ -296,11 +302,17 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
   forward_args(h, kind, n_slots, B, P, am_out, logits, slot_tab, f, conf_part);
   if (h->op_trace_next) {
     // launch records in forward order: per layer QKV, attention, O, gate/up, down; then the LM head
+    const size_t rec = (size_t)TRACE_WORDS * (h->op_trace_cta ? TRACE_CTA_SLOTS : 1);
     for (int l = 0; l < c.n_layers; ++l) {
-      for (int k = 0; k < 4; ++k) f.g[(size_t)l * 4 + k].trace = h->op_trace + TRACE_WORDS * (5 * l + (k == 0 ? 0 : k + 1));
-      f.at[l].trace = h->op_trace + TRACE_WORDS * (5 * l + 1);
+      for (int k = 0; k < 4; ++k) {
+        f.g[(size_t)l * 4 + k].trace = h->op_trace + rec * (5 * l + (k == 0 ? 0 : k + 1));
+        f.g[(size_t)l * 4 + k].trace_cta = h->op_trace_cta;
+      }
+      f.at[l].trace = h->op_trace + rec * (5 * l + 1);
+      f.at[l].trace_cta = h->op_trace_cta;
     }
-    f.g[(size_t)c.n_layers * 4].trace = h->op_trace + TRACE_WORDS * (5 * c.n_layers);
+    f.g[(size_t)c.n_layers * 4].trace = h->op_trace + rec * (5 * c.n_layers);
+    f.g[(size_t)c.n_layers * 4].trace_cta = h->op_trace_cta;
   }
   for (int l = 0; l < c.n_layers; ++l) {
     ok &= launch_gemm(h->dtype, f.g[(size_t)l * 4 + 0], h->hs, pdl);
@@ -711,7 +723,10 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
   }
   if (h->dtype == GOCR_DTYPE_BF16) {
     const char* ot = getenv("GOCR_OP_TRACE");
-    if (ot && ot[0] == '1') h->op_trace = (unsigned long long*)A((size_t)TRACE_WORDS * (5 * c.n_layers + 1) * 8);
+    if (ot && (ot[0] == '1' || ot[0] == '2')) {
+      h->op_trace_cta = ot[0] == '2';
+      h->op_trace = (unsigned long long*)A(op_trace_words(h) * 8);
+    }
   }
   if (!ok) {
     int r = fail(h, GOCR_ENOMEM, "device allocation failed");
@@ -844,8 +859,9 @@ int gocr_debug_forward_batch(gocr_handle* h, int n_req, const int32_t* reqs, int
   CK(cudaMemcpyAsync(h->slot_one, reqs, sizeof(int) * n_req, cudaMemcpyHostToDevice, h->hs));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), h->hs));
   if (h->op_trace) {
-    std::vector<unsigned long long> init((size_t)TRACE_WORDS * (5 * h->cfg.n_layers + 1));
-    for (size_t i = 0; i < init.size(); ++i) init[i] = (i % TRACE_WORDS) < 2 ? ~0ull : 0ull;
+    // aggregate records start at (max, max, 0, ...) for their atomic min / max; per-CTA records at zero
+    std::vector<unsigned long long> init(op_trace_words(h));
+    for (size_t i = 0; i < init.size(); ++i) init[i] = !h->op_trace_cta && (i % TRACE_WORDS) < 2 ? ~0ull : 0ull;
     CK(cudaMemcpy(h->op_trace, init.data(), init.size() * 8, cudaMemcpyHostToDevice));
     h->op_trace_next = true;
   }
@@ -950,9 +966,10 @@ int gocr_get_option(const gocr_handle* h, int option, int* value) {
 
 int gocr_read_trace(gocr_handle* h, int which, uint64_t* out, size_t n_words) {
   if (!h || !out) return fail(h, GOCR_EINVAL, "null argument");
-  if (which != GOCR_TRACE_KERNELS) return fail(h, GOCR_EINVAL, "bad trace kind %d", which);
-  if (!h->op_trace) return fail(h, GOCR_ESTATE, "kernel tracing is off (GOCR_OP_TRACE)");
-  const size_t words = (size_t)TRACE_WORDS * (5 * h->cfg.n_layers + 1);
+  if (which != GOCR_TRACE_KERNELS && which != GOCR_TRACE_CTAS) return fail(h, GOCR_EINVAL, "bad trace kind %d", which);
+  if (!h->op_trace || h->op_trace_cta != (which == GOCR_TRACE_CTAS))
+    return fail(h, GOCR_ESTATE, "this kernel trace is off (GOCR_OP_TRACE=1 or 2 at create)");
+  const size_t words = op_trace_words(h);
   if (n_words < words) return fail(h, GOCR_ECAPACITY, "trace needs %zu words", words);
   CK(cudaStreamSynchronize(h->hs));
   CK(cudaMemcpy(out, h->op_trace, words * 8, cudaMemcpyDeviceToHost));

@@ -83,6 +83,7 @@ struct alignas(16) GemmArgs {  // 16-byte aligned: tables of them are copied by 
   // optional launch timeline record (4 words: first CTA start, first and last
   // release from the dependency wait, last CTA end; globaltimer ns)
   unsigned long long* trace;
+  int trace_cta;                 // 1: `trace` holds one record per CTA (TRACE_CTA_SLOTS of them)
 };
 
 // Split-K GEMM with fused epilogue (bf16: tcgen05 + TMA, split-K reduced
@@ -123,6 +124,7 @@ struct alignas(16) AttnArgs {
   int kind;                   // bf16 models: ATTN_TCGEN05 or ATTN_MMA_SYNC
   int* err;                   // device error word (bounded waits), or NULL
   unsigned long long* trace;  // launch timeline record, as GemmArgs::trace
+  int trace_cta;              // as GemmArgs::trace_cta (merge CTAs from slot TRACE_MERGE_SLOT)
 };
 // Tensor-core attention kernels of bf16 models.  ATTN_MMA_SYNC: 64-row tiles
 // on mma.sync.  ATTN_TCGEN05:
@@ -206,6 +208,25 @@ __device__ __forceinline__ void trace_mark(unsigned long long* r, int word) {
   if (word == 0 || word == 1) atomicMin(r + word, t);
   else atomicMax(r + word, t);
   if (word == 1) atomicMax(r + 2, t);
+}
+// Per-CTA timelines (GOCR_OP_TRACE=2): each launch has TRACE_CTA_SLOTS
+// records of TRACE_WORDS words; CTA c of a kernel writes record c (the
+// attention merge kernel from TRACE_MERGE_SLOT on) with plain stores: word
+// 0 start, 1 release from the dependency wait, then the kernel's own marks
+// (GEMMs: 4 mainloop done, 7 accumulator drained, 6 cluster barrier passed,
+// 5 split-K exchange done, 2 epilogue start; attention: 4 first chunk
+// ready, 5 chunk loop done, 6 merge start), 3 end.
+constexpr int TRACE_CTA_SLOTS = 2048;
+constexpr int TRACE_MERGE_SLOT = 1024;
+template <class Args>
+__device__ __forceinline__ void trace_at(const Args& a, int word, int slot0 = 0) {
+  if (!a.trace) return;
+  if (a.trace_cta) {
+    const unsigned cta = slot0 + blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (cta < (unsigned)TRACE_CTA_SLOTS) a.trace[(size_t)cta * TRACE_WORDS + word] = trace_now();
+  } else if (word != 2) {
+    trace_mark(a.trace, word);
+  }
 }
 
 // Library-level error message returned by gocr_last_error(NULL).

@@ -216,6 +216,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // Programmatic dependent launch.
+// Split cluster barrier: every thread of every CTA of the cluster arrives
+// (release: its earlier writes, e.g. barrier initialisation, are visible to
+// the cluster) and later waits (acquire).
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -25,7 +25,8 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 MODE_AR, MODE_SELFSPEC, MODE_DIFFUSION, MODE_REFINED = 0, 1, 2, 3
 FWD_AR, FWD_DRAFT, FWD_VERIFY = 0, 1, 2
 OPT_ATTENTION, OPT_ATTN_RANKS = 5, 6
-TRACE_KERNELS = 1
+TRACE_KERNELS, TRACE_CTAS = 1, 2
+TRACE_CTA_SLOTS = 2048
 ATTN_TCGEN05, ATTN_MMA_SYNC = 0, 1
 MAX_BLOCK = 64
 LAYER_TENSORS = 9
@@ -339,6 +340,14 @@ class Decoder:
         release, last end, last mainloop end, last split-K exchange end; ns)."""
         out = np.zeros((5 * self.cfg.n_layers + 1, 8), np.uint64)
         _check(self.lib.gocr_read_trace(self.h, TRACE_KERNELS, out.ctypes.data, out.size), self.h)
+        return out
+
+    def read_cta_trace(self) -> np.ndarray:
+        """Per-CTA timelines of the last debug forward (GOCR_OP_TRACE=2 at
+        create): uint64 [5 L + 1, 2048, 8]; CTA c of a launch in slot c, the
+        attention merge kernel's CTAs from slot 1024; zero where unreached."""
+        out = np.zeros((5 * self.cfg.n_layers + 1, TRACE_CTA_SLOTS, 8), np.uint64)
+        _check(self.lib.gocr_read_trace(self.h, TRACE_CTAS, out.ctypes.data, out.size), self.h)
         return out
 
     def state(self, req: int):
