@@ -8,7 +8,8 @@ none of the method's arithmetic, are the only thing both sides consume).
 Plain NumPy in float64 by default, with explicit dense mask matrices.
 model.py: the decoder and the masks; decode.py: AR greedy and the
 self-speculative round; diffusion.py: direct block-diffusion decoding and
-rounds with refined drafts.
+rounds with refined drafts; sampling.py: AR sampling and the
+acceptance-rejection round, with the Philox4x32-10 generator.
 
 Parity notes: the pages print no worked numeric example (their B = 4 example
 and their Figure 4 are images missing from the text), so no function here is
@@ -26,6 +27,7 @@ from .decode import (RoundLog, State, accept_length, ar_decode, ar_forward, ar_s
 from .diffusion import (BlockLog, RefinedRoundLog, StepLog, choose_slots, confidence,
                         diffusion_block, diffusion_decode, diffusion_stats, refined_decode,
                         refined_round, refined_stats, window_forward)
+from . import sampling
 
 __all__ = [
     "Model", "argmax_lowest", "attention", "causal_mask", "draft_mask", "forward",
@@ -35,5 +37,5 @@ __all__ = [
     "selfspec_round", "tokens_per_forward", "verify_forward",
     "BlockLog", "RefinedRoundLog", "StepLog", "choose_slots", "confidence", "diffusion_block",
     "diffusion_decode", "diffusion_stats", "refined_decode", "refined_round", "refined_stats",
-    "window_forward",
+    "window_forward", "sampling",
 ]
