@@ -138,6 +138,10 @@ typedef struct gocr_decode_opts {
                            draft-side threshold.  Confidence = the largest softmax
                            probability of a row; a value equal to tau passes. */
   int32_t draft_steps;  /* REFINED: draft forwards per round at most, 1..64 */
+  float temperature;    /* AR, SELFSPEC: 0 = greedy; > 0 = sampling from
+                           softmax(logits / temperature) (see below) */
+  uint32_t reserved;    /* 0 */
+  uint64_t seed;        /* sampling: key of the random numbers */
 } gocr_decode_opts;
 
 /* gocr_decode_batch with every mode, one forward per device-loop iteration
@@ -167,9 +171,28 @@ typedef struct gocr_decode_opts {
  *     draft_steps = 1 is the one-shot round (the same tokens, stats and bits
  *     as GOCR_MODE_SELFSPEC).  Stats: forwards = draft steps + verifies.
  *
- * No forced-acceptance override applies to the block-step modes.
- * Errors as gocr_decode_batch; GOCR_EINVAL for a NaN threshold or
- * draft_steps out of range. */
+ *   Sampling (GOCR_MODE_AR or GOCR_MODE_SELFSPEC with temperature > 0): the
+ *     decode tokens are drawn from softmax(logits / temperature) (the
+ *     prefill token stays the greedy argmax).  Self-speculative rounds then
+ *     use the speculative acceptance-rejection rule (review §2 "Speculative
+ *     Decoding"; the blog: the rule preserves the AR distribution): a0 is
+ *     drawn from the boundary row, d_j from [M] row j (draft distribution
+ *     q_j); verify row j - 1 gives the target p_j; d_j is accepted when a
+ *     uniform u_j < min(1, p_j(d_j) / q_j(d_j)); the first rejection draws
+ *     the replacement from max(0, p_j - q_j) renormalised, B acceptances
+ *     draw the bonus from verify row B; commit and rollback as in the greedy
+ *     round.  Random numbers: Philox4x32-10 (Salmon et al., SC 2011), key
+ *     (seed low word, seed high word), counter (v / 4, position, purpose,
+ *     request slot), lane v % 4, uniform ((x >> 9) + 0.5) / 2^23; a draw is
+ *     a Gumbel-max, argmax of score_v - log(-log u_v) with the lowest index
+ *     among equals; purposes 0 a target token at its position (AR steps, a0,
+ *     the bonus), 1 a draft token, 2 an acceptance uniform (v = 0), 3 a
+ *     replacement; the token at absolute position t uses position t.
+ *
+ * No forced-acceptance override applies to the block-step modes or to
+ * sampling.  Errors as gocr_decode_batch; GOCR_EINVAL for a NaN threshold,
+ * draft_steps out of range, a negative or NaN temperature, or a temperature
+ * with the block-step modes. */
 int gocr_decode_ex(gocr_handle* h, int n_req, const int32_t* reqs, int mode, int B, const gocr_decode_opts* opts,
                    const int32_t* max_new, int32_t* const* out_tokens, gocr_stats* stats);
 

@@ -29,7 +29,8 @@ Readings where the pages are silent (each listed in the design notes):
   implement from that definition: key (seed low, seed high word) and counter
   (v / 4, position, purpose, request), lane v % 4; a draw from a
   distribution is a Gumbel-max over the vocabulary with uniforms
-  u = ((x >> 8) + 0.5) / 2^24; purposes: 0 target token at its position
+  u = ((x >> 9) + 0.5) / 2^23 (exact in fp32, so both sides take the same
+  value: a 25-bit uniform rounds near 1, where -log(-log u) is steep); purposes: 0 target token at its position
   (AR steps, a0, the bonus), 1 draft token, 2 the acceptance uniform (v = 0),
   3 the replacement after a rejection.  The token at absolute position t uses
   position t.
@@ -37,7 +38,7 @@ Readings where the pages are silent (each listed in the design notes):
 from __future__ import annotations
 
 import dataclasses
-from typing import List, Sequence
+from typing import List, Optional, Sequence
 
 import numpy as np
 
@@ -82,14 +83,18 @@ def uniforms(seed: int, req: int, pos: int, purpose: int, n: int) -> np.ndarray:
     ctr[:, 2] = purpose & M32
     ctr[:, 3] = req & M32
     x = philox4x32_10(ctr, (seed & M32, (seed >> 32) & M32)).reshape(-1)[:n].astype(np.float64)
-    return (np.floor(x / 256.0) + 0.5) / float(1 << 24)
+    return (np.floor(x / 512.0) + 0.5) / float(1 << 23)
 
 
-def gumbel_argmax(scores: np.ndarray, u: np.ndarray) -> int:
+def gumbel_argmax(scores: np.ndarray, u: np.ndarray, diag: Optional[list] = None) -> int:
     """argmax over v of scores[v] - log(-log u[v]) (lowest index among equals);
     entries at -inf are never chosen.  With scores = log-probabilities (up to a
-    constant) this is a draw from that distribution."""
+    constant) this is a draw from that distribution.  diag (optional) receives
+    the gap between the two largest perturbed scores (a diagnostic)."""
     g = np.asarray(scores, np.float64) - np.log(-np.log(u))
+    if diag is not None:
+        top = np.sort(g[np.isfinite(g)])
+        diag.append(float(top[-1] - top[-2]) if top.size > 1 else np.inf)
     return int(np.argmax(g))
 
 
@@ -99,22 +104,23 @@ def probs(logits_row: np.ndarray, T: float) -> np.ndarray:
     return z / z.sum()
 
 
-def sample_target(logits_row, T, seed, req, pos) -> int:
+def sample_target(logits_row, T, seed, req, pos, diag: Optional[list] = None) -> int:
     u = uniforms(seed, req, pos, PURPOSE_TARGET, len(logits_row))
-    return gumbel_argmax(np.asarray(logits_row, np.float64) / T, u)
+    return gumbel_argmax(np.asarray(logits_row, np.float64) / T, u, diag)
 
 
 def ar_sample_decode(model: Model, prefix: np.ndarray, max_new: int, T: float, seed: int, req: int = 0,
-                     eos_id: int = -1) -> List[int]:
+                     eos_id: int = -1, diag: Optional[list] = None) -> List[int]:
     """AR sampling: the token at position t drawn from softmax(logits / T) of
-    the row at t - 1 (the prefill token is the greedy argmax)."""
+    the row at t - 1 (the prefill token is the greedy argmax).  diag
+    (optional) receives each draw's top-two perturbed-score gap."""
     st = prefill(model, prefix)
     while not _stopped(st.out, max_new, eos_id):
         p = st.p
         logits, k, v = forward(model, token_rows(model, [st.x0]), [p], st.cache_k, st.cache_v,
                                causal_mask([p], p + 1))
         st.append(k, v)
-        t = sample_target(logits[0], T, seed, req, p + 1)
+        t = sample_target(logits[0], T, seed, req, p + 1, diag)
         st.out.append(t)
         st.x0 = t
     return list(st.out)
@@ -130,6 +136,8 @@ class SampleRoundLog:
     A: int                    # accepted drafts
     last: int                 # the replacement (A < B) or the bonus (A = B)
     committed: List[int]
+    margin: float = np.inf    # smallest top-two perturbed-score gap of the round's draws (diagnostic)
+    accept_gap: float = np.inf  # smallest |u_j - min(1, ratio_j)| of the examined drafts (diagnostic)
 
 
 def accept_reject(drafts: Sequence[int], q_rows: np.ndarray, p_rows: np.ndarray, u_acc: Sequence[float]):
@@ -150,11 +158,14 @@ def accept_reject(drafts: Sequence[int], q_rows: np.ndarray, p_rows: np.ndarray,
     return A, ratios
 
 
-def residual_sample(p_row: np.ndarray, q_row: np.ndarray, u: np.ndarray) -> int:
-    """A draw from max(0, p - q) renormalised (Gumbel-max over its log)."""
+def residual_sample(p_row: np.ndarray, q_row: np.ndarray, u: np.ndarray, diag: Optional[list] = None) -> int:
+    """A draw from max(0, p - q) renormalised (Gumbel-max over its log); from
+    p itself when rounding leaves max(0, p - q) without mass."""
     w = np.maximum(0.0, np.asarray(p_row, np.float64) - np.asarray(q_row, np.float64))
+    if not (w > 0).any():
+        w = np.asarray(p_row, np.float64)
     with np.errstate(divide="ignore"):
-        return gumbel_argmax(np.log(w), u)
+        return gumbel_argmax(np.log(w), u, diag)
 
 
 def selfspec_sample_round(model: Model, st: State, B: int, max_new: int, T: float, seed: int, req: int = 0,
@@ -171,8 +182,10 @@ def selfspec_sample_round(model: Model, st: State, B: int, max_new: int, T: floa
     c = len(st.out)
     V = model.cfg.vocab
     lg_d, kd, vd = draft_forward(model, st, B)
-    a0 = sample_target(lg_d[0], T, seed, req, p + 1)
-    drafts = [gumbel_argmax(lg_d[j] / T, uniforms(seed, req, p + 1 + j, PURPOSE_DRAFT, V)) for j in range(1, B + 1)]
+    gaps: list = []
+    a0 = sample_target(lg_d[0], T, seed, req, p + 1, gaps)
+    drafts = [gumbel_argmax(lg_d[j] / T, uniforms(seed, req, p + 1 + j, PURPOSE_DRAFT, V), gaps)
+              for j in range(1, B + 1)]
     st.append([k[:1] for k in kd], [v[:1] for v in vd])
     rows = token_rows(model, [a0] + drafts)
     pos = np.arange(p + 1, p + B + 2)
@@ -182,9 +195,10 @@ def selfspec_sample_round(model: Model, st: State, B: int, max_new: int, T: floa
     u_acc = [float(uniforms(seed, req, p + 1 + j, PURPOSE_ACCEPT, 1)[0]) for j in range(1, B + 1)]
     A, ratios = accept_reject(drafts, q_rows, p_rows, u_acc)
     if A < B:
-        last = residual_sample(p_rows[A], q_rows[A], uniforms(seed, req, p + 2 + A, PURPOSE_RESIDUAL, V))
+        last = residual_sample(p_rows[A], q_rows[A], uniforms(seed, req, p + 2 + A, PURPOSE_RESIDUAL, V), gaps)
     else:
-        last = sample_target(lg_v[B], T, seed, req, p + B + 2)
+        last = sample_target(lg_v[B], T, seed, req, p + B + 2, gaps)
+    acc_gap = min((abs(u_acc[j] - min(1.0, ratios[j])) for j in range(len(ratios))), default=np.inf)
     commit = ([a0] + drafts[:A] + [last])[: max_new - c]
     if eos_id >= 0 and eos_id in commit:
         commit = commit[: commit.index(eos_id) + 1]
@@ -193,7 +207,7 @@ def selfspec_sample_round(model: Model, st: State, B: int, max_new: int, T: floa
     st.out.extend(commit)
     st.x0 = last
     return SampleRoundLog(p=p, a0=a0, drafts=drafts, accept_u=u_acc, ratio=ratios, A=A, last=last,
-                          committed=commit)
+                          committed=commit, margin=min(gaps), accept_gap=acc_gap)
 
 
 def selfspec_sample_decode(model: Model, prefix: np.ndarray, B: int, max_new: int, T: float, seed: int,

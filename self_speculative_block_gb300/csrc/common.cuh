@@ -64,6 +64,9 @@ struct ReqState {
   float tau;           // confidence threshold (tau_c, or the draft-side tau_d)
   int blk[64];         // slot tokens of the window, -1 = [M] (slot s at position cache_len + 1 + s)
   int win[65];         // refined drafts: the verify window [a0, d1..dB] of the last draft step
+  // sampling decodes: softmax temperature and the random-number seed
+  float temp;
+  unsigned long long seed;
 };
 enum BlockPhase : int { PHASE_STEP = 0, PHASE_WRITE = 1, PHASE_VERIFY = 2 };
 

@@ -87,7 +87,8 @@ struct gocr_handle {
   float* ssq = nullptr;       // per-128-column sums of squares of resid [T][H/128]
   void* q_hi = nullptr;       // rotated query planes [T][q_dim]
   void* q_lo = nullptr;
-  float* logits = nullptr;
+  float* logits = nullptr;     // [T_dec][vocab]: debug forwards, and the draft (or AR) rows of sampling decodes
+  float* logits_v = nullptr;   // [T_dec][vocab]: the verify rows of sampling rounds (allocated on first use)
   float2* conf_part = nullptr;  // LM-head softmax partials [T_dec][vocab / 128] (block-step decodes)
   float* att_part = nullptr;  // attention partial rows of the key-chunk ranks (bf16 models)
   int* att_chunks = nullptr;  // chunks per (slot, kv head x row group) of the last attention
@@ -326,12 +327,34 @@ bool enqueue_forward(gocr_handle* h, int kind, int n_slots, int B, int P, int* a
   return ok;
 }
 
+// Graph-cache modes of the sampling decodes (AR / SELFSPEC with a temperature).
+constexpr int MODE_AR_SAMPLE = 16 + GOCR_MODE_AR, MODE_SELFSPEC_SAMPLE = 16 + GOCR_MODE_SELFSPEC;
+
 // One round (or one AR step) of the decode loop.
 bool enqueue_round(gocr_handle* h, int mode, int B, int n_slots, unsigned long long cond,
                    int use_cond) {
   bool ok = true;
   const int cap = h->cap;
   const int out_stride = cap;
+  const int V = h->cfg.vocab;
+  if (mode == MODE_AR_SAMPLE) {
+    launch_plan(PLAN_AR, h->rows, h->st, h->slot_req, n_slots, 0, 0, nullptr, nullptr, cap, h->hs, h->pdl);
+    ok &= enqueue_forward(h, PLAN_AR, n_slots, 0, 0, h->am, h->logits, h->slot_req);
+    launch_sample_rows(h->st, h->slot_req, n_slots, 1, h->logits, V, h->abuf, h->hs, h->pdl);
+    launch_ar_commit(h->st, h->slot_req, n_slots, h->abuf, h->out, out_stride, h->err, cond, use_cond, h->hs,
+                     h->pdl);
+    return ok;
+  }
+  if (mode == MODE_SELFSPEC_SAMPLE) {
+    launch_plan(PLAN_DRAFT, h->rows, h->st, h->slot_req, n_slots, B, 0, nullptr, nullptr, cap, h->hs, h->pdl);
+    ok &= enqueue_forward(h, PLAN_DRAFT, n_slots, B, 0, h->am, h->logits, h->slot_req);
+    launch_sample_rows(h->st, h->slot_req, n_slots, B + 1, h->logits, V, h->dbuf, h->hs, h->pdl);
+    launch_plan(PLAN_VERIFY, h->rows, h->st, h->slot_req, n_slots, B, 0, h->dbuf, nullptr, cap, h->hs, h->pdl);
+    ok &= enqueue_forward(h, PLAN_VERIFY, n_slots, B, 0, h->vbuf, h->logits_v, h->slot_req);
+    launch_accept_sample(h->st, h->slot_req, n_slots, B, h->dbuf, h->logits, h->logits_v, V, h->out, out_stride,
+                         h->err, cond, use_cond, h->hs, h->pdl);
+    return ok;
+  }
   if (mode == GOCR_MODE_DIFFUSION || mode == GOCR_MODE_REFINED) {
     // one forward per iteration; its rows follow each request's phase
     launch_plan(PLAN_BLOCK, h->rows, h->st, h->slot_req, n_slots, B, 0, nullptr, nullptr, cap, h->hs, h->pdl);
@@ -442,7 +465,8 @@ const char* dev_err_name(int e) {
 }
 
 int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const int* max_new,
-               int32_t* const* out_tokens, gocr_stats* stats, float tau = 0.f, int draft_steps = 1) {
+               int32_t* const* out_tokens, gocr_stats* stats, float tau = 0.f, int draft_steps = 1,
+               float temperature = 0.f, unsigned long long seed = 0) {
   const gocr_config& c = h->cfg;
   if (mode != GOCR_MODE_AR && mode != GOCR_MODE_SELFSPEC && mode != GOCR_MODE_DIFFUSION &&
       mode != GOCR_MODE_REFINED)
@@ -450,6 +474,10 @@ int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const in
   if (n < 1 || n > c.max_requests) return fail(h, GOCR_EINVAL, "bad request count %d", n);
   if (mode != GOCR_MODE_AR && (B < 1 || B > c.max_block))
     return fail(h, GOCR_ECAPACITY, "block size %d outside 1..%d", B, c.max_block);
+  if (!(temperature >= 0.f) || temperature > 1e30f) return fail(h, GOCR_EINVAL, "bad temperature");
+  const bool sampling = temperature > 0.f;
+  if (sampling && mode != GOCR_MODE_AR && mode != GOCR_MODE_SELFSPEC)
+    return fail(h, GOCR_EINVAL, "sampling applies to the AR and self-speculative modes");
   if (mode == GOCR_MODE_DIFFUSION || mode == GOCR_MODE_REFINED) {
     if (!(tau == tau)) return fail(h, GOCR_EINVAL, "threshold is NaN");
     if (mode == GOCR_MODE_REFINED && (draft_steps < 1 || draft_steps > GOCR_MAX_BLOCK))
@@ -487,11 +515,15 @@ int run_decode(gocr_handle* h, int n, const int* reqs, int mode, int B, const in
   if (mode == GOCR_MODE_DIFFUSION) iters = (long long)(B + 1) * ((bound + B - 1) / B) + 2;
   if (mode == GOCR_MODE_REFINED) iters = (long long)(draft_steps + 1) * (bound + 2);
   if (iters > (1 << 30)) iters = 1 << 30;
+  if (sampling && mode == GOCR_MODE_SELFSPEC && !h->logits_v) {
+    h->logits_v = (float*)dev_alloc(h, (size_t)h->T_dec * c.vocab * 4);
+    if (!h->logits_v) return fail(h, GOCR_ENOMEM, "device allocation failed");
+  }
   launch_begin_decode(h->st, h->slot_req, n, h->max_new_dev, (int)iters, c.eos_id, tau,
-                      mode == GOCR_MODE_REFINED ? draft_steps : 1, h->hs);
+                      mode == GOCR_MODE_REFINED ? draft_steps : 1, temperature, seed, h->hs);
   CK(cudaGetLastError());
   cudaGraphExec_t exec;
-  int rc = get_graph(h, mode, B, n, &exec);
+  int rc = get_graph(h, sampling ? 16 + mode : mode, B, n, &exec);
   if (rc) return rc;
   CK(cudaEventRecord(h->ev0, h->hs));
   if (!h->host_loop) {
@@ -793,7 +825,7 @@ int gocr_decode_ex(gocr_handle* h, int n_req, const int32_t* reqs, int mode, int
   int r = sync_user(h);
   if (r) return r;
   return run_decode(h, n_req, reqs, mode, B, max_new, out_tokens, stats, opts ? opts->tau : 0.f,
-                    opts ? opts->draft_steps : 1);
+                    opts ? opts->draft_steps : 1, opts ? opts->temperature : 0.f, opts ? opts->seed : 0ull);
 }
 
 int gocr_set_draft_override(gocr_handle* h, int req, const int32_t* ref_tokens, int n_ref,

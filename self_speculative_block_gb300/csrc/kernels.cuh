@@ -181,7 +181,16 @@ void launch_prefill_finish(ReqState* st, int req, int P, const int* am, int* out
 // Arms request slots for a decode call: max_new, the loop bound, eos, stats
 // reset, and the block-step state (threshold, draft steps, masked slots).
 void launch_begin_decode(ReqState* st, const int* slot_req, int n_slots, const int* max_new,
-                         int max_rounds, int eos_id, float tau, int n_steps, cudaStream_t s);
+                         int max_rounds, int eos_id, float tau, int n_steps, float temp, unsigned long long seed,
+                         cudaStream_t s);
+// Sampling decodes (sampling.cu): Gumbel-max draws of AR or draft rows from
+// the forward's logits [n_slots * rows_per_slot, V]; the acceptance-rejection
+// commit of a sampling round (then the device-loop condition).
+void launch_sample_rows(const ReqState* st, const int* slot_req, int n_slots, int rows_per_slot, const float* logits,
+                        int V, int* out, cudaStream_t s, bool pdl);
+void launch_accept_sample(ReqState* st, const int* slot_req, int n_slots, int B, const int* dbuf, const float* ld,
+                          const float* lv, int V, int* out, int out_stride, const int* err, unsigned long long cond,
+                          int use_cond, cudaStream_t s, bool pdl);
 // The step kernel of a block-step decode (refined = 0: direct block
 // diffusion; 1: self-speculative rounds with refined drafts), after the
 // forward whose LM head wrote argmaxes `am` and confidence partials.

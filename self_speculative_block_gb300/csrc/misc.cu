@@ -10,6 +10,7 @@
 //     a_(A+1) (at most max_new - committed, cut after eos), keeps cache
 //     positions 0..p+A+1 and makes a_(A+1) the next boundary.
 #include "epilogue.cuh"
+#include "round.cuh"
 
 #include <mutex>
 #include <map>
@@ -198,39 +199,6 @@ void launch_plan(int kind, const Rows& r, ReqState* st, const int* slot_req, int
                  int prefill_len, const int* dbuf, const int* toks, int cap, cudaStream_t s, bool pdl) {
   launch_k(plan_kernel, dim3(1), dim3(1024), 0, s, pdl, kind, r, st, slot_req, n_slots, B, prefill_len, dbuf,
            toks, cap);
-}
-
-// ---------------------------------------------------------------- commit helpers
-__device__ void finish_round(ReqState& q, int* out_row, const int* commit, int n_commit, int A,
-                             int new_cache_len, int new_x0, int forwards, const int* err) {
-  const int room = q.max_new - q.committed;
-  int n = n_commit < room ? n_commit : room;
-  bool eos = false;
-  if (q.eos_id >= 0) {
-    for (int i = 0; i < n; ++i)
-      if (commit[i] == q.eos_id) { n = i + 1; eos = true; break; }
-  }
-  for (int i = 0; i < n; ++i) out_row[q.committed + i] = commit[i];
-  q.committed += n;
-  q.cache_len = new_cache_len;
-  q.x0 = new_x0;
-  q.st_rounds += 1;
-  q.st_forwards += forwards;
-  q.st_committed += n;
-  q.st_accepted += A;
-  if (A >= 0 && A <= 64) q.hist[A] += 1;
-  q.round += 1;
-  if (err && *err) { q.error = *err; q.done = 1; }
-  if (q.committed >= q.max_new || eos) q.done = 1;
-  if (!q.done && q.round >= q.max_rounds) { q.error = DERR_ROUND_LIMIT; q.done = 1; }
-}
-
-__device__ void set_loop_condition(ReqState* st, const int* slot_req, int n_slots,
-                                   unsigned long long cond, int use_cond) {
-  if (!use_cond) return;
-  int any = 0;
-  for (int s = 0; s < n_slots; ++s) any |= !st[slot_req[s]].done;
-  cudaGraphSetConditional((cudaGraphConditionalHandle)cond, any ? 1u : 0u);
 }
 
 // One thread per slot, one CTA: updates every request, then sets the loop flag.
@@ -514,7 +482,8 @@ void launch_prefill_finish(ReqState* st, int req, int P, const int* am, int* out
 }
 
 __global__ void begin_decode_kernel(ReqState* st, const int* slot_req, int n_slots,
-                                    const int* max_new, int max_rounds, int eos_id, float tau, int n_steps) {
+                                    const int* max_new, int max_rounds, int eos_id, float tau, int n_steps,
+                                    float temp, unsigned long long seed) {
   const int s = threadIdx.x;
   if (s >= n_slots) return;
   ReqState& q = st[slot_req[s]];
@@ -532,11 +501,15 @@ __global__ void begin_decode_kernel(ReqState* st, const int* slot_req, int n_slo
   q.tau = tau;
   for (int i = 0; i < 64; ++i) q.blk[i] = -1;
   for (int i = 0; i < 65; ++i) q.win[i] = q.x0;
+  q.temp = temp;
+  q.seed = seed;
 }
 
 void launch_begin_decode(ReqState* st, const int* slot_req, int n_slots, const int* max_new,
-                         int max_rounds, int eos_id, float tau, int n_steps, cudaStream_t s) {
-  begin_decode_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, max_new, max_rounds, eos_id, tau, n_steps);
+                         int max_rounds, int eos_id, float tau, int n_steps, float temp, unsigned long long seed,
+                         cudaStream_t s) {
+  begin_decode_kernel<<<1, 64, 0, s>>>(st, slot_req, n_slots, max_new, max_rounds, eos_id, tau, n_steps, temp,
+                                       seed);
 }
 
 __global__ void set_override_kernel(ReqState* st, int req, int n_ref, int n_sched) {

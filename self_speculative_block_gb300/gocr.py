@@ -75,7 +75,8 @@ class Stats(ctypes.Structure):
 
 
 class DecodeOpts(ctypes.Structure):
-    _fields_ = [("tau", ctypes.c_float), ("draft_steps", ctypes.c_int32)]
+    _fields_ = [("tau", ctypes.c_float), ("draft_steps", ctypes.c_int32), ("temperature", ctypes.c_float),
+                ("reserved", ctypes.c_uint32), ("seed", ctypes.c_uint64)]
 
 
 ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p)
@@ -270,17 +271,18 @@ class Decoder:
         return outs, [s.as_dict() for s in sts]
 
     def decode_ex(self, reqs: Sequence[int], mode: int, B: int, max_new: Sequence[int], tau: float = 0.0,
-                  draft_steps: int = 1):
+                  draft_steps: int = 1, temperature: float = 0.0, seed: int = 0):
         """Any decode mode over several requests; MODE_DIFFUSION takes the
         confidence threshold tau, MODE_REFINED the draft-side threshold tau and
-        at most draft_steps draft forwards per round."""
+        at most draft_steps draft forwards per round; MODE_AR and MODE_SELFSPEC
+        sample at temperature > 0 with the random-number key seed."""
         n = len(reqs)
         r = _i32(reqs)
         mn = _i32(max_new)
         outs = [np.zeros(int(m), np.int32) for m in max_new]
         optr = (ctypes.POINTER(ctypes.c_int32) * n)(*[_p32(o) for o in outs])
         sts = (Stats * n)()
-        opts = DecodeOpts(float(tau), int(draft_steps))
+        opts = DecodeOpts(float(tau), int(draft_steps), float(temperature), 0, int(seed))
         _check(self.lib.gocr_decode_ex(self.h, n, _p32(r), mode, B, ctypes.byref(opts), _p32(mn), optr, sts),
                self.h)
         return outs, [s.as_dict() for s in sts]
