@@ -318,6 +318,29 @@ int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void*
                       const void* v_hi, const void* v_lo, float* o, const int32_t* lim, int T, int Hq, int Hkv,
                       int d, int cap, void* stream);
 
+/* gocr_op_attention with a second key interval per row: row t reads keys
+ * 0..lim[t] and lo2[t]..hi2[t] (none when hi2[t] < lo2[t]); lo2, hi2:
+ * device int32[T], both NULL = the plain call.  The bf16 path runs the
+ * mma.sync tile kernel (whatever GOCR_ATTN says). */
+int gocr_op_attention_ranges(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
+                             const void* v_hi, const void* v_lo, float* o, const int32_t* lim, const int32_t* lo2,
+                             const int32_t* hi2, int T, int Hq, int Hkv, int d, int cap, void* stream);
+
+/* Row key intervals of the joint AR / block-diffusion training attention
+ * (GravityOCR review §3.1 "Joint AR-Diffusion Training"; the Trillion Labs
+ * blog's three-stream figure): one forward over the packed sequence
+ * [prefix (P), clean response (N), corrupted stream 1 (N), corrupted stream
+ * 2 (N)], responses cut into blocks of B tokens.  The prefix (image and
+ * prompt, never corrupted) and the clean stream are causal; a token of block
+ * b of a corrupted stream reads the prefix, the clean blocks before b and
+ * the whole of its own corrupted block b (bidirectional), and nothing of the
+ * other corrupted stream, of its own stream's other blocks, or of clean
+ * block b and later.  Host outputs, [P + 3 N] each: lim, lo2, hi2 as
+ * gocr_op_attention_ranges reads them, and pos (or NULL) the rotary
+ * position of each row (a stream's response token i sits at P + i).
+ * GOCR_EINVAL for negative sizes, B < 1, or a null output. */
+int gocr_three_stream_ranges(int P, int N, int B, int32_t* lim, int32_t* lo2, int32_t* hi2, int32_t* pos);
+
 /* ---- allocation-free GEMM ------------------------------------------------ */
 
 /* Bytes of the device scratch array behind gocr_op_linear_static (per GPU). */

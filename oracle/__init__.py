@@ -19,7 +19,7 @@ constructions and the method's own invariants (exact AR equivalence, commit
 bounds, the causal-cache invariant) in the CPU tests.
 """
 from .model import (Model, argmax_lowest, attention, causal_mask, draft_mask, forward,
-                    prefill_cache, rmsnorm, rope, silu, softmax_masked, token_rows,
+                    prefill_cache, rmsnorm, rope, silu, softmax_masked, three_stream_mask, token_rows,
                     top2_margin, verify_mask)
 from .decode import (RoundLog, State, accept_length, ar_decode, ar_forward, ar_step,
                      draft_forward, forced_override, prefill, round_stats, selfspec_decode,
@@ -31,7 +31,8 @@ from . import sampling
 
 __all__ = [
     "Model", "argmax_lowest", "attention", "causal_mask", "draft_mask", "forward",
-    "prefill_cache", "rmsnorm", "rope", "silu", "softmax_masked", "token_rows", "top2_margin",
+    "prefill_cache", "rmsnorm", "rope", "silu", "softmax_masked", "three_stream_mask", "token_rows",
+    "top2_margin",
     "verify_mask", "RoundLog", "State", "accept_length", "ar_decode", "ar_forward", "ar_step",
     "draft_forward", "forced_override", "prefill", "round_stats", "selfspec_decode",
     "selfspec_round", "tokens_per_forward", "verify_forward",

@@ -125,6 +125,44 @@ def verify_mask(p: int, B: int) -> np.ndarray:
     return causal_mask(np.arange(p + 1, p + B + 2), p + B + 2)
 
 
+def three_stream_mask(P: int, N: int, B: int) -> np.ndarray:
+    """Attention mask of the joint AR / block-diffusion training forward over
+    the packed sequence [prefix (P), clean response (N), corrupted stream 1
+    (N), corrupted stream 2 (N)] (review §3.1 "Joint AR-Diffusion Training";
+    the blog's three-stream figure).
+
+    Rows and columns index the packed sequence.  Written from the rule text,
+    entry by entry:
+    * the prefix (image and prompt, never corrupted) is causal;
+    * the clean stream sees the prefix and its own earlier tokens (causal);
+    * a token of block b of a corrupted stream sees the prefix, the clean
+      blocks before b, and every token of its own block b of its own stream
+      (bidirectional inside the block); not clean block b or later, not its
+      stream's other blocks, not the other corrupted stream.
+    """
+    L = P + 3 * N
+    m = np.zeros((L, L), dtype=bool)
+
+    def where(r):
+        if r < P:
+            return "prefix", r, -1
+        s, i = divmod(r - P, N)
+        return ("clean" if s == 0 else f"corrupt{s}"), i, i // B
+
+    for q in range(L):
+        qs, qi, qb = where(q)
+        for k in range(L):
+            ks, ki, kb = where(k)
+            if qs == "prefix":
+                ok = ks == "prefix" and k <= q
+            elif qs == "clean":
+                ok = ks == "prefix" or (ks == "clean" and ki <= qi)
+            else:
+                ok = ks == "prefix" or (ks == "clean" and kb < qb) or (ks == qs and kb == qb)
+            m[q, k] = ok
+    return m
+
+
 # --------------------------------------------------------------------------
 # forward over a window of rows, given the cache for keys before the window
 # --------------------------------------------------------------------------

@@ -79,10 +79,13 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
   const int t = row0 + (valid ? gi / G : 0);
   const int hq = kvh * G + (valid ? gi % G : 0);
   const int lim = valid ? a.row_lim[t] : -1;
+  const int lo2 = valid && a.row_lo2 ? a.row_lo2[t] : 1;
+  const int hi2 = valid && a.row_hi2 ? a.row_hi2[t] : 0;
 
   if (i == 0) s_maxlim = -1;
   __syncthreads();
   if (valid) atomicMax(&s_maxlim, lim);
+  if (valid && hi2 >= lo2) atomicMax(&s_maxlim, hi2);
   for (int dd = 0; dd < D; ++dd) {
     Qs[i * (D + 1) + dd] = valid ? qf[((size_t)t * a.Hq + hq) * D + dd] : 0.f;
     Os[i * (D + 1) + dd] = 0.f;
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
     float mc = -INFINITY;
 #pragma unroll
     for (int j = 0; j < CH; ++j) {
-      if (kbase + j <= lim) {
+      if (kbase + j <= lim || (kbase + j >= lo2 && kbase + j <= hi2)) {
         float dot = 0.f;
 #pragma unroll 1
         for (int dd = 0; dd < D; ++dd) dot = fmaf(Qs[i * (D + 1) + dd], Ks[j * D + dd], dot);
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
 // every context length, dispatch first.  Ranks whose first chunk lies past
 // the group's last visible key exit after the row limits are read; the others
 // write their partial rows to a.part.
-template <int D, bool TRACE>
+template <int D, bool TRACE, bool R2 = false>
 __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
   using Gm = attn::Geo<D>;
   constexpr int RLD = Gm::RLD;
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
     attn::cp_async_wait<0>();
     return;
   }
-  const int n_chunks = attn::tile_partial<D, TRACE>(a, sm_raw, grp, attn::kv_planes(a, req, kvh, D), rank, R, kvh,
+  const int n_chunks = attn::tile_partial<D, TRACE, R2>(a, sm_raw, grp, attn::kv_planes(a, req, kvh, D), rank, R, kvh,
                                                     qr0, row0, nrows, pre, &s_maxlim, kv_kmax);
   if (rank == 0 && tid == 0) a.part_chunks[(size_t)slot * gridDim.x + group] = n_chunks;
   if (rank >= n_chunks) return;
@@ -299,30 +302,33 @@ static bool launch_attn_tc_t(const AttnArgs& a, int n_slots, int max_rows, cudaS
   return launch_attn_merge<D, attn_tc::QR, TRACE>(a, R, a.Hkv * n_rg, n_slots, s);
 }
 
-template <int D, bool TRACE>
+template <int D, bool TRACE, bool R2 = false>
 static bool launch_attn_mma_t(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
   const int G = a.Hq / a.Hkv;
   const int n_rg = (max_rows * G + attn::QR - 1) / attn::QR;
-  if (!kernel_smem_at_least(reinterpret_cast<const void*>(attention_part_kernel<D, TRACE>),
-                            attn::Geo<D>::TILE_SMEM))
+  const size_t smem = R2 ? attn::Geo<D>::TILE_SMEM_R2 : attn::Geo<D>::TILE_SMEM;
+  if (!kernel_smem_at_least(reinterpret_cast<const void*>(attention_part_kernel<D, TRACE, R2>), smem))
     return false;
   cudaLaunchConfig_t cfg{};
   const int R = a.ranks > 0 ? a.ranks : attention_ranks(a.cap, 1);
   cfg.gridDim = dim3(a.Hkv * n_rg, R, n_slots);
   cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = attn::Geo<D>::TILE_SMEM;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, attention_part_kernel<D, TRACE>, a) != cudaSuccess) return false;
+  if (cudaLaunchKernelEx(&cfg, attention_part_kernel<D, TRACE, R2>, a) != cudaSuccess) return false;
   return launch_attn_merge<D, attn::QR, TRACE>(a, R, a.Hkv * n_rg, n_slots, s);
 }
 
 template <int D>
 static bool launch_attn_mma(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
+  // rows with a second key interval (the joint-training mask) run the
+  // mma.sync tile's R2 instantiation
+  if (a.row_lo2) return launch_attn_mma_t<D, false, true>(a, n_slots, max_rows, s, pdl);
   if (a.kind == ATTN_TCGEN05)
     return a.trace ? launch_attn_tc_t<D, true>(a, n_slots, max_rows, s, pdl)
                    : launch_attn_tc_t<D, false>(a, n_slots, max_rows, s, pdl);

@@ -34,6 +34,8 @@ template <int D> struct Geo {
   static constexpr size_t KV_BYTES = (size_t)4 * TILE * 2;
   static constexpr size_t LIM_BYTES = QR * 4;
   static constexpr size_t TILE_SMEM = Q_BYTES + KV_BYTES + LIM_BYTES + 16;
+  // tiles with a second key interval per row: its bounds after the limits
+  static constexpr size_t TILE_SMEM_R2 = TILE_SMEM + 2 * LIM_BYTES;
   // the staged partial rows (CL x RPC = QR rows) live where K/V were
   static_assert((size_t)QR * RLD * 4 <= KV_BYTES, "staged rows fit the K/V region");
   static_assert((size_t)QR * OLD * 4 + 2 * QR * 4 <= Q_BYTES, "half-1 partial fits the Q region");
@@ -148,7 +150,9 @@ __device__ __forceinline__ float* staged_rows(uint8_t* sm) {
 // up to kv_kmax right away, together with Q, instead of after the rows' key
 // limits are known.  Keys past a row's limit contribute exact zeros either
 // way.
-template <int D, bool TRACE = false>
+// R2: rows also read a second key interval (a.row_lo2 / a.row_hi2), whose
+// bounds sit in TILE_SMEM_R2's extra shared memory.
+template <int D, bool TRACE = false, bool R2 = false>
 __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, const KvPlanes& kv, int rank,
                             int stride, int kvh, int qr0, int row0, int nrows, bool pre, int* s_maxlim,
                             int kv_kmax = -1) {
@@ -158,6 +162,8 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   bf16* Ql = Qh + QR * QLD;
   bf16* KV = Ql + QR * QLD;                             // {Kh, Kl, Vh, Vl} [AC][QLD]
   int* Lim = reinterpret_cast<int*>(sm + Gm::Q_BYTES + Gm::KV_BYTES);  // [QR]
+  int* Lo2 = Lim + QR;                                  // [QR] (R2 only)
+  int* Hi2 = Lo2 + QR;                                  // [QR] (R2 only)
   float* Oh = reinterpret_cast<float*>(Qh);             // [QR][OLD] half-1 partial (Q is dead by then)
   float* Mh = Oh + QR * OLD;                            // [QR]
   float* Lh = Mh + QR;                                  // [QR]
@@ -194,6 +200,16 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
     if (gi < nq) lim = min(a.row_lim[row0 + gi / G], a.cap - 1);
     Lim[tid] = lim;
     if (lim >= 0) atomicMax(s_maxlim, lim);
+    if (R2) {
+      int lo2 = 1, hi2 = 0;
+      if (gi < nq) {
+        lo2 = max(a.row_lo2[row0 + gi / G], 0);
+        hi2 = min(a.row_hi2[row0 + gi / G], a.cap - 1);
+      }
+      Lo2[tid] = lo2;
+      Hi2[tid] = hi2;
+      if (hi2 >= lo2) atomicMax(s_maxlim, hi2);
+    }
   }
   grp.sync();
   const int maxlim = *s_maxlim;
@@ -206,6 +222,8 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
 
   const int r_lo = mt * 16 + g, r_hi = r_lo + 8;
   const int lim_lo = Lim[r_lo], lim_hi = Lim[r_hi];
+  const int a_lo = R2 ? Lo2[r_lo] : 1, b_lo = R2 ? Hi2[r_lo] : 0;
+  const int a_hi = R2 ? Lo2[r_hi] : 1, b_hi = R2 ? Hi2[r_hi] : 0;
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
   float oacc[D / 8][4];
 #pragma unroll
@@ -272,8 +290,10 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = kbase + nt * 8 + tq * 2 + e;
-        float s0 = key <= lim_lo ? sacc[nt][e] * sl2 : -INFINITY;
-        float s1 = key <= lim_hi ? sacc[nt][2 + e] * sl2 : -INFINITY;
+        const bool in_lo = key <= lim_lo || (R2 && key >= a_lo && key <= b_lo);
+        const bool in_hi = key <= lim_hi || (R2 && key >= a_hi && key <= b_hi);
+        float s0 = in_lo ? sacc[nt][e] * sl2 : -INFINITY;
+        float s1 = in_hi ? sacc[nt][2 + e] * sl2 : -INFINITY;
         sacc[nt][e] = s0;
         sacc[nt][2 + e] = s1;
         mc_lo = fmaxf(mc_lo, s0);
@@ -390,27 +410,6 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   }
   grp.sync();
   return n_chunks;
-}
-
-// Chunks of a (request, kv head, row group) tile set: the last key any of
-// its 64 rows reads decides how many ranks hold partial rows.  All 64 rows'
-// limits are read, by the group's first 64 threads; s_maxlim is shared.
-__device__ __forceinline__ int tile_chunks(const AttnArgs& a, const Grp& grp, int qr0, int row0, int nrows,
-                                           int* s_maxlim) {
-  const int G = a.Hq / a.Hkv;
-  if (grp.tid == 0) *s_maxlim = -1;
-  grp.sync();
-  if (grp.tid < QR) {
-    const int gi = qr0 + grp.tid;
-    if (gi < nrows * G) {
-      const int lim = min(a.row_lim[row0 + gi / G], a.cap - 1);
-      if (lim >= 0) atomicMax(s_maxlim, lim);
-    }
-  }
-  grp.sync();
-  const int maxlim = *s_maxlim;
-  grp.sync();
-  return maxlim < 0 ? 0 : maxlim / AC + 1;
 }
 
 // Merge of tile rows i0 and i0 + step (cnt = 1 or 2 of them, < QR) from the

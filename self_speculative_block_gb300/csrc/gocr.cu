@@ -1083,7 +1083,41 @@ int gocr_op_linear_planes(const void* x_hi, const void* x_lo, const void* w, flo
 int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
                       const void* v_hi, const void* v_lo, float* o, const int32_t* lim, int T, int Hq, int Hkv,
                       int d, int cap, void* stream) {
+  return gocr_op_attention_ranges(dtype, q_hi, q_lo, k_hi, k_lo, v_hi, v_lo, o, lim, nullptr, nullptr, T, Hq, Hkv,
+                                  d, cap, stream);
+}
+
+int gocr_three_stream_ranges(int P, int N, int B, int32_t* lim, int32_t* lo2, int32_t* hi2, int32_t* pos) {
+  if (P < 0 || N < 0 || B < 1 || (long long)P + 3LL * N > (1 << 28)) return fail(nullptr, GOCR_EINVAL, "bad sizes");
+  if (!lim || !lo2 || !hi2) return fail(nullptr, GOCR_EINVAL, "null argument");
+  for (int r = 0; r < P + 3 * N; ++r) {
+    int l, a = 1, b = 0, p;
+    if (r < P) {                     // image + prompt prefix: causal
+      l = r;
+      p = r;
+    } else if (r < P + N) {          // clean response stream: causal over prefix and clean tokens
+      l = r;
+      p = r;
+    } else {                         // corrupted stream s, response token i of block blk
+      const int s = (r - P) / N, i = (r - P) % N, blk = i / B;
+      l = P + blk * B - 1;           // the prefix and the clean blocks before this one
+      a = P + s * N + blk * B;       // its own corrupted block, bidirectionally
+      b = P + s * N + (N < (blk + 1) * B ? N : (blk + 1) * B) - 1;
+      p = P + i;
+    }
+    lim[r] = l;
+    lo2[r] = a;
+    hi2[r] = b;
+    if (pos) pos[r] = p;
+  }
+  return GOCR_OK;
+}
+
+int gocr_op_attention_ranges(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
+                             const void* v_hi, const void* v_lo, float* o, const int32_t* lim, const int32_t* lo2,
+                             const int32_t* hi2, int T, int Hq, int Hkv, int d, int cap, void* stream) {
   gocr_handle* h = nullptr;
+  if ((lo2 == nullptr) != (hi2 == nullptr)) return fail(h, GOCR_EINVAL, "lo2 and hi2 come together");
   if (dtype != GOCR_DTYPE_F32 && dtype != GOCR_DTYPE_BF16) return fail(h, GOCR_EINVAL, "bad dtype");
   if (!q_hi || !k_hi || !v_hi || !o || !lim) return fail(h, GOCR_EINVAL, "null pointer");
   if (dtype == GOCR_DTYPE_BF16 && (!q_lo || !k_lo || !v_lo)) return fail(h, GOCR_EINVAL, "missing lo plane");
@@ -1093,6 +1127,7 @@ int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void*
   a.q_hi = q_hi; a.q_lo = q_lo; a.k_hi = k_hi; a.k_lo = k_lo; a.v_hi = v_hi; a.v_lo = v_lo;
   a.req_stride = 0; a.o_hi = o; a.o_lo = nullptr; a.out_bf16 = 0;
   a.row_lim = lim; a.plan = nullptr;
+  a.row_lo2 = lo2; a.row_hi2 = hi2;
   a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.cap = cap; a.scale = 1.0f / sqrtf((float)d);
   {
     const char* ak = getenv("GOCR_ATTN");

@@ -111,6 +111,9 @@ struct alignas(16) AttnArgs {
   void* o_hi; void* o_lo;  // output planes [T, Hq*d] (bf16 hi/lo, or fp32 in o_hi)
   int out_bf16;            // output planes are bf16 (1) or fp32 (0)
   const int* row_lim;      // [T]
+  // optional second key interval per row (the joint-training mask): row t
+  // also reads keys row_lo2[t]..row_hi2[t] (empty when hi2 < lo2); NULL = none
+  const int* row_lo2; const int* row_hi2;
   const Plan* plan;        // slot layout; NULL = one slot of T rows, request 0
   // decode launches: the slot table and request states, constant during a
   // forward, let CTAs fetch committed cache chunks before the dependency wait

@@ -36,7 +36,7 @@ EXPORTS = ("gocr_create", "gocr_prefill", "gocr_decode", "gocr_decode_batch", "g
            "gocr_set_draft_override", "gocr_debug_forward", "gocr_debug_forward_batch", "gocr_read_kv", "gocr_get_state",
            "gocr_get_option", "gocr_read_trace", "gocr_last_error", "gocr_free",
            "gocr_op_linear_workspace", "gocr_op_linear", "gocr_op_linear_planes", "gocr_op_attention",
-           "gocr_op_linear_static")
+           "gocr_op_linear_static", "gocr_op_attention_ranges", "gocr_three_stream_ranges")
 
 
 class GocrError(RuntimeError):
@@ -118,6 +118,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "gocr_op_linear_planes": (i32, [vp, vp, vp, vp, i32, i32, i32, vp, sz, ctypes.c_uint, vp]),
         "gocr_op_attention": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
         "gocr_op_linear_static": (i32, [i32, vp, vp, vp, i32, i32, i32, vp]),
+        "gocr_op_attention_ranges": (i32, [i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
+        "gocr_three_stream_ranges": (i32, [i32, i32, i32, P32, P32, P32, P32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -422,12 +424,23 @@ def op_linear_static(x, w):
     return y
 
 
-def op_attention(q, kc, vc, lim, dtype: int):
+def three_stream_ranges(P: int, N: int, B: int):
+    """Row key intervals (lim, lo2, hi2) and rotary positions of the joint
+    training mask over [prefix, clean, corrupted 1, corrupted 2] (host int32
+    arrays of P + 3 N), from the library."""
+    n = P + 3 * N
+    lim, lo2, hi2, pos = (np.zeros(n, np.int32) for _ in range(4))
+    _check(load().gocr_three_stream_ranges(P, N, B, _p32(lim), _p32(lo2), _p32(hi2), _p32(pos)))
+    return lim, lo2, hi2, pos
+
+
+def op_attention(q, kc, vc, lim, dtype: int, lo2=None, hi2=None):
     """The decoder's attention kernel for `dtype` (DTYPE_BF16 / DTYPE_F32).
 
     q [T, Hq, d], kc and vc [Hkv, cap, d]: fp32 tensors for DTYPE_F32, or
     (hi, lo) pairs of bf16 tensors for DTYPE_BF16; lim int32 [T] on the
-    device.  Returns fp32 [T, Hq, d]."""
+    device; lo2, hi2 (optional) int32 [T] on the device: a second key
+    interval per row.  Returns fp32 [T, Hq, d]."""
     torch = _torch()
     lib = load()
     pair = lambda t: (t[0], t[1]) if isinstance(t, (tuple, list)) else (t, None)
@@ -437,6 +450,6 @@ def op_attention(q, kc, vc, lim, dtype: int):
     o = torch.empty((T, Hq, d), dtype=torch.float32, device=qh.device)
     ptr = lambda t: t.data_ptr() if t is not None else None
     stream = torch.cuda.current_stream(qh.device).cuda_stream
-    _check(lib.gocr_op_attention(dtype, ptr(qh), ptr(ql), ptr(kh), ptr(kl), ptr(vh), ptr(vl), o.data_ptr(),
-                                 lim.data_ptr(), T, Hq, Hkv, d, cap, stream))
+    _check(lib.gocr_op_attention_ranges(dtype, ptr(qh), ptr(ql), ptr(kh), ptr(kl), ptr(vh), ptr(vl), o.data_ptr(),
+                                        lim.data_ptr(), ptr(lo2), ptr(hi2), T, Hq, Hkv, d, cap, stream))
     return o

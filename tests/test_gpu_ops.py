@@ -156,3 +156,26 @@ def test_attention_row_bits_do_not_depend_on_other_rows(g, monkeypatch, dt):
     for j in (0, 1, 31, 64):
         one = g.op_attention(_planes(qn[j:j + 1], dtype), k, v, lim[j:j + 1].contiguous(), dtype)
         assert torch.equal(one[0], full[j]), j
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("P,N,B,Hq,Hkv,d", [(5, 24, 8, 4, 2, 64), (40, 90, 32, 12, 4, 128), (0, 33, 7, 12, 4, 128),
+                                            (130, 200, 32, 6, 2, 128)])
+def test_attention_three_stream_training_mask(g, dt, P, N, B, Hq, Hkv, d):
+    """The joint-training mask (review §3.1; blog three-stream figure) as a
+    second key interval per row, against the oracle's mask built from the
+    rule text, over the packed [prefix, clean, corrupted 1, corrupted 2]."""
+    rng = np.random.default_rng(P + N + B + d)
+    L = P + 3 * N
+    dtype = g.DTYPE_F32 if dt == "f32" else g.DTYPE_BF16
+    tol = 2e-5 if dt == "f32" else 5e-3
+    lim, lo2, hi2, _ = g.three_stream_ranges(P, N, B)
+    q = rng.standard_normal((L, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((Hkv, L, d)).astype(np.float32)
+    v = rng.standard_normal((Hkv, L, d)).astype(np.float32)
+    ref = oracle.attention(q.astype(np.float64), k.transpose(1, 0, 2).astype(np.float64),
+                           v.transpose(1, 0, 2).astype(np.float64), oracle.three_stream_mask(P, N, B))
+    dev = lambda a: torch.from_numpy(a).cuda()
+    o = g.op_attention(_planes(q, dtype), _planes(k, dtype), _planes(v, dtype), dev(lim), dtype,
+                       lo2=dev(lo2), hi2=dev(hi2)).cpu().numpy()
+    np.testing.assert_allclose(o, ref, rtol=tol, atol=tol)
