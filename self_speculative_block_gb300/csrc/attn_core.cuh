@@ -432,12 +432,27 @@ __device__ void merge_rows(const AttnArgs& a, const Grp& grp, const Part& part, 
   const int G = a.Hq / a.Hkv;
   const int nq = nrows * G;
   auto ld = [&](const float* p) -> float { return GLOBAL ? __ldcg(p) : *p; };
-  if (warp < cnt) {
-    const int k = warp;
+  // thread: residue q = tid / 64 of the ranks, output quad (row k, d4) = tid % 64
+  const int q = tid >> 6, slot = tid & 63, k = slot / (D / 4), d4 = (slot % (D / 4)) * 4;
+  // the (at most 16) partials of this residue: every rank slot is loaded,
+  // before n_ranks is used, so that these loads, the (max, sum) loads below
+  // and the caller's share one round trip; slots past n_ranks are not added
+  float4 v[16];
+  if (k < cnt) {
     const int i = i0 + k * step;
-    // every rank slot's (max, sum) is read before n_ranks is used, so the
-    // loads share one round trip with the caller's; slots past n_ranks hold
-    // stale values and are masked
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int c = q + 4 * u;
+      if (c < r_all)
+        v[u] = GLOBAL ? __ldcg(reinterpret_cast<const float4*>(part(c, i) + d4))
+                      : *reinterpret_cast<const float4*>(part(c, i) + d4);
+    }
+  }
+  if (warp < cnt) {
+    const int kw = warp;
+    const int i = i0 + kw * step;
+    // every rank slot's (max, sum) is read before n_ranks is used; slots
+    // past n_ranks hold stale values and are masked
     const float lm0 = lane < r_all ? ld(part(lane, i) + D) : 0.f;
     const float lm1 = lane + 32 < r_all ? ld(part(lane + 32, i) + D) : 0.f;
     const float ll0 = lane < r_all ? ld(part(lane, i) + D + 1) : 0.f;
@@ -453,25 +468,14 @@ __device__ void merge_rows(const AttnArgs& a, const Grp& grp, const Part& part, 
     L += w1 * (lane + 32 < n_ranks ? ll1 : 0.f);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    WS[k * 64 + lane] = w0;
-    WS[k * 64 + lane + 32] = w1;
-    if (lane == 0) IL[k] = L > 0.f ? 1.f / L : 0.f;
+    WS[kw * 64 + lane] = w0;
+    WS[kw * 64 + lane + 32] = w1;
+    if (lane == 0) IL[kw] = L > 0.f ? 1.f / L : 0.f;
   }
   grp.sync();
-  // thread: residue q = tid / 64 of the ranks, output quad (row k, d4) = tid % 64
-  const int q = tid >> 6, slot = tid & 63, k = slot / (D / 4), d4 = (slot % (D / 4)) * 4;
   if (k < cnt) {
-    const int i = i0 + k * step;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    // the (at most 16) partials of this residue load together, then add in rank order
-    float4 v[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int c = q + 4 * u;
-      if (c < n_ranks)
-        v[u] = GLOBAL ? __ldcg(reinterpret_cast<const float4*>(part(c, i) + d4))
-                      : *reinterpret_cast<const float4*>(part(c, i) + d4);
-    }
+    // add in rank order
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       const int c = q + 4 * u;

@@ -131,6 +131,44 @@ __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int 
     const bool first = g0 == 0;
     const float* rs = rs_in ? rs_in + g0 : rs_s;
     const float* rr = rr_in ? rr_in + (size_t)g0 * NTILE : rr_s;
+    if (EPI == EPI_ARGMAX && !e.logits && !e.conf_part && grp.n >= 4 * EPI_GROUP) {
+      // argmax alone: four threads per token scan the tile's columns q, q + 4,
+      // ... in increasing order (a strict > keeps the lowest index among
+      // equal maxima) and merge with the same rule: the tokens run side by
+      // side instead of one warp reduction per token
+      const int tl = tid >> 2, q = tid & 3;
+      const bool act = tl < gn;
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      int nan = 0;
+      if (act) {
+        const float r = norm ? rs[tl] : 1.f;
+        const float* yrow = Ys + (size_t)(g0 + tl) * ys_ld;
+#pragma unroll 8
+        for (int k = 0; k < NTILE / 4; ++k) {
+          const int c = q + 4 * k, n = n0 + c;
+          const float v = yrow[c] * r;
+          if (n < a.N) {
+            nan |= v != v;
+            argmax_merge(bv, bi, v, n);
+          }
+        }
+      }
+      // every lane of the warp takes part; inactive lanes hold (-inf, none)
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+        argmax_merge(bv, bi, ov, oi);
+      }
+      if (act && q == 0) {
+        if (nan) set_err(e.err, DERR_NAN_LOGITS);
+        if (bi != 0x7fffffff) atomicMax(e.amax + t0 + g0 + tl, argmax_key(bv, bi));
+      }
+      grp.sync();
+      continue;
+    }
     for (int tl = warp; tl < gn; tl += nwarp) {
       const int t = t0 + g0 + tl;
       const float r = norm ? rs[tl] : 1.f;

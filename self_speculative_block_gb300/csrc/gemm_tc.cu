@@ -282,13 +282,30 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   const bool pre_rope = EPI == EPI_QKV && a.e.head_dim <= NTILE;  // [EG][head_dim / 2] float2 fits rr_pre
   if (warp >= 2) {
     // warps 2 and 3 have no mainloop role: fetch the epilogue's inputs now
+    // (the residual rows as one batch of loads, issued with the norm partials)
     const int it = tid - 64;
+    constexpr int RR4 = EG * NTILE / 4 / 64;  // residual float4 per thread
+    float4 rr[EPI == EPI_RESID ? RR4 : 1];
+    const int n4 = pre_n * (NTILE / 4);
+    if (EPI == EPI_RESID) {
+#pragma unroll
+      for (int u = 0; u < RR4; ++u) {
+        const int x = it + 64 * u;
+        if (x < n4)
+          rr[u] = *reinterpret_cast<const float4*>(a.e.resid + (size_t)(t0 + ea + x / (NTILE / 4)) * a.e.H + n0 +
+                                                   (x % (NTILE / 4)) * 4);
+      }
+    }
     if (a.e.ssq_in)
       for (int tl = it; tl < tn; tl += 64)
         rs_all[tl] = row_rstd(a.e, a.e.in_rows ? a.e.in_rows[t0 + tl] : t0 + tl);
-    if (EPI == EPI_RESID)
-      for (int x = it; x < pre_n * NTILE; x += 64)
-        rr_pre[x] = a.e.resid[(size_t)(t0 + ea + x / NTILE) * a.e.H + n0 + x % NTILE];
+    if (EPI == EPI_RESID) {
+#pragma unroll
+      for (int u = 0; u < RR4; ++u) {
+        const int x = it + 64 * u;
+        if (x < n4) reinterpret_cast<float4*>(rr_pre)[x] = rr[u];
+      }
+    }
     if (EPI == EPI_QKV) {
       if (it < pre_n) {
         const int t = t0 + ea + it;
