@@ -209,12 +209,13 @@ __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int 
           break;
         }
         case EPI_QKV: {
-          const int d = e.head_dim, half = d >> 1;
+          // head_dim is 64 or 128: index arithmetic by shifts and masks
+          const int d = e.head_dim, half = d >> 1, dsh = d == 128 ? 7 : 6, dm = d - 1;
           const bool pq = first && pre.pos;
           const int pos = pq ? pre.pos[tl] : e.row_pos[t];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const int c = lane + 32 * j, n = n0 + c, jj = n % d;
+            const int c = lane + 32 * j, n = n0 + c, jj = n & dm;
             float out = v[j];
             if (n < e.q_dim + e.kv_dim) {  // q and k are rotated, v is not
               const int ri = jj < half ? jj : jj - half;
@@ -229,7 +230,7 @@ __device__ inline void apply_epilogue_k(const GemmArgs& a, const float* Ys, int 
               if (pos < 0 || pos >= e.cap) { set_err(e.err, DERR_CAPACITY); continue; }
               const bool is_k = n < e.q_dim + e.kv_dim;
               const int nn = is_k ? n - e.q_dim : n - e.q_dim - e.kv_dim;
-              const size_t off = (size_t)req * e.req_stride + ((size_t)(nn / d) * e.cap + pos) * d + nn % d;
+              const size_t off = (size_t)req * e.req_stride + (((size_t)(nn >> dsh) * e.cap + pos) << dsh) + (nn & dm);
               if (is_k) put_plane(e.k_hi, e.k_lo, e.plane_bf16, off, out);
               else put_plane(e.v_hi, e.v_lo, e.plane_bf16, off, out);
             }

@@ -284,6 +284,12 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     // warps 2 and 3 have no mainloop role: fetch the epilogue's inputs now
     // (the residual rows as one batch of loads, issued with the norm partials)
     const int it = tid - 64;
+    // QKV: the rows' positions and slots go out with the norm partials
+    int pos_l = 0, slot_l = 0;
+    if (EPI == EPI_QKV && it < pre_n) {
+      pos_l = a.e.row_pos[t0 + ea + it];
+      slot_l = a.e.row_slot[t0 + ea + it];
+    }
     constexpr int RR4 = EG * NTILE / 4 / 64;  // residual float4 per thread
     float4 rr[EPI == EPI_RESID ? RR4 : 1];
     const int n4 = pre_n * (NTILE / 4);
@@ -308,9 +314,8 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
     }
     if (EPI == EPI_QKV) {
       if (it < pre_n) {
-        const int t = t0 + ea + it;
-        pos_pre[it] = a.e.row_pos[t];
-        req_pre[it] = a.e.plan->slot_req[a.e.row_slot[t]];
+        pos_pre[it] = pos_l;
+        req_pre[it] = a.e.plan->slot_req[slot_l];
       }
       asm volatile("bar.sync 1, 64;" ::: "memory");  // warps 2 and 3 only
       if (pre_rope) {
