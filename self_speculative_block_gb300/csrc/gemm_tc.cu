@@ -474,6 +474,160 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
   if (TRACE && tid == 0) trace_at(a, 3);
 }
 
+// Streaming variant for wide matrices without split K at decode shapes (the
+// LM head: 512 weight tiles, at most 64 tokens): two CTAs per SM walk the
+// tiles tile0, tile0 + gridDim.x, ... with one TMA ring that runs across tile
+// boundaries, so the weight stream does not stop between tiles or waves.
+// Warp 0 lane 0 loads, warp 1 lane 0 issues the MMAs into one of two tensor
+// memory accumulators (tile i uses buffer i % 2), warps 2..5 drain an
+// accumulator into shared memory and run the epilogue while the next tile's
+// MMAs run.  The MMAs, the drain (hi + lo columns) and the epilogue are those
+// of gemm_tc_kernel, so the results are the same bits.
+constexpr int STREAM_THREADS = 192;
+template <int EPI, bool TRACE>
+__global__ void __launch_bounds__(STREAM_THREADS, 2)
+    gemm_tc_stream_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx_hi,
+                          const __grid_constant__ CUtensorMap tmx_lo, GemmArgs a, int nt, int stages) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int b_bytes = 2 * nt * 128;
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + stages * A_BYTES;
+  float* Yp = reinterpret_cast<float*>(sB + stages * b_bytes);  // [nt][YLD] drained accumulator
+  float* rs_all = Yp + nt * YLD;                                 // [TZ_TC] rstd of the tokens
+  uint64_t* full = reinterpret_cast<uint64_t*>(rs_all + TZ_TC);
+  uint64_t* empty = full + stages;
+  uint64_t* tfull = empty + stages;   // [2] accumulator written
+  uint64_t* tempty = tfull + 2;       // [2] accumulator drained
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  __shared__ int s_fail;
+  __shared__ int s_efail;  // written by the epilogue warps only, read by them after their barrier
+  __shared__ int s_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles = cdiv_i(a.N, NTILE);
+  const int my_tiles = n_tiles > (int)blockIdx.x ? cdiv_i(n_tiles - (int)blockIdx.x, (int)gridDim.x) : 0;
+  const int nkb = cdiv_i(a.K, 64);
+  const int total = my_tiles * nkb;  // k-blocks this CTA streams
+  const int tn = min(TZ_TC, a.T);
+  const int nmma = 2 * nt;
+  const uint32_t ncols = nmma <= 32 ? 32 : (nmma <= 64 ? 64 : 128);  // per accumulator (nt <= 64)
+
+  if (tid == 0) {
+    if (TRACE) trace_at(a, 0);
+    tc::prefetch_tmap(&tmw);
+    tc::prefetch_tmap(&tmx_hi);
+    tc::prefetch_tmap(&tmx_lo);
+    for (int s = 0; s < stages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], 128);
+    }
+    tc::fence_mbar_init();
+    s_fail = 0;
+    s_efail = 0;
+    tc::grid_dep_launch();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_holder, 2 * ncols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_holder;
+
+  if (tid == 0) {
+    // TMA producer: the weight tiles of the first stages go out before the
+    // grid dependency wait, the token planes after it
+    const uint64_t pol = tc::policy_evict_first();
+    const int pre = total < stages ? total : stages;
+    for (int it = 0; it < pre; ++it) {
+      const int tile = blockIdx.x + (it / nkb) * gridDim.x, kb = it % nkb;
+      tc::mbar_expect_tx(&full[it], A_BYTES + b_bytes);
+      tc::tma_load_2d_hint(sA + it * A_BYTES, &tmw, kb * 64, tile * NTILE, &full[it], pol);
+    }
+    tc::grid_dep_wait();
+    if (TRACE) trace_at(a, 1);
+    for (int it = 0; it < total; ++it) {
+      const int s = it % stages, use = it / stages;
+      const int tile = blockIdx.x + (it / nkb) * gridDim.x, kb = it % nkb;
+      if (it >= pre) {
+        if (!tc::mbar_wait(&empty[s], (use - 1) & 1)) { s_fail = 1; break; }
+        tc::mbar_expect_tx(&full[s], A_BYTES + b_bytes);
+        tc::tma_load_2d_hint(sA + s * A_BYTES, &tmw, kb * 64, tile * NTILE, &full[s], pol);
+      }
+      uint8_t* b = sB + s * b_bytes;
+      tc::tma_load_2d(b, &tmx_hi, kb * 64, 0, &full[s]);
+      tc::tma_load_2d(b + nt * 128, &tmx_lo, kb * 64, 0, &full[s]);
+    }
+  } else if (tid == 32) {
+    // MMA issuer: tile i accumulates in buffer i % 2 once the epilogue has
+    // drained that buffer's previous tile
+    const uint32_t idesc = tc::idesc_bf16(NTILE, nmma);
+    int it = 0;
+    for (int li = 0; li < my_tiles && !s_fail; ++li) {
+      const int buf = li & 1;
+      if (li >= 2 && !tc::mbar_wait(&tempty[buf], ((li >> 1) - 1) & 1)) { s_fail = 1; break; }
+      tc::fence_after_sync();
+      const uint32_t acc = tmem + (uint32_t)buf * ncols;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % stages, use = it / stages;
+        if (!tc::mbar_wait(&full[s], use & 1)) { s_fail = 1; break; }
+        tc::fence_after_sync();
+        const uint32_t a_base = tc::smem_u32(sA + s * A_BYTES);
+        const uint32_t b_base = tc::smem_u32(sB + s * b_bytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_bf16(acc, tc::sdesc_sw128(a_base + kk * 32), tc::sdesc_sw128(b_base + kk * 32), idesc,
+                       (kb > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(&empty[s]);
+      }
+      tc::mma_commit(&tfull[buf]);
+    }
+  } else if (warp >= 2) {
+    // epilogue warps: warp w drains tensor-memory lanes 32 (w % 4) .. +31
+    const Grp eg{tid - 64, 128, 1};
+    const int q = warp & 3, row = q * 32 + lane;
+    tc::grid_dep_wait();  // the norm partials are written by the previous kernel
+    if (a.e.ssq_in)
+      for (int tl = eg.tid; tl < tn; tl += 128)
+        rs_all[tl] = row_rstd(a.e, a.e.in_rows ? a.e.in_rows[tl] : tl);
+    eg.sync();
+    for (int li = 0; li < my_tiles; ++li) {
+      const int buf = li & 1, tile = blockIdx.x + li * gridDim.x;
+      const bool ok = tc::mbar_wait(&tfull[buf], (li >> 1) & 1);
+      tc::fence_after_sync();
+      const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)buf * ncols;
+      for (int g = 0; g < nt / 16; ++g) {
+        float vh[16], vl[16];
+        tc::tmem_ld16(acc + g * 16, vh);
+        tc::tmem_ld16(acc + nt + g * 16, vl);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) Yp[(g * 16 + j) * YLD + row] = ok ? vh[j] + vl[j] : 0.f;
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&tempty[buf]);  // this lane's accumulator columns are read
+      if (!ok) s_efail = 1;
+      eg.sync();
+      if (s_efail) break;  // the same decision in every epilogue thread
+      // the row scales come prefetched, so the epilogue needs no scratch
+      for (int g0 = 0; g0 < tn; g0 += EG) {
+        EpiPre pre;
+        pre.rs = a.e.ssq_in ? rs_all + g0 : nullptr;
+        apply_epilogue_k<EPI>(a, Yp + g0 * YLD, YLD, tile, g0, min(EG, tn - g0), nullptr, pre, eg);
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  const bool failed = s_fail || s_efail;
+  if (failed && tid == 0) set_err(a.e.err, DERR_TIMEOUT);
+  if (warp == 1) tc::tmem_dealloc(tmem, 2 * ncols);
+  if (EPI == EPI_ARGMAX && !failed) argmax_grid_finish(a, &s_flag);
+  if (TRACE && tid == 0) trace_at(a, 3);
+}
+
 // Many-slice variant (more than two 128-token slices, e.g. prefill and the
 // batched round): one CTA per (128-row weight tile, NT-token slice) runs the S
 // K chunks of the split rule one after another.  Each chunk's MMAs start a
@@ -876,6 +1030,36 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
                             yl.ys, yl.scratch, -1, EG) == cudaSuccess;
 }
 
+// Two CTAs per SM (at most the tile count), the deepest ring that keeps
+// two CTAs' shared memory on one SM.
+template <int EPI, bool TRACE>
+static bool launch_gemm_tc_stream(const GemmArgs& a, cudaStream_t s, bool pdl) {
+  CUtensorMap tmw, tmh, tml;
+  const int nt = (a.T + 15) / 16 * 16;
+  if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE) || !tmap_2d(&tmh, a.x, a.T, a.K, nt) ||
+      !tmap_2d(&tml, a.x_lo, a.T, a.K, nt))
+    return false;
+  const int stage_bytes = A_BYTES + 2 * nt * 128;
+  const size_t fixed = 1024 + (size_t)nt * YLD * 4 + TZ_TC * 4 + 64 + 16;
+  int stages = (int)((TWO_CTA_SMEM - fixed) / (stage_bytes + 16));
+  if (stages > 8) stages = 8;
+  if (stages < 2) return false;
+  const size_t smem = fixed + (size_t)stages * (stage_bytes + 16);
+  if (!kernel_smem_at_least(reinterpret_cast<const void*>(gemm_tc_stream_kernel<EPI, TRACE>), smem)) return false;
+  const int n_tiles = cdiv_i(a.N, NTILE);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(n_tiles < 2 * SM_COUNT ? n_tiles : 2 * SM_COUNT);
+  cfg.blockDim = dim3(STREAM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_stream_kernel<EPI, TRACE>, tmw, tmh, tml, a, nt, stages) == cudaSuccess;
+}
+
 // Launches of more than two 128-token slices of hi + lo planes run the K
 // chunks in one CTA (gemm_tc_seq_kernel); the others split them over a
 // cluster.  Both add the chunk sums in chunk order.
@@ -890,6 +1074,9 @@ static int seq_slice_tokens() {
 
 template <int EPI>
 static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
+  // the LM head at decode shapes (up to 64 tokens): streaming CTAs instead of waves of tile CTAs
+  if (EPI == EPI_ARGMAX && a.splits == 1 && a.T <= 64 && a.x_lo && !getenv_flag("GOCR_LM_WAVES"))
+    return a.trace ? launch_gemm_tc_stream<EPI, true>(a, s, pdl) : launch_gemm_tc_stream<EPI, false>(a, s, pdl);
   if (cdiv_i(a.T, TZ_TC) > 2 && a.x_lo) {
     if (seq_slice_tokens() == 128)
       return a.trace ? launch_gemm_tc_seq<EPI, true, 128>(a, s, pdl) : launch_gemm_tc_seq<EPI, false, 128>(a, s, pdl);
