@@ -95,7 +95,7 @@ struct gocr_handle {
   unsigned long long* amax = nullptr;
   int* grid_ctr = nullptr;
   bool pdl = true;            // programmatic dependent launch between forward kernels
-  bool l2_prefetch = true;    // GEMMs prefetch the next GEMM's weights into L2 (GOCR_L2_PREFETCH=0: off)
+  bool l2_prefetch = false;   // GEMMs prefetch the next GEMM's weights into L2 (GOCR_L2_PREFETCH=1: on)
   bool host_loop = false;     // GOCR_HOST_LOOP=1: per-round graphs driven by the host
   int* dbuf = nullptr;
   int* vbuf = nullptr;
@@ -278,7 +278,7 @@ void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_o
   gl.e.conf_part = conf_part;
   gl.e.amax = h->amax; gl.e.am_out = am_out; gl.e.grid_ctr = h->grid_ctr;
   f.g.push_back(gl);
-  // each GEMM brings the next GEMM's weights into L2 (at most 48 MB of them)
+  // GOCR_L2_PREFETCH=1: each GEMM brings the next GEMM's weights into L2 (at most 48 MB of them)
   if (h->l2_prefetch)
     for (size_t i = 0; i + 1 < f.g.size(); ++i) {
       const GemmArgs& nx = f.g[i + 1];
@@ -621,7 +621,7 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     const char* hl = getenv("GOCR_HOST_LOOP");
     h->host_loop = hl && hl[0] == '1';
     const char* lp = getenv("GOCR_L2_PREFETCH");
-    h->l2_prefetch = !(lp && lp[0] == '0');
+    h->l2_prefetch = lp && lp[0] == '1';  // off: measured faster at the decode shapes
     // key-chunk ranks by the rule; GOCR_ATTN_RANKS=<n> replaces the rule's count
     h->attn_ranks = attention_ranks(h->cap, c.max_requests);
     // handles that batch requests run their batched GEMMs on the many-slice
