@@ -102,7 +102,10 @@ typedef struct gocr_handle gocr_handle;
 /* Create a decoder on the current CUDA device.
  *   stream      cudaStream_t every launch goes to (NULL = legacy default).
  *   alloc/free  device allocator; both NULL = cudaMalloc/cudaFree.
- * Returns GOCR_EINVAL for an unsupported shape, GOCR_ENOMEM, GOCR_ECUDA. */
+ * Returns GOCR_EINVAL for an unsupported shape (including more than 64 q
+ * heads per kv head, or more than 2^20 attention rows (token, q head) in one
+ * forward: max(max_ctx, max_requests x (max_block + 1)) x q heads per kv
+ * head), GOCR_ENOMEM, GOCR_ECUDA. */
 int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream,
                 gocr_alloc_fn alloc, gocr_free_fn free_fn, void* alloc_user,
                 gocr_handle** out);
@@ -311,7 +314,8 @@ int gocr_op_linear_planes(const void* x_hi, const void* x_lo, const void* w, flo
  * with the lo pointers NULL.  q [T, Hq, d], k and v [Hkv, cap, d] (device);
  * o [T, Hq, d] fp32 (device); lim: device int32[T], row t reads keys
  * 0..lim[t] (draft: row 0 = p, rows 1..B = p+B; verify/AR: the row's own
- * position).  d in {64, 128}.  GOCR_DTYPE_BF16 keeps its partial rows in a
+ * position).  d in {64, 128}; Hq / Hkv <= 64 and T x Hq / Hkv <= 2^20
+ * (GOCR_EINVAL otherwise).  GOCR_DTYPE_BF16 keeps its partial rows in a
  * device scratch buffer of the library (one per device, allocated or grown
  * by the first call that needs more): calls that overlap on the GPU race. */
 int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,

@@ -78,6 +78,12 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// floor(n / g) for 0 <= n < 2^20 and 1 <= g <= 64 by a multiply-high with
+// gm = floor((2^32 - 1) / g) + 1 (exact in that range; g = 1 passes n through).
+__device__ __forceinline__ int div_small(int n, int g, unsigned gm) {
+  return g == 1 ? n : (int)__umulhi((unsigned)n, gm);
+}
+
 // Cache planes of one (request, kv head): K hi, K lo, V hi, V lo.
 struct KvPlanes {
   const bf16* p[4];
@@ -185,26 +191,30 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
     load_planes<D>(KV, kv, 2, 2, rank, kv_kmax, tid);
   }
   // Q planes of this row group (zero past the window) and the rows' key limits
+  const unsigned gm = 0xFFFFFFFFu / (unsigned)G + 1u;
   for (int x = tid; x < 2 * QR * (D / 8); x += 256) {
     const int pl = x / (QR * (D / 8)), rem = x % (QR * (D / 8));
     const int r = rem / (D / 8), v = rem % (D / 8);
     const int gi = qr0 + r;
     size_t src = 0;
-    if (gi < nq) src = ((size_t)(row0 + gi / G) * a.Hq + kvh * G + gi % G) * D + v * 8;
+    if (gi < nq) {
+      const int tq = div_small(gi, G, gm);
+      src = ((size_t)(row0 + tq) * a.Hq + kvh * G + (gi - tq * G)) * D + v * 8;
+    }
     cp_async16((pl ? Ql : Qh) + r * QLD + v * 8, (pl ? ql : qh) + src, gi < nq ? 16 : 0);
   }
   cp_async_commit();
   if (tid < QR) {
     const int gi = qr0 + tid;
     int lim = -1;
-    if (gi < nq) lim = min(a.row_lim[row0 + gi / G], a.cap - 1);
+    if (gi < nq) lim = min(a.row_lim[row0 + div_small(gi, G, gm)], a.cap - 1);
     Lim[tid] = lim;
     if (lim >= 0) atomicMax(s_maxlim, lim);
     if (R2) {
       int lo2 = 1, hi2 = 0;
       if (gi < nq) {
-        lo2 = max(a.row_lo2[row0 + gi / G], 0);
-        hi2 = min(a.row_hi2[row0 + gi / G], a.cap - 1);
+        lo2 = max(a.row_lo2[row0 + div_small(gi, G, gm)], 0);
+        hi2 = min(a.row_hi2[row0 + div_small(gi, G, gm)], a.cap - 1);
       }
       Lo2[tid] = lo2;
       Hi2[tid] = hi2;

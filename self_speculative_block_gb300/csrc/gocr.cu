@@ -587,6 +587,12 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
   if (c.max_block < 1 || c.max_block > GOCR_MAX_BLOCK || c.max_requests < 1 || c.max_requests > MAX_REQ ||
       c.max_ctx < c.max_block + 4 || c.max_ctx > (1 << 20) || c.eos_id >= c.vocab)
     return fail(nullptr, GOCR_EINVAL, "bad capacity settings");
+  {
+    // attention rows (token, q head) of one forward are indexed below 2^20 with at most 64 q heads per kv head
+    const long long rows = c.max_ctx > c.max_requests * (c.max_block + 1) ? c.max_ctx : c.max_requests * (c.max_block + 1);
+    if (c.n_q_heads / c.n_kv_heads > 64 || rows * (c.n_q_heads / c.n_kv_heads) > (1 << 20))
+      return fail(nullptr, GOCR_EINVAL, "more attention rows than supported (q heads per kv head x rows > 2^20)");
+  }
   if (!w->embed || !w->mask_embed || !w->lm_head || !w->g_final || !w->layer)
     return fail(nullptr, GOCR_EINVAL, "null weight pointer");
   for (int i = 0; i < c.n_layers * GOCR_LAYER_TENSORS; ++i)
@@ -1121,7 +1127,8 @@ int gocr_op_attention_ranges(int dtype, const void* q_hi, const void* q_lo, cons
   if (dtype != GOCR_DTYPE_F32 && dtype != GOCR_DTYPE_BF16) return fail(h, GOCR_EINVAL, "bad dtype");
   if (!q_hi || !k_hi || !v_hi || !o || !lim) return fail(h, GOCR_EINVAL, "null pointer");
   if (dtype == GOCR_DTYPE_BF16 && (!q_lo || !k_lo || !v_lo)) return fail(h, GOCR_EINVAL, "missing lo plane");
-  if (T < 1 || Hkv < 1 || Hq % Hkv || (d != 64 && d != 128) || cap < 1)
+  if (T < 1 || Hkv < 1 || Hq % Hkv || Hq / Hkv > 64 || (long long)T * (Hq / Hkv) > (1 << 20) || (d != 64 && d != 128) ||
+      cap < 1)
     return fail(h, GOCR_EINVAL, "bad shape");
   AttnArgs a{};
   a.q_hi = q_hi; a.q_lo = q_lo; a.k_hi = k_hi; a.k_lo = k_lo; a.v_hi = v_hi; a.v_lo = v_lo;
