@@ -508,7 +508,8 @@ __device__ void merge_rows(const AttnArgs& a, const Grp& grp, const Part& part, 
       const float il = IL[k];
       const float ox = ((s0.x + s1.x) + s2.x) + s3.x, oy = ((s0.y + s1.y) + s2.y) + s3.y;
       const float oz = ((s0.z + s1.z) + s2.z) + s3.z, ow = ((s0.w + s1.w) + s2.w) + s3.w;
-      const int t = row0 + gi / G, hq = kvh * G + gi % G;
+      const int tq = div_small(gi, G, 0xFFFFFFFFu / (unsigned)G + 1u);
+      const int t = row0 + tq, hq = kvh * G + (gi - tq * G);
       const size_t o = ((size_t)t * a.Hq + hq) * D + d4;
       put_plane(a.o_hi, a.o_lo, a.out_bf16, o, ox * il);
       put_plane(a.o_hi, a.o_lo, a.out_bf16, o + 1, oy * il);

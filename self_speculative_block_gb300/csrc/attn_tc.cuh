@@ -191,19 +191,23 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
     // Q planes of the row group (swizzled; zero past the window) and the row limits
     const bf16* qp[2] = {reinterpret_cast<const bf16*>(a.q_hi), reinterpret_cast<const bf16*>(a.q_lo)};
     constexpr int CPR = D / 8;
+    const unsigned gm = 0xFFFFFFFFu / (unsigned)G + 1u;
     for (int x = tid; x < 2 * QR * CPR; x += THREADS) {
       const int pl = x / (QR * CPR), rem = x % (QR * CPR);
       const int r = rem / CPR, v = rem % CPR;
       const int gi = qr0 + r;
       size_t src = 0;
-      if (gi < nq) src = ((size_t)(row0 + gi / G) * a.Hq + kvh * G + gi % G) * D + v * 8;
+      if (gi < nq) {
+        const int tq = attn::div_small(gi, G, gm);
+        src = ((size_t)(row0 + tq) * a.Hq + kvh * G + (gi - tq * G)) * D + v * 8;
+      }
       attn::cp_async16(sm + Gm::OFF_Q + pl * Gm::Q_PLANE + (v >> 3) * (QR * 128) + sw128(r, v & 7), qp[pl] + src,
                        gi < nq ? 16 : 0);
     }
     if (tid < QR) {
       const int gi = qr0 + tid;
       int lim = -1;
-      if (gi < nq) lim = min(a.row_lim[row0 + gi / G], a.cap - 1);
+      if (gi < nq) lim = min(a.row_lim[row0 + attn::div_small(gi, G, gm)], a.cap - 1);
       Lim[tid] = lim;
       if (lim >= 0) atomicMax(&s_maxlim, lim);
     }
