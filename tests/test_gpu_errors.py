@@ -2,9 +2,10 @@
 
 * Lowest index on ties: an LM head with two identical rows gives two bitwise
   equal logits; when they are the row maximum, the committed token is the
-  lower index (the argmax reading shared with the oracle).  Checked for both
-  GEMM paths (bf16 tcgen05, fp32 CUDA cores), with the tied rows in one
-  128-row weight tile and in two tiles.
+  lower index (the argmax reading shared with the oracle).  Checked for the
+  GEMM paths (bf16 tcgen05: the streaming LM-head kernel of decode shapes and,
+  with GOCR_LM_WAVES=1, the tile-CTA kernel that larger forwards use; fp32 CUDA
+  cores), with the tied rows in one 128-row weight tile and in two tiles.
 * NaN logits are a device error: a NaN placed in a weight on the host comes
   back as GOCR_EDEVICE from the call whose forward met it, with no fault, and
   other handles keep working.
@@ -29,7 +30,7 @@ def lib():
 
 
 def _cfg(synth, dt):
-    if dt == "bf16":
+    if dt.startswith("bf16"):
         return synth.ModelConfig(n_layers=2, hidden=512, n_q_heads=6, n_kv_heads=2, head_dim=128, ffn=1024,
                                  vocab=2048, dtype=synth.BF16)
     return synth.TINY
@@ -47,9 +48,17 @@ def _first_token(g, cfg, W, prefix):
         dec.close()
 
 
-@pytest.mark.parametrize("dt", ["bf16", "f32"])
-def test_argmax_ties_go_to_the_lowest_index(lib, dt):
+def _lm_kernel(monkeypatch, dt):
+    if dt == "bf16-waves":
+        monkeypatch.setenv("GOCR_LM_WAVES", "1")
+    else:
+        monkeypatch.delenv("GOCR_LM_WAVES", raising=False)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "bf16-waves", "f32"])
+def test_argmax_ties_go_to_the_lowest_index(lib, monkeypatch, dt):
     g, synth = lib
+    _lm_kernel(monkeypatch, dt)
     cfg = _cfg(synth, dt)
     W = synth.make_weights(cfg, seed=31)
     for seed in range(40, 60):
@@ -70,10 +79,11 @@ def test_argmax_ties_go_to_the_lowest_index(lib, dt):
         assert lgb[j].view(np.uint32) == lgb[t0].view(np.uint32)
 
 
-@pytest.mark.parametrize("dt", ["bf16", "f32"])
+@pytest.mark.parametrize("dt", ["bf16", "bf16-waves", "f32"])
 @pytest.mark.parametrize("where", ["lm_head", "wo"])
-def test_nan_weight_is_a_device_error(lib, dt, where):
+def test_nan_weight_is_a_device_error(lib, monkeypatch, dt, where):
     g, synth = lib
+    _lm_kernel(monkeypatch, dt)
     cfg = _cfg(synth, dt)
     W = synth.make_weights(cfg, seed=33)
     prefix = synth.make_prefix(cfg, 24, seed=3)
