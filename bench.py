@@ -413,7 +413,7 @@ def in_situ_gemm(cfg, W, wl, dev, hbm, round_us):
     launch_us = round_us / 2 * share / n
     alg = gemm_launch_bytes(cfg, B + 1)
     ach = alg / (launch_us * 1e-6) / 1e9
-    return {"kernel": "gemm_tc_kernel (tcgen05 split-K GEMM, fused epilogues) in the decode forward",
+    return {"kernel": "decode-forward GEMMs: gemm_tc_kernel (tcgen05 split-K, fused epilogues) and the LM head on gemm_tc_stream_kernel",
             "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
             "traffic": profiled_traffic("draft_forward"), "launch_us": launch_us, "algorithmic_bytes": alg,
             "gemm_share_of_forward": share, "launches_per_forward": n, "trace_run_us": run_us,

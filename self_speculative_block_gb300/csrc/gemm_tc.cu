@@ -1075,8 +1075,10 @@ static int seq_slice_tokens() {
 template <int EPI>
 static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
   // the LM head at decode shapes (up to 64 tokens): streaming CTAs instead of waves of tile CTAs
-  if (EPI == EPI_ARGMAX && a.splits == 1 && a.T <= 64 && a.x_lo && !getenv_flag("GOCR_LM_WAVES"))
-    return a.trace ? launch_gemm_tc_stream<EPI, true>(a, s, pdl) : launch_gemm_tc_stream<EPI, false>(a, s, pdl);
+  if constexpr (EPI == EPI_ARGMAX) {
+    if (a.splits == 1 && a.T <= 64 && a.x_lo && !getenv_flag("GOCR_LM_WAVES"))
+      return a.trace ? launch_gemm_tc_stream<EPI, true>(a, s, pdl) : launch_gemm_tc_stream<EPI, false>(a, s, pdl);
+  }
   if (cdiv_i(a.T, TZ_TC) > 2 && a.x_lo) {
     if (seq_slice_tokens() == 128)
       return a.trace ? launch_gemm_tc_seq<EPI, true, 128>(a, s, pdl) : launch_gemm_tc_seq<EPI, false, 128>(a, s, pdl);
