@@ -32,6 +32,7 @@
 // writes).  The result is written as the O projection's input planes.
 // fp32 models: CUDA-core kernel with one CTA sweeping every chunk.
 #include <cstdlib>
+#include <cstring>
 
 #include "attn_core.cuh"
 #include "attn_tc.cuh"
@@ -154,11 +155,14 @@ __global__ void __launch_bounds__(ROWS) attention_simt_kernel(AttnArgs a) {
 // the group's last visible key exit after the row limits are read; the others
 // write their partial rows to a.part.
 template <int D, bool TRACE, bool R2 = false>
-__global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(256, 2)
+    attention_part_kernel(const __grid_constant__ attn::KvMaps tms, AttnArgs a) {
   using Gm = attn::Geo<D>;
   constexpr int RLD = Gm::RLD;
-  extern __shared__ __align__(16) uint8_t sm_raw[];
+  extern __shared__ __align__(16) uint8_t sm_in[];
+  uint8_t* sm_raw = attn::tile_base(sm_in);
   __shared__ int s_maxlim;
+  __shared__ __align__(8) uint64_t s_kbar, s_vbar;  // a chunk's K, V landed
   const Grp grp = Grp::block();
   const int group = blockIdx.x, rank = blockIdx.y, R = gridDim.y;
   const int slot = blockIdx.z;
@@ -168,15 +172,23 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
 
   if (tid == 0) {
     if (TRACE) trace_at(a, 0);
+    tc::mbar_init(&s_kbar, 1);
+    tc::mbar_init(&s_vbar, 1);
+    tc::fence_mbar_init();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   }
+  __syncthreads();
+  // cache row of key 0 of this CTA's (request, kv head): the planes' tensor
+  // maps span every request and layer
+  auto kv_row = [&](int req) { return a.kv_row0 + (long long)req * a.kv_req_rows + (long long)kvh * a.cap; };
   // committed cache before the dependency wait (decode launches only)
   int req_pre = -1, kv_kmax = -1;
   bool pre = false;
   if (a.st && a.slot_req) {
     req_pre = a.slot_req[slot];
     const int pc = a.st[req_pre].cache_len;
-    pre = attn::tile_prefetch<D>(sm_raw, attn::kv_planes(a, req_pre, kvh, D), rank, R, pc, tid);
+    pre = attn::tile_prefetch<D>(sm_raw, tms, attn::kv_planes(a, req_pre, kvh, D), kv_row(req_pre), rank, R, pc,
+                                 tid, &s_kbar, &s_vbar);
     // no row of this forward reads past the round-start length plus its rows
     kv_kmax = min(a.cap - 1, pc + a.rows_per_slot);
   }
@@ -195,11 +207,12 @@ __global__ void __launch_bounds__(256, 2) attention_part_kernel(AttnArgs a) {
   }
   const int qr0 = rg * attn::QR;
   if (qr0 >= nrows * G) {  // uniform: a row group past the window
-    attn::cp_async_wait<0>();
+    if (pre && !(tc::mbar_wait(&s_kbar, 0) && tc::mbar_wait(&s_vbar, 0)) && tid == 0)
+      set_err(a.err, DERR_TIMEOUT);  // no copy outlives the CTA
     return;
   }
-  const int n_chunks = attn::tile_partial<D, TRACE, R2>(a, sm_raw, grp, attn::kv_planes(a, req, kvh, D), rank, R, kvh,
-                                                    qr0, row0, nrows, pre, &s_maxlim, kv_kmax);
+  const int n_chunks = attn::tile_partial<D, TRACE, R2>(a, sm_raw, grp, tms, kv_row(req), &s_kbar, &s_vbar, rank, R,
+                                                        kvh, qr0, row0, nrows, pre, &s_maxlim, kv_kmax);
   if (rank == 0 && tid == 0) a.part_chunks[(size_t)slot * gridDim.x + group] = n_chunks;
   if (rank >= n_chunks) return;
   // all 64 rows, also those past the window (which the merge reads but does
@@ -304,6 +317,9 @@ static bool launch_attn_tc_t(const AttnArgs& a, int n_slots, int max_rows, cudaS
 
 template <int D, bool TRACE, bool R2 = false>
 static bool launch_attn_mma_t(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
+  if (!a.kv_maps) return false;
+  attn::KvMaps tms;
+  memcpy(&tms, a.kv_maps, sizeof(tms));
   const int G = a.Hq / a.Hkv;
   const int n_rg = (max_rows * G + attn::QR - 1) / attn::QR;
   const size_t smem = R2 ? attn::Geo<D>::TILE_SMEM_R2 : attn::Geo<D>::TILE_SMEM;
@@ -320,7 +336,7 @@ static bool launch_attn_mma_t(const AttnArgs& a, int n_slots, int max_rows, cuda
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, attention_part_kernel<D, TRACE, R2>, a) != cudaSuccess) return false;
+  if (cudaLaunchKernelEx(&cfg, attention_part_kernel<D, TRACE, R2>, tms, a) != cudaSuccess) return false;
   return launch_attn_merge<D, attn::QR, TRACE>(a, R, a.Hkv * n_rg, n_slots, s);
 }
 

@@ -14,8 +14,14 @@
 // unchanged, so a row's result does not depend on the other rows.  q and the
 // KV cache are bf16 hi + lo planes: QK^T takes qh kh + qh kl + ql kh and PV
 // takes P vh + P vl on mma.sync tiles (P in bf16), accumulating in fp32.
+// K and V chunks come into shared memory by TMA (128-byte swizzled 32 x 64
+// boxes of the cache planes, counted on one mbarrier for K and one for V);
+// q rows by cp.async.
 #pragma once
+#include <cuda.h>
+
 #include "epilogue.cuh"
+#include "tc.cuh"
 
 namespace gocr {
 namespace attn {
@@ -25,21 +31,55 @@ constexpr int AC = 32;      // keys per chunk
 constexpr float LOG2E = 1.4426950408889634f;
 
 template <int D> struct Geo {
-  static constexpr int QLD = D + 8;    // bf16 row stride of the Q, K and V tiles
+  static constexpr int QLD = D + 8;    // bf16 row stride of the Q tiles
   static constexpr int OLD = D + 4;    // fp32 row stride of the half-1 partial
-  static constexpr int TILE = AC * QLD;
+  static constexpr int KVP = AC * D;   // bf16 elements of one K/V chunk plane (swizzled 128-byte rows)
   static constexpr int RLD = D + 4;    // fp32 stride of a partial row: D outputs, max, sum, pad
-  // shared memory of one tile: Q planes, the four K/V chunk planes, row limits
+  // shared memory of one tile (from a 1024-byte aligned base): Q planes, the
+  // four K/V chunk planes (their region also holds the staged partial rows),
+  // row limits; 1024 bytes of slack for the alignment
   static constexpr size_t Q_BYTES = (size_t)2 * QR * QLD * 2;
-  static constexpr size_t KV_BYTES = (size_t)4 * TILE * 2;
+  static constexpr size_t KV_MIN = (size_t)4 * KVP * 2 > (size_t)QR * RLD * 4 ? (size_t)4 * KVP * 2 : (size_t)QR * RLD * 4;
+  static constexpr size_t KV_BYTES = (KV_MIN + 1023) / 1024 * 1024;
   static constexpr size_t LIM_BYTES = QR * 4;
-  static constexpr size_t TILE_SMEM = Q_BYTES + KV_BYTES + LIM_BYTES + 16;
+  static constexpr size_t TILE_SMEM = 1024 + Q_BYTES + KV_BYTES + LIM_BYTES + 16;
   // tiles with a second key interval per row: its bounds after the limits
   static constexpr size_t TILE_SMEM_R2 = TILE_SMEM + 2 * LIM_BYTES;
-  // the staged partial rows (CL x RPC = QR rows) live where K/V were
-  static_assert((size_t)QR * RLD * 4 <= KV_BYTES, "staged rows fit the K/V region");
+  static_assert(Q_BYTES % 1024 == 0, "the K/V planes start on a 1024-byte boundary (128-byte swizzle)");
   static_assert((size_t)QR * OLD * 4 + 2 * QR * 4 <= Q_BYTES, "half-1 partial fits the Q region");
 };
+
+// The four cache planes (K hi, K lo, V hi, V lo) as 2-D tensor maps over rows
+// of D values, boxes of AC rows x 64 values with the 128-byte swizzle; passed
+// to the kernels as one __grid_constant__ parameter.
+struct KvMaps {
+  CUtensorMap m[4];
+};
+
+// The tile's shared memory from a 1024-byte aligned address.
+__device__ __forceinline__ uint8_t* tile_base(uint8_t* raw) {
+  return raw + ((1024u - (tc::smem_u32(raw) & 1023u)) & 1023u);
+}
+
+// Element offset of (key row r, value c) in a K/V chunk plane as TMA writes
+// it: 64-value halves of AC rows, 128-byte rows whose 16-byte chunks are
+// XOR-swizzled by r % 8.
+__device__ __forceinline__ int kv_el(int r, int c) {
+  return (c >> 6) * (AC * 64) + r * 64 + ((((c & 63) >> 3) ^ (r & 7)) << 3) + (c & 7);
+}
+
+// TMA loads of the two planes [pl0, pl0 + 2) (K or V) of the chunk whose first
+// key is cache row `row`, counted on `bar`; one thread issues them.
+template <int D>
+__device__ __forceinline__ void tma_planes(bf16* KV, const KvMaps& tms, int pl0, long long row, uint64_t* bar) {
+  constexpr int HALVES = D / 64;
+  tc::mbar_expect_tx(bar, (uint32_t)(2 * HALVES * AC * 64 * 2));
+#pragma unroll
+  for (int pl = pl0; pl < pl0 + 2; ++pl)
+#pragma unroll
+    for (int h = 0; h < HALVES; ++h)
+      tc::tma_load_2d(KV + pl * Geo<D>::KVP + h * AC * 64, &tms.m[pl], h * 64, (int)row, bar);
+}
 
 __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, const uint32_t* b) {
   asm volatile(
@@ -99,35 +139,22 @@ __device__ __forceinline__ KvPlanes kv_planes(const AttnArgs& a, int req, int kv
   return k;
 }
 
-// cp.async copies of planes [pl0, pl0 + npl) of chunk c (keys c*AC .. c*AC+AC-1,
-// zero past kmax) into the tile's K/V region, by the group's 256 threads.
-template <int D>
-__device__ __forceinline__ void load_planes(bf16* KV, const KvPlanes& kv, int pl0, int npl, int c, int kmax,
-                                            int tid) {
-  using G = Geo<D>;
-  for (int x = tid; x < npl * AC * (D / 8); x += 256) {
-    const int pl = pl0 + x / (AC * (D / 8)), rem = x % (AC * (D / 8));
-    const int j = rem / (D / 8), v = rem % (D / 8);
-    const int key = c * AC + j;
-    const bool in = key <= kmax;
-    cp_async16(KV + pl * G::TILE + j * G::QLD + v * 8, kv.p[pl] + (size_t)(in ? key : 0) * D + v * 8, in ? 16 : 0);
-  }
-}
-
 // Work a tile may start before the rows' q and the window's K/V exist: when
 // its first chunk holds only committed cache positions (below the round-start
-// cache length pc, which no kernel of the forward writes), that chunk goes to
-// shared memory as one committed cp.async group and the tile's later
-// committed chunks (rank + stride, ...) into L2.  Returns whether the first
-// chunk was issued.
+// cache length pc, which no kernel of the forward writes), that chunk's K and
+// V go to shared memory (TMA on kbar and vbar; kvrow is the cache row of key
+// 0 of this tile's (request, kv head)) and the tile's later committed chunks
+// (rank + stride, ...) into L2.  Returns whether the first chunk was issued.
 template <int D>
-__device__ __forceinline__ bool tile_prefetch(uint8_t* sm, const KvPlanes& kv, int rank, int stride, int pc,
-                                              int tid) {
+__device__ __forceinline__ bool tile_prefetch(uint8_t* sm, const KvMaps& tms, const KvPlanes& kv, long long kvrow,
+                                              int rank, int stride, int pc, int tid, uint64_t* kbar, uint64_t* vbar) {
   bf16* KV = reinterpret_cast<bf16*>(sm + Geo<D>::Q_BYTES);
   const bool pre = (rank + 1) * AC <= pc;
   if (pre) {
-    load_planes<D>(KV, kv, 0, 4, rank, pc - 1, tid);
-    cp_async_commit();
+    if (tid == 0) {
+      tma_planes<D>(KV, tms, 0, kvrow + (long long)rank * AC, kbar);
+      tma_planes<D>(KV, tms, 2, kvrow + (long long)rank * AC, vbar);
+    }
     for (int i = tid; i < 4 * 8; i += 256) {
       const int c = rank + (1 + i / 4) * stride;
       if ((c + 1) * AC <= pc) prefetch_l2(kv.p[i % 4] + (size_t)c * AC * D, AC * D * 2);
@@ -150,23 +177,23 @@ __device__ __forceinline__ float* staged_rows(uint8_t* sm) {
 }
 
 // TRACE: record timeline marks in a.trace (first chunk ready, loop done).
-// kv_kmax >= 0 (decode launches): every cache position up to kv_kmax holds a
-// finite value (the cache is zeroed at allocation and only ever written with
-// finite k, v), so a first chunk that tile_prefetch did not fetch is loaded
-// up to kv_kmax right away, together with Q, instead of after the rows' key
-// limits are known.  Keys past a row's limit contribute exact zeros either
-// way.
+// kv_kmax >= 0 (decode launches): no row of the forward reads past cache
+// position kv_kmax, so a first chunk that tile_prefetch did not fetch and
+// that starts at or below it is loaded right away, together with Q, instead
+// of after the rows' key limits are known.  Keys past a row's limit
+// contribute exact zeros: their scores are masked before the softmax, and
+// the V rows past the tile's last visible key are zeroed after they land.
 // R2: rows also read a second key interval (a.row_lo2 / a.row_hi2), whose
 // bounds sit in TILE_SMEM_R2's extra shared memory.
 template <int D, bool TRACE = false, bool R2 = false>
-__device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, const KvPlanes& kv, int rank,
-                            int stride, int kvh, int qr0, int row0, int nrows, bool pre, int* s_maxlim,
-                            int kv_kmax = -1) {
+__device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, const KvMaps& tms, long long kvrow,
+                            uint64_t* kbar, uint64_t* vbar, int rank, int stride, int kvh, int qr0, int row0,
+                            int nrows, bool pre, int* s_maxlim, int kv_kmax = -1) {
   using Gm = Geo<D>;
-  constexpr int QLD = Gm::QLD, OLD = Gm::OLD, TILE = Gm::TILE, RLD = Gm::RLD;
+  constexpr int QLD = Gm::QLD, OLD = Gm::OLD, KVP = Gm::KVP, RLD = Gm::RLD;
   bf16* Qh = reinterpret_cast<bf16*>(sm);               // [QR][QLD]
   bf16* Ql = Qh + QR * QLD;
-  bf16* KV = Ql + QR * QLD;                             // {Kh, Kl, Vh, Vl} [AC][QLD]
+  bf16* KV = Ql + QR * QLD;                             // {Kh, Kl, Vh, Vl} [AC][D] swizzled (kv_el)
   int* Lim = reinterpret_cast<int*>(sm + Gm::Q_BYTES + Gm::KV_BYTES);  // [QR]
   int* Lo2 = Lim + QR;                                  // [QR] (R2 only)
   int* Hi2 = Lo2 + QR;                                  // [QR] (R2 only)
@@ -186,9 +213,9 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   if (tid == 0) *s_maxlim = -1;
   grp.sync();
   const bool early = !pre && kv_kmax >= 0 && rank * AC <= kv_kmax;
-  if (early) {
-    load_planes<D>(KV, kv, 0, 2, rank, kv_kmax, tid);
-    load_planes<D>(KV, kv, 2, 2, rank, kv_kmax, tid);
+  if (early && tid == 0) {
+    tma_planes<D>(KV, tms, 0, kvrow + (long long)rank * AC, kbar);
+    tma_planes<D>(KV, tms, 2, kvrow + (long long)rank * AC, vbar);
   }
   // Q planes of this row group (zero past the window) and the rows' key limits
   const unsigned gm = 0xFFFFFFFFu / (unsigned)G + 1u;
@@ -226,6 +253,10 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   const int n_chunks = maxlim < 0 ? 0 : maxlim / AC + 1;
   if (rank >= n_chunks) {  // uniform: this rank holds no chunk
     cp_async_wait<0>();
+    if (pre || early) {  // no copy outlives the CTA
+      const bool ok = tc::mbar_wait(kbar, 0) && tc::mbar_wait(vbar, 0);
+      if (!ok && tid == 0) set_err(a.err, DERR_TIMEOUT);
+    }
     return n_chunks;
   }
   const float sl2 = a.scale * LOG2E;
@@ -240,25 +271,25 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
   const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
   const int lcol = (lane >> 4) * 8;
-  const bf16* Kh = KV + kh * 16 * QLD;  // this warp's 16 keys of the chunk
-  const bf16* Kl = Kh + TILE;
-  const bf16* Vh = Kl + TILE;
-  const bf16* Vl = Vh + TILE;
+  const bf16* Kh = KV;  // this warp's 16 keys of the chunk: rows kh * 16 .. of each plane
+  const bf16* Kl = KV + KVP;
+  const bf16* Vh = KV + 2 * KVP;
+  const bf16* Vl = KV + 3 * KVP;
 
-  // K and V of a chunk are separate cp.async groups: K of the next chunk
-  // streams in while this chunk's softmax and PV run, V of the next chunk
-  // while the next QK^T runs.  Group order: [K+V of the first chunk] (issued
-  // early when it is committed cache), Q, then K, V per chunk.
-  if (!pre && !early && rank < n_chunks) {
-    load_planes<D>(KV, kv, 0, 2, rank, maxlim, tid);
-    load_planes<D>(KV, kv, 2, 2, rank, maxlim, tid);
+  // K and V of a chunk arrive on kbar and vbar (one phase per chunk): K of the
+  // next chunk streams in while this chunk's softmax and PV run, V of the next
+  // chunk while the next QK^T runs.  The first chunk went out before the
+  // dependency wait (pre), right after it (early), or goes out now.
+  if (!pre && !early && tid == 0) {
+    tma_planes<D>(KV, tms, 0, kvrow + (long long)rank * AC, kbar);
+    tma_planes<D>(KV, tms, 2, kvrow + (long long)rank * AC, vbar);
   }
-  cp_async_commit();
   int it = 0;
   for (int c = rank; c < n_chunks; c += stride, ++it) {
     const int kbase = c * AC + kh * 16;
     const bool next = c + stride < n_chunks;
-    if (it == 0) cp_async_wait<0>(); else cp_async_wait<1>();  // this chunk's K (and Q, first chunk)
+    if (it == 0) cp_async_wait<0>();  // q
+    if (!tc::mbar_wait(kbar, it & 1) && tid == 0) set_err(a.err, DERR_TIMEOUT);  // this chunk's K
     grp.sync();
     if (TRACE && it == 0 && tid == 0) trace_at(a, 4);
     // S = Q K^T for this warp's 16 rows and 16 keys
@@ -279,20 +310,20 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
       al[3] = *reinterpret_cast<const uint32_t*>(Ql + qo + 8 * QLD + 8);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const int ko = (nt * 8 + g) * QLD + ks * 16 + tq * 2;
+        const int kr = kh * 16 + nt * 8 + g, kc = ks * 16 + tq * 2;
+        const int ko0 = kv_el(kr, kc), ko1 = kv_el(kr, kc + 8);
         uint32_t bh[2], bl[2];
-        bh[0] = *reinterpret_cast<const uint32_t*>(Kh + ko);
-        bh[1] = *reinterpret_cast<const uint32_t*>(Kh + ko + 8);
-        bl[0] = *reinterpret_cast<const uint32_t*>(Kl + ko);
-        bl[1] = *reinterpret_cast<const uint32_t*>(Kl + ko + 8);
+        bh[0] = *reinterpret_cast<const uint32_t*>(Kh + ko0);
+        bh[1] = *reinterpret_cast<const uint32_t*>(Kh + ko1);
+        bl[0] = *reinterpret_cast<const uint32_t*>(Kl + ko0);
+        bl[1] = *reinterpret_cast<const uint32_t*>(Kl + ko1);
         mma16816(sacc[nt], al, bh);
         mma16816(sacc[nt], ah, bl);
         mma16816(sacc[nt], ah, bh);
       }
     }
     grp.sync();  // every warp is done with this chunk's K
-    if (next) load_planes<D>(KV, kv, 0, 2, c + stride, maxlim, tid);
-    cp_async_commit();
+    if (next && tid == 0) tma_planes<D>(KV, tms, 0, kvrow + (long long)(c + stride) * AC, kbar);
     // mask, scale to log2 units, row maxima over the 16 keys
     float mc_lo = -INFINITY, mc_hi = -INFINITY;
 #pragma unroll
@@ -345,15 +376,24 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
       oacc[dn][0] *= corr_lo; oacc[dn][1] *= corr_lo;
       oacc[dn][2] *= corr_hi; oacc[dn][3] *= corr_hi;
     }
-    if (it > 0) {
-      cp_async_wait<1>();  // this chunk's V (the next chunk's K may still be in flight)
+    // this chunk's V (the next chunk's K may still be in flight)
+    if (!tc::mbar_wait(vbar, it & 1) && tid == 0) set_err(a.err, DERR_TIMEOUT);
+    if (c * AC + AC - 1 > maxlim) {  // uniform: the chunk of the tile's last visible key
+      // keys past it may hold stale (even non-finite) cache contents, which
+      // TMA copies as they are: zero their V rows so that P = 0 adds exact zeros
+      const int r0 = maxlim - c * AC + 1, nr = AC - r0;
+      for (int x = tid; x < 2 * nr * (D / 8); x += 256) {
+        const int pl = 2 + x / (nr * (D / 8)), rem = x % (nr * (D / 8));
+        *reinterpret_cast<uint4*>(KV + pl * KVP + kv_el(r0 + rem / (D / 8), (rem % (D / 8)) * 8)) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
       grp.sync();
     }
     // O += P (V_hi + V_lo); B fragments of two d-tiles per ldmatrix.x4.trans
     uint32_t af[4] = {pf[0][0], pf[0][1], pf[1][0], pf[1][1]};
 #pragma unroll
     for (int dn = 0; dn < D / 8; dn += 2) {
-      const int vo = lrow * QLD + dn * 8 + lcol;
+      const int vo = kv_el(kh * 16 + lrow, dn * 8 + lcol);
       uint32_t bh[4], bl[4];
       ldsm_x4_trans(bh, Vh + vo);
       ldsm_x4_trans(bl, Vl + vo);
@@ -363,10 +403,8 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
       mma16816(oacc[dn + 1], af, bh + 2);
     }
     grp.sync();  // every warp is done with this chunk's V
-    if (next) load_planes<D>(KV, kv, 2, 2, c + stride, maxlim, tid);
-    cp_async_commit();
+    if (next && tid == 0) tma_planes<D>(KV, tms, 2, kvrow + (long long)(c + stride) * AC, vbar);
   }
-  cp_async_wait<0>();
   grp.sync();
   if (TRACE && tid == 0) trace_at(a, 5);
   // merge the two key halves of this tile: half 0 + half 1, in that order

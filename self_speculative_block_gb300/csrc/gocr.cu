@@ -96,6 +96,8 @@ struct gocr_handle {
   int* grid_ctr = nullptr;
   bool pdl = true;            // programmatic dependent launch between forward kernels
   bool l2_prefetch = false;   // GEMMs prefetch the next GEMM's weights into L2 (GOCR_L2_PREFETCH=1: on)
+  // TMA maps of the KV-cache planes (K hi, K lo, V hi, V lo; bf16 models), 128 bytes each
+  alignas(64) unsigned char kv_maps[4][128] = {};
   bool host_loop = false;     // GOCR_HOST_LOOP=1: per-round graphs driven by the host
   int* dbuf = nullptr;
   int* vbuf = nullptr;
@@ -244,6 +246,9 @@ void forward_args(gocr_handle* h, int kind, int n_slots, int B, int P, int* am_o
     at.part_chunks = h->att_chunks;
     at.ranks = h->attn_ranks;
     at.kind = h->attn_kind;
+    at.kv_maps = h->kv_maps;
+    at.kv_row0 = (long long)l * c.n_kv_heads * h->cap;
+    at.kv_req_rows = (long long)c.n_layers * c.n_kv_heads * h->cap;
     at.err = h->err;
     f.at.push_back(at);
     // O projection + residual; planes of resid * g_mlp for the MLP
@@ -698,6 +703,16 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     h->vc_lo = A(kv_elems * kv_es);
     h->q_lo = A((size_t)T * q_dim * kv_es);
   }
+  if (ok && h->dtype == GOCR_DTYPE_BF16) {
+    // the attention's TMA maps over each cache plane: every request, layer and kv head, rows of head_dim values
+    const long long rows = (long long)R * c.n_layers * c.n_kv_heads * h->cap;
+    const void* planes[4] = {h->kc_hi, h->kc_lo, h->vc_hi, h->vc_lo};
+    for (int i = 0; i < 4 && ok; ++i)
+      if (rows > 0x7FFFFFFFLL || !encode_tmap_bf16(h->kv_maps[i], planes[i], (int)rows, c.head_dim, 32)) {
+        int r_ = fail(h, GOCR_EINVAL, "KV cache too large for the attention's tensor maps");
+        g_lib_error = h->msg; gocr_free(h); *out = nullptr; return r_;
+      }
+  }
   h->resid = (float*)A((size_t)T * H * 4);
   h->xg_hi = A((size_t)T * H * es);
   h->at_hi = A((size_t)T * q_dim * es);
@@ -1139,6 +1154,18 @@ int gocr_op_attention_ranges(int dtype, const void* q_hi, const void* q_lo, cons
   {
     const char* ak = getenv("GOCR_ATTN");
     a.kind = ak && strcmp(ak, "tc") == 0 ? ATTN_TCGEN05 : ATTN_MMA_SYNC;
+  }
+  alignas(64) unsigned char maps[4][128];
+  if (dtype == GOCR_DTYPE_BF16) {
+    // TMA maps over the K and V planes: rows of d values, [Hkv * cap] rows
+    const void* planes[4] = {k_hi, k_lo, v_hi, v_lo};
+    if ((long long)Hkv * cap > 0x7FFFFFFFLL) return fail(h, GOCR_EINVAL, "bad shape");
+    for (int i = 0; i < 4; ++i)
+      if (!encode_tmap_bf16(maps[i], planes[i], Hkv * cap, d, 32))
+        return fail(h, GOCR_EINVAL, "K/V planes not usable by TMA (16-byte aligned device memory required)");
+    a.kv_maps = maps;
+    a.kv_row0 = 0;
+    a.kv_req_rows = 0;
   }
   if (dtype == GOCR_DTYPE_BF16) {
     // partial rows of the attention ranks: a process-wide scratch buffer per

@@ -124,6 +124,11 @@ struct alignas(16) AttnArgs {
   float* part;
   int* part_chunks;           // [slot][kv head x row group] chunks the group's rows read
   int ranks;                  // key-chunk ranks R (attention_ranks); 0: attention_ranks(cap, 1)
+  // mma.sync kernel: host copy of the four cache planes' TMA maps (attn::KvMaps:
+  // rows of d values, AC-row x 64-value boxes, 128-byte swizzle), and the map
+  // row of key 0 of (request 0, this layer, kv head 0) and the rows per request
+  const void* kv_maps;
+  long long kv_row0, kv_req_rows;
   int kind;                   // bf16 models: ATTN_TCGEN05 or ATTN_MMA_SYNC
   int* err;                   // device error word (bounded waits), or NULL
   unsigned long long* trace;  // launch timeline record, as GemmArgs::trace
