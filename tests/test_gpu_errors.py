@@ -31,8 +31,10 @@ def lib():
 
 def _cfg(synth, dt):
     if dt.startswith("bf16"):
+        # 160 LM-head tiles: the split rule gives the LM head one K split, so at
+        # decode shapes it runs on the streaming kernel (GOCR_LM_WAVES=1: tile CTAs)
         return synth.ModelConfig(n_layers=2, hidden=512, n_q_heads=6, n_kv_heads=2, head_dim=128, ffn=1024,
-                                 vocab=2048, dtype=synth.BF16)
+                                 vocab=20480, dtype=synth.BF16)
     return synth.TINY
 
 
