@@ -315,7 +315,8 @@ int gocr_op_linear_planes(const void* x_hi, const void* x_lo, const void* w, flo
  * o [T, Hq, d] fp32 (device); lim: device int32[T], row t reads keys
  * 0..lim[t] (draft: row 0 = p, rows 1..B = p+B; verify/AR: the row's own
  * position).  d in {64, 128}; Hq / Hkv <= 64 and T x Hq / Hkv <= 2^20
- * (GOCR_EINVAL otherwise).  GOCR_DTYPE_BF16 keeps its partial rows in a
+ * (GOCR_EINVAL otherwise).  GOCR_DTYPE_BF16 reads K and V by TMA: the four
+ * K/V planes must be 16-byte aligned (GOCR_EINVAL otherwise).  GOCR_DTYPE_BF16 keeps its partial rows in a
  * device scratch buffer of the library (one per device, allocated or grown
  * by the first call that needs more): calls that overlap on the GPU race. */
 int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
