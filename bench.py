@@ -337,6 +337,77 @@ def table_record(cfg, W, hbm, dev, steps, warmup):
             "selfspec_equals_ar": same, "steps": steps, "warmup": warmup}
 
 
+def next_rows_record(cfg, W, hbm, dev, steps, warmup):
+    """The survey's NEXT rows on the text region (prefix 1024, B = 32, 73
+    tokens): direct block-diffusion decoding (threshold 0.9), self-speculative
+    rounds with refined drafts (at most 4 draft forwards, draft threshold 0.9),
+    sampling (temperature 1) self-speculative against AR sampling, each as
+    committed tokens/s, tokens per forward and us per forward (the forwards'
+    share of the per-forward weight roofline); and the joint-training mask's
+    attention (one kernel launch over prefix 1024 + 3 x 512 packed rows, block
+    32) as us per launch and attention TFLOP/s over the mask's visible
+    (row, key) pairs.  Synthetic random-init weights: the decodes' confidence
+    and acceptance are those of an untrained model, so these time the
+    mechanisms, not the method's quality."""
+    import torch
+    from self_speculative_block_gb300 import gocr
+    wl = synth.WORKLOADS["text"]
+    B, n = wl.block, wl.max_new
+    dec = gocr.Decoder(cfg, W, max_ctx=wl.prefix_len + n + B + 8, max_block=B, device=str(dev))
+    rec = {"workload": wl.name}
+    try:
+        prefix = upload_prefixes(cfg, [wl.prefix_len], [synth.PREFIX_SEED], dev)[0][1]
+
+        def run(mode, blk, **kw):
+            ms = tok = fw = 0
+            for i in range(warmup + steps):
+                dec.prefill(0, prefix)
+                _, sts = dec.decode_ex([0], mode, blk, [n], **kw)
+                if i >= warmup:
+                    ms += sts[0]["device_ms"]; tok += sts[0]["committed"]; fw += sts[0]["forwards"]
+            us_fw = 1e3 * ms / fw
+            return {"tokens_per_s": tok / (ms / 1e3), "tokens_per_forward": tok / fw, "us_per_forward": us_fw,
+                    "forward_roofline_frac": (cfg.weight_bytes_per_forward() / (hbm * 1e9)) / (us_fw * 1e-6)}
+
+        rec["direct_diffusion"] = dict(run(gocr.MODE_DIFFUSION, B, tau=0.9), tau=0.9, B=B)
+        rec["refined_drafts"] = dict(run(gocr.MODE_REFINED, B, tau=0.9, draft_steps=4), tau=0.9, draft_steps=4, B=B)
+        rec["sampling_selfspec"] = dict(run(gocr.MODE_SELFSPEC, B, temperature=1.0, seed=1), temperature=1.0, B=B)
+        rec["sampling_ar"] = dict(run(gocr.MODE_AR, 0, temperature=1.0, seed=1), temperature=1.0)
+    finally:
+        dec.close()
+    # the joint-training mask as a second key interval per row
+    P, N, blk = 1024, 512, 32
+    L = P + 3 * N
+    lim, lo2, hi2, _ = gocr.three_stream_ranges(P, N, blk)
+    g = torch.Generator(device="cpu").manual_seed(0)
+
+    def planes(shape):
+        x = torch.randn(*shape, generator=g)
+        hi = x.to(torch.bfloat16)
+        return hi.to(dev), (x - hi.float()).to(torch.bfloat16).to(dev)
+
+    q = planes((L, cfg.n_q_heads, cfg.head_dim))
+    k = planes((cfg.n_kv_heads, L, cfg.head_dim))
+    v = planes((cfg.n_kv_heads, L, cfg.head_dim))
+    t_lim, t_lo2, t_hi2 = (torch.from_numpy(a).to(dev) for a in (lim, lo2, hi2))
+    for _ in range(3):
+        gocr.op_attention(q, k, v, t_lim, gocr.DTYPE_BF16, lo2=t_lo2, hi2=t_hi2)
+    torch.cuda.synchronize()
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        gocr.op_attention(q, k, v, t_lim, gocr.DTYPE_BF16, lo2=t_lo2, hi2=t_hi2)
+    e1.record()
+    torch.cuda.synchronize()
+    us = 1e3 * e0.elapsed_time(e1) / reps
+    pairs = int(np.sum(lim + 1) + np.sum(np.maximum(hi2 - lo2 + 1, 0)))
+    flops = 4.0 * pairs * cfg.n_q_heads * cfg.head_dim  # QK^T and PV, 2 flops per multiply-add
+    rec["training_mask_attention"] = {"rows": L, "prefix": P, "stream": N, "block": blk, "us_per_launch": us,
+                                      "visible_pairs": pairs, "tflops": flops / (us * 1e-6) / 1e12}
+    return rec
+
+
 # --------------------------------------------------------------------------- kernel rooflines
 
 GEMM_SOURCES = ("gemm_tc.cu", "gemm.cu", "epilogue.cuh", "tc.cuh", "kernels.cuh", "common.cuh")
@@ -625,8 +696,10 @@ def main():
             if kind != "batch" else None
         if extras:
             sweep_k = kernel_sweep(cfg, B, hbm, dev)
+    nxt = None
     if extras and kind == "text":
         table = table_record(cfg, W, hbm, dev, args.steps, args.warmup)
+        nxt = next_rows_record(cfg, W, hbm, dev, min(args.steps, 3), 1)
 
     cpu, equality = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -659,6 +732,7 @@ def main():
             "roofline_sweep": sweep_k,
             "ar": ar_rec,
             "table": table,
+            "next": nxt,
             "equality": equality,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_tok / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,

@@ -210,7 +210,12 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   const bf16* qh = reinterpret_cast<const bf16*>(a.q_hi);
   const bf16* ql = reinterpret_cast<const bf16*>(a.q_lo);
 
-  if (tid == 0) *s_maxlim = -1;
+  __shared__ int s_lim1, s_lo2min;  // R2: the rows' largest limit, smallest second-interval start
+  if (tid == 0) {
+    *s_maxlim = -1;
+    s_lim1 = -1;
+    s_lo2min = 0x7fffffff;
+  }
   grp.sync();
   const bool early = !pre && kv_kmax >= 0 && rank * AC <= kv_kmax;
   if (early && tid == 0) {
@@ -236,7 +241,10 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
     int lim = -1;
     if (gi < nq) lim = min(a.row_lim[row0 + div_small(gi, G, gm)], a.cap - 1);
     Lim[tid] = lim;
-    if (lim >= 0) atomicMax(s_maxlim, lim);
+    if (lim >= 0) {
+      atomicMax(s_maxlim, lim);
+      if (R2) atomicMax(&s_lim1, lim);
+    }
     if (R2) {
       int lo2 = 1, hi2 = 0;
       if (gi < nq) {
@@ -245,12 +253,28 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
       }
       Lo2[tid] = lo2;
       Hi2[tid] = hi2;
-      if (hi2 >= lo2) atomicMax(s_maxlim, hi2);
+      if (hi2 >= lo2) {
+        atomicMax(s_maxlim, hi2);
+        atomicMin(&s_lo2min, lo2);
+      }
     }
   }
   grp.sync();
   const int maxlim = *s_maxlim;
   const int n_chunks = maxlim < 0 ? 0 : maxlim / AC + 1;
+  // R2: a chunk whose keys all lie past every row's limit and before every
+  // row's second interval is an exact no-op for the tile: the rank skips it.
+  // next_chunk(c): the rank's next chunk after c that is not skipped.
+  const int lim1 = R2 ? s_lim1 : maxlim, lo2min = R2 ? s_lo2min : 0x7fffffff;
+  auto skip = [&](int c) { return R2 && c * AC > lim1 && (c + 1) * AC - 1 < lo2min; };
+  auto next_chunk = [&](int c) {
+    c += stride;
+    if (skip(c)) {
+      const int c0 = lo2min / AC;  // the chunk of the smallest start: not skipped, nor any after it
+      c = c0 + ((rank - c0) % stride + stride) % stride;
+    }
+    return c;
+  };
   if (rank >= n_chunks) {  // uniform: this rank holds no chunk
     cp_async_wait<0>();
     if (pre || early) {  // no copy outlives the CTA
@@ -280,14 +304,18 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   // next chunk streams in while this chunk's softmax and PV run, V of the next
   // chunk while the next QK^T runs.  The first chunk went out before the
   // dependency wait (pre), right after it (early), or goes out now.
-  if (!pre && !early && tid == 0) {
-    tma_planes<D>(KV, tms, 0, kvrow + (long long)rank * AC, kbar);
-    tma_planes<D>(KV, tms, 2, kvrow + (long long)rank * AC, vbar);
+  // (the first chunk issued before the limits were known is chunk `rank`)
+  const int c_first = (!pre && !early && skip(rank)) ? next_chunk(rank - stride) : rank;
+  if (!pre && !early && tid == 0 && c_first < n_chunks) {
+    tma_planes<D>(KV, tms, 0, kvrow + (long long)c_first * AC, kbar);
+    tma_planes<D>(KV, tms, 2, kvrow + (long long)c_first * AC, vbar);
   }
+  if (c_first >= n_chunks) cp_async_wait<0>();  // every chunk of this rank skipped: q only
   int it = 0;
-  for (int c = rank; c < n_chunks; c += stride, ++it) {
+  for (int c = c_first; c < n_chunks; ++it) {
     const int kbase = c * AC + kh * 16;
-    const bool next = c + stride < n_chunks;
+    const int cn = next_chunk(c);
+    const bool next = cn < n_chunks;
     if (it == 0) cp_async_wait<0>();  // q
     if (!tc::mbar_wait(kbar, it & 1) && tid == 0) set_err(a.err, DERR_TIMEOUT);  // this chunk's K
     grp.sync();
@@ -323,7 +351,7 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
       }
     }
     grp.sync();  // every warp is done with this chunk's K
-    if (next && tid == 0) tma_planes<D>(KV, tms, 0, kvrow + (long long)(c + stride) * AC, kbar);
+    if (next && tid == 0) tma_planes<D>(KV, tms, 0, kvrow + (long long)cn * AC, kbar);
     // mask, scale to log2 units, row maxima over the 16 keys
     float mc_lo = -INFINITY, mc_hi = -INFINITY;
 #pragma unroll
@@ -403,7 +431,8 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
       mma16816(oacc[dn + 1], af, bh + 2);
     }
     grp.sync();  // every warp is done with this chunk's V
-    if (next && tid == 0) tma_planes<D>(KV, tms, 2, kvrow + (long long)(c + stride) * AC, vbar);
+    if (next && tid == 0) tma_planes<D>(KV, tms, 2, kvrow + (long long)cn * AC, vbar);
+    c = cn;
   }
   grp.sync();
   if (TRACE && tid == 0) trace_at(a, 5);

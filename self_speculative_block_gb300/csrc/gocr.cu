@@ -1134,6 +1134,9 @@ int gocr_three_stream_ranges(int P, int N, int B, int32_t* lim, int32_t* lo2, in
   return GOCR_OK;
 }
 
+// waves of two attention CTAs per SM that the rank count of a second-interval call fills
+static constexpr int OP_R2_WAVES = 2;
+
 int gocr_op_attention_ranges(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
                              const void* v_hi, const void* v_lo, float* o, const int32_t* lim, const int32_t* lo2,
                              const int32_t* hi2, int T, int Hq, int Hkv, int d, int cap, void* stream) {
@@ -1154,6 +1157,25 @@ int gocr_op_attention_ranges(int dtype, const void* q_hi, const void* q_lo, cons
   {
     const char* ak = getenv("GOCR_ATTN");
     a.kind = ak && strcmp(ak, "tc") == 0 ? ATTN_TCGEN05 : ATTN_MMA_SYNC;
+  }
+  {
+    // key-chunk ranks: the rule's count, which keeps every row's bits the same
+    // whatever the number of rows in the call.  Rows with a second key interval
+    // (joint-training forwards, one call over the whole packed sequence) take
+    // instead no more ranks than fill OP_R2_WAVES waves of two CTAs per SM over
+    // the (kv head, row tile) groups: many tiles need few ranks, and each rank
+    // costs a partial row set and its merge.  GOCR_ATTN_RANKS=<n> replaces the
+    // count (1 .. the rule's).
+    const int rule = attention_ranks(cap, 1);
+    int R = rule;
+    if (lo2) {
+      const long long groups = (long long)Hkv * ((T * (Hq / Hkv) + 63) / 64);
+      const long long fill = (OP_R2_WAVES * 2LL * SM_COUNT + groups - 1) / groups;
+      R = fill < R ? (int)fill : R;
+    }
+    const char* ar = getenv("GOCR_ATTN_RANKS");
+    if (ar && atoi(ar) >= 1) R = atoi(ar) < rule ? atoi(ar) : rule;
+    a.ranks = R < 1 ? 1 : R;
   }
   alignas(64) unsigned char maps[4][128];
   if (dtype == GOCR_DTYPE_BF16) {
