@@ -376,35 +376,22 @@ def next_rows_record(cfg, W, hbm, dev, steps, warmup):
     finally:
         dec.close()
     # the joint-training mask as a second key interval per row
-    P, N, blk = 1024, 512, 32
-    L = P + 3 * N
-    lim, lo2, hi2, _ = gocr.three_stream_ranges(P, N, blk)
-    g = torch.Generator(device="cpu").manual_seed(0)
-
-    def planes(shape):
-        x = torch.randn(*shape, generator=g)
-        hi = x.to(torch.bfloat16)
-        return hi.to(dev), (x - hi.float()).to(torch.bfloat16).to(dev)
-
-    q = planes((L, cfg.n_q_heads, cfg.head_dim))
-    k = planes((cfg.n_kv_heads, L, cfg.head_dim))
-    v = planes((cfg.n_kv_heads, L, cfg.head_dim))
-    t_lim, t_lo2, t_hi2 = (torch.from_numpy(a).to(dev) for a in (lim, lo2, hi2))
+    from self_speculative_block_gb300.profile_cases import TrainMask
+    tm = TrainMask(cfg, dev)
     for _ in range(3):
-        gocr.op_attention(q, k, v, t_lim, gocr.DTYPE_BF16, lo2=t_lo2, hi2=t_hi2)
+        tm.run()
     torch.cuda.synchronize()
     reps = 20
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(reps):
-        gocr.op_attention(q, k, v, t_lim, gocr.DTYPE_BF16, lo2=t_lo2, hi2=t_hi2)
+        tm.run()
     e1.record()
     torch.cuda.synchronize()
     us = 1e3 * e0.elapsed_time(e1) / reps
-    pairs = int(np.sum(lim + 1) + np.sum(np.maximum(hi2 - lo2 + 1, 0)))
-    flops = 4.0 * pairs * cfg.n_q_heads * cfg.head_dim  # QK^T and PV, 2 flops per multiply-add
-    rec["training_mask_attention"] = {"rows": L, "prefix": P, "stream": N, "block": blk, "us_per_launch": us,
-                                      "visible_pairs": pairs, "tflops": flops / (us * 1e-6) / 1e12}
+    rec["training_mask_attention"] = {"rows": tm.L, "prefix": tm.P, "stream": tm.N, "block": tm.block,
+                                      "us_per_launch": us, "visible_pairs": tm.visible_pairs(),
+                                      "tflops": tm.flops() / (us * 1e-6) / 1e12}
     return rec
 
 

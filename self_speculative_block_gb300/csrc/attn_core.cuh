@@ -6,7 +6,9 @@
 // ranks' partial rows in rank order.
 //
 // Layout of the work: keys sit in chunks of AC = 32 at absolute positions;
-// rank r of the R ranks visits chunks r, r + R, ...  In a tile,
+// rank r of the R ranks visits chunks r, r + R, ... (with a second key
+// interval per row, minus the chunks masked for every row of its tile, which
+// would change nothing).  In a tile,
 // warp w owns query rows 16 (w % 4) .. +15 and key half w / 4 (keys
 // 16 (w / 4) .. +15 of every chunk), so each (rank, key half) runs its own
 // online softmax over a fixed set of key positions.  A chunk with no key

@@ -27,6 +27,13 @@
         GOCR_HOST_LOOP=1 so that the round's kernels are profilable: they
         start at launch 1600.
 
+    python -m self_speculative_block_gb300.profile_cases train_mask
+        The joint-training mask's attention over the packed sequence [prefix
+        1024, clean 512, corrupted 512, corrupted 512], blocks of 32, the
+        0.5B-class decoder's heads (12 q, 4 kv, d 128): three launches of the
+        second-interval attention (attention_part_kernel then
+        attention_merge_kernel each), the shapes bench.py times.
+
 All hold a few GB on the device.  The sweep's shapes and inputs are the ones
 bench.py times for its kernel roofline.
 """
@@ -105,6 +112,51 @@ class GemmSweep:
         return sum(n * k * 2 + 2 * T * k * 2 + T * n * 4 for n, k in self.shapes) / len(self.shapes)
 
 
+class TrainMask:
+    """bf16 hi + lo planes of seeded Gaussian q [L, Hq, d], k and v [Hkv, L, d]
+    and the three-stream key intervals on the device, for one attention call
+    over the whole packed training sequence."""
+
+    def __init__(self, cfg: synth.ModelConfig, device, P: int = 1024, N: int = 512, block: int = 32, seed: int = 0):
+        import torch
+        from . import gocr
+        self.P, self.N, self.block, self.L = P, N, block, P + 3 * N
+        self.cfg = cfg
+        self.lim, self.lo2, self.hi2, _ = gocr.three_stream_ranges(P, N, block)
+        g = torch.Generator(device="cpu").manual_seed(seed)
+
+        def planes(shape):
+            x = torch.randn(*shape, generator=g)
+            hi = x.to(torch.bfloat16)
+            return hi.to(device), (x - hi.float()).to(torch.bfloat16).to(device)
+
+        self.q = planes((self.L, cfg.n_q_heads, cfg.head_dim))
+        self.k = planes((cfg.n_kv_heads, self.L, cfg.head_dim))
+        self.v = planes((cfg.n_kv_heads, self.L, cfg.head_dim))
+        self.d_lim, self.d_lo2, self.d_hi2 = (torch.from_numpy(a).to(device) for a in (self.lim, self.lo2, self.hi2))
+
+    def run(self):
+        from . import gocr
+        return gocr.op_attention(self.q, self.k, self.v, self.d_lim, gocr.DTYPE_BF16, lo2=self.d_lo2, hi2=self.d_hi2)
+
+    def visible_pairs(self) -> int:
+        """(row, key) pairs the mask lets through (both intervals)."""
+        import numpy as np
+        return int(np.sum(self.lim + 1) + np.sum(np.maximum(self.hi2 - self.lo2 + 1, 0)))
+
+    def flops(self) -> float:
+        """QK^T and PV multiply-adds over the visible pairs, 2 flops each."""
+        return 4.0 * self.visible_pairs() * self.cfg.n_q_heads * self.cfg.head_dim
+
+
+def train_mask_case():
+    import torch
+    tm = TrainMask(synth.BASE, torch.device("cuda:0"))
+    for _ in range(3):
+        tm.run()
+    torch.cuda.synchronize()
+
+
 def draft_case(B: int = 32):
     from . import gocr
     cfg = synth.BASE
@@ -149,6 +201,8 @@ def main(argv):
         sweep_case()
     elif what == "batch":
         batch_case()
+    elif what == "train_mask":
+        train_mask_case()
     else:
         print(__doc__)
         return 2
