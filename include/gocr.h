@@ -325,11 +325,13 @@ int gocr_op_attention(int dtype, const void* q_hi, const void* q_lo, const void*
 
 /* gocr_op_attention with a second key interval per row: row t reads keys
  * 0..lim[t] and lo2[t]..hi2[t] (none when hi2[t] < lo2[t]); lo2, hi2:
- * device int32[T], both NULL = the plain call.  The bf16 path runs the
- * mma.sync tile kernel (whatever GOCR_ATTN says) and, with lo2/hi2 given,
- * splits each row tile's keys over fewer ranks as T grows: a row's result
- * then depends on T in its last bits (the plain call's does not).  Key
- * chunks masked for every row of a tile are skipped, which changes no bits. */
+ * device int32[T], both NULL = the plain call.  With lo2/hi2 given, the
+ * bf16 path splits each row tile's keys over fewer ranks as T grows (at most
+ * two waves of the kernel's resident CTAs) and runs the tcgen05 kernel when
+ * its ranks average at least four 32-key chunks, else the mma.sync kernel
+ * (GOCR_ATTN=tc / mma forces one): a row's result then depends on T in its
+ * last bits (the plain call's does not).  Key chunks masked for every row of
+ * a tile are skipped, which changes no bits. */
 int gocr_op_attention_ranges(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
                              const void* v_hi, const void* v_lo, float* o, const int32_t* lim, const int32_t* lo2,
                              const int32_t* hi2, int T, int Hq, int Hkv, int d, int cap, void* stream);

@@ -25,6 +25,10 @@
 //     or two chunks;
 //   attention_tc_part_kernel: 128-row groups on tcgen05 (attn_tc.cuh), for
 //     handles whose ranks average at least four chunks.
+// Both have an instantiation for rows with a second key interval (the
+// joint-training mask).  The partial rows of the ranks are then added in rank
+// order by attention_merge_kernel, or for second-interval calls with at most
+// eight ranks by attention_merge_few_kernel (one warp per row, no barrier).
 // There is no thread-block cluster: the CTAs need no co-scheduling.  Under
 // programmatic dependent launch a CTA fetches its first chunk before the
 // grid-dependency wait when that chunk holds only committed cache positions
@@ -264,6 +268,67 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R)
   if (TRACE && threadIdx.x == 0) trace_at(a, 3, TRACE_MERGE_SLOT);
 }
 
+// Merge for few ranks (R <= MERGE_FEW): one warp per (row, head) pair, each
+// lane a run of D / 32 output columns; every load in one round trip, no CTA
+// barrier.  Ranks are added in rank order.  Used by calls whose rows carry a
+// second key interval (training forwards over many row tiles, few ranks).
+constexpr int MERGE_FEW = 8;
+template <int D, int TQR>
+__global__ void __launch_bounds__(256) attention_merge_few_kernel(AttnArgs a, int R) {
+  constexpr int RLD = (TQR == attn::QR ? attn::Geo<D>::RLD : attn_tc::Geo<D>::RLD);
+  constexpr int CL = D / 32;  // columns per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int group = blockIdx.y;
+  const int kvh = group % a.Hkv, rg = group / a.Hkv;
+  const int G = a.Hq / a.Hkv;
+  const int i = blockIdx.x * 8 + warp;  // row of the group's tile
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int nq = a.T * G, gi = rg * TQR + i;
+  if (i >= TQR || gi >= nq) return;
+  const int n_chunks = a.part_chunks[group];
+  const int n_ranks = n_chunks < R ? n_chunks : R;
+  const float* base = a.part + (size_t)group * R * TQR * RLD + (size_t)i * RLD;
+  float m[MERGE_FEW], l[MERGE_FEW], v[MERGE_FEW][CL];
+#pragma unroll
+  for (int r = 0; r < MERGE_FEW; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int j = 0; j < CL; ++j) v[r][j] = 0.f;
+    if (r < n_ranks) {
+      const float* p = base + (size_t)r * TQR * RLD;
+      m[r] = __ldcg(p + D);
+      l[r] = __ldcg(p + D + 1);
+      if constexpr (CL == 4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(p + lane * 4));
+        v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
+      } else {
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(p + lane * 2));
+        v[r][0] = x.x; v[r][1] = x.y;
+      }
+    }
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < MERGE_FEW; ++r) M = fmaxf(M, m[r]);
+  float L = 0.f, o[CL];
+#pragma unroll
+  for (int j = 0; j < CL; ++j) o[j] = 0.f;
+#pragma unroll
+  for (int r = 0; r < MERGE_FEW; ++r) {
+    const float w = m[r] == -INFINITY ? 0.f : exp2f(m[r] - M);
+    L = fmaf(w, l[r], L);
+#pragma unroll
+    for (int j = 0; j < CL; ++j) o[j] = fmaf(w, v[r][j], o[j]);
+  }
+  const float il = L > 0.f ? 1.f / L : 0.f;
+  const int tq = attn::div_small(gi, G, 0xFFFFFFFFu / (unsigned)G + 1u);
+  const size_t off = ((size_t)tq * a.Hq + kvh * G + (gi - tq * G)) * D + lane * CL;
+#pragma unroll
+  for (int j = 0; j < CL; ++j) put_plane(a.o_hi, a.o_lo, a.out_bf16, off + j, o[j] * il);
+}
+
 size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, int R) {
   const int G = Hq / Hkv;
   size_t best = 0;
@@ -278,6 +343,18 @@ size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, 
 // The merge after a partial kernel of TQR-row tiles (always ordered after it).
 template <int D, int TQR, bool TRACE>
 static bool launch_attn_merge(const AttnArgs& a, int R, int n_groups, int n_slots, cudaStream_t s) {
+  if (a.row_lo2 && R <= MERGE_FEW && n_slots == 1 && !a.plan && a.rows_per_slot == 0) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(TQR / 8, n_groups, 1);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attention_merge_few_kernel<D, TQR>, a, R) == cudaSuccess;
+  }
   // with few ranks a row pair is little work: four pairs per CTA then
   const int ppc = R <= 16 ? 4 : 1;
   cudaLaunchConfig_t cfg{};
@@ -293,12 +370,12 @@ static bool launch_attn_merge(const AttnArgs& a, int R, int n_groups, int n_slot
                    : cudaLaunchKernelEx(&cfg, attention_merge_kernel<D, TQR, 1, TRACE>, a, R)) == cudaSuccess;
 }
 
-template <int D, bool TRACE>
+template <int D, bool TRACE, bool R2 = false>
 static bool launch_attn_tc_t(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
   using Gm = attn_tc::Geo<D>;
   const int G = a.Hq / a.Hkv;
   const int n_rg = (max_rows * G + attn_tc::QR - 1) / attn_tc::QR;
-  if (!kernel_smem_at_least(reinterpret_cast<const void*>(attention_tc_part_kernel<D, TRACE>), Gm::SMEM))
+  if (!kernel_smem_at_least(reinterpret_cast<const void*>(attention_tc_part_kernel<D, TRACE, R2>), Gm::SMEM))
     return false;
   const int R = a.ranks > 0 ? a.ranks : attention_ranks(a.cap, 1);
   cudaLaunchConfig_t cfg{};
@@ -311,7 +388,7 @@ static bool launch_attn_tc_t(const AttnArgs& a, int n_slots, int max_rows, cudaS
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, attention_tc_part_kernel<D, TRACE>, a) != cudaSuccess) return false;
+  if (cudaLaunchKernelEx(&cfg, attention_tc_part_kernel<D, TRACE, R2>, a) != cudaSuccess) return false;
   return launch_attn_merge<D, attn_tc::QR, TRACE>(a, R, a.Hkv * n_rg, n_slots, s);
 }
 
@@ -342,9 +419,11 @@ static bool launch_attn_mma_t(const AttnArgs& a, int n_slots, int max_rows, cuda
 
 template <int D>
 static bool launch_attn_mma(const AttnArgs& a, int n_slots, int max_rows, cudaStream_t s, bool pdl) {
-  // rows with a second key interval (the joint-training mask) run the
-  // mma.sync tile's R2 instantiation
-  if (a.row_lo2) return launch_attn_mma_t<D, false, true>(a, n_slots, max_rows, s, pdl);
+  // rows with a second key interval (the joint-training mask): the R2
+  // instantiation of the kernel of a.kind
+  if (a.row_lo2)
+    return a.kind == ATTN_TCGEN05 ? launch_attn_tc_t<D, false, true>(a, n_slots, max_rows, s, pdl)
+                                  : launch_attn_mma_t<D, false, true>(a, n_slots, max_rows, s, pdl);
   if (a.kind == ATTN_TCGEN05)
     return a.trace ? launch_attn_tc_t<D, true>(a, n_slots, max_rows, s, pdl)
                    : launch_attn_tc_t<D, false>(a, n_slots, max_rows, s, pdl);

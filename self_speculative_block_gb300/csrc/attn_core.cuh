@@ -272,7 +272,8 @@ __device__ int tile_partial(const AttnArgs& a, uint8_t* sm, const Grp& grp, cons
   auto next_chunk = [&](int c) {
     c += stride;
     if (skip(c)) {
-      const int c0 = lo2min / AC;  // the chunk of the smallest start: not skipped, nor any after it
+      // the chunk of the smallest start (not skipped, nor any after it), at most n_chunks
+      const int c0 = lo2min / AC < n_chunks ? lo2min / AC : n_chunks;
       c = c0 + ((rank - c0) % stride + stride) % stride;
     }
     return c;

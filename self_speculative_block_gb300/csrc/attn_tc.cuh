@@ -51,7 +51,9 @@ template <int D> struct Geo {
   static constexpr int OFF_P = OFF_VT + 2 * VT_PLANE;
   static constexpr int OFF_V = OFF_P + P_BYTES;              // [stage][hi, lo]
   static constexpr int OFF_LIM = OFF_V + 4 * V_PLANE;        // int [QR]
-  static constexpr int OFF_CORR = OFF_LIM + QR * 4;          // float [QR]
+  static constexpr int OFF_LO2 = OFF_LIM + QR * 4;           // int [QR]: second key interval (training mask)
+  static constexpr int OFF_HI2 = OFF_LO2 + QR * 4;           // int [QR]
+  static constexpr int OFF_CORR = OFF_HI2 + QR * 4;          // float [QR]
   static constexpr int OFF_BAR = OFF_CORR + QR * 4;          // three mbarriers, the TMEM address
   static constexpr int SMEM = OFF_BAR + 32 + 1024;           // + slack for the 1024-byte alignment
   static constexpr int RLD = D + 4;                          // fp32 stride of a staged partial row
@@ -115,19 +117,24 @@ __device__ __forceinline__ void transpose_v(uint8_t* sm, int st, int warp, int l
 
 namespace gocr {
 
-// Partial kernel: one CTA per (kv head x 128-row group, rank, slot).
-template <int D, bool TRACE>
+// Partial kernel: one CTA per (kv head x 128-row group, rank, slot).  R2: rows
+// also read a second key interval lo2..hi2 (the joint-training mask), and the
+// rank skips the chunks that are masked for every row of its tile.
+template <int D, bool TRACE, bool R2 = false>
 __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(AttnArgs a) {
   using namespace attn_tc;
   using Gm = Geo<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   int* Lim = reinterpret_cast<int*>(sm + Gm::OFF_LIM);
+  int* Lo2 = reinterpret_cast<int*>(sm + Gm::OFF_LO2);
+  int* Hi2 = reinterpret_cast<int*>(sm + Gm::OFF_HI2);
   float* Corr = reinterpret_cast<float*>(sm + Gm::OFF_CORR);
   uint64_t* s_full = reinterpret_cast<uint64_t*>(sm + Gm::OFF_BAR);  // [2] score buffers
   uint64_t* pv_full = s_full + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(pv_full + 1);
   __shared__ int s_maxlim;
+  __shared__ int s_lim1, s_lo2min;  // R2: the rows' largest limit, smallest second-interval start
   __shared__ int s_fail;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -143,6 +150,8 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
     tc::mbar_init(pv_full, 1);
     tc::fence_mbar_init();
     s_maxlim = -1;
+    s_lim1 = -1;
+    s_lo2min = 0x7fffffff;
     s_fail = 0;
   }
   // committed cache before the dependency wait (decode launches only): the
@@ -207,9 +216,26 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
     if (tid < QR) {
       const int gi = qr0 + tid;
       int lim = -1;
-      if (gi < nq) lim = min(a.row_lim[row0 + attn::div_small(gi, G, gm)], a.cap - 1);
+      const int t = gi < nq ? row0 + attn::div_small(gi, G, gm) : 0;
+      if (gi < nq) lim = min(a.row_lim[t], a.cap - 1);
       Lim[tid] = lim;
-      if (lim >= 0) atomicMax(&s_maxlim, lim);
+      if (lim >= 0) {
+        atomicMax(&s_maxlim, lim);
+        if (R2) atomicMax(&s_lim1, lim);
+      }
+      if (R2) {
+        int lo2 = 1, hi2 = 0;
+        if (gi < nq) {
+          lo2 = max(a.row_lo2[t], 0);
+          hi2 = min(a.row_hi2[t], a.cap - 1);
+        }
+        Lo2[tid] = lo2;
+        Hi2[tid] = hi2;
+        if (hi2 >= lo2) {
+          atomicMax(&s_maxlim, hi2);
+          atomicMin(&s_lo2min, lo2);
+        }
+      }
     }
     __syncthreads();
     const int maxlim = s_maxlim;
@@ -217,18 +243,32 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
     if (rank == 0 && tid == 0) a.part_chunks[(size_t)slot * gridDim.x + group] = n_chunks;
     if (rank < n_chunks) {  // uniform
       const attn::KvPlanes kv = attn::kv_planes(a, req, kvh, D);
-      // a rank's chunks: c_it = rank + it * R, it = 0 .. n_it - 1; chunk c_it
-      // sits in stage it & 1 (K swizzled, V row-major), its scores in S buffer
-      // it & 1
-      const int n_it = (n_chunks - rank + R - 1) / R;
-      if (!pre) load_kv<D>(sm, kv, 0, rank, maxlim, tid);
+      // a rank's chunks: rank, rank + R, ... below n_chunks; with a second
+      // interval (R2) minus the chunks cA .. c0 - 1, whose keys all lie past
+      // every row's limit and before every row's second interval (for those
+      // a row's state would not change).  chunk(it) is the it-th of them, in
+      // increasing order: chunk it sits in stage it & 1 (K swizzled, V
+      // row-major), its scores in S buffer it & 1.  n_it may be 0 (R2): the
+      // rank then writes the empty partial (m = -inf, l = 0, O = 0).
+      int cA = n_chunks, c0 = n_chunks;
+      if (R2) {
+        cA = s_lim1 < 0 ? 0 : s_lim1 / AC + 1;
+        c0 = s_lo2min / AC < n_chunks ? s_lo2min / AC : n_chunks;
+        if (c0 <= cA) cA = c0 = n_chunks;  // nothing to skip
+      }
+      const int n_a = rank < cA ? (cA - rank + R - 1) / R : 0;  // chunks below the skipped range
+      const int cB = c0 + ((rank - c0) % R + R) % R;             // the first chunk past it
+      const int n_it = n_a + (cB < n_chunks ? (n_chunks - cB + R - 1) / R : 0);
+      auto chunk = [&](int it) { return it < n_a ? rank + it * R : cB + (it - n_a) * R; };
+      if (!pre && n_it > 0) load_kv<D>(sm, kv, 0, chunk(0), maxlim, tid);
       attn::cp_async_commit();  // Q (and chunk 0)
-      if (n_it > 1) load_kv<D>(sm, kv, 1, rank + R, maxlim, tid);
+      if (n_it > 1) load_kv<D>(sm, kv, 1, chunk(1), maxlim, tid);
       attn::cp_async_commit();  // chunk 1
       const float sl2 = a.scale * attn::LOG2E;
       const int q4 = warp & 3, h = warp >> 2;
       const int r = q4 * 32 + lane;  // this thread's tile row
       const int lim_r = Lim[r];
+      const int lo2_r = R2 ? Lo2[r] : 1, hi2_r = R2 ? Hi2[r] : 0;
       const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
       constexpr int OH = D / 2;  // output columns per warp
       float O[OH];
@@ -260,12 +300,12 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
       if (n_it > 1) attn::cp_async_wait<1>(); else attn::cp_async_wait<0>();
       tc::fence_proxy_async_smem();
       __syncthreads();
-      if (tid == 0) {
+      if (tid == 0 && n_it > 0) {
         tc::fence_after_sync();
         issue_qk(0);
       }
       for (int it = 0; it < n_it; ++it) {
-        const int st = it & 1, c = rank + it * R;
+        const int st = it & 1, c = chunk(it);
         // chunk it + 1 landed; V of chunk it transposed (the last P V has completed)
         attn::cp_async_wait<0>();
         transpose_v<D>(sm, st, warp, lane);
@@ -287,7 +327,9 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
           float mc = -INFINITY;
 #pragma unroll
           for (int j = 0; j < AC; ++j) {
-            const float v = c * AC + j <= lim_r ? sv[j] * sl2 : -INFINITY;
+            const int key = c * AC + j;
+            const bool vis = key <= lim_r || (R2 && key >= lo2_r && key <= hi2_r);
+            const float v = vis ? sv[j] * sl2 : -INFINITY;
             sv[j] = v;
             mc = fmaxf(mc, v);
           }
@@ -327,7 +369,7 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
           tc::mma_commit(pv_full);
         }
         // chunk it + 2 into this chunk's stage
-        if (it + 2 < n_it) load_kv<D>(sm, kv, st, c + 2 * R, maxlim, tid);
+        if (it + 2 < n_it) load_kv<D>(sm, kv, st, chunk(it + 2), maxlim, tid);
         attn::cp_async_commit();
         // O = O * corr + PV for this warp's rows and output columns
         if (!tc::mbar_wait(pv_full, it & 1)) s_fail = 1;

@@ -1134,7 +1134,7 @@ int gocr_three_stream_ranges(int P, int N, int B, int32_t* lim, int32_t* lo2, in
   return GOCR_OK;
 }
 
-// waves of two attention CTAs per SM that the rank count of a second-interval call fills
+// waves of resident attention CTAs that the rank count of a second-interval call fills
 static constexpr int OP_R2_WAVES = 2;
 
 int gocr_op_attention_ranges(int dtype, const void* q_hi, const void* q_lo, const void* k_hi, const void* k_lo,
@@ -1155,23 +1155,32 @@ int gocr_op_attention_ranges(int dtype, const void* q_hi, const void* q_lo, cons
   a.row_lo2 = lo2; a.row_hi2 = hi2;
   a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.d = d; a.cap = cap; a.scale = 1.0f / sqrtf((float)d);
   {
-    const char* ak = getenv("GOCR_ATTN");
-    a.kind = ak && strcmp(ak, "tc") == 0 ? ATTN_TCGEN05 : ATTN_MMA_SYNC;
-  }
-  {
-    // key-chunk ranks: the rule's count, which keeps every row's bits the same
-    // whatever the number of rows in the call.  Rows with a second key interval
-    // (joint-training forwards, one call over the whole packed sequence) take
-    // instead no more ranks than fill OP_R2_WAVES waves of two CTAs per SM over
-    // the (kv head, row tile) groups: many tiles need few ranks, and each rank
-    // costs a partial row set and its merge.  GOCR_ATTN_RANKS=<n> replaces the
+    // kernel and key-chunk ranks.  Plain calls: the mma.sync kernel (GOCR_ATTN=tc:
+    // tcgen05) over the rule's ranks, which keeps every row's bits the same
+    // whatever the number of rows in the call.  Rows with a second key
+    // interval (joint-training forwards, one call over the whole packed
+    // sequence) take instead no more ranks than fill OP_R2_WAVES waves of the
+    // kernel's resident CTAs over its (kv head, row tile) groups (many tiles
+    // need few ranks, and each rank costs a partial row set and its merge),
+    // and the tcgen05 kernel when its ranks average at least four chunks.
+    // GOCR_ATTN=tc / mma forces the kernel; GOCR_ATTN_RANKS=<n> replaces the
     // count (1 .. the rule's).
+    const char* ak = getenv("GOCR_ATTN");
+    const bool force_tc = ak && strcmp(ak, "tc") == 0, force_mma = ak && strcmp(ak, "mma") == 0;
     const int rule = attention_ranks(cap, 1);
+    const int G = Hq / Hkv, n_chunk = (cap + 31) / 32;
+    auto r2_ranks = [&](int tile_rows, int per_sm) {
+      const long long groups = (long long)Hkv * (((long long)T * G + tile_rows - 1) / tile_rows);
+      const long long fill = (OP_R2_WAVES * (long long)per_sm * SM_COUNT + groups - 1) / groups;
+      return fill < rule ? (int)fill : rule;
+    };
     int R = rule;
+    a.kind = force_tc ? ATTN_TCGEN05 : ATTN_MMA_SYNC;
     if (lo2) {
-      const long long groups = (long long)Hkv * ((T * (Hq / Hkv) + 63) / 64);
-      const long long fill = (OP_R2_WAVES * 2LL * SM_COUNT + groups - 1) / groups;
-      R = fill < R ? (int)fill : R;
+      const int r_tc = r2_ranks(128, 1);
+      const bool tc = force_tc || (!force_mma && n_chunk >= 4 * r_tc);
+      a.kind = tc ? ATTN_TCGEN05 : ATTN_MMA_SYNC;
+      R = tc ? r_tc : r2_ranks(64, 2);
     }
     const char* ar = getenv("GOCR_ATTN_RANKS");
     if (ar && atoi(ar) >= 1) R = atoi(ar) < rule ? atoi(ar) : rule;

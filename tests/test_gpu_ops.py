@@ -158,13 +158,17 @@ def test_attention_row_bits_do_not_depend_on_other_rows(g, monkeypatch, dt):
         assert torch.equal(one[0], full[j]), j
 
 
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("dt", ["f32", "bf16-mma", "bf16-tc"])
 @pytest.mark.parametrize("P,N,B,Hq,Hkv,d", [(5, 24, 8, 4, 2, 64), (40, 90, 32, 12, 4, 128), (0, 33, 7, 12, 4, 128),
-                                            (130, 200, 32, 6, 2, 128)])
-def test_attention_three_stream_training_mask(g, dt, P, N, B, Hq, Hkv, d):
+                                            (130, 200, 32, 6, 2, 128), (300, 160, 16, 12, 4, 128)])
+def test_attention_three_stream_training_mask(g, monkeypatch, dt, P, N, B, Hq, Hkv, d):
     """The joint-training mask (review §3.1; blog three-stream figure) as a
     second key interval per row, against the oracle's mask built from the
-    rule text, over the packed [prefix, clean, corrupted 1, corrupted 2]."""
+    rule text, over the packed [prefix, clean, corrupted 1, corrupted 2]; bf16
+    on the mma.sync and on the tcgen05 kernel (both skip the key chunks masked
+    for a whole row tile)."""
+    if dt != "f32":
+        monkeypatch.setenv("GOCR_ATTN", dt.split("-")[1])
     rng = np.random.default_rng(P + N + B + d)
     L = P + 3 * N
     dtype = g.DTYPE_F32 if dt == "f32" else g.DTYPE_BF16
@@ -179,3 +183,26 @@ def test_attention_three_stream_training_mask(g, dt, P, N, B, Hq, Hkv, d):
     o = g.op_attention(_planes(q, dtype), _planes(k, dtype), _planes(v, dtype), dev(lim), dtype,
                        lo2=dev(lo2), hi2=dev(hi2)).cpu().numpy()
     np.testing.assert_allclose(o, ref, rtol=tol, atol=tol)
+
+
+@pytest.mark.parametrize("kind", ["mma", "tc"])
+@pytest.mark.parametrize("ranks", [1, 3, 7])
+def test_attention_three_stream_few_ranks(g, monkeypatch, kind, ranks):
+    """The training mask with few key-chunk ranks, so that each rank walks
+    many chunks across the span it skips (past the clean limit, before the
+    corrupted block) on both bf16 kernels, against the oracle."""
+    monkeypatch.setenv("GOCR_ATTN", kind)
+    monkeypatch.setenv("GOCR_ATTN_RANKS", str(ranks))
+    P, N, B, Hq, Hkv, d = 200, 256, 32, 12, 4, 128
+    rng = np.random.default_rng(ranks)
+    L = P + 3 * N
+    lim, lo2, hi2, _ = g.three_stream_ranges(P, N, B)
+    q = rng.standard_normal((L, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((Hkv, L, d)).astype(np.float32)
+    v = rng.standard_normal((Hkv, L, d)).astype(np.float32)
+    ref = oracle.attention(q.astype(np.float64), k.transpose(1, 0, 2).astype(np.float64),
+                           v.transpose(1, 0, 2).astype(np.float64), oracle.three_stream_mask(P, N, B))
+    dev = lambda a: torch.from_numpy(a).cuda()
+    o = g.op_attention(_planes(q, g.DTYPE_BF16), _planes(k, g.DTYPE_BF16), _planes(v, g.DTYPE_BF16), dev(lim),
+                       g.DTYPE_BF16, lo2=dev(lo2), hi2=dev(hi2)).cpu().numpy()
+    np.testing.assert_allclose(o, ref, rtol=5e-3, atol=5e-3)
