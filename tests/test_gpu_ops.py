@@ -185,6 +185,35 @@ def test_attention_three_stream_training_mask(g, monkeypatch, dt, P, N, B, Hq, H
     np.testing.assert_allclose(o, ref, rtol=tol, atol=tol)
 
 
+@pytest.mark.parametrize("kind", [None, "mma"])
+def test_attention_three_stream_full_size_sampled(g, monkeypatch, kind):
+    """The training-mask call at the size bench.py times (prefix 1024, three
+    512-token streams, blocks of 32, 12 q / 4 kv heads, d 128: 2,560 rows)
+    with the call's own kernel and rank choice (and on the mma.sync kernel),
+    against the oracle on sampled rows: the first and last rows of every
+    stream and block edge, plus seeded random rows, every head."""
+    if kind:
+        monkeypatch.setenv("GOCR_ATTN", kind)
+    P, N, B, Hq, Hkv, d = 1024, 512, 32, 12, 4, 128
+    L = P + 3 * N
+    rng = np.random.default_rng(2560)
+    lim, lo2, hi2, _ = g.three_stream_ranges(P, N, B)
+    q = rng.standard_normal((L, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((Hkv, L, d)).astype(np.float32)
+    v = rng.standard_normal((Hkv, L, d)).astype(np.float32)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    o = g.op_attention(_planes(q, g.DTYPE_BF16), _planes(k, g.DTYPE_BF16), _planes(v, g.DTYPE_BF16), dev(lim),
+                       g.DTYPE_BF16, lo2=dev(lo2), hi2=dev(hi2)).cpu().numpy()
+    edges = [0, 1, 31, 32, P - 1]
+    for s0 in (P, P + N, P + 2 * N):
+        edges += [s0, s0 + 1, s0 + B - 1, s0 + B, s0 + N // 2, s0 + N - B, s0 + N - 1]
+    rows = np.unique(np.concatenate([edges, rng.integers(0, L, 24)]))
+    mask = oracle.three_stream_mask(P, N, B)[rows]
+    ref = oracle.attention(q[rows].astype(np.float64), k.transpose(1, 0, 2).astype(np.float64),
+                           v.transpose(1, 0, 2).astype(np.float64), mask)
+    np.testing.assert_allclose(o[rows], ref, rtol=5e-3, atol=5e-3)
+
+
 @pytest.mark.parametrize("kind", ["mma", "tc"])
 @pytest.mark.parametrize("ranks", [1, 3, 7])
 def test_attention_three_stream_few_ranks(g, monkeypatch, kind, ranks):
