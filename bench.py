@@ -592,40 +592,48 @@ def main():
         prefix_lens, new_lens = synth.batch_lengths(wl.n_requests)
         max_ctx = max(prefix_lens) + max(new_lens) + B + 8
         n_req = wl.n_requests
-    elif kind == "sweep":
-        max_ctx = wl.prefix_len + wl.max_new + max(synth.SWEEP_BLOCKS) + 8
-        prefix_lens, new_lens, n_req = [wl.prefix_len], [wl.max_new], 1
     else:
         max_ctx = wl.prefix_len + wl.max_new + B + 8
         prefix_lens, new_lens, n_req = [wl.prefix_len], [wl.max_new], 1
-    dec = gocr.Decoder(cfg, W, max_ctx=max_ctx, max_block=max(B, max(synth.SWEEP_BLOCKS) if kind == "sweep" else B),
-                       max_requests=n_req, device=str(dev))
+    dec = gocr.Decoder(cfg, W, max_ctx=max_ctx, max_block=B, max_requests=n_req, device=str(dev))
     seeds = [synth.REQUEST_PREFIX_SEED0 + r if kind == "batch" else synth.PREFIX_SEED for r in range(n_req)]
     prefixes = upload_prefixes(cfg, prefix_lens, seeds, dev)
-    refs = []
-    if wl.forced_mean is not None:
+
+    def ar_refs(d):
         # the AR-greedy continuation each forced draft copies (setup, not timed)
+        out = []
         for r in range(n_req):
-            dec.prefill(r, prefixes[r][1])
-            ref, _ = dec.decode(r, gocr.MODE_AR, 0, new_lens[r])
-            refs.append(ref)
+            d.prefill(r, prefixes[r][1])
+            ref, _ = d.decode(r, gocr.MODE_AR, 0, new_lens[r])
+            out.append(ref)
+        return out
 
-    def arm(mean, seed_off=0):
+    def arm(d, refs_d, mean, seed_off=0):
         for r in range(n_req):
-            dec.set_draft_override(r, refs[r], synth.accept_schedule(mean, new_lens[r], seed=synth.SCHEDULE_SEED + r + seed_off))
+            d.set_draft_override(r, refs_d[r], synth.accept_schedule(mean, new_lens[r], seed=synth.SCHEDULE_SEED + r + seed_off))
 
+    refs = ar_refs(dec) if wl.forced_mean is not None else []
     sweep = None
     if kind == "sweep":
+        # one handle per block size, as a deployment would size it: a handle's
+        # attention ranks are fixed for its largest forward
         sweep = []
         for Bv in synth.SWEEP_BLOCKS:
-            for mean in synth.SWEEP_MEANS:
-                arm(mean)
-                r = time_decode(dec, prefixes, n_req, new_lens, Bv, gocr.MODE_SELFSPEC, 3, 2)
-                sweep.append({"B": Bv, "mean_accepted": mean, "round_us": 1e3 * sum(r["ms"]) / r["rounds"],
-                              "tokens_per_s": r["tokens"] / (sum(r["ms"]) / 1e3),
-                              "tpf": r["tokens"] / r["forwards"]})
+            dv = dec if Bv == B else gocr.Decoder(cfg, W, max_ctx=wl.prefix_len + wl.max_new + Bv + 8, max_block=Bv,
+                                                  max_requests=n_req, device=str(dev))
+            try:
+                refs_v = refs if dv is dec else ar_refs(dv)
+                for mean in synth.SWEEP_MEANS:
+                    arm(dv, refs_v, mean)
+                    r = time_decode(dv, prefixes, n_req, new_lens, Bv, gocr.MODE_SELFSPEC, 3, 2)
+                    sweep.append({"B": Bv, "mean_accepted": mean, "round_us": 1e3 * sum(r["ms"]) / r["rounds"],
+                                  "tokens_per_s": r["tokens"] / (sum(r["ms"]) / 1e3),
+                                  "tpf": r["tokens"] / r["forwards"], "attention_ranks": dv.attention_ranks()})
+            finally:
+                if dv is not dec:
+                    dv.close()
     if wl.forced_mean is not None:
-        arm(wl.forced_mean)
+        arm(dec, refs, wl.forced_mean)
 
     if world > 1:
         torch.distributed.barrier()

@@ -649,11 +649,12 @@ int gocr_create(const gocr_config* cfg, const gocr_weights* w, void* stream, goc
     if (c.max_requests <= 1 && h->attn_kind == ATTN_MMA_SYNC) {
       // one request on the mma.sync kernel (64-row tiles, two CTAs per SM):
       // no more ranks than fill two CTAs per SM in one wave for the (kv head,
-      // 64-row group) tiles of a B + 1 = 33-row forward (or of the handle's
-      // largest forward when that is smaller); measured on the table region
-      // (2,992 positions, B = 32): 38 ranks 1,641 us per round against 48
-      // ranks 1,785 us
-      const int fw_rows = (c.max_block < 32 ? c.max_block : 32) + 1;
+      // 64-row group) tiles of the handle's largest forward (max_block + 1
+      // rows); measured on the table region (2,992 positions, B = 32): 38
+      // ranks 1,641 us per round against 48 ranks 1,785 us; on a 65-row draft
+      // forward after 2,048 positions: 19 ranks 1,072 us against 38 ranks
+      // 1,165 us
+      const int fw_rows = c.max_block + 1;
       const int fw_groups = c.n_kv_heads * ((fw_rows * (c.n_q_heads / c.n_kv_heads) + 63) / 64);
       const int wave = 2 * SM_COUNT / (fw_groups > 0 ? fw_groups : 1);
       const int cap_r = wave < ATTN_RANKS_MIN ? ATTN_RANKS_MIN : wave;
