@@ -475,9 +475,10 @@ __global__ void __launch_bounds__(TC_THREADS) gemm_tc_kernel(const __grid_consta
 }
 
 // Streaming variant for wide matrices without split K at decode shapes (the
-// LM head: 512 weight tiles, at most 64 tokens): two CTAs per SM walk the
-// tiles tile0, tile0 + gridDim.x, ... with one TMA ring that runs across tile
-// boundaries, so the weight stream does not stop between tiles or waves.
+// LM head: 512 weight tiles, at most 128 tokens): the CTAs (two per SM up to
+// 64 tokens, one above) walk the tiles tile0, tile0 + gridDim.x, ... with one
+// TMA ring that runs across tile boundaries, so the weight stream does not
+// stop between tiles or waves.
 // Warp 0 lane 0 loads, warp 1 lane 0 issues the MMAs into one of two tensor
 // memory accumulators (tile i uses buffer i % 2), warps 2..5 drain an
 // accumulator into shared memory and run the epilogue while the next tile's
@@ -511,7 +512,9 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
   const int total = my_tiles * nkb;  // k-blocks this CTA streams
   const int tn = min(TZ_TC, a.T);
   const int nmma = 2 * nt;
-  const uint32_t ncols = nmma <= 32 ? 32 : (nmma <= 64 ? 64 : 128);  // per accumulator (nt <= 64)
+  // per accumulator: 2 x ncols columns of tensor memory, 256 per CTA up to 64
+  // tokens (two CTAs per SM), 512 above (one CTA per SM)
+  const uint32_t ncols = nmma <= 32 ? 32 : (nmma <= 64 ? 64 : (nmma <= 128 ? 128 : 256));
 
   if (tid == 0) {
     if (TRACE) trace_at(a, 0);
@@ -1030,25 +1033,28 @@ static bool launch_gemm_tc_kt(const GemmArgs& a, cudaStream_t s, bool pdl) {
                             yl.ys, yl.scratch, -1, EG) == cudaSuccess;
 }
 
-// Two CTAs per SM (at most the tile count), the deepest ring that keeps
-// two CTAs' shared memory on one SM.
+// Up to 64 tokens two CTAs per SM, above one (at most the tile count), with
+// the deepest ring that fits their shared memory; at most 128 tokens.
 template <int EPI, bool TRACE>
 static bool launch_gemm_tc_stream(const GemmArgs& a, cudaStream_t s, bool pdl) {
   CUtensorMap tmw, tmh, tml;
+  if (a.T < 1 || a.T > 128) return false;
   const int nt = (a.T + 15) / 16 * 16;
+  const int per_sm = nt <= 64 ? 2 : 1;
+  const size_t budget = per_sm == 2 ? TWO_CTA_SMEM : (size_t)227 * 1024;
   if (!tmap_2d(&tmw, a.w, a.N, a.K, NTILE) || !tmap_2d(&tmh, a.x, a.T, a.K, nt) ||
       !tmap_2d(&tml, a.x_lo, a.T, a.K, nt))
     return false;
   const int stage_bytes = A_BYTES + 2 * nt * 128;
   const size_t fixed = 1024 + (size_t)nt * YLD * 4 + TZ_TC * 4 + 64 + 16;
-  int stages = (int)((TWO_CTA_SMEM - fixed) / (stage_bytes + 16));
+  int stages = (int)((budget - fixed) / (stage_bytes + 16));
   if (stages > 8) stages = 8;
   if (stages < 2) return false;
   const size_t smem = fixed + (size_t)stages * (stage_bytes + 16);
   if (!kernel_smem_at_least(reinterpret_cast<const void*>(gemm_tc_stream_kernel<EPI, TRACE>), smem)) return false;
   const int n_tiles = cdiv_i(a.N, NTILE);
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(n_tiles < 2 * SM_COUNT ? n_tiles : 2 * SM_COUNT);
+  cfg.gridDim = dim3(n_tiles < per_sm * SM_COUNT ? n_tiles : per_sm * SM_COUNT);
   cfg.blockDim = dim3(STREAM_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -1074,9 +1080,9 @@ static int seq_slice_tokens() {
 
 template <int EPI>
 static bool launch_gemm_tc_k(const GemmArgs& a, cudaStream_t s, bool pdl) {
-  // the LM head at decode shapes (up to 64 tokens): streaming CTAs instead of waves of tile CTAs
+  // the LM head at decode shapes (up to 128 tokens): streaming CTAs instead of waves of tile CTAs
   if constexpr (EPI == EPI_ARGMAX) {
-    if (a.splits == 1 && a.T <= 64 && a.x_lo && !getenv_flag("GOCR_LM_WAVES"))
+    if (a.splits == 1 && a.T <= 128 && a.x_lo && !getenv_flag("GOCR_LM_WAVES"))
       return a.trace ? launch_gemm_tc_stream<EPI, true>(a, s, pdl) : launch_gemm_tc_stream<EPI, false>(a, s, pdl);
   }
   if (cdiv_i(a.T, TZ_TC) > 2 && a.x_lo) {

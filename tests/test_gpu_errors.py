@@ -111,3 +111,28 @@ def test_nan_weight_is_a_device_error(lib, monkeypatch, dt, where):
     # the context is intact: a clean handle decodes
     t0, out, _ = _first_token(g, cfg, W, prefix)
     assert len(out) == 3 and out[0] == t0
+
+
+def test_streaming_lm_head_above_64_rows_equals_tile_ctas(lib, monkeypatch):
+    """A 65-row draft forward (B = 64) runs its LM head on the streaming kernel
+    with one CTA per SM (above 64 rows); its logits and committed argmax are
+    bitwise those of the tile-CTA kernel (GOCR_LM_WAVES=1)."""
+    g, synth = lib
+    cfg = _cfg(synth, "bf16")
+    W = synth.make_weights(cfg, seed=35)
+    prefix = synth.make_prefix(cfg, 40, seed=5)
+    res = {}
+    for kind in ("bf16", "bf16-waves"):
+        _lm_kernel(monkeypatch, kind)
+        dec = g.Decoder(cfg, W, max_ctx=prefix.shape[0] + 160, max_block=64)
+        try:
+            dec.prefill(0, prefix)
+            x0 = dec.state(0)[1]
+            lg = dec.debug_forward(0, g.FWD_DRAFT, [x0] + [0] * 64)
+            out, _ = dec.decode(0, g.MODE_SELFSPEC, 64, 70)
+            res[kind] = (lg, list(out))
+        finally:
+            dec.close()
+    assert res["bf16"][0].shape == (65, cfg.vocab)
+    assert np.array_equal(res["bf16"][0].view(np.uint32), res["bf16-waves"][0].view(np.uint32))
+    assert res["bf16"][1] == res["bf16-waves"][1]
