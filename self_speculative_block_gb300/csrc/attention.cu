@@ -27,8 +27,8 @@
 //     handles whose ranks average at least four chunks.
 // Both have an instantiation for rows with a second key interval (the
 // joint-training mask).  The partial rows of the ranks are then added in rank
-// order by attention_merge_kernel, or for second-interval calls with at most
-// eight ranks by attention_merge_few_kernel (one warp per row, no barrier).
+// order by attention_merge_kernel, or with at most eight ranks by
+// attention_merge_few_kernel (one warp per row, no barrier).
 // There is no thread-block cluster: the CTAs need no co-scheduling.  Under
 // programmatic dependent launch a CTA fetches its first chunk before the
 // grid-dependency wait when that chunk holds only committed cache positions
@@ -270,63 +270,77 @@ __global__ void __launch_bounds__(256) attention_merge_kernel(AttnArgs a, int R)
 
 // Merge for few ranks (R <= MERGE_FEW): one warp per (row, head) pair, each
 // lane a run of D / 32 output columns; every load in one round trip, no CTA
-// barrier.  Ranks are added in rank order.  Used by calls whose rows carry a
-// second key interval (training forwards over many row tiles, few ranks).
+// barrier.  Ranks are added in rank order.  The choice depends on R alone,
+// which a handle fixes, so every forward of a handle merges the same way.
 constexpr int MERGE_FEW = 8;
-template <int D, int TQR>
+template <int D, int TQR, bool TRACE>
 __global__ void __launch_bounds__(256) attention_merge_few_kernel(AttnArgs a, int R) {
   constexpr int RLD = (TQR == attn::QR ? attn::Geo<D>::RLD : attn_tc::Geo<D>::RLD);
   constexpr int CL = D / 32;  // columns per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int group = blockIdx.y;
+  const int group = blockIdx.y, slot = blockIdx.z;
   const int kvh = group % a.Hkv, rg = group / a.Hkv;
   const int G = a.Hq / a.Hkv;
   const int i = blockIdx.x * 8 + warp;  // row of the group's tile
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (TRACE && a.trace_cta && threadIdx.x == 0) trace_at(a, 0, TRACE_MERGE_SLOT);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int nq = a.T * G, gi = rg * TQR + i;
-  if (i >= TQR || gi >= nq) return;
-  const int n_chunks = a.part_chunks[group];
-  const int n_ranks = n_chunks < R ? n_chunks : R;
-  const float* base = a.part + (size_t)group * R * TQR * RLD + (size_t)i * RLD;
-  float m[MERGE_FEW], l[MERGE_FEW], v[MERGE_FEW][CL];
+  if (TRACE && a.trace_cta && threadIdx.x == 0) trace_at(a, 1, TRACE_MERGE_SLOT);
+  if (TRACE && threadIdx.x == 0) trace_at(a, 6, TRACE_MERGE_SLOT);
+  int row0 = 0, nrows = a.T;
+  if (a.rows_per_slot > 0) {
+    row0 = slot * a.rows_per_slot;
+    nrows = a.rows_per_slot;
+  } else if (a.plan) {
+    row0 = a.plan->slot_row0[slot];
+    nrows = a.plan->slot_nrows[slot];
+  }
+  const int nq = nrows * G, gi = rg * TQR + i;
+  if (i < TQR && gi < nq) {
+    const size_t gs = (size_t)slot * gridDim.y + group;
+    const int n_chunks = a.part_chunks[gs];
+    const int n_ranks = n_chunks < R ? n_chunks : R;
+    const float* base = a.part + gs * R * TQR * RLD + (size_t)i * RLD;
+    float m[MERGE_FEW], l[MERGE_FEW], v[MERGE_FEW][CL];
 #pragma unroll
-  for (int r = 0; r < MERGE_FEW; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.f;
+    for (int r = 0; r < MERGE_FEW; ++r) {
+      m[r] = -INFINITY;
+      l[r] = 0.f;
 #pragma unroll
-    for (int j = 0; j < CL; ++j) v[r][j] = 0.f;
-    if (r < n_ranks) {
-      const float* p = base + (size_t)r * TQR * RLD;
-      m[r] = __ldcg(p + D);
-      l[r] = __ldcg(p + D + 1);
-      if constexpr (CL == 4) {
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(p + lane * 4));
-        v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
-      } else {
-        const float2 x = __ldcg(reinterpret_cast<const float2*>(p + lane * 2));
-        v[r][0] = x.x; v[r][1] = x.y;
+      for (int j = 0; j < CL; ++j) v[r][j] = 0.f;
+      if (r < n_ranks) {
+        const float* p = base + (size_t)r * TQR * RLD;
+        m[r] = __ldcg(p + D);
+        l[r] = __ldcg(p + D + 1);
+        if constexpr (CL == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(p + lane * 4));
+          v[r][0] = x.x; v[r][1] = x.y; v[r][2] = x.z; v[r][3] = x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(p + lane * 2));
+          v[r][0] = x.x; v[r][1] = x.y;
+        }
       }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < MERGE_FEW; ++r) M = fmaxf(M, m[r]);
+    float L = 0.f, o[CL];
+#pragma unroll
+    for (int j = 0; j < CL; ++j) o[j] = 0.f;
+#pragma unroll
+    for (int r = 0; r < MERGE_FEW; ++r) {
+      const float w = m[r] == -INFINITY ? 0.f : exp2f(m[r] - M);
+      L = fmaf(w, l[r], L);
+#pragma unroll
+      for (int j = 0; j < CL; ++j) o[j] = fmaf(w, v[r][j], o[j]);
+    }
+    const float il = L > 0.f ? 1.f / L : 0.f;
+    const int tq = attn::div_small(gi, G, 0xFFFFFFFFu / (unsigned)G + 1u);
+    const size_t off = ((size_t)(row0 + tq) * a.Hq + kvh * G + (gi - tq * G)) * D + lane * CL;
+#pragma unroll
+    for (int j = 0; j < CL; ++j) put_plane(a.o_hi, a.o_lo, a.out_bf16, off + j, o[j] * il);
   }
-  float M = -INFINITY;
-#pragma unroll
-  for (int r = 0; r < MERGE_FEW; ++r) M = fmaxf(M, m[r]);
-  float L = 0.f, o[CL];
-#pragma unroll
-  for (int j = 0; j < CL; ++j) o[j] = 0.f;
-#pragma unroll
-  for (int r = 0; r < MERGE_FEW; ++r) {
-    const float w = m[r] == -INFINITY ? 0.f : exp2f(m[r] - M);
-    L = fmaf(w, l[r], L);
-#pragma unroll
-    for (int j = 0; j < CL; ++j) o[j] = fmaf(w, v[r][j], o[j]);
-  }
-  const float il = L > 0.f ? 1.f / L : 0.f;
-  const int tq = attn::div_small(gi, G, 0xFFFFFFFFu / (unsigned)G + 1u);
-  const size_t off = ((size_t)tq * a.Hq + kvh * G + (gi - tq * G)) * D + lane * CL;
-#pragma unroll
-  for (int j = 0; j < CL; ++j) put_plane(a.o_hi, a.o_lo, a.out_bf16, off + j, o[j] * il);
+  if (TRACE && threadIdx.x == 0) trace_at(a, 3, TRACE_MERGE_SLOT);
 }
 
 size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, int R) {
@@ -343,9 +357,9 @@ size_t attention_part_floats(int n_slots, int max_rows, int Hq, int Hkv, int d, 
 // The merge after a partial kernel of TQR-row tiles (always ordered after it).
 template <int D, int TQR, bool TRACE>
 static bool launch_attn_merge(const AttnArgs& a, int R, int n_groups, int n_slots, cudaStream_t s) {
-  if (a.row_lo2 && R <= MERGE_FEW && n_slots == 1 && !a.plan && a.rows_per_slot == 0) {
+  if (R <= MERGE_FEW) {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(TQR / 8, n_groups, 1);
+    cfg.gridDim = dim3(TQR / 8, n_groups, n_slots);
     cfg.blockDim = dim3(256);
     cfg.stream = s;
     cudaLaunchAttribute at[1];
@@ -353,7 +367,7 @@ static bool launch_attn_merge(const AttnArgs& a, int R, int n_groups, int n_slot
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attention_merge_few_kernel<D, TQR>, a, R) == cudaSuccess;
+    return cudaLaunchKernelEx(&cfg, attention_merge_few_kernel<D, TQR, TRACE>, a, R) == cudaSuccess;
   }
   // with few ranks a row pair is little work: four pairs per CTA then
   const int ppc = R <= 16 ? 4 : 1;
