@@ -13,9 +13,9 @@
 // softmax with one thread per query row (a row's 32 scores come from its own
 // TMEM lane, so no cross-thread reduction); all eight warps fold each chunk's
 // PV into the running output, O = O * corr + PV (warp w: rows 32 (w % 4) ..
-// +31, output columns (w / 4) d/2 .. +d/2).  The next chunk's QK^T is issued
-// right after this chunk's P V and runs under its fold and the next V
-// transpose (two score buffers); K/V are fetched two chunks ahead.
+// +31, output columns (w / 4) d/2 .. +d/2).  Two score buffers let the next
+// chunk's QK^T run under this chunk's softmax; K/V are fetched two chunks
+// ahead.
 //
 // A chunk with no key visible to a row leaves that row's (max, sum, output)
 // bit for bit unchanged (corr = 1, P = 0), so a row's result does not depend
@@ -313,6 +313,11 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
         tc::fence_before_sync();
         __syncthreads();
         if (TRACE && it == 0 && tid == 0) trace_at(a, 4);
+        // the next chunk's scores while this chunk's softmax runs
+        if (tid == 0 && it + 1 < n_it) {
+          tc::fence_after_sync();
+          issue_qk(it + 1);
+        }
         if (warp >= 4) {
           // online softmax of row r over the chunk's 32 keys
           if (!tc::mbar_wait(s_full + st, (it >> 1) & 1)) s_fail = 1;
@@ -362,10 +367,6 @@ __global__ void __launch_bounds__(attn_tc::THREADS, 1) attention_tc_part_kernel(
               tc::mma_bf16(tmem + PV_COL, tc::sdesc_sw128(p_s + ks * 32),
                            tc::sdesc_sw128((t ? vt_lo : vt_hi) + ks * 32), idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
           tc::mma_commit(pv_full);
-          // then the next chunk's scores (its K landed before this chunk's
-          // V transpose), which run under this chunk's fold and the next V
-          // transpose; issued after P V so the fold does not wait behind them
-          if (it + 1 < n_it) issue_qk(it + 1);
         }
         // chunk it + 2 into this chunk's stage
         if (it + 2 < n_it) load_kv<D>(sm, kv, st, chunk(it + 2), maxlim, tid);
