@@ -338,7 +338,7 @@ def table_record(cfg, W, hbm, dev, steps, warmup):
 
 
 def next_rows_record(cfg, W, hbm, dev, steps, warmup):
-    """The survey's NEXT rows on the text region (prefix 1024, B = 32, 73
+    """The decoding modes beyond the greedy round on the text region (prefix 1024, B = 32, 73
     tokens): direct block-diffusion decoding (threshold 0.9), self-speculative
     rounds with refined drafts (at most 4 draft forwards, draft threshold 0.9),
     sampling (temperature 1) self-speculative against AR sampling, each as

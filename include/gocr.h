@@ -362,7 +362,7 @@ int gocr_three_stream_ranges(int P, int N, int B, int32_t* lim, int32_t* lo2, in
  * layouts and results as gocr_op_linear, but no workspace: the split-K partial
  * sums and tile counters live in one file-scope device array of
  * GOCR_STATIC_SCRATCH_BYTES that every GPU loading this library keeps until
- * the process exits.  The paper has no counterpart: this is a deployment
+ * the process exits.  GravityOCR has no counterpart: this is a deployment
  * convenience of this library.
  *   - Calls nothing that allocates (no cudaMalloc/cudaFree, no library
  *     allocator): it clears the counters with cudaMemsetAsync and launches.

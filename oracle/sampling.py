@@ -5,9 +5,10 @@ rule (the algorithm).
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this module.
 
 Sources (page title, section):
-* GravityOCR review (euisuk-chung), §2 "Speculative Decoding": besides the
-  greedy top-1 verification the paper introduces the standard stochastic
-  acceptance-rejection rule; its equality claims are for top-1.
+* GravityOCR review (euisuk-chung), §2 "Speculative Decoding": describes,
+  besides the greedy top-1 verification GravityOCR uses, the standard
+  stochastic acceptance-rejection rule; GravityOCR's equality claims are for
+  top-1.
 * Trillion Labs blog post, the paragraph on AR equivalence: with sampling the
   speculative rejection rule preserves the AR distribution.
 
