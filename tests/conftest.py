@@ -15,5 +15,5 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     # A gpu-marked test run without a GPU is an error of the caller, not a skip
-    # that could hide a missing CUDA path; the driver selects -m gpu on GPU machines.
+    # that could hide a missing CUDA path; runs on a GPU machine select -m gpu.
     pass
