@@ -147,8 +147,11 @@ enum { ATTN_TCGEN05 = 0, ATTN_MMA_SYNC = 1 };
 // tile reads more chunks; never more than a KV capacity of cap keys has chunks
 // of 32.  A handle fixes R at creation, so every forward of a handle (one row
 // or B + 1, one request or a batch) splits a row's keys the same way.
+// Measured on the 16-request page batch (tcgen05 attention, round us): 3, 4,
+// 5, 6, 7, 8, 10, 12 ranks: 7,241, 7,209, 7,105, 7,026, 7,171, 7,245, 7,690,
+// 7,821.
 constexpr int ATTN_RANKS = 48;
-constexpr int ATTN_RANKS_MIN = 8;
+constexpr int ATTN_RANKS_MIN = 6;
 inline int attention_ranks(int cap, int n_req) {
   const int c = (cap + 31) / 32;
   int r = ATTN_RANKS / (n_req < 1 ? 1 : n_req);
