@@ -36,6 +36,7 @@ from self_speculative_block_gb300 import synth  # noqa: E402
 
 MEASURED_PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def peaks():
@@ -45,6 +46,15 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def bf16_peak():
+    """Dense bf16 tensor TFLOP/s (burst) and its source."""
+    try:
+        with open(MEASURED_PEAKS) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 # --------------------------------------------------------------------------- clocks
@@ -389,9 +399,18 @@ def next_rows_record(cfg, W, hbm, dev, steps, warmup):
     e1.record()
     torch.cuda.synchronize()
     us = 1e3 * e0.elapsed_time(e1) / reps
+    # tensor roofline: the hi/lo planes make 3 bf16 products for QK^T and 2 for
+    # PV, 2.5 x the arithmetic of the visible pairs
+    peak, peak_kind = bf16_peak()
+    mma_tflops = 2.5 * tm.flops() / (us * 1e-6) / 1e12
     rec["training_mask_attention"] = {"rows": tm.L, "prefix": tm.P, "stream": tm.N, "block": tm.block,
                                       "us_per_launch": us, "visible_pairs": tm.visible_pairs(),
-                                      "tflops": tm.flops() / (us * 1e-6) / 1e12}
+                                      "tflops": tm.flops() / (us * 1e-6) / 1e12,
+                                      "roofline": {"bound": "tensor", "achieved": mma_tflops, "peak": peak,
+                                                   "unit": "TFLOP/s", "frac": mma_tflops / peak,
+                                                   "peak_kind": peak_kind,
+                                                   "how": "bf16 MMA work of the visible pairs (hi/lo products) "
+                                                          "over the call's CUDA-event time"}}
     return rec
 
 
